@@ -1,0 +1,360 @@
+"""Throughput of diffuser_forward: edge-hops per second on one GB300.
+
+A step is one whole forward (scores + masked softmax + K diffusion hops +
+output) of the configured workload, inputs resident in HBM.  Default
+workload: batch 2, 12 heads, n = 4096, d = 64, bf16 I/O, window radius 256,
+16 globals, 32 random edges per row, K = 5, alpha = 0.1.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Prints one JSON line.  `value` = edge-hops/s = units * nnz * hops / step time,
+summed over ranks (weak scaling: every rank runs its own copy of the
+workload), time from CUDA events around each forward, L2 flushed between
+steps outside the events.  `e2e` runs the same forward through the host-buffer
+entry point, host<->device copies inside the timed region.  `roofline` is for
+the dominant kernel (the diffusion hop): algorithmic bytes per launch over
+its mean device time, against the measured HBM copy bandwidth.
+`--impl reference` times the fp64 CPU oracle instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_long_sequence_gb300 import synthetic, workloads  # noqa: E402
+
+METRIC = "edge-hops/sec for diffuser_forward (n=4096, K=5); % of GB300 HBM roofline"
+UNIT = "edge-hops/s"
+L2_FLUSH_BYTES = 256 << 20          # > 129 MB of L2
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- byte model
+def algorithmic_bytes(w: workloads.Workload, nnz: int) -> dict:
+    """"Score once, store A, read it K times" model, per forward.
+
+    Per unit: Q, K, V read and out written once (4 n d s), A written once and
+    read K times (4 E (K+1)), the fp32 hop state Z_k written and read between
+    hops with V re-read per hop ((K-1)(8 n d + n d s)); plus the graph (once).
+    The hop kernels' share per unit: 4 E K + 2 n d s + (K-1)(8 n d + n d s).
+    """
+    s = 2 if w.dtype == "bf16" else 4
+    n, d, K, E, U = w.n, w.d, w.hops, nnz, w.units
+    per_unit_total = 4 * n * d * s + (1 + K) * E * 4 + (K - 1) * (2 * n * d * 4 + n * d * s)
+    per_unit_hops = 4 * E * K + 2 * n * d * s + (K - 1) * (8 * n * d + n * d * s)
+    return dict(total=U * per_unit_total + (n + 1) * 8 + E * 4,
+                hops_total=U * per_unit_hops,
+                per_hop_launch=U * per_unit_hops / max(K, 1))
+
+
+def measured_peaks() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def hop_kernel_traffic(workload: str) -> float | None:
+    """ncu DRAM bytes per hop launch, if recorded for the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("source_sha") != kernel_source_sha():
+        return None
+    return float(rec["bytes_per_launch"])
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_long_sequence_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".h", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, p[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+def oracle_sample(w: workloads.Workload, units: int, nthreads: int) -> tuple[float, int, int]:
+    """Run the fp64 oracle on `units` units of the workload; returns (seconds,
+    edge-hops, nnz)."""
+    import oracle
+    gargs = w.graph_args()
+    row_ptr, col = (oracle.token_graph(**gargs) if w.kind == "token"
+                    else oracle.block_graph(**gargs))
+    nnz = int(row_ptr[-1])
+    Q, K, V = synthetic.qkv(1, units, w.n, w.d, w.dtype, seed=w.seed)
+    Qw, Kw, Vw = (oracle.widen(x, w.dtype) for x in (Q, K, V))
+    t0 = time.perf_counter()
+    oracle.forward(Qw, Kw, Vw, row_ptr, col, w.hops, w.alpha, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, units * nnz * w.hops, nnz
+
+
+def cpu_sample_units(w) -> tuple[int, int]:
+    cores = os.cpu_count() or 1
+    return min(w.units, cores), cores
+
+
+def run_reference(args, w) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    units, cores = cpu_sample_units(w)
+    for _ in range(args.warmup):        # warm-up steps: one unit each (loads, page-ins)
+        oracle_sample(w, 1, 1)
+    times, eh = [], 0
+    for _ in range(args.steps):
+        dt, eh, nnz = oracle_sample(w, units, cores)
+        times.append(dt)
+    value = eh / statistics.mean(times)
+    sample = (f"{units} of {w.units} (batch, head) units of {w.name} per step, "
+              f"fp64 oracle, {cores} threads over units")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args, w) -> None:
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from sparse_long_sequence_gb300 import binding as dl
+
+    # graph + inputs (each rank its own copy of the workload: weak scaling)
+    if w.kind == "token":
+        g = dl.diffuser_build_graph(w.n, w.r, w.n_globals, rand_per_row=w.rand_per_row,
+                                    seed=w.seed)
+    else:
+        g = dl.diffuser_build_block_graph(w.n, w.block, w.window_blocks, w.rand_blocks,
+                                          w.global_blocks, seed=w.seed)
+    Qh, Kh, Vh = synthetic.qkv(w.B, w.H, w.n, w.d, w.dtype, seed=w.seed)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def host(x):
+        t = torch.from_numpy(x)
+        return (t.view(torch.bfloat16) if w.dtype == "bf16" else t).pin_memory()
+
+    Qp, Kp, Vp = host(Qh), host(Kh), host(Vh)
+    Q, K, V = Qp.cuda(), Kp.cuda(), Vp.cuda()
+    out = torch.empty_like(V)
+    code = dl.DIFFUSER_DTYPE_BF16 if w.dtype == "bf16" else dl.DIFFUSER_DTYPE_FP32
+    ws = dl.alloc_workspace(dl.diffuser_workspace_size(g, w.B, w.H, w.d, code))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dl.diffuser_forward(Q, K, V, g, w.hops, w.alpha, out=out, workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, CUDA events around each forward
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0, _ = dl.diffuser_launch_count()
+    dl.diffuser_profile_begin()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        starts[k].record(stream)
+        step()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    prof = dl.diffuser_profile_end()
+    launches1, _ = dl.diffuser_launch_count()
+    if world > 1:
+        dist.barrier()
+    clock_info = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    t_step = statistics.mean(step_ms)
+    if world > 1:
+        tt = torch.tensor([t_step], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+
+    # ---- end to end through the host-buffer entry point
+    Oh = torch.empty_like(Vp).pin_memory()
+    ws_h = dl.alloc_workspace(dl.diffuser_host_workspace_size(g, w.B, w.H, w.d, code))
+    for _ in range(2):
+        dl.diffuser_forward_host(Qp, Kp, Vp, g, w.hops, w.alpha, Oh, ws_h, stream=stream)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dl.diffuser_forward_host(Qp, Kp, Vp, g, w.hops, w.alpha, Oh, ws_h, stream=stream)
+        stream.synchronize()
+        e2e_ms.append(1e3 * (time.perf_counter() - t0))
+    t_e2e = statistics.mean(e2e_ms)
+    if world > 1:
+        tt = torch.tensor([t_e2e], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    assert torch.equal(Oh, out.cpu()), "end-to-end output differs from the device forward"
+
+    edge_hops = w.units * g.nnz * w.hops
+    value = world * edge_hops / (t_step / 1e3)
+    io_bytes = w.units * w.n * w.d * (2 if w.dtype == "bf16" else 4)
+    model = algorithmic_bytes(w, g.nnz)
+    hop_ms, hop_launches = prof["hop"]
+    peak, peak_kind = measured_peaks()
+    roofline = None
+    if hop_launches:
+        per_launch_s = hop_ms / hop_launches / 1e3
+        achieved = model["per_hop_launch"] / per_launch_s / 1e9
+        traffic = hop_kernel_traffic(w.name)
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": traffic,
+                    "kernel": "diffusion hop", "peak_kind": peak_kind,
+                    "algorithmic_bytes_per_launch": model["per_hop_launch"],
+                    "mean_launch_ms": hop_ms / hop_launches}
+    whole_frac = model["total"] / (t_step / 1e3) / 1e9 / peak
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        units, cores = cpu_sample_units(w)
+        dt, eh, _ = oracle_sample(w, units, cores)
+        cpu = {"value": eh / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{units} of {w.units} (batch, head) units of {w.name}, fp64 oracle, "
+                         f"{cores} threads over units, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
+            "config": {**w.describe(), "nnz": g.nnz, "units_per_gpu": w.units,
+                       "parallelism": f"dp{world}" if world > 1 else "single GPU",
+                       "l2": "flushed between steps (256 MB write outside the timed events)",
+                       "arith": "A and Z_k fp32, fp32 accumulate"},
+            "e2e": {"value": world * edge_hops / (t_e2e / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": 3 * io_bytes, "d2h_bytes_per_step": io_bytes},
+            "roofline": roofline,
+            "whole_forward_hbm_frac": whole_frac,
+            "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
+            "gpu_launches": int(launches1 - launches0),
+            "clocks": clock_info,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.TEXT.name, choices=sorted(workloads.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
+    w = workloads.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,246 @@
+/*
+ * diffuser.h -- C ABI of libdiffuser.so, the GB300 (sm_103a) implementation of
+ * the Diffuser hot path:
+ *
+ *   1. a fixed sparse edge set N(i): local window u global tokens u random
+ *      edges (token level), or the BigBird ITC block pattern;
+ *   2. attention weights A_ij = softmax over N(i) of q_i.k_j / sqrt(d);
+ *   3. K personalized-PageRank hops  Z_0 = V,
+ *      Z_{k+1} = (1 - alpha) A Z_k + alpha V,  written out as Z_K.
+ *
+ * Sources (page title, section / equation):
+ *   [D] "Diffuser: modelling long sequences with multi-hop attention diffusion"
+ *       (reading notes on arXiv 2210.11794v2): sec 2.1 eq S.1-S.5, sec 2.2,
+ *       sec 2.4 eq S.7, sec 2.6 (cost model: score once, aggregate K times).
+ *   [S] "1.2.1 Static sparsity: Longformer, BigBird and sliding windows":
+ *       eq 1-4, sec 1.1 eq 5-6, sec 1.2 eq 12, sec 2 eq 13, sec 2.1.
+ *   [B] "038 BigBird: keeping long-sequence information paths with sparse
+ *       connections", sec 2.
+ *
+ * Conventions for every entry point:
+ *   - Returns a diffuser_status (0 = DIFFUSER_OK).  No C++ exception crosses
+ *     the ABI.  diffuser_last_error() gives a one-line message for the last
+ *     failure on the calling thread.
+ *   - "device" pointers are CUDA global-memory addresses on the device that
+ *     was current when the graph was built; "host" pointers are ordinary CPU
+ *     memory.  Every pointer is owned by the caller unless stated otherwise.
+ *   - Tensors Q, K, V, out are contiguous [B][H][n][d] (batch, head, token,
+ *     feature), 16-byte aligned, in the I/O dtype.  d must be 64.
+ *   - Work is enqueued on `stream` (NULL = legacy default stream) and is
+ *     asynchronous with respect to the host unless stated otherwise.
+ *   - Argument checks happen on the host before anything is enqueued; a
+ *     failing call launches nothing.
+ */
+#ifndef DIFFUSER_H
+#define DIFFUSER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DIFFUSER_API __attribute__((visibility("default")))
+#else
+#define DIFFUSER_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that the header needs no CUDA
+ * include. */
+typedef struct CUstream_st* diffuser_stream;
+
+typedef struct diffuser_graph diffuser_graph;
+
+typedef enum {
+    DIFFUSER_OK = 0,
+    DIFFUSER_ERR_INVALID_ARG = 1,  /* a null pointer, a size out of range, misalignment */
+    DIFFUSER_ERR_UNSUPPORTED = 2,  /* a dtype, head width or option this build lacks */
+    DIFFUSER_ERR_OVERFLOW = 3,     /* an edge count or buffer size overflows its index type */
+    DIFFUSER_ERR_ALLOC = 4,        /* a device or host allocation failed */
+    DIFFUSER_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+    DIFFUSER_ERR_DEVICE = 6,       /* a kernel reported an error through its status word */
+    DIFFUSER_ERR_WORKSPACE = 7     /* workspace pointer null/misaligned or too small */
+} diffuser_status;
+
+typedef enum {
+    DIFFUSER_DTYPE_FP32 = 0,       /* float32 I/O; all arithmetic in fp32 FMA */
+    DIFFUSER_DTYPE_BF16 = 1        /* bfloat16 I/O; fp32 accumulation and fp32 A, Z_k */
+} diffuser_dtype;
+
+/* Text for a status code (static storage, never NULL). */
+DIFFUSER_API const char* diffuser_status_string(int status);
+
+/* Message of the last failure on the calling thread ("" if none). */
+DIFFUSER_API const char* diffuser_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+DIFFUSER_API int diffuser_version(void);
+
+/* ---------------------------------------------------------------- graphs
+ *
+ * A graph is an immutable, deduplicated CSR edge set (rows and columns
+ * ascending) plus the device-side layouts the kernels use.  It is built on
+ * the device that is current at the call, holds its own device and host
+ * memory, and may be shared by any number of streams and calls on that
+ * device.  The build is synchronous (it returns when the graph is ready).
+ */
+
+/*
+ * Token-level Diffuser/Longformer graph ([D] sec 2.2; [S] eq 5, eq 12;
+ * [B] sec 2).  For i in G: N(i) = {0..n-1}.  Otherwise
+ *   N(i) = {j : |i-j| <= r} u G u {splitmix64(seed ^ (i*R + t)) mod n : t < R}
+ * with R = rand_per_row, splitmix64 the published SplitMix64 output
+ * function, the modulo unsigned 64-bit, and duplicates entering once.
+ *
+ *   n            sequence length, 1 <= n <= 2^31-1
+ *   r            window radius >= 0 (truncated at the ends, never refilled)
+ *   n_globals    |G|, 0 <= n_globals <= n
+ *   global_idx   host, n_globals strictly increasing positions in [0,n);
+ *                NULL means G = {0..n_globals-1}
+ *   rand_per_row R, 0 <= R <= 1024 (draws per non-global row)
+ *   seed         64-bit seed of the random draws
+ *   out          receives the new graph (caller frees with diffuser_graph_free)
+ * Errors: INVALID_ARG (ranges, unsorted globals, null out), OVERFLOW (nnz
+ * beyond 2^40), ALLOC, CUDA.
+ */
+DIFFUSER_API int diffuser_build_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* global_idx,
+                         int32_t rand_per_row, uint64_t seed, diffuser_graph** out);
+
+/*
+ * BigBird ITC block graph ([S] sec 2 eq 13 and its 12-block example; [B]
+ * sec 2).  N = ceil(n/block) blocks (the last one may be ragged).  Block row
+ * J < global_blocks reads every block.  Any other block row J reads the
+ * window_blocks blocks centred on J (truncated at the ends), blocks
+ * 0..global_blocks-1, and the blocks splitmix64(seed ^ (J*rand_blocks + t))
+ * mod N for t < rand_blocks.  Token i reads token j iff block(j) is allowed
+ * for block(i).
+ *
+ *   block >= 1; window_blocks odd, 1..63; rand_blocks 0..64;
+ *   0 <= global_blocks <= N.
+ * Errors: as diffuser_build_graph.
+ */
+DIFFUSER_API int diffuser_build_block_graph(int64_t n, int32_t block, int32_t window_blocks,
+                               int32_t rand_blocks, int32_t global_blocks, uint64_t seed,
+                               diffuser_graph** out);
+
+/* n and nnz (= number of edges) of a graph; either output may be NULL. */
+DIFFUSER_API int diffuser_graph_info(const diffuser_graph* g, int64_t* n, int64_t* nnz);
+
+/*
+ * Copy the CSR to caller-owned HOST buffers: row_ptr[n+1] (int64, row_ptr[0]
+ * = 0, row_ptr[n] = nnz) and col_idx[nnz] (int32, ascending within a row).
+ */
+DIFFUSER_API int diffuser_graph_copy_csr(const diffuser_graph* g, int64_t* row_ptr, int32_t* col_idx);
+
+/* Release a graph (NULL is a no-op).  No call using it may still be running. */
+DIFFUSER_API void diffuser_graph_free(diffuser_graph* g);
+
+/* ---------------------------------------------------------------- forward */
+
+/*
+ * Bytes of device workspace diffuser_forward needs for this graph and shape.
+ * The workspace holds the stored weights A (fp32, "score once, aggregate K
+ * times", [D] sec 2.4 / 2.6) and the fp32 hop state Z_k.
+ *   B, H >= 1; d == 64; dtype a diffuser_dtype.
+ */
+DIFFUSER_API int diffuser_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32_t d,
+                            int32_t dtype, size_t* bytes);
+
+/*
+ * The hot path ([D] eq S.1-S.5 then eq S.7; [S] eq 1-4):
+ *   A_ij = exp(s_ij - m_i) / sum_{t in N(i)} exp(s_it - m_i),  s_ij = q_i.k_j / sqrt(d)
+ *   Z_0 = V,  Z_{k+1} = (1 - alpha) A Z_k + alpha V  (k < hops),  out = Z_hops
+ * for every (batch, head) unit independently, all units sharing graph g.
+ *
+ *   Q, K, V     device, [B][H][n][d] in `dtype`, n = the graph's n
+ *   out         device, [B][H][n][d] in `dtype`; must not overlap Q or K; may
+ *               equal V only when hops == 0
+ *   hops        K >= 0 (0 copies V to out)
+ *   alpha       restart weight, 0 <= alpha <= 1 (alpha = 0 is allowed: the
+ *               finite recursion is well defined)
+ *   workspace   device, >= diffuser_workspace_size bytes, 256-byte aligned;
+ *               contents on entry are ignored and on return undefined; one
+ *               workspace must not be used by two calls in flight at once
+ *   stream      stream on which everything is enqueued
+ * Precision: A and Z_k are fp32; bf16 outputs are rounded to nearest-even
+ * once, from fp32.  Errors: INVALID_ARG, UNSUPPORTED (d != 64, dtype),
+ * WORKSPACE, CUDA.
+ */
+DIFFUSER_API int diffuser_forward(const void* Q, const void* K, const void* V, int32_t dtype, int64_t B,
+                     int64_t H, int32_t d, const diffuser_graph* g, int32_t hops, float alpha,
+                     void* out, void* workspace, size_t workspace_bytes, diffuser_stream stream);
+
+/*
+ * Bytes of device workspace diffuser_forward_host needs: the forward's
+ * workspace plus device staging for Q, K, V and out.
+ */
+DIFFUSER_API int diffuser_host_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32_t d,
+                                 int32_t dtype, size_t* bytes);
+
+/*
+ * diffuser_forward on HOST buffers: enqueues the host-to-device copies of Q,
+ * K and V, the forward, and the device-to-host copy of out, all on `stream`.
+ * Q, K, V, out are host [B][H][n][d] buffers (page-locked memory makes the
+ * copies asynchronous; pageable memory works but the copies then block).
+ * The caller must synchronize `stream` before reading `out`.
+ * Errors: as diffuser_forward.
+ */
+DIFFUSER_API int diffuser_forward_host(const void* Q, const void* K, const void* V, int32_t dtype, int64_t B,
+                          int64_t H, int32_t d, const diffuser_graph* g, int32_t hops,
+                          float alpha, void* out, void* workspace, size_t workspace_bytes,
+                          diffuser_stream stream);
+
+/* ---------------------------------------------------------------- test exports */
+
+/*
+ * Attention weights only ([D] eq S.1-S.5): writes A for every unit in CSR
+ * edge order to A_out (device, fp32 [B*H][nnz]).  Same arguments and
+ * workspace as diffuser_forward.
+ */
+DIFFUSER_API int diffuser_attention_weights(const void* Q, const void* K, int32_t dtype, int64_t B, int64_t H,
+                               int32_t d, const diffuser_graph* g, float* A_out, void* workspace,
+                               size_t workspace_bytes, diffuser_stream stream);
+
+/*
+ * Diffusion only ([D] eq S.7) on caller-given weights: A (device, fp32
+ * [B*H][nnz] in CSR edge order of g, rows need not sum to 1), V and out as
+ * in diffuser_forward.  Runs the same hop kernels as the forward's general
+ * path.  workspace >= diffuser_workspace_size bytes.
+ */
+DIFFUSER_API int diffuser_diffuse_csr(const diffuser_graph* g, const float* A, const void* V, int32_t dtype,
+                         int64_t B, int64_t H, int32_t d, int32_t hops, float alpha, void* out,
+                         void* workspace, size_t workspace_bytes, diffuser_stream stream);
+
+/* ---------------------------------------------------------------- measurement */
+
+/* Kinds of kernel launch, for the counters below. */
+typedef enum {
+    DIFFUSER_KERNEL_BUILD = 0,    /* graph construction */
+    DIFFUSER_KERNEL_SCORE = 1,    /* scores + masked softmax -> A */
+    DIFFUSER_KERNEL_HOP = 2,      /* one diffusion hop */
+    DIFFUSER_KERNEL_AUX = 3,      /* copies, conversions, split-reduction merges */
+    DIFFUSER_KERNEL_KINDS = 4
+} diffuser_kernel_kind;
+
+/* Number of kernels this library has launched in this process, per kind
+ * (array of DIFFUSER_KERNEL_KINDS entries; may be NULL) and in total (return
+ * value). */
+DIFFUSER_API int64_t diffuser_launch_count(int64_t* per_kind);
+
+/*
+ * Device-time profiling of the library's own kernels.  Between begin and
+ * end, every launch is bracketed by CUDA events recorded on the stream it is
+ * launched on.  end synchronizes those events and writes, per kind, the
+ * summed device milliseconds and the number of launches (arrays of
+ * DIFFUSER_KERNEL_KINDS entries).  Thread-safe; one profile at a time.
+ */
+DIFFUSER_API int diffuser_profile_begin(void);
+DIFFUSER_API int diffuser_profile_end(double* ms_per_kind, int64_t* launches_per_kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIFFUSER_H */

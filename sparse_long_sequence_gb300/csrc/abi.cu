@@ -1,0 +1,491 @@
+// C ABI of libdiffuser: argument checks, graph objects, workspace layout,
+// launch sequence, launch accounting and device-time profiling.  Every entry
+// point returns a status and never lets a C++ exception out.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace dfs {
+
+namespace {
+thread_local std::string g_last_error;
+
+std::atomic<int64_t> g_launches[DIFFUSER_KERNEL_KINDS];
+
+// ---- profiler: events recorded around launches while a profile is open ----
+struct ProfileRecord {
+    int kind;
+    cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfileRecord> g_prof_records;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool mul_overflows(size_t a, size_t b, size_t* out) {
+    if (a != 0 && b > SIZE_MAX / a) return true;
+    *out = a * b;
+    return false;
+}
+}  // namespace
+
+int fail(int status, const std::string& msg) {
+    g_last_error = msg;
+    return status;
+}
+
+int cuda_fail(cudaError_t err, const char* what) {
+    g_last_error = std::string(what) + ": " + cudaGetErrorString(err);
+    return DIFFUSER_ERR_CUDA;
+}
+
+LaunchScope::LaunchScope(diffuser_kernel_kind kind, cudaStream_t stream) : stream_(stream) {
+    g_launches[kind].fetch_add(1, std::memory_order_relaxed);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return;
+    cudaEvent_t a = take_event(), b = take_event();
+    if (!a || !b) return;
+    cudaEventRecord(a, stream);
+    g_prof_records.push_back({(int)kind, a, b});
+    slot_ = (int)g_prof_records.size() - 1;
+}
+
+LaunchScope::~LaunchScope() {
+    if (slot_ < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (slot_ < (int)g_prof_records.size()) cudaEventRecord(g_prof_records[slot_].stop, stream_);
+}
+
+// ---- workspace layout ---------------------------------------------------------
+// [A: units*nnz fp32][Z ping: units*n*64 fp32][Z pong: units*n*64 fp32]
+struct Layout {
+    size_t a_off, z0_off, z1_off, total;
+};
+
+int plan_layout(const diffuser_graph* g, int64_t B, int64_t H, Layout* L) {
+    size_t units = (size_t)B * (size_t)H;
+    size_t a_bytes, z_elems, z_bytes;
+    if (mul_overflows(units, (size_t)g->nnz, &a_bytes) || mul_overflows(a_bytes, 4, &a_bytes) ||
+        mul_overflows(units, (size_t)g->n * kHeadDim, &z_elems) ||
+        mul_overflows(z_elems, 4, &z_bytes))
+        return fail(DIFFUSER_ERR_OVERFLOW, "workspace size overflows size_t");
+    L->a_off = 0;
+    L->z0_off = align_up(a_bytes);
+    L->z1_off = L->z0_off + align_up(z_bytes);
+    L->total = L->z1_off + align_up(z_bytes);
+    return DIFFUSER_OK;
+}
+
+int check_shape(const diffuser_graph* g, int64_t B, int64_t H, int32_t d, int32_t dtype) {
+    if (!g) return fail(DIFFUSER_ERR_INVALID_ARG, "graph is NULL");
+    if (B < 1 || H < 1 || B > (int64_t(1) << 31) || H > (int64_t(1) << 31))
+        return fail(DIFFUSER_ERR_INVALID_ARG, "B and H must be >= 1");
+    if (d != kHeadDim) return fail(DIFFUSER_ERR_UNSUPPORTED, "head width d must be 64");
+    if (dtype != DIFFUSER_DTYPE_FP32 && dtype != DIFFUSER_DTYPE_BF16)
+        return fail(DIFFUSER_ERR_UNSUPPORTED, "dtype must be FP32 or BF16");
+    return DIFFUSER_OK;
+}
+
+int check_device(const diffuser_graph* g) {
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+    if (dev != g->device)
+        return fail(DIFFUSER_ERR_INVALID_ARG, "the current device is not the graph's device");
+    return DIFFUSER_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t io_bytes(const diffuser_graph* g, int64_t B, int64_t H, int32_t dtype) {
+    return (size_t)B * H * g->n * kHeadDim * (dtype == DIFFUSER_DTYPE_BF16 ? 2 : 4);
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int check_workspace(const Layout& L, void* ws, size_t ws_bytes) {
+    if (!ws) return fail(DIFFUSER_ERR_WORKSPACE, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign)
+        return fail(DIFFUSER_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < L.total)
+        return fail(DIFFUSER_ERR_WORKSPACE, "workspace too small: need " +
+                                                std::to_string(L.total) + " bytes");
+    return DIFFUSER_OK;
+}
+
+// The hops over weights already in A (CSR order): Z_0 = V, last hop -> out.
+int run_hops_csr(const diffuser_graph* g, const CsrArgs& a, const float* A, const void* V,
+                 int32_t dtype, int32_t hops, float alpha, void* out, char* ws, const Layout& L,
+                 cudaStream_t stream) {
+    if (hops == 0) {
+        if (out == V) return DIFFUSER_OK;
+        size_t bytes = io_bytes(g, a.units, 1, dtype);
+        cudaError_t err = cudaMemcpyAsync(out, V, bytes, cudaMemcpyDeviceToDevice, stream);
+        return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "copying V to out (hops = 0)");
+    }
+    float* zbuf[2] = {reinterpret_cast<float*>(ws + L.z0_off),
+                      reinterpret_cast<float*>(ws + L.z1_off)};
+    for (int32_t k = 0; k < hops; ++k) {
+        const bool first = (k == 0), last = (k == hops - 1);
+        const void* src = first ? V : zbuf[(k - 1) & 1];
+        void* dst = last ? out : zbuf[k & 1];
+        int st = launch_hop_csr(a, A, src, first, V, dst, last, dtype, alpha, stream);
+        if (st != DIFFUSER_OK) return st;
+    }
+    return DIFFUSER_OK;
+}
+
+int forward_device(const void* Q, const void* K, const void* V, int32_t dtype, int64_t B,
+                   int64_t H, int32_t d, const diffuser_graph* g, int32_t hops, float alpha,
+                   void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    int st = check_shape(g, B, H, d, dtype);
+    if (st) return st;
+    if (!Q || !K || !V || !out) return fail(DIFFUSER_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out))
+        return fail(DIFFUSER_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+    if (hops < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "hops must be >= 0");
+    if (!(alpha >= 0.f && alpha <= 1.f))
+        return fail(DIFFUSER_ERR_INVALID_ARG, "alpha must lie in [0, 1]");
+    const size_t bytes = io_bytes(g, B, H, dtype);
+    if (overlaps(out, bytes, Q, bytes) || overlaps(out, bytes, K, bytes))
+        return fail(DIFFUSER_ERR_INVALID_ARG, "out overlaps Q or K");
+    if (hops > 0 && overlaps(out, bytes, V, bytes))
+        return fail(DIFFUSER_ERR_INVALID_ARG, "out may alias V only when hops == 0");
+    Layout L;
+    if ((st = plan_layout(g, B, H, &L))) return st;
+    if ((st = check_workspace(L, workspace, workspace_bytes))) return st;
+    if ((st = check_device(g))) return st;
+
+    char* ws = static_cast<char*>(workspace);
+    CsrArgs a{g->d_row_ptr, g->d_col, g->n, g->nnz, B * H};
+    if (hops == 0) return run_hops_csr(g, a, nullptr, V, dtype, 0, alpha, out, ws, L, stream);
+    float* A = reinterpret_cast<float*>(ws + L.a_off);
+    if ((st = launch_score_csr(a, Q, K, dtype, A, stream))) return st;
+    return run_hops_csr(g, a, A, V, dtype, hops, alpha, out, ws, L, stream);
+}
+
+int new_graph(diffuser_graph** out, diffuser_graph** g) {
+    if (!out) return fail(DIFFUSER_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    *g = new (std::nothrow) diffuser_graph();
+    if (!*g) return fail(DIFFUSER_ERR_ALLOC, "host allocation failed");
+    cudaError_t err = cudaGetDevice(&(*g)->device);
+    if (err != cudaSuccess) {
+        delete *g;
+        *g = nullptr;
+        return cuda_fail(err, "cudaGetDevice");
+    }
+    return DIFFUSER_OK;
+}
+
+int finish_graph(int status, diffuser_graph* g, diffuser_graph** out) {
+    if (status != DIFFUSER_OK) {
+        diffuser_graph_free(g);
+        return status;
+    }
+    *out = g;
+    return DIFFUSER_OK;
+}
+
+}  // namespace dfs
+
+using namespace dfs;
+
+extern "C" {
+
+const char* diffuser_status_string(int status) {
+    switch (status) {
+        case DIFFUSER_OK: return "ok";
+        case DIFFUSER_ERR_INVALID_ARG: return "invalid argument";
+        case DIFFUSER_ERR_UNSUPPORTED: return "unsupported dtype, head width or option";
+        case DIFFUSER_ERR_OVERFLOW: return "size overflows its index type";
+        case DIFFUSER_ERR_ALLOC: return "allocation failed";
+        case DIFFUSER_ERR_CUDA: return "CUDA runtime error";
+        case DIFFUSER_ERR_DEVICE: return "a kernel reported an error";
+        case DIFFUSER_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        default: return "unknown status";
+    }
+}
+
+const char* diffuser_last_error(void) { return g_last_error.c_str(); }
+
+int diffuser_version(void) { return 100; }
+
+int diffuser_build_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* global_idx,
+                         int32_t rand_per_row, uint64_t seed, diffuser_graph** out) {
+    try {
+        if (n < 1 || n > INT32_MAX) return fail(DIFFUSER_ERR_INVALID_ARG, "n out of range");
+        if (r < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "r must be >= 0");
+        if (n_globals < 0 || n_globals > n)
+            return fail(DIFFUSER_ERR_INVALID_ARG, "n_globals out of range");
+        if (rand_per_row < 0 || rand_per_row > kMaxRandPerRow)
+            return fail(DIFFUSER_ERR_INVALID_ARG, "rand_per_row must lie in [0, 1024]");
+        std::vector<int32_t> G(n_globals);
+        for (int32_t t = 0; t < n_globals; ++t) {
+            G[t] = global_idx ? global_idx[t] : t;
+            if (G[t] < 0 || G[t] >= n || (t > 0 && G[t] <= G[t - 1]))
+                return fail(DIFFUSER_ERR_INVALID_ARG,
+                            "global positions must be strictly increasing in [0, n)");
+        }
+        // the CSR must stay addressable: a crude upper bound on nnz
+        const double bound = (double)n * ((double)n_globals + 2.0 * r + 1 + rand_per_row) +
+                             (double)n_globals * n;
+        if (bound > (double)kMaxNnz * 4)
+            return fail(DIFFUSER_ERR_OVERFLOW, "graph too large");
+        diffuser_graph* g = nullptr;
+        int st = new_graph(out, &g);
+        if (st) return st;
+        g->kind = kTokenGraph;
+        g->n = n;
+        g->r = r;
+        g->n_globals = n_globals;
+        g->rand_per_row = rand_per_row;
+        g->seed = seed;
+        g->h_globals = std::move(G);
+        st = build_token_graph_device(g, nullptr);
+        return finish_graph(st, g, out);
+    } catch (const std::bad_alloc&) {
+        return fail(DIFFUSER_ERR_ALLOC, "host allocation failed");
+    } catch (...) {
+        return fail(DIFFUSER_ERR_INVALID_ARG, "unexpected exception");
+    }
+}
+
+int diffuser_build_block_graph(int64_t n, int32_t block, int32_t window_blocks,
+                               int32_t rand_blocks, int32_t global_blocks, uint64_t seed,
+                               diffuser_graph** out) {
+    try {
+        if (n < 1 || n > INT32_MAX) return fail(DIFFUSER_ERR_INVALID_ARG, "n out of range");
+        if (block < 1) return fail(DIFFUSER_ERR_INVALID_ARG, "block must be >= 1");
+        if (window_blocks < 1 || window_blocks > kMaxWindowBlocks || window_blocks % 2 == 0)
+            return fail(DIFFUSER_ERR_INVALID_ARG, "window_blocks must be odd, 1..63");
+        if (rand_blocks < 0 || rand_blocks > kMaxRandBlocks)
+            return fail(DIFFUSER_ERR_INVALID_ARG, "rand_blocks must lie in [0, 64]");
+        const int64_t nb = (n + block - 1) / block;
+        if (global_blocks < 0 || global_blocks > nb)
+            return fail(DIFFUSER_ERR_INVALID_ARG, "global_blocks must lie in [0, ceil(n/block)]");
+        diffuser_graph* g = nullptr;
+        int st = new_graph(out, &g);
+        if (st) return st;
+        g->kind = kBlockGraph;
+        g->n = n;
+        g->block = block;
+        g->window_blocks = window_blocks;
+        g->rand_blocks = rand_blocks;
+        g->global_blocks = global_blocks;
+        g->seed = seed;
+        st = build_block_graph_device(g, nullptr);
+        return finish_graph(st, g, out);
+    } catch (const std::bad_alloc&) {
+        return fail(DIFFUSER_ERR_ALLOC, "host allocation failed");
+    } catch (...) {
+        return fail(DIFFUSER_ERR_INVALID_ARG, "unexpected exception");
+    }
+}
+
+int diffuser_graph_info(const diffuser_graph* g, int64_t* n, int64_t* nnz) {
+    if (!g) return fail(DIFFUSER_ERR_INVALID_ARG, "graph is NULL");
+    if (n) *n = g->n;
+    if (nnz) *nnz = g->nnz;
+    return DIFFUSER_OK;
+}
+
+int diffuser_graph_copy_csr(const diffuser_graph* g, int64_t* row_ptr, int32_t* col_idx) {
+    if (!g || !row_ptr || !col_idx) return fail(DIFFUSER_ERR_INVALID_ARG, "NULL argument");
+    std::memcpy(row_ptr, g->h_row_ptr.data(), sizeof(int64_t) * (g->n + 1));
+    std::memcpy(col_idx, g->h_col.data(), sizeof(int32_t) * g->nnz);
+    return DIFFUSER_OK;
+}
+
+void diffuser_graph_free(diffuser_graph* g) {
+    if (!g) return;
+    cudaFree(g->d_row_ptr);
+    cudaFree(g->d_col);
+    cudaFree(g->d_globals);
+    cudaFree(g->d_is_global);
+    delete g;
+}
+
+int diffuser_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32_t d,
+                            int32_t dtype, size_t* bytes) {
+    int st = check_shape(g, B, H, d, dtype);
+    if (st) return st;
+    if (!bytes) return fail(DIFFUSER_ERR_INVALID_ARG, "bytes is NULL");
+    Layout L;
+    if ((st = plan_layout(g, B, H, &L))) return st;
+    *bytes = L.total;
+    return DIFFUSER_OK;
+}
+
+int diffuser_forward(const void* Q, const void* K, const void* V, int32_t dtype, int64_t B,
+                     int64_t H, int32_t d, const diffuser_graph* g, int32_t hops, float alpha,
+                     void* out, void* workspace, size_t workspace_bytes, diffuser_stream stream) {
+    try {
+        return forward_device(Q, K, V, dtype, B, H, d, g, hops, alpha, out, workspace,
+                              workspace_bytes, stream);
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+int diffuser_host_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32_t d,
+                                 int32_t dtype, size_t* bytes) {
+    size_t base = 0;
+    int st = diffuser_workspace_size(g, B, H, d, dtype, &base);
+    if (st) return st;
+    *bytes = base + 4 * align_up(io_bytes(g, B, H, dtype));
+    return DIFFUSER_OK;
+}
+
+int diffuser_forward_host(const void* Q, const void* K, const void* V, int32_t dtype, int64_t B,
+                          int64_t H, int32_t d, const diffuser_graph* g, int32_t hops,
+                          float alpha, void* out, void* workspace, size_t workspace_bytes,
+                          diffuser_stream stream) {
+    try {
+        int st = check_shape(g, B, H, d, dtype);
+        if (st) return st;
+        if (!Q || !K || !V || !out) return fail(DIFFUSER_ERR_INVALID_ARG, "a pointer is NULL");
+        size_t need = 0;
+        if ((st = diffuser_host_workspace_size(g, B, H, d, dtype, &need))) return st;
+        if (!workspace || reinterpret_cast<uintptr_t>(workspace) % kAlign)
+            return fail(DIFFUSER_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+        if (workspace_bytes < need)
+            return fail(DIFFUSER_ERR_WORKSPACE, "workspace too small: need " +
+                                                    std::to_string(need) + " bytes");
+        if ((st = check_device(g))) return st;
+        const size_t bytes = io_bytes(g, B, H, dtype), slot = align_up(bytes);
+        char* ws = static_cast<char*>(workspace);
+        char* dQ = ws;
+        char* dK = ws + slot;
+        char* dV = ws + 2 * slot;
+        char* dO = ws + 3 * slot;
+        cudaError_t err = cudaMemcpyAsync(dQ, Q, bytes, cudaMemcpyHostToDevice, stream);
+        if (err == cudaSuccess) err = cudaMemcpyAsync(dK, K, bytes, cudaMemcpyHostToDevice, stream);
+        if (err == cudaSuccess) err = cudaMemcpyAsync(dV, V, bytes, cudaMemcpyHostToDevice, stream);
+        if (err != cudaSuccess) return cuda_fail(err, "host-to-device copies");
+        st = forward_device(dQ, dK, dV, dtype, B, H, d, g, hops, alpha, dO, ws + 4 * slot,
+                            workspace_bytes - 4 * slot, stream);
+        if (st) return st;
+        err = cudaMemcpyAsync(out, dO, bytes, cudaMemcpyDeviceToHost, stream);
+        return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "device-to-host copy");
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+int diffuser_attention_weights(const void* Q, const void* K, int32_t dtype, int64_t B, int64_t H,
+                               int32_t d, const diffuser_graph* g, float* A_out, void* workspace,
+                               size_t workspace_bytes, diffuser_stream stream) {
+    try {
+        int st = check_shape(g, B, H, d, dtype);
+        if (st) return st;
+        if (!Q || !K || !A_out) return fail(DIFFUSER_ERR_INVALID_ARG, "a pointer is NULL");
+        if (!aligned16(Q) || !aligned16(K) || !aligned16(A_out))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+        Layout L;
+        if ((st = plan_layout(g, B, H, &L))) return st;
+        if ((st = check_workspace(L, workspace, workspace_bytes))) return st;
+        if ((st = check_device(g))) return st;
+        CsrArgs a{g->d_row_ptr, g->d_col, g->n, g->nnz, B * H};
+        return launch_score_csr(a, Q, K, dtype, A_out, stream);
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+int diffuser_diffuse_csr(const diffuser_graph* g, const float* A, const void* V, int32_t dtype,
+                         int64_t B, int64_t H, int32_t d, int32_t hops, float alpha, void* out,
+                         void* workspace, size_t workspace_bytes, diffuser_stream stream) {
+    try {
+        int st = check_shape(g, B, H, d, dtype);
+        if (st) return st;
+        if (!A || !V || !out) return fail(DIFFUSER_ERR_INVALID_ARG, "a pointer is NULL");
+        if (!aligned16(A) || !aligned16(V) || !aligned16(out))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+        if (hops < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "hops must be >= 0");
+        if (!(alpha >= 0.f && alpha <= 1.f))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "alpha must lie in [0, 1]");
+        const size_t bytes = io_bytes(g, B, H, dtype);
+        if (hops > 0 && overlaps(out, bytes, V, bytes))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "out may alias V only when hops == 0");
+        Layout L;
+        if ((st = plan_layout(g, B, H, &L))) return st;
+        if ((st = check_workspace(L, workspace, workspace_bytes))) return st;
+        if ((st = check_device(g))) return st;
+        CsrArgs a{g->d_row_ptr, g->d_col, g->n, g->nnz, B * H};
+        return run_hops_csr(g, a, A, V, dtype, hops, alpha, out, static_cast<char*>(workspace),
+                            L, stream);
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+int64_t diffuser_launch_count(int64_t* per_kind) {
+    int64_t total = 0;
+    for (int k = 0; k < DIFFUSER_KERNEL_KINDS; ++k) {
+        int64_t v = g_launches[k].load(std::memory_order_relaxed);
+        if (per_kind) per_kind[k] = v;
+        total += v;
+    }
+    return total;
+}
+
+int diffuser_profile_begin(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof_on) return fail(DIFFUSER_ERR_INVALID_ARG, "a profile is already open");
+    g_prof_on = true;
+    g_prof_records.clear();
+    return DIFFUSER_OK;
+}
+
+int diffuser_profile_end(double* ms_per_kind, int64_t* launches_per_kind) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return fail(DIFFUSER_ERR_INVALID_ARG, "no profile is open");
+    g_prof_on = false;
+    double ms[DIFFUSER_KERNEL_KINDS] = {0};
+    int64_t cnt[DIFFUSER_KERNEL_KINDS] = {0};
+    int status = DIFFUSER_OK;
+    for (auto& r : g_prof_records) {
+        cudaError_t err = cudaEventSynchronize(r.stop);
+        float t = 0.f;
+        if (err == cudaSuccess) err = cudaEventElapsedTime(&t, r.start, r.stop);
+        if (err != cudaSuccess && status == DIFFUSER_OK) status = cuda_fail(err, "profile events");
+        ms[r.kind] += t;
+        cnt[r.kind] += 1;
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_prof_records.clear();
+    for (int k = 0; k < DIFFUSER_KERNEL_KINDS; ++k) {
+        if (ms_per_kind) ms_per_kind[k] = ms[k];
+        if (launches_per_kind) launches_per_kind[k] = cnt[k];
+    }
+    return status;
+}
+
+}  // extern "C"

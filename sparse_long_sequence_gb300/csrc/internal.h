@@ -1,0 +1,91 @@
+// Internal declarations of libdiffuser (host dispatch <-> kernels).  Not part
+// of the public ABI; see include/diffuser.h for that.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/diffuser.h"
+
+namespace dfs {
+
+constexpr int kHeadDim = 64;          // d = d_h = d_v, fixed by the kernels
+constexpr int32_t kMaxRandPerRow = 1024;
+constexpr int32_t kMaxWindowBlocks = 63;
+constexpr int32_t kMaxRandBlocks = 64;
+constexpr int64_t kMaxNnz = int64_t(1) << 40;
+
+enum GraphKind { kTokenGraph = 0, kBlockGraph = 1 };
+
+}  // namespace dfs
+
+struct diffuser_graph {
+    int kind = dfs::kTokenGraph;
+    int device = 0;
+    int64_t n = 0;
+    int64_t nnz = 0;
+    // token graph parameters
+    int32_t r = 0, n_globals = 0, rand_per_row = 0;
+    // block graph parameters
+    int32_t block = 0, window_blocks = 0, rand_blocks = 0, global_blocks = 0;
+    uint64_t seed = 0;
+    // device CSR
+    int64_t* d_row_ptr = nullptr;
+    int32_t* d_col = nullptr;
+    int32_t* d_globals = nullptr;     // token graph: sorted global positions
+    uint8_t* d_is_global = nullptr;   // token graph: per-position flag
+    // host copy of the CSR
+    std::vector<int64_t> h_row_ptr;
+    std::vector<int32_t> h_col;
+    std::vector<int32_t> h_globals;
+};
+
+namespace dfs {
+
+// ---- status plumbing (abi.cu) -------------------------------------------------
+int fail(int status, const std::string& msg);
+int cuda_fail(cudaError_t err, const char* what);
+
+// ---- launch accounting and profiling (abi.cu) ------------------------------
+// Brackets one kernel launch: counts it and, while a profile is open, records
+// CUDA events around it on `stream`.
+class LaunchScope {
+  public:
+    LaunchScope(diffuser_kernel_kind kind, cudaStream_t stream);
+    ~LaunchScope();
+    LaunchScope(const LaunchScope&) = delete;
+    LaunchScope& operator=(const LaunchScope&) = delete;
+
+  private:
+    int slot_ = -1;
+    cudaStream_t stream_;
+};
+
+// ---- graph construction kernels (graph_build.cu) ---------------------------
+int build_token_graph_device(diffuser_graph* g, cudaStream_t stream);
+int build_block_graph_device(diffuser_graph* g, cudaStream_t stream);
+
+// ---- CSR SIMT path (simt_path.cu) ------------------------------------------
+struct CsrArgs {
+    const int64_t* row_ptr;
+    const int32_t* col;
+    int64_t n;
+    int64_t nnz;
+    int64_t units;   // B*H
+};
+
+// A[u][e] = masked row softmax of q_i.k_j / sqrt(64), CSR edge order.
+int launch_score_csr(const CsrArgs& a, const void* Q, const void* K, int32_t dtype, float* A,
+                     cudaStream_t stream);
+
+// One PPR hop over CSR weights:  dst = (1-alpha) * A src + alpha * V.
+//   src is the I/O dtype when src_is_io (hop 0 reads V), fp32 otherwise;
+//   dst is the I/O dtype when dst_is_io (the last hop writes out), fp32 otherwise.
+int launch_hop_csr(const CsrArgs& a, const float* A, const void* src, bool src_is_io,
+                   const void* V, void* dst, bool dst_is_io, int32_t dtype, float alpha,
+                   cudaStream_t stream);
+
+}  // namespace dfs

@@ -1,0 +1,225 @@
+// CSR SIMT path: general over any graph, fp32 arithmetic throughout.  It is
+// the path for fp32 I/O (whose error budget rules out tf32 tensor cores) and
+// for graphs without a fast layout, and the reference implementation the
+// tensor-core kernels are checked against on the device.
+//
+//  * score_csr_kernel: one warp per (unit, row).  Lanes take edges
+//    round-robin; each lane holds q_i (64 fp32 registers) and dots it with
+//    k_j, keeping an online (max, sum) pair; the pairs are merged across the
+//    warp, then each lane normalises the weights it wrote.
+//    ("Diffuser: modelling long sequences with multi-hop attention
+//    diffusion", eq S.1-S.5; "1.2.1 Static sparsity", eq 1-3.)
+//  * hop_csr_kernel: one warp per (unit, row).  Lanes own two of the 64
+//    features; for each edge the warp reads one 256-byte (fp32) or 128-byte
+//    (bf16) row of Z_k, coalesced, and accumulates A_ij * Z_k[j]; the
+//    restart term is fused:  dst_i = (1 - alpha) acc + alpha V_i
+//    (same Diffuser notes, sec 2.4 eq S.7).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace dfs {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Load a 64-wide row (fp32 or bf16) into 64 fp32 registers.
+template <bool kBf16>
+__device__ __forceinline__ void load_row64(const void* base, float (&x)[64]) {
+    if constexpr (kBf16) {
+        const uint4* p = reinterpret_cast<const uint4*>(base);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint4 v = __ldg(p + c);
+            x[8 * c + 0] = bf16lo(v.x); x[8 * c + 1] = bf16hi(v.x);
+            x[8 * c + 2] = bf16lo(v.y); x[8 * c + 3] = bf16hi(v.y);
+            x[8 * c + 4] = bf16lo(v.z); x[8 * c + 5] = bf16hi(v.z);
+            x[8 * c + 6] = bf16lo(v.w); x[8 * c + 7] = bf16hi(v.w);
+        }
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(base);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            float4 v = __ldg(p + c);
+            x[4 * c + 0] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
+        }
+    }
+}
+
+// q . k over 64 features, k streamed in 16-byte pieces.
+template <bool kBf16>
+__device__ __forceinline__ float dot64(const float (&q)[64], const void* kbase) {
+    float acc = 0.f;
+    if constexpr (kBf16) {
+        const uint4* p = reinterpret_cast<const uint4*>(kbase);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint4 v = __ldg(p + c);
+            acc = fmaf(q[8 * c + 0], bf16lo(v.x), acc); acc = fmaf(q[8 * c + 1], bf16hi(v.x), acc);
+            acc = fmaf(q[8 * c + 2], bf16lo(v.y), acc); acc = fmaf(q[8 * c + 3], bf16hi(v.y), acc);
+            acc = fmaf(q[8 * c + 4], bf16lo(v.z), acc); acc = fmaf(q[8 * c + 5], bf16hi(v.z), acc);
+            acc = fmaf(q[8 * c + 6], bf16lo(v.w), acc); acc = fmaf(q[8 * c + 7], bf16hi(v.w), acc);
+        }
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(kbase);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            float4 v = __ldg(p + c);
+            acc = fmaf(q[4 * c + 0], v.x, acc); acc = fmaf(q[4 * c + 1], v.y, acc);
+            acc = fmaf(q[4 * c + 2], v.z, acc); acc = fmaf(q[4 * c + 3], v.w, acc);
+        }
+    }
+    return acc;
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+score_csr_kernel(CsrArgs a, const void* __restrict__ Q, const void* __restrict__ K,
+                 float* __restrict__ A) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (gw >= a.units * a.n) return;
+    const int64_t u = gw / a.n, i = gw - u * a.n;
+    const size_t esz = kBf16 ? 2 : 4;
+    const char* Qb = static_cast<const char*>(Q) + (size_t)u * a.n * kHeadDim * esz;
+    const char* Kb = static_cast<const char*>(K) + (size_t)u * a.n * kHeadDim * esz;
+    float* Au = A + (size_t)u * a.nnz;
+
+    float q[64];
+    load_row64<kBf16>(Qb + (size_t)i * kHeadDim * esz, q);
+    const float scale = 0.125f;  // 1/sqrt(64), exact
+    const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+
+    float m = -INFINITY, l = 0.f;
+    for (int64_t e = e0 + lane; e < e1; e += 32) {
+        const int64_t j = a.col[e];
+        float s = dot64<kBf16>(q, Kb + (size_t)j * kHeadDim * esz) * scale;
+        Au[e] = s;
+        if (s > m) { l = l * expf(m - s) + 1.f; m = s; }
+        else       { l += expf(s - m); }
+    }
+    // merge the per-lane (max, sum) pairs
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+        float mm = fmaxf(m, m2);
+        float a1 = (m == -INFINITY) ? 0.f : l * expf(m - mm);
+        float a2 = (m2 == -INFINITY) ? 0.f : l2 * expf(m2 - mm);
+        m = mm;
+        l = a1 + a2;
+    }
+    for (int64_t e = e0 + lane; e < e1; e += 32) Au[e] = expf(Au[e] - m) / l;
+}
+
+template <typename T> struct Pair;
+template <> struct Pair<float> {
+    static __device__ __forceinline__ float2 load(const float* p) {
+        return *reinterpret_cast<const float2*>(p);
+    }
+};
+template <> struct Pair<__nv_bfloat16> {
+    static __device__ __forceinline__ float2 load(const __nv_bfloat16* p) {
+        uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+        return make_float2(bf16lo(w), bf16hi(w));
+    }
+};
+
+__device__ __forceinline__ void store_pair(float* p, float2 v) {
+    *reinterpret_cast<float2*>(p) = v;
+}
+__device__ __forceinline__ void store_pair(__nv_bfloat16* p, float2 v) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
+}
+
+template <typename TSrc, typename TV, typename TDst>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+hop_csr_kernel(CsrArgs a, const float* __restrict__ A, const TSrc* __restrict__ src,
+               const TV* __restrict__ V, TDst* __restrict__ dst, float alpha) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (gw >= a.units * a.n) return;
+    const int64_t u = gw / a.n, i = gw - u * a.n;
+    const size_t unit = (size_t)u * a.n * kHeadDim;
+    const TSrc* Z = src + unit + 2 * lane;
+    const float* Au = A + (size_t)u * a.nnz;
+    const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+
+    float2 acc = make_float2(0.f, 0.f);
+    for (int64_t base = e0; base < e1; base += 32) {
+        const int64_t e = base + lane;
+        const float a_l = e < e1 ? Au[e] : 0.f;
+        const int32_t j_l = e < e1 ? a.col[e] : 0;
+        const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
+#pragma unroll 8
+        for (int t = 0; t < cnt; ++t) {
+            const float w = __shfl_sync(0xffffffffu, a_l, t);
+            const int32_t j = __shfl_sync(0xffffffffu, j_l, t);
+            const float2 z = Pair<TSrc>::load(Z + (size_t)j * kHeadDim);
+            acc.x = fmaf(w, z.x, acc.x);
+            acc.y = fmaf(w, z.y, acc.y);
+        }
+    }
+    const float2 v = Pair<TV>::load(V + unit + (size_t)i * kHeadDim + 2 * lane);
+    const float keep = 1.f - alpha;
+    float2 r = make_float2(fmaf(keep, acc.x, alpha * v.x), fmaf(keep, acc.y, alpha * v.y));
+    store_pair(dst + unit + (size_t)i * kHeadDim + 2 * lane, r);
+}
+
+unsigned grid_for(const CsrArgs& a) {
+    return (unsigned)((a.units * a.n + kWarpsPerBlock - 1) / kWarpsPerBlock);
+}
+
+template <typename TIo>
+int hop_dispatch(const CsrArgs& a, const float* A, const void* src, bool src_is_io,
+                 const void* V, void* dst, bool dst_is_io, float alpha, cudaStream_t stream) {
+    const TIo* v = static_cast<const TIo*>(V);
+    dim3 grid(grid_for(a)), block(kWarpsPerBlock * 32);
+    LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
+    if (src_is_io && dst_is_io)
+        hop_csr_kernel<TIo, TIo, TIo><<<grid, block, 0, stream>>>(
+            a, A, static_cast<const TIo*>(src), v, static_cast<TIo*>(dst), alpha);
+    else if (src_is_io)
+        hop_csr_kernel<TIo, TIo, float><<<grid, block, 0, stream>>>(
+            a, A, static_cast<const TIo*>(src), v, static_cast<float*>(dst), alpha);
+    else if (dst_is_io)
+        hop_csr_kernel<float, TIo, TIo><<<grid, block, 0, stream>>>(
+            a, A, static_cast<const float*>(src), v, static_cast<TIo*>(dst), alpha);
+    else
+        hop_csr_kernel<float, TIo, float><<<grid, block, 0, stream>>>(
+            a, A, static_cast<const float*>(src), v, static_cast<float*>(dst), alpha);
+    cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_csr_kernel");
+}
+
+}  // namespace
+
+int launch_score_csr(const CsrArgs& a, const void* Q, const void* K, int32_t dtype, float* A,
+                     cudaStream_t stream) {
+    dim3 grid(grid_for(a)), block(kWarpsPerBlock * 32);
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
+        if (dtype == DIFFUSER_DTYPE_BF16)
+            score_csr_kernel<true><<<grid, block, 0, stream>>>(a, Q, K, A);
+        else
+            score_csr_kernel<false><<<grid, block, 0, stream>>>(a, Q, K, A);
+    }
+    cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "score_csr_kernel");
+}
+
+int launch_hop_csr(const CsrArgs& a, const float* A, const void* src, bool src_is_io,
+                   const void* V, void* dst, bool dst_is_io, int32_t dtype, float alpha,
+                   cudaStream_t stream) {
+    if (dtype == DIFFUSER_DTYPE_BF16)
+        return hop_dispatch<__nv_bfloat16>(a, A, src, src_is_io, V, dst, dst_is_io, alpha, stream);
+    return hop_dispatch<float>(a, A, src, src_is_io, V, dst, dst_is_io, alpha, stream);
+}
+
+}  // namespace dfs

@@ -1,0 +1,277 @@
+"""GPU parity of the CUDA path against the fp64 oracle, through the C ABI.
+
+Graphs must match bit for bit; outputs within the tolerances in helpers.py.
+Small cases span several tiles and ragged tails; the full-size workloads run
+in the benchmark's launch configuration and are compared on sampled units
+(whole (batch, head) units, which the oracle computes independently), plus
+properties that hold at any size for every unit.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_long_sequence_gb300 import synthetic, workloads
+from tests.helpers import check_output, to_device, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dl():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_long_sequence_gb300 import binding
+    return binding
+
+
+def oracle_graph(w_or_args, kind="token"):
+    if kind == "token":
+        return oracle.token_graph(**w_or_args)
+    return oracle.block_graph(**w_or_args)
+
+
+def build_graph(dl, args, kind="token"):
+    if kind == "token":
+        a = dict(args)
+        gi = a.pop("globals_idx", None)
+        return dl.diffuser_build_graph(a["n"], a["r"], a["n_globals"], global_idx=gi,
+                                       rand_per_row=a["rand_per_row"], seed=a["seed"])
+    return dl.diffuser_build_block_graph(**args)
+
+
+# ---------------------------------------------------------------- graphs (bit-exact)
+TOKEN_CASES = [
+    dict(n=1, r=0, n_globals=0, rand_per_row=0, seed=0),
+    dict(n=1, r=5, n_globals=1, rand_per_row=3, seed=0),
+    dict(n=2, r=0, n_globals=0, rand_per_row=3, seed=7),
+    dict(n=17, r=2, n_globals=2, rand_per_row=4, seed=0),
+    dict(n=300, r=8, n_globals=3, rand_per_row=5, seed=0),
+    dict(n=500, r=0, n_globals=0, rand_per_row=40, seed=99),
+    dict(n=640, r=600, n_globals=5, rand_per_row=2, seed=3),
+    dict(n=1000, r=31, n_globals=0, rand_per_row=0, seed=0),
+    dict(n=777, r=13, n_globals=4, rand_per_row=9, seed=2 ** 63 + 11, globals_idx=[0, 100, 401, 776]),
+    dict(n=4096, r=256, n_globals=16, rand_per_row=32, seed=1),
+]
+BLOCK_CASES = [
+    dict(n=50, block=16, window_blocks=3, rand_blocks=1, global_blocks=1, seed=0),
+    dict(n=1000, block=64, window_blocks=3, rand_blocks=3, global_blocks=2, seed=0),
+    dict(n=48, block=4, window_blocks=3, rand_blocks=2, global_blocks=1, seed=0),
+    dict(n=130, block=64, window_blocks=5, rand_blocks=3, global_blocks=0, seed=5),
+    dict(n=7, block=64, window_blocks=1, rand_blocks=0, global_blocks=1, seed=0),
+]
+
+
+@pytest.mark.parametrize("args", TOKEN_CASES)
+def test_token_graph_bit_exact(dl, args):
+    g = build_graph(dl, args)
+    row_ptr, col = dl.diffuser_graph_copy_csr(g)
+    o_ptr, o_col = oracle_graph(args)
+    np.testing.assert_array_equal(row_ptr, o_ptr)
+    np.testing.assert_array_equal(col, o_col)
+
+
+@pytest.mark.parametrize("args", BLOCK_CASES)
+def test_block_graph_bit_exact(dl, args):
+    g = build_graph(dl, args, "block")
+    row_ptr, col = dl.diffuser_graph_copy_csr(g)
+    o_ptr, o_col = oracle_graph(args, "block")
+    np.testing.assert_array_equal(row_ptr, o_ptr)
+    np.testing.assert_array_equal(col, o_col)
+
+
+@pytest.mark.parametrize("w", workloads.ALL, ids=lambda w: w.name)
+def test_workload_graph_bit_exact(dl, w):
+    g = build_graph(dl, w.graph_args(), w.kind)
+    row_ptr, col = dl.diffuser_graph_copy_csr(g)
+    o_ptr, o_col = oracle_graph(w.graph_args(), w.kind)
+    assert g.nnz == o_ptr[-1]
+    np.testing.assert_array_equal(row_ptr, o_ptr)
+    np.testing.assert_array_equal(col, o_col)
+
+
+# ---------------------------------------------------------------- pins on the device
+def test_eight_position_one_hop_example_on_device(dl):
+    # "1.2.1 Static sparsity", eq 8-10: weights (1/4, 1/2, 1/4), o_4 = (1, 1.5)
+    import torch
+    n, d = 8, 64
+    Q = np.zeros((1, 1, n, d), np.float32); K = np.zeros_like(Q); V = np.zeros_like(Q)
+    K[0, 0, 3, 0] = 1.0
+    Q[0, 0, 3, 0] = 8.0 * math.log(2.0)
+    V[0, 0, 2, :2] = (2, 0); V[0, 0, 3, :2] = (0, 2); V[0, 0, 4, :2] = (2, 2)
+    g = dl.diffuser_build_graph(n, 1, 0, rand_per_row=0)
+    Qd, Kd, Vd = (to_device(x, "fp32") for x in (Q, K, V))
+    A = dl.diffuser_attention_weights(Qd, Kd, g)
+    out = dl.diffuser_forward(Qd, Kd, Vd, g, hops=1, alpha=0.0)
+    torch.cuda.synchronize()
+    row_ptr, _ = dl.diffuser_graph_copy_csr(g)
+    np.testing.assert_allclose(A[0, row_ptr[3]:row_ptr[4]].cpu().numpy(), [0.25, 0.5, 0.25],
+                               atol=1e-7)
+    np.testing.assert_allclose(out[0, 0, 3, :2].cpu().numpy(), [1.0, 1.5], atol=1e-6)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_three_token_example_on_device(dl, dtype):
+    # Diffuser notes sec 2.5: Z_(2),1 = 0.3475 V1 + 0.45 V2 + 0.2025 V3
+    import torch
+    g = dl.diffuser_build_graph(3, 1, 0, rand_per_row=0)
+    row_ptr, col = dl.diffuser_graph_copy_csr(g)
+    dense = np.array([[0.5, 0.5, 0], [0, 0.5, 0.5], [0, 0, 1]])
+    A = np.array([dense[i, j] for i in range(3) for j in col[row_ptr[i]:row_ptr[i + 1]]],
+                 np.float32)
+    V = np.zeros((1, 1, 3, 64), np.float32)
+    V[0, 0, 0, 0] = V[0, 0, 1, 1] = V[0, 0, 2, 2] = 1.0
+    Vd = to_device(synthetic.to_bf16_bits(V) if dtype == "bf16" else V, dtype)
+    out = dl.diffuser_diffuse_csr(g, torch.from_numpy(A).cuda(), Vd, hops=2, alpha=0.1)
+    torch.cuda.synchronize()
+    got = to_f64(out)[0, 0, 0, :3]
+    tol = 1e-6 if dtype == "fp32" else 2e-3
+    np.testing.assert_allclose(got, [0.3475, 0.45, 0.2025], atol=tol)
+
+
+# ---------------------------------------------------------------- forward parity, small
+SMALL = [
+    # (B, H, n, r, g, R, hops, alpha)
+    (1, 1, 1, 0, 0, 0, 5, 0.1),
+    (1, 2, 300, 8, 3, 5, 5, 0.1),
+    (2, 3, 257, 32, 4, 8, 5, 0.1),
+    (1, 2, 1000, 64, 8, 16, 3, 0.25),
+    (1, 1, 640, 640, 0, 0, 1, 0.0),      # full graph, one hop, alpha 0: dense attention
+    (2, 2, 513, 20, 2, 4, 2, 1.0),       # alpha 1 returns V
+    (1, 4, 700, 17, 5, 3, 0, 0.1),       # hops 0 returns V
+    (1, 1, 389, 128, 2, 32, 5, 0.1),     # ragged tail against 128-row tiles
+]
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "B%dH%dn%dr%dg%dR%dK%da%s" % c)
+def test_forward_small(dl, case, dtype):
+    import torch
+    B, H, n, r, gn, R, hops, alpha = case
+    g = dl.diffuser_build_graph(n, r, gn, rand_per_row=R, seed=0)
+    o_ptr, o_col = oracle.token_graph(n, r, gn, R, seed=0)
+    Q, K, V = synthetic.qkv(B, H, n, 64, dtype, seed=n)
+    out = dl.diffuser_forward(to_device(Q, dtype), to_device(K, dtype), to_device(V, dtype), g,
+                              hops, alpha)
+    torch.cuda.synchronize()
+    ref = oracle.forward(oracle.widen(Q, dtype), oracle.widen(K, dtype), oracle.widen(V, dtype),
+                         o_ptr, o_col, hops, alpha, nthreads=4)
+    check_output(to_f64(out), ref, dtype)
+    if hops == 0 or alpha == 1.0:
+        np.testing.assert_array_equal(to_f64(out), oracle.widen(V, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("args", BLOCK_CASES[:4], ids=lambda a: "n%d_b%d" % (a["n"], a["block"]))
+def test_forward_block_graph_small(dl, args, dtype):
+    import torch
+    g = build_graph(dl, args, "block")
+    o_ptr, o_col = oracle_graph(args, "block")
+    B, H, n = 2, 2, args["n"]
+    Q, K, V = synthetic.qkv(B, H, n, 64, dtype, seed=5)
+    out = dl.diffuser_forward(to_device(Q, dtype), to_device(K, dtype), to_device(V, dtype), g,
+                              5, 0.1)
+    torch.cuda.synchronize()
+    ref = oracle.forward(oracle.widen(Q, dtype), oracle.widen(K, dtype), oracle.widen(V, dtype),
+                         o_ptr, o_col, 5, 0.1, nthreads=4)
+    check_output(to_f64(out), ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_attention_weights_parity(dl, dtype):
+    import torch
+    B, H, n = 1, 3, 600
+    g = dl.diffuser_build_graph(n, 40, 4, rand_per_row=12, seed=0)
+    o_ptr, o_col = oracle.token_graph(n, 40, 4, 12, seed=0)
+    Q, K, _ = synthetic.qkv(B, H, n, 64, dtype, seed=2)
+    A = dl.diffuser_attention_weights(to_device(Q, dtype), to_device(K, dtype), g)
+    torch.cuda.synchronize()
+    A = A.cpu().numpy().astype(np.float64)
+    Qw, Kw = oracle.widen(Q, dtype), oracle.widen(K, dtype)
+    for u in range(B * H):
+        ref = oracle.attention_weights(Qw[0, u], Kw[0, u], o_ptr, o_col)
+        np.testing.assert_allclose(A[u], ref, rtol=2e-5, atol=1e-8)
+
+
+def test_constant_v_is_preserved(dl):
+    # A is row-stochastic, so a constant V is a fixed point of every hop
+    import torch
+    B, H, n = 2, 2, 1100
+    g = dl.diffuser_build_graph(n, 100, 6, rand_per_row=10)
+    Q, K, _ = synthetic.qkv(B, H, n, 64, "bf16", seed=3)
+    V = torch.full((B, H, n, 64), 0.75, dtype=torch.bfloat16, device="cuda")
+    out = dl.diffuser_forward(to_device(Q, "bf16"), to_device(K, "bf16"), V, g, 5, 0.1)
+    torch.cuda.synchronize()
+    assert float((out.float() - 0.75).abs().max()) <= 0.75 * 2 ** -8
+
+
+def test_bad_workspace_launches_nothing(dl):
+    import torch
+    g = dl.diffuser_build_graph(256, 8, 1, rand_per_row=2)
+    Q = torch.zeros((1, 1, 256, 64), dtype=torch.bfloat16, device="cuda")
+    need = dl.diffuser_workspace_size(g, 1, 1, 64, dl.DIFFUSER_DTYPE_BF16)
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    before, _ = dl.diffuser_launch_count()
+    with pytest.raises(dl.DiffuserError) as e:
+        dl.diffuser_forward(Q, Q.clone(), Q.clone(), g, 5, 0.1, workspace=small)
+    assert e.value.status == 7
+    with pytest.raises(dl.DiffuserError) as e:
+        dl.diffuser_forward(Q, Q.clone(), Q.clone(), g, 5, 1.5)
+    assert e.value.status == 1
+    after, _ = dl.diffuser_launch_count()
+    assert after == before
+
+
+def test_forward_host_buffers(dl):
+    # the end-to-end entry point: host buffers in, host buffer out
+    import torch
+    B, H, n = 1, 2, 513
+    g = dl.diffuser_build_graph(n, 16, 2, rand_per_row=4)
+    Q, K, V = synthetic.qkv(B, H, n, 64, "bf16", seed=8)
+    Qh, Kh, Vh = (torch.from_numpy(x).view(torch.bfloat16).pin_memory() for x in (Q, K, V))
+    out = torch.empty_like(Vh).pin_memory()
+    ws = dl.alloc_workspace(dl.diffuser_host_workspace_size(g, B, H, 64, dl.DIFFUSER_DTYPE_BF16))
+    dl.diffuser_forward_host(Qh, Kh, Vh, g, 5, 0.1, out, ws)
+    torch.cuda.synchronize()
+    ref_dev = dl.diffuser_forward(Qh.cuda(), Kh.cuda(), Vh.cuda(), g, 5, 0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_dev.cpu())
+
+
+# ---------------------------------------------------------------- full-size workloads
+def _sample_units(units: int):
+    return sorted({0, units // 2, units - 1})
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", workloads.ALL, ids=lambda w: w.name)
+def test_workload_full_size(dl, w):
+    """Full-size forward (the benchmark's launch configuration); sampled units
+    against the oracle, plus alpha=1 and constant-V properties on every unit."""
+    import torch
+    g = build_graph(dl, w.graph_args(), w.kind)
+    o_ptr, o_col = oracle_graph(w.graph_args(), w.kind)
+    Q, K, V = synthetic.qkv(w.B, w.H, w.n, w.d, w.dtype, seed=w.seed)
+    Qd, Kd, Vd = (to_device(x, w.dtype) for x in (Q, K, V))
+    ws = dl.alloc_workspace(dl.diffuser_workspace_size(g, w.B, w.H, w.d,
+                                                       1 if w.dtype == "bf16" else 0))
+    out = dl.diffuser_forward(Qd, Kd, Vd, g, w.hops, w.alpha, workspace=ws)
+    torch.cuda.synchronize()
+    got = to_f64(out).reshape(w.units, w.n, w.d)
+    Qw = oracle.widen(Q, w.dtype).reshape(w.units, w.n, w.d)
+    Kw = oracle.widen(K, w.dtype).reshape(w.units, w.n, w.d)
+    Vw = oracle.widen(V, w.dtype).reshape(w.units, w.n, w.d)
+    units = _sample_units(w.units)
+    ref = oracle.forward(Qw[units], Kw[units], Vw[units], o_ptr, o_col, w.hops, w.alpha,
+                         nthreads=len(units))
+    check_output(got[units], ref, w.dtype)
+    # properties on every unit: alpha = 1 gives V exactly; constant V is preserved
+    out1 = dl.diffuser_forward(Qd, Kd, Vd, g, w.hops, 1.0, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, Vd)
+    Vc = torch.full_like(Vd, 0.5)
+    outc = dl.diffuser_forward(Qd, Kd, Vc, g, w.hops, w.alpha, workspace=ws)
+    torch.cuda.synchronize()
+    assert float((outc.float() - 0.5).abs().max()) <= 0.5 * 2 ** -8
