@@ -140,9 +140,10 @@ DIFFUSER_API void diffuser_graph_free(diffuser_graph* g);
 /* ---------------------------------------------------------------- forward */
 
 /*
- * Bytes of device workspace diffuser_forward needs for this graph and shape.
- * The workspace holds the stored weights A (fp32, "score once, aggregate K
- * times", [D] sec 2.4 / 2.6) and the fp32 hop state Z_k.
+ * Bytes of device workspace diffuser_forward needs for this graph and shape,
+ * whichever kernel path is selected.  The workspace holds the stored weights
+ * A (fp32, "score once, aggregate K times", [D] sec 2.4 / 2.6) and the fp32
+ * hop state Z_k.
  *   B, H >= 1; d == 64; dtype a diffuser_dtype.
  */
 DIFFUSER_API int diffuser_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32_t d,
@@ -212,6 +213,32 @@ DIFFUSER_API int diffuser_attention_weights(const void* Q, const void* K, int32_
 DIFFUSER_API int diffuser_diffuse_csr(const diffuser_graph* g, const float* A, const void* V, int32_t dtype,
                          int64_t B, int64_t H, int32_t d, int32_t hops, float alpha, void* out,
                          void* workspace, size_t workspace_bytes, diffuser_stream stream);
+
+/* ---------------------------------------------------------------- path and status */
+
+typedef enum {
+    DIFFUSER_PATH_AUTO = 0,       /* band tensor-core path where eligible, else CSR */
+    DIFFUSER_PATH_CSR = 1         /* always the general CSR SIMT path */
+} diffuser_path;
+
+/*
+ * Select the kernel path for later calls in this process (thread-safe; the
+ * default is DIFFUSER_PATH_AUTO).  The band path serves token graphs with
+ * bf16 I/O, window radius >= 8 and at most 32 globals; it stores the weights
+ * in a decomposed window/global/extra layout and runs the window part of
+ * every hop on tcgen05 tensor cores (3xTF32 split, fp32 accumulation).
+ * The workspace size depends on the path: query diffuser_workspace_size
+ * after changing it.  Errors: INVALID_ARG for an unknown path.
+ */
+DIFFUSER_API int diffuser_set_path(int path);
+DIFFUSER_API int diffuser_get_path(void);
+
+/*
+ * Read (synchronously) the device status word that the graph's kernels set
+ * when a bounded internal wait gives up (0 = no error); reset != 0 clears it.
+ * A nonzero word means results computed since the last reset are invalid.
+ */
+DIFFUSER_API int diffuser_graph_status(const diffuser_graph* g, int* status, int reset);
 
 /* ---------------------------------------------------------------- measurement */
 

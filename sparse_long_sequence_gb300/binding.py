@@ -21,6 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libdiffuser.so")
 DIFFUSER_OK = 0
 DIFFUSER_DTYPE_FP32 = 0
 DIFFUSER_DTYPE_BF16 = 1
+DIFFUSER_PATH_AUTO = 0
+DIFFUSER_PATH_CSR = 1
 KERNEL_KINDS = ("build", "score", "hop", "aux")
 
 
@@ -58,6 +60,9 @@ def _load() -> ctypes.CDLL:
                                                  c.c_size_t, vp]),
         "diffuser_diffuse_csr": (c.c_int, [vp, vp, vp, i32, i64, i64, i32, i32, f32, vp, vp,
                                            c.c_size_t, vp]),
+        "diffuser_set_path": (c.c_int, [c.c_int]),
+        "diffuser_get_path": (c.c_int, []),
+        "diffuser_graph_status": (c.c_int, [vp, c.POINTER(c.c_int), c.c_int]),
         "diffuser_launch_count": (c.c_int64, [i64p]),
         "diffuser_profile_begin": (c.c_int, []),
         "diffuser_profile_end": (c.c_int, [c.POINTER(c.c_double), i64p]),
@@ -250,6 +255,21 @@ def diffuser_diffuse_csr(g: Graph, A, V, hops: int, alpha: float, out=None, work
                                      alpha, out.data_ptr(), workspace.data_ptr(),
                                      workspace.numel(), _stream(stream)), "diffuser_diffuse_csr")
     return out
+
+
+def diffuser_set_path(path: int) -> None:
+    _check(_lib.diffuser_set_path(path), "diffuser_set_path")
+
+
+def diffuser_get_path() -> int:
+    return int(_lib.diffuser_get_path())
+
+
+def diffuser_graph_status(g: Graph, reset: bool = False) -> int:
+    st = ctypes.c_int()
+    _check(_lib.diffuser_graph_status(g.handle, ctypes.byref(st), int(reset)),
+           "diffuser_graph_status")
+    return st.value
 
 
 def diffuser_launch_count() -> tuple[int, dict]:

@@ -19,6 +19,7 @@ namespace {
 thread_local std::string g_last_error;
 
 std::atomic<int64_t> g_launches[DIFFUSER_KERNEL_KINDS];
+std::atomic<int> g_path{DIFFUSER_PATH_AUTO};
 
 // ---- profiler: events recorded around launches while a profile is open ----
 struct ProfileRecord {
@@ -128,13 +129,42 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-int check_workspace(const Layout& L, void* ws, size_t ws_bytes) {
+int check_workspace_bytes(size_t need, void* ws, size_t ws_bytes) {
     if (!ws) return fail(DIFFUSER_ERR_WORKSPACE, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(ws) % kAlign)
         return fail(DIFFUSER_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-    if (ws_bytes < L.total)
+    if (ws_bytes < need)
         return fail(DIFFUSER_ERR_WORKSPACE, "workspace too small: need " +
-                                                std::to_string(L.total) + " bytes");
+                                                std::to_string(need) + " bytes");
+    return DIFFUSER_OK;
+}
+
+int check_workspace(const Layout& L, void* ws, size_t ws_bytes) {
+    return check_workspace_bytes(L.total, ws, ws_bytes);
+}
+
+// The band path (tensor-core window tiles) serves token graphs with bf16 I/O;
+// everything else runs the CSR SIMT path.
+bool use_band(const diffuser_graph* g, int32_t dtype, BandPlan* p) {
+    if (g_path.load() == DIFFUSER_PATH_CSR) return false;
+    if (dtype != DIFFUSER_DTYPE_BF16) return false;
+    return band_plan(g, p);
+}
+
+// Workspace bytes: enough for the CSR layout and, where the graph and dtype
+// are eligible, the band layout, so that the size does not depend on the
+// selected path.
+int workspace_need(const diffuser_graph* g, int64_t B, int64_t H, int32_t dtype, size_t* need) {
+    Layout L;
+    int st = plan_layout(g, B, H, &L);
+    if (st) return st;
+    *need = L.total;
+    BandPlan bp;
+    if (dtype == DIFFUSER_DTYPE_BF16 && band_plan(g, &bp)) {
+        BandLayout BL;
+        if ((st = plan_band_layout(g, bp, B * H, &BL))) return st;
+        if (BL.total > *need) *need = BL.total;
+    }
     return DIFFUSER_OK;
 }
 
@@ -176,14 +206,23 @@ int forward_device(const void* Q, const void* K, const void* V, int32_t dtype, i
         return fail(DIFFUSER_ERR_INVALID_ARG, "out overlaps Q or K");
     if (hops > 0 && overlaps(out, bytes, V, bytes))
         return fail(DIFFUSER_ERR_INVALID_ARG, "out may alias V only when hops == 0");
-    Layout L;
-    if ((st = plan_layout(g, B, H, &L))) return st;
-    if ((st = check_workspace(L, workspace, workspace_bytes))) return st;
+    size_t need = 0;
+    if ((st = workspace_need(g, B, H, dtype, &need))) return st;
+    if ((st = check_workspace_bytes(need, workspace, workspace_bytes))) return st;
     if ((st = check_device(g))) return st;
 
     char* ws = static_cast<char*>(workspace);
     CsrArgs a{g->d_row_ptr, g->d_col, g->n, g->nnz, B * H};
+    Layout L;
+    if ((st = plan_layout(g, B, H, &L))) return st;
     if (hops == 0) return run_hops_csr(g, a, nullptr, V, dtype, 0, alpha, out, ws, L, stream);
+    BandPlan bp;
+    if (use_band(g, dtype, &bp)) {
+        BandLayout BL;
+        if ((st = plan_band_layout(g, bp, B * H, &BL))) return st;
+        if ((st = launch_band_scores(g, bp, B * H, Q, K, ws, BL, stream))) return st;
+        return launch_band_hops(g, bp, B * H, V, hops, alpha, out, ws, BL, stream);
+    }
     float* A = reinterpret_cast<float*>(ws + L.a_off);
     if ((st = launch_score_csr(a, Q, K, dtype, A, stream))) return st;
     return run_hops_csr(g, a, A, V, dtype, hops, alpha, out, ws, L, stream);
@@ -195,10 +234,13 @@ int new_graph(diffuser_graph** out, diffuser_graph** g) {
     *g = new (std::nothrow) diffuser_graph();
     if (!*g) return fail(DIFFUSER_ERR_ALLOC, "host allocation failed");
     cudaError_t err = cudaGetDevice(&(*g)->device);
+    if (err == cudaSuccess) err = cudaMalloc(&(*g)->d_status, sizeof(int));
+    if (err == cudaSuccess) err = cudaMemset((*g)->d_status, 0, sizeof(int));
     if (err != cudaSuccess) {
+        cudaFree((*g)->d_status);
         delete *g;
         *g = nullptr;
-        return cuda_fail(err, "cudaGetDevice");
+        return cuda_fail(err, "graph set-up");
     }
     return DIFFUSER_OK;
 }
@@ -328,6 +370,10 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_col);
     cudaFree(g->d_globals);
     cudaFree(g->d_is_global);
+    cudaFree(g->d_gslot);
+    cudaFree(g->d_x_ptr);
+    cudaFree(g->d_x_col);
+    cudaFree(g->d_status);
     delete g;
 }
 
@@ -336,10 +382,7 @@ int diffuser_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32
     int st = check_shape(g, B, H, d, dtype);
     if (st) return st;
     if (!bytes) return fail(DIFFUSER_ERR_INVALID_ARG, "bytes is NULL");
-    Layout L;
-    if ((st = plan_layout(g, B, H, &L))) return st;
-    *bytes = L.total;
-    return DIFFUSER_OK;
+    return workspace_need(g, B, H, dtype, bytes);
 }
 
 int diffuser_forward(const void* Q, const void* K, const void* V, int32_t dtype, int64_t B,
@@ -407,10 +450,18 @@ int diffuser_attention_weights(const void* Q, const void* K, int32_t dtype, int6
         if (!Q || !K || !A_out) return fail(DIFFUSER_ERR_INVALID_ARG, "a pointer is NULL");
         if (!aligned16(Q) || !aligned16(K) || !aligned16(A_out))
             return fail(DIFFUSER_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-        Layout L;
-        if ((st = plan_layout(g, B, H, &L))) return st;
-        if ((st = check_workspace(L, workspace, workspace_bytes))) return st;
+        size_t need = 0;
+        if ((st = workspace_need(g, B, H, dtype, &need))) return st;
+        if ((st = check_workspace_bytes(need, workspace, workspace_bytes))) return st;
         if ((st = check_device(g))) return st;
+        BandPlan bp;
+        if (use_band(g, dtype, &bp)) {
+            BandLayout BL;
+            char* ws = static_cast<char*>(workspace);
+            if ((st = plan_band_layout(g, bp, B * H, &BL))) return st;
+            if ((st = launch_band_scores(g, bp, B * H, Q, K, ws, BL, stream))) return st;
+            return launch_band_to_csr(g, bp, B * H, ws, BL, A_out, stream);
+        }
         CsrArgs a{g->d_row_ptr, g->d_col, g->n, g->nnz, B * H};
         return launch_score_csr(a, Q, K, dtype, A_out, stream);
     } catch (...) {
@@ -443,6 +494,27 @@ int diffuser_diffuse_csr(const diffuser_graph* g, const float* A, const void* V,
     } catch (...) {
         return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
     }
+}
+
+int diffuser_set_path(int path) {
+    if (path != DIFFUSER_PATH_AUTO && path != DIFFUSER_PATH_CSR)
+        return fail(DIFFUSER_ERR_INVALID_ARG, "unknown path");
+    g_path.store(path);
+    return DIFFUSER_OK;
+}
+
+int diffuser_get_path(void) { return g_path.load(); }
+
+int diffuser_graph_status(const diffuser_graph* g, int* status, int reset) {
+    if (!g || !status) return fail(DIFFUSER_ERR_INVALID_ARG, "NULL argument");
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+    if (dev != g->device) return fail(DIFFUSER_ERR_INVALID_ARG, "not the graph's device");
+    err = cudaMemcpy(status, g->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (err == cudaSuccess && reset) err = cudaMemset(g->d_status, 0, sizeof(int));
+    if (err != cudaSuccess) return cuda_fail(err, "reading the device status word");
+    return DIFFUSER_OK;
 }
 
 int64_t diffuser_launch_count(int64_t* per_kind) {

@@ -1,0 +1,782 @@
+// Band path for token graphs with bf16 I/O: the weights are stored in a
+// decomposed layout that turns the local window into dense tensor-core tiles,
+// and each diffusion hop runs the window part on tcgen05 tensor cores.
+//
+// Layout of the weights A of one (batch, head) unit ("Diffuser: modelling long
+// sequences with multi-hop attention diffusion", sec 2.2 / 2.4: score once,
+// aggregate K times):
+//   band   [rows4][W]  row i, column w <-> key j = 4*floor(i/4) - r_up + w;
+//                      A_ij where |i-j| <= r, 0 <= j < n and i not global, else 0
+//   gcol   [n][g_pad]  slot s <-> key G[s], for the globals outside row i's window
+//   extra  [nx]        the random edges outside window and G, in CSR order
+//   grow   [g][n]      the full rows of the global tokens
+// Row i's stored window starts on a multiple of 4 keys, so a 4-D TMA tensor
+// map whose third stride is 16*(W-1) bytes reads 128 consecutive rows of one
+// tile de-skewed: one box = 128 rows x 32 absolute keys.
+//
+// Hop Z_{k+1} = (1-alpha) A Z_k + alpha V ("Diffuser...", sec 2.4 eq S.7):
+//   band:    tcgen05 MMA, M = 128 rows, N = 64 features, K = 32 keys per chunk,
+//            3xTF32 split (hi = operand as stored, which the tensor core
+//            truncates to tf32; lo = operand - trunc(operand)):
+//            A_hi*Z_hi + A_hi*Z_lo + A_lo*Z_hi, fp32 accumulation in TMEM.
+//   gcol, extras: warp-cooperative gathers of 256-byte Z_k rows, fp32 FMA.
+//   global rows:  every tile adds its keys' share; the last tile of a unit
+//            sums the shares (fixed order) and writes the global rows.
+// Z_k lives in three fp32 planes: row-major (for gathers) and transposed
+// raw/lo planes (the K-major B operand of the MMA).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace dfs {
+namespace {
+
+constexpr int kTileRows = 128;
+constexpr int kChunkKeys = 32;
+constexpr int kThreads = 320;            // 10 warps
+constexpr int kAStages = 2;              // smem stages of A (16 KB each)
+constexpr int kZStages = 2;              // smem stages of Z^T hi+lo (16 KB each)
+constexpr int kTStages = 3;              // TMEM stages of A hi+lo (64 columns each)
+constexpr int kTmemCols = 256;
+constexpr int kPStride = 68;             // floats per row of the gather partial buffer
+constexpr int kAStageBytes = kTileRows * kChunkKeys * 4;
+constexpr int kZPlaneBytes = kHeadDim * kChunkKeys * 4;
+constexpr int kSmemBytes = 1024 + kAStages * kAStageBytes + kZStages * 2 * kZPlaneBytes +
+                           kTileRows * kPStride * 4 + 256;
+
+__device__ __forceinline__ float tf32_trunc(float x) {
+    return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+struct HopArgs {
+    BandPlan plan;
+    int64_t units;
+    float alpha;
+    const uint8_t* is_global;
+    const int32_t* globals;
+    const int64_t* x_ptr;
+    const int32_t* x_col;
+    int64_t nx;
+    const float* A_gc;
+    const float* A_x;
+    const float* A_gr;
+    const void* Zr_in;    // hop 0: V (bf16); otherwise fp32 row-major Z_k
+    const __nv_bfloat16* V;
+    float* Zr_out;
+    float* Zt_out;
+    float* Ztl_out;
+    __nv_bfloat16* out;   // last hop
+    float* gpart;         // [units][tiles][g][64]
+    int* counters;        // [units]
+    int* status;
+};
+
+// Two features (2*lane, 2*lane+1) of row j of Z_k.
+template <bool kHop0>
+__device__ __forceinline__ float2 zpair(const HopArgs& a, int64_t u, int64_t j, int lane) {
+    const size_t off = ((size_t)u * a.plan.n + j) * kHeadDim + 2 * lane;
+    if constexpr (kHop0) {
+        uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(
+            static_cast<const __nv_bfloat16*>(a.Zr_in) + off));
+        return make_float2(bf16lo(w), bf16hi(w));
+    } else {
+        return __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(a.Zr_in) + off));
+    }
+}
+
+template <bool kHop0, bool kLast>
+__global__ void __launch_bounds__(kThreads, 2)
+hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmZt,
+                const __grid_constant__ CUtensorMap tmZl, HopArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sA = smem;                                          // kAStages x 16 KB
+    uint8_t* sZ = sA + kAStages * kAStageBytes;                  // kZStages x (hi 8 KB, lo 8 KB)
+    float* sP = reinterpret_cast<float*>(sZ + kZStages * 2 * kZPlaneBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTileRows * kPStride);
+    uint64_t* full_sA = bars;
+    uint64_t* empty_sA = full_sA + kAStages;
+    uint64_t* full_tA = empty_sA + kAStages;
+    uint64_t* empty_tA = full_tA + kTStages;
+    uint64_t* full_Z = empty_tA + kTStages;
+    uint64_t* empty_Z = full_Z + kZStages;
+    uint64_t* acc_full = empty_Z + kZStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    int* ticket = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const BandPlan& P = a.plan;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t u = blockIdx.x / P.tiles;
+    const int tile = (int)(blockIdx.x - u * P.tiles);
+    const int64_t i0 = (int64_t)tile * kTileRows;
+    const int64_t jb = i0 - P.r_up;          // absolute key of chunk 0, column 0
+    const int chunks = P.chunks;
+
+    if (warp == 9) ptx::tmem_alloc(tmem_slot, kTmemCols);
+    if (tid == 0) {
+        for (int s = 0; s < kAStages; ++s) { ptx::mbar_init(&full_sA[s], 1); ptx::mbar_init(&empty_sA[s], 128); }
+        for (int s = 0; s < kTStages; ++s) { ptx::mbar_init(&full_tA[s], 128); ptx::mbar_init(&empty_tA[s], 1); }
+        for (int s = 0; s < kZStages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
+        ptx::mbar_init(acc_full, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 8 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmZt);
+        if (!kHop0) ptx::prefetch_tensormap(&tmZl);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 8) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            for (int c = 0; c < chunks; ++c) {
+                const int sa = c % kAStages;
+                if (c >= kAStages) ptx::mbar_wait(&empty_sA[sa], ((c / kAStages) - 1) & 1, a.status);
+                ptx::mbar_arrive_expect_tx(&full_sA[sa], kAStageBytes);
+                ptx::tma_load_4d(sA + sa * kAStageBytes, &tmA, &full_sA[sa],
+                                 (int)(i0 + kChunkKeys * c), 0, (int)(i0 / 4), (int)u);
+                const int sz = c % kZStages;
+                if (c >= kZStages) ptx::mbar_wait(&empty_Z[sz], ((c / kZStages) - 1) & 1, a.status);
+                uint8_t* zdst = sZ + sz * 2 * kZPlaneBytes;
+                ptx::mbar_arrive_expect_tx(&full_Z[sz], kHop0 ? kZPlaneBytes : 2 * kZPlaneBytes);
+                const int key = (int)(jb + kChunkKeys * c);
+                ptx::tma_load_3d(zdst, &tmZt, &full_Z[sz], key, 0, (int)u);
+                if (!kHop0) ptx::tma_load_3d(zdst + kZPlaneBytes, &tmZl, &full_Z[sz], key, 0, (int)u);
+            }
+        }
+    } else if (warp == 9) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::mma_idesc(2, kHeadDim);
+            for (int c = 0; c < chunks; ++c) {
+                const int ta = c % kTStages, sz = c % kZStages;
+                ptx::mbar_wait(&full_tA[ta], (c / kTStages) & 1, a.status);
+                ptx::mbar_wait(&full_Z[sz], (c / kZStages) & 1, a.status);
+                ptx::tc_fence_after();
+                const uint32_t zhi = ptx::smem_u32(sZ + sz * 2 * kZPlaneBytes);
+                const uint32_t zlo = zhi + kZPlaneBytes;
+#pragma unroll
+                for (int k = 0; k < kChunkKeys / 8; ++k) {
+                    const uint32_t a_hi = tmem + 64 + 64 * ta + 8 * k;
+                    const uint32_t a_lo = a_hi + 32;
+                    const uint64_t bhi = ptx::sw128_kmajor_desc(zhi + 32 * k);
+                    ptx::mma_tf32_ts(tmem, a_hi, bhi, idesc, (c | k) != 0);
+                    if (!kHop0) ptx::mma_tf32_ts(tmem, a_hi, ptx::sw128_kmajor_desc(zlo + 32 * k), idesc, 1);
+                    ptx::mma_tf32_ts(tmem, a_lo, bhi, idesc, 1);
+                }
+                ptx::mma_commit(&empty_tA[ta]);
+                ptx::mma_commit(&empty_Z[sz]);
+            }
+            ptx::mma_commit(acc_full);
+        }
+    } else if (warp < 4) {
+        // ---------------- A splitter: smem (raw, de-skewed) -> masked hi / lo -> TMEM
+        const int t = tid;                       // row within the tile
+        const int64_t i = i0 + t;
+        const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
+        const int64_t lo_key = i - P.r < 0 ? 0 : i - P.r;
+        const int64_t hi_key = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        for (int c = 0; c < chunks; ++c) {
+            const int sa = c % kAStages, ta = c % kTStages;
+            ptx::mbar_wait(&full_sA[sa], (c / kAStages) & 1, a.status);
+            float v[32];
+            const uint8_t* rowp = sA + sa * kAStageBytes + t * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = *reinterpret_cast<const float4*>(rowp + ((q ^ (t & 7)) << 4));
+                v[4 * q + 0] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+            }
+            ptx::mbar_arrive(&empty_sA[sa]);
+            if (c >= kTStages) ptx::mbar_wait(&empty_tA[ta], ((c / kTStages) - 1) & 1, a.status);
+            ptx::tc_fence_after();
+            const int64_t j0 = jb + kChunkKeys * c;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int64_t j = j0 + k;
+                const bool ok = row_ok && j >= lo_key && j <= hi_key;
+                v[k] = ok ? v[k] : 0.f;
+            }
+            const uint32_t col = tmem + lane_base + 64 + 64 * ta;
+            ptx::tmem_st32(col, v);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = v[k] - tf32_trunc(v[k]);
+            ptx::tmem_st32(col + 32, v);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&full_tA[ta]);
+        }
+    } else {
+        // ---------------- gathers (global rows share, gcol, extras) + epilogue
+        const int q = warp - 4;                  // TMEM lane quadrant and row block
+        const int sim_tid = tid - 128;           // 0..127
+        const int g = P.g;
+        // (1) global rows: this tile's keys contribute sum_j A_gr[s][j] Z_k[j]
+        if (g > 0) {
+            for (int s0 = 0; s0 < g; s0 += 8) {
+                float2 acc[8];
+#pragma unroll
+                for (int s = 0; s < 8; ++s) acc[s] = make_float2(0.f, 0.f);
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int64_t j = i0 + 32 * q + jj;
+                    if (j >= P.n) break;
+                    const float2 z = zpair<kHop0>(a, u, j, lane);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        if (s0 + s < g) {
+                            const float w = __ldg(a.A_gr + ((size_t)u * g + s0 + s) * P.n + j);
+                            acc[s].x = fmaf(w, z.x, acc[s].x);
+                            acc[s].y = fmaf(w, z.y, acc[s].y);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    if (s0 + s < g) {
+                        float* dst = sP + (q * 32 + s0 + s) * kHeadDim + 2 * lane;
+                        dst[0] = acc[s].x;
+                        dst[1] = acc[s].y;
+                    }
+                }
+            }
+            ptx::named_barrier_sync(1, 128);
+            float* part = a.gpart + (((size_t)u * P.tiles + tile) * g) * kHeadDim;
+            for (int e = sim_tid; e < g * kHeadDim; e += 128) {
+                const int s = e / kHeadDim, dd = e % kHeadDim;
+                float sum = 0.f;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) sum += sP[(qq * 32 + s) * kHeadDim + dd];
+                part[e] = sum;
+            }
+            __threadfence();
+            ptx::named_barrier_sync(1, 128);
+            if (sim_tid == 0) *ticket = atomicAdd(&a.counters[u], 1);
+            ptx::named_barrier_sync(1, 128);
+            if (*ticket == P.tiles - 1) {
+                // last tile of this unit: sum the shares in tile order, write the global rows
+                __threadfence();
+                const float keep = 1.f - a.alpha;
+                for (int e = sim_tid; e < g * kHeadDim; e += 128) {
+                    const int s = e / kHeadDim, dd = e % kHeadDim;
+                    float sum = 0.f;
+                    for (int tt = 0; tt < P.tiles; ++tt)
+                        sum += __ldcg(a.gpart + (((size_t)u * P.tiles + tt) * g + s) * kHeadDim + dd);
+                    const int64_t gi = a.globals[s];
+                    const size_t row = ((size_t)u * P.n + gi) * kHeadDim + dd;
+                    const float z = fmaf(keep, sum, a.alpha * __bfloat162float(a.V[row]));
+                    if (kLast) {
+                        a.out[row] = __float2bfloat16_rn(z);
+                    } else {
+                        a.Zr_out[row] = z;
+                        const size_t tr = ((size_t)u * kHeadDim + dd) * P.nz + gi;
+                        a.Zt_out[tr] = z;
+                        a.Ztl_out[tr] = z - tf32_trunc(z);
+                    }
+                }
+                if (sim_tid == 0) a.counters[u] = 0;
+            }
+            ptx::named_barrier_sync(1, 128);
+        }
+        // (2) globals outside the window and random extras, one row at a time
+        for (int rr = 0; rr < 32; ++rr) {
+            const int t = q * 32 + rr;
+            const int64_t i = i0 + t;
+            float2 acc = make_float2(0.f, 0.f);
+            if (i < P.n && !a.is_global[i]) {
+                const float* wg = a.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+                for (int s = 0; s < g; ++s) {
+                    const float w = __ldg(wg + s);
+                    if (w != 0.f) {
+                        const float2 z = zpair<kHop0>(a, u, a.globals[s], lane);
+                        acc.x = fmaf(w, z.x, acc.x);
+                        acc.y = fmaf(w, z.y, acc.y);
+                    }
+                }
+                const int64_t e0 = a.x_ptr[i], e1 = a.x_ptr[i + 1];
+                const float* ax = a.A_x + (size_t)u * a.nx;
+                for (int64_t base = e0; base < e1; base += 32) {
+                    const int64_t e = base + lane;
+                    const float w_l = e < e1 ? __ldg(ax + e) : 0.f;
+                    const int32_t j_l = e < e1 ? __ldg(a.x_col + e) : 0;
+                    const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
+                    for (int tt = 0; tt < cnt; ++tt) {
+                        const float w = __shfl_sync(0xffffffffu, w_l, tt);
+                        const int32_t j = __shfl_sync(0xffffffffu, j_l, tt);
+                        const float2 z = zpair<kHop0>(a, u, j, lane);
+                        acc.x = fmaf(w, z.x, acc.x);
+                        acc.y = fmaf(w, z.y, acc.y);
+                    }
+                }
+            }
+            sP[t * kPStride + 2 * lane] = acc.x;
+            sP[t * kPStride + 2 * lane + 1] = acc.y;
+        }
+        __syncwarp();
+        // (3) epilogue: accumulator + gathers, restart term, outputs
+        ptx::mbar_wait(acc_full, 0, a.status);
+        ptx::tc_fence_after();
+        const int t = q * 32 + lane;
+        const int64_t i = i0 + t;
+        const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
+        const float keep = 1.f - a.alpha;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            float d[32];
+            ptx::tmem_ld32(tmem + lane_base + 32 * half, d);
+            if (!row_ok) continue;
+            const size_t row = ((size_t)u * P.n + i) * kHeadDim + 32 * half;
+            const uint4* vp = reinterpret_cast<const uint4*>(a.V + row);
+            float z[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint4 vv = __ldg(vp + c);
+                const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int k = 8 * c + 2 * e;
+                    const float p0 = sP[t * kPStride + 32 * half + k];
+                    const float p1 = sP[t * kPStride + 32 * half + k + 1];
+                    z[k] = fmaf(keep, d[k] + p0, a.alpha * bf16lo(w4[e]));
+                    z[k + 1] = fmaf(keep, d[k + 1] + p1, a.alpha * bf16hi(w4[e]));
+                }
+            }
+            if (kLast) {
+                uint4* op = reinterpret_cast<uint4*>(a.out + row);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        __nv_bfloat162 h = __floats2bfloat162_rn(z[8 * c + 2 * e], z[8 * c + 2 * e + 1]);
+                        w4[e] = *reinterpret_cast<uint32_t*>(&h);
+                    }
+                    op[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            } else {
+                float4* zr = reinterpret_cast<float4*>(a.Zr_out + row);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) zr[c] = make_float4(z[4 * c], z[4 * c + 1], z[4 * c + 2], z[4 * c + 3]);
+                const size_t tbase = ((size_t)u * kHeadDim + 32 * half) * P.nz + i;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    a.Zt_out[tbase + (size_t)k * P.nz] = z[k];
+                    a.Ztl_out[tbase + (size_t)k * P.nz] = z[k] - tf32_trunc(z[k]);
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- scores (SIMT)
+// One warp per (unit, row): scores of the row's allowed keys, masked softmax,
+// weights written into the decomposed layout.  ("Diffuser...", eq S.1-S.5.)
+struct ScoreArgs {
+    BandPlan plan;
+    int64_t units;
+    const uint8_t* is_global;
+    const int32_t* gslot;
+    const int32_t* globals;
+    const int64_t* x_ptr;
+    const int32_t* x_col;
+    int64_t nx;
+    float* A_band;
+    float* A_gc;
+    float* A_x;
+    float* A_gr;
+};
+
+__device__ __forceinline__ void load_q64(const __nv_bfloat16* p, float (&x)[64]) {
+    const uint4* v = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 w = __ldg(v + c);
+        x[8 * c + 0] = bf16lo(w.x); x[8 * c + 1] = bf16hi(w.x);
+        x[8 * c + 2] = bf16lo(w.y); x[8 * c + 3] = bf16hi(w.y);
+        x[8 * c + 4] = bf16lo(w.z); x[8 * c + 5] = bf16hi(w.z);
+        x[8 * c + 6] = bf16lo(w.w); x[8 * c + 7] = bf16hi(w.w);
+    }
+}
+
+__device__ __forceinline__ float dot64(const float (&q)[64], const __nv_bfloat16* kp) {
+    const uint4* v = reinterpret_cast<const uint4*>(kp);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 w = __ldg(v + c);
+        acc = fmaf(q[8 * c + 0], bf16lo(w.x), acc); acc = fmaf(q[8 * c + 1], bf16hi(w.x), acc);
+        acc = fmaf(q[8 * c + 2], bf16lo(w.y), acc); acc = fmaf(q[8 * c + 3], bf16hi(w.y), acc);
+        acc = fmaf(q[8 * c + 4], bf16lo(w.z), acc); acc = fmaf(q[8 * c + 5], bf16hi(w.z), acc);
+        acc = fmaf(q[8 * c + 6], bf16lo(w.w), acc); acc = fmaf(q[8 * c + 7], bf16hi(w.w), acc);
+    }
+    return acc;
+}
+
+__device__ __forceinline__ void online(float s, float& m, float& l) {
+    if (s > m) { l = l * expf(m - s) + 1.f; m = s; }
+    else       { l += expf(s - m); }
+}
+
+__device__ __forceinline__ void warp_merge(float& m, float& l) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+        const float mm = fmaxf(m, m2);
+        const float a1 = (m == -INFINITY) ? 0.f : l * expf(m - mm);
+        const float a2 = (m2 == -INFINITY) ? 0.f : l2 * expf(m2 - mm);
+        m = mm;
+        l = a1 + a2;
+    }
+}
+
+__global__ void __launch_bounds__(256)
+score_band_simt_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
+                       const __nv_bfloat16* __restrict__ K) {
+    const BandPlan& P = a.plan;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= a.units * P.n) return;
+    const int64_t u = gw / P.n, i = gw - u * P.n;
+    const __nv_bfloat16* Ku = K + (size_t)u * P.n * kHeadDim;
+    float q[64];
+    load_q64(Q + ((size_t)u * P.n + i) * kHeadDim, q);
+    const float scale = 0.125f;
+    float* Ab = a.A_band + (size_t)u * (P.band_unit / 4) + (size_t)i * P.W;
+    float* Agc = a.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+    float m = -INFINITY, l = 0.f;
+    if (a.is_global[i]) {
+        float* Ag = a.A_gr + ((size_t)u * P.g + a.gslot[i]) * P.n;
+        for (int64_t j = lane; j < P.n; j += 32) {
+            const float s = dot64(q, Ku + (size_t)j * kHeadDim) * scale;
+            Ag[j] = s;
+            online(s, m, l);
+        }
+        warp_merge(m, l);
+        for (int64_t j = lane; j < P.n; j += 32) Ag[j] = expf(Ag[j] - m) / l;
+        for (int w = lane; w < P.W; w += 32) Ab[w] = 0.f;
+        for (int s = lane; s < P.g_pad; s += 32) Agc[s] = 0.f;
+        return;
+    }
+    const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
+    const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+    const int64_t ws = 4 * (i / 4) - P.r_up;
+    float* Ax = a.A_x + (size_t)u * a.nx;
+    const int64_t e0 = a.x_ptr[i], e1 = a.x_ptr[i + 1];
+    for (int w = lane; w < P.W; w += 32) {
+        const int64_t j = ws + w;
+        if (j >= lo && j <= hi) {
+            const float s = dot64(q, Ku + (size_t)j * kHeadDim) * scale;
+            Ab[w] = s;
+            online(s, m, l);
+        }
+    }
+    for (int s = lane; s < P.g; s += 32) {
+        const int64_t j = a.globals[s];
+        if (j < lo || j > hi) {
+            const float sc = dot64(q, Ku + (size_t)j * kHeadDim) * scale;
+            Agc[s] = sc;
+            online(sc, m, l);
+        }
+    }
+    for (int64_t e = e0 + lane; e < e1; e += 32) {
+        const float s = dot64(q, Ku + (size_t)a.x_col[e] * kHeadDim) * scale;
+        Ax[e] = s;
+        online(s, m, l);
+    }
+    warp_merge(m, l);
+    const float inv = 1.f / l;
+    for (int w = lane; w < P.W; w += 32) {
+        const int64_t j = ws + w;
+        Ab[w] = (j >= lo && j <= hi) ? expf(Ab[w] - m) * inv : 0.f;
+    }
+    for (int s = lane; s < P.g_pad; s += 32) {
+        bool edge = false;
+        if (s < P.g) { const int64_t j = a.globals[s]; edge = j < lo || j > hi; }
+        Agc[s] = edge ? expf(Agc[s] - m) * inv : 0.f;
+    }
+    for (int64_t e = e0 + lane; e < e1; e += 32) Ax[e] = expf(Ax[e] - m) * inv;
+}
+
+// V [units][n][64] bf16 -> transposed fp32 plane [units][64][nz] (Z_0 for the MMA)
+__global__ void __launch_bounds__(256)
+v_to_zt_kernel(const __nv_bfloat16* __restrict__ V, float* __restrict__ Zt, int64_t n, int64_t nz,
+               int64_t units) {
+    __shared__ float tile[32][65];
+    const int64_t u = blockIdx.y;
+    const int64_t j0 = (int64_t)blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 8 warps
+    for (int r = ty; r < 32; r += 8) {
+        const int64_t j = j0 + r;
+        if (j < n) {
+            const __nv_bfloat162 h = reinterpret_cast<const __nv_bfloat162*>(
+                V + ((size_t)u * n + j) * kHeadDim)[tx];
+            tile[r][2 * tx] = __low2float(h);
+            tile[r][2 * tx + 1] = __high2float(h);
+        }
+    }
+    __syncthreads();
+    for (int dd = ty; dd < kHeadDim; dd += 8) {
+        const int64_t j = j0 + tx;
+        if (j < n) Zt[((size_t)u * kHeadDim + dd) * nz + j] = tile[tx][dd];
+    }
+}
+
+// Decomposed weights -> CSR edge order (test export of the attention weights).
+__global__ void __launch_bounds__(256)
+band_to_csr_kernel(ScoreArgs a, const int64_t* __restrict__ row_ptr,
+                   const int32_t* __restrict__ col, int64_t nnz, float* __restrict__ out) {
+    const BandPlan& P = a.plan;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= a.units * P.n) return;
+    const int64_t u = gw / P.n, i = gw - u * P.n;
+    const int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
+    float* o = out + (size_t)u * nnz;
+    if (a.is_global[i]) {
+        const float* Ag = a.A_gr + ((size_t)u * P.g + a.gslot[i]) * P.n;
+        for (int64_t e = e0 + lane; e < e1; e += 32) o[e] = Ag[col[e]];
+        return;
+    }
+    const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
+    const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+    const int64_t ws = 4 * (i / 4) - P.r_up;
+    const float* Ab = a.A_band + (size_t)u * (P.band_unit / 4) + (size_t)i * P.W;
+    const float* Agc = a.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+    const float* Ax = a.A_x + (size_t)u * a.nx;
+    int64_t xb = a.x_ptr[i];
+    // extras are the row's edges that are neither window nor global, in order
+    for (int64_t base = e0; base < e1; base += 32) {
+        const int64_t e = base + lane;
+        int64_t j = e < e1 ? col[e] : -1;
+        const bool is_x = e < e1 && (j < lo || j > hi) && !a.is_global[j < 0 ? 0 : j];
+        const unsigned mask = __ballot_sync(0xffffffffu, is_x);
+        const int rank = __popc(mask & ((1u << lane) - 1));
+        if (e < e1) {
+            float v;
+            if (j >= lo && j <= hi) v = Ab[j - ws];
+            else if (a.is_global[j]) v = Agc[a.gslot[j]];
+            else v = Ax[xb + rank];
+            o[e] = v;
+        }
+        xb += __popc(mask);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int encode(CUtensorMap* m, int rank, void* base, const cuuint64_t* dims, const cuuint64_t* strides,
+           const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, base, dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
+    return DIFFUSER_OK;
+}
+
+template <bool kHop0, bool kLast>
+int launch_hop(const CUtensorMap& tmA, const CUtensorMap& tmZt, const CUtensorMap& tmZl,
+               const HopArgs& a, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(hop_band_kernel<kHop0, kLast>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(hop)");
+    dim3 grid((unsigned)(a.units * a.plan.tiles));
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
+        hop_band_kernel<kHop0, kLast><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmZt, tmZl, a);
+    }
+    cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_band_kernel");
+}
+
+}  // namespace
+
+bool band_plan(const diffuser_graph* g, BandPlan* p) {
+    if (g->kind != kTokenGraph || g->r < 8 || g->n_globals > kBandMaxGlobals) return false;
+    p->n = g->n;
+    p->r = g->r;
+    p->r_up = (g->r + 3) / 4 * 4;
+    p->W = (p->r_up + g->r + 4 + 3) / 4 * 4;
+    p->g = g->n_globals;
+    p->g_pad = (g->n_globals + 3) / 4 * 4;
+    if (p->g_pad == 0) p->g_pad = 4;
+    p->rows4 = (g->n + 3) / 4 * 4;
+    p->nz = (g->n + 3) / 4 * 4;
+    p->tiles = (int32_t)((g->n + kTileRows - 1) / kTileRows);
+    p->chunks = (kTileRows + g->r + p->r_up + kChunkKeys - 1) / kChunkKeys;
+    const size_t need = (size_t)p->rows4 * p->W * 4 + 8 * (size_t)p->r_up + 64;
+    p->band_unit = (need + 1023) / 1024 * 1024;
+    return true;
+}
+
+int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, BandLayout* L) {
+    auto al = [](size_t x) { return (x + 1023) / 1024 * 1024; };
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off += al(bytes); return o; };
+    const size_t U = (size_t)units;
+    L->a_band = take(U * p.band_unit);
+    L->a_gc = take(U * (size_t)p.n * p.g_pad * 4);
+    L->a_x = take(U * (size_t)(g->nx > 0 ? g->nx : 1) * 4);
+    L->a_gr = take(U * (size_t)(p.g > 0 ? p.g : 1) * p.n * 4);
+    for (int s = 0; s < 2; ++s) {
+        L->zr[s] = take(U * (size_t)p.n * kHeadDim * 4);
+        L->zt[s] = take(U * (size_t)kHeadDim * p.nz * 4);
+        L->ztl[s] = take(U * (size_t)kHeadDim * p.nz * 4);
+    }
+    L->gpart = take(U * (size_t)p.tiles * (p.g > 0 ? p.g : 1) * kHeadDim * 4);
+    L->counters = take(U * 4);
+    L->total = off;
+    return DIFFUSER_OK;
+}
+
+namespace {
+ScoreArgs score_args(const diffuser_graph* g, const BandPlan& p, int64_t units, char* ws,
+                     const BandLayout& L) {
+    ScoreArgs s;
+    s.plan = p;
+    s.units = units;
+    s.is_global = g->d_is_global;
+    s.gslot = g->d_gslot;
+    s.globals = g->d_globals;
+    s.x_ptr = g->d_x_ptr;
+    s.x_col = g->d_x_col;
+    s.nx = g->nx;
+    s.A_band = reinterpret_cast<float*>(ws + L.a_band);
+    s.A_gc = reinterpret_cast<float*>(ws + L.a_gc);
+    s.A_x = reinterpret_cast<float*>(ws + L.a_x);
+    s.A_gr = reinterpret_cast<float*>(ws + L.a_gr);
+    return s;
+}
+}  // namespace
+
+int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
+                       const void* K, char* ws, const BandLayout& L, cudaStream_t stream) {
+    ScoreArgs s = score_args(g, p, units, ws, L);
+    const unsigned grid = (unsigned)((units * p.n + 7) / 8);
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
+        score_band_simt_kernel<<<grid, 256, 0, stream>>>(
+            s, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K));
+    }
+    cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "score_band_simt_kernel");
+}
+
+int launch_band_to_csr(const diffuser_graph* g, const BandPlan& p, int64_t units, char* ws,
+                       const BandLayout& L, float* A_out, cudaStream_t stream) {
+    ScoreArgs s = score_args(g, p, units, ws, L);
+    const unsigned grid = (unsigned)((units * p.n + 7) / 8);
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_AUX, stream);
+        band_to_csr_kernel<<<grid, 256, 0, stream>>>(s, g->d_row_ptr, g->d_col, g->nnz, A_out);
+    }
+    cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "band_to_csr_kernel");
+}
+
+int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* V,
+                     int32_t hops, float alpha, void* out, char* ws, const BandLayout& L,
+                     cudaStream_t stream) {
+    cudaError_t err;
+    float* zt0 = reinterpret_cast<float*>(ws + L.zt[0]);
+    {
+        dim3 grid((unsigned)((p.n + 31) / 32), (unsigned)units);
+        LaunchScope scope(DIFFUSER_KERNEL_AUX, stream);
+        v_to_zt_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(V), zt0, p.n,
+                                                 p.nz, units);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "v_to_zt_kernel");
+    err = cudaMemsetAsync(ws + L.counters, 0, (size_t)units * 4, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "clearing the tile counters");
+
+    // tensor maps: band weights (sheared 4-D view) and the two transposed Z planes
+    CUtensorMap tmA, tmZt[2], tmZl[2];
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)(p.n + 2 * p.r_up + 4), 4,
+                                    (cuuint64_t)(p.rows4 / 4), (cuuint64_t)units};
+        const cuuint64_t strides[3] = {(cuuint64_t)p.W * 4, (cuuint64_t)(p.W - 1) * 16,
+                                       (cuuint64_t)p.band_unit};
+        const cuuint32_t box[4] = {32, 4, 32, 1};
+        int st = encode(&tmA, 4, ws + L.a_band, dims, strides, box);
+        if (st) return st;
+    }
+    for (int s = 0; s < 2; ++s) {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.n, (cuuint64_t)kHeadDim, (cuuint64_t)units};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.nz * 4, (cuuint64_t)p.nz * 4 * kHeadDim};
+        const cuuint32_t box[3] = {32, (cuuint32_t)kHeadDim, 1};
+        int st = encode(&tmZt[s], 3, ws + L.zt[s], dims, strides, box);
+        if (!st) st = encode(&tmZl[s], 3, ws + L.ztl[s], dims, strides, box);
+        if (st) return st;
+    }
+
+    HopArgs a;
+    a.plan = p;
+    a.units = units;
+    a.alpha = alpha;
+    a.is_global = g->d_is_global;
+    a.globals = g->d_globals;
+    a.x_ptr = g->d_x_ptr;
+    a.x_col = g->d_x_col;
+    a.nx = g->nx;
+    a.A_gc = reinterpret_cast<const float*>(ws + L.a_gc);
+    a.A_x = reinterpret_cast<const float*>(ws + L.a_x);
+    a.A_gr = reinterpret_cast<const float*>(ws + L.a_gr);
+    a.V = static_cast<const __nv_bfloat16*>(V);
+    a.gpart = reinterpret_cast<float*>(ws + L.gpart);
+    a.counters = reinterpret_cast<int*>(ws + L.counters);
+    a.status = g->d_status;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    for (int32_t k = 0; k < hops; ++k) {
+        const int cur = k & 1, nxt = (k + 1) & 1;
+        a.Zr_in = k == 0 ? V : static_cast<const void*>(ws + L.zr[cur]);
+        a.Zr_out = reinterpret_cast<float*>(ws + L.zr[nxt]);
+        a.Zt_out = reinterpret_cast<float*>(ws + L.zt[nxt]);
+        a.Ztl_out = reinterpret_cast<float*>(ws + L.ztl[nxt]);
+        const bool first = k == 0, last = k == hops - 1;
+        int st;
+        if (first && last) st = launch_hop<true, true>(tmA, tmZt[cur], tmZl[cur], a, stream);
+        else if (first) st = launch_hop<true, false>(tmA, tmZt[cur], tmZl[cur], a, stream);
+        else if (last) st = launch_hop<false, true>(tmA, tmZt[cur], tmZl[cur], a, stream);
+        else st = launch_hop<false, false>(tmA, tmZt[cur], tmZl[cur], a, stream);
+        if (st) return st;
+    }
+    return DIFFUSER_OK;
+}
+
+}  // namespace dfs

@@ -97,6 +97,27 @@ __device__ int64_t merge_range(const int32_t* G, int32_t g, const int32_t* xs, i
     return w;
 }
 
+__global__ void extras_count_kernel(TokenParams p, int64_t* counts) {
+    extern __shared__ int32_t smem_xs[];
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n) return;
+    if (p.is_global[i]) { counts[i] = 0; return; }
+    int64_t lo = i - p.r < 0 ? 0 : i - p.r;
+    int64_t hi = i + p.r > p.n - 1 ? p.n - 1 : i + p.r;
+    counts[i] = row_extras(p, i, lo, hi, smem_xs + (size_t)threadIdx.x * p.R);
+}
+
+__global__ void extras_fill_kernel(TokenParams p, const int64_t* x_ptr, int32_t* x_col) {
+    extern __shared__ int32_t smem_xs[];
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n || p.is_global[i]) return;
+    int64_t lo = i - p.r < 0 ? 0 : i - p.r;
+    int64_t hi = i + p.r > p.n - 1 ? p.n - 1 : i + p.r;
+    int32_t* xs = smem_xs + (size_t)threadIdx.x * p.R;
+    int32_t nx = row_extras(p, i, lo, hi, xs);
+    for (int32_t q = 0; q < nx; ++q) x_col[x_ptr[i] + q] = xs[q];
+}
+
 __global__ void token_fill_kernel(TokenParams p, const int64_t* row_ptr, int32_t* col) {
     extern __shared__ int32_t smem_xs[];
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -241,6 +262,37 @@ int scan_and_alloc(diffuser_graph* g, int64_t* d_counts, cudaStream_t stream) {
     return DIFFUSER_OK;
 }
 
+// Extras list (random edges outside the window and G): count, scan, fill.
+int build_extras(diffuser_graph* g, const TokenParams& p, unsigned blocks, int threads,
+                 size_t shmem, int64_t* d_counts, cudaStream_t stream) {
+    cudaError_t err;
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_BUILD, stream);
+        extras_count_kernel<<<blocks, threads, shmem, stream>>>(p, d_counts);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "extras_count_kernel");
+    err = cudaMalloc(&g->d_x_ptr, sizeof(int64_t) * (g->n + 1));
+    if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(x_ptr) failed");
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_BUILD, stream);
+        exclusive_scan_kernel<<<1, 1024, 0, stream>>>(d_counts, g->n, g->d_x_ptr);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "exclusive_scan_kernel");
+    int64_t nx = 0;
+    err = cudaMemcpyAsync(&nx, g->d_x_ptr + g->n, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) return cuda_fail(err, "reading the extras count");
+    g->nx = nx;
+    err = cudaMalloc(&g->d_x_col, sizeof(int32_t) * (nx > 0 ? nx : 1));
+    if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(x_col) failed");
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_BUILD, stream);
+        extras_fill_kernel<<<blocks, threads, shmem, stream>>>(p, g->d_x_ptr, g->d_x_col);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "extras_fill_kernel");
+    return DIFFUSER_OK;
+}
+
 int copy_csr_to_host(diffuser_graph* g, cudaStream_t stream) {
     g->h_row_ptr.resize(g->n + 1);
     g->h_col.resize(g->nnz);
@@ -260,9 +312,18 @@ int build_token_graph_device(diffuser_graph* g, cudaStream_t stream) {
     const int64_t n = g->n;
     cudaError_t err;
     std::vector<uint8_t> flags(n, 0);
-    for (int32_t v : g->h_globals) flags[v] = 1;
+    std::vector<int32_t> slots(n, -1);
+    for (size_t s = 0; s < g->h_globals.size(); ++s) {
+        flags[g->h_globals[s]] = 1;
+        slots[g->h_globals[s]] = (int32_t)s;
+    }
     err = cudaMalloc(&g->d_is_global, n);
     if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(is_global) failed");
+    err = cudaMalloc(&g->d_gslot, sizeof(int32_t) * n);
+    if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(gslot) failed");
+    err = cudaMemcpyAsync(g->d_gslot, slots.data(), sizeof(int32_t) * n, cudaMemcpyHostToDevice,
+                          stream);
+    if (err != cudaSuccess) return cuda_fail(err, "uploading the global slots");
     err = cudaMalloc(&g->d_globals, sizeof(int32_t) * (g->n_globals > 0 ? g->n_globals : 1));
     if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(globals) failed");
     err = cudaMemcpyAsync(g->d_is_global, flags.data(), n, cudaMemcpyHostToDevice, stream);
@@ -295,6 +356,7 @@ int build_token_graph_device(diffuser_graph* g, cudaStream_t stream) {
         }
         if ((err = cudaGetLastError()) != cudaSuccess) status = cuda_fail(err, "token_fill_kernel");
     }
+    if (status == DIFFUSER_OK) status = build_extras(g, p, blocks, threads, shmem, d_counts, stream);
     if (status == DIFFUSER_OK) status = copy_csr_to_host(g, stream);
     cudaFree(d_counts);
     return status;

@@ -17,8 +17,29 @@ constexpr int32_t kMaxRandPerRow = 1024;
 constexpr int32_t kMaxWindowBlocks = 63;
 constexpr int32_t kMaxRandBlocks = 64;
 constexpr int64_t kMaxNnz = int64_t(1) << 40;
+constexpr int32_t kBandMaxGlobals = 32;   // the band path handles at most this many globals
 
 enum GraphKind { kTokenGraph = 0, kBlockGraph = 1 };
+
+// Geometry of the band path's decomposed weight layout (token graphs).
+struct BandPlan {
+    int64_t n;          // sequence length
+    int32_t r, r_up;    // window radius, and the radius rounded up to a multiple of 4
+    int32_t W;          // stored window width per row (multiple of 4, covers 2r+1 keys)
+    int32_t g, g_pad;   // number of globals, padded to a multiple of 4
+    int64_t rows4;      // n rounded up to a multiple of 4
+    int64_t nz;         // key stride of the transposed Z planes (multiple of 4)
+    int32_t tiles;      // 128-row tiles per unit
+    int32_t chunks;     // 32-key chunks per tile
+    size_t band_unit;   // bytes of one unit's band weights (with slack for the sheared reads)
+};
+
+// Byte offsets of the band path's workspace regions.
+struct BandLayout {
+    size_t a_band, a_gc, a_x, a_gr;
+    size_t zr[2], zt[2], ztl[2];
+    size_t gpart, counters, total;
+};
 
 }  // namespace dfs
 
@@ -37,6 +58,12 @@ struct diffuser_graph {
     int32_t* d_col = nullptr;
     int32_t* d_globals = nullptr;     // token graph: sorted global positions
     uint8_t* d_is_global = nullptr;   // token graph: per-position flag
+    int32_t* d_gslot = nullptr;       // token graph: slot of a position in G, or -1
+    // token graph, decomposed layout: random edges outside the window and G
+    int64_t nx = 0;                   // number of such "extra" edges
+    int64_t* d_x_ptr = nullptr;       // [n+1]
+    int32_t* d_x_col = nullptr;       // [nx], ascending within a row
+    int* d_status = nullptr;          // device status word written by kernels (0 = ok)
     // host copy of the CSR
     std::vector<int64_t> h_row_ptr;
     std::vector<int32_t> h_col;
@@ -87,5 +114,16 @@ int launch_score_csr(const CsrArgs& a, const void* Q, const void* K, int32_t dty
 int launch_hop_csr(const CsrArgs& a, const float* A, const void* src, bool src_is_io,
                    const void* V, void* dst, bool dst_is_io, int32_t dtype, float alpha,
                    cudaStream_t stream);
+
+// ---- band path (band_path.cu): token graphs, bf16 I/O ----------------------
+bool band_plan(const diffuser_graph* g, BandPlan* p);   // false: graph not eligible
+int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, BandLayout* L);
+int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
+                       const void* K, char* ws, const BandLayout& L, cudaStream_t stream);
+int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* V,
+                     int32_t hops, float alpha, void* out, char* ws, const BandLayout& L,
+                     cudaStream_t stream);
+int launch_band_to_csr(const diffuser_graph* g, const BandPlan& p, int64_t units, char* ws,
+                       const BandLayout& L, float* A_out, cudaStream_t stream);
 
 }  // namespace dfs

@@ -195,6 +195,33 @@ def test_attention_weights_parity(dl, dtype):
         np.testing.assert_allclose(A[u], ref, rtol=2e-5, atol=1e-8)
 
 
+@pytest.mark.parametrize("case", [(1, 2, 300, 8, 3, 5), (2, 3, 1000, 64, 8, 16),
+                                  (1, 2, 777, 33, 0, 7), (1, 1, 4096, 256, 16, 32)],
+                         ids=lambda c: "B%dH%dn%dr%dg%dR%d" % c)
+def test_band_path_matches_csr_path(dl, case):
+    # the tensor-core band path and the general CSR path on the same inputs
+    import torch
+    B, H, n, r, gn, R = case
+    g = dl.diffuser_build_graph(n, r, gn, rand_per_row=R, seed=3)
+    Q, K, V = synthetic.qkv(B, H, n, 64, "bf16", seed=11)
+    Qd, Kd, Vd = (to_device(x, "bf16") for x in (Q, K, V))
+    try:
+        dl.diffuser_set_path(dl.DIFFUSER_PATH_CSR)
+        ref = to_f64(dl.diffuser_forward(Qd, Kd, Vd, g, 5, 0.1))
+    finally:
+        dl.diffuser_set_path(dl.DIFFUSER_PATH_AUTO)
+    out = to_f64(dl.diffuser_forward(Qd, Kd, Vd, g, 5, 0.1))
+    torch.cuda.synchronize()
+    assert dl.diffuser_graph_status(g) == 0
+    o_ptr, o_col = oracle.token_graph(n, r, gn, R, seed=3)
+    oref = oracle.forward(oracle.widen(Q, "bf16"), oracle.widen(K, "bf16"),
+                          oracle.widen(V, "bf16"), o_ptr, o_col, 5, 0.1, nthreads=4)
+    check_output(out, oref, "bf16")
+    check_output(ref, oref, "bf16")
+    # both round the same fp32-accurate values to bf16: at most one bf16 ulp apart
+    assert np.abs(out - ref).max() <= 2 ** -7 * np.abs(oref).max()
+
+
 def test_constant_v_is_preserved(dl):
     # A is row-stochastic, so a constant V is a fixed point of every hop
     import torch
