@@ -40,16 +40,22 @@ namespace {
 
 constexpr int kTileRows = 128;
 constexpr int kChunkKeys = 32;
+// One CTA per SM: with two co-resident CTAs of this kernel, stale shared-memory
+// tiles were observed in the first chunk of some tiles, so the kernel claims a
+// whole SM (its shared memory alone rules out a second CTA) and uses the room
+// for deeper pipelines.
 constexpr int kThreads = 320;            // 10 warps
-constexpr int kAStages = 2;              // smem stages of A (16 KB each)
-constexpr int kZStages = 2;              // smem stages of Z^T hi+lo (16 KB each)
-constexpr int kTStages = 3;              // TMEM stages of A hi+lo (64 columns each)
-constexpr int kTmemCols = 256;
+constexpr int kAStages = 4;              // smem stages of A (16 KB each)
+constexpr int kZStages = 4;              // smem stages of Z^T hi+lo (16 KB each)
+constexpr int kTStages = 7;              // TMEM stages of A hi+lo (64 columns each)
+constexpr int kTmemCols = 512;
 constexpr int kPStride = 68;             // floats per row of the gather partial buffer
 constexpr int kAStageBytes = kTileRows * kChunkKeys * 4;
 constexpr int kZPlaneBytes = kHeadDim * kChunkKeys * 4;
 constexpr int kSmemBytes = 1024 + kAStages * kAStageBytes + kZStages * 2 * kZPlaneBytes +
                            kTileRows * kPStride * 4 + 256;
+static_assert(kSmemBytes > 116 * 1024, "must exclude a second CTA per SM");
+static_assert(64 + 64 * kTStages <= kTmemCols, "TMEM columns");
 
 __device__ __forceinline__ float tf32_trunc(float x) {
     return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
@@ -94,7 +100,7 @@ __device__ __forceinline__ float2 zpair(const HopArgs& a, int64_t u, int64_t j, 
 }
 
 template <bool kHop0, bool kLast>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmZt,
                 const __grid_constant__ CUtensorMap tmZl, HopArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -182,6 +188,18 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 ptx::mma_commit(&empty_Z[sz]);
             }
             ptx::mma_commit(acc_full);
+            // Drain: the commits arrive asynchronously when the MMAs finish.  Wait
+            // for the last phase of every empty barrier so that no arrival can land
+            // in this shared memory after the CTA exits (it would hit the barriers
+            // of the next CTA placed here).
+            for (int s = 0; s < kTStages; ++s) {
+                const int uses = (chunks - s + kTStages - 1) / kTStages;
+                if (uses > 0) ptx::mbar_wait(&empty_tA[s], (uses - 1) & 1, a.status);
+            }
+            for (int s = 0; s < kZStages; ++s) {
+                const int uses = (chunks - s + kZStages - 1) / kZStages;
+                if (uses > 0) ptx::mbar_wait(&empty_Z[s], (uses - 1) & 1, a.status);
+            }
         }
     } else if (warp < 4) {
         // ---------------- A splitter: smem (raw, de-skewed) -> masked hi / lo -> TMEM
@@ -203,6 +221,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             ptx::mbar_arrive(&empty_sA[sa]);
             if (c >= kTStages) ptx::mbar_wait(&empty_tA[ta], ((c / kTStages) - 1) & 1, a.status);
+            __syncwarp();   // lanes leave the spin at different times; tcgen05.st is warp-collective
             ptx::tc_fence_after();
             const int64_t j0 = jb + kChunkKeys * c;
 #pragma unroll
@@ -327,6 +346,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         __syncwarp();
         // (3) epilogue: accumulator + gathers, restart term, outputs
         ptx::mbar_wait(acc_full, 0, a.status);
+        __syncwarp();       // reconverge before the warp-collective tcgen05.ld
         ptx::tc_fence_after();
         const int t = q * 32 + lane;
         const int64_t i = i0 + t;

@@ -234,6 +234,24 @@ def test_constant_v_is_preserved(dl):
     assert float((out.float() - 0.75).abs().max()) <= 0.75 * 2 ** -8
 
 
+def test_band_path_repeatable_under_load(dl):
+    # Many tiles per SM over repeated calls: a constant V must come back exactly
+    # (A is row-stochastic) on every unit, every call.  Guards the tensor-core
+    # pipeline against stale shared-memory or TMEM stages.
+    import torch
+    B, H, n = 32, 8, 1024
+    g = dl.diffuser_build_graph(n, 32, 8, rand_per_row=16)
+    Q, K, _ = synthetic.qkv(B, H, n, 64, "bf16", seed=5)
+    Qd, Kd = to_device(Q, "bf16"), to_device(K, "bf16")
+    V = torch.full((B, H, n, 64), 0.5, dtype=torch.bfloat16, device="cuda")
+    ws = dl.alloc_workspace(dl.diffuser_workspace_size(g, B, H, 64, dl.DIFFUSER_DTYPE_BF16))
+    for hops in (1, 5, 5, 5, 5, 5):
+        out = dl.diffuser_forward(Qd, Kd, V, g, hops, 0.1, workspace=ws)
+        torch.cuda.synchronize()
+        assert float((out.float() - 0.5).abs().max()) <= 0.5 * 2 ** -8
+    assert dl.diffuser_graph_status(g) == 0
+
+
 def test_bad_workspace_launches_nothing(dl):
     import torch
     g = dl.diffuser_build_graph(256, 8, 1, rand_per_row=2)
