@@ -84,6 +84,7 @@ struct HopArgs {
     float* gpart;         // [units][tiles][g][64]
     int* counters;        // [units]
     int* status;
+    float* Psum;          // [units][n][64]: gathered part of (A Z_k) per row
 };
 
 // Two features (2*lane, 2*lane+1) of row j of Z_k.
@@ -118,7 +119,6 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t* empty_Z = full_Z + kZStages;
     uint64_t* acc_full = empty_Z + kZStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
-    int* ticket = reinterpret_cast<int*>(tmem_slot + 1);
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -239,112 +239,19 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             ptx::mbar_arrive(&full_tA[ta]);
         }
     } else {
-        // ---------------- gathers (global rows share, gcol, extras) + epilogue
+        // ---------------- epilogue: accumulator + gathered part, restart term, outputs
         const int q = warp - 4;                  // TMEM lane quadrant and row block
-        const int sim_tid = tid - 128;           // 0..127
-        const int g = P.g;
-        // (1) global rows: this tile's keys contribute sum_j A_gr[s][j] Z_k[j]
-        if (g > 0) {
-            for (int s0 = 0; s0 < g; s0 += 8) {
-                float2 acc[8];
-#pragma unroll
-                for (int s = 0; s < 8; ++s) acc[s] = make_float2(0.f, 0.f);
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int64_t j = i0 + 32 * q + jj;
-                    if (j >= P.n) break;
-                    const float2 z = zpair<kHop0>(a, u, j, lane);
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        if (s0 + s < g) {
-                            const float w = __ldg(a.A_gr + ((size_t)u * g + s0 + s) * P.n + j);
-                            acc[s].x = fmaf(w, z.x, acc[s].x);
-                            acc[s].y = fmaf(w, z.y, acc[s].y);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    if (s0 + s < g) {
-                        float* dst = sP + (q * 32 + s0 + s) * kHeadDim + 2 * lane;
-                        dst[0] = acc[s].x;
-                        dst[1] = acc[s].y;
-                    }
-                }
-            }
-            ptx::named_barrier_sync(1, 128);
-            float* part = a.gpart + (((size_t)u * P.tiles + tile) * g) * kHeadDim;
-            for (int e = sim_tid; e < g * kHeadDim; e += 128) {
-                const int s = e / kHeadDim, dd = e % kHeadDim;
-                float sum = 0.f;
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) sum += sP[(qq * 32 + s) * kHeadDim + dd];
-                part[e] = sum;
-            }
-            __threadfence();
-            ptx::named_barrier_sync(1, 128);
-            if (sim_tid == 0) *ticket = atomicAdd(&a.counters[u], 1);
-            ptx::named_barrier_sync(1, 128);
-            if (*ticket == P.tiles - 1) {
-                // last tile of this unit: sum the shares in tile order, write the global rows
-                __threadfence();
-                const float keep = 1.f - a.alpha;
-                for (int e = sim_tid; e < g * kHeadDim; e += 128) {
-                    const int s = e / kHeadDim, dd = e % kHeadDim;
-                    float sum = 0.f;
-                    for (int tt = 0; tt < P.tiles; ++tt)
-                        sum += __ldcg(a.gpart + (((size_t)u * P.tiles + tt) * g + s) * kHeadDim + dd);
-                    const int64_t gi = a.globals[s];
-                    const size_t row = ((size_t)u * P.n + gi) * kHeadDim + dd;
-                    const float z = fmaf(keep, sum, a.alpha * __bfloat162float(a.V[row]));
-                    if (kLast) {
-                        a.out[row] = __float2bfloat16_rn(z);
-                    } else {
-                        a.Zr_out[row] = z;
-                        const size_t tr = ((size_t)u * kHeadDim + dd) * P.nz + gi;
-                        a.Zt_out[tr] = z;
-                        a.Ztl_out[tr] = z - tf32_trunc(z);
-                    }
-                }
-                if (sim_tid == 0) a.counters[u] = 0;
-            }
-            ptx::named_barrier_sync(1, 128);
-        }
-        // (2) globals outside the window and random extras, one row at a time
+        // stage this block's gathered partial sums (coalesced) while the MMAs run
         for (int rr = 0; rr < 32; ++rr) {
             const int t = q * 32 + rr;
             const int64_t i = i0 + t;
-            float2 acc = make_float2(0.f, 0.f);
-            if (i < P.n && !a.is_global[i]) {
-                const float* wg = a.A_gc + ((size_t)u * P.n + i) * P.g_pad;
-                for (int s = 0; s < g; ++s) {
-                    const float w = __ldg(wg + s);
-                    if (w != 0.f) {
-                        const float2 z = zpair<kHop0>(a, u, a.globals[s], lane);
-                        acc.x = fmaf(w, z.x, acc.x);
-                        acc.y = fmaf(w, z.y, acc.y);
-                    }
-                }
-                const int64_t e0 = a.x_ptr[i], e1 = a.x_ptr[i + 1];
-                const float* ax = a.A_x + (size_t)u * a.nx;
-                for (int64_t base = e0; base < e1; base += 32) {
-                    const int64_t e = base + lane;
-                    const float w_l = e < e1 ? __ldg(ax + e) : 0.f;
-                    const int32_t j_l = e < e1 ? __ldg(a.x_col + e) : 0;
-                    const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
-                    for (int tt = 0; tt < cnt; ++tt) {
-                        const float w = __shfl_sync(0xffffffffu, w_l, tt);
-                        const int32_t j = __shfl_sync(0xffffffffu, j_l, tt);
-                        const float2 z = zpair<kHop0>(a, u, j, lane);
-                        acc.x = fmaf(w, z.x, acc.x);
-                        acc.y = fmaf(w, z.y, acc.y);
-                    }
-                }
-            }
-            sP[t * kPStride + 2 * lane] = acc.x;
-            sP[t * kPStride + 2 * lane + 1] = acc.y;
+            float2 pv = make_float2(0.f, 0.f);
+            if (i < P.n)
+                pv = __ldg(reinterpret_cast<const float2*>(a.Psum + ((size_t)u * P.n + i) * kHeadDim) + lane);
+            sP[t * kPStride + 2 * lane] = pv.x;
+            sP[t * kPStride + 2 * lane + 1] = pv.y;
         }
         __syncwarp();
-        // (3) epilogue: accumulator + gathers, restart term, outputs
         ptx::mbar_wait(acc_full, 0, a.status);
         __syncwarp();       // reconverge before the warp-collective tcgen05.ld
         ptx::tc_fence_after();
@@ -402,6 +309,138 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+
+// ---------------------------------------------------------------- sparse part of a hop
+// One CTA per (unit, 128-row block), 8 warps.  (1) The global rows: this
+// block's keys contribute sum_j A_gr[s][j] Z_k[j]; the last block of a unit
+// sums the shares in block order and writes Z_{k+1} of the global rows.
+// (2) Every other row: the globals outside its window and its random extras,
+// gathered as whole 256-byte Z_k rows in batches of independent loads, into
+// Psum[u][i] (fp32), which the band kernel's epilogue adds.
+constexpr int kSparseThreads = 256;
+constexpr int kGatherBatch = 8;
+
+template <bool kHop0, bool kLast>
+__global__ void __launch_bounds__(kSparseThreads)
+hop_sparse_kernel(HopArgs a) {
+    extern __shared__ float red[];           // [8 warps][g][65]: per-warp global-row shares
+    __shared__ int ticket;
+    const BandPlan& P = a.plan;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t u = blockIdx.x / P.tiles;
+    const int tile = (int)(blockIdx.x - u * P.tiles);
+    const int64_t i0 = (int64_t)tile * kTileRows;
+    const int g = P.g;
+
+    if (g > 0) {
+        // (1) this warp's 16 keys j = i0 + 16 warp + jj
+        float2 z[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int64_t j = i0 + 16 * warp + jj;
+            z[jj] = j < P.n ? zpair<kHop0>(a, u, j, lane) : make_float2(0.f, 0.f);
+        }
+        for (int s = 0; s < g; ++s) {
+            const float* wrow = a.A_gr + ((size_t)u * g + s) * P.n;
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const int64_t j = i0 + 16 * warp + jj;
+                const float w = j < P.n ? __ldg(wrow + j) : 0.f;
+                acc.x = fmaf(w, z[jj].x, acc.x);
+                acc.y = fmaf(w, z[jj].y, acc.y);
+            }
+            red[(warp * g + s) * 65 + 2 * lane] = acc.x;
+            red[(warp * g + s) * 65 + 2 * lane + 1] = acc.y;
+        }
+        __syncthreads();
+        float* part = a.gpart + (((size_t)u * P.tiles + tile) * g) * kHeadDim;
+        for (int e = tid; e < g * kHeadDim; e += kSparseThreads) {
+            const int s = e / kHeadDim, dd = e % kHeadDim;
+            float sum = 0.f;
+#pragma unroll
+            for (int w8 = 0; w8 < 8; ++w8) sum += red[(w8 * g + s) * 65 + dd];
+            part[e] = sum;
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) ticket = atomicAdd(&a.counters[u], 1);
+        __syncthreads();
+        if (ticket == P.tiles - 1) {
+            __threadfence();
+            const float keep = 1.f - a.alpha;
+            for (int e = tid; e < g * kHeadDim; e += kSparseThreads) {
+                const int s = e / kHeadDim, dd = e % kHeadDim;
+                float sum = 0.f;
+                for (int tt = 0; tt < P.tiles; ++tt)
+                    sum += __ldcg(a.gpart + (((size_t)u * P.tiles + tt) * g + s) * kHeadDim + dd);
+                const int64_t gi = a.globals[s];
+                const size_t row = ((size_t)u * P.n + gi) * kHeadDim + dd;
+                const float zz = fmaf(keep, sum, a.alpha * __bfloat162float(a.V[row]));
+                if (kLast) {
+                    a.out[row] = __float2bfloat16_rn(zz);
+                } else {
+                    a.Zr_out[row] = zz;
+                    const size_t tr = ((size_t)u * kHeadDim + dd) * P.nz + gi;
+                    a.Zt_out[tr] = zz;
+                    a.Ztl_out[tr] = zz - tf32_trunc(zz);
+                }
+            }
+            if (tid == 0) a.counters[u] = 0;
+        }
+    }
+    // (2) rows of this block: 16 per warp
+    const float* ax = a.A_x + (size_t)u * a.nx;
+    for (int rr = 0; rr < 16; ++rr) {
+        const int64_t i = i0 + 16 * warp + rr;
+        if (i >= P.n) break;
+        if (a.is_global[i]) continue;
+        float2 acc = make_float2(0.f, 0.f);
+        // globals outside the window (weight 0 marks "inside the window")
+        const float* wg = a.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+        for (int s0 = 0; s0 < g; s0 += kGatherBatch) {
+            float w[kGatherBatch];
+            float2 zz[kGatherBatch];
+#pragma unroll
+            for (int b = 0; b < kGatherBatch; ++b) {
+                w[b] = s0 + b < g ? __ldg(wg + s0 + b) : 0.f;
+                zz[b] = w[b] != 0.f ? zpair<kHop0>(a, u, a.globals[s0 + b], lane) : make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int b = 0; b < kGatherBatch; ++b) {
+                acc.x = fmaf(w[b], zz[b].x, acc.x);
+                acc.y = fmaf(w[b], zz[b].y, acc.y);
+            }
+        }
+        // random extras: lanes fetch (weight, column) 32 at a time, then batches of loads
+        const int64_t e0 = a.x_ptr[i], e1 = a.x_ptr[i + 1];
+        for (int64_t base = e0; base < e1; base += 32) {
+            const int64_t e = base + lane;
+            const float w_l = e < e1 ? __ldg(ax + e) : 0.f;
+            const int32_t j_l = e < e1 ? __ldg(a.x_col + e) : 0;
+            const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
+            for (int t0 = 0; t0 < cnt; t0 += kGatherBatch) {
+                float w[kGatherBatch];
+                float2 zz[kGatherBatch];
+#pragma unroll
+                for (int b = 0; b < kGatherBatch; ++b) {
+                    const int src = t0 + b < cnt ? t0 + b : 0;
+                    w[b] = __shfl_sync(0xffffffffu, w_l, src);
+                    const int32_t j = __shfl_sync(0xffffffffu, j_l, src);
+                    if (t0 + b >= cnt) w[b] = 0.f;
+                    zz[b] = zpair<kHop0>(a, u, j, lane);
+                }
+#pragma unroll
+                for (int b = 0; b < kGatherBatch; ++b) {
+                    acc.x = fmaf(w[b], zz[b].x, acc.x);
+                    acc.y = fmaf(w[b], zz[b].y, acc.y);
+                }
+            }
+        }
+        reinterpret_cast<float2*>(a.Psum + ((size_t)u * P.n + i) * kHeadDim)[lane] = acc;
+    }
 }
 
 // ---------------------------------------------------------------- scores (SIMT)
@@ -629,13 +668,26 @@ int encode(CUtensorMap* m, int rank, void* base, const cuuint64_t* dims, const c
 template <bool kHop0, bool kLast>
 int launch_hop(const CUtensorMap& tmA, const CUtensorMap& tmZt, const CUtensorMap& tmZl,
                const HopArgs& a, cudaStream_t stream) {
+
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(hop_band_kernel<kHop0, kLast>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(hop_sparse_kernel<kHop0, kLast>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            8 * kBandMaxGlobals * 65 * (int)sizeof(float));
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(hop)");
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
+        const size_t shmem = (size_t)8 * a.plan.g * 65 * sizeof(float);
+        hop_sparse_kernel<kHop0, kLast><<<(unsigned)(a.units * a.plan.tiles), kSparseThreads,
+                                          shmem, stream>>>(a);
+    }
+    cudaError_t serr = cudaGetLastError();
+    if (serr != cudaSuccess) return cuda_fail(serr, "hop_sparse_kernel");
     dim3 grid((unsigned)(a.units * a.plan.tiles));
     {
         LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
@@ -680,6 +732,7 @@ int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, 
         L->ztl[s] = take(U * (size_t)kHeadDim * p.nz * 4);
     }
     L->gpart = take(U * (size_t)p.tiles * (p.g > 0 ? p.g : 1) * kHeadDim * 4);
+    L->psum = take(U * (size_t)p.n * kHeadDim * 4);
     L->counters = take(U * 4);
     L->total = off;
     return DIFFUSER_OK;
@@ -782,6 +835,7 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     a.counters = reinterpret_cast<int*>(ws + L.counters);
     a.status = g->d_status;
     a.out = static_cast<__nv_bfloat16*>(out);
+    a.Psum = reinterpret_cast<float*>(ws + L.psum);
     for (int32_t k = 0; k < hops; ++k) {
         const int cur = k & 1, nxt = (k + 1) & 1;
         a.Zr_in = k == 0 ? V : static_cast<const void*>(ws + L.zr[cur]);
