@@ -1,0 +1,67 @@
+// Shared pieces of the band path (token graphs, bf16 I/O): kernel argument
+// blocks and small device helpers used by the score and hop kernels.
+//
+// Weight layout of one (batch, head) unit u ("Diffuser: modelling long
+// sequences with multi-hop attention diffusion", sec 2.2 / 2.4: score once,
+// aggregate K times).  The weights are stored unnormalized, e_ij =
+// exp(s_ij - m_i), together with inv_l_i = 1 / sum_j e_ij, so that
+// A_ij = e_ij * inv_l_i ("1.2.1 Static sparsity", eq 3):
+//   band   [rows4][W]  row i, column w <-> key j = 4*floor(i/4) - r_up + w;
+//                      e_ij for |i-j| <= r, 0 <= j < n (other entries are masked)
+//   gcol   [n][g_pad]  slot s <-> key G[s]: e for globals outside row i's window, else 0
+//   extra  [nx]        e of the random edges outside window and G, CSR order
+//   inv_l  [n]         per-row normalizer of the rows not in G
+//   grow   [g][n]      raw scores s_ij of the global rows, with
+//   gstat  [g][2]      their (row max, 1 / row sum of exp(s - max))
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace dfs {
+namespace band {
+
+constexpr int kTileRows = 128;
+
+__device__ __forceinline__ float tf32_trunc(float x) {
+    return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Pointers into the band layout of the workspace (see plan_band_layout).
+struct Weights {
+    float* A_band;     // units x band_unit bytes
+    float* A_gc;       // [units][n][g_pad]
+    float* A_x;        // [units][nx]
+    float* A_gr;       // [units][g][n] raw global-row scores
+    float* inv_l;      // [units][n]
+    float* m_sparse;   // [units][n] max raw score over a row's gcol + extras
+    float* gstat;      // [units][g][2]
+    float* sstat;      // [units][tiles][g][2] per-tile (max, sum) of the global rows
+};
+
+struct GraphRefs {
+    const uint8_t* is_global;
+    const int32_t* gslot;
+    const int32_t* globals;
+    const int64_t* x_ptr;
+    const int32_t* x_col;
+    int64_t nx;
+};
+
+// Driver entry point of cuTensorMapEncodeTiled (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+}  // namespace band
+
+band::GraphRefs band_graph_refs(const diffuser_graph* g);
+band::Weights band_weights(char* ws, const BandLayout& L);
+
+}  // namespace dfs

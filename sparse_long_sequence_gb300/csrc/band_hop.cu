@@ -1,15 +1,5 @@
-// Band path for token graphs with bf16 I/O: the weights are stored in a
-// decomposed layout that turns the local window into dense tensor-core tiles,
-// and each diffusion hop runs the window part on tcgen05 tensor cores.
-//
-// Layout of the weights A of one (batch, head) unit ("Diffuser: modelling long
-// sequences with multi-hop attention diffusion", sec 2.2 / 2.4: score once,
-// aggregate K times):
-//   band   [rows4][W]  row i, column w <-> key j = 4*floor(i/4) - r_up + w;
-//                      A_ij where |i-j| <= r, 0 <= j < n and i not global, else 0
-//   gcol   [n][g_pad]  slot s <-> key G[s], for the globals outside row i's window
-//   extra  [nx]        the random edges outside window and G, in CSR order
-//   grow   [g][n]      the full rows of the global tokens
+// Diffusion hops of the band path (token graphs, bf16 I/O), over the weight
+// layout described in band_common.cuh (unnormalized e_ij plus 1/l_i).
 // Row i's stored window starts on a multiple of 4 keys, so a 4-D TMA tensor
 // map whose third stride is 16*(W-1) bytes reads 128 consecutive rows of one
 // tile de-skewed: one box = 128 rows x 32 absolute keys.
@@ -18,10 +8,12 @@
 //   band:    tcgen05 MMA, M = 128 rows, N = 64 features, K = 32 keys per chunk,
 //            3xTF32 split (hi = operand as stored, which the tensor core
 //            truncates to tf32; lo = operand - trunc(operand)):
-//            A_hi*Z_hi + A_hi*Z_lo + A_lo*Z_hi, fp32 accumulation in TMEM.
-//   gcol, extras: warp-cooperative gathers of 256-byte Z_k rows, fp32 FMA.
+//            e_hi*Z_hi + e_hi*Z_lo + e_lo*Z_hi, fp32 accumulation in TMEM.
+//   gcol, extras: warp-cooperative gathers of 256-byte Z_k rows, fp32 FMA
+//            (hop_sparse_kernel, into a per-row partial).
 //   global rows:  every tile adds its keys' share; the last tile of a unit
 //            sums the shares (fixed order) and writes the global rows.
+//   epilogue: z_i = (1 - alpha) * inv_l_i * (band_i + partial_i) + alpha * V_i.
 // Z_k lives in three fp32 planes: row-major (for gathers) and transposed
 // raw/lo planes (the K-major B operand of the MMA).
 #include <cuda.h>
@@ -32,13 +24,17 @@
 #include <cstdint>
 #include <mutex>
 
+#include "band_common.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
 namespace dfs {
 namespace {
 
-constexpr int kTileRows = 128;
+using band::bf16hi;
+using band::bf16lo;
+using band::kTileRows;
+using band::tf32_trunc;
 constexpr int kChunkKeys = 32;
 // One CTA per SM: with two co-resident CTAs of this kernel, stale shared-memory
 // tiles were observed in the first chunk of some tiles, so the kernel claims a
@@ -57,11 +53,6 @@ constexpr int kSmemBytes = 1024 + kAStages * kAStageBytes + kZStages * 2 * kZPla
 static_assert(kSmemBytes > 116 * 1024, "must exclude a second CTA per SM");
 static_assert(64 + 64 * kTStages <= kTmemCols, "TMEM columns");
 
-__device__ __forceinline__ float tf32_trunc(float x) {
-    return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-}
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 struct HopArgs {
     BandPlan plan;
@@ -74,7 +65,9 @@ struct HopArgs {
     int64_t nx;
     const float* A_gc;
     const float* A_x;
-    const float* A_gr;
+    const float* A_gr;    // raw global-row scores
+    const float* gstat;   // [units][g][2]: (max, 1/sum) of the global rows
+    const float* inv_l;   // [units][n]
     const void* Zr_in;    // hop 0: V (bf16); otherwise fp32 row-major Z_k
     const __nv_bfloat16* V;
     float* Zr_out;
@@ -258,7 +251,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int t = q * 32 + lane;
         const int64_t i = i0 + t;
         const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
-        const float keep = 1.f - a.alpha;
+        const float keep = (1.f - a.alpha) * (row_ok ? __ldg(a.inv_l + (size_t)u * P.n + i) : 0.f);
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
@@ -344,11 +337,13 @@ hop_sparse_kernel(HopArgs a) {
         }
         for (int s = 0; s < g; ++s) {
             const float* wrow = a.A_gr + ((size_t)u * g + s) * P.n;
+            const float gm = __ldg(a.gstat + ((size_t)u * g + s) * 2);
+            const float ginv = __ldg(a.gstat + ((size_t)u * g + s) * 2 + 1);
             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int64_t j = i0 + 16 * warp + jj;
-                const float w = j < P.n ? __ldg(wrow + j) : 0.f;
+                const float w = j < P.n ? expf(__ldg(wrow + j) - gm) * ginv : 0.f;
                 acc.x = fmaf(w, z[jj].x, acc.x);
                 acc.y = fmaf(w, z[jj].y, acc.y);
             }
@@ -443,136 +438,6 @@ hop_sparse_kernel(HopArgs a) {
     }
 }
 
-// ---------------------------------------------------------------- scores (SIMT)
-// One warp per (unit, row): scores of the row's allowed keys, masked softmax,
-// weights written into the decomposed layout.  ("Diffuser...", eq S.1-S.5.)
-struct ScoreArgs {
-    BandPlan plan;
-    int64_t units;
-    const uint8_t* is_global;
-    const int32_t* gslot;
-    const int32_t* globals;
-    const int64_t* x_ptr;
-    const int32_t* x_col;
-    int64_t nx;
-    float* A_band;
-    float* A_gc;
-    float* A_x;
-    float* A_gr;
-};
-
-__device__ __forceinline__ void load_q64(const __nv_bfloat16* p, float (&x)[64]) {
-    const uint4* v = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 w = __ldg(v + c);
-        x[8 * c + 0] = bf16lo(w.x); x[8 * c + 1] = bf16hi(w.x);
-        x[8 * c + 2] = bf16lo(w.y); x[8 * c + 3] = bf16hi(w.y);
-        x[8 * c + 4] = bf16lo(w.z); x[8 * c + 5] = bf16hi(w.z);
-        x[8 * c + 6] = bf16lo(w.w); x[8 * c + 7] = bf16hi(w.w);
-    }
-}
-
-__device__ __forceinline__ float dot64(const float (&q)[64], const __nv_bfloat16* kp) {
-    const uint4* v = reinterpret_cast<const uint4*>(kp);
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 w = __ldg(v + c);
-        acc = fmaf(q[8 * c + 0], bf16lo(w.x), acc); acc = fmaf(q[8 * c + 1], bf16hi(w.x), acc);
-        acc = fmaf(q[8 * c + 2], bf16lo(w.y), acc); acc = fmaf(q[8 * c + 3], bf16hi(w.y), acc);
-        acc = fmaf(q[8 * c + 4], bf16lo(w.z), acc); acc = fmaf(q[8 * c + 5], bf16hi(w.z), acc);
-        acc = fmaf(q[8 * c + 6], bf16lo(w.w), acc); acc = fmaf(q[8 * c + 7], bf16hi(w.w), acc);
-    }
-    return acc;
-}
-
-__device__ __forceinline__ void online(float s, float& m, float& l) {
-    if (s > m) { l = l * expf(m - s) + 1.f; m = s; }
-    else       { l += expf(s - m); }
-}
-
-__device__ __forceinline__ void warp_merge(float& m, float& l) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-        const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
-        const float mm = fmaxf(m, m2);
-        const float a1 = (m == -INFINITY) ? 0.f : l * expf(m - mm);
-        const float a2 = (m2 == -INFINITY) ? 0.f : l2 * expf(m2 - mm);
-        m = mm;
-        l = a1 + a2;
-    }
-}
-
-__global__ void __launch_bounds__(256)
-score_band_simt_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
-                       const __nv_bfloat16* __restrict__ K) {
-    const BandPlan& P = a.plan;
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (gw >= a.units * P.n) return;
-    const int64_t u = gw / P.n, i = gw - u * P.n;
-    const __nv_bfloat16* Ku = K + (size_t)u * P.n * kHeadDim;
-    float q[64];
-    load_q64(Q + ((size_t)u * P.n + i) * kHeadDim, q);
-    const float scale = 0.125f;
-    float* Ab = a.A_band + (size_t)u * (P.band_unit / 4) + (size_t)i * P.W;
-    float* Agc = a.A_gc + ((size_t)u * P.n + i) * P.g_pad;
-    float m = -INFINITY, l = 0.f;
-    if (a.is_global[i]) {
-        float* Ag = a.A_gr + ((size_t)u * P.g + a.gslot[i]) * P.n;
-        for (int64_t j = lane; j < P.n; j += 32) {
-            const float s = dot64(q, Ku + (size_t)j * kHeadDim) * scale;
-            Ag[j] = s;
-            online(s, m, l);
-        }
-        warp_merge(m, l);
-        for (int64_t j = lane; j < P.n; j += 32) Ag[j] = expf(Ag[j] - m) / l;
-        for (int w = lane; w < P.W; w += 32) Ab[w] = 0.f;
-        for (int s = lane; s < P.g_pad; s += 32) Agc[s] = 0.f;
-        return;
-    }
-    const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
-    const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
-    const int64_t ws = 4 * (i / 4) - P.r_up;
-    float* Ax = a.A_x + (size_t)u * a.nx;
-    const int64_t e0 = a.x_ptr[i], e1 = a.x_ptr[i + 1];
-    for (int w = lane; w < P.W; w += 32) {
-        const int64_t j = ws + w;
-        if (j >= lo && j <= hi) {
-            const float s = dot64(q, Ku + (size_t)j * kHeadDim) * scale;
-            Ab[w] = s;
-            online(s, m, l);
-        }
-    }
-    for (int s = lane; s < P.g; s += 32) {
-        const int64_t j = a.globals[s];
-        if (j < lo || j > hi) {
-            const float sc = dot64(q, Ku + (size_t)j * kHeadDim) * scale;
-            Agc[s] = sc;
-            online(sc, m, l);
-        }
-    }
-    for (int64_t e = e0 + lane; e < e1; e += 32) {
-        const float s = dot64(q, Ku + (size_t)a.x_col[e] * kHeadDim) * scale;
-        Ax[e] = s;
-        online(s, m, l);
-    }
-    warp_merge(m, l);
-    const float inv = 1.f / l;
-    for (int w = lane; w < P.W; w += 32) {
-        const int64_t j = ws + w;
-        Ab[w] = (j >= lo && j <= hi) ? expf(Ab[w] - m) * inv : 0.f;
-    }
-    for (int s = lane; s < P.g_pad; s += 32) {
-        bool edge = false;
-        if (s < P.g) { const int64_t j = a.globals[s]; edge = j < lo || j > hi; }
-        Agc[s] = edge ? expf(Agc[s] - m) * inv : 0.f;
-    }
-    for (int64_t e = e0 + lane; e < e1; e += 32) Ax[e] = expf(Ax[e] - m) * inv;
-}
-
 // V [units][n][64] bf16 -> transposed fp32 plane [units][64][nz] (Z_0 for the MMA)
 __global__ void __launch_bounds__(256)
 v_to_zt_kernel(const __nv_bfloat16* __restrict__ V, float* __restrict__ Zt, int64_t n, int64_t nz,
@@ -597,64 +462,9 @@ v_to_zt_kernel(const __nv_bfloat16* __restrict__ V, float* __restrict__ Zt, int6
     }
 }
 
-// Decomposed weights -> CSR edge order (test export of the attention weights).
-__global__ void __launch_bounds__(256)
-band_to_csr_kernel(ScoreArgs a, const int64_t* __restrict__ row_ptr,
-                   const int32_t* __restrict__ col, int64_t nnz, float* __restrict__ out) {
-    const BandPlan& P = a.plan;
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (gw >= a.units * P.n) return;
-    const int64_t u = gw / P.n, i = gw - u * P.n;
-    const int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
-    float* o = out + (size_t)u * nnz;
-    if (a.is_global[i]) {
-        const float* Ag = a.A_gr + ((size_t)u * P.g + a.gslot[i]) * P.n;
-        for (int64_t e = e0 + lane; e < e1; e += 32) o[e] = Ag[col[e]];
-        return;
-    }
-    const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
-    const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
-    const int64_t ws = 4 * (i / 4) - P.r_up;
-    const float* Ab = a.A_band + (size_t)u * (P.band_unit / 4) + (size_t)i * P.W;
-    const float* Agc = a.A_gc + ((size_t)u * P.n + i) * P.g_pad;
-    const float* Ax = a.A_x + (size_t)u * a.nx;
-    int64_t xb = a.x_ptr[i];
-    // extras are the row's edges that are neither window nor global, in order
-    for (int64_t base = e0; base < e1; base += 32) {
-        const int64_t e = base + lane;
-        int64_t j = e < e1 ? col[e] : -1;
-        const bool is_x = e < e1 && (j < lo || j > hi) && !a.is_global[j < 0 ? 0 : j];
-        const unsigned mask = __ballot_sync(0xffffffffu, is_x);
-        const int rank = __popc(mask & ((1u << lane) - 1));
-        if (e < e1) {
-            float v;
-            if (j >= lo && j <= hi) v = Ab[j - ws];
-            else if (a.is_global[j]) v = Agc[a.gslot[j]];
-            else v = Ax[xb + rank];
-            o[e] = v;
-        }
-        xb += __popc(mask);
-    }
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 int encode(CUtensorMap* m, int rank, void* base, const cuuint64_t* dims, const cuuint64_t* strides,
            const cuuint32_t* box) {
-    auto fn = encode_fn();
+    auto fn = band::tensor_map_encoder();
     if (!fn) return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, base, dims, strides, box, es,
@@ -699,6 +509,39 @@ int launch_hop(const CUtensorMap& tmA, const CUtensorMap& tmZt, const CUtensorMa
 
 }  // namespace
 
+namespace band {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+}  // namespace band
+
+band::GraphRefs band_graph_refs(const diffuser_graph* g) {
+    return band::GraphRefs{g->d_is_global, g->d_gslot, g->d_globals, g->d_x_ptr, g->d_x_col, g->nx};
+}
+
+band::Weights band_weights(char* ws, const BandLayout& L) {
+    band::Weights w;
+    w.A_band = reinterpret_cast<float*>(ws + L.a_band);
+    w.A_gc = reinterpret_cast<float*>(ws + L.a_gc);
+    w.A_x = reinterpret_cast<float*>(ws + L.a_x);
+    w.A_gr = reinterpret_cast<float*>(ws + L.a_gr);
+    w.inv_l = reinterpret_cast<float*>(ws + L.inv_l);
+    w.m_sparse = reinterpret_cast<float*>(ws + L.m_sparse);
+    w.gstat = reinterpret_cast<float*>(ws + L.gstat);
+    w.sstat = reinterpret_cast<float*>(ws + L.sstat);
+    return w;
+}
+
 bool band_plan(const diffuser_graph* g, BandPlan* p) {
     if (g->kind != kTokenGraph || g->r < 8 || g->n_globals > kBandMaxGlobals) return false;
     p->n = g->n;
@@ -733,54 +576,13 @@ int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     }
     L->gpart = take(U * (size_t)p.tiles * (p.g > 0 ? p.g : 1) * kHeadDim * 4);
     L->psum = take(U * (size_t)p.n * kHeadDim * 4);
+    L->inv_l = take(U * (size_t)p.n * 4);
+    L->m_sparse = take(U * (size_t)p.n * 4);
+    L->gstat = take(U * (size_t)(p.g > 0 ? p.g : 1) * 2 * 4);
+    L->sstat = take(U * (size_t)p.tiles * (p.g > 0 ? p.g : 1) * 2 * 4);
     L->counters = take(U * 4);
     L->total = off;
     return DIFFUSER_OK;
-}
-
-namespace {
-ScoreArgs score_args(const diffuser_graph* g, const BandPlan& p, int64_t units, char* ws,
-                     const BandLayout& L) {
-    ScoreArgs s;
-    s.plan = p;
-    s.units = units;
-    s.is_global = g->d_is_global;
-    s.gslot = g->d_gslot;
-    s.globals = g->d_globals;
-    s.x_ptr = g->d_x_ptr;
-    s.x_col = g->d_x_col;
-    s.nx = g->nx;
-    s.A_band = reinterpret_cast<float*>(ws + L.a_band);
-    s.A_gc = reinterpret_cast<float*>(ws + L.a_gc);
-    s.A_x = reinterpret_cast<float*>(ws + L.a_x);
-    s.A_gr = reinterpret_cast<float*>(ws + L.a_gr);
-    return s;
-}
-}  // namespace
-
-int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
-                       const void* K, char* ws, const BandLayout& L, cudaStream_t stream) {
-    ScoreArgs s = score_args(g, p, units, ws, L);
-    const unsigned grid = (unsigned)((units * p.n + 7) / 8);
-    {
-        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
-        score_band_simt_kernel<<<grid, 256, 0, stream>>>(
-            s, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K));
-    }
-    cudaError_t err = cudaGetLastError();
-    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "score_band_simt_kernel");
-}
-
-int launch_band_to_csr(const diffuser_graph* g, const BandPlan& p, int64_t units, char* ws,
-                       const BandLayout& L, float* A_out, cudaStream_t stream) {
-    ScoreArgs s = score_args(g, p, units, ws, L);
-    const unsigned grid = (unsigned)((units * p.n + 7) / 8);
-    {
-        LaunchScope scope(DIFFUSER_KERNEL_AUX, stream);
-        band_to_csr_kernel<<<grid, 256, 0, stream>>>(s, g->d_row_ptr, g->d_col, g->nnz, A_out);
-    }
-    cudaError_t err = cudaGetLastError();
-    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "band_to_csr_kernel");
 }
 
 int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* V,
@@ -830,6 +632,8 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     a.A_gc = reinterpret_cast<const float*>(ws + L.a_gc);
     a.A_x = reinterpret_cast<const float*>(ws + L.a_x);
     a.A_gr = reinterpret_cast<const float*>(ws + L.a_gr);
+    a.gstat = reinterpret_cast<const float*>(ws + L.gstat);
+    a.inv_l = reinterpret_cast<const float*>(ws + L.inv_l);
     a.V = static_cast<const __nv_bfloat16*>(V);
     a.gpart = reinterpret_cast<float*>(ws + L.gpart);
     a.counters = reinterpret_cast<int*>(ws + L.counters);

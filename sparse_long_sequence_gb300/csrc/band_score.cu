@@ -1,0 +1,476 @@
+// Scores and masked softmax for the band path ("Diffuser: modelling long
+// sequences with multi-hop attention diffusion", eq S.1-S.5; "1.2.1 Static
+// sparsity", eq 1-3), in two kernels:
+//
+//  * score_sparse_kernel (SIMT): per row, the raw scores q_i.k_j/8 of the
+//    globals outside the window and of the random extras (one lane per key,
+//    the 128-byte k_j row read whole), and their maximum; per tile, the raw
+//    scores of the global rows against the tile's keys with per-tile
+//    (max, sum of exp); the last tile of a unit merges those into the global
+//    rows' (max, 1/sum).
+//  * score_band_tc_kernel (tcgen05): S = Q K^T for a 128-row tile against
+//    64-key chunks of its window on bf16 tensor cores (fp32 accumulation in
+//    TMEM), in two passes over the chunks: the row maximum, then
+//    e = exp(s - m) written into the band storage with the row sum; the row
+//    threads then turn the row's sparse raw scores into e and store
+//    inv_l = 1 / (band sum + sparse sum).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "band_common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace dfs {
+namespace {
+
+using band::bf16hi;
+using band::bf16lo;
+using band::kTileRows;
+
+constexpr float kScale = 0.125f;   // 1/sqrt(64), exact
+
+struct ScoreArgs {
+    BandPlan plan;
+    int64_t units;
+    band::GraphRefs gr;
+    band::Weights w;
+    int* counters;      // [units] tile tickets
+};
+
+__device__ __forceinline__ void load_row64(const __nv_bfloat16* p, float (&x)[64]) {
+    const uint4* v = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 w = __ldg(v + c);
+        x[8 * c + 0] = bf16lo(w.x); x[8 * c + 1] = bf16hi(w.x);
+        x[8 * c + 2] = bf16lo(w.y); x[8 * c + 3] = bf16hi(w.y);
+        x[8 * c + 4] = bf16lo(w.z); x[8 * c + 5] = bf16hi(w.z);
+        x[8 * c + 6] = bf16lo(w.w); x[8 * c + 7] = bf16hi(w.w);
+    }
+}
+
+__device__ __forceinline__ float dot64(const float (&q)[64], const __nv_bfloat16* kp) {
+    const uint4* v = reinterpret_cast<const uint4*>(kp);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 w = __ldg(v + c);
+        acc = fmaf(q[8 * c + 0], bf16lo(w.x), acc); acc = fmaf(q[8 * c + 1], bf16hi(w.x), acc);
+        acc = fmaf(q[8 * c + 2], bf16lo(w.y), acc); acc = fmaf(q[8 * c + 3], bf16hi(w.y), acc);
+        acc = fmaf(q[8 * c + 4], bf16lo(w.z), acc); acc = fmaf(q[8 * c + 5], bf16hi(w.z), acc);
+        acc = fmaf(q[8 * c + 6], bf16lo(w.w), acc); acc = fmaf(q[8 * c + 7], bf16hi(w.w), acc);
+    }
+    return acc;
+}
+
+// ---------------------------------------------------------------- sparse scores
+constexpr int kSparseThreads = 256;
+
+__global__ void __launch_bounds__(kSparseThreads)
+score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
+                    const __nv_bfloat16* __restrict__ K) {
+    extern __shared__ float sm[];            // [g][65] global-row scores of this tile's keys
+    __shared__ int ticket;
+    const BandPlan& P = a.plan;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t u = blockIdx.x / P.tiles;
+    const int tile = (int)(blockIdx.x - u * P.tiles);
+    const int64_t i0 = (int64_t)tile * kTileRows;
+    const int g = P.g;
+    const __nv_bfloat16* Qu = Q + (size_t)u * P.n * kHeadDim;
+    const __nv_bfloat16* Ku = K + (size_t)u * P.n * kHeadDim;
+
+    if (g > 0) {
+        // (1) global rows x this tile's keys: thread t < 128 owns key j = i0 + t
+        float* scr = sm;                     // [g][kTileRows]
+        if (tid < kTileRows) {
+            const int64_t j = i0 + tid;
+            if (j < P.n) {
+                float k[64];
+                load_row64(Ku + (size_t)j * kHeadDim, k);
+                for (int s = 0; s < g; ++s) {
+                    const float sc = dot64(k, Qu + (size_t)a.gr.globals[s] * kHeadDim) * kScale;
+                    a.w.A_gr[((size_t)u * g + s) * P.n + j] = sc;
+                    scr[s * kTileRows + tid] = sc;
+                }
+            } else {
+                for (int s = 0; s < g; ++s) scr[s * kTileRows + tid] = -INFINITY;
+            }
+        }
+        __syncthreads();
+        // per-tile (max, sum of exp) of each global row: one warp per row slot
+        for (int s = warp; s < g; s += kSparseThreads / 32) {
+            float m = -INFINITY;
+            for (int t = lane; t < kTileRows; t += 32) m = fmaxf(m, scr[s * kTileRows + t]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            float l = 0.f;
+            for (int t = lane; t < kTileRows; t += 32) {
+                const float v = scr[s * kTileRows + t];
+                l += v == -INFINITY ? 0.f : expf(v - m);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (lane == 0) {
+                float* st = a.w.sstat + (((size_t)u * P.tiles + tile) * g + s) * 2;
+                st[0] = m;
+                st[1] = l;
+            }
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) ticket = atomicAdd(&a.counters[u], 1);
+        __syncthreads();
+        if (ticket == P.tiles - 1) {
+            __threadfence();
+            for (int s = tid; s < g; s += kSparseThreads) {
+                float M = -INFINITY;
+                for (int tt = 0; tt < P.tiles; ++tt)
+                    M = fmaxf(M, __ldcg(a.w.sstat + (((size_t)u * P.tiles + tt) * g + s) * 2));
+                float L = 0.f;
+                for (int tt = 0; tt < P.tiles; ++tt) {
+                    const float* st = a.w.sstat + (((size_t)u * P.tiles + tt) * g + s) * 2;
+                    const float mt = __ldcg(st);
+                    if (mt != -INFINITY) L += __ldcg(st + 1) * expf(mt - M);
+                }
+                a.w.gstat[((size_t)u * g + s) * 2] = M;
+                a.w.gstat[((size_t)u * g + s) * 2 + 1] = 1.f / L;
+            }
+            if (tid == 0) a.counters[u] = 0;
+        }
+    }
+    // (2) rows of this tile, 16 per warp: globals outside the window + extras
+    for (int rr = 0; rr < 16; ++rr) {
+        const int64_t i = i0 + 16 * warp + rr;
+        if (i >= P.n) break;
+        if (a.gr.is_global[i]) continue;
+        const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
+        const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+        float q[64];
+        load_row64(Qu + (size_t)i * kHeadDim, q);
+        const int64_t e0 = a.gr.x_ptr[i], e1 = a.gr.x_ptr[i + 1];
+        const int total = g + (int)(e1 - e0);
+        float* wg = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+        float* wx = a.w.A_x + (size_t)u * a.gr.nx;
+        float m = -INFINITY;
+        for (int k = lane; k < total; k += 32) {
+            if (k < g) {
+                const int64_t j = a.gr.globals[k];
+                float sc = 0.f;
+                if (j < lo || j > hi) {
+                    sc = dot64(q, Ku + (size_t)j * kHeadDim) * kScale;
+                    m = fmaxf(m, sc);
+                }
+                wg[k] = sc;
+            } else {
+                const int64_t e = e0 + (k - g);
+                const float sc = dot64(q, Ku + (size_t)a.gr.x_col[e] * kHeadDim) * kScale;
+                wx[e] = sc;
+                m = fmaxf(m, sc);
+            }
+        }
+        for (int s = g + lane; s < P.g_pad; s += 32) wg[s] = 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) a.w.m_sparse[(size_t)u * P.n + i] = m;
+    }
+}
+
+// ---------------------------------------------------------------- band scores (tcgen05)
+constexpr int kBThreads = 256;           // warp 0 TMA, warp 1 MMA, warps 4-7 rows
+constexpr int kSChunk = 64;              // keys per chunk (MMA N)
+constexpr int kKStages = 6;              // smem ring of K chunks (8 KB each)
+constexpr int kSBufs = 4;                // TMEM S buffers (64 columns each)
+constexpr int kBTmemCols = 256;
+constexpr int kQBytes = kTileRows * kHeadDim * 2;
+constexpr int kKBytes = kSChunk * kHeadDim * 2;
+// One CTA per SM (shared memory alone excludes a second one).
+constexpr int kBSmemBytes = 120 * 1024;
+static_assert(1024 + kQBytes + kKStages * kKBytes + 256 <= kBSmemBytes, "smem");
+
+__global__ void __launch_bounds__(kBThreads, 1)
+score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     ScoreArgs a, int* status) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sK = sQ + kQBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sK + kKStages * kKBytes);
+    uint64_t* full_Q = bars;
+    uint64_t* full_K = full_Q + 1;
+    uint64_t* empty_K = full_K + kKStages;
+    uint64_t* full_S = empty_K + kKStages;
+    uint64_t* empty_S = full_S + kSBufs;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_S + kSBufs);
+
+    const BandPlan& P = a.plan;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t u = blockIdx.x / P.tiles;
+    const int tile = (int)(blockIdx.x - u * P.tiles);
+    const int64_t i0 = (int64_t)tile * kTileRows;
+    const int64_t jb = i0 - P.r_up;                     // first key of chunk 0
+    const int nc = (124 + P.W + kSChunk - 1) / kSChunk;  // chunks covering every stored window
+    const int iters = 2 * nc;                            // pass 1 (max), pass 2 (exp + write)
+
+    if (warp == 1) ptx::tmem_alloc(tmem_slot, kBTmemCols);
+    if (tid == 0) {
+        ptx::mbar_init(full_Q, 1);
+        for (int s = 0; s < kKStages; ++s) { ptx::mbar_init(&full_K[s], 1); ptx::mbar_init(&empty_K[s], 1); }
+        for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], 128); }
+        ptx::fence_mbar_init();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(full_Q, kQBytes);
+            ptx::tma_load_3d(sQ, &tmQ, full_Q, 0, (int)i0, (int)u);
+            for (int it = 0; it < iters; ++it) {
+                const int c = it % nc, s = it % kKStages;
+                if (it >= kKStages) ptx::mbar_wait(&empty_K[s], ((it / kKStages) - 1) & 1, status);
+                ptx::mbar_arrive_expect_tx(&full_K[s], kKBytes);
+                ptx::tma_load_3d(sK + s * kKBytes, &tmK, &full_K[s], 0, (int)(jb + kSChunk * c), (int)u);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::mma_idesc(1, kSChunk);
+            ptx::mbar_wait(full_Q, 0, status);
+            const uint32_t qa = ptx::smem_u32(sQ);
+            for (int it = 0; it < iters; ++it) {
+                const int s = it % kKStages, b = it % kSBufs;
+                ptx::mbar_wait(&full_K[s], (it / kKStages) & 1, status);
+                if (it >= kSBufs) ptx::mbar_wait(&empty_S[b], ((it / kSBufs) - 1) & 1, status);
+                ptx::tc_fence_after();
+                const uint32_t kb = ptx::smem_u32(sK + s * kKBytes);
+#pragma unroll
+                for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                    ptx::mma_bf16_ss(tmem + kSChunk * b, ptx::sw128_kmajor_desc(qa + 32 * ks),
+                                     ptx::sw128_kmajor_desc(kb + 32 * ks), idesc, ks > 0);
+                ptx::mma_commit(&empty_K[s]);
+                ptx::mma_commit(&full_S[b]);
+            }
+            // drain the asynchronous commit arrivals before the CTA can exit
+            for (int s = 0; s < kKStages; ++s) {
+                const int uses = (iters - s + kKStages - 1) / kKStages;
+                if (uses > 0) ptx::mbar_wait(&empty_K[s], (uses - 1) & 1, status);
+            }
+        }
+    } else if (warp >= 4) {
+        const int q = warp - 4;
+        const int t = q * 32 + lane;
+        const int64_t i = i0 + t;
+        const bool row_ok = i < P.n && !a.gr.is_global[i < P.n ? i : 0];
+        const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
+        const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        float m = row_ok ? a.w.m_sparse[(size_t)u * P.n + i] : 0.f;
+        float lsum = 0.f;
+        float* brow = a.w.A_band + (size_t)u * (P.band_unit / 4) + (size_t)i * P.W;
+        const int wshift = 4 * (t / 4);                  // window start of row i minus jb
+        for (int it = 0; it < iters; ++it) {
+            const int b = it % kSBufs, c = it % nc;
+            const bool pass2 = it >= nc;
+            ptx::mbar_wait(&full_S[b], (it / kSBufs) & 1, status);
+            __syncwarp();
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                float s[32];
+                ptx::tmem_ld32(tmem + lane_base + kSChunk * b + 32 * half, s);
+                const int64_t j0 = jb + kSChunk * c + 32 * half;
+                if (!pass2) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int64_t j = j0 + k;
+                        if (row_ok && j >= lo && j <= hi) m = fmaxf(m, s[k] * kScale);
+                    }
+                } else if (row_ok) {
+                    const int w0 = kSChunk * c + 32 * half - wshift;   // multiple of 4
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4) {
+                        float e[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const int64_t j = j0 + 4 * k4 + x;
+                            e[x] = (j >= lo && j <= hi) ? expf(s[4 * k4 + x] * kScale - m) : 0.f;
+                            lsum += e[x];
+                        }
+                        const int w = w0 + 4 * k4;
+                        if (w >= 0 && w < P.W)
+                            *reinterpret_cast<float4*>(brow + w) = make_float4(e[0], e[1], e[2], e[3]);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&empty_S[b]);
+        }
+        // the row's sparse part: raw scores -> e, and the normalizer
+        if (row_ok) {
+            float* wg = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+            for (int s = 0; s < P.g; ++s) {
+                const int64_t j = a.gr.globals[s];
+                const float e = (j < lo || j > hi) ? expf(wg[s] - m) : 0.f;
+                wg[s] = e;
+                lsum += e;
+            }
+            float* wx = a.w.A_x + (size_t)u * a.gr.nx;
+            for (int64_t e = a.gr.x_ptr[i]; e < a.gr.x_ptr[i + 1]; ++e) {
+                const float v = expf(wx[e] - m);
+                wx[e] = v;
+                lsum += v;
+            }
+            a.w.inv_l[(size_t)u * P.n + i] = 1.f / lsum;
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) ptx::tmem_dealloc(tmem, kBTmemCols);
+}
+
+// ---------------------------------------------------------------- weights -> CSR order
+__global__ void __launch_bounds__(256)
+band_to_csr_kernel(ScoreArgs a, const int64_t* __restrict__ row_ptr,
+                   const int32_t* __restrict__ col, int64_t nnz, float* __restrict__ out) {
+    const BandPlan& P = a.plan;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= a.units * P.n) return;
+    const int64_t u = gw / P.n, i = gw - u * P.n;
+    const int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
+    float* o = out + (size_t)u * nnz;
+    if (a.gr.is_global[i]) {
+        const int s = a.gr.gslot[i];
+        const float* Ag = a.w.A_gr + ((size_t)u * P.g + s) * P.n;
+        const float m = a.w.gstat[((size_t)u * P.g + s) * 2];
+        const float inv = a.w.gstat[((size_t)u * P.g + s) * 2 + 1];
+        for (int64_t e = e0 + lane; e < e1; e += 32) o[e] = expf(Ag[col[e]] - m) * inv;
+        return;
+    }
+    const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
+    const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+    const int64_t ws = 4 * (i / 4) - P.r_up;
+    const float inv = a.w.inv_l[(size_t)u * P.n + i];
+    const float* Ab = a.w.A_band + (size_t)u * (P.band_unit / 4) + (size_t)i * P.W;
+    const float* Agc = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+    const float* Ax = a.w.A_x + (size_t)u * a.gr.nx;
+    int64_t xb = a.gr.x_ptr[i];
+    // extras are the row's edges that are neither window nor global, in order
+    for (int64_t base = e0; base < e1; base += 32) {
+        const int64_t e = base + lane;
+        const int64_t j = e < e1 ? col[e] : -1;
+        const bool is_x = e < e1 && (j < lo || j > hi) && !a.gr.is_global[j < 0 ? 0 : j];
+        const unsigned mask = __ballot_sync(0xffffffffu, is_x);
+        const int rank = __popc(mask & ((1u << lane) - 1));
+        if (e < e1) {
+            float v;
+            if (j >= lo && j <= hi) v = Ab[j - ws];
+            else if (a.gr.is_global[j]) v = Agc[a.gr.gslot[j]];
+            else v = Ax[xb + rank];
+            o[e] = v * inv;
+        }
+        xb += __popc(mask);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+ScoreArgs make_args(const diffuser_graph* g, const BandPlan& p, int64_t units, char* ws,
+                    const BandLayout& L) {
+    ScoreArgs s;
+    s.plan = p;
+    s.units = units;
+    s.gr = band_graph_refs(g);
+    s.w = band_weights(ws, L);
+    s.counters = reinterpret_cast<int*>(ws + L.counters);
+    return s;
+}
+
+}  // namespace
+
+int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
+                       const void* K, char* ws, const BandLayout& L, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(score_band_tc_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmemBytes);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(score_sparse_kernel,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kBandMaxGlobals * kTileRows * (int)sizeof(float));
+    });
+    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(scores)");
+    cudaError_t err = cudaMemsetAsync(ws + L.counters, 0, (size_t)units * 4, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "clearing the tile counters");
+    ScoreArgs a = make_args(g, p, units, ws, L);
+    const auto* Qb = static_cast<const __nv_bfloat16*>(Q);
+    const auto* Kb = static_cast<const __nv_bfloat16*>(K);
+    const unsigned grid = (unsigned)(units * p.tiles);
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
+        score_sparse_kernel<<<grid, kSparseThreads, (size_t)p.g * kTileRows * sizeof(float),
+                              stream>>>(a, Qb, Kb);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_sparse_kernel");
+
+    auto fn = encode_fn();
+    if (!fn) return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    CUtensorMap tmQ, tmK;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)p.n, (cuuint64_t)units};
+    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)p.n * kHeadDim * 2};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const cuuint32_t boxQ[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)kTileRows, 1};
+    const cuuint32_t boxK[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)kSChunk, 1};
+    CUresult r = fn(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(Q), dims, strides,
+                    boxQ, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS)
+        r = fn(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(K), dims, strides, boxK,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled (Q/K) failed: " + std::to_string((int)r));
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
+        score_band_tc_kernel<<<grid, kBThreads, kBSmemBytes, stream>>>(tmQ, tmK, a, g->d_status);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_band_tc_kernel");
+    return DIFFUSER_OK;
+}
+
+int launch_band_to_csr(const diffuser_graph* g, const BandPlan& p, int64_t units, char* ws,
+                       const BandLayout& L, float* A_out, cudaStream_t stream) {
+    ScoreArgs a = make_args(g, p, units, ws, L);
+    const unsigned grid = (unsigned)((units * p.n + 7) / 8);
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_AUX, stream);
+        band_to_csr_kernel<<<grid, 256, 0, stream>>>(a, g->d_row_ptr, g->d_col, g->nnz, A_out);
+    }
+    cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "band_to_csr_kernel");
+}
+
+}  // namespace dfs

@@ -38,7 +38,7 @@ struct BandPlan {
 struct BandLayout {
     size_t a_band, a_gc, a_x, a_gr;
     size_t zr[2], zt[2], ztl[2];
-    size_t gpart, psum, counters, total;
+    size_t gpart, psum, inv_l, m_sparse, gstat, sstat, counters, total;
 };
 
 }  // namespace dfs
