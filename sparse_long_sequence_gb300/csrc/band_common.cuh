@@ -11,8 +11,9 @@
 //   gcol   [n][g_pad]  slot s <-> key G[s]: e for globals outside row i's window, else 0
 //   extra  [nx]        e of the random edges outside window and G, CSR order
 //   inv_l  [n]         per-row normalizer of the rows not in G
-//   grow   [g][n]      raw scores s_ij of the global rows, with
-//   gstat  [g][2]      their (row max, 1 / row sum of exp(s - max))
+//   grow   [g][n]      the global rows' weights A_ij (raw scores until the
+//                      band score kernel normalizes them with
+//   gstat  [g][2]      their (row max, 1 / row sum of exp(s - max)))
 #pragma once
 
 #include <cuda.h>
@@ -40,7 +41,7 @@ struct Weights {
     float* A_band;     // units x band_unit bytes
     float* A_gc;       // [units][n][g_pad]
     float* A_x;        // [units][nx]
-    float* A_gr;       // [units][g][n] raw global-row scores
+    float* A_gr;       // [units][g][n] global-row weights (raw scores before normalization)
     float* inv_l;      // [units][n]
     float* m_sparse;   // [units][n] max raw score over a row's gcol + extras
     float* gstat;      // [units][g][2]

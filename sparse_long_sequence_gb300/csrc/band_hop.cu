@@ -65,8 +65,7 @@ struct HopArgs {
     int64_t nx;
     const float* A_gc;
     const float* A_x;
-    const float* A_gr;    // raw global-row scores
-    const float* gstat;   // [units][g][2]: (max, 1/sum) of the global rows
+    const float* A_gr;    // normalized global-row weights [units][g][n]
     const float* inv_l;   // [units][n]
     const void* Zr_in;    // hop 0: V (bf16); otherwise fp32 row-major Z_k
     const __nv_bfloat16* V;
@@ -80,17 +79,11 @@ struct HopArgs {
     float* Psum;          // [units][n][64]: gathered part of (A Z_k) per row
 };
 
-// Two features (2*lane, 2*lane+1) of row j of Z_k.
-template <bool kHop0>
-__device__ __forceinline__ float2 zpair(const HopArgs& a, int64_t u, int64_t j, int lane) {
-    const size_t off = ((size_t)u * a.plan.n + j) * kHeadDim + 2 * lane;
-    if constexpr (kHop0) {
-        uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(
-            static_cast<const __nv_bfloat16*>(a.Zr_in) + off));
-        return make_float2(bf16lo(w), bf16hi(w));
-    } else {
-        return __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(a.Zr_in) + off));
-    }
+__device__ __forceinline__ void fma4(float4& acc, float w, const float4& z) {
+    acc.x = fmaf(w, z.x, acc.x);
+    acc.y = fmaf(w, z.y, acc.y);
+    acc.z = fmaf(w, z.z, acc.z);
+    acc.w = fmaf(w, z.w, acc.w);
 }
 
 template <bool kHop0, bool kLast>
@@ -314,11 +307,34 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // Psum[u][i] (fp32), which the band kernel's epilogue adds.
 constexpr int kSparseThreads = 256;
 constexpr int kGatherBatch = 8;
+// rows whose gathers run in one warp-iteration: two (one per half-warp)
+
+// Row j of Z_k for unit u, 4 features per lane (hl = lane within a half-warp).
+template <bool kHop0>
+struct ZRows {
+    const void* base;     // Z_k of this unit, offset to this lane's 4 features
+    __device__ __forceinline__ ZRows(const HopArgs& a, int64_t u, int hl) {
+        if constexpr (kHop0)
+            base = static_cast<const __nv_bfloat16*>(a.Zr_in) + (size_t)u * a.plan.n * kHeadDim + 4 * hl;
+        else
+            base = static_cast<const float*>(a.Zr_in) + (size_t)u * a.plan.n * kHeadDim + 4 * hl;
+    }
+    __device__ __forceinline__ float4 operator()(int32_t j) const {
+        if constexpr (kHop0) {
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(
+                static_cast<const __nv_bfloat16*>(base) + ((uint32_t)j << 6)));
+            return make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
+        } else {
+            return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) +
+                                                         ((uint32_t)j << 6)));
+        }
+    }
+};
 
 template <bool kHop0, bool kLast>
-__global__ void __launch_bounds__(kSparseThreads)
+__global__ void __launch_bounds__(kSparseThreads, 4)
 hop_sparse_kernel(HopArgs a) {
-    extern __shared__ float red[];           // [8 warps][g][65]: per-warp global-row shares
+    extern __shared__ float red[];           // [8 warps][g][65] shares, then [g][64] Z rows of G
     __shared__ int ticket;
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -326,29 +342,36 @@ hop_sparse_kernel(HopArgs a) {
     const int tile = (int)(blockIdx.x - u * P.tiles);
     const int64_t i0 = (int64_t)tile * kTileRows;
     const int g = P.g;
+    const int half = lane >> 4, hl = lane & 15;
+    const unsigned hmask = 0xffffu << (16 * half);
+    const ZRows<kHop0> zrow(a, u, hl);
 
     if (g > 0) {
-        // (1) this warp's 16 keys j = i0 + 16 warp + jj
-        float2 z[16];
+        // (1) global rows: this warp's 16 keys j = i0 + 16 warp + jj; half-warp
+        //     `half` takes keys jj = half, half + 2, ..., 4 features per lane
+        const int64_t jbase = i0 + 16 * warp;
+        float4 z[8];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            const int64_t j = i0 + 16 * warp + jj;
-            z[jj] = j < P.n ? zpair<kHop0>(a, u, j, lane) : make_float2(0.f, 0.f);
+        for (int k = 0; k < 8; ++k) {
+            const int64_t j = jbase + 2 * k + half;
+            z[k] = j < P.n ? zrow((int32_t)j) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         for (int s = 0; s < g; ++s) {
-            const float* wrow = a.A_gr + ((size_t)u * g + s) * P.n;
-            const float gm = __ldg(a.gstat + ((size_t)u * g + s) * 2);
-            const float ginv = __ldg(a.gstat + ((size_t)u * g + s) * 2 + 1);
-            float2 acc = make_float2(0.f, 0.f);
+            // lanes 0..15 fetch the 16 normalized weights of this warp's keys
+            const int64_t jl = jbase + hl;
+            const float wv = jl < P.n ? __ldg(a.A_gr + ((size_t)u * g + s) * P.n + jl) : 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const int64_t j = i0 + 16 * warp + jj;
-                const float w = j < P.n ? expf(__ldg(wrow + j) - gm) * ginv : 0.f;
-                acc.x = fmaf(w, z[jj].x, acc.x);
-                acc.y = fmaf(w, z[jj].y, acc.y);
+            for (int k = 0; k < 8; ++k) fma4(acc, __shfl_sync(0xffffffffu, wv, 2 * k + half, 16), z[k]);
+            // combine the two half-warps (even / odd keys)
+            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 16);
+            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 16);
+            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 16);
+            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 16);
+            if (half == 0) {
+                float* r = red + (warp * g + s) * 65 + 4 * hl;
+                r[0] = acc.x; r[1] = acc.y; r[2] = acc.z; r[3] = acc.w;
             }
-            red[(warp * g + s) * 65 + 2 * lane] = acc.x;
-            red[(warp * g + s) * 65 + 2 * lane + 1] = acc.y;
         }
         __syncthreads();
         float* part = a.gpart + (((size_t)u * P.tiles + tile) * g) * kHeadDim;
@@ -385,56 +408,51 @@ hop_sparse_kernel(HopArgs a) {
             }
             if (tid == 0) a.counters[u] = 0;
         }
+        __syncthreads();
+        // stage the Z_k rows of the global keys for the out-of-window global columns
+        for (int e = tid; e < g * 16; e += kSparseThreads) {
+            const int s = e >> 4, q = e & 15;
+            const ZRows<kHop0> zq(a, u, q);
+            reinterpret_cast<float4*>(red)[e] = zq(a.globals[s]);
+        }
+        __syncthreads();
     }
-    // (2) rows of this block: 16 per warp
+    // (2) rows of this block: each half-warp owns a row (16 lanes x 4 features);
+    //     kGatherBatch gathers are issued before their FMAs.
     const float* ax = a.A_x + (size_t)u * a.nx;
-    for (int rr = 0; rr < 16; ++rr) {
-        const int64_t i = i0 + 16 * warp + rr;
-        if (i >= P.n) break;
-        if (a.is_global[i]) continue;
-        float2 acc = make_float2(0.f, 0.f);
+    const float4* zg = reinterpret_cast<const float4*>(red) + hl;     // Z rows of G, this lane
+    for (int rr = 0; rr < 16; rr += 2) {
+        const int64_t i = i0 + 16 * warp + rr + half;
+        const bool live = i < P.n && !a.is_global[i < P.n ? i : 0];
+        if (!live) continue;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         // globals outside the window (weight 0 marks "inside the window")
         const float* wg = a.A_gc + ((size_t)u * P.n + i) * P.g_pad;
-        for (int s0 = 0; s0 < g; s0 += kGatherBatch) {
-            float w[kGatherBatch];
-            float2 zz[kGatherBatch];
-#pragma unroll
-            for (int b = 0; b < kGatherBatch; ++b) {
-                w[b] = s0 + b < g ? __ldg(wg + s0 + b) : 0.f;
-                zz[b] = w[b] != 0.f ? zpair<kHop0>(a, u, a.globals[s0 + b], lane) : make_float2(0.f, 0.f);
-            }
-#pragma unroll
-            for (int b = 0; b < kGatherBatch; ++b) {
-                acc.x = fmaf(w[b], zz[b].x, acc.x);
-                acc.y = fmaf(w[b], zz[b].y, acc.y);
-            }
+        for (int s0 = 0; s0 < g; s0 += 16) {
+            const float wv = s0 + hl < g ? __ldg(wg + s0 + hl) : 0.f;
+            const int cnt = g - s0 < 16 ? g - s0 : 16;
+            for (int b = 0; b < cnt; ++b)
+                fma4(acc, __shfl_sync(hmask, wv, b, 16), zg[(s0 + b) * 16]);
         }
-        // random extras: lanes fetch (weight, column) 32 at a time, then batches of loads
+        // random extras: (weight, column) pairs fetched 16 at a time; padded
+        // slots carry weight 0 and column i, so every batch runs in full
         const int64_t e0 = a.x_ptr[i], e1 = a.x_ptr[i + 1];
-        for (int64_t base = e0; base < e1; base += 32) {
-            const int64_t e = base + lane;
+        for (int64_t base = e0; base < e1; base += 16) {
+            const int64_t e = base + hl;
             const float w_l = e < e1 ? __ldg(ax + e) : 0.f;
-            const int32_t j_l = e < e1 ? __ldg(a.x_col + e) : 0;
-            const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
+            const int32_t j_l = e < e1 ? __ldg(a.x_col + e) : (int32_t)i;
+            const int cnt = (e1 - base) < 16 ? (int)(e1 - base) : 16;
             for (int t0 = 0; t0 < cnt; t0 += kGatherBatch) {
-                float w[kGatherBatch];
-                float2 zz[kGatherBatch];
+                float4 zz[kGatherBatch];
 #pragma unroll
-                for (int b = 0; b < kGatherBatch; ++b) {
-                    const int src = t0 + b < cnt ? t0 + b : 0;
-                    w[b] = __shfl_sync(0xffffffffu, w_l, src);
-                    const int32_t j = __shfl_sync(0xffffffffu, j_l, src);
-                    if (t0 + b >= cnt) w[b] = 0.f;
-                    zz[b] = zpair<kHop0>(a, u, j, lane);
-                }
+                for (int b = 0; b < kGatherBatch; ++b)
+                    zz[b] = zrow(__shfl_sync(hmask, j_l, t0 + b, 16));
 #pragma unroll
-                for (int b = 0; b < kGatherBatch; ++b) {
-                    acc.x = fmaf(w[b], zz[b].x, acc.x);
-                    acc.y = fmaf(w[b], zz[b].y, acc.y);
-                }
+                for (int b = 0; b < kGatherBatch; ++b)
+                    fma4(acc, __shfl_sync(hmask, w_l, t0 + b, 16), zz[b]);
             }
         }
-        reinterpret_cast<float2*>(a.Psum + ((size_t)u * P.n + i) * kHeadDim)[lane] = acc;
+        reinterpret_cast<float4*>(a.Psum + ((size_t)u * P.n + i) * kHeadDim)[hl] = acc;
     }
 }
 
@@ -632,7 +650,6 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     a.A_gc = reinterpret_cast<const float*>(ws + L.a_gc);
     a.A_x = reinterpret_cast<const float*>(ws + L.a_x);
     a.A_gr = reinterpret_cast<const float*>(ws + L.a_gr);
-    a.gstat = reinterpret_cast<const float*>(ws + L.gstat);
     a.inv_l = reinterpret_cast<const float*>(ws + L.inv_l);
     a.V = static_cast<const __nv_bfloat16*>(V);
     a.gpart = reinterpret_cast<float*>(ws + L.gpart);

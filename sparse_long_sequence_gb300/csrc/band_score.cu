@@ -266,6 +266,18 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (uses > 0) ptx::mbar_wait(&empty_K[s], (uses - 1) & 1, status);
             }
         }
+    } else if (warp == 2 || warp == 3) {
+        // normalize the global rows' weights over this tile's keys:
+        // A_gr = exp(s - max) / sum, with (max, 1/sum) from score_sparse_kernel
+        const int64_t tkeys = P.n - i0 < kTileRows ? P.n - i0 : kTileRows;
+        for (int e = tid - 64; e < P.g * kTileRows; e += 64) {
+            const int sl = e / kTileRows, jj = e % kTileRows;
+            if (jj >= tkeys) continue;
+            const float gm = a.w.gstat[((size_t)u * P.g + sl) * 2];
+            const float ginv = a.w.gstat[((size_t)u * P.g + sl) * 2 + 1];
+            float* v = a.w.A_gr + ((size_t)u * P.g + sl) * P.n + i0 + jj;
+            *v = expf(*v - gm) * ginv;
+        }
     } else if (warp >= 4) {
         const int q = warp - 4;
         const int t = q * 32 + lane;
@@ -352,9 +364,7 @@ band_to_csr_kernel(ScoreArgs a, const int64_t* __restrict__ row_ptr,
     if (a.gr.is_global[i]) {
         const int s = a.gr.gslot[i];
         const float* Ag = a.w.A_gr + ((size_t)u * P.g + s) * P.n;
-        const float m = a.w.gstat[((size_t)u * P.g + s) * 2];
-        const float inv = a.w.gstat[((size_t)u * P.g + s) * 2 + 1];
-        for (int64_t e = e0 + lane; e < e1; e += 32) o[e] = expf(Ag[col[e]] - m) * inv;
+        for (int64_t e = e0 + lane; e < e1; e += 32) o[e] = Ag[col[e]];
         return;
     }
     const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
