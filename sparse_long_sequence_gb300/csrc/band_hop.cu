@@ -1,8 +1,9 @@
 // Diffusion hops of the band path (token graphs, bf16 I/O), over the weight
 // layout described in band_common.cuh (unnormalized e_ij plus 1/l_i).
-// Row i's stored window starts on a multiple of 4 keys, so a 4-D TMA tensor
-// map whose third stride is 16*(W-1) bytes reads 128 consecutive rows of one
-// tile de-skewed: one box = 128 rows x 32 absolute keys.
+// Row i's stored window starts on a multiple of 4 keys, so the 32 keys of a
+// chunk are eight 16-byte pieces of the row's storage: each row thread
+// streams its own pieces with cp.async (de-skewing for free) and no two
+// threads share a shared-memory slot.
 //
 // Hop Z_{k+1} = (1-alpha) A Z_k + alpha V ("Diffuser...", sec 2.4 eq S.7):
 //   band:    tcgen05 MMA, M = 128 rows, N = 64 features, K = 32 keys per chunk,
@@ -41,9 +42,10 @@ constexpr int kChunkKeys = 32;
 // whole SM (its shared memory alone rules out a second CTA) and uses the room
 // for deeper pipelines.
 constexpr int kThreads = 320;            // 10 warps
-constexpr int kAStages = 4;              // smem stages of A (16 KB each)
+constexpr int kAStages = 6;              // per-thread cp.async ring of A chunks (16 KB per stage)
 constexpr int kZStages = 4;              // smem stages of Z^T hi+lo (16 KB each)
-constexpr int kTStages = 7;              // TMEM stages of A hi+lo (64 columns each)
+constexpr int kAccCols = 128;            // two 64-column accumulators (double-buffered tiles)
+constexpr int kTStages = 6;              // TMEM stages of A hi+lo (64 columns each)
 constexpr int kTmemCols = 512;
 constexpr int kPStride = 68;             // floats per row of the gather partial buffer
 constexpr int kAStageBytes = kTileRows * kChunkKeys * 4;
@@ -51,7 +53,7 @@ constexpr int kZPlaneBytes = kHeadDim * kChunkKeys * 4;
 constexpr int kSmemBytes = 1024 + kAStages * kAStageBytes + kZStages * 2 * kZPlaneBytes +
                            kTileRows * kPStride * 4 + 256;
 static_assert(kSmemBytes > 116 * 1024, "must exclude a second CTA per SM");
-static_assert(64 + 64 * kTStages <= kTmemCols, "TMEM columns");
+static_assert(kAccCols + 64 * kTStages <= kTmemCols, "TMEM columns");
 
 
 struct HopArgs {
@@ -77,6 +79,7 @@ struct HopArgs {
     int* counters;        // [units]
     int* status;
     float* Psum;          // [units][n][64]: gathered part of (A Z_k) per row
+    const float* A_band;  // band weights, units x band_unit bytes
 };
 
 __device__ __forceinline__ void fma4(float4& acc, float w, const float4& z) {
@@ -88,8 +91,8 @@ __device__ __forceinline__ void fma4(float4& acc, float w, const float4& z) {
 
 template <bool kHop0, bool kLast>
 __global__ void __launch_bounds__(kThreads, 1)
-hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmZt,
-                const __grid_constant__ CUtensorMap tmZl, HopArgs a) {
+hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant__ CUtensorMap tmZl,
+                HopArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -97,33 +100,30 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint8_t* sZ = sA + kAStages * kAStageBytes;                  // kZStages x (hi 8 KB, lo 8 KB)
     float* sP = reinterpret_cast<float*>(sZ + kZStages * 2 * kZPlaneBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTileRows * kPStride);
-    uint64_t* full_sA = bars;
-    uint64_t* empty_sA = full_sA + kAStages;
-    uint64_t* full_tA = empty_sA + kAStages;
+    uint64_t* full_tA = bars;
     uint64_t* empty_tA = full_tA + kTStages;
     uint64_t* full_Z = empty_tA + kTStages;
     uint64_t* empty_Z = full_Z + kZStages;
-    uint64_t* acc_full = empty_Z + kZStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    uint64_t* acc_full = empty_Z + kZStages;                     // [2]
+    uint64_t* acc_empty = acc_full + 2;                          // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t u = blockIdx.x / P.tiles;
-    const int tile = (int)(blockIdx.x - u * P.tiles);
-    const int64_t i0 = (int64_t)tile * kTileRows;
-    const int64_t jb = i0 - P.r_up;          // absolute key of chunk 0, column 0
     const int chunks = P.chunks;
+    const int64_t total_tiles = a.units * P.tiles;
+    // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int my_tiles = blockIdx.x < total_tiles
+        ? (int)((total_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
 
     if (warp == 9) ptx::tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
-        for (int s = 0; s < kAStages; ++s) { ptx::mbar_init(&full_sA[s], 1); ptx::mbar_init(&empty_sA[s], 128); }
         for (int s = 0; s < kTStages; ++s) { ptx::mbar_init(&full_tA[s], 128); ptx::mbar_init(&empty_tA[s], 1); }
         for (int s = 0; s < kZStages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
-        ptx::mbar_init(acc_full, 1);
+        for (int s = 0; s < 2; ++s) { ptx::mbar_init(&acc_full[s], 1); ptx::mbar_init(&acc_empty[s], 128); }
         ptx::fence_mbar_init();
     }
     if (warp == 8 && lane == 0) {
-        ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmZt);
         if (!kHop0) ptx::prefetch_tensormap(&tmZl);
     }
@@ -135,161 +135,217 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (warp == 8) {
         // ---------------- TMA producer
         if (lane == 0) {
-            for (int c = 0; c < chunks; ++c) {
-                const int sa = c % kAStages;
-                if (c >= kAStages) ptx::mbar_wait(&empty_sA[sa], ((c / kAStages) - 1) & 1, a.status);
-                ptx::mbar_arrive_expect_tx(&full_sA[sa], kAStageBytes);
-                ptx::tma_load_4d(sA + sa * kAStageBytes, &tmA, &full_sA[sa],
-                                 (int)(i0 + kChunkKeys * c), 0, (int)(i0 / 4), (int)u);
-                const int sz = c % kZStages;
-                if (c >= kZStages) ptx::mbar_wait(&empty_Z[sz], ((c / kZStages) - 1) & 1, a.status);
-                uint8_t* zdst = sZ + sz * 2 * kZPlaneBytes;
-                ptx::mbar_arrive_expect_tx(&full_Z[sz], kHop0 ? kZPlaneBytes : 2 * kZPlaneBytes);
-                const int key = (int)(jb + kChunkKeys * c);
-                ptx::tma_load_3d(zdst, &tmZt, &full_Z[sz], key, 0, (int)u);
-                if (!kHop0) ptx::tma_load_3d(zdst + kZPlaneBytes, &tmZl, &full_Z[sz], key, 0, (int)u);
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+                const int64_t u = tix / P.tiles;
+                const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+                const int64_t jb = i0 - P.r_up;
+                for (int c = 0; c < chunks; ++c) {
+                    const int gc = lt * chunks + c;
+                    const int sz = gc % kZStages;
+                    if (gc >= kZStages) ptx::mbar_wait(&empty_Z[sz], ((gc / kZStages) - 1) & 1, a.status);
+                    uint8_t* zdst = sZ + sz * 2 * kZPlaneBytes;
+                    ptx::mbar_arrive_expect_tx(&full_Z[sz], kHop0 ? kZPlaneBytes : 2 * kZPlaneBytes);
+                    const int key = (int)(jb + kChunkKeys * c);
+                    ptx::tma_load_3d(zdst, &tmZt, &full_Z[sz], key, 0, (int)u);
+                    if (!kHop0) ptx::tma_load_3d(zdst + kZPlaneBytes, &tmZl, &full_Z[sz], key, 0, (int)u);
+                }
             }
         }
     } else if (warp == 9) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer: accumulator lt & 1 of TMEM columns [64 (lt & 1), +64)
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::mma_idesc(2, kHeadDim);
-            for (int c = 0; c < chunks; ++c) {
-                const int ta = c % kTStages, sz = c % kZStages;
-                ptx::mbar_wait(&full_tA[ta], (c / kTStages) & 1, a.status);
-                ptx::mbar_wait(&full_Z[sz], (c / kZStages) & 1, a.status);
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const int ab = lt & 1;
+                if (lt >= 2) ptx::mbar_wait(&acc_empty[ab], ((lt / 2) - 1) & 1, a.status);
                 ptx::tc_fence_after();
-                const uint32_t zhi = ptx::smem_u32(sZ + sz * 2 * kZPlaneBytes);
-                const uint32_t zlo = zhi + kZPlaneBytes;
+                const uint32_t dacc = tmem + 64 * ab;
+                for (int c = 0; c < chunks; ++c) {
+                    const int gc = lt * chunks + c;
+                    const int ta = gc % kTStages, sz = gc % kZStages;
+                    ptx::mbar_wait(&full_tA[ta], (gc / kTStages) & 1, a.status);
+                    ptx::mbar_wait(&full_Z[sz], (gc / kZStages) & 1, a.status);
+                    ptx::tc_fence_after();
+                    const uint32_t zhi = ptx::smem_u32(sZ + sz * 2 * kZPlaneBytes);
+                    const uint32_t zlo = zhi + kZPlaneBytes;
 #pragma unroll
-                for (int k = 0; k < kChunkKeys / 8; ++k) {
-                    const uint32_t a_hi = tmem + 64 + 64 * ta + 8 * k;
-                    const uint32_t a_lo = a_hi + 32;
-                    const uint64_t bhi = ptx::sw128_kmajor_desc(zhi + 32 * k);
-                    ptx::mma_tf32_ts(tmem, a_hi, bhi, idesc, (c | k) != 0);
-                    if (!kHop0) ptx::mma_tf32_ts(tmem, a_hi, ptx::sw128_kmajor_desc(zlo + 32 * k), idesc, 1);
-                    ptx::mma_tf32_ts(tmem, a_lo, bhi, idesc, 1);
+                    for (int k = 0; k < kChunkKeys / 8; ++k) {
+                        const uint32_t a_hi = tmem + kAccCols + 64 * ta + 8 * k;
+                        const uint32_t a_lo = a_hi + 32;
+                        const uint64_t bhi = ptx::sw128_kmajor_desc(zhi + 32 * k);
+                        ptx::mma_tf32_ts(dacc, a_hi, bhi, idesc, (c | k) != 0);
+                        if (!kHop0) ptx::mma_tf32_ts(dacc, a_hi, ptx::sw128_kmajor_desc(zlo + 32 * k), idesc, 1);
+                        ptx::mma_tf32_ts(dacc, a_lo, bhi, idesc, 1);
+                    }
+                    ptx::mma_commit(&empty_tA[ta]);
+                    ptx::mma_commit(&empty_Z[sz]);
                 }
-                ptx::mma_commit(&empty_tA[ta]);
-                ptx::mma_commit(&empty_Z[sz]);
+                ptx::mma_commit(&acc_full[ab]);
             }
-            ptx::mma_commit(acc_full);
             // Drain: the commits arrive asynchronously when the MMAs finish.  Wait
             // for the last phase of every empty barrier so that no arrival can land
-            // in this shared memory after the CTA exits (it would hit the barriers
-            // of the next CTA placed here).
+            // in this shared memory after the CTA exits.
+            const int total = my_tiles * chunks;
             for (int s = 0; s < kTStages; ++s) {
-                const int uses = (chunks - s + kTStages - 1) / kTStages;
+                const int uses = (total - s + kTStages - 1) / kTStages;
                 if (uses > 0) ptx::mbar_wait(&empty_tA[s], (uses - 1) & 1, a.status);
             }
             for (int s = 0; s < kZStages; ++s) {
-                const int uses = (chunks - s + kZStages - 1) / kZStages;
+                const int uses = (total - s + kZStages - 1) / kZStages;
                 if (uses > 0) ptx::mbar_wait(&empty_Z[s], (uses - 1) & 1, a.status);
             }
         }
     } else if (warp < 4) {
-        // ---------------- A splitter: smem (raw, de-skewed) -> masked hi / lo -> TMEM
+        // ---------------- A splitter.  Each thread streams its own row's stored
+        // window, 32 keys per chunk, with cp.async into its slot of a ring (zero
+        // fill outside the row's storage), then writes the masked hi / lo split
+        // into the TMEM A stage.  Only the thread itself reads its slot, so a
+        // per-thread cp.async.wait_group is the only synchronization needed.
         const int t = tid;                       // row within the tile
-        const int64_t i = i0 + t;
-        const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
-        const int64_t lo_key = i - P.r < 0 ? 0 : i - P.r;
-        const int64_t hi_key = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        for (int c = 0; c < chunks; ++c) {
-            const int sa = c % kAStages, ta = c % kTStages;
-            ptx::mbar_wait(&full_sA[sa], (c / kAStages) & 1, a.status);
-            float v[32];
-            const uint8_t* rowp = sA + sa * kAStageBytes + t * 128;
+        const int total = my_tiles * chunks;
+        const uint32_t slot0 = ptx::smem_u32(sA) + t * 128;
+        auto issue = [&](int gx) {
+            if (gx < total) {
+                const int lx = gx / chunks, cx = gx - lx * chunks;
+                const int64_t tix = blockIdx.x + (int64_t)lx * gridDim.x;
+                const int64_t u = tix / P.tiles;
+                const int64_t i = (tix - u * P.tiles) * kTileRows + t;
+                const bool in_rows = i < P.n;
+                const float* rowp = a.A_band + (size_t)u * (P.band_unit / 4) +
+                                    (size_t)(in_rows ? i : 0) * P.W;
+                const int w0 = kChunkKeys * cx - 4 * (t / 4);   // window column of the chunk's first key
+                const uint32_t dst = slot0 + (uint32_t)((gx % kAStages) * kAStageBytes);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 x = *reinterpret_cast<const float4*>(rowp + ((q ^ (t & 7)) << 4));
-                v[4 * q + 0] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+                for (int q = 0; q < 8; ++q) {
+                    const int w = w0 + 4 * q;
+                    const bool ok = in_rows && w >= 0 && w < P.W;
+                    ptx::cp_async16(dst + ((q ^ (t & 7)) << 4), ok ? rowp + w : rowp, ok ? 16 : 0);
+                }
             }
-            ptx::mbar_arrive(&empty_sA[sa]);
-            if (c >= kTStages) ptx::mbar_wait(&empty_tA[ta], ((c / kTStages) - 1) & 1, a.status);
-            __syncwarp();   // lanes leave the spin at different times; tcgen05.st is warp-collective
-            ptx::tc_fence_after();
-            const int64_t j0 = jb + kChunkKeys * c;
+            ptx::cp_async_commit();
+        };
+        for (int gx = 0; gx < kAStages; ++gx) issue(gx);
+        for (int lt = 0; lt < my_tiles; ++lt) {
+            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+            const int64_t u = tix / P.tiles;
+            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+            const int64_t jb = i0 - P.r_up;
+            const int64_t i = i0 + t;
+            const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
+            const int64_t lo_key = i - P.r < 0 ? 0 : i - P.r;
+            const int64_t hi_key = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+            for (int c = 0; c < chunks; ++c) {
+                const int gc = lt * chunks + c;
+                const int ta = gc % kTStages;
+                ptx::cp_async_wait<kAStages - 1>();
+                float v[32];
+                const uint8_t* rowp = sA + (gc % kAStages) * kAStageBytes + t * 128;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int64_t j = j0 + k;
-                const bool ok = row_ok && j >= lo_key && j <= hi_key;
-                v[k] = ok ? v[k] : 0.f;
+                for (int q = 0; q < 8; ++q) {
+                    const float4 x = *reinterpret_cast<const float4*>(rowp + ((q ^ (t & 7)) << 4));
+                    v[4 * q + 0] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+                }
+                if (gc >= kTStages) ptx::mbar_wait(&empty_tA[ta], ((gc / kTStages) - 1) & 1, a.status);
+                __syncwarp();   // lanes leave the spin at different times; tcgen05.st is warp-collective
+                ptx::tc_fence_after();
+                const int64_t j0 = jb + kChunkKeys * c;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int64_t j = j0 + k;
+                    const bool ok = row_ok && j >= lo_key && j <= hi_key;
+                    v[k] = ok ? v[k] : 0.f;
+                }
+                const uint32_t col = tmem + lane_base + kAccCols + 64 * ta;
+                ptx::tmem_st32(col, v);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] = v[k] - tf32_trunc(v[k]);
+                ptx::tmem_st32(col + 32, v);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&full_tA[ta]);
+                issue(gc + kAStages);            // refill this slot (its data are in TMEM now)
             }
-            const uint32_t col = tmem + lane_base + 64 + 64 * ta;
-            ptx::tmem_st32(col, v);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = v[k] - tf32_trunc(v[k]);
-            ptx::tmem_st32(col + 32, v);
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&full_tA[ta]);
         }
+        ptx::cp_async_wait<0>();
     } else {
         // ---------------- epilogue: accumulator + gathered part, restart term, outputs
         const int q = warp - 4;                  // TMEM lane quadrant and row block
-        // stage this block's gathered partial sums (coalesced) while the MMAs run
-        for (int rr = 0; rr < 32; ++rr) {
-            const int t = q * 32 + rr;
-            const int64_t i = i0 + t;
-            float2 pv = make_float2(0.f, 0.f);
-            if (i < P.n)
-                pv = __ldg(reinterpret_cast<const float2*>(a.Psum + ((size_t)u * P.n + i) * kHeadDim) + lane);
-            sP[t * kPStride + 2 * lane] = pv.x;
-            sP[t * kPStride + 2 * lane + 1] = pv.y;
-        }
-        __syncwarp();
-        ptx::mbar_wait(acc_full, 0, a.status);
-        __syncwarp();       // reconverge before the warp-collective tcgen05.ld
-        ptx::tc_fence_after();
-        const int t = q * 32 + lane;
-        const int64_t i = i0 + t;
-        const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
-        const float keep = (1.f - a.alpha) * (row_ok ? __ldg(a.inv_l + (size_t)u * P.n + i) : 0.f);
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-            float d[32];
-            ptx::tmem_ld32(tmem + lane_base + 32 * half, d);
-            if (!row_ok) continue;
-            const size_t row = ((size_t)u * P.n + i) * kHeadDim + 32 * half;
-            const uint4* vp = reinterpret_cast<const uint4*>(a.V + row);
-            float z[32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint4 vv = __ldg(vp + c);
-                const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int k = 8 * c + 2 * e;
-                    const float p0 = sP[t * kPStride + 32 * half + k];
-                    const float p1 = sP[t * kPStride + 32 * half + k + 1];
-                    z[k] = fmaf(keep, d[k] + p0, a.alpha * bf16lo(w4[e]));
-                    z[k + 1] = fmaf(keep, d[k + 1] + p1, a.alpha * bf16hi(w4[e]));
-                }
+        for (int lt = 0; lt < my_tiles; ++lt) {
+            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+            const int64_t u = tix / P.tiles;
+            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+            // stage this block's gathered partial sums (coalesced) while the MMAs run
+            for (int rr = 0; rr < 32; ++rr) {
+                const int t = q * 32 + rr;
+                const int64_t i = i0 + t;
+                float2 pv = make_float2(0.f, 0.f);
+                if (i < P.n)
+                    pv = __ldg(reinterpret_cast<const float2*>(a.Psum + ((size_t)u * P.n + i) * kHeadDim) + lane);
+                sP[t * kPStride + 2 * lane] = pv.x;
+                sP[t * kPStride + 2 * lane + 1] = pv.y;
             }
-            if (kLast) {
-                uint4* op = reinterpret_cast<uint4*>(a.out + row);
+            __syncwarp();
+            const int ab = lt & 1;
+            ptx::mbar_wait(&acc_full[ab], (lt / 2) & 1, a.status);
+            __syncwarp();       // reconverge before the warp-collective tcgen05.ld
+            ptx::tc_fence_after();
+            const int t = q * 32 + lane;
+            const int64_t i = i0 + t;
+            const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
+            const float keep = (1.f - a.alpha) * (row_ok ? __ldg(a.inv_l + (size_t)u * P.n + i) : 0.f);
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                float d[32];
+                ptx::tmem_ld32(tmem + lane_base + 64 * ab + 32 * half, d);
+                if (half == 1) {
+                    // both halves of this accumulator are in registers: hand it back
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&acc_empty[ab]);
+                }
+                if (!row_ok) continue;
+                const size_t row = ((size_t)u * P.n + i) * kHeadDim + 32 * half;
+                const uint4* vp = reinterpret_cast<const uint4*>(a.V + row);
+                float z[32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t w4[4];
+                    const uint4 vv = __ldg(vp + c);
+                    const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        __nv_bfloat162 h = __floats2bfloat162_rn(z[8 * c + 2 * e], z[8 * c + 2 * e + 1]);
-                        w4[e] = *reinterpret_cast<uint32_t*>(&h);
+                        const int k = 8 * c + 2 * e;
+                        const float p0 = sP[t * kPStride + 32 * half + k];
+                        const float p1 = sP[t * kPStride + 32 * half + k + 1];
+                        z[k] = fmaf(keep, d[k] + p0, a.alpha * bf16lo(w4[e]));
+                        z[k + 1] = fmaf(keep, d[k + 1] + p1, a.alpha * bf16hi(w4[e]));
                     }
-                    op[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
-            } else {
-                float4* zr = reinterpret_cast<float4*>(a.Zr_out + row);
+                if (kLast) {
+                    uint4* op = reinterpret_cast<uint4*>(a.out + row);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) zr[c] = make_float4(z[4 * c], z[4 * c + 1], z[4 * c + 2], z[4 * c + 3]);
-                const size_t tbase = ((size_t)u * kHeadDim + 32 * half) * P.nz + i;
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w4[4];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    a.Zt_out[tbase + (size_t)k * P.nz] = z[k];
-                    a.Ztl_out[tbase + (size_t)k * P.nz] = z[k] - tf32_trunc(z[k]);
+                        for (int e = 0; e < 4; ++e) {
+                            __nv_bfloat162 h = __floats2bfloat162_rn(z[8 * c + 2 * e], z[8 * c + 2 * e + 1]);
+                            w4[e] = *reinterpret_cast<uint32_t*>(&h);
+                        }
+                        op[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                } else {
+                    float4* zr = reinterpret_cast<float4*>(a.Zr_out + row);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) zr[c] = make_float4(z[4 * c], z[4 * c + 1], z[4 * c + 2], z[4 * c + 3]);
+                    const size_t tbase = ((size_t)u * kHeadDim + 32 * half) * P.nz + i;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        a.Zt_out[tbase + (size_t)k * P.nz] = z[k];
+                        a.Ztl_out[tbase + (size_t)k * P.nz] = z[k] - tf32_trunc(z[k]);
+                    }
                 }
             }
+            __syncwarp();       // sP is restaged for the next tile
         }
     }
     ptx::tc_fence_before();
@@ -297,17 +353,15 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
-
 // ---------------------------------------------------------------- sparse part of a hop
 // One CTA per (unit, 128-row block), 8 warps.  (1) The global rows: this
 // block's keys contribute sum_j A_gr[s][j] Z_k[j]; the last block of a unit
 // sums the shares in block order and writes Z_{k+1} of the global rows.
 // (2) Every other row: the globals outside its window and its random extras,
-// gathered as whole 256-byte Z_k rows in batches of independent loads, into
+// gathered as whole Z_k rows with several independent loads in flight, into
 // Psum[u][i] (fp32), which the band kernel's epilogue adds.
 constexpr int kSparseThreads = 256;
 constexpr int kGatherBatch = 8;
-// rows whose gathers run in one warp-iteration: two (one per half-warp)
 
 // Row j of Z_k for unit u, 4 features per lane (hl = lane within a half-warp).
 template <bool kHop0>
@@ -494,8 +548,8 @@ int encode(CUtensorMap* m, int rank, void* base, const cuuint64_t* dims, const c
 }
 
 template <bool kHop0, bool kLast>
-int launch_hop(const CUtensorMap& tmA, const CUtensorMap& tmZt, const CUtensorMap& tmZl,
-               const HopArgs& a, cudaStream_t stream) {
+int launch_hop(const CUtensorMap& tmZt, const CUtensorMap& tmZl, const HopArgs& a,
+               cudaStream_t stream) {
 
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -516,10 +570,18 @@ int launch_hop(const CUtensorMap& tmA, const CUtensorMap& tmZt, const CUtensorMa
     }
     cudaError_t serr = cudaGetLastError();
     if (serr != cudaSuccess) return cuda_fail(serr, "hop_sparse_kernel");
-    dim3 grid((unsigned)(a.units * a.plan.tiles));
+    static int num_sms = 0;
+    if (num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms < 1)
+            num_sms = 1;
+    }
+    const int64_t total_tiles = a.units * a.plan.tiles;
+    dim3 grid((unsigned)(total_tiles < num_sms ? total_tiles : num_sms));
     {
         LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
-        hop_band_kernel<kHop0, kLast><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmZt, tmZl, a);
+        hop_band_kernel<kHop0, kLast><<<grid, kThreads, kSmemBytes, stream>>>(tmZt, tmZl, a);
     }
     cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_band_kernel");
@@ -618,17 +680,8 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     err = cudaMemsetAsync(ws + L.counters, 0, (size_t)units * 4, stream);
     if (err != cudaSuccess) return cuda_fail(err, "clearing the tile counters");
 
-    // tensor maps: band weights (sheared 4-D view) and the two transposed Z planes
-    CUtensorMap tmA, tmZt[2], tmZl[2];
-    {
-        const cuuint64_t dims[4] = {(cuuint64_t)(p.n + 2 * p.r_up + 4), 4,
-                                    (cuuint64_t)(p.rows4 / 4), (cuuint64_t)units};
-        const cuuint64_t strides[3] = {(cuuint64_t)p.W * 4, (cuuint64_t)(p.W - 1) * 16,
-                                       (cuuint64_t)p.band_unit};
-        const cuuint32_t box[4] = {32, 4, 32, 1};
-        int st = encode(&tmA, 4, ws + L.a_band, dims, strides, box);
-        if (st) return st;
-    }
+    // tensor maps of the two transposed Z planes (the MMA's B operand)
+    CUtensorMap tmZt[2], tmZl[2];
     for (int s = 0; s < 2; ++s) {
         const cuuint64_t dims[3] = {(cuuint64_t)p.n, (cuuint64_t)kHeadDim, (cuuint64_t)units};
         const cuuint64_t strides[2] = {(cuuint64_t)p.nz * 4, (cuuint64_t)p.nz * 4 * kHeadDim};
@@ -657,6 +710,7 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     a.status = g->d_status;
     a.out = static_cast<__nv_bfloat16*>(out);
     a.Psum = reinterpret_cast<float*>(ws + L.psum);
+    a.A_band = reinterpret_cast<const float*>(ws + L.a_band);
     for (int32_t k = 0; k < hops; ++k) {
         const int cur = k & 1, nxt = (k + 1) & 1;
         a.Zr_in = k == 0 ? V : static_cast<const void*>(ws + L.zr[cur]);
@@ -665,10 +719,10 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
         a.Ztl_out = reinterpret_cast<float*>(ws + L.ztl[nxt]);
         const bool first = k == 0, last = k == hops - 1;
         int st;
-        if (first && last) st = launch_hop<true, true>(tmA, tmZt[cur], tmZl[cur], a, stream);
-        else if (first) st = launch_hop<true, false>(tmA, tmZt[cur], tmZl[cur], a, stream);
-        else if (last) st = launch_hop<false, true>(tmA, tmZt[cur], tmZl[cur], a, stream);
-        else st = launch_hop<false, false>(tmA, tmZt[cur], tmZl[cur], a, stream);
+        if (first && last) st = launch_hop<true, true>(tmZt[cur], tmZl[cur], a, stream);
+        else if (first) st = launch_hop<true, false>(tmZt[cur], tmZl[cur], a, stream);
+        else if (last) st = launch_hop<false, true>(tmZt[cur], tmZl[cur], a, stream);
+        else st = launch_hop<false, false>(tmZt[cur], tmZl[cur], a, stream);
         if (st) return st;
     }
     return DIFFUSER_OK;

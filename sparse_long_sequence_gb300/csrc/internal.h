@@ -31,7 +31,7 @@ struct BandPlan {
     int64_t nz;         // key stride of the transposed Z planes (multiple of 4)
     int32_t tiles;      // 128-row tiles per unit
     int32_t chunks;     // 32-key chunks per tile
-    size_t band_unit;   // bytes of one unit's band weights (with slack for the sheared reads)
+    size_t band_unit;   // bytes of one unit's band weights (with slack at the end)
 };
 
 // Byte offsets of the band path's workspace regions.
