@@ -41,7 +41,11 @@ constexpr int kChunkKeys = 32;
 // tiles were observed in the first chunk of some tiles, so the kernel claims a
 // whole SM (its shared memory alone rules out a second CTA) and uses the room
 // for deeper pipelines.
-constexpr int kThreads = 320;            // 10 warps
+// warps 0-7: A splitters (two per TMEM lane quadrant, 16 columns each),
+// warps 8-11: epilogue, warp 12: TMA producer, warp 13: MMA issuer
+constexpr int kThreads = 448;
+constexpr int kSplitThreads = 256;
+constexpr int kEpiWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13;
 constexpr int kAStages = 6;              // per-thread cp.async ring of A chunks (16 KB per stage)
 constexpr int kZStages = 4;              // smem stages of Z^T hi+lo (16 KB each)
 constexpr int kAccCols = 128;            // two 64-column accumulators (double-buffered tiles)
@@ -116,14 +120,14 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
     const int my_tiles = blockIdx.x < total_tiles
         ? (int)((total_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
 
-    if (warp == 9) ptx::tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kMmaWarp) ptx::tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
-        for (int s = 0; s < kTStages; ++s) { ptx::mbar_init(&full_tA[s], 128); ptx::mbar_init(&empty_tA[s], 1); }
+        for (int s = 0; s < kTStages; ++s) { ptx::mbar_init(&full_tA[s], kSplitThreads); ptx::mbar_init(&empty_tA[s], 1); }
         for (int s = 0; s < kZStages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
         for (int s = 0; s < 2; ++s) { ptx::mbar_init(&acc_full[s], 1); ptx::mbar_init(&acc_empty[s], 128); }
         ptx::fence_mbar_init();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == kTmaWarp && lane == 0) {
         ptx::prefetch_tensormap(&tmZt);
         if (!kHop0) ptx::prefetch_tensormap(&tmZl);
     }
@@ -132,7 +136,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp == kTmaWarp) {
         // ---------------- TMA producer
         if (lane == 0) {
             for (int lt = 0; lt < my_tiles; ++lt) {
@@ -152,7 +156,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
                 }
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer: accumulator lt & 1 of TMEM columns [64 (lt & 1), +64)
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::mma_idesc(2, kHeadDim);
@@ -196,14 +200,17 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
                 if (uses > 0) ptx::mbar_wait(&empty_Z[s], (uses - 1) & 1, a.status);
             }
         }
-    } else if (warp < 4) {
-        // ---------------- A splitter.  Each thread streams its own row's stored
-        // window, 32 keys per chunk, with cp.async into its slot of a ring (zero
-        // fill outside the row's storage), then writes the masked hi / lo split
-        // into the TMEM A stage.  Only the thread itself reads its slot, so a
-        // per-thread cp.async.wait_group is the only synchronization needed.
-        const int t = tid;                       // row within the tile
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    } else if (warp < kEpiWarp0) {
+        // ---------------- A splitters.  Warp w serves TMEM lane quadrant w % 4 (rows
+        // 32 (w % 4) .. +31) and columns 16 (w / 4) .. +15 of every 32-key chunk.
+        // Each thread streams its own 64-byte share of its row's stored window
+        // with cp.async into its slot of a ring (zero fill outside the row's
+        // storage), then writes the masked hi / lo split into the TMEM A stage.
+        // Only the thread itself reads its slot: cp.async.wait_group is the only
+        // synchronization the copies need.
+        const int quad = warp & 3, hcol = warp >> 2;
+        const int t = quad * 32 + lane;          // row within the tile
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int total = my_tiles * chunks;
         const uint32_t slot0 = ptx::smem_u32(sA) + t * 128;
         auto issue = [&](int gx) {
@@ -215,13 +222,15 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
                 const bool in_rows = i < P.n;
                 const float* rowp = a.A_band + (size_t)u * (P.band_unit / 4) +
                                     (size_t)(in_rows ? i : 0) * P.W;
-                const int w0 = kChunkKeys * cx - 4 * (t / 4);   // window column of the chunk's first key
+                // window column of this thread's first key in the chunk
+                const int w0 = kChunkKeys * cx + 16 * hcol - 4 * (t / 4);
                 const uint32_t dst = slot0 + (uint32_t)((gx % kAStages) * kAStageBytes);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < 4; ++q) {
                     const int w = w0 + 4 * q;
                     const bool ok = in_rows && w >= 0 && w < P.W;
-                    ptx::cp_async16(dst + ((q ^ (t & 7)) << 4), ok ? rowp + w : rowp, ok ? 16 : 0);
+                    ptx::cp_async16(dst + (((4 * hcol + q) ^ (t & 7)) << 4), ok ? rowp + w : rowp,
+                                    ok ? 16 : 0);
                 }
             }
             ptx::cp_async_commit();
@@ -231,37 +240,39 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
             const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
             const int64_t u = tix / P.tiles;
             const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-            const int64_t jb = i0 - P.r_up;
             const int64_t i = i0 + t;
             const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
             const int64_t lo_key = i - P.r < 0 ? 0 : i - P.r;
             const int64_t hi_key = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+            // first absolute key of this thread's columns in chunk 0
+            const int64_t jt = i0 - P.r_up + 16 * hcol;
             for (int c = 0; c < chunks; ++c) {
                 const int gc = lt * chunks + c;
                 const int ta = gc % kTStages;
                 ptx::cp_async_wait<kAStages - 1>();
-                float v[32];
+                float hi[16], lo[16];
                 const uint8_t* rowp = sA + (gc % kAStages) * kAStageBytes + t * 128;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 x = *reinterpret_cast<const float4*>(rowp + ((q ^ (t & 7)) << 4));
-                    v[4 * q + 0] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x = *reinterpret_cast<const float4*>(rowp + (((4 * hcol + q) ^ (t & 7)) << 4));
+                    hi[4 * q + 0] = x.x; hi[4 * q + 1] = x.y; hi[4 * q + 2] = x.z; hi[4 * q + 3] = x.w;
                 }
+                const int64_t j0 = jt + kChunkKeys * c;
+                if (!(row_ok && j0 >= lo_key && j0 + 15 <= hi_key)) {
+                    // partly (or not at all) inside the row's window
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int64_t j = j0 + k;
+                        hi[k] = (row_ok && j >= lo_key && j <= hi_key) ? hi[k] : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 16; ++k) lo[k] = hi[k] - tf32_trunc(hi[k]);
                 if (gc >= kTStages) ptx::mbar_wait(&empty_tA[ta], ((gc / kTStages) - 1) & 1, a.status);
                 __syncwarp();   // lanes leave the spin at different times; tcgen05.st is warp-collective
                 ptx::tc_fence_after();
-                const int64_t j0 = jb + kChunkKeys * c;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int64_t j = j0 + k;
-                    const bool ok = row_ok && j >= lo_key && j <= hi_key;
-                    v[k] = ok ? v[k] : 0.f;
-                }
-                const uint32_t col = tmem + lane_base + kAccCols + 64 * ta;
-                ptx::tmem_st32(col, v);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = v[k] - tf32_trunc(v[k]);
-                ptx::tmem_st32(col + 32, v);
+                const uint32_t col = tmem + lane_base + kAccCols + 64 * ta + 16 * hcol;
+                ptx::tmem_st16x2(col, hi, col + 32, lo);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&full_tA[ta]);
                 issue(gc + kAStages);            // refill this slot (its data are in TMEM now)
@@ -270,7 +281,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
         ptx::cp_async_wait<0>();
     } else {
         // ---------------- epilogue: accumulator + gathered part, restart term, outputs
-        const int q = warp - 4;                  // TMEM lane quadrant and row block
+        const int q = warp - kEpiWarp0;          // TMEM lane quadrant and row block
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         for (int lt = 0; lt < my_tiles; ++lt) {
             const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
@@ -350,7 +361,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 9) ptx::tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------- sparse part of a hop

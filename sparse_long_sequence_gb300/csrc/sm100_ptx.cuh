@@ -219,6 +219,30 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
+// Two 16-column stores (hi, lo) of this warp's lanes, then one wait.
+__device__ __forceinline__ void tmem_st16x2(uint32_t taddr_a, const float (&a)[16], uint32_t taddr_b,
+                                            const float (&b)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};\n"
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%1], "
+        "{%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr_a), "r"(taddr_b),
+        "r"(__float_as_uint(a[0])), "r"(__float_as_uint(a[1])), "r"(__float_as_uint(a[2])),
+        "r"(__float_as_uint(a[3])), "r"(__float_as_uint(a[4])), "r"(__float_as_uint(a[5])),
+        "r"(__float_as_uint(a[6])), "r"(__float_as_uint(a[7])), "r"(__float_as_uint(a[8])),
+        "r"(__float_as_uint(a[9])), "r"(__float_as_uint(a[10])), "r"(__float_as_uint(a[11])),
+        "r"(__float_as_uint(a[12])), "r"(__float_as_uint(a[13])), "r"(__float_as_uint(a[14])),
+        "r"(__float_as_uint(a[15])),
+        "r"(__float_as_uint(b[0])), "r"(__float_as_uint(b[1])), "r"(__float_as_uint(b[2])),
+        "r"(__float_as_uint(b[3])), "r"(__float_as_uint(b[4])), "r"(__float_as_uint(b[5])),
+        "r"(__float_as_uint(b[6])), "r"(__float_as_uint(b[7])), "r"(__float_as_uint(b[8])),
+        "r"(__float_as_uint(b[9])), "r"(__float_as_uint(b[10])), "r"(__float_as_uint(b[11])),
+        "r"(__float_as_uint(b[12])), "r"(__float_as_uint(b[13])), "r"(__float_as_uint(b[14])),
+        "r"(__float_as_uint(b[15]))
+        : "memory");
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
