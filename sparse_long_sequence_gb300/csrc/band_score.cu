@@ -8,11 +8,11 @@
 //    scores of the global rows against the tile's keys with per-tile
 //    (max, sum of exp); the last tile of a unit merges those into the global
 //    rows' (max, 1/sum).
-//  * score_band_tc_kernel (tcgen05): S = Q K^T for a 128-row tile against
-//    64-key chunks of its window on bf16 tensor cores (fp32 accumulation in
-//    TMEM), in two passes over the chunks: the row maximum, then
-//    e = exp(s - m) written into the band storage with the row sum; the row
-//    threads then turn the row's sparse raw scores into e and store
+//  * score_band_tc_kernel (tcgen05, persistent): S = Q K^T for a 128-row
+//    tile against 64-key chunks of its window on bf16 tensor cores (fp32
+//    accumulation in TMEM), in two passes over the chunks: the row maximum,
+//    then e = exp(s - m) written into the band storage with the row sum; the
+//    row threads then turn the row's sparse raw scores into e and store
 //    inv_l = 1 / (band sum + sparse sum).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -183,16 +183,24 @@ score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
 }
 
 // ---------------------------------------------------------------- band scores (tcgen05)
-constexpr int kBThreads = 256;           // warp 0 TMA, warp 1 MMA, warps 4-7 rows
+// Persistent: one CTA per SM walks tiles round-robin.  Warp 0 loads Q tiles
+// (two buffers) and K chunks (ring) by TMA; warp 1 issues the MMAs into a ring
+// of TMEM S buffers; warps 2-3 normalize the global rows' weights of the tile's
+// keys; warps 4-11 are row warps: warp w serves TMEM lane quadrant w % 4 and
+// columns 32 ((w - 4) / 4) .. +31 of each 64-key S chunk.
+constexpr int kBThreads = 384;
+constexpr int kRowWarp0 = 4;
+constexpr int kRowThreads = 256;
 constexpr int kSChunk = 64;              // keys per chunk (MMA N)
-constexpr int kKStages = 6;              // smem ring of K chunks (8 KB each)
-constexpr int kSBufs = 4;                // TMEM S buffers (64 columns each)
-constexpr int kBTmemCols = 256;
+constexpr int kKStages = 8;              // smem ring of K chunks (8 KB each)
+constexpr int kSBufs = 8;                // TMEM S buffers (64 columns each)
+constexpr int kBTmemCols = 512;
 constexpr int kQBytes = kTileRows * kHeadDim * 2;
 constexpr int kKBytes = kSChunk * kHeadDim * 2;
-// One CTA per SM (shared memory alone excludes a second one).
-constexpr int kBSmemBytes = 120 * 1024;
-static_assert(1024 + kQBytes + kKStages * kKBytes + 256 <= kBSmemBytes, "smem");
+constexpr int kBSmemUsed = 1024 + 2 * kQBytes + kKStages * kKBytes + 2 * kRowThreads * 4 + 512;
+// request at least 120 KB so that the shared memory alone keeps it to one CTA per SM
+constexpr int kBSmemBytes = kBSmemUsed > 120 * 1024 ? kBSmemUsed : 120 * 1024;
+constexpr float kLog2e = 1.4426950408889634f;
 
 __global__ void __launch_bounds__(kBThreads, 1)
 score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -200,30 +208,31 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sK = sQ + kQBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sK + kKStages * kKBytes);
-    uint64_t* full_Q = bars;
-    uint64_t* full_K = full_Q + 1;
+    uint8_t* sQ = smem;                                   // 2 x 16 KB
+    uint8_t* sK = sQ + 2 * kQBytes;                       // kKStages x 8 KB
+    float* xch = reinterpret_cast<float*>(sK + kKStages * kKBytes);   // [2][256] row partials
+    uint64_t* bars = reinterpret_cast<uint64_t*>(xch + 2 * kRowThreads);
+    uint64_t* full_Q = bars;                  // [2]
+    uint64_t* empty_Q = full_Q + 2;           // [2]
+    uint64_t* full_K = empty_Q + 2;           // [kKStages]
     uint64_t* empty_K = full_K + kKStages;
-    uint64_t* full_S = empty_K + kKStages;
+    uint64_t* full_S = empty_K + kKStages;    // [kSBufs]
     uint64_t* empty_S = full_S + kSBufs;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_S + kSBufs);
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t u = blockIdx.x / P.tiles;
-    const int tile = (int)(blockIdx.x - u * P.tiles);
-    const int64_t i0 = (int64_t)tile * kTileRows;
-    const int64_t jb = i0 - P.r_up;                     // first key of chunk 0
     const int nc = (124 + P.W + kSChunk - 1) / kSChunk;  // chunks covering every stored window
-    const int iters = 2 * nc;                            // pass 1 (max), pass 2 (exp + write)
+    const int per_tile = 2 * nc;                          // pass 1 (max), pass 2 (exp + write)
+    const int64_t total_tiles = a.units * P.tiles;
+    const int my_tiles = blockIdx.x < total_tiles
+        ? (int)((total_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
 
     if (warp == 1) ptx::tmem_alloc(tmem_slot, kBTmemCols);
     if (tid == 0) {
-        ptx::mbar_init(full_Q, 1);
+        for (int s = 0; s < 2; ++s) { ptx::mbar_init(&full_Q[s], 1); ptx::mbar_init(&empty_Q[s], 1); }
         for (int s = 0; s < kKStages; ++s) { ptx::mbar_init(&full_K[s], 1); ptx::mbar_init(&empty_K[s], 1); }
-        for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], 128); }
+        for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], kRowThreads); }
         ptx::fence_mbar_init();
     }
     ptx::tc_fence_before();
@@ -233,116 +242,174 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 
     if (warp == 0) {
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(full_Q, kQBytes);
-            ptx::tma_load_3d(sQ, &tmQ, full_Q, 0, (int)i0, (int)u);
-            for (int it = 0; it < iters; ++it) {
-                const int c = it % nc, s = it % kKStages;
-                if (it >= kKStages) ptx::mbar_wait(&empty_K[s], ((it / kKStages) - 1) & 1, status);
-                ptx::mbar_arrive_expect_tx(&full_K[s], kKBytes);
-                ptx::tma_load_3d(sK + s * kKBytes, &tmK, &full_K[s], 0, (int)(jb + kSChunk * c), (int)u);
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+                const int64_t u = tix / P.tiles;
+                const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+                const int64_t jb = i0 - P.r_up;
+                const int qb = lt & 1;
+                if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, status);
+                ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
+                ptx::tma_load_3d(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, (int)i0, (int)u);
+                for (int it = 0; it < per_tile; ++it) {
+                    const int gi = lt * per_tile + it;
+                    const int c = it % nc, s = gi % kKStages;
+                    if (gi >= kKStages) ptx::mbar_wait(&empty_K[s], ((gi / kKStages) - 1) & 1, status);
+                    ptx::mbar_arrive_expect_tx(&full_K[s], kKBytes);
+                    ptx::tma_load_3d(sK + s * kKBytes, &tmK, &full_K[s], 0, (int)(jb + kSChunk * c), (int)u);
+                }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::mma_idesc(1, kSChunk);
-            ptx::mbar_wait(full_Q, 0, status);
-            const uint32_t qa = ptx::smem_u32(sQ);
-            for (int it = 0; it < iters; ++it) {
-                const int s = it % kKStages, b = it % kSBufs;
-                ptx::mbar_wait(&full_K[s], (it / kKStages) & 1, status);
-                if (it >= kSBufs) ptx::mbar_wait(&empty_S[b], ((it / kSBufs) - 1) & 1, status);
-                ptx::tc_fence_after();
-                const uint32_t kb = ptx::smem_u32(sK + s * kKBytes);
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const int qb = lt & 1;
+                ptx::mbar_wait(&full_Q[qb], (lt / 2) & 1, status);
+                const uint32_t qa = ptx::smem_u32(sQ + qb * kQBytes);
+                for (int it = 0; it < per_tile; ++it) {
+                    const int gi = lt * per_tile + it;
+                    const int s = gi % kKStages, b = gi % kSBufs;
+                    ptx::mbar_wait(&full_K[s], (gi / kKStages) & 1, status);
+                    if (gi >= kSBufs) ptx::mbar_wait(&empty_S[b], ((gi / kSBufs) - 1) & 1, status);
+                    ptx::tc_fence_after();
+                    const uint32_t kb = ptx::smem_u32(sK + s * kKBytes);
 #pragma unroll
-                for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                    ptx::mma_bf16_ss(tmem + kSChunk * b, ptx::sw128_kmajor_desc(qa + 32 * ks),
-                                     ptx::sw128_kmajor_desc(kb + 32 * ks), idesc, ks > 0);
-                ptx::mma_commit(&empty_K[s]);
-                ptx::mma_commit(&full_S[b]);
+                    for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                        ptx::mma_bf16_ss(tmem + kSChunk * b, ptx::sw128_kmajor_desc(qa + 32 * ks),
+                                         ptx::sw128_kmajor_desc(kb + 32 * ks), idesc, ks > 0);
+                    ptx::mma_commit(&empty_K[s]);
+                    ptx::mma_commit(&full_S[b]);
+                }
+                ptx::mma_commit(&empty_Q[qb]);
             }
             // drain the asynchronous commit arrivals before the CTA can exit
+            const int total = my_tiles * per_tile;
             for (int s = 0; s < kKStages; ++s) {
-                const int uses = (iters - s + kKStages - 1) / kKStages;
+                const int uses = (total - s + kKStages - 1) / kKStages;
                 if (uses > 0) ptx::mbar_wait(&empty_K[s], (uses - 1) & 1, status);
+            }
+            for (int s = 0; s < 2; ++s) {
+                const int uses = (my_tiles - s + 1) / 2;
+                if (uses > 0) ptx::mbar_wait(&empty_Q[s], (uses - 1) & 1, status);
             }
         }
     } else if (warp == 2 || warp == 3) {
-        // normalize the global rows' weights over this tile's keys:
+        // normalize the global rows' weights over each tile's keys:
         // A_gr = exp(s - max) / sum, with (max, 1/sum) from score_sparse_kernel
-        const int64_t tkeys = P.n - i0 < kTileRows ? P.n - i0 : kTileRows;
-        for (int e = tid - 64; e < P.g * kTileRows; e += 64) {
-            const int sl = e / kTileRows, jj = e % kTileRows;
-            if (jj >= tkeys) continue;
-            const float gm = a.w.gstat[((size_t)u * P.g + sl) * 2];
-            const float ginv = a.w.gstat[((size_t)u * P.g + sl) * 2 + 1];
-            float* v = a.w.A_gr + ((size_t)u * P.g + sl) * P.n + i0 + jj;
-            *v = expf(*v - gm) * ginv;
+        for (int lt = 0; lt < my_tiles; ++lt) {
+            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+            const int64_t u = tix / P.tiles;
+            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+            const int64_t tkeys = P.n - i0 < kTileRows ? P.n - i0 : kTileRows;
+            for (int e = tid - 64; e < P.g * kTileRows; e += 64) {
+                const int sl = e / kTileRows, jj = e % kTileRows;
+                if (jj >= tkeys) continue;
+                const float gm = a.w.gstat[((size_t)u * P.g + sl) * 2];
+                const float ginv = a.w.gstat[((size_t)u * P.g + sl) * 2 + 1];
+                float* v = a.w.A_gr + ((size_t)u * P.g + sl) * P.n + i0 + jj;
+                *v = expf(*v - gm) * ginv;
+            }
         }
-    } else if (warp >= 4) {
-        const int q = warp - 4;
-        const int t = q * 32 + lane;
-        const int64_t i = i0 + t;
-        const bool row_ok = i < P.n && !a.gr.is_global[i < P.n ? i : 0];
-        const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
-        const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        float m = row_ok ? a.w.m_sparse[(size_t)u * P.n + i] : 0.f;
-        float lsum = 0.f;
-        float* brow = a.w.A_band + (size_t)u * (P.band_unit / 4) + (size_t)i * P.W;
-        const int wshift = 4 * (t / 4);                  // window start of row i minus jb
-        for (int it = 0; it < iters; ++it) {
-            const int b = it % kSBufs, c = it % nc;
-            const bool pass2 = it >= nc;
-            ptx::mbar_wait(&full_S[b], (it / kSBufs) & 1, status);
-            __syncwarp();
-            ptx::tc_fence_after();
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                float s[32];
-                ptx::tmem_ld32(tmem + lane_base + kSChunk * b + 32 * half, s);
-                const int64_t j0 = jb + kSChunk * c + 32 * half;
+    } else {
+        const int rw = warp - kRowWarp0;          // 0..7
+        const int quad = warp & 3, hcol = rw >> 2;
+        const int t = quad * 32 + lane;           // row within the tile
+        const int rtid = rw * 32 + lane;          // 0..255
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const float a_sc = kLog2e * kScale;
+        for (int lt = 0; lt < my_tiles; ++lt) {
+            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+            const int64_t u = tix / P.tiles;
+            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+            const int64_t jb = i0 - P.r_up;
+            const int64_t i = i0 + t;
+            const bool row_ok = i < P.n && !a.gr.is_global[i < P.n ? i : 0];
+            const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
+            const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+            float* brow = a.w.A_band + (size_t)u * (P.band_unit / 4) + (size_t)(row_ok ? i : 0) * P.W;
+            const int wshift = 4 * (t / 4);       // window start of row i minus jb
+            float mraw = -INFINITY;               // max of the raw dot products q.k (unscaled)
+            float m = 0.f, b2 = 0.f, lsum = 0.f;
+            for (int it = 0; it < per_tile; ++it) {
+                const int gi = lt * per_tile + it;
+                const int b = gi % kSBufs, c = it % nc;
+                const bool pass2 = it >= nc;
+                if (it == nc) {
+                    // both column halves of a row agree on the row maximum
+                    xch[rtid] = mraw;
+                    ptx::named_barrier_sync(1, kRowThreads);
+                    const float other = xch[(rtid + 128) & 255];
+                    const float ms = row_ok ? a.w.m_sparse[(size_t)u * P.n + i] : 0.f;
+                    m = fmaxf(ms, fmaxf(mraw, other) * kScale);
+                    b2 = m * kLog2e;
+                    ptx::named_barrier_sync(1, kRowThreads);   // xch is reused below
+                }
+                ptx::mbar_wait(&full_S[b], (gi / kSBufs) & 1, status);
+                __syncwarp();
+                ptx::tc_fence_after();
+                float sv[32];
+                ptx::tmem_ld32(tmem + lane_base + kSChunk * b + 32 * hcol, sv);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&empty_S[b]);
+                const int64_t j0 = jb + kSChunk * c + 32 * hcol;
+                const bool full_in = row_ok && j0 >= lo && j0 + 31 <= hi;
+                const bool none_in = !row_ok || j0 > hi || j0 + 31 < lo;
                 if (!pass2) {
+                    if (full_in) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int64_t j = j0 + k;
-                        if (row_ok && j >= lo && j <= hi) m = fmaxf(m, s[k] * kScale);
+                        for (int k = 0; k < 32; ++k) mraw = fmaxf(mraw, sv[k]);
+                    } else if (!none_in) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const int64_t j = j0 + k;
+                            if (j >= lo && j <= hi) mraw = fmaxf(mraw, sv[k]);
+                        }
                     }
                 } else if (row_ok) {
-                    const int w0 = kSChunk * c + 32 * half - wshift;   // multiple of 4
+                    float e[32];
+                    if (full_in) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) { e[k] = exp2f(fmaf(sv[k], a_sc, -b2)); lsum += e[k]; }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const int64_t j = j0 + k;
+                            e[k] = (j >= lo && j <= hi) ? exp2f(fmaf(sv[k], a_sc, -b2)) : 0.f;
+                            lsum += e[k];
+                        }
+                    }
+                    const int w0 = kSChunk * c + 32 * hcol - wshift;   // multiple of 4
 #pragma unroll
                     for (int k4 = 0; k4 < 8; ++k4) {
-                        float e[4];
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const int64_t j = j0 + 4 * k4 + x;
-                            e[x] = (j >= lo && j <= hi) ? expf(s[4 * k4 + x] * kScale - m) : 0.f;
-                            lsum += e[x];
-                        }
                         const int w = w0 + 4 * k4;
                         if (w >= 0 && w < P.W)
-                            *reinterpret_cast<float4*>(brow + w) = make_float4(e[0], e[1], e[2], e[3]);
+                            *reinterpret_cast<float4*>(brow + w) =
+                                make_float4(e[4 * k4], e[4 * k4 + 1], e[4 * k4 + 2], e[4 * k4 + 3]);
                     }
                 }
             }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&empty_S[b]);
-        }
-        // the row's sparse part: raw scores -> e, and the normalizer
-        if (row_ok) {
-            float* wg = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
-            for (int s = 0; s < P.g; ++s) {
-                const int64_t j = a.gr.globals[s];
-                const float e = (j < lo || j > hi) ? expf(wg[s] - m) : 0.f;
-                wg[s] = e;
-                lsum += e;
+            // the row's sparse part (first column half) and the normalizer
+            xch[rtid] = lsum;
+            ptx::named_barrier_sync(1, kRowThreads);
+            if (hcol == 0 && row_ok) {
+                float l = lsum + xch[rtid + 128];
+                float* wg = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+                for (int s2 = 0; s2 < P.g; ++s2) {
+                    const int64_t j = a.gr.globals[s2];
+                    const float e = (j < lo || j > hi) ? expf(wg[s2] - m) : 0.f;
+                    wg[s2] = e;
+                    l += e;
+                }
+                float* wx = a.w.A_x + (size_t)u * a.gr.nx;
+                for (int64_t e = a.gr.x_ptr[i]; e < a.gr.x_ptr[i + 1]; ++e) {
+                    const float v = expf(wx[e] - m);
+                    wx[e] = v;
+                    l += v;
+                }
+                a.w.inv_l[(size_t)u * P.n + i] = 1.f / l;
             }
-            float* wx = a.w.A_x + (size_t)u * a.gr.nx;
-            for (int64_t e = a.gr.x_ptr[i]; e < a.gr.x_ptr[i + 1]; ++e) {
-                const float v = expf(wx[e] - m);
-                wx[e] = v;
-                lsum += v;
-            }
-            a.w.inv_l[(size_t)u * P.n + i] = 1.f / lsum;
+            ptx::named_barrier_sync(1, kRowThreads);   // xch is reused by the next tile
         }
     }
     ptx::tc_fence_before();
@@ -463,9 +530,17 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled (Q/K) failed: " + std::to_string((int)r));
+    static int num_sms = 0;
+    if (num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms < 1)
+            num_sms = 1;
+    }
+    const unsigned pgrid = grid < (unsigned)num_sms ? grid : (unsigned)num_sms;
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
-        score_band_tc_kernel<<<grid, kBThreads, kBSmemBytes, stream>>>(tmQ, tmK, a, g->d_status);
+        score_band_tc_kernel<<<pgrid, kBThreads, kBSmemBytes, stream>>>(tmQ, tmK, a, g->d_status);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_band_tc_kernel");
     return DIFFUSER_OK;
