@@ -193,6 +193,42 @@ DIFFUSER_API int diffuser_forward_host(const void* Q, const void* K, const void*
                           float alpha, void* out, void* workspace, size_t workspace_bytes,
                           diffuser_stream stream);
 
+/* ---------------------------------------------------------------- no-allocation forward */
+
+/*
+ * diffuser_forward without any device allocation, for callers that cannot
+ * call cudaMalloc while the forward runs: code recording a CUDA stream
+ * capture, serving loops whose device memory is fixed at start-up, or host
+ * frameworks that own every allocation and forbid allocating calls on their
+ * hot path.  (The pages have no counterpart: this is a library convenience,
+ * not part of the method.)
+ *
+ * Same arguments and results as diffuser_forward, without the workspace: the
+ * weights A and the hop state live in one fixed array in device global
+ * memory defined by the library (diffuser_no_alloc_scratch_bytes() bytes,
+ * 32 MiB), which every GPU that loads the library holds until the process
+ * exits.  It runs the general CSR kernels.  The graph must be built
+ * beforehand (diffuser_build_graph allocates).
+ *   - Problems whose weights and hop state need more than the array holds
+ *     (units * nnz * 4 + 2 * units * n * 64 * 4 bytes, each part rounded up
+ *     to 256) are rejected with DIFFUSER_ERR_WORKSPACE before anything runs.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (make it before any stream capture); later calls only launch
+ *     kernels.  No cudaMalloc, cudaFree or allocating library routine is
+ *     called.
+ *   - All calls share the array: two calls that overlap on the GPU (on
+ *     different streams, or different host threads) race and corrupt each
+ *     other's results.  Calls on one stream are serialized and safe.
+ * Errors: as diffuser_forward, plus WORKSPACE when the problem is too large.
+ */
+DIFFUSER_API int diffuser_forward_no_alloc(const void* Q, const void* K, const void* V,
+                                           int32_t dtype, int64_t B, int64_t H, int32_t d,
+                                           const diffuser_graph* g, int32_t hops, float alpha,
+                                           void* out, diffuser_stream stream);
+
+/* Size in bytes of the fixed device array diffuser_forward_no_alloc uses. */
+DIFFUSER_API size_t diffuser_no_alloc_scratch_bytes(void);
+
 /* ---------------------------------------------------------------- test exports */
 
 /*

@@ -60,6 +60,9 @@ def _load() -> ctypes.CDLL:
                                                  c.c_size_t, vp]),
         "diffuser_diffuse_csr": (c.c_int, [vp, vp, vp, i32, i64, i64, i32, i32, f32, vp, vp,
                                            c.c_size_t, vp]),
+        "diffuser_forward_no_alloc": (c.c_int, [vp, vp, vp, i32, i64, i64, i32, vp, i32, f32, vp,
+                                                vp]),
+        "diffuser_no_alloc_scratch_bytes": (c.c_size_t, []),
         "diffuser_set_path": (c.c_int, [c.c_int]),
         "diffuser_get_path": (c.c_int, []),
         "diffuser_graph_status": (c.c_int, [vp, c.POINTER(c.c_int), c.c_int]),
@@ -223,6 +226,20 @@ def diffuser_forward_host(Q, K, V, g: Graph, hops: int, alpha: float, out, works
                                       workspace.data_ptr(), workspace.numel(), _stream(stream)),
            "diffuser_forward_host")
     return out
+
+
+def diffuser_forward_no_alloc(Q, K, V, g: Graph, hops: int, alpha: float, out, stream=None):
+    """The forward with the library's fixed device scratch array (no workspace)."""
+    B, H, d = _shape(Q, g)
+    code = _dtype_code(Q)
+    _check(_lib.diffuser_forward_no_alloc(Q.data_ptr(), K.data_ptr(), V.data_ptr(), code, B, H, d,
+                                          g.handle, hops, alpha, out.data_ptr(), _stream(stream)),
+           "diffuser_forward_no_alloc")
+    return out
+
+
+def diffuser_no_alloc_scratch_bytes() -> int:
+    return int(_lib.diffuser_no_alloc_scratch_bytes())
 
 
 def diffuser_attention_weights(Q, K, g: Graph, A_out=None, workspace=None, stream=None):
