@@ -282,9 +282,10 @@ DIFFUSER_API int diffuser_graph_status(const diffuser_graph* g, int* status, int
 typedef enum {
     DIFFUSER_KERNEL_BUILD = 0,    /* graph construction */
     DIFFUSER_KERNEL_SCORE = 1,    /* scores + masked softmax -> A */
-    DIFFUSER_KERNEL_HOP = 2,      /* one diffusion hop */
+    DIFFUSER_KERNEL_HOP = 2,      /* one diffusion hop (the window part, on the band path) */
     DIFFUSER_KERNEL_AUX = 3,      /* copies, conversions, split-reduction merges */
-    DIFFUSER_KERNEL_KINDS = 4
+    DIFFUSER_KERNEL_GATHER = 4,   /* band path: a hop's random-edge / global gathers */
+    DIFFUSER_KERNEL_KINDS = 5
 } diffuser_kernel_kind;
 
 /* Number of kernels this library has launched in this process, per kind

@@ -23,7 +23,7 @@ DIFFUSER_DTYPE_FP32 = 0
 DIFFUSER_DTYPE_BF16 = 1
 DIFFUSER_PATH_AUTO = 0
 DIFFUSER_PATH_CSR = 1
-KERNEL_KINDS = ("build", "score", "hop", "aux")
+KERNEL_KINDS = ("build", "score", "hop", "aux", "gather")
 
 
 class DiffuserError(RuntimeError):

@@ -574,7 +574,7 @@ int launch_hop(const CUtensorMap& tmZt, const CUtensorMap& tmZl, const HopArgs& 
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(hop)");
     {
-        LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
+        LaunchScope scope(DIFFUSER_KERNEL_GATHER, stream);
         const size_t shmem = (size_t)8 * a.plan.g * 65 * sizeof(float);
         hop_sparse_kernel<kHop0, kLast><<<(unsigned)(a.units * a.plan.tiles), kSparseThreads,
                                           shmem, stream>>>(a);

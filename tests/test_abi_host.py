@@ -86,15 +86,15 @@ def test_invalid_arguments_rejected_on_host(lib):
 
 
 def test_launch_counter_and_profiler_without_gpu(lib):
-    arr = (ctypes.c_int64 * 4)()
+    arr = (ctypes.c_int64 * 5)()
     lib.diffuser_launch_count.restype = ctypes.c_int64
     before = lib.diffuser_launch_count(arr)
     assert before == sum(arr)
     assert lib.diffuser_profile_begin() == 0
     assert lib.diffuser_profile_begin() == 1     # one profile at a time
-    ms = (ctypes.c_double * 4)()
-    cnt = (ctypes.c_int64 * 4)()
+    ms = (ctypes.c_double * 5)()
+    cnt = (ctypes.c_int64 * 5)()
     assert lib.diffuser_profile_end(ms, cnt) == 0
-    assert list(cnt) == [0, 0, 0, 0]
+    assert list(cnt) == [0, 0, 0, 0, 0]
     assert lib.diffuser_profile_end(ms, cnt) == 1
     assert lib.diffuser_launch_count(None) == before   # failed calls launched nothing
