@@ -211,31 +211,45 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
         const int quad = warp & 3, hcol = warp >> 2;
         const int t = quad * 32 + lane;          // row within the tile
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const int total = my_tiles * chunks;
+        // this thread's four 16-byte pieces inside a stage (row t, columns 16 hcol ..)
         const uint32_t slot0 = ptx::smem_u32(sA) + t * 128;
-        auto issue = [&](int gx) {
-            if (gx < total) {
-                const int lx = gx / chunks, cx = gx - lx * chunks;
-                const int64_t tix = blockIdx.x + (int64_t)lx * gridDim.x;
-                const int64_t u = tix / P.tiles;
-                const int64_t i = (tix - u * P.tiles) * kTileRows + t;
-                const bool in_rows = i < P.n;
-                const float* rowp = a.A_band + (size_t)u * (P.band_unit / 4) +
-                                    (size_t)(in_rows ? i : 0) * P.W;
-                // window column of this thread's first key in the chunk
-                const int w0 = kChunkKeys * cx + 16 * hcol - 4 * (t / 4);
-                const uint32_t dst = slot0 + (uint32_t)((gx % kAStages) * kAStageBytes);
+        uint32_t piece_off[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) piece_off[q] = (uint32_t)(((4 * hcol + q) ^ (t & 7)) << 4);
+        const int wbase = 16 * hcol - 4 * (t / 4);   // window column of the thread's first key, chunk 0
+        // copy cursor: chunk (cl, cc) of this CTA's tile sequence, advanced one chunk per refill
+        int cl = 0, cc = 0, cslot = 0;
+        const float* crow = nullptr;
+        bool crow_ok = false;
+        auto set_row = [&](int lx) {
+            const int64_t tix = blockIdx.x + (int64_t)lx * gridDim.x;
+            const int64_t u = tix / P.tiles;
+            const int64_t i = (tix - u * P.tiles) * kTileRows + t;
+            crow_ok = i < P.n;
+            crow = a.A_band + (size_t)u * (P.band_unit / 4) + (size_t)(crow_ok ? i : 0) * P.W;
+        };
+        auto issue = [&]() {
+            if (cl < my_tiles) {
+                const int w0 = wbase + kChunkKeys * cc;
+                const uint32_t dst = slot0 + (uint32_t)(cslot * kAStageBytes);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int w = w0 + 4 * q;
-                    const bool ok = in_rows && w >= 0 && w < P.W;
-                    ptx::cp_async16(dst + (((4 * hcol + q) ^ (t & 7)) << 4), ok ? rowp + w : rowp,
-                                    ok ? 16 : 0);
+                    const bool ok = crow_ok && w >= 0 && w < P.W;
+                    ptx::cp_async16(dst + piece_off[q], ok ? crow + w : crow, ok ? 16 : 0);
                 }
+                if (++cc == chunks) {
+                    cc = 0;
+                    if (++cl < my_tiles) set_row(cl);
+                }
+                if (++cslot == kAStages) cslot = 0;
             }
             ptx::cp_async_commit();
         };
-        for (int gx = 0; gx < kAStages; ++gx) issue(gx);
+        if (my_tiles > 0) set_row(0);
+        for (int gx = 0; gx < kAStages; ++gx) issue();
+        int rslot = 0, ta = 0;                   // smem slot and TMEM stage of chunk gc
+        int gc = 0;
         for (int lt = 0; lt < my_tiles; ++lt) {
             const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
             const int64_t u = tix / P.tiles;
@@ -244,27 +258,26 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
             const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
             const int64_t lo_key = i - P.r < 0 ? 0 : i - P.r;
             const int64_t hi_key = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
-            // first absolute key of this thread's columns in chunk 0
-            const int64_t jt = i0 - P.r_up + 16 * hcol;
-            for (int c = 0; c < chunks; ++c) {
-                const int gc = lt * chunks + c;
-                const int ta = gc % kTStages;
+            // keys of this thread's columns relative to lo_key / hi_key, chunk 0
+            const int jrel_lo = (int)(i0 - P.r_up + 16 * hcol - lo_key);
+            const int jrel_hi = (int)(hi_key - (i0 - P.r_up + 16 * hcol));
+            for (int c = 0; c < chunks; ++c, ++gc) {
                 ptx::cp_async_wait<kAStages - 1>();
                 float hi[16], lo[16];
-                const uint8_t* rowp = sA + (gc % kAStages) * kAStageBytes + t * 128;
+                const uint8_t* rowp = sA + rslot * kAStageBytes + t * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float4 x = *reinterpret_cast<const float4*>(rowp + (((4 * hcol + q) ^ (t & 7)) << 4));
+                    const float4 x = *reinterpret_cast<const float4*>(rowp + piece_off[q]);
                     hi[4 * q + 0] = x.x; hi[4 * q + 1] = x.y; hi[4 * q + 2] = x.z; hi[4 * q + 3] = x.w;
                 }
-                const int64_t j0 = jt + kChunkKeys * c;
-                if (!(row_ok && j0 >= lo_key && j0 + 15 <= hi_key)) {
+                // first key of the segment minus lo_key, and hi_key minus it
+                const int d_lo = jrel_lo + kChunkKeys * c;
+                const int d_hi = jrel_hi - kChunkKeys * c;
+                if (!(row_ok && d_lo >= 0 && d_hi >= 15)) {
                     // partly (or not at all) inside the row's window
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int64_t j = j0 + k;
-                        hi[k] = (row_ok && j >= lo_key && j <= hi_key) ? hi[k] : 0.f;
-                    }
+                    for (int k = 0; k < 16; ++k)
+                        hi[k] = (row_ok && d_lo + k >= 0 && k <= d_hi) ? hi[k] : 0.f;
                 }
 #pragma unroll
                 for (int k = 0; k < 16; ++k) lo[k] = hi[k] - tf32_trunc(hi[k]);
@@ -275,7 +288,9 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZt, const __grid_constant_
                 ptx::tmem_st16x2(col, hi, col + 32, lo);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&full_tA[ta]);
-                issue(gc + kAStages);            // refill this slot (its data are in TMEM now)
+                issue();                         // refill the slot just read (its data are in TMEM now)
+                if (++rslot == kAStages) rslot = 0;
+                if (++ta == kTStages) ta = 0;
             }
         }
         ptx::cp_async_wait<0>();
