@@ -6,14 +6,22 @@
 // aggregate K times).  The weights are stored unnormalized, e_ij =
 // exp(s_ij - m_i), together with inv_l_i = 1 / sum_j e_ij, so that
 // A_ij = e_ij * inv_l_i ("1.2.1 Static sparsity", eq 3):
-//   band   [rows4][W]  row i, column w <-> key j = 4*floor(i/4) - r_up + w;
-//                      e_ij for |i-j| <= r, 0 <= j < n (other entries are masked)
+//   band   [tiles][chunks][hi | lo][128 rows x 64 keys] bf16: tile T holds
+//                      rows 128 T .. +127 against keys of the chunk grid
+//                      jb + 64 c + k, jb = 128 T - r64, as the exact
+//                      shared-memory image of the tensor-core A operand
+//                      (K-major, 128-byte swizzle: row t at 1024 (t / 8) +
+//                      128 (t % 8), 16-byte slot q at q ^ (t % 8)); e_ij =
+//                      hi + lo (hi = e rounded to bf16, lo = the remainder
+//                      rounded to bf16) for |i-j| <= r, 0 <= j < n, else 0
 //   gcol   [n][g_pad]  slot s <-> key G[s]: e for globals outside row i's window, else 0
 //   extra  [nx]        e of the random edges outside window and G, CSR order
 //   inv_l  [n]         per-row normalizer of the rows not in G
 //   grow   [g][n]      the global rows' weights A_ij (raw scores until the
 //                      band score kernel normalizes them with
 //   gstat  [g][2]      their (row max, 1 / row sum of exp(s - max)))
+// The hop state Z_k is kept as [n][hi 64 | lo 64] bf16 rows (Z = hi + lo),
+// the B operand of the band MMA and the source of the row gathers alike.
 #pragma once
 
 #include <cuda.h>
@@ -29,6 +37,9 @@ namespace dfs {
 namespace band {
 
 constexpr int kTileRows = 128;
+constexpr int kChunkKeys = 64;
+constexpr int kChunkPlaneBytes = kTileRows * kChunkKeys * 2;      // one bf16 plane of a chunk
+constexpr int kChunkImageBytes = 2 * kChunkPlaneBytes;            // hi + lo
 
 __device__ __forceinline__ float tf32_trunc(float x) {
     return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
@@ -38,7 +49,7 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 
 // Pointers into the band layout of the workspace (see plan_band_layout).
 struct Weights {
-    float* A_band;     // units x band_unit bytes
+    __nv_bfloat16* A_band;   // units x band_unit bytes
     float* A_gc;       // [units][n][g_pad]
     float* A_x;        // [units][nx]
     float* A_gr;       // [units][g][n] global-row weights (raw scores before normalization)

@@ -11,7 +11,8 @@
 //  * score_band_tc_kernel (tcgen05, persistent): S = Q K^T for a 128-row
 //    tile against 64-key chunks of its window on bf16 tensor cores (fp32
 //    accumulation in TMEM), in two passes over the chunks: the row maximum,
-//    then e = exp(s - m) written into the band storage with the row sum; the
+//    then e = exp(s - m) written into the band storage as a bf16 hi / lo
+//    pair (zero outside the row's window) with the row sum; the
 //    row threads then turn the row's sparse raw scores into e and store
 //    inv_l = 1 / (band sum + sparse sum).
 #include <cuda.h>
@@ -222,7 +223,7 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nc = (124 + P.W + kSChunk - 1) / kSChunk;  // chunks covering every stored window
+    const int nc = P.chunks;                              // the tile's key chunks (from i0 - r64)
     const int per_tile = 2 * nc;                          // pass 1 (max), pass 2 (exp + write)
     const int64_t total_tiles = a.units * P.tiles;
     const int my_tiles = blockIdx.x < total_tiles
@@ -246,7 +247,7 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
                 const int64_t u = tix / P.tiles;
                 const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-                const int64_t jb = i0 - P.r_up;
+                const int64_t jb = i0 - P.r64;
                 const int qb = lt & 1;
                 if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, status);
                 ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
@@ -322,13 +323,16 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
             const int64_t u = tix / P.tiles;
             const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-            const int64_t jb = i0 - P.r_up;
+            const int64_t jb = i0 - P.r64;
             const int64_t i = i0 + t;
             const bool row_ok = i < P.n && !a.gr.is_global[i < P.n ? i : 0];
             const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
             const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
-            float* brow = a.w.A_band + (size_t)u * (P.band_unit / 4) + (size_t)(row_ok ? i : 0) * P.W;
-            const int wshift = 4 * (t / 4);       // window start of row i minus jb
+            // this tile's weight image; row t of a chunk's plane sits at
+            // 1024 (t / 8) + 128 (t % 8), 16-byte slot q of the row at q ^ (t % 8)
+            uint8_t* timg = reinterpret_cast<uint8_t*>(a.w.A_band) +
+                            (size_t)(u * P.tiles + (i0 / kTileRows)) * P.chunks * band::kChunkImageBytes +
+                            (t >> 3) * 1024 + (t & 7) * 128;
             float mraw = -INFINITY;               // max of the raw dot products q.k (unscaled)
             float m = 0.f, b2 = 0.f, lsum = 0.f;
             for (int it = 0; it < per_tile; ++it) {
@@ -379,13 +383,23 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                             lsum += e[k];
                         }
                     }
-                    const int w0 = kSChunk * c + 32 * hcol - wshift;   // multiple of 4
+                    uint8_t* cimg = timg + (size_t)c * band::kChunkImageBytes;
 #pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4) {
-                        const int w = w0 + 4 * k4;
-                        if (w >= 0 && w < P.W)
-                            *reinterpret_cast<float4*>(brow + w) =
-                                make_float4(e[4 * k4], e[4 * k4 + 1], e[4 * k4 + 2], e[4 * k4 + 3]);
+                    for (int k8 = 0; k8 < 4; ++k8) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int p2 = 0; p2 < 4; ++p2) {
+                            const float x0 = e[8 * k8 + 2 * p2], x1 = e[8 * k8 + 2 * p2 + 1];
+                            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                            const __nv_bfloat162 l =
+                                __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+                            hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
+                            lw[p2] = *reinterpret_cast<const uint32_t*>(&l);
+                        }
+                        const int slot = ((4 * hcol + k8) ^ (t & 7)) << 4;
+                        *reinterpret_cast<uint4*>(cimg + slot) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(cimg + band::kChunkPlaneBytes + slot) =
+                            make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
                 }
             }
@@ -436,9 +450,12 @@ band_to_csr_kernel(ScoreArgs a, const int64_t* __restrict__ row_ptr,
     }
     const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
     const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
-    const int64_t ws = 4 * (i / 4) - P.r_up;
+    const int64_t tile = i / kTileRows, t = i - tile * kTileRows;
+    const int64_t jb = tile * kTileRows - P.r64;       // first key of the tile's chunk grid
     const float inv = a.w.inv_l[(size_t)u * P.n + i];
-    const float* Ab = a.w.A_band + (size_t)u * (P.band_unit / 4) + (size_t)i * P.W;
+    const uint8_t* timg = reinterpret_cast<const uint8_t*>(a.w.A_band) +
+                          (size_t)(u * P.tiles + tile) * P.chunks * band::kChunkImageBytes +
+                          (t >> 3) * 1024 + (t & 7) * 128;
     const float* Agc = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
     const float* Ax = a.w.A_x + (size_t)u * a.gr.nx;
     int64_t xb = a.gr.x_ptr[i];
@@ -451,7 +468,13 @@ band_to_csr_kernel(ScoreArgs a, const int64_t* __restrict__ row_ptr,
         const int rank = __popc(mask & ((1u << lane) - 1));
         if (e < e1) {
             float v;
-            if (j >= lo && j <= hi) v = Ab[j - ws];
+            if (j >= lo && j <= hi) {
+                const int64_t kk = j - jb;
+                const uint8_t* pe = timg + (size_t)(kk >> 6) * band::kChunkImageBytes +
+                                    ((((kk & 63) >> 3) ^ (t & 7)) << 4) + (kk & 7) * 2;
+                v = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(pe)) +
+                    __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(pe + band::kChunkPlaneBytes));
+            }
             else if (a.gr.is_global[j]) v = Agc[a.gr.gslot[j]];
             else v = Ax[xb + rank];
             o[e] = v * inv;

@@ -24,21 +24,22 @@ enum GraphKind { kTokenGraph = 0, kBlockGraph = 1 };
 // Geometry of the band path's decomposed weight layout (token graphs).
 struct BandPlan {
     int64_t n;          // sequence length
-    int32_t r, r_up;    // window radius, and the radius rounded up to a multiple of 4
-    int32_t W;          // stored window width per row (multiple of 4, covers 2r+1 keys)
+    int32_t r;          // window radius
+    int32_t r64;        // the radius rounded up to a multiple of 64 (start of a tile's key chunks)
     int32_t g, g_pad;   // number of globals, padded to a multiple of 4
-    int64_t rows4;      // n rounded up to a multiple of 4
-    int64_t nz;         // key stride of the transposed Z planes (multiple of 4)
     int32_t tiles;      // 128-row tiles per unit
-    int32_t chunks;     // 32-key chunks per tile
-    size_t band_unit;   // bytes of one unit's band weights (with slack at the end)
+    int32_t chunks;     // 64-key chunks per tile
+    int32_t gchunks;    // key chunks of the global-row reduction per unit
+    size_t band_unit;   // bytes of one unit's band weights (tiles x chunks x 32 KB)
 };
 
 // Byte offsets of the band path's workspace regions.
 struct BandLayout {
     size_t a_band, a_gc, a_x, a_gr;
-    size_t zr[2], zt[2], ztl[2];
-    size_t gpart, psum, inv_l, m_sparse, gstat, sstat, counters, total;
+    size_t z[2];        // hop state Z_k, [units][n][hi 64 | lo 64] bf16, ping-pong
+    size_t zf[2];       // the same Z_k as fp32 rows [units][n][64] (row gathers)
+    size_t psum;        // sparse partial of the rows not in G, [units][n][64] fp32
+    size_t gpart, inv_l, m_sparse, gstat, sstat, counters, total;
 };
 
 }  // namespace dfs

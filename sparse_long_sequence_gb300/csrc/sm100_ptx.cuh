@@ -92,6 +92,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Contiguous global -> shared copy by the bulk-copy engine (no tensor map);
+// addresses 16-byte aligned, size a multiple of 16; completes on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---- cp.async (16-byte global -> shared copies; src_bytes 0 writes zeros) ----
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -143,11 +153,37 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor: MN-major, 128-byte swizzle.  Each K row
+// holds 64 consecutive 16-bit MN elements (128 bytes); 8 K rows form a
+// 1024-byte swizzle atom, K atoms are 1024 bytes apart, and the next 64 MN
+// elements start `mn_atom_bytes` further on.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t mn_atom_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((mn_atom_bytes >> 4) & 0x3FFF) << 16;   // leading byte offset: next MN atom
+    d |= (uint64_t)(1024 >> 4) << 32;                        // stride byte offset: next 8 K rows
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Instruction descriptor: D fp32, A and B of `ab_format` (1 = bf16, 2 = tf32),
 // both K-major, M = 128, N = n.
 __host__ __device__ constexpr uint32_t mma_idesc(uint32_t ab_format, uint32_t n) {
     return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((n >> 3) << 17) |
            ((128u >> 4) << 24);
+}
+
+// Instruction descriptor: D fp32, bf16 A (K-major) and B (MN-major), M = 128, N = n.
+__host__ __device__ constexpr uint32_t mma_idesc_bf16_bmn(uint32_t n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((n >> 3) << 17) |
+           ((128u >> 4) << 24);
+}
+
+// Orders this thread's completed generic-proxy shared-memory writes (for
+// example cp.async results) before later async-proxy reads (tcgen05.mma).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem], kind::tf32
