@@ -20,6 +20,10 @@
 //   grow   [g][n]      the global rows' weights A_ij (raw scores until the
 //                      band score kernel normalizes them with
 //   gstat  [g][2]      their (row max, 1 / row sum of exp(s - max)))
+//   gimg   [tiles][2][hi | lo][32 rows x 64 keys] bf16: the normalized
+//                      global-row weights of tile T's own keys 128 T .. +127
+//                      (two 64-key halves), as the tensor-core A operand
+//                      image (rows s < g; keys past n are 0)
 // The hop state Z_k is kept as [n][hi 64 | lo 64] bf16 rows (Z = hi + lo),
 // the B operand of the band MMA and the source of the row gathers alike.
 #pragma once
@@ -40,6 +44,9 @@ constexpr int kTileRows = 128;
 constexpr int kChunkKeys = 64;
 constexpr int kChunkPlaneBytes = kTileRows * kChunkKeys * 2;      // one bf16 plane of a chunk
 constexpr int kChunkImageBytes = 2 * kChunkPlaneBytes;            // hi + lo
+constexpr int kGImgRows = 32;                                      // the global rows' operand rows
+constexpr int kGImgPlaneBytes = kGImgRows * kChunkKeys * 2;        // 4 KB
+constexpr int kGImgBytes = 2 * 2 * kGImgPlaneBytes;                // 2 halves x (hi, lo): 16 KB
 
 __device__ __forceinline__ float tf32_trunc(float x) {
     return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
@@ -53,6 +60,7 @@ struct Weights {
     float* A_gc;       // [units][n][g_pad]
     float* A_x;        // [units][nx]
     float* A_gr;       // [units][g][n] global-row weights (raw scores before normalization)
+    uint8_t* A_gimg;   // [units][tiles] global-row weight images (kGImgBytes each)
     float* inv_l;      // [units][n]
     float* m_sparse;   // [units][n] max raw score over a row's gcol + extras
     float* gstat;      // [units][g][2]

@@ -10,7 +10,6 @@
 //            gathered from L2).  Each quarter-warp walks the extras of 4
 //            consecutive rows as one stream with many rows in flight; every
 //            load instruction reads whole 128-byte lines.
-//   hop_global_kernel: the global rows (full rows of A).
 //   hop_band_kernel (persistent, 128-row tiles): tcgen05 MMA, M = 128 rows,
 //            K = 64 keys per chunk, bf16 operands split into hi + lo (each the
 //            bf16 rounding of what is left): e_hi*[Z_hi | Z_lo] (N = 128) +
@@ -18,7 +17,13 @@
 //            (below 2^-16 of the product) is the only one left out.  The
 //            score kernel stores each chunk's A tile as the exact shared-memory
 //            image of the operand, so a chunk is two 16 KB bulk copies; the
-//            Z_k rows come by TMA as the MN-major B operand.  Epilogue:
+//            Z_k rows come by TMA as the MN-major B operand.  The global rows
+//            (full rows of A) ride along: on the two chunks that hold the
+//            tile's own keys, the same Z_k tiles also multiply the global rows'
+//            weights of those keys (a 32-row operand image) into a second
+//            accumulator; each tile writes that share, and
+//            hop_global_rows_kernel sums the shares in tile order and writes
+//            the rows.  Epilogue:
 //            z_i = (1 - alpha) * inv_l_i * (band_i + P_i) + alpha * V_i,
 //            written as the next [hi | lo] bf16 row and fp32 row, or as the
 //            bf16 output.
@@ -46,15 +51,18 @@ using band::kTileRows;
 // One CTA per SM (its shared memory alone rules out a second one).
 constexpr int kThreads = 384;
 constexpr int kTmaWarp = 0, kMmaWarp = 1, kEpiWarp0 = 4, kEpiThreads = 256;
-constexpr int kAStages = 5;              // A ring: hi tile + lo tile, 32 KB per stage
-constexpr int kZStages = 3;              // Z ring: hi tile + lo tile, 16 KB per stage
+constexpr int kAStages = 4;              // A ring: hi tile + lo tile, 32 KB per stage
+constexpr int kZStages = 4;              // Z ring: hi tile + lo tile, 16 KB per stage
 constexpr int kAccCols = 128;            // one accumulator: columns [0,64) A Z_hi, [64,128) A_hi Z_lo
-constexpr int kTmemCols = 256;           // two accumulators (double-buffered tiles)
+constexpr int kGlobCol0 = 256;           // the global rows' accumulators: columns 256 + 128 (lt & 1)
+constexpr int kTmemCols = 512;           // band and global accumulators, double-buffered tiles
 constexpr int kATileBytes = band::kChunkPlaneBytes;
 constexpr int kAStageBytes = 2 * kATileBytes;
 constexpr int kZTileBytes = kChunkKeys * 128;
 constexpr int kZStageBytes = 2 * kZTileBytes;
-constexpr int kSmemBytes = 1024 + kAStages * kAStageBytes + kZStages * kZStageBytes + 256;
+// the global rows' operand image comes first: its descriptors span 16 KB past
+// their start (rows 32..127 read whatever follows; those rows are not used)
+constexpr int kSmemBytes = 1024 + band::kGImgBytes + kAStages * kAStageBytes + kZStages * kZStageBytes + 256;
 static_assert(kSmemBytes > 116 * 1024, "must exclude a second CTA per SM");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
@@ -69,7 +77,7 @@ struct HopArgs {
     int64_t nx;
     const float* A_gc;
     const float* A_x;
-    const float* A_gr;    // normalized global-row weights [units][g][n]
+    const uint8_t* A_gimg;       // global-row weight images [units][tiles] (kGImgBytes each)
     const float* inv_l;   // [units][n]
     const __nv_bfloat16* V;
     const __nv_bfloat16* A_band; // the tiles' A images [units][tiles][chunks][hi | lo]
@@ -78,7 +86,7 @@ struct HopArgs {
     float* Zf_out;               // Z_{k+1} as fp32 rows [n][64], all hops but the last
     __nv_bfloat16* out;          // the last hop's output [n][64]
     float* Psum;                 // [units][n][64] sparse partial of the rows not in G
-    float* gpart;                // [units][gchunks][g][64]
+    float* gpart;                // [units][tiles][g][64]
     int* counters;               // [units]
     int* status;
 };
@@ -131,6 +139,65 @@ __device__ __forceinline__ uint4 pack8(const float* z) {
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
+// Z_{k+1} of global row s from the shares sum_j A_gr[s][j] Z_k[j] of every tile
+// (summed in tile order): written as the next [hi | lo] bf16 and fp32 rows, or
+// as the bf16 output.  Threads (s, features 4 fq .. +3).
+template <bool kLast>
+__device__ void finish_global_rows(const HopArgs& a, int64_t u, int tid, int nthreads) {
+    const BandPlan& P = a.plan;
+    const int g = P.g;
+    const float keep = 1.f - a.alpha;
+    const size_t tstride = (size_t)g * (kHeadDim / 4);
+    for (int e = tid; e < g * 16; e += nthreads) {
+        const int s = e >> 4, fq = e & 15;
+        const float4* src = reinterpret_cast<const float4*>(a.gpart) +
+                            ((size_t)u * P.tiles * g + s) * (kHeadDim / 4) + fq;
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < P.tiles; c0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+                v[b] = c0 + b < P.tiles ? __ldcg(src + (size_t)(c0 + b) * tstride)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                sum.x += v[b].x; sum.y += v[b].y; sum.z += v[b].z; sum.w += v[b].w;
+            }
+        }
+        const int64_t gi = a.globals[s];
+        const size_t vrow = ((size_t)u * P.n + gi) * kHeadDim + 4 * fq;
+        const uint2 vv = __ldg(reinterpret_cast<const uint2*>(a.V + vrow));
+        float z[4] = {fmaf(keep, sum.x, a.alpha * bf16lo(vv.x)), fmaf(keep, sum.y, a.alpha * bf16hi(vv.x)),
+                      fmaf(keep, sum.z, a.alpha * bf16lo(vv.y)), fmaf(keep, sum.w, a.alpha * bf16hi(vv.y))};
+        if (kLast) {
+            const __nv_bfloat162 h0 = __floats2bfloat162_rn(z[0], z[1]);
+            const __nv_bfloat162 h1 = __floats2bfloat162_rn(z[2], z[3]);
+            *reinterpret_cast<uint2*>(a.out + vrow) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+        } else {
+            uint32_t hw[2], lw[2];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const __nv_bfloat162 hh = __floats2bfloat162_rn(z[2 * p], z[2 * p + 1]);
+                const __nv_bfloat162 ll =
+                    __floats2bfloat162_rn(z[2 * p] - __low2float(hh), z[2 * p + 1] - __high2float(hh));
+                hw[p] = *reinterpret_cast<const uint32_t*>(&hh);
+                lw[p] = *reinterpret_cast<const uint32_t*>(&ll);
+            }
+            __nv_bfloat16* zr = a.Z_out + ((size_t)u * P.n + gi) * (2 * kHeadDim) + 4 * fq;
+            *reinterpret_cast<uint2*>(zr) = make_uint2(hw[0], hw[1]);
+            *reinterpret_cast<uint2*>(zr + kHeadDim) = make_uint2(lw[0], lw[1]);
+            *reinterpret_cast<float4*>(a.Zf_out + vrow) = make_float4(z[0], z[1], z[2], z[3]);
+        }
+    }
+}
+
+// one CTA per unit: the global rows of Z_{k+1}
+template <bool kLast>
+__global__ void __launch_bounds__(256) hop_global_rows_kernel(HopArgs a) {
+    finish_global_rows<kLast>(a, blockIdx.x, threadIdx.x, blockDim.x);
+}
+
 // ---------------------------------------------------------------- band part of a hop
 template <bool kHop0, bool kLast>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -138,7 +205,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint8_t* sA = smem;                                          // kAStages x (hi 16 KB, lo 16 KB)
+    uint8_t* sGA = smem;                                         // global rows: 2 halves x (hi, lo) 4 KB
+    uint8_t* sA = sGA + band::kGImgBytes;                        // kAStages x (hi 16 KB, lo 16 KB)
     uint8_t* sZ = sA + kAStages * kAStageBytes;                  // kZStages x (hi 8 KB, lo 8 KB)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sZ + kZStages * kZStageBytes);
     uint64_t* full_A = bars;
@@ -147,11 +215,15 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
     uint64_t* empty_Z = full_Z + kZStages;
     uint64_t* acc_full = empty_Z + kZStages;                     // [2]
     uint64_t* acc_empty = acc_full + 2;                          // [2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* full_G = acc_empty + 2;
+    uint64_t* empty_G = full_G + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_G + 1);
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunks = P.chunks;
+    const int c0 = P.r64 / kChunkKeys;           // chunks c0 and c0 + 1 hold the tile's own keys
+    const bool has_g = P.g > 0;
     const int64_t total_tiles = a.units * P.tiles;
     // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
     const int my_tiles = blockIdx.x < total_tiles
@@ -162,6 +234,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
         for (int s = 0; s < kAStages; ++s) { ptx::mbar_init(&full_A[s], 1); ptx::mbar_init(&empty_A[s], 1); }
         for (int s = 0; s < kZStages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
         for (int s = 0; s < 2; ++s) { ptx::mbar_init(&acc_full[s], 1); ptx::mbar_init(&acc_empty[s], kEpiThreads); }
+        ptx::mbar_init(full_G, 1);
+        ptx::mbar_init(empty_G, 1);
         ptx::fence_mbar_init();
     }
     if (warp == kTmaWarp && lane == 0) ptx::prefetch_tensormap(&tmZ);
@@ -174,6 +248,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
         // ---------------- TMA producer.  The chunk grid of a tile starts at key
         // jb = i0 - r64; chunk c's A tile is one contiguous image (hi, lo).
         if (lane == 0) {
+            // the weights are read once per hop; Z_k is re-read by neighbouring tiles
+            const uint64_t pol_a = ptx::l2_evict_first(), pol_z = ptx::l2_evict_last();
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
                 const int64_t u = tix / P.tiles;
@@ -181,6 +257,12 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                 const int64_t jb = i0 - P.r64;
                 const uint8_t* timg = reinterpret_cast<const uint8_t*>(a.A_band) +
                                       (size_t)tix * chunks * band::kChunkImageBytes;
+                if (has_g) {
+                    if (lt >= 1) ptx::mbar_wait(empty_G, (lt - 1) & 1, a.status);
+                    ptx::mbar_arrive_expect_tx(full_G, band::kGImgBytes);
+                    ptx::bulk_load_hint(sGA, a.A_gimg + (size_t)tix * band::kGImgBytes, band::kGImgBytes,
+                                        full_G, pol_a);
+                }
                 for (int c = 0; c < chunks; ++c) {
                     const int gc = lt * chunks + c;
                     const int sa = gc % kAStages;
@@ -188,15 +270,16 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                     ptx::mbar_arrive_expect_tx(&full_A[sa], kAStageBytes);
                     uint8_t* adst = sA + sa * kAStageBytes;
                     const uint8_t* asrc = timg + (size_t)c * band::kChunkImageBytes;
-                    ptx::bulk_load(adst, asrc, kATileBytes, &full_A[sa]);
-                    ptx::bulk_load(adst + kATileBytes, asrc + kATileBytes, kATileBytes, &full_A[sa]);
+                    ptx::bulk_load_hint(adst, asrc, kATileBytes, &full_A[sa], pol_a);
+                    ptx::bulk_load_hint(adst + kATileBytes, asrc + kATileBytes, kATileBytes, &full_A[sa], pol_a);
                     const int sz = gc % kZStages;
                     if (gc >= kZStages) ptx::mbar_wait(&empty_Z[sz], ((gc / kZStages) - 1) & 1, a.status);
                     uint8_t* zdst = sZ + sz * kZStageBytes;
                     ptx::mbar_arrive_expect_tx(&full_Z[sz], kHop0 ? kZTileBytes : 2 * kZTileBytes);
                     const int key = (int)(jb + kChunkKeys * c);
-                    ptx::tma_load_3d(zdst, &tmZ, &full_Z[sz], 0, key, (int)u);
-                    if (!kHop0) ptx::tma_load_3d(zdst + kZTileBytes, &tmZ, &full_Z[sz], kHeadDim, key, (int)u);
+                    ptx::tma_load_3d_hint(zdst, &tmZ, &full_Z[sz], 0, key, (int)u, pol_z);
+                    if (!kHop0)
+                        ptx::tma_load_3d_hint(zdst + kZTileBytes, &tmZ, &full_Z[sz], kHeadDim, key, (int)u, pol_z);
                 }
             }
         }
@@ -226,6 +309,25 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                                          kHop0 ? idesc64 : idesc128, (c | ks) != 0);
                         ptx::mma_bf16_ss(dacc, ptx::sw128_kmajor_desc(alo + 32 * ks), bdesc, idesc64, 1);
                     }
+                    const int h = c - c0;
+                    if (has_g && (h == 0 || h == 1)) {
+                        // the global rows x this tile's own keys (same Z_k tile)
+                        if (h == 0) {
+                            ptx::mbar_wait(full_G, lt & 1, a.status);
+                            ptx::tc_fence_after();
+                        }
+                        const uint32_t dglob = tmem + kGlobCol0 + kAccCols * ab;
+                        const uint32_t ghi = ptx::smem_u32(sGA + h * 2 * band::kGImgPlaneBytes);
+                        const uint32_t glo = ghi + band::kGImgPlaneBytes;
+#pragma unroll
+                        for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
+                            const uint64_t bdesc = ptx::sw128_mnmajor_desc(zb + 2048 * ks, kZTileBytes);
+                            ptx::mma_bf16_ss(dglob, ptx::sw128_kmajor_desc(ghi + 32 * ks), bdesc,
+                                             kHop0 ? idesc64 : idesc128, (h | ks) != 0);
+                            ptx::mma_bf16_ss(dglob, ptx::sw128_kmajor_desc(glo + 32 * ks), bdesc, idesc64, 1);
+                        }
+                        if (h == 1) ptx::mma_commit(empty_G);
+                    }
                     ptx::mma_commit(&empty_A[sa]);
                     ptx::mma_commit(&empty_Z[sz]);
                 }
@@ -243,6 +345,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                 const int uses = (total - s + kZStages - 1) / kZStages;
                 if (uses > 0) ptx::mbar_wait(&empty_Z[s], (uses - 1) & 1, a.status);
             }
+            if (has_g && my_tiles > 0) ptx::mbar_wait(empty_G, (my_tiles - 1) & 1, a.status);
         }
     } else if (warp >= kEpiWarp0) {
         // ---------------- epilogue: thread <-> row t = 32 quad + lane, features 32 fhalf .. +31
@@ -273,6 +376,25 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
             ptx::mbar_wait(&acc_full[ab], (lt / 2) & 1, a.status);
             __syncwarp();       // reconverge before the warp-collective tcgen05.ld
             ptx::tc_fence_after();
+            if (has_g && quad == 0) {
+                // TMEM lanes 0..31 of the global accumulator are the global slots s:
+                // this tile's share of the global rows (hop_global_rows_kernel sums them)
+                float gd[32];
+                ptx::tmem_ld32(tmem + kGlobCol0 + kAccCols * ab + 32 * fhalf, gd);
+                if (!kHop0) {
+                    float g2[32];
+                    ptx::tmem_ld32(tmem + kGlobCol0 + kAccCols * ab + kHeadDim + 32 * fhalf, g2);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) gd[k] += g2[k];
+                }
+                if (lane < P.g) {
+                    float4* gp = reinterpret_cast<float4*>(
+                        a.gpart + (((size_t)u * P.tiles + (i0 / kTileRows)) * P.g + lane) * kHeadDim + 32 * fhalf);
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        gp[c4] = make_float4(gd[4 * c4], gd[4 * c4 + 1], gd[4 * c4 + 2], gd[4 * c4 + 3]);
+                }
+            }
             float d[32];
             ptx::tmem_ld32(tmem + lane_base + kAccCols * ab + 32 * fhalf, d);
             if (!kHop0) {
@@ -282,7 +404,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                 for (int k = 0; k < 32; ++k) d[k] += d2[k];
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&acc_empty[ab]);                    // the accumulator is in registers
+            ptx::mbar_arrive(&acc_empty[ab]);                    // the accumulators are in registers
             if (!row_ok) continue;
             float z[32];
 #pragma unroll
@@ -324,13 +446,13 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
 // ---------------------------------------------------------------- sparse part of a hop
 // Persistent over 128-row tiles, 8 warps.  Quarter-warp q of a tile owns rows
 // 4 q .. 4 q + 3, whose random extras are one contiguous stretch of the extras
-// list: it walks that stretch in batches of kGatherBatch slots (every slot's
-// Z_k row in flight at once, the next batch's (weight, column) prefetched), and
-// on leaving a row adds the row's out-of-window globals and writes P_i.
-// Lane l of a quarter owns features 4 l .. 4 l + 3 and 32 + 4 l .. 32 + 4 l + 3,
-// so each load instruction reads whole 128-byte lines of the gathered rows.
+// list: it walks that stretch in batches of kB slots (every slot's Z_k row in
+// flight at once; a slot past the end reads row 0 with weight 0), and on
+// leaving a row stores the row's sum in shared memory.  Then each row adds its
+// out-of-window globals and writes P_i.  Lane l of a quarter owns features
+// 4 l .. 4 l + 3 and 32 + 4 l .. 32 + 4 l + 3, so each load instruction reads
+// whole 128-byte lines of the gathered rows.
 constexpr int kGThreadsG = 256;
-constexpr int kGatherBatch = 8;
 
 template <bool kHop0>
 __device__ __forceinline__ void load_zrow(const HopArgs& a, size_t row, int ql, float4& z0, float4& z1) {
@@ -345,8 +467,8 @@ __device__ __forceinline__ void load_zrow(const HopArgs& a, size_t row, int ql, 
     }
 }
 
-template <bool kHop0>
-__global__ void __launch_bounds__(kGThreadsG, 2)
+template <bool kHop0, int kB, int kMinBlocks>
+__global__ void __launch_bounds__(kGThreadsG, kMinBlocks)
 hop_gather_kernel(HopArgs a) {
     __shared__ float4 sG[kBandMaxGlobals * 16];   // Z_k rows of the global keys (fp32)
     __shared__ float4 sR[32 * 4 * 16];            // [quarter][row][16]: the rows' extras sums
@@ -375,62 +497,48 @@ hop_gather_kernel(HopArgs a) {
         }
         const int64_t ib = i0 + 4 * qi;
         const int64_t rlim = P.n;
-        // extras of row ib + m: [b_m, b_{m+1})
+        // extras of row ib + m: [d_m, d_{m+1}) relative to the first
         const int64_t xb = a.x_ptr[ib < rlim ? ib : rlim];
-        const int64_t b1 = a.x_ptr[ib + 1 < rlim ? ib + 1 : rlim];
-        const int64_t b2 = a.x_ptr[ib + 2 < rlim ? ib + 2 : rlim];
-        const int64_t b3 = a.x_ptr[ib + 3 < rlim ? ib + 3 : rlim];
-        const int64_t xe = a.x_ptr[ib + 4 < rlim ? ib + 4 : rlim];
+        const int d1 = (int)(a.x_ptr[ib + 1 < rlim ? ib + 1 : rlim] - xb);
+        const int d2 = (int)(a.x_ptr[ib + 2 < rlim ? ib + 2 : rlim] - xb);
+        const int d3 = (int)(a.x_ptr[ib + 3 < rlim ? ib + 3 : rlim] - xb);
+        const int nslot = (int)(a.x_ptr[ib + 4 < rlim ? ib + 4 : rlim] - xb);
         const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < 4; ++m) { rq[m * 16 + ql] = zero4; rq[m * 16 + 8 + ql] = zero4; }
-        const float* ax = a.A_x + (size_t)u * a.nx;
+        const float* wq = a.A_x + (size_t)u * a.nx + xb;
+        const int32_t* jq = a.x_col + xb;
+        const size_t ubase = (size_t)u * P.n;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         int cur = 0;                              // row (0..3) being accumulated
-        constexpr int kIdx = (kGatherBatch + 7) / 8;
-        float wl[kIdx];
-        int32_t jl[kIdx];
-        auto load_idx = [&](int64_t base) {
+        for (int e0 = 0; e0 < nslot; e0 += kB) {
+            int32_t j[kB];
+            float w[kB];
 #pragma unroll
-            for (int k = 0; k < kIdx; ++k) {
-                const int64_t e = base + 8 * k + ql;
-                const bool ok = e < xe && 8 * k + ql < kGatherBatch;
-                wl[k] = ok ? __ldg(ax + e) : 0.f;
-                jl[k] = ok ? __ldg(a.x_col + e) : 0;
+            for (int b = 0; b < kB; ++b) {
+                const bool v = e0 + b < nslot;
+                j[b] = v ? __ldg(jq + e0 + b) : 0;
+                w[b] = v ? __ldg(wq + e0 + b) : 0.f;
             }
-        };
-        if (xb < xe) load_idx(xb);
-        for (int64_t base = xb; base < xe; base += kGatherBatch) {
-            const int cnt = xe - base < kGatherBatch ? (int)(xe - base) : kGatherBatch;
-            float4 z0[kGatherBatch], z1[kGatherBatch];
+            float4 z0[kB], z1[kB];
 #pragma unroll
-            for (int b = 0; b < kGatherBatch; ++b) {
-                const int32_t j = __shfl_sync(qmask, jl[b / 8], b % 8, 8);
-                if (b < cnt) load_zrow<kHop0>(a, (size_t)u * P.n + j, ql, z0[b], z1[b]);
-            }
-            float wc[kIdx];
+            for (int b = 0; b < kB; ++b) load_zrow<kHop0>(a, ubase + j[b], ql, z0[b], z1[b]);
 #pragma unroll
-            for (int k = 0; k < kIdx; ++k) wc[k] = wl[k];
-            if (base + kGatherBatch < xe) load_idx(base + kGatherBatch);
+            for (int b = 0; b < kB; ++b) {
+                const int e = e0 + b;
+                const int m = (e >= d1) + (e >= d2) + (e >= d3);
+                if (e < nslot && m != cur) {
+                    // each row's extras are one contiguous span: stash its sum once
+                    rq[cur * 16 + ql] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    rq[cur * 16 + 8 + ql] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 #pragma unroll
-            for (int b = 0; b < kGatherBatch; ++b) {
-                const float w = __shfl_sync(qmask, wc[b / 8], b % 8, 8);
-                if (b < cnt) {
-                    const int64_t e = base + b;
-                    const int m = (e >= b1) + (e >= b2) + (e >= b3);
-                    if (m != cur) {
-                        // each row's extras are one contiguous span: stash its sum once
-                        rq[cur * 16 + ql] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                        rq[cur * 16 + 8 + ql] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-                        cur = m;
-                    }
-                    fma8f(acc, w, z0[b], z1[b]);
+                    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+                    cur = m;
                 }
+                fma8f(acc, w[b], z0[b], z1[b]);    // w = 0 past the end
             }
         }
-        if (xb < xe) {
+        if (nslot > 0) {
             rq[cur * 16 + ql] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             rq[cur * 16 + 8 + ql] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
@@ -446,8 +554,8 @@ hop_gather_kernel(HopArgs a) {
                 const float wv = s0 + ql < g ? __ldg(wg + s0 + ql) : 0.f;
                 const int cnt = g - s0 < 8 ? g - s0 : 8;
                 for (int b = 0; b < cnt; ++b) {
-                    const float w = __shfl_sync(qmask, wv, b, 8);
-                    fma8f(v, w, sG[(s0 + b) * 16 + ql], sG[(s0 + b) * 16 + 8 + ql]);
+                    const float wb = __shfl_sync(qmask, wv, b, 8);
+                    fma8f(v, wb, sG[(s0 + b) * 16 + ql], sG[(s0 + b) * 16 + 8 + ql]);
                 }
             }
             float4* pr = reinterpret_cast<float4*>(a.Psum + ((size_t)u * P.n + i) * kHeadDim);
@@ -458,170 +566,8 @@ hop_gather_kernel(HopArgs a) {
     }
 }
 
-// ---------------------------------------------------------------- global rows of a hop
-// One CTA per (unit, chunk of kGChunk keys): the share sum_j A_gr[s][j] Z_k[j]
-// of its keys for every global row s (4 x 4 register blocks: 4 rows s x 4
-// features per thread, over a quarter of the keys); the last chunk of a unit
-// sums the shares in chunk order and writes Z_{k+1} of the global rows.
-constexpr int kGChunk = 256;
-constexpr int kGThreads = 256;
-constexpr int kGZStride = 68;            // floats per staged Z row
-constexpr int kGWStride = 36;            // floats per staged key of weights (up to 32 rows)
-constexpr int kGSmemFloats = kGChunk * kGZStride + kGChunk * kGWStride;
-
-template <bool kHop0, bool kLast>
-__global__ void __launch_bounds__(kGThreads)
-hop_global_kernel(HopArgs a) {
-    extern __shared__ float gsm[];           // [kGChunk][kGZStride] Z_k rows, [kGChunk][kGWStride] weights
-    __shared__ int ticket;
-    const BandPlan& P = a.plan;
-    const int tid = threadIdx.x;
-    const int64_t u = blockIdx.x / P.gchunks;
-    const int gch = (int)(blockIdx.x - u * P.gchunks);
-    const int64_t j0 = (int64_t)gch * kGChunk;
-    const int g = P.g;
-    float* sZr = gsm;
-    float* sW = gsm + kGChunk * kGZStride;
-    {
-        // thread t stages key j0 + t: its Z_k row (fp32) and its g weights
-        const int64_t j = j0 + tid;
-        float4* dst = reinterpret_cast<float4*>(sZr + tid * kGZStride);
-        if (j < P.n) {
-            const size_t row = (size_t)u * P.n + j;
-            if (kHop0) {
-                const uint4* zp = reinterpret_cast<const uint4*>(a.V + row * kHeadDim);
-#pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    const uint4 h = __ldg(zp + p);
-                    dst[2 * p] = make_float4(bf16lo(h.x), bf16hi(h.x), bf16lo(h.y), bf16hi(h.y));
-                    dst[2 * p + 1] = make_float4(bf16lo(h.z), bf16hi(h.z), bf16lo(h.w), bf16hi(h.w));
-                }
-            } else {
-                const float4* zp = reinterpret_cast<const float4*>(a.Zf_in + row * kHeadDim);
-                float4 v[16];
-#pragma unroll
-                for (int p = 0; p < 16; ++p) v[p] = __ldg(zp + p);
-#pragma unroll
-                for (int p = 0; p < 16; ++p) dst[p] = v[p];
-            }
-        } else {
-#pragma unroll
-            for (int p = 0; p < 16; ++p) dst[p] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        // the g weights of key j: 8 independent loads in flight, then the stores
-        float* wd = sW + tid * kGWStride;
-        const float* wsrc = a.A_gr + (size_t)u * g * P.n + j;
-        for (int s0 = 0; s0 < g; s0 += 8) {
-            float v[8];
-#pragma unroll
-            for (int b = 0; b < 8; ++b)
-                v[b] = (s0 + b < g && j < P.n) ? __ldg(wsrc + (size_t)(s0 + b) * P.n) : 0.f;
-#pragma unroll
-            for (int b = 0; b < 8; ++b) wd[s0 + b] = v[b];
-        }
-    }
-    __syncthreads();
-    // thread: key quarter kq, rows 4 sb .. +3 (sb += 4 while below g), features 4 fb .. +3
-    const int kq = tid >> 6, sb0 = (tid >> 4) & 3, fb = tid & 15;
-    float* part = a.gpart + ((size_t)u * P.gchunks + gch) * (size_t)g * kHeadDim;
-    float* red = gsm;                        // reused after the sums: [4][32][64]
-    // at most two row blocks per thread (g <= 32): sb0 and sb0 + 4
-    const bool has0 = 4 * sb0 < g, has1 = 4 * (sb0 + 4) < g;
-    float4 ac0[4], ac1[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) ac0[r] = ac1[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (has0) {
-        const int jb = kq * (kGChunk / 4);
-#pragma unroll 4
-        for (int jj = 0; jj < kGChunk / 4; ++jj) {
-            const float* wrow = sW + (jb + jj) * kGWStride;
-            const float4 z = *reinterpret_cast<const float4*>(sZr + (jb + jj) * kGZStride + 4 * fb);
-            const float4 w = *reinterpret_cast<const float4*>(wrow + 4 * sb0);
-            fma4(ac0[0], w.x, z);
-            fma4(ac0[1], w.y, z);
-            fma4(ac0[2], w.z, z);
-            fma4(ac0[3], w.w, z);
-            if (has1) {
-                const float4 w1 = *reinterpret_cast<const float4*>(wrow + 4 * sb0 + 16);
-                fma4(ac1[0], w1.x, z);
-                fma4(ac1[1], w1.y, z);
-                fma4(ac1[2], w1.z, z);
-                fma4(ac1[3], w1.w, z);
-            }
-        }
-    }
-    __syncthreads();                         // staged rows are no longer read
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        if (has0 && 4 * sb0 + r < g)
-            reinterpret_cast<float4*>(red + ((size_t)kq * 32 + 4 * sb0 + r) * kHeadDim)[fb] = ac0[r];
-        if (has1 && 4 * sb0 + 16 + r < g)
-            reinterpret_cast<float4*>(red + ((size_t)kq * 32 + 4 * sb0 + 16 + r) * kHeadDim)[fb] = ac1[r];
-    }
-    __syncthreads();
-    for (int e = tid; e < g * (kHeadDim / 4); e += kGThreads) {
-        const int s = e / (kHeadDim / 4), f4 = e - s * (kHeadDim / 4);
-        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 v = reinterpret_cast<const float4*>(red + ((size_t)q * 32 + s) * kHeadDim)[f4];
-            t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
-        }
-        reinterpret_cast<float4*>(part + s * kHeadDim)[f4] = t;
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) ticket = atomicAdd(&a.counters[u], 1);
-    __syncthreads();
-    if (ticket != P.gchunks - 1) return;
-    __threadfence();
-    // thread (s, features 4 fq .. +3): sum the shares of every chunk, 8 loads in flight
-    const int fq = tid & 15;
-    const float keep = 1.f - a.alpha;
-    for (int s = tid >> 4; s < g; s += kGThreads / 16) {
-        const float4* src = reinterpret_cast<const float4*>(a.gpart) +
-                            (((size_t)u * P.gchunks) * g + s) * (kHeadDim / 4) + fq;
-        const size_t cstride = (size_t)g * (kHeadDim / 4);
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = 0; c0 < P.gchunks; c0 += 8) {
-            float4 v[8];
-#pragma unroll
-            for (int b = 0; b < 8; ++b)
-                v[b] = c0 + b < P.gchunks ? __ldcg(src + (size_t)(c0 + b) * cstride)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                sum.x += v[b].x; sum.y += v[b].y; sum.z += v[b].z; sum.w += v[b].w;
-            }
-        }
-        const int64_t gi = a.globals[s];
-        const size_t vrow = ((size_t)u * P.n + gi) * kHeadDim + 4 * fq;
-        const uint2 vv = __ldg(reinterpret_cast<const uint2*>(a.V + vrow));
-        float z[4] = {fmaf(keep, sum.x, a.alpha * bf16lo(vv.x)), fmaf(keep, sum.y, a.alpha * bf16hi(vv.x)),
-                      fmaf(keep, sum.z, a.alpha * bf16lo(vv.y)), fmaf(keep, sum.w, a.alpha * bf16hi(vv.y))};
-        if (kLast) {
-            const __nv_bfloat162 h0 = __floats2bfloat162_rn(z[0], z[1]);
-            const __nv_bfloat162 h1 = __floats2bfloat162_rn(z[2], z[3]);
-            *reinterpret_cast<uint2*>(a.out + vrow) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-        } else {
-            uint32_t hw[2], lw[2];
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const __nv_bfloat162 hh = __floats2bfloat162_rn(z[2 * p], z[2 * p + 1]);
-                const __nv_bfloat162 ll =
-                    __floats2bfloat162_rn(z[2 * p] - __low2float(hh), z[2 * p + 1] - __high2float(hh));
-                hw[p] = *reinterpret_cast<const uint32_t*>(&hh);
-                lw[p] = *reinterpret_cast<const uint32_t*>(&ll);
-            }
-            __nv_bfloat16* zr = a.Z_out + ((size_t)u * P.n + gi) * (2 * kHeadDim) + 4 * fq;
-            *reinterpret_cast<uint2*>(zr) = make_uint2(hw[0], hw[1]);
-            *reinterpret_cast<uint2*>(zr + kHeadDim) = make_uint2(lw[0], lw[1]);
-            *reinterpret_cast<float4*>(a.Zf_out + vrow) = make_float4(z[0], z[1], z[2], z[3]);
-        }
-    }
-    if (tid == 0) a.counters[u] = 0;
-}
+// the gather configuration: rows in flight per quarter-warp, CTAs per SM
+constexpr int kGatherBatch = 4, kGatherBlocks = 4;
 
 // bf16 tensor map over rows of `row_elems` elements: box of 64 elements x 64 rows
 int encode_rows(CUtensorMap* m, const void* base, int64_t n, int64_t units, int row_elems) {
@@ -657,37 +603,31 @@ int launch_hop(const CUtensorMap& tmZ, const HopArgs& a, cudaStream_t stream) {
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(hop_band_kernel<kHop0, kLast>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(
-                hop_global_kernel<kHop0, kLast>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                kGSmemFloats * (int)sizeof(float));
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(hop)");
     const int sms = sm_count();
     const int64_t total_tiles = a.units * a.plan.tiles;
     {
         LaunchScope scope(DIFFUSER_KERNEL_GATHER, stream);
-        const int64_t gmax = (int64_t)sms * 2;
-        hop_gather_kernel<kHop0><<<(unsigned)(total_tiles < gmax ? total_tiles : gmax), kGThreadsG, 0,
-                                   stream>>>(a);
+        const int64_t gmax = (int64_t)sms * kGatherBlocks;
+        hop_gather_kernel<kHop0, kGatherBatch, kGatherBlocks>
+            <<<(unsigned)(total_tiles < gmax ? total_tiles : gmax), kGThreadsG, 0, stream>>>(a);
     }
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return cuda_fail(err, "hop_gather_kernel");
-    if (a.plan.g > 0) {
-        LaunchScope scope(DIFFUSER_KERNEL_GATHER, stream);
-        const size_t shmem = (size_t)kGSmemFloats * sizeof(float);
-        hop_global_kernel<kHop0, kLast><<<(unsigned)(a.units * a.plan.gchunks), kGThreads, shmem,
-                                          stream>>>(a);
-    }
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return cuda_fail(err, "hop_global_kernel");
     dim3 grid((unsigned)(total_tiles < sms ? total_tiles : sms));
     {
         LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
         hop_band_kernel<kHop0, kLast><<<grid, kThreads, kSmemBytes, stream>>>(tmZ, a);
     }
     err = cudaGetLastError();
-    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_band_kernel");
+    if (err != cudaSuccess) return cuda_fail(err, "hop_band_kernel");
+    if (a.plan.g > 0) {
+        LaunchScope scope(DIFFUSER_KERNEL_GATHER, stream);
+        hop_global_rows_kernel<kLast><<<(unsigned)a.units, 256, 0, stream>>>(a);
+    }
+    err = cudaGetLastError();
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_global_rows_kernel");
 }
 
 }  // namespace
@@ -718,6 +658,7 @@ band::Weights band_weights(char* ws, const BandLayout& L) {
     w.A_gc = reinterpret_cast<float*>(ws + L.a_gc);
     w.A_x = reinterpret_cast<float*>(ws + L.a_x);
     w.A_gr = reinterpret_cast<float*>(ws + L.a_gr);
+    w.A_gimg = reinterpret_cast<uint8_t*>(ws + L.a_gimg);
     w.inv_l = reinterpret_cast<float*>(ws + L.inv_l);
     w.m_sparse = reinterpret_cast<float*>(ws + L.m_sparse);
     w.gstat = reinterpret_cast<float*>(ws + L.gstat);
@@ -735,7 +676,6 @@ bool band_plan(const diffuser_graph* g, BandPlan* p) {
     if (p->g_pad == 0) p->g_pad = 4;
     p->tiles = (int32_t)((g->n + kTileRows - 1) / kTileRows);
     p->chunks = (int32_t)((p->r64 + kTileRows + g->r + kChunkKeys - 1) / kChunkKeys);
-    p->gchunks = (int32_t)((g->n + kGChunk - 1) / kGChunk);
     p->band_unit = (size_t)p->tiles * p->chunks * band::kChunkImageBytes;
     return true;
 }
@@ -750,10 +690,11 @@ int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     L->a_gc = take(U * (size_t)p.n * p.g_pad * 4);
     L->a_x = take(U * (size_t)(g->nx > 0 ? g->nx : 1) * 4);
     L->a_gr = take(U * gg * p.n * 4);
+    L->a_gimg = take(U * (size_t)p.tiles * band::kGImgBytes);
     for (int s = 0; s < 2; ++s) L->z[s] = take(U * (size_t)p.n * 2 * kHeadDim * 2);
     for (int s = 0; s < 2; ++s) L->zf[s] = take(U * (size_t)p.n * kHeadDim * 4);
     L->psum = take(U * (size_t)p.n * kHeadDim * 4);
-    L->gpart = take(U * (size_t)p.gchunks * gg * kHeadDim * 4);
+    L->gpart = take(U * (size_t)p.tiles * gg * kHeadDim * 4);
     L->inv_l = take(U * (size_t)p.n * 4);
     L->m_sparse = take(U * (size_t)p.n * 4);
     L->gstat = take(U * gg * 2 * 4);
@@ -785,7 +726,7 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     a.nx = g->nx;
     a.A_gc = reinterpret_cast<const float*>(ws + L.a_gc);
     a.A_x = reinterpret_cast<const float*>(ws + L.a_x);
-    a.A_gr = reinterpret_cast<const float*>(ws + L.a_gr);
+    a.A_gimg = reinterpret_cast<const uint8_t*>(ws + L.a_gimg);
     a.inv_l = reinterpret_cast<const float*>(ws + L.inv_l);
     a.Psum = reinterpret_cast<float*>(ws + L.psum);
     a.A_band = reinterpret_cast<const __nv_bfloat16*>(ws + L.a_band);

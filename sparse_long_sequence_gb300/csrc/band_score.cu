@@ -297,19 +297,31 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
     } else if (warp == 2 || warp == 3) {
         // normalize the global rows' weights over each tile's keys:
-        // A_gr = exp(s - max) / sum, with (max, 1/sum) from score_sparse_kernel
+        // A_gr = exp(s - max) / sum, with (max, 1/sum) from score_sparse_kernel;
+        // also the tile's global-row operand image (hi / lo bf16, zero past n)
         for (int lt = 0; lt < my_tiles; ++lt) {
             const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
             const int64_t u = tix / P.tiles;
             const int64_t i0 = (tix - u * P.tiles) * kTileRows;
             const int64_t tkeys = P.n - i0 < kTileRows ? P.n - i0 : kTileRows;
+            uint8_t* gimg = a.w.A_gimg + (size_t)tix * band::kGImgBytes;
             for (int e = tid - 64; e < P.g * kTileRows; e += 64) {
                 const int sl = e / kTileRows, jj = e % kTileRows;
-                if (jj >= tkeys) continue;
-                const float gm = a.w.gstat[((size_t)u * P.g + sl) * 2];
-                const float ginv = a.w.gstat[((size_t)u * P.g + sl) * 2 + 1];
-                float* v = a.w.A_gr + ((size_t)u * P.g + sl) * P.n + i0 + jj;
-                *v = expf(*v - gm) * ginv;
+                float w = 0.f;
+                if (jj < tkeys) {
+                    const float gm = a.w.gstat[((size_t)u * P.g + sl) * 2];
+                    const float ginv = a.w.gstat[((size_t)u * P.g + sl) * 2 + 1];
+                    float* v = a.w.A_gr + ((size_t)u * P.g + sl) * P.n + i0 + jj;
+                    w = expf(*v - gm) * ginv;
+                    *v = w;
+                }
+                const int h = jj >> 6, k = jj & 63;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+                uint8_t* pe = gimg + h * 2 * band::kGImgPlaneBytes + (sl >> 3) * 1024 + (sl & 7) * 128 +
+                              ((((k >> 3) ^ (sl & 7))) << 4) + (k & 7) * 2;
+                *reinterpret_cast<__nv_bfloat16*>(pe) = hi;
+                *reinterpret_cast<__nv_bfloat16*>(pe + band::kGImgPlaneBytes) = lo;
             }
         }
     } else {
