@@ -103,13 +103,6 @@ __device__ __forceinline__ void fma8f(float (&acc)[8], float w, const float4& z0
     acc[7] = fmaf(w, z1.w, acc[7]);
 }
 
-__device__ __forceinline__ void fma4(float4& acc, float w, const float4& z) {
-    acc.x = fmaf(w, z.x, acc.x);
-    acc.y = fmaf(w, z.y, acc.y);
-    acc.z = fmaf(w, z.z, acc.z);
-    acc.w = fmaf(w, z.w, acc.w);
-}
-
 __device__ __forceinline__ float4 bf16x4(const uint2& h) {
     return make_float4(bf16lo(h.x), bf16hi(h.x), bf16lo(h.y), bf16hi(h.y));
 }

@@ -1,20 +1,21 @@
 // Scores and masked softmax for the band path ("Diffuser: modelling long
 // sequences with multi-hop attention diffusion", eq S.1-S.5; "1.2.1 Static
-// sparsity", eq 1-3), in two kernels:
+// sparsity", eq 1-3), in three kernels:
 //
-//  * score_sparse_kernel (SIMT): per row, the raw scores q_i.k_j/8 of the
-//    globals outside the window and of the random extras (one lane per key,
-//    the 128-byte k_j row read whole), and their maximum; per tile, the raw
+//  * score_sparse_kernel: per row, the raw scores q_i.k_j/8 of the globals
+//    outside the window (-inf inside it) and of the random extras, and their
+//    maximum; a quarter-warp per row, each K row read as one 128-byte line,
+//    8 dot products reduced across the quarter at once.  Per tile, the raw
 //    scores of the global rows against the tile's keys with per-tile
 //    (max, sum of exp); the last tile of a unit merges those into the global
 //    rows' (max, 1/sum).
 //  * score_band_tc_kernel (tcgen05, persistent): S = Q K^T for a 128-row
 //    tile against 64-key chunks of its window on bf16 tensor cores (fp32
-//    accumulation in TMEM), in two passes over the chunks: the row maximum,
-//    then e = exp(s - m) written into the band storage as a bf16 hi / lo
-//    pair (zero outside the row's window) with the row sum; the
-//    row threads then turn the row's sparse raw scores into e and store
-//    inv_l = 1 / (band sum + sparse sum).
+//    accumulation in TMEM), in two passes over the chunks: the row maximum
+//    m_i (band and sparse), then e = exp(s - m_i) written as the tile's
+//    operand image, and the band part of the row sum.
+//  * score_finalize_kernel: a warp per row turns the sparse raw scores into
+//    e = exp(s - m_i) and stores inv_l = 1 / (band sum + sparse sum).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -56,27 +57,44 @@ __device__ __forceinline__ void load_row64(const __nv_bfloat16* p, float (&x)[64
     }
 }
 
-__device__ __forceinline__ float dot64(const float (&q)[64], const __nv_bfloat16* kp) {
-    const uint4* v = reinterpret_cast<const uint4*>(kp);
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 w = __ldg(v + c);
-        acc = fmaf(q[8 * c + 0], bf16lo(w.x), acc); acc = fmaf(q[8 * c + 1], bf16hi(w.x), acc);
-        acc = fmaf(q[8 * c + 2], bf16lo(w.y), acc); acc = fmaf(q[8 * c + 3], bf16hi(w.y), acc);
-        acc = fmaf(q[8 * c + 4], bf16lo(w.z), acc); acc = fmaf(q[8 * c + 5], bf16hi(w.z), acc);
-        acc = fmaf(q[8 * c + 6], bf16lo(w.w), acc); acc = fmaf(q[8 * c + 7], bf16hi(w.w), acc);
-    }
-    return acc;
-}
 
 // ---------------------------------------------------------------- sparse scores
 constexpr int kSparseThreads = 256;
 
-__global__ void __launch_bounds__(kSparseThreads)
+// v[b] (b < 8) are this lane's partial sums of slot b; afterwards v[0] on
+// lane l of the 8-lane group is the full sum of slot l (butterfly transpose).
+__device__ __forceinline__ float reduce8_transpose(float (&v)[8], int ql, unsigned mask) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const bool up = ql & 4;
+        const float send = up ? v[b] : v[b + 4];
+        const float keep = up ? v[b + 4] : v[b];
+        v[b] = keep + __shfl_xor_sync(mask, send, 4, 8);
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const bool up = ql & 2;
+        const float send = up ? v[b] : v[b + 2];
+        const float keep = up ? v[b + 2] : v[b];
+        v[b] = keep + __shfl_xor_sync(mask, send, 2, 8);
+    }
+    const bool up = ql & 1;
+    const float send = up ? v[0] : v[1];
+    const float keep = up ? v[1] : v[0];
+    return keep + __shfl_xor_sync(mask, send, 1, 8);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
+    x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+    x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+}
+
+__global__ void __launch_bounds__(kSparseThreads, 3)
 score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
                     const __nv_bfloat16* __restrict__ K) {
-    extern __shared__ float sm[];            // [g][65] global-row scores of this tile's keys
+    __shared__ float4 sQG[kBandMaxGlobals * 16];   // q rows of the global positions (fp32)
+    __shared__ float4 sKG[kBandMaxGlobals * 16];   // k rows of the global positions (fp32)
+    __shared__ float scr[kBandMaxGlobals * kTileRows];   // the global rows' scores of this tile's keys
     __shared__ int ticket;
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -86,17 +104,35 @@ score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
     const int g = P.g;
     const __nv_bfloat16* Qu = Q + (size_t)u * P.n * kHeadDim;
     const __nv_bfloat16* Ku = K + (size_t)u * P.n * kHeadDim;
+    for (int e = tid; e < g * 8; e += kSparseThreads) {
+        const int sl = e >> 3, p = e & 7;
+        const size_t off = (size_t)a.gr.globals[sl] * kHeadDim;
+        float x[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(Qu + off) + p), x);
+        sQG[sl * 16 + 2 * p] = make_float4(x[0], x[1], x[2], x[3]);
+        sQG[sl * 16 + 2 * p + 1] = make_float4(x[4], x[5], x[6], x[7]);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(Ku + off) + p), x);
+        sKG[sl * 16 + 2 * p] = make_float4(x[0], x[1], x[2], x[3]);
+        sKG[sl * 16 + 2 * p + 1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+    __syncthreads();
 
     if (g > 0) {
         // (1) global rows x this tile's keys: thread t < 128 owns key j = i0 + t
-        float* scr = sm;                     // [g][kTileRows]
         if (tid < kTileRows) {
             const int64_t j = i0 + tid;
             if (j < P.n) {
                 float k[64];
                 load_row64(Ku + (size_t)j * kHeadDim, k);
                 for (int s = 0; s < g; ++s) {
-                    const float sc = dot64(k, Qu + (size_t)a.gr.globals[s] * kHeadDim) * kScale;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float4 q = sQG[s * 16 + c];
+                        acc = fmaf(q.x, k[4 * c], acc); acc = fmaf(q.y, k[4 * c + 1], acc);
+                        acc = fmaf(q.z, k[4 * c + 2], acc); acc = fmaf(q.w, k[4 * c + 3], acc);
+                    }
+                    const float sc = acc * kScale;
                     a.w.A_gr[((size_t)u * g + s) * P.n + j] = sc;
                     scr[s * kTileRows + tid] = sc;
                 }
@@ -146,41 +182,98 @@ score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
             if (tid == 0) a.counters[u] = 0;
         }
     }
-    // (2) rows of this tile, 16 per warp: globals outside the window + extras
-    for (int rr = 0; rr < 16; ++rr) {
-        const int64_t i = i0 + 16 * warp + rr;
-        if (i >= P.n) break;
-        if (a.gr.is_global[i]) continue;
+    // (2) rows of this tile: quarter-warp qi owns rows 4 qi .. +3; lane ql holds
+    //     features 8 ql .. +7 of q_i and reads the same 16 bytes of each k row
+    const int ql = lane & 7, qi = 4 * warp + (lane >> 3);
+    const unsigned qmask = 0xffu << (lane & 24);
+    for (int mrow = 0; mrow < 4; ++mrow) {
+        const int64_t i = i0 + 4 * qi + mrow;
+        if (i >= P.n || a.gr.is_global[i]) continue;      // uniform within the quarter
         const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
         const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
-        float q[64];
-        load_row64(Qu + (size_t)i * kHeadDim, q);
-        const int64_t e0 = a.gr.x_ptr[i], e1 = a.gr.x_ptr[i + 1];
-        const int total = g + (int)(e1 - e0);
-        float* wg = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
-        float* wx = a.w.A_x + (size_t)u * a.gr.nx;
+        float q[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(Qu + (size_t)i * kHeadDim) + ql), q);
         float m = -INFINITY;
-        for (int k = lane; k < total; k += 32) {
-            if (k < g) {
-                const int64_t j = a.gr.globals[k];
-                float sc = 0.f;
-                if (j < lo || j > hi) {
-                    sc = dot64(q, Ku + (size_t)j * kHeadDim) * kScale;
-                    m = fmaxf(m, sc);
-                }
-                wg[k] = sc;
-            } else {
-                const int64_t e = e0 + (k - g);
-                const float sc = dot64(q, Ku + (size_t)a.gr.x_col[e] * kHeadDim) * kScale;
-                wx[e] = sc;
+        float* wg = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+        for (int s0 = 0; s0 < g; s0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const int sl = s0 + b < g ? s0 + b : 0;
+                const float4 k0 = sKG[sl * 16 + 2 * ql], k1 = sKG[sl * 16 + 2 * ql + 1];
+                v[b] = q[0] * k0.x + q[1] * k0.y + q[2] * k0.z + q[3] * k0.w +
+                       q[4] * k1.x + q[5] * k1.y + q[6] * k1.z + q[7] * k1.w;
+            }
+            const float dot = reduce8_transpose(v, ql, qmask);   // slot s0 + ql
+            const int sl = s0 + ql;
+            if (sl < g) {
+                const int64_t j = a.gr.globals[sl];
+                const float sc = (j < lo || j > hi) ? dot * kScale : -INFINITY;   // -inf: inside the window
+                wg[sl] = sc;
                 m = fmaxf(m, sc);
             }
         }
-        for (int s = g + lane; s < P.g_pad; s += 32) wg[s] = 0.f;
+        const int64_t e0 = a.gr.x_ptr[i], e1 = a.gr.x_ptr[i + 1];
+        float* wx = a.w.A_x + (size_t)u * a.gr.nx;
+        for (int64_t base = e0; base < e1; base += 8) {
+            const int cnt = e1 - base < 8 ? (int)(e1 - base) : 8;
+            uint4 kr[8];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (lane == 0) a.w.m_sparse[(size_t)u * P.n + i] = m;
+            for (int b = 0; b < 8; ++b) {
+                const int32_t j = b < cnt ? __ldg(a.gr.x_col + base + b) : (int32_t)i;
+                kr[b] = __ldg(reinterpret_cast<const uint4*>(Ku + (size_t)j * kHeadDim) + ql);
+            }
+            float v[8];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                float kx[8];
+                unpack8(kr[b], kx);
+                v[b] = q[0] * kx[0] + q[1] * kx[1] + q[2] * kx[2] + q[3] * kx[3] +
+                       q[4] * kx[4] + q[5] * kx[5] + q[6] * kx[6] + q[7] * kx[7];
+            }
+            const float dot = reduce8_transpose(v, ql, qmask);   // slot base + ql
+            if (ql < cnt) {
+                const float sc = dot * kScale;
+                wx[base + ql] = sc;
+                m = fmaxf(m, sc);
+            }
+        }
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(qmask, m, off, 8));
+        if (ql == 0) a.w.m_sparse[(size_t)u * P.n + i] = m;
     }
+}
+
+// A warp per row: e = exp(s - m_i) for the globals outside the window and the
+// random extras (in place), and inv_l_i = 1 / (band sum + sparse sum).  On
+// entry m_sparse holds m_i and inv_l the band part of the row sum.
+__global__ void __launch_bounds__(256)
+score_finalize_kernel(ScoreArgs a) {
+    const BandPlan& P = a.plan;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= a.units * P.n) return;
+    const int64_t u = gw / P.n, i = gw - u * P.n;
+    if (a.gr.is_global[i]) return;
+    const size_t row = (size_t)u * P.n + i;
+    const float m = a.w.m_sparse[row];
+    float l = 0.f;
+    if (lane < P.g) {
+        float* wg = a.w.A_gc + row * P.g_pad + lane;
+        const float e = expf(*wg - m);          // exp(-inf) = 0 inside the window
+        *wg = e;
+        l += e;
+    }
+    const int64_t e0 = a.gr.x_ptr[i], e1 = a.gr.x_ptr[i + 1];
+    float* wx = a.w.A_x + (size_t)u * a.gr.nx;
+    for (int64_t e = e0 + lane; e < e1; e += 32) {
+        const float v = expf(wx[e] - m);
+        wx[e] = v;
+        l += v;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    if (lane == 0) a.w.inv_l[row] = 1.f / (a.w.inv_l[row] + l);
 }
 
 // ---------------------------------------------------------------- band scores (tcgen05)
@@ -415,25 +508,12 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     }
                 }
             }
-            // the row's sparse part (first column half) and the normalizer
+            // the row's maximum m_i and the band part of its sum (score_finalize_kernel adds the rest)
             xch[rtid] = lsum;
             ptx::named_barrier_sync(1, kRowThreads);
             if (hcol == 0 && row_ok) {
-                float l = lsum + xch[rtid + 128];
-                float* wg = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
-                for (int s2 = 0; s2 < P.g; ++s2) {
-                    const int64_t j = a.gr.globals[s2];
-                    const float e = (j < lo || j > hi) ? expf(wg[s2] - m) : 0.f;
-                    wg[s2] = e;
-                    l += e;
-                }
-                float* wx = a.w.A_x + (size_t)u * a.gr.nx;
-                for (int64_t e = a.gr.x_ptr[i]; e < a.gr.x_ptr[i + 1]; ++e) {
-                    const float v = expf(wx[e] - m);
-                    wx[e] = v;
-                    l += v;
-                }
-                a.w.inv_l[(size_t)u * P.n + i] = 1.f / l;
+                a.w.inv_l[(size_t)u * P.n + i] = lsum + xch[rtid + 128];
+                a.w.m_sparse[(size_t)u * P.n + i] = m;
             }
             ptx::named_barrier_sync(1, kRowThreads);   // xch is reused by the next tile
         }
@@ -529,10 +609,7 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(score_band_tc_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmemBytes);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(score_sparse_kernel,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            kBandMaxGlobals * kTileRows * (int)sizeof(float));
+
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(scores)");
     cudaError_t err = cudaMemsetAsync(ws + L.counters, 0, (size_t)units * 4, stream);
@@ -543,8 +620,7 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
     const unsigned grid = (unsigned)(units * p.tiles);
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
-        score_sparse_kernel<<<grid, kSparseThreads, (size_t)p.g * kTileRows * sizeof(float),
-                              stream>>>(a, Qb, Kb);
+        score_sparse_kernel<<<grid, kSparseThreads, 0, stream>>>(a, Qb, Kb);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_sparse_kernel");
 
@@ -578,6 +654,11 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
         score_band_tc_kernel<<<pgrid, kBThreads, kBSmemBytes, stream>>>(tmQ, tmK, a, g->d_status);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_band_tc_kernel");
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
+        score_finalize_kernel<<<(unsigned)((units * p.n + 7) / 8), 256, 0, stream>>>(a);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_finalize_kernel");
     return DIFFUSER_OK;
 }
 

@@ -61,12 +61,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // two seconds (or at once when another wait has already given up), records
 // kStatusTimeout in *status and returns false; callers carry on so that the
 // kernel always terminates.
+// The status word and the clock are looked at only every 64 polls, so that a
+// waiting thread keeps polling the barrier itself at full rate.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    while (true) {
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*reinterpret_cast<volatile int*>(status) != 0 || globaltimer() - t0 > kWaitLimitNs) {
+        if ((it & 63) == 0 &&
+            (*reinterpret_cast<volatile int*>(status) != 0 || globaltimer() - t0 > kWaitLimitNs)) {
             atomicExch(status, kStatusTimeout);
             return false;
         }
