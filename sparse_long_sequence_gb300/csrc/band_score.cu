@@ -1,19 +1,21 @@
 // Scores and masked softmax for the band path ("Diffuser: modelling long
 // sequences with multi-hop attention diffusion", eq S.1-S.5; "1.2.1 Static
-// sparsity", eq 1-3), in three kernels:
+// sparsity", eq 1-3), in four kernels:
 //
 //  * score_sparse_kernel: per row, the raw scores q_i.k_j/8 of the globals
 //    outside the window (-inf inside it) and of the random extras, and their
 //    maximum; a quarter-warp per row, each K row read as one 128-byte line,
 //    8 dot products reduced across the quarter at once.  Per tile, the raw
 //    scores of the global rows against the tile's keys with per-tile
-//    (max, sum of exp); the last tile of a unit merges those into the global
-//    rows' (max, 1/sum).
+//    (max, sum of exp).
 //  * score_band_tc_kernel (tcgen05, persistent): S = Q K^T for a 128-row
 //    tile against 64-key chunks of its window on bf16 tensor cores (fp32
 //    accumulation in TMEM), in two passes over the chunks: the row maximum
 //    m_i (band and sparse), then e = exp(s - m_i) written as the tile's
 //    operand image, and the band part of the row sum.
+//  * score_global_norm_kernel: merges the per-tile statistics into the global
+//    rows' (max, 1/sum), normalizes their weights and writes each tile's
+//    global-row operand image.
 //  * score_finalize_kernel: a warp per row turns the sparse raw scores into
 //    e = exp(s - m_i) and stores inv_l = 1 / (band sum + sparse sum).
 #include <cuda.h>
@@ -89,13 +91,12 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
     x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
 }
 
-__global__ void __launch_bounds__(kSparseThreads, 3)
+__global__ void __launch_bounds__(kSparseThreads, 2)
 score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
                     const __nv_bfloat16* __restrict__ K) {
     __shared__ float4 sQG[kBandMaxGlobals * 16];   // q rows of the global positions (fp32)
     __shared__ float4 sKG[kBandMaxGlobals * 16];   // k rows of the global positions (fp32)
     __shared__ float scr[kBandMaxGlobals * kTileRows];   // the global rows' scores of this tile's keys
-    __shared__ int ticket;
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t u = blockIdx.x / P.tiles;
@@ -160,27 +161,6 @@ score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
                 st[1] = l;
             }
         }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) ticket = atomicAdd(&a.counters[u], 1);
-        __syncthreads();
-        if (ticket == P.tiles - 1) {
-            __threadfence();
-            for (int s = tid; s < g; s += kSparseThreads) {
-                float M = -INFINITY;
-                for (int tt = 0; tt < P.tiles; ++tt)
-                    M = fmaxf(M, __ldcg(a.w.sstat + (((size_t)u * P.tiles + tt) * g + s) * 2));
-                float L = 0.f;
-                for (int tt = 0; tt < P.tiles; ++tt) {
-                    const float* st = a.w.sstat + (((size_t)u * P.tiles + tt) * g + s) * 2;
-                    const float mt = __ldcg(st);
-                    if (mt != -INFINITY) L += __ldcg(st + 1) * expf(mt - M);
-                }
-                a.w.gstat[((size_t)u * g + s) * 2] = M;
-                a.w.gstat[((size_t)u * g + s) * 2 + 1] = 1.f / L;
-            }
-            if (tid == 0) a.counters[u] = 0;
-        }
     }
     // (2) rows of this tile: quarter-warp qi owns rows 4 qi .. +3; lane ql holds
     //     features 8 ql .. +7 of q_i and reads the same 16 bytes of each k row
@@ -215,27 +195,42 @@ score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
         }
         const int64_t e0 = a.gr.x_ptr[i], e1 = a.gr.x_ptr[i + 1];
         float* wx = a.w.A_x + (size_t)u * a.gr.nx;
-        for (int64_t base = e0; base < e1; base += 8) {
-            const int cnt = e1 - base < 8 ? (int)(e1 - base) : 8;
-            uint4 kr[8];
+        // 32 slots at a time: their columns loaded together (4 per lane), then four
+        // batches of 8 k rows with the next batch's rows in flight during this one's math
+        for (int64_t base = e0; base < e1; base += 32) {
+            const int cnt = e1 - base < 32 ? (int)(e1 - base) : 32;
+            int32_t jv[4];
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                const int32_t j = b < cnt ? __ldg(a.gr.x_col + base + b) : (int32_t)i;
-                kr[b] = __ldg(reinterpret_cast<const uint4*>(Ku + (size_t)j * kHeadDim) + ql);
-            }
-            float v[8];
+            for (int k = 0; k < 4; ++k) jv[k] = 8 * k + ql < cnt ? __ldg(a.gr.x_col + base + 8 * k + ql) : (int32_t)i;
+            uint4 kr[2][8];
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                float kx[8];
-                unpack8(kr[b], kx);
-                v[b] = q[0] * kx[0] + q[1] * kx[1] + q[2] * kx[2] + q[3] * kx[3] +
-                       q[4] * kx[4] + q[5] * kx[5] + q[6] * kx[6] + q[7] * kx[7];
-            }
-            const float dot = reduce8_transpose(v, ql, qmask);   // slot base + ql
-            if (ql < cnt) {
-                const float sc = dot * kScale;
-                wx[base + ql] = sc;
-                m = fmaxf(m, sc);
+            for (int b = 0; b < 8; ++b)
+                kr[0][b] = __ldg(reinterpret_cast<const uint4*>(
+                                     Ku + (size_t)__shfl_sync(qmask, jv[0], b, 8) * kHeadDim) + ql);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (k < 3 && 8 * (k + 1) < cnt) {
+#pragma unroll
+                    for (int b = 0; b < 8; ++b)
+                        kr[(k + 1) & 1][b] = __ldg(reinterpret_cast<const uint4*>(
+                                                 Ku + (size_t)__shfl_sync(qmask, jv[k + 1], b, 8) * kHeadDim) + ql);
+                }
+                if (8 * k < cnt) {
+                    float v[8];
+#pragma unroll
+                    for (int b = 0; b < 8; ++b) {
+                        float kx[8];
+                        unpack8(kr[k & 1][b], kx);
+                        v[b] = q[0] * kx[0] + q[1] * kx[1] + q[2] * kx[2] + q[3] * kx[3] +
+                               q[4] * kx[4] + q[5] * kx[5] + q[6] * kx[6] + q[7] * kx[7];
+                    }
+                    const float dot = reduce8_transpose(v, ql, qmask);   // slot base + 8 k + ql
+                    if (8 * k + ql < cnt) {
+                        const float sc = dot * kScale;
+                        wx[base + 8 * k + ql] = sc;
+                        m = fmaxf(m, sc);
+                    }
+                }
             }
         }
 #pragma unroll
@@ -291,7 +286,8 @@ constexpr int kSBufs = 8;                // TMEM S buffers (64 columns each)
 constexpr int kBTmemCols = 512;
 constexpr int kQBytes = kTileRows * kHeadDim * 2;
 constexpr int kKBytes = kSChunk * kHeadDim * 2;
-constexpr int kBSmemUsed = 1024 + 2 * kQBytes + kKStages * kKBytes + 2 * kRowThreads * 4 + 512;
+constexpr int kBSmemUsed = 1024 + 2 * kQBytes + kKStages * kKBytes + 2 * band::kChunkImageBytes +
+                           2 * kRowThreads * 4 + 512;
 // request at least 120 KB so that the shared memory alone keeps it to one CTA per SM
 constexpr int kBSmemBytes = kBSmemUsed > 120 * 1024 ? kBSmemUsed : 120 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -304,7 +300,8 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                                ~uintptr_t(1023));
     uint8_t* sQ = smem;                                   // 2 x 16 KB
     uint8_t* sK = sQ + 2 * kQBytes;                       // kKStages x 8 KB
-    float* xch = reinterpret_cast<float*>(sK + kKStages * kKBytes);   // [2][256] row partials
+    uint8_t* sOut = sK + kKStages * kKBytes;                  // 2 x one chunk's weight image
+    float* xch = reinterpret_cast<float*>(sOut + 2 * band::kChunkImageBytes);   // [2][256] row partials
     uint64_t* bars = reinterpret_cast<uint64_t*>(xch + 2 * kRowThreads);
     uint64_t* full_Q = bars;                  // [2]
     uint64_t* empty_Q = full_Q + 2;           // [2]
@@ -388,40 +385,17 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (uses > 0) ptx::mbar_wait(&empty_Q[s], (uses - 1) & 1, status);
             }
         }
-    } else if (warp == 2 || warp == 3) {
-        // normalize the global rows' weights over each tile's keys:
-        // A_gr = exp(s - max) / sum, with (max, 1/sum) from score_sparse_kernel;
-        // also the tile's global-row operand image (hi / lo bf16, zero past n)
-        for (int lt = 0; lt < my_tiles; ++lt) {
-            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
-            const int64_t u = tix / P.tiles;
-            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-            const int64_t tkeys = P.n - i0 < kTileRows ? P.n - i0 : kTileRows;
-            uint8_t* gimg = a.w.A_gimg + (size_t)tix * band::kGImgBytes;
-            for (int e = tid - 64; e < P.g * kTileRows; e += 64) {
-                const int sl = e / kTileRows, jj = e % kTileRows;
-                float w = 0.f;
-                if (jj < tkeys) {
-                    const float gm = a.w.gstat[((size_t)u * P.g + sl) * 2];
-                    const float ginv = a.w.gstat[((size_t)u * P.g + sl) * 2 + 1];
-                    float* v = a.w.A_gr + ((size_t)u * P.g + sl) * P.n + i0 + jj;
-                    w = expf(*v - gm) * ginv;
-                    *v = w;
-                }
-                const int h = jj >> 6, k = jj & 63;
-                const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
-                uint8_t* pe = gimg + h * 2 * band::kGImgPlaneBytes + (sl >> 3) * 1024 + (sl & 7) * 128 +
-                              ((((k >> 3) ^ (sl & 7))) << 4) + (k & 7) * 2;
-                *reinterpret_cast<__nv_bfloat16*>(pe) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(pe + band::kGImgPlaneBytes) = lo;
-            }
-        }
+    } else if (warp < kRowWarp0) {
+        // warps 2-3 have no role
     } else {
         const int rw = warp - kRowWarp0;          // 0..7
         const int quad = warp & 3, hcol = rw >> 2;
         const int t = quad * 32 + lane;           // row within the tile
         const int rtid = rw * 32 + lane;          // 0..255
+        // the two warps of a TMEM lane quadrant own the same 32 rows: they meet
+        // on barrier 2 + quad, and lane 0 of the first one issues their copies
+        const int pair_bar = 2 + quad;
+        const bool pair_leader = hcol == 0 && lane == 0;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const float a_sc = kLog2e * kScale;
         for (int lt = 0; lt < my_tiles; ++lt) {
@@ -433,11 +407,12 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const bool row_ok = i < P.n && !a.gr.is_global[i < P.n ? i : 0];
             const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
             const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
-            // this tile's weight image; row t of a chunk's plane sits at
-            // 1024 (t / 8) + 128 (t % 8), 16-byte slot q of the row at q ^ (t % 8)
+            // this tile's weight image in global memory; a chunk's image is built
+            // in shared memory (row t of a plane at 1024 (t / 8) + 128 (t % 8),
+            // 16-byte slot q of the row at q ^ (t % 8)) and written by one bulk copy
             uint8_t* timg = reinterpret_cast<uint8_t*>(a.w.A_band) +
-                            (size_t)(u * P.tiles + (i0 / kTileRows)) * P.chunks * band::kChunkImageBytes +
-                            (t >> 3) * 1024 + (t & 7) * 128;
+                            (size_t)(u * P.tiles + (i0 / kTileRows)) * P.chunks * band::kChunkImageBytes;
+            const int trow = (t >> 3) * 1024 + (t & 7) * 128;
             float mraw = -INFINITY;               // max of the raw dot products q.k (unscaled)
             float m = 0.f, b2 = 0.f, lsum = 0.f;
             for (int it = 0; it < per_tile; ++it) {
@@ -447,12 +422,12 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (it == nc) {
                     // both column halves of a row agree on the row maximum
                     xch[rtid] = mraw;
-                    ptx::named_barrier_sync(1, kRowThreads);
+                    ptx::named_barrier_sync(pair_bar, 64);
                     const float other = xch[(rtid + 128) & 255];
                     const float ms = row_ok ? a.w.m_sparse[(size_t)u * P.n + i] : 0.f;
                     m = fmaxf(ms, fmaxf(mraw, other) * kScale);
                     b2 = m * kLog2e;
-                    ptx::named_barrier_sync(1, kRowThreads);   // xch is reused below
+                    ptx::named_barrier_sync(pair_bar, 64);     // xch is reused below
                 }
                 ptx::mbar_wait(&full_S[b], (gi / kSBufs) & 1, status);
                 __syncwarp();
@@ -475,20 +450,27 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                             if (j >= lo && j <= hi) mraw = fmaxf(mraw, sv[k]);
                         }
                     }
-                } else if (row_ok) {
+                } else {
+                    // the staging buffer of this chunk is free once its previous bulk copy has read it
+                    const int gs = lt * nc + c;           // pass-2 chunk count of this CTA
+                    uint8_t* stg = sOut + (gs & 1) * band::kChunkImageBytes + trow;
+                    if (pair_leader) ptx::bulk_wait_read<1>();
+                    ptx::named_barrier_sync(pair_bar, 64);
                     float e[32];
-                    if (full_in) {
+                    if (!row_ok || none_in) {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) { e[k] = exp2f(fmaf(sv[k], a_sc, -b2)); lsum += e[k]; }
+                        for (int k = 0; k < 32; ++k) e[k] = 0.f;
+                    } else if (full_in) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) { e[k] = ptx::ex2_approx(fmaf(sv[k], a_sc, -b2)); lsum += e[k]; }
                     } else {
+                        const int dlo = (int)(lo - j0), dhi = (int)(hi - j0);   // in-window keys k in [dlo, dhi]
 #pragma unroll
                         for (int k = 0; k < 32; ++k) {
-                            const int64_t j = j0 + k;
-                            e[k] = (j >= lo && j <= hi) ? exp2f(fmaf(sv[k], a_sc, -b2)) : 0.f;
+                            e[k] = (k >= dlo && k <= dhi) ? ptx::ex2_approx(fmaf(sv[k], a_sc, -b2)) : 0.f;
                             lsum += e[k];
                         }
                     }
-                    uint8_t* cimg = timg + (size_t)c * band::kChunkImageBytes;
 #pragma unroll
                     for (int k8 = 0; k8 < 4; ++k8) {
                         uint32_t hw[4], lw[4];
@@ -502,25 +484,96 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                             lw[p2] = *reinterpret_cast<const uint32_t*>(&l);
                         }
                         const int slot = ((4 * hcol + k8) ^ (t & 7)) << 4;
-                        *reinterpret_cast<uint4*>(cimg + slot) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4*>(cimg + band::kChunkPlaneBytes + slot) =
+                        *reinterpret_cast<uint4*>(stg + slot) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(stg + band::kChunkPlaneBytes + slot) =
                             make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                    ptx::fence_proxy_async_smem();        // the pieces are visible to the bulk copy
+                    ptx::named_barrier_sync(pair_bar, 64);
+                    if (pair_leader) {
+                        // rows 32 quad .. +31: 4 KB of each plane
+                        const size_t qoff = (size_t)quad * 4096;
+                        uint8_t* gdst = timg + (size_t)c * band::kChunkImageBytes + qoff;
+                        const uint8_t* ssrc = sOut + (gs & 1) * band::kChunkImageBytes + qoff;
+                        ptx::bulk_store(gdst, ssrc, 4096);
+                        ptx::bulk_store(gdst + band::kChunkPlaneBytes, ssrc + band::kChunkPlaneBytes, 4096);
+                        ptx::bulk_commit();
                     }
                 }
             }
             // the row's maximum m_i and the band part of its sum (score_finalize_kernel adds the rest)
             xch[rtid] = lsum;
-            ptx::named_barrier_sync(1, kRowThreads);
+            ptx::named_barrier_sync(pair_bar, 64);
             if (hcol == 0 && row_ok) {
                 a.w.inv_l[(size_t)u * P.n + i] = lsum + xch[rtid + 128];
                 a.w.m_sparse[(size_t)u * P.n + i] = m;
             }
-            ptx::named_barrier_sync(1, kRowThreads);   // xch is reused by the next tile
+            ptx::named_barrier_sync(pair_bar, 64);     // xch is reused by the next tile
         }
+        if (pair_leader) ptx::bulk_wait<0>();     // the last images are written before exit
     }
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) ptx::tmem_dealloc(tmem, kBTmemCols);
+}
+
+// ---------------------------------------------------------------- global rows' weights
+// One CTA per (unit, 128-key tile): A_gr = exp(s - max) / sum with the global
+// rows' (max, 1/sum) from score_sparse_kernel, in place, and the tile's
+// global-row operand image (hi / lo bf16; keys past n are 0).
+__global__ void __launch_bounds__(256)
+score_global_norm_kernel(ScoreArgs a) {
+    __shared__ float2 st[kBandMaxGlobals];        // (max, 1 / sum) of each global row
+    const BandPlan& P = a.plan;
+    const int64_t u = blockIdx.x / P.tiles;
+    const int64_t tile = blockIdx.x - u * P.tiles;
+    const int64_t i0 = tile * kTileRows;
+    // merge the per-tile (max, sum of exp) of every global row: 16 lanes per row,
+    // each lane over tiles l, l + 16, ..., in a fixed order
+    for (int s0 = 0; s0 < P.g; s0 += 16) {
+        const int sl = s0 + (threadIdx.x >> 4), l = threadIdx.x & 15;
+        const bool ok = sl < P.g;
+        float M = -INFINITY;
+        for (int tt = l; ok && tt < P.tiles; tt += 16)
+            M = fmaxf(M, __ldg(a.w.sstat + (((size_t)u * P.tiles + tt) * P.g + sl) * 2));
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off, 16));
+        float L = 0.f;
+        for (int tt = l; ok && tt < P.tiles; tt += 16) {
+            const float* sp = a.w.sstat + (((size_t)u * P.tiles + tt) * P.g + sl) * 2;
+            const float mt = __ldg(sp);
+            if (mt != -INFINITY) L += __ldg(sp + 1) * expf(mt - M);
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off, 16);
+        if (ok && l == 0) {
+            st[sl] = make_float2(M, 1.f / L);
+            if (tile == 0) {
+                a.w.gstat[((size_t)u * P.g + sl) * 2] = M;
+                a.w.gstat[((size_t)u * P.g + sl) * 2 + 1] = 1.f / L;
+            }
+        }
+    }
+    __syncthreads();
+    uint8_t* gimg = a.w.A_gimg + (size_t)blockIdx.x * band::kGImgBytes;
+    for (int e = threadIdx.x; e < P.g * kTileRows; e += blockDim.x) {
+        const int sl = e / kTileRows, jj = e % kTileRows;
+        float w = 0.f;
+        if (i0 + jj < P.n) {
+            const float gm = st[sl].x;
+            const float ginv = st[sl].y;
+            float* v = a.w.A_gr + ((size_t)u * P.g + sl) * P.n + i0 + jj;
+            w = expf(*v - gm) * ginv;
+            *v = w;
+        }
+        const int h = jj >> 6, k = jj & 63;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+        uint8_t* pe = gimg + h * 2 * band::kGImgPlaneBytes + (sl >> 3) * 1024 + (sl & 7) * 128 +
+                      ((((k >> 3) ^ (sl & 7))) << 4) + (k & 7) * 2;
+        *reinterpret_cast<__nv_bfloat16*>(pe) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(pe + band::kGImgPlaneBytes) = lo;
+    }
 }
 
 // ---------------------------------------------------------------- weights -> CSR order
@@ -623,6 +676,11 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
         score_sparse_kernel<<<grid, kSparseThreads, 0, stream>>>(a, Qb, Kb);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_sparse_kernel");
+    if (p.g > 0) {
+        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
+        score_global_norm_kernel<<<grid, 256, 0, stream>>>(a);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_global_norm_kernel");
 
     auto fn = encode_fn();
     if (!fn) return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");

@@ -136,6 +136,35 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// Contiguous shared -> global copy by the bulk-copy engine (bulk_group
+// completion): addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// at most kPending of this thread's bulk groups still read their shared source
+template <int kPending>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
+}
+// at most kPending of this thread's bulk groups are still incomplete
+template <int kPending>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+// 2^x by the hardware approximation (PTX ex2.approx; results below the
+// normal range flush to zero)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- cp.async (16-byte global -> shared copies; src_bytes 0 writes zeros) ----
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
