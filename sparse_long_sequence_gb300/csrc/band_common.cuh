@@ -14,7 +14,13 @@
 //                      128 (t % 8), 16-byte slot q at q ^ (t % 8)); e_ij =
 //                      hi + lo (hi = e rounded to bf16, lo = the remainder
 //                      rounded to bf16) for |i-j| <= r, 0 <= j < n, else 0
-//   gcol   [n][g_pad]  slot s <-> key G[s]: e for globals outside row i's window, else 0
+//   gcol   [n][g_pad]  slot s <-> key G[s]: raw scores (-inf inside row i's window)
+//   gcimg  [tiles][hi | lo][128 rows x g16 slots] bf16: e of those scores
+//                      (0 inside the window and for slots past g), as the
+//                      tensor-core A operand image (K-major, no swizzle:
+//                      8-row x 16-byte core matrices, the next 8 slots 128
+//                      bytes on, the next 8 rows 16 g16 bytes on); g16 = g
+//                      rounded up to 16
 //   extra  [nx]        e of the random edges outside window and G, CSR order
 //   inv_l  [n]         per-row normalizer of the rows not in G
 //   grow   [g][n]      the global rows' weights A_ij (raw scores until the
@@ -48,6 +54,13 @@ constexpr int kGImgRows = 32;                                      // the global
 constexpr int kGImgPlaneBytes = kGImgRows * kChunkKeys * 2;        // 4 KB
 constexpr int kGImgBytes = 2 * 2 * kGImgPlaneBytes;                // 2 halves x (hi, lo): 16 KB
 
+// the out-of-window globals' operand image of a tile: one plane holds 128 rows
+// x g16 bf16 slots; byte offset of (row t, slot s) within a plane
+__host__ __device__ constexpr int gc_plane_bytes(int g16) { return kTileRows * g16 * 2; }
+__host__ __device__ constexpr int gc_offset(int t, int s, int g16) {
+    return (t >> 3) * (16 * g16) + (t & 7) * 16 + (s >> 3) * 128 + (s & 7) * 2;
+}
+
 __device__ __forceinline__ float tf32_trunc(float x) {
     return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
@@ -61,6 +74,7 @@ struct Weights {
     float* A_x;        // [units][nx]
     float* A_gr;       // [units][g][n] global-row weights (raw scores before normalization)
     uint8_t* A_gimg;   // [units][tiles] global-row weight images (kGImgBytes each)
+    uint8_t* A_gcimg;  // [units][tiles] out-of-window global weight images (gc_image_bytes each)
     float* inv_l;      // [units][n]
     float* m_sparse;   // [units][n] max raw score over a row's gcol + extras
     float* gstat;      // [units][g][2]

@@ -4,12 +4,11 @@
 //
 // Hop Z_{k+1} = (1-alpha) A Z_k + alpha V ("Diffuser...", sec 2.4 eq S.7),
 // three kernels per hop:
-//   hop_gather_kernel: the sparse part of every row not in G, into a per-row
-//            partial P_i: the globals outside the window (their Z_k rows
-//            staged in shared memory) and the random extras (whole Z_k rows
-//            gathered from L2).  Each quarter-warp walks the extras of 4
-//            consecutive rows as one stream with many rows in flight; every
-//            load instruction reads whole 128-byte lines.
+//   hop_gather_kernel: the random extras of every row not in G, into a
+//            per-row partial P_i (whole Z_k rows gathered from L2).  Each
+//            quarter-warp walks the extras of 4 consecutive rows as one stream
+//            with several rows in flight; every load instruction reads whole
+//            128-byte lines.
 //   hop_band_kernel (persistent, 128-row tiles): tcgen05 MMA, M = 128 rows,
 //            K = 64 keys per chunk, bf16 operands split into hi + lo (each the
 //            bf16 rounding of what is left): e_hi*[Z_hi | Z_lo] (N = 128) +
@@ -17,7 +16,10 @@
 //            (below 2^-16 of the product) is the only one left out.  The
 //            score kernel stores each chunk's A tile as the exact shared-memory
 //            image of the operand, so a chunk is two 16 KB bulk copies; the
-//            Z_k rows come by TMA as the MN-major B operand.  The global rows
+//            Z_k rows come by TMA as the MN-major B operand.  The globals
+//            outside each row's window are one more K step into the same
+//            accumulator: their weights' operand image [128 x g16] against the
+//            global keys' Z_k rows (staged by warp 2).  The global rows
 //            (full rows of A) ride along: on the two chunks that hold the
 //            tile's own keys, the same Z_k tiles also multiply the global rows'
 //            weights of those keys (a 32-row operand image) into a second
@@ -46,13 +48,14 @@ using band::bf16hi;
 using band::bf16lo;
 using band::kChunkKeys;
 using band::kTileRows;
-// warp 0: TMA producer (A and Z), warp 1: MMA, warps 4-11: epilogue (warp w
+// warp 0: TMA producer (A and Z), warp 1: MMA, warp 2: stages the global keys'
+// Z_k rows, warps 4-11: epilogue (warp w
 // reads TMEM lane quadrant w % 4, features 32 ((w - 4) / 4) .. +31).
 // One CTA per SM (its shared memory alone rules out a second one).
 constexpr int kThreads = 384;
 constexpr int kTmaWarp = 0, kMmaWarp = 1, kEpiWarp0 = 4, kEpiThreads = 256;
 constexpr int kAStages = 4;              // A ring: hi tile + lo tile, 32 KB per stage
-constexpr int kZStages = 4;              // Z ring: hi tile + lo tile, 16 KB per stage
+constexpr int kZStagesMax = 4;           // Z ring: hi tile + lo tile, 16 KB per stage (3 when g > 16)
 constexpr int kAccCols = 128;            // one accumulator: columns [0,64) A Z_hi, [64,128) A_hi Z_lo
 constexpr int kGlobCol0 = 256;           // the global rows' accumulators: columns 256 + 128 (lt & 1)
 constexpr int kTmemCols = 512;           // band and global accumulators, double-buffered tiles
@@ -62,9 +65,19 @@ constexpr int kZTileBytes = kChunkKeys * 128;
 constexpr int kZStageBytes = 2 * kZTileBytes;
 // the global rows' operand image comes first: its descriptors span 16 KB past
 // their start (rows 32..127 read whatever follows; those rows are not used)
-constexpr int kSmemBytes = 1024 + band::kGImgBytes + kAStages * kAStageBytes + kZStages * kZStageBytes + 256;
-static_assert(kSmemBytes > 116 * 1024, "must exclude a second CTA per SM");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// the out-of-window globals: their weights' operand image (hi, lo; g16 slots)
+// and the Z_k rows of the global keys as an MN-major B tile (hi, lo)
+// Shared memory of a launch: the Z ring gets 4 stages when the globals' tiles
+// are small enough (g16 <= 16), else 3.
+__host__ __device__ constexpr int z_stages(int g16) { return g16 > 16 ? 3 : 4; }
+__host__ __device__ constexpr int band_smem_bytes(int g16) {
+    return 1024 + band::kGImgBytes + kAStages * kAStageBytes + z_stages(g16) * kZStageBytes +
+           2 * kTileRows * (g16 > 0 ? g16 : 16) * 2 + 2 * (g16 > 0 ? g16 : 16) * 128 + 256;
+}
+constexpr int kSmemBytesMax = band_smem_bytes(16) > band_smem_bytes(kBandMaxGlobals)
+                                  ? band_smem_bytes(16) : band_smem_bytes(kBandMaxGlobals);
+static_assert(band_smem_bytes(16) <= 227 * 1024 && kSmemBytesMax <= 227 * 1024, "shared memory per CTA");
+static_assert(band_smem_bytes(0) > 116 * 1024, "must exclude a second CTA per SM");
 
 struct HopArgs {
     BandPlan plan;
@@ -81,6 +94,7 @@ struct HopArgs {
     const float* inv_l;   // [units][n]
     const __nv_bfloat16* V;
     const __nv_bfloat16* A_band; // the tiles' A images [units][tiles][chunks][hi | lo]
+    const uint8_t* A_gcimg;      // out-of-window globals' weight images [units][tiles][hi | lo]
     const float* Zf_in;          // Z_k as fp32 rows [n][64] (hops after the first)
     __nv_bfloat16* Z_out;        // Z_{k+1} ([n][hi 64 | lo 64]), all hops but the last
     float* Zf_out;               // Z_{k+1} as fp32 rows [n][64], all hops but the last
@@ -91,16 +105,13 @@ struct HopArgs {
     int* status;
 };
 
-// acc[0..7] += w * (z0, z1)
-__device__ __forceinline__ void fma8f(float (&acc)[8], float w, const float4& z0, const float4& z1) {
-    acc[0] = fmaf(w, z0.x, acc[0]);
-    acc[1] = fmaf(w, z0.y, acc[1]);
-    acc[2] = fmaf(w, z0.z, acc[2]);
-    acc[3] = fmaf(w, z0.w, acc[3]);
-    acc[4] = fmaf(w, z1.x, acc[4]);
-    acc[5] = fmaf(w, z1.y, acc[5]);
-    acc[6] = fmaf(w, z1.z, acc[6]);
-    acc[7] = fmaf(w, z1.w, acc[7]);
+// acc[0..3] += w * (z0, z1) with packed pairs (the same rounding as fmaf per element)
+__device__ __forceinline__ void ffma8(float2 (&acc)[4], float w, const float4& z0, const float4& z1) {
+    const float2 ww = make_float2(w, w);
+    acc[0] = __ffma2_rn(ww, make_float2(z0.x, z0.y), acc[0]);
+    acc[1] = __ffma2_rn(ww, make_float2(z0.z, z0.w), acc[1]);
+    acc[2] = __ffma2_rn(ww, make_float2(z1.x, z1.y), acc[2]);
+    acc[3] = __ffma2_rn(ww, make_float2(z1.z, z1.w), acc[3]);
 }
 
 __device__ __forceinline__ float4 bf16x4(const uint2& h) {
@@ -132,63 +143,76 @@ __device__ __forceinline__ uint4 pack8(const float* z) {
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-// Z_{k+1} of global row s from the shares sum_j A_gr[s][j] Z_k[j] of every tile
-// (summed in tile order): written as the next [hi | lo] bf16 and fp32 rows, or
-// as the bf16 output.  Threads (s, features 4 fq .. +3).
+// One CTA per unit, 1024 threads: Z_{k+1} of the global rows from the shares
+// sum_j A_gr[s][j] Z_k[j] of every tile, summed in a fixed order (tile quarter
+// q adds tiles q, q + 4, ... with all its loads in flight; then the quarters in
+// order), written as the next [hi | lo] bf16 and fp32 rows, or as the output.
+constexpr int kGRThreads = 1024;
+
 template <bool kLast>
-__device__ void finish_global_rows(const HopArgs& a, int64_t u, int tid, int nthreads) {
+__global__ void __launch_bounds__(kGRThreads) hop_global_rows_kernel(HopArgs a) {
+    __shared__ float4 red[4][16][16];             // [tile quarter][row s (16 at a time)][feature quad]
     const BandPlan& P = a.plan;
+    const int64_t u = blockIdx.x;
     const int g = P.g;
+    const int tq = threadIdx.x >> 8, sl0 = (threadIdx.x >> 4) & 15, fq = threadIdx.x & 15;
     const float keep = 1.f - a.alpha;
     const size_t tstride = (size_t)g * (kHeadDim / 4);
-    for (int e = tid; e < g * 16; e += nthreads) {
-        const int s = e >> 4, fq = e & 15;
-        const float4* src = reinterpret_cast<const float4*>(a.gpart) +
-                            ((size_t)u * P.tiles * g + s) * (kHeadDim / 4) + fq;
+    for (int s0 = 0; s0 < g; s0 += 16) {
+        const int s = s0 + sl0;
         float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = 0; c0 < P.tiles; c0 += 8) {
-            float4 v[8];
+        if (s < g) {
+            const float4* src = reinterpret_cast<const float4*>(a.gpart) +
+                                ((size_t)u * P.tiles * g + s) * (kHeadDim / 4) + fq;
+            for (int c0 = tq; c0 < P.tiles; c0 += 32) {
+                float4 v[8];
 #pragma unroll
-            for (int b = 0; b < 8; ++b)
-                v[b] = c0 + b < P.tiles ? __ldcg(src + (size_t)(c0 + b) * tstride)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int b = 0; b < 8; ++b) {
+                    const int tt = c0 + 4 * b;
+                    v[b] = tt < P.tiles ? __ldcg(src + (size_t)tt * tstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                sum.x += v[b].x; sum.y += v[b].y; sum.z += v[b].z; sum.w += v[b].w;
+                for (int b = 0; b < 8; ++b) {
+                    sum.x += v[b].x; sum.y += v[b].y; sum.z += v[b].z; sum.w += v[b].w;
+                }
             }
         }
-        const int64_t gi = a.globals[s];
-        const size_t vrow = ((size_t)u * P.n + gi) * kHeadDim + 4 * fq;
-        const uint2 vv = __ldg(reinterpret_cast<const uint2*>(a.V + vrow));
-        float z[4] = {fmaf(keep, sum.x, a.alpha * bf16lo(vv.x)), fmaf(keep, sum.y, a.alpha * bf16hi(vv.x)),
-                      fmaf(keep, sum.z, a.alpha * bf16lo(vv.y)), fmaf(keep, sum.w, a.alpha * bf16hi(vv.y))};
-        if (kLast) {
-            const __nv_bfloat162 h0 = __floats2bfloat162_rn(z[0], z[1]);
-            const __nv_bfloat162 h1 = __floats2bfloat162_rn(z[2], z[3]);
-            *reinterpret_cast<uint2*>(a.out + vrow) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-        } else {
-            uint32_t hw[2], lw[2];
+        red[tq][sl0][fq] = sum;
+        __syncthreads();
+        if (tq == 0 && s < g) {
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const __nv_bfloat162 hh = __floats2bfloat162_rn(z[2 * p], z[2 * p + 1]);
-                const __nv_bfloat162 ll =
-                    __floats2bfloat162_rn(z[2 * p] - __low2float(hh), z[2 * p + 1] - __high2float(hh));
-                hw[p] = *reinterpret_cast<const uint32_t*>(&hh);
-                lw[p] = *reinterpret_cast<const uint32_t*>(&ll);
+            for (int q = 1; q < 4; ++q) {
+                const float4 v = red[q][sl0][fq];
+                sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
             }
-            __nv_bfloat16* zr = a.Z_out + ((size_t)u * P.n + gi) * (2 * kHeadDim) + 4 * fq;
-            *reinterpret_cast<uint2*>(zr) = make_uint2(hw[0], hw[1]);
-            *reinterpret_cast<uint2*>(zr + kHeadDim) = make_uint2(lw[0], lw[1]);
-            *reinterpret_cast<float4*>(a.Zf_out + vrow) = make_float4(z[0], z[1], z[2], z[3]);
+            const int64_t gi = a.globals[s];
+            const size_t vrow = ((size_t)u * P.n + gi) * kHeadDim + 4 * fq;
+            const uint2 vv = __ldg(reinterpret_cast<const uint2*>(a.V + vrow));
+            float z[4] = {fmaf(keep, sum.x, a.alpha * bf16lo(vv.x)), fmaf(keep, sum.y, a.alpha * bf16hi(vv.x)),
+                          fmaf(keep, sum.z, a.alpha * bf16lo(vv.y)), fmaf(keep, sum.w, a.alpha * bf16hi(vv.y))};
+            if (kLast) {
+                const __nv_bfloat162 h0 = __floats2bfloat162_rn(z[0], z[1]);
+                const __nv_bfloat162 h1 = __floats2bfloat162_rn(z[2], z[3]);
+                *reinterpret_cast<uint2*>(a.out + vrow) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+            } else {
+                uint32_t hw[2], lw[2];
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const __nv_bfloat162 hh = __floats2bfloat162_rn(z[2 * p], z[2 * p + 1]);
+                    const __nv_bfloat162 ll =
+                        __floats2bfloat162_rn(z[2 * p] - __low2float(hh), z[2 * p + 1] - __high2float(hh));
+                    hw[p] = *reinterpret_cast<const uint32_t*>(&hh);
+                    lw[p] = *reinterpret_cast<const uint32_t*>(&ll);
+                }
+                __nv_bfloat16* zr = a.Z_out + ((size_t)u * P.n + gi) * (2 * kHeadDim) + 4 * fq;
+                *reinterpret_cast<uint2*>(zr) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2*>(zr + kHeadDim) = make_uint2(lw[0], lw[1]);
+                *reinterpret_cast<float4*>(a.Zf_out + vrow) = make_float4(z[0], z[1], z[2], z[3]);
+            }
         }
+        __syncthreads();                          // red is reused by the next 16 rows
     }
-}
-
-// one CTA per unit: the global rows of Z_{k+1}
-template <bool kLast>
-__global__ void __launch_bounds__(256) hop_global_rows_kernel(HopArgs a) {
-    finish_global_rows<kLast>(a, blockIdx.x, threadIdx.x, blockDim.x);
 }
 
 // ---------------------------------------------------------------- band part of a hop
@@ -200,23 +224,30 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                                                ~uintptr_t(1023));
     uint8_t* sGA = smem;                                         // global rows: 2 halves x (hi, lo) 4 KB
     uint8_t* sA = sGA + band::kGImgBytes;                        // kAStages x (hi 16 KB, lo 16 KB)
-    uint8_t* sZ = sA + kAStages * kAStageBytes;                  // kZStages x (hi 8 KB, lo 8 KB)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sZ + kZStages * kZStageBytes);
+    const int g16 = a.plan.g16, g16s = g16 > 0 ? g16 : 16;
+    const int zstages = z_stages(g16);
+    uint8_t* sZ = sA + kAStages * kAStageBytes;                  // zstages x (hi 8 KB, lo 8 KB)
+    uint8_t* sGC = sZ + zstages * kZStageBytes;                 // out-of-window globals' weights
+    uint8_t* sZG = sGC + 2 * kTileRows * g16s * 2;               // Z_k rows of the global keys
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sZG + 2 * g16s * 128);
     uint64_t* full_A = bars;
     uint64_t* empty_A = full_A + kAStages;
     uint64_t* full_Z = empty_A + kAStages;
-    uint64_t* empty_Z = full_Z + kZStages;
-    uint64_t* acc_full = empty_Z + kZStages;                     // [2]
+    uint64_t* empty_Z = full_Z + kZStagesMax;
+    uint64_t* acc_full = empty_Z + kZStagesMax;                  // [2]
     uint64_t* acc_empty = acc_full + 2;                          // [2]
     uint64_t* full_G = acc_empty + 2;
     uint64_t* empty_G = full_G + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_G + 1);
+    uint64_t* full_GC = empty_G + 1;       // the image by bulk copy + the staged Z rows
+    uint64_t* empty_GC = full_GC + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_GC + 1);
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunks = P.chunks;
     const int c0 = P.r64 / kChunkKeys;           // chunks c0 and c0 + 1 hold the tile's own keys
     const bool has_g = P.g > 0;
+    const int gc_plane = band::gc_plane_bytes(g16);
     const int64_t total_tiles = a.units * P.tiles;
     // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
     const int my_tiles = blockIdx.x < total_tiles
@@ -225,10 +256,12 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
     if (warp == kMmaWarp) ptx::tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
         for (int s = 0; s < kAStages; ++s) { ptx::mbar_init(&full_A[s], 1); ptx::mbar_init(&empty_A[s], 1); }
-        for (int s = 0; s < kZStages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
+        for (int s = 0; s < zstages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
         for (int s = 0; s < 2; ++s) { ptx::mbar_init(&acc_full[s], 1); ptx::mbar_init(&acc_empty[s], kEpiThreads); }
         ptx::mbar_init(full_G, 1);
         ptx::mbar_init(empty_G, 1);
+        ptx::mbar_init(full_GC, 2);
+        ptx::mbar_init(empty_GC, 1);
         ptx::fence_mbar_init();
     }
     if (warp == kTmaWarp && lane == 0) ptx::prefetch_tensormap(&tmZ);
@@ -251,6 +284,10 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                 const uint8_t* timg = reinterpret_cast<const uint8_t*>(a.A_band) +
                                       (size_t)tix * chunks * band::kChunkImageBytes;
                 if (has_g) {
+                    if (lt >= 1) ptx::mbar_wait(empty_GC, (lt - 1) & 1, a.status);
+                    ptx::mbar_arrive_expect_tx(full_GC, 2 * gc_plane);
+                    ptx::bulk_load_hint(sGC, a.A_gcimg + (size_t)tix * 2 * gc_plane, 2 * gc_plane, full_GC,
+                                        pol_a);
                     if (lt >= 1) ptx::mbar_wait(empty_G, (lt - 1) & 1, a.status);
                     ptx::mbar_arrive_expect_tx(full_G, band::kGImgBytes);
                     ptx::bulk_load_hint(sGA, a.A_gimg + (size_t)tix * band::kGImgBytes, band::kGImgBytes,
@@ -265,8 +302,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                     const uint8_t* asrc = timg + (size_t)c * band::kChunkImageBytes;
                     ptx::bulk_load_hint(adst, asrc, kATileBytes, &full_A[sa], pol_a);
                     ptx::bulk_load_hint(adst + kATileBytes, asrc + kATileBytes, kATileBytes, &full_A[sa], pol_a);
-                    const int sz = gc % kZStages;
-                    if (gc >= kZStages) ptx::mbar_wait(&empty_Z[sz], ((gc / kZStages) - 1) & 1, a.status);
+                    const int sz = gc % zstages;
+                    if (gc >= zstages) ptx::mbar_wait(&empty_Z[sz], ((gc / zstages) - 1) & 1, a.status);
                     uint8_t* zdst = sZ + sz * kZStageBytes;
                     ptx::mbar_arrive_expect_tx(&full_Z[sz], kHop0 ? kZTileBytes : 2 * kZTileBytes);
                     const int key = (int)(jb + kChunkKeys * c);
@@ -286,11 +323,26 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                 if (lt >= 2) ptx::mbar_wait(&acc_empty[ab], ((lt / 2) - 1) & 1, a.status);
                 ptx::tc_fence_after();
                 const uint32_t dacc = tmem + kAccCols * ab;
+                if (has_g) {
+                    // the globals outside each row's window: [128 x g16] x [g16 x (hi | lo)]
+                    ptx::mbar_wait(full_GC, lt & 1, a.status);
+                    ptx::tc_fence_after();
+                    const uint32_t gch = ptx::smem_u32(sGC), gcl = gch + gc_plane;
+                    const uint32_t zg = ptx::smem_u32(sZG);
+                    for (int ks = 0; ks < g16 / 16; ++ks) {
+                        const uint64_t bdesc = ptx::sw128_mnmajor_desc(zg + 2048 * ks, g16 * 128);
+                        ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gch + 256 * ks, 128, 16 * g16), bdesc,
+                                         kHop0 ? idesc64 : idesc128, ks != 0);
+                        ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gcl + 256 * ks, 128, 16 * g16), bdesc,
+                                         idesc64, 1);
+                    }
+                    ptx::mma_commit(empty_GC);
+                }
                 for (int c = 0; c < chunks; ++c) {
                     const int gc = lt * chunks + c;
-                    const int sa = gc % kAStages, sz = gc % kZStages;
+                    const int sa = gc % kAStages, sz = gc % zstages;
                     ptx::mbar_wait(&full_A[sa], (gc / kAStages) & 1, a.status);
-                    ptx::mbar_wait(&full_Z[sz], (gc / kZStages) & 1, a.status);
+                    ptx::mbar_wait(&full_Z[sz], (gc / zstages) & 1, a.status);
                     ptx::tc_fence_after();
                     const uint32_t ahi = ptx::smem_u32(sA + sa * kAStageBytes);
                     const uint32_t alo = ahi + kATileBytes;
@@ -299,7 +351,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                     for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
                         const uint64_t bdesc = ptx::sw128_mnmajor_desc(zb + 2048 * ks, kZTileBytes);
                         ptx::mma_bf16_ss(dacc, ptx::sw128_kmajor_desc(ahi + 32 * ks), bdesc,
-                                         kHop0 ? idesc64 : idesc128, (c | ks) != 0);
+                                         kHop0 ? idesc64 : idesc128, has_g || (c | ks) != 0);
                         ptx::mma_bf16_ss(dacc, ptx::sw128_kmajor_desc(alo + 32 * ks), bdesc, idesc64, 1);
                     }
                     const int h = c - c0;
@@ -334,11 +386,51 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                 const int uses = (total - s + kAStages - 1) / kAStages;
                 if (uses > 0) ptx::mbar_wait(&empty_A[s], (uses - 1) & 1, a.status);
             }
-            for (int s = 0; s < kZStages; ++s) {
-                const int uses = (total - s + kZStages - 1) / kZStages;
+            for (int s = 0; s < zstages; ++s) {
+                const int uses = (total - s + zstages - 1) / zstages;
                 if (uses > 0) ptx::mbar_wait(&empty_Z[s], (uses - 1) & 1, a.status);
             }
-            if (has_g && my_tiles > 0) ptx::mbar_wait(empty_G, (my_tiles - 1) & 1, a.status);
+            if (has_g && my_tiles > 0) {
+                ptx::mbar_wait(empty_G, (my_tiles - 1) & 1, a.status);
+                ptx::mbar_wait(empty_GC, (my_tiles - 1) & 1, a.status);
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------- the global keys' Z_k rows as the B tile of the out-of-window
+        // globals' MMA: key row s (hi 128 bytes; lo g16 * 128 bytes on), 16-byte chunk
+        // c at (c ^ (s % 8)) * 16; rows past g are zero
+        if (has_g) {
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+                const int64_t u = tix / P.tiles;
+                if (lt >= 1) ptx::mbar_wait(empty_GC, (lt - 1) & 1, a.status);
+                for (int e = lane; e < g16 * 8; e += 32) {
+                    const int sl = e >> 3, cch = e & 7;
+                    float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    if (sl < P.g) {
+                        const size_t row = (size_t)u * P.n + a.globals[sl];
+                        if (kHop0) {
+                            const uint4 h = __ldg(reinterpret_cast<const uint4*>(a.V + row * kHeadDim) + cch);
+                            const uint32_t w4[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) { z[2 * q] = bf16lo(w4[q]); z[2 * q + 1] = bf16hi(w4[q]); }
+                        } else {
+                            const float4* zp = reinterpret_cast<const float4*>(a.Zf_in + row * kHeadDim) + 2 * cch;
+                            const float4 z0 = __ldg(zp), z1 = __ldg(zp + 1);
+                            z[0] = z0.x; z[1] = z0.y; z[2] = z0.z; z[3] = z0.w;
+                            z[4] = z1.x; z[5] = z1.y; z[6] = z1.z; z[7] = z1.w;
+                        }
+                    }
+                    uint4 hi, lo;
+                    split8(z, hi, lo);
+                    const int off = sl * 128 + ((cch ^ (sl & 7)) << 4);
+                    *reinterpret_cast<uint4*>(sZG + off) = hi;
+                    *reinterpret_cast<uint4*>(sZG + g16 * 128 + off) = lo;
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(full_GC);
+            }
         }
     } else if (warp >= kEpiWarp0) {
         // ---------------- epilogue: thread <-> row t = 32 quad + lane, features 32 fhalf .. +31
@@ -441,53 +533,25 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
 // 4 q .. 4 q + 3, whose random extras are one contiguous stretch of the extras
 // list: it walks that stretch in batches of kB slots (every slot's Z_k row in
 // flight at once; a slot past the end reads row 0 with weight 0), and on
-// leaving a row stores the row's sum in shared memory.  Then each row adds its
-// out-of-window globals and writes P_i.  Lane l of a quarter owns features
+// leaving a row stores the row's sum in shared memory; then each row writes P_i.
+// Lane l of a quarter owns features
 // 4 l .. 4 l + 3 and 32 + 4 l .. 32 + 4 l + 3, so each load instruction reads
 // whole 128-byte lines of the gathered rows.
 constexpr int kGThreadsG = 256;
 
-template <bool kHop0>
-__device__ __forceinline__ void load_zrow(const HopArgs& a, size_t row, int ql, float4& z0, float4& z1) {
-    if (kHop0) {
-        const uint2* vp = reinterpret_cast<const uint2*>(a.V + row * kHeadDim);
-        z0 = bf16x4(__ldg(vp + ql));
-        z1 = bf16x4(__ldg(vp + 8 + ql));
-    } else {
-        const float4* zp = reinterpret_cast<const float4*>(a.Zf_in + row * kHeadDim);
-        z0 = __ldg(zp + ql);
-        z1 = __ldg(zp + 8 + ql);
-    }
-}
-
 template <bool kHop0, int kB, int kMinBlocks>
 __global__ void __launch_bounds__(kGThreadsG, kMinBlocks)
 hop_gather_kernel(HopArgs a) {
-    __shared__ float4 sG[kBandMaxGlobals * 16];   // Z_k rows of the global keys (fp32)
     __shared__ float4 sR[32 * 4 * 16];            // [quarter][row][16]: the rows' extras sums
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ql = lane & 7;
     const int qi = 4 * warp + (lane >> 3);        // quarter 0..31: rows 4 qi .. +3
-    const unsigned qmask = 0xffu << (lane & 24);
-    const int g = P.g;
     float4* rq = sR + qi * 64;                    // this quarter's 4 rows
     const int64_t total_tiles = a.units * P.tiles;
-    int64_t staged_u = -1;
     for (int64_t tix = blockIdx.x; tix < total_tiles; tix += gridDim.x) {
         const int64_t u = tix / P.tiles;
         const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-        if (u != staged_u) {
-            __syncthreads();                      // the previous unit's rows are no longer read
-            for (int e = tid; e < g * 16; e += kGThreadsG) {
-                const int sl = e >> 4, p = e & 15;
-                const size_t row = (size_t)u * P.n + a.globals[sl];
-                if (kHop0) sG[e] = bf16x4(__ldg(reinterpret_cast<const uint2*>(a.V + row * kHeadDim) + p));
-                else sG[e] = __ldg(reinterpret_cast<const float4*>(a.Zf_in + row * kHeadDim) + p);
-            }
-            __syncthreads();
-            staged_u = u;
-        }
         const int64_t ib = i0 + 4 * qi;
         const int64_t rlim = P.n;
         // extras of row ib + m: [d_m, d_{m+1}) relative to the first
@@ -502,8 +566,19 @@ hop_gather_kernel(HopArgs a) {
         const float* wq = a.A_x + (size_t)u * a.nx + xb;
         const int32_t* jq = a.x_col + xb;
         const size_t ubase = (size_t)u * P.n;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // this lane's features of row j of Z_k: zrow + 16 j (fp32) or vrow + 16 j (bf16 V)
+        const float4* zrow = reinterpret_cast<const float4*>(a.Zf_in) + ubase * 16 + ql;
+        const uint2* vrow = reinterpret_cast<const uint2*>(a.V) + ubase * 16 + ql;
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
         int cur = 0;                              // row (0..3) being accumulated
+        int nb = d1;                              // first slot past row cur
+        auto stash = [&]() {
+            rq[cur * 16 + ql] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+            rq[cur * 16 + 8 + ql] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
+        };
         for (int e0 = 0; e0 < nslot; e0 += kB) {
             int32_t j[kB];
             float w[kB];
@@ -515,52 +590,53 @@ hop_gather_kernel(HopArgs a) {
             }
             float4 z0[kB], z1[kB];
 #pragma unroll
-            for (int b = 0; b < kB; ++b) load_zrow<kHop0>(a, ubase + j[b], ql, z0[b], z1[b]);
-#pragma unroll
             for (int b = 0; b < kB; ++b) {
-                const int e = e0 + b;
-                const int m = (e >= d1) + (e >= d2) + (e >= d3);
-                if (e < nslot && m != cur) {
-                    // each row's extras are one contiguous span: stash its sum once
-                    rq[cur * 16 + ql] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                    rq[cur * 16 + 8 + ql] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-                    cur = m;
+                if (kHop0) {
+                    z0[b] = bf16x4(__ldg(vrow + 16 * j[b]));
+                    z1[b] = bf16x4(__ldg(vrow + 16 * j[b] + 8));
+                } else {
+                    z0[b] = __ldg(zrow + 16 * j[b]);
+                    z1[b] = __ldg(zrow + 16 * j[b] + 8);
                 }
-                fma8f(acc, w[b], z0[b], z1[b]);    // w = 0 past the end
+            }
+            if (e0 + kB <= nb) {
+                // the whole batch belongs to row cur (slots past the end carry weight 0)
+#pragma unroll
+                for (int b = 0; b < kB; ++b) ffma8(acc, w[b], z0[b], z1[b]);
+            } else {
+#pragma unroll
+                for (int b = 0; b < kB; ++b) {
+                    const int e = e0 + b;
+                    const int m = (e >= d1) + (e >= d2) + (e >= d3);
+                    if (e < nslot && m != cur) {
+                        // each row's extras are one contiguous span: stash its sum once
+                        stash();
+                        cur = m;
+                        nb = m == 1 ? d2 : (m == 2 ? d3 : nslot);
+                    }
+                    ffma8(acc, w[b], z0[b], z1[b]);
+                }
             }
         }
-        if (nslot > 0) {
-            rq[cur * 16 + ql] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            rq[cur * 16 + 8 + ql] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        }
+        if (nslot > 0) stash();
         __syncwarp();
-        // each row: add the globals outside its window, write P_i
+        // each row: write P_i
         for (int m = 0; m < 4; ++m) {
             const int64_t i = ib + m;
             if (i >= P.n || a.is_global[i]) continue;     // uniform within the quarter
             const float4 r0 = rq[m * 16 + ql], r1 = rq[m * 16 + 8 + ql];
-            float v[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-            const float* wg = a.A_gc + ((size_t)u * P.n + i) * P.g_pad;
-            for (int s0 = 0; s0 < g; s0 += 8) {
-                const float wv = s0 + ql < g ? __ldg(wg + s0 + ql) : 0.f;
-                const int cnt = g - s0 < 8 ? g - s0 : 8;
-                for (int b = 0; b < cnt; ++b) {
-                    const float wb = __shfl_sync(qmask, wv, b, 8);
-                    fma8f(v, wb, sG[(s0 + b) * 16 + ql], sG[(s0 + b) * 16 + 8 + ql]);
-                }
-            }
+            float2 v[4] = {make_float2(r0.x, r0.y), make_float2(r0.z, r0.w), make_float2(r1.x, r1.y),
+                           make_float2(r1.z, r1.w)};
             float4* pr = reinterpret_cast<float4*>(a.Psum + ((size_t)u * P.n + i) * kHeadDim);
-            pr[ql] = make_float4(v[0], v[1], v[2], v[3]);
-            pr[8 + ql] = make_float4(v[4], v[5], v[6], v[7]);
+            pr[ql] = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+            pr[8 + ql] = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
         }
         __syncwarp();                                     // rq is reused by the next tile
     }
 }
 
 // the gather configuration: rows in flight per quarter-warp, CTAs per SM
-constexpr int kGatherBatch = 4, kGatherBlocks = 4;
+constexpr int kGatherBatch = 6, kGatherBlocks = 3;
 
 // bf16 tensor map over rows of `row_elems` elements: box of 64 elements x 64 rows
 int encode_rows(CUtensorMap* m, const void* base, int64_t n, int64_t units, int row_elems) {
@@ -595,7 +671,7 @@ int launch_hop(const CUtensorMap& tmZ, const HopArgs& a, cudaStream_t stream) {
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(hop_band_kernel<kHop0, kLast>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesMax);
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(hop)");
     const int sms = sm_count();
@@ -611,13 +687,13 @@ int launch_hop(const CUtensorMap& tmZ, const HopArgs& a, cudaStream_t stream) {
     dim3 grid((unsigned)(total_tiles < sms ? total_tiles : sms));
     {
         LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
-        hop_band_kernel<kHop0, kLast><<<grid, kThreads, kSmemBytes, stream>>>(tmZ, a);
+        hop_band_kernel<kHop0, kLast><<<grid, kThreads, band_smem_bytes(a.plan.g16), stream>>>(tmZ, a);
     }
     err = cudaGetLastError();
     if (err != cudaSuccess) return cuda_fail(err, "hop_band_kernel");
     if (a.plan.g > 0) {
         LaunchScope scope(DIFFUSER_KERNEL_GATHER, stream);
-        hop_global_rows_kernel<kLast><<<(unsigned)a.units, 256, 0, stream>>>(a);
+        hop_global_rows_kernel<kLast><<<(unsigned)a.units, kGRThreads, 0, stream>>>(a);
     }
     err = cudaGetLastError();
     return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_global_rows_kernel");
@@ -649,6 +725,7 @@ band::Weights band_weights(char* ws, const BandLayout& L) {
     band::Weights w;
     w.A_band = reinterpret_cast<__nv_bfloat16*>(ws + L.a_band);
     w.A_gc = reinterpret_cast<float*>(ws + L.a_gc);
+    w.A_gcimg = reinterpret_cast<uint8_t*>(ws + L.a_gcimg);
     w.A_x = reinterpret_cast<float*>(ws + L.a_x);
     w.A_gr = reinterpret_cast<float*>(ws + L.a_gr);
     w.A_gimg = reinterpret_cast<uint8_t*>(ws + L.a_gimg);
@@ -667,6 +744,7 @@ bool band_plan(const diffuser_graph* g, BandPlan* p) {
     p->g = g->n_globals;
     p->g_pad = (g->n_globals + 3) / 4 * 4;
     if (p->g_pad == 0) p->g_pad = 4;
+    p->g16 = (g->n_globals + 15) / 16 * 16;
     p->tiles = (int32_t)((g->n + kTileRows - 1) / kTileRows);
     p->chunks = (int32_t)((p->r64 + kTileRows + g->r + kChunkKeys - 1) / kChunkKeys);
     p->band_unit = (size_t)p->tiles * p->chunks * band::kChunkImageBytes;
@@ -681,6 +759,7 @@ int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     const size_t gg = p.g > 0 ? (size_t)p.g : 1;
     L->a_band = take(U * p.band_unit);
     L->a_gc = take(U * (size_t)p.n * p.g_pad * 4);
+    L->a_gcimg = take(U * (size_t)p.tiles * 2 * band::gc_plane_bytes(p.g16 > 0 ? p.g16 : 16));
     L->a_x = take(U * (size_t)(g->nx > 0 ? g->nx : 1) * 4);
     L->a_gr = take(U * gg * p.n * 4);
     L->a_gimg = take(U * (size_t)p.tiles * band::kGImgBytes);
@@ -723,6 +802,7 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     a.inv_l = reinterpret_cast<const float*>(ws + L.inv_l);
     a.Psum = reinterpret_cast<float*>(ws + L.psum);
     a.A_band = reinterpret_cast<const __nv_bfloat16*>(ws + L.a_band);
+    a.A_gcimg = reinterpret_cast<const uint8_t*>(ws + L.a_gcimg);
     a.V = static_cast<const __nv_bfloat16*>(V);
     a.gpart = reinterpret_cast<float*>(ws + L.gpart);
     a.counters = reinterpret_cast<int*>(ws + L.counters);

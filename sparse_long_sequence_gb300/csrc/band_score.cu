@@ -17,7 +17,8 @@
 //    rows' (max, 1/sum), normalizes their weights and writes each tile's
 //    global-row operand image.
 //  * score_finalize_kernel: a warp per row turns the sparse raw scores into
-//    e = exp(s - m_i) and stores inv_l = 1 / (band sum + sparse sum).
+//    e = exp(s - m_i) (the out-of-window globals' as a tensor-core operand
+//    image) and stores inv_l = 1 / (band sum + sparse sum).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -253,11 +254,17 @@ score_finalize_kernel(ScoreArgs a) {
     const size_t row = (size_t)u * P.n + i;
     const float m = a.w.m_sparse[row];
     float l = 0.f;
-    if (lane < P.g) {
-        float* wg = a.w.A_gc + row * P.g_pad + lane;
-        const float e = expf(*wg - m);          // exp(-inf) = 0 inside the window
-        *wg = e;
+    if (lane < P.g16) {
+        // the tile's out-of-window globals' operand image (hi, lo planes)
+        const float e = lane < P.g ? expf(a.w.A_gc[row * P.g_pad + lane] - m) : 0.f;   // exp(-inf) = 0
         l += e;
+        const int64_t tile = i / kTileRows;
+        uint8_t* img = a.w.A_gcimg + (size_t)(u * P.tiles + tile) * 2 * band::gc_plane_bytes(P.g16) +
+                       band::gc_offset((int)(i - tile * kTileRows), lane, P.g16);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(e);
+        *reinterpret_cast<__nv_bfloat16*>(img) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(img + band::gc_plane_bytes(P.g16)) =
+            __float2bfloat16_rn(e - __bfloat162float(hi));
     }
     const int64_t e0 = a.gr.x_ptr[i], e1 = a.gr.x_ptr[i + 1];
     float* wx = a.w.A_x + (size_t)u * a.gr.nx;
@@ -601,7 +608,7 @@ band_to_csr_kernel(ScoreArgs a, const int64_t* __restrict__ row_ptr,
     const uint8_t* timg = reinterpret_cast<const uint8_t*>(a.w.A_band) +
                           (size_t)(u * P.tiles + tile) * P.chunks * band::kChunkImageBytes +
                           (t >> 3) * 1024 + (t & 7) * 128;
-    const float* Agc = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
+    const uint8_t* gcimg = a.w.A_gcimg + (size_t)(u * P.tiles + tile) * 2 * band::gc_plane_bytes(P.g16);
     const float* Ax = a.w.A_x + (size_t)u * a.gr.nx;
     int64_t xb = a.gr.x_ptr[i];
     // extras are the row's edges that are neither window nor global, in order
@@ -620,7 +627,11 @@ band_to_csr_kernel(ScoreArgs a, const int64_t* __restrict__ row_ptr,
                 v = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(pe)) +
                     __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(pe + band::kChunkPlaneBytes));
             }
-            else if (a.gr.is_global[j]) v = Agc[a.gr.gslot[j]];
+            else if (a.gr.is_global[j]) {
+                const uint8_t* pe = gcimg + band::gc_offset((int)t, a.gr.gslot[j], P.g16);
+                v = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(pe)) +
+                    __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(pe + band::gc_plane_bytes(P.g16)));
+            }
             else v = Ax[xb + rank];
             o[e] = v * inv;
         }

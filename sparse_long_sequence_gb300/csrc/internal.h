@@ -27,6 +27,7 @@ struct BandPlan {
     int32_t r;          // window radius
     int32_t r64;        // the radius rounded up to a multiple of 64 (start of a tile's key chunks)
     int32_t g, g_pad;   // number of globals, padded to a multiple of 4
+    int32_t g16;        // g rounded up to 16 (the K of the out-of-window globals' MMA), 0 if g = 0
     int32_t tiles;      // 128-row tiles per unit
     int32_t chunks;     // 64-key chunks per tile
     size_t band_unit;   // bytes of one unit's band weights (tiles x chunks x 32 KB)
@@ -34,7 +35,7 @@ struct BandPlan {
 
 // Byte offsets of the band path's workspace regions.
 struct BandLayout {
-    size_t a_band, a_gc, a_x, a_gr, a_gimg;
+    size_t a_band, a_gc, a_gcimg, a_x, a_gr, a_gimg;
     size_t z[2];        // hop state Z_k, [units][n][hi 64 | lo 64] bf16, ping-pong
     size_t zf[2];       // the same Z_k as fp32 rows [units][n][64] (row gathers)
     size_t psum;        // sparse partial of the rows not in G, [units][n][64] fp32

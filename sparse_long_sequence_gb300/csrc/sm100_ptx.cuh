@@ -216,6 +216,19 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor: K-major, no swizzle.  Core matrices of
+// 8 rows x 16 bytes (rows 16 bytes apart); the next core matrix along K starts
+// `k_core_bytes` on, the next 8 rows `row8_bytes` on.
+__device__ __forceinline__ uint64_t noswz_kmajor_desc(uint32_t saddr, uint32_t k_core_bytes,
+                                                      uint32_t row8_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((k_core_bytes >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((row8_bytes >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;                              // layout field 0: no swizzle
+}
+
 // Shared-memory matrix descriptor: MN-major, 128-byte swizzle.  Each K row
 // holds 64 consecutive 16-bit MN elements (128 bytes); 8 K rows form a
 // 1024-byte swizzle atom, K atoms are 1024 bytes apart, and the next 64 MN
