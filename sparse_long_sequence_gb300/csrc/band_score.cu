@@ -2,23 +2,21 @@
 // sequences with multi-hop attention diffusion", eq S.1-S.5; "1.2.1 Static
 // sparsity", eq 1-3), in four kernels:
 //
-//  * score_sparse_kernel: per row, the raw scores q_i.k_j/8 of the globals
-//    outside the window (-inf inside it) and of the random extras, and their
-//    maximum; a quarter-warp per row, each K row read as one 128-byte line,
-//    8 dot products reduced across the quarter at once.  Per tile, the raw
-//    scores of the global rows against the tile's keys with per-tile
-//    (max, sum of exp).
+//  * score_sparse_kernel: per row, the raw scores q_i.k_j/8 of the random
+//    extras and their maximum; a quarter-warp per row, each K row read as one
+//    128-byte line, 8 dot products reduced across the quarter at once.
 //  * score_band_tc_kernel (tcgen05, persistent): S = Q K^T for a 128-row
 //    tile against 64-key chunks of its window on bf16 tensor cores (fp32
 //    accumulation in TMEM), in two passes over the chunks: the row maximum
-//    m_i (band and sparse), then e = exp(s - m_i) written as the tile's
-//    operand image, and the band part of the row sum.
-//  * score_global_norm_kernel: merges the per-tile statistics into the global
-//    rows' (max, 1/sum), normalizes their weights and writes each tile's
-//    global-row operand image.
-//  * score_finalize_kernel: a warp per row turns the sparse raw scores into
-//    e = exp(s - m_i) (the out-of-window globals' as a tensor-core operand
-//    image) and stores inv_l = 1 / (band sum + sparse sum).
+//    m_i, then e = exp(s - m_i) written as the tile's operand image, and the
+//    band part of the row sum.  On the same tensor cores: q_i.k_G for the
+//    globals outside each row's window (N = g16; their e as an operand image)
+//    and q_G.k_j for the global rows against the tile's own keys (raw scores).
+//  * score_global_norm_kernel: per global row, its (max, 1/sum) over all keys,
+//    the normalized weights, and its row of each tile's global-row operand
+//    image.
+//  * score_finalize_kernel: a warp per row turns the extras' raw scores into
+//    e = exp(s - m_i) and stores inv_l = 1 / (band + globals + extras sum).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -46,20 +44,9 @@ struct ScoreArgs {
     band::GraphRefs gr;
     band::Weights w;
     int* counters;      // [units] tile tickets
+    const __nv_bfloat16* Q;
+    const __nv_bfloat16* K;
 };
-
-__device__ __forceinline__ void load_row64(const __nv_bfloat16* p, float (&x)[64]) {
-    const uint4* v = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 w = __ldg(v + c);
-        x[8 * c + 0] = bf16lo(w.x); x[8 * c + 1] = bf16hi(w.x);
-        x[8 * c + 2] = bf16lo(w.y); x[8 * c + 3] = bf16hi(w.y);
-        x[8 * c + 4] = bf16lo(w.z); x[8 * c + 5] = bf16hi(w.z);
-        x[8 * c + 6] = bf16lo(w.w); x[8 * c + 7] = bf16hi(w.w);
-    }
-}
-
 
 // ---------------------------------------------------------------- sparse scores
 constexpr int kSparseThreads = 256;
@@ -95,105 +82,23 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
 __global__ void __launch_bounds__(kSparseThreads, 2)
 score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
                     const __nv_bfloat16* __restrict__ K) {
-    __shared__ float4 sQG[kBandMaxGlobals * 16];   // q rows of the global positions (fp32)
-    __shared__ float4 sKG[kBandMaxGlobals * 16];   // k rows of the global positions (fp32)
-    __shared__ float scr[kBandMaxGlobals * kTileRows];   // the global rows' scores of this tile's keys
     const BandPlan& P = a.plan;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t u = blockIdx.x / P.tiles;
     const int tile = (int)(blockIdx.x - u * P.tiles);
     const int64_t i0 = (int64_t)tile * kTileRows;
-    const int g = P.g;
     const __nv_bfloat16* Qu = Q + (size_t)u * P.n * kHeadDim;
     const __nv_bfloat16* Ku = K + (size_t)u * P.n * kHeadDim;
-    for (int e = tid; e < g * 8; e += kSparseThreads) {
-        const int sl = e >> 3, p = e & 7;
-        const size_t off = (size_t)a.gr.globals[sl] * kHeadDim;
-        float x[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(Qu + off) + p), x);
-        sQG[sl * 16 + 2 * p] = make_float4(x[0], x[1], x[2], x[3]);
-        sQG[sl * 16 + 2 * p + 1] = make_float4(x[4], x[5], x[6], x[7]);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(Ku + off) + p), x);
-        sKG[sl * 16 + 2 * p] = make_float4(x[0], x[1], x[2], x[3]);
-        sKG[sl * 16 + 2 * p + 1] = make_float4(x[4], x[5], x[6], x[7]);
-    }
-    __syncthreads();
-
-    if (g > 0) {
-        // (1) global rows x this tile's keys: thread t < 128 owns key j = i0 + t
-        if (tid < kTileRows) {
-            const int64_t j = i0 + tid;
-            if (j < P.n) {
-                float k[64];
-                load_row64(Ku + (size_t)j * kHeadDim, k);
-                for (int s = 0; s < g; ++s) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float4 q = sQG[s * 16 + c];
-                        acc = fmaf(q.x, k[4 * c], acc); acc = fmaf(q.y, k[4 * c + 1], acc);
-                        acc = fmaf(q.z, k[4 * c + 2], acc); acc = fmaf(q.w, k[4 * c + 3], acc);
-                    }
-                    const float sc = acc * kScale;
-                    a.w.A_gr[((size_t)u * g + s) * P.n + j] = sc;
-                    scr[s * kTileRows + tid] = sc;
-                }
-            } else {
-                for (int s = 0; s < g; ++s) scr[s * kTileRows + tid] = -INFINITY;
-            }
-        }
-        __syncthreads();
-        // per-tile (max, sum of exp) of each global row: one warp per row slot
-        for (int s = warp; s < g; s += kSparseThreads / 32) {
-            float m = -INFINITY;
-            for (int t = lane; t < kTileRows; t += 32) m = fmaxf(m, scr[s * kTileRows + t]);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            float l = 0.f;
-            for (int t = lane; t < kTileRows; t += 32) {
-                const float v = scr[s * kTileRows + t];
-                l += v == -INFINITY ? 0.f : expf(v - m);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-            if (lane == 0) {
-                float* st = a.w.sstat + (((size_t)u * P.tiles + tile) * g + s) * 2;
-                st[0] = m;
-                st[1] = l;
-            }
-        }
-    }
-    // (2) rows of this tile: quarter-warp qi owns rows 4 qi .. +3; lane ql holds
-    //     features 8 ql .. +7 of q_i and reads the same 16 bytes of each k row
+    // quarter-warp qi owns rows 4 qi .. +3; lane ql holds features 8 ql .. +7 of
+    // q_i and reads the same 16 bytes of each k row (whole 128-byte lines)
     const int ql = lane & 7, qi = 4 * warp + (lane >> 3);
     const unsigned qmask = 0xffu << (lane & 24);
     for (int mrow = 0; mrow < 4; ++mrow) {
         const int64_t i = i0 + 4 * qi + mrow;
         if (i >= P.n || a.gr.is_global[i]) continue;      // uniform within the quarter
-        const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
-        const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
         float q[8];
         unpack8(__ldg(reinterpret_cast<const uint4*>(Qu + (size_t)i * kHeadDim) + ql), q);
         float m = -INFINITY;
-        float* wg = a.w.A_gc + ((size_t)u * P.n + i) * P.g_pad;
-        for (int s0 = 0; s0 < g; s0 += 8) {
-            float v[8];
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                const int sl = s0 + b < g ? s0 + b : 0;
-                const float4 k0 = sKG[sl * 16 + 2 * ql], k1 = sKG[sl * 16 + 2 * ql + 1];
-                v[b] = q[0] * k0.x + q[1] * k0.y + q[2] * k0.z + q[3] * k0.w +
-                       q[4] * k1.x + q[5] * k1.y + q[6] * k1.z + q[7] * k1.w;
-            }
-            const float dot = reduce8_transpose(v, ql, qmask);   // slot s0 + ql
-            const int sl = s0 + ql;
-            if (sl < g) {
-                const int64_t j = a.gr.globals[sl];
-                const float sc = (j < lo || j > hi) ? dot * kScale : -INFINITY;   // -inf: inside the window
-                wg[sl] = sc;
-                m = fmaxf(m, sc);
-            }
-        }
         const int64_t e0 = a.gr.x_ptr[i], e1 = a.gr.x_ptr[i + 1];
         float* wx = a.w.A_x + (size_t)u * a.gr.nx;
         // 32 slots at a time: their columns loaded together (4 per lane), then four
@@ -254,18 +159,6 @@ score_finalize_kernel(ScoreArgs a) {
     const size_t row = (size_t)u * P.n + i;
     const float m = a.w.m_sparse[row];
     float l = 0.f;
-    if (lane < P.g16) {
-        // the tile's out-of-window globals' operand image (hi, lo planes)
-        const float e = lane < P.g ? expf(a.w.A_gc[row * P.g_pad + lane] - m) : 0.f;   // exp(-inf) = 0
-        l += e;
-        const int64_t tile = i / kTileRows;
-        uint8_t* img = a.w.A_gcimg + (size_t)(u * P.tiles + tile) * 2 * band::gc_plane_bytes(P.g16) +
-                       band::gc_offset((int)(i - tile * kTileRows), lane, P.g16);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(e);
-        *reinterpret_cast<__nv_bfloat16*>(img) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(img + band::gc_plane_bytes(P.g16)) =
-            __float2bfloat16_rn(e - __bfloat162float(hi));
-    }
     const int64_t e0 = a.gr.x_ptr[i], e1 = a.gr.x_ptr[i + 1];
     float* wx = a.w.A_x + (size_t)u * a.gr.nx;
     for (int64_t e = e0 + lane; e < e1; e += 32) {
@@ -289,15 +182,57 @@ constexpr int kRowWarp0 = 4;
 constexpr int kRowThreads = 256;
 constexpr int kSChunk = 64;              // keys per chunk (MMA N)
 constexpr int kKStages = 8;              // smem ring of K chunks (8 KB each)
-constexpr int kSBufs = 8;                // TMEM S buffers (64 columns each)
+constexpr int kSBufs = 5;                // TMEM S buffers (64 columns each), columns 0..319
+constexpr int kGcCol0 = 320;             // q_i . k_G (out-of-window globals): 2 x 32 columns
+constexpr int kGrCol0 = 384;             // q_G . k_j of the tile's own keys: 2 chunks x 64 columns
+constexpr int kGBufBytes = kBandMaxGlobals * 128;   // k or q rows of the globals (bf16, 128-byte swizzle)
 constexpr int kBTmemCols = 512;
 constexpr int kQBytes = kTileRows * kHeadDim * 2;
 constexpr int kKBytes = kSChunk * kHeadDim * 2;
-constexpr int kBSmemUsed = 1024 + 2 * kQBytes + kKStages * kKBytes + 2 * band::kChunkImageBytes +
-                           2 * kRowThreads * 4 + 512;
+// the globals' q rows (the A operand of the global rows' scores; its descriptor
+// spans 16 KB, so the buffers sit in front of larger ones) and k rows, 2 of each
+constexpr int kBSmemUsed = 1024 + 2 * kQBytes + 2 * 2 * kGBufBytes + kKStages * kKBytes +
+                           2 * band::kChunkImageBytes + 2 * kRowThreads * 4 + 512 + 4 * kBandMaxGlobals;
 // request at least 120 KB so that the shared memory alone keeps it to one CTA per SM
 constexpr int kBSmemBytes = kBSmemUsed > 120 * 1024 ? kBSmemUsed : 120 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// The two warps of TMEM lane quadrant 0 (lanes = global slots s): the global
+// rows' raw scores against the tile's own keys (half hcol: keys i0 + 64 hcol
+// .. +63), stored in A_gr.
+__device__ __forceinline__ void global_row_scores(const ScoreArgs& a, int64_t u, int64_t i0, int lt, int hcol,
+                                                  int lane, uint32_t tmem, uint64_t* full_GR,
+                                                  uint64_t* empty_GR, int* status) {
+    const BandPlan& P = a.plan;
+    ptx::mbar_wait(full_GR, lt & 1, status);
+    __syncwarp();
+    ptx::tc_fence_after();
+    float v0[32], v1[32];
+    ptx::tmem_ld32(tmem + kGrCol0 + kSChunk * hcol, v0);
+    ptx::tmem_ld32(tmem + kGrCol0 + kSChunk * hcol + 32, v1);
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(empty_GR);
+    const int64_t jb = i0 + kSChunk * hcol;
+    if (lane < P.g && jb < P.n) {
+        float* dst = a.w.A_gr + ((size_t)u * P.g + lane) * P.n + jb;
+        if (jb + kSChunk <= P.n && (P.n & 3) == 0) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                reinterpret_cast<float4*>(dst)[c] = make_float4(v0[4 * c] * kScale, v0[4 * c + 1] * kScale,
+                                                                v0[4 * c + 2] * kScale, v0[4 * c + 3] * kScale);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                reinterpret_cast<float4*>(dst + 32)[c] = make_float4(v1[4 * c] * kScale, v1[4 * c + 1] * kScale,
+                                                                     v1[4 * c + 2] * kScale, v1[4 * c + 3] * kScale);
+        } else {
+            const int nk = (int)(P.n - jb < kSChunk ? P.n - jb : kSChunk);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) if (k < nk) dst[k] = v0[k] * kScale;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) if (32 + k < nk) dst[32 + k] = v1[k] * kScale;
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kBThreads, 1)
 score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -306,7 +241,9 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* sQ = smem;                                   // 2 x 16 KB
-    uint8_t* sK = sQ + 2 * kQBytes;                       // kKStages x 8 KB
+    uint8_t* sQG = sQ + 2 * kQBytes;                      // 2 x the globals' q rows
+    uint8_t* sKG = sQG + 2 * kGBufBytes;                  // 2 x the globals' k rows
+    uint8_t* sK = sKG + 2 * kGBufBytes;                   // kKStages x 8 KB
     uint8_t* sOut = sK + kKStages * kKBytes;                  // 2 x one chunk's weight image
     float* xch = reinterpret_cast<float*>(sOut + 2 * band::kChunkImageBytes);   // [2][256] row partials
     uint64_t* bars = reinterpret_cast<uint64_t*>(xch + 2 * kRowThreads);
@@ -316,7 +253,12 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     uint64_t* empty_K = full_K + kKStages;
     uint64_t* full_S = empty_K + kKStages;    // [kSBufs]
     uint64_t* empty_S = full_S + kSBufs;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_S + kSBufs);
+    uint64_t* full_G = empty_S + kSBufs;      // [2] the globals' q and k rows staged
+    uint64_t* empty_G = full_G + 2;           // [2]
+    uint64_t* full_GR = empty_G + 2;          // the global rows' scores of the tile are in TMEM
+    uint64_t* empty_GR = full_GR + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_GR + 1);
+    int* sGpos = reinterpret_cast<int*>(tmem_slot + 2);            // the global positions
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -325,14 +267,20 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int64_t total_tiles = a.units * P.tiles;
     const int my_tiles = blockIdx.x < total_tiles
         ? (int)((total_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+    const bool has_g = P.g > 0;
+    const int c0 = P.r64 / kSChunk;                       // chunks c0, c0 + 1: the tile's own keys
 
     if (warp == 1) ptx::tmem_alloc(tmem_slot, kBTmemCols);
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) { ptx::mbar_init(&full_Q[s], 1); ptx::mbar_init(&empty_Q[s], 1); }
         for (int s = 0; s < kKStages; ++s) { ptx::mbar_init(&full_K[s], 1); ptx::mbar_init(&empty_K[s], 1); }
         for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], kRowThreads); }
+        for (int s = 0; s < 2; ++s) { ptx::mbar_init(&full_G[s], 1); ptx::mbar_init(&empty_G[s], 1); }
+        ptx::mbar_init(full_GR, 1);
+        ptx::mbar_init(empty_GR, 64);
         ptx::fence_mbar_init();
     }
+    if (tid < kBandMaxGlobals) sGpos[tid] = tid < P.g ? a.gr.globals[tid] : 0;
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -361,10 +309,22 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::mma_idesc(1, kSChunk);
+            const uint32_t idesc_gc = ptx::mma_idesc(1, P.g16 > 0 ? P.g16 : 16);
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const int qb = lt & 1;
                 ptx::mbar_wait(&full_Q[qb], (lt / 2) & 1, status);
                 const uint32_t qa = ptx::smem_u32(sQ + qb * kQBytes);
+                const uint32_t qg = ptx::smem_u32(sQG + qb * kGBufBytes);
+                if (has_g) {
+                    // q_i . k_G for the tile's rows (N = g16) into columns kGcCol0 + 32 (lt & 1)
+                    ptx::mbar_wait(&full_G[qb], (lt / 2) & 1, status);
+                    ptx::tc_fence_after();
+                    const uint32_t kg = ptx::smem_u32(sKG + qb * kGBufBytes);
+#pragma unroll
+                    for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                        ptx::mma_bf16_ss(tmem + kGcCol0 + 32 * qb, ptx::sw128_kmajor_desc(qa + 32 * ks),
+                                         ptx::sw128_kmajor_desc(kg + 32 * ks), idesc_gc, ks > 0);
+                }
                 for (int it = 0; it < per_tile; ++it) {
                     const int gi = lt * per_tile + it;
                     const int s = gi % kKStages, b = gi % kSBufs;
@@ -376,6 +336,21 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     for (int ks = 0; ks < kHeadDim / 16; ++ks)
                         ptx::mma_bf16_ss(tmem + kSChunk * b, ptx::sw128_kmajor_desc(qa + 32 * ks),
                                          ptx::sw128_kmajor_desc(kb + 32 * ks), idesc, ks > 0);
+                    const int h = it - c0;
+                    if (has_g && (h == 0 || h == 1)) {
+                        // q_G . k_j for the tile's own keys (the global rows' scores):
+                        // rows 0..g-1 of an M = 128 operand whose other rows are not used
+                        if (h == 0 && lt >= 1) ptx::mbar_wait(empty_GR, (lt - 1) & 1, status);
+                        ptx::tc_fence_after();
+#pragma unroll
+                        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                            ptx::mma_bf16_ss(tmem + kGrCol0 + kSChunk * h, ptx::sw128_kmajor_desc(qg + 32 * ks),
+                                             ptx::sw128_kmajor_desc(kb + 32 * ks), idesc, ks > 0);
+                        if (h == 1) {
+                            ptx::mma_commit(full_GR);
+                            ptx::mma_commit(&empty_G[qb]);
+                        }
+                    }
                     ptx::mma_commit(&empty_K[s]);
                     ptx::mma_commit(&full_S[b]);
                 }
@@ -390,10 +365,38 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             for (int s = 0; s < 2; ++s) {
                 const int uses = (my_tiles - s + 1) / 2;
                 if (uses > 0) ptx::mbar_wait(&empty_Q[s], (uses - 1) & 1, status);
+                if (has_g && uses > 0) ptx::mbar_wait(&empty_G[s], (uses - 1) & 1, status);
+            }
+        }
+    } else if (warp == 2) {
+        // the globals' q rows (A operand of the global rows' scores) and k rows
+        // (B operand of the out-of-window globals' scores) of the tile's unit,
+        // 128-byte swizzled: row s, 16-byte piece c at s * 128 + (c ^ (s % 8)) * 16
+        if (has_g) {
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+                const int64_t u = tix / P.tiles;
+                const int qb = lt & 1;
+                if (lt >= 2) ptx::mbar_wait(&empty_G[qb], ((lt / 2) - 1) & 1, status);
+                for (int e = lane; e < kBandMaxGlobals * 8; e += 32) {
+                    const int sl = e >> 3, cch = e & 7;
+                    uint4 qv = make_uint4(0u, 0u, 0u, 0u), kv = qv;
+                    if (sl < P.g) {
+                        const size_t off = ((size_t)u * P.n + a.gr.globals[sl]) * kHeadDim;
+                        qv = __ldg(reinterpret_cast<const uint4*>(a.Q + off) + cch);
+                        kv = __ldg(reinterpret_cast<const uint4*>(a.K + off) + cch);
+                    }
+                    const int o = sl * 128 + ((cch ^ (sl & 7)) << 4);
+                    *reinterpret_cast<uint4*>(sQG + qb * kGBufBytes + o) = qv;
+                    *reinterpret_cast<uint4*>(sKG + qb * kGBufBytes + o) = kv;
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&full_G[qb]);
             }
         }
     } else if (warp < kRowWarp0) {
-        // warps 2-3 have no role
+        // warp 3 has no role
     } else {
         const int rw = warp - kRowWarp0;          // 0..7
         const int quad = warp & 3, hcol = rw >> 2;
@@ -427,12 +430,25 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 const int b = gi % kSBufs, c = it % nc;
                 const bool pass2 = it >= nc;
                 if (it == nc) {
-                    // both column halves of a row agree on the row maximum
+                    // both column halves of a row agree on the row maximum (band, the
+                    // out-of-window globals, and the extras from score_sparse_kernel)
                     xch[rtid] = mraw;
                     ptx::named_barrier_sync(pair_bar, 64);
                     const float other = xch[(rtid + 128) & 255];
                     const float ms = row_ok ? a.w.m_sparse[(size_t)u * P.n + i] : 0.f;
                     m = fmaxf(ms, fmaxf(mraw, other) * kScale);
+                    if (has_g) {
+                        float gs[32];
+                        ptx::tmem_ld32(tmem + lane_base + kGcCol0 + 32 * (lt & 1), gs);
+#pragma unroll
+                        for (int sl = 0; sl < kBandMaxGlobals; ++sl) {
+                            if (sl < P.g) {
+                                const int64_t j = sGpos[sl];
+                                if (row_ok && (j < lo || j > hi)) m = fmaxf(m, gs[sl] * kScale);
+                            }
+                        }
+                        if (quad == 0) global_row_scores(a, u, i0, lt, hcol, lane, tmem, full_GR, empty_GR, status);
+                    }
                     b2 = m * kLog2e;
                     ptx::named_barrier_sync(pair_bar, 64);     // xch is reused below
                 }
@@ -508,7 +524,40 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     }
                 }
             }
-            // the row's maximum m_i and the band part of its sum (score_finalize_kernel adds the rest)
+            if (has_g) {
+                // the out-of-window globals: e = exp(s - m) as the tile's operand image
+                // (this half's slots 8 hcol .. +7 and 16 + 8 hcol .. +7; 0 inside the window)
+                float gs[32];
+                ptx::tmem_ld32(tmem + lane_base + kGcCol0 + 32 * (lt & 1), gs);
+                uint8_t* img = a.w.A_gcimg + (size_t)tix * 2 * band::gc_plane_bytes(P.g16);
+#pragma unroll
+                for (int q8 = 0; q8 < kBandMaxGlobals / 8; ++q8) {
+                    if ((q8 & 1) != hcol || 8 * q8 >= P.g16) continue;
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int p2 = 0; p2 < 4; ++p2) {
+                        float x[2];
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int sl = 8 * q8 + 2 * p2 + h2;
+                            const int64_t j = sGpos[sl < P.g ? sl : 0];
+                            x[h2] = (row_ok && sl < P.g && (j < lo || j > hi))
+                                        ? ptx::ex2_approx(fmaf(gs[sl], a_sc, -b2)) : 0.f;
+                            lsum += x[h2];
+                        }
+                        const __nv_bfloat162 hh = __floats2bfloat162_rn(x[0], x[1]);
+                        const __nv_bfloat162 ll =
+                            __floats2bfloat162_rn(x[0] - __low2float(hh), x[1] - __high2float(hh));
+                        hw[p2] = *reinterpret_cast<const uint32_t*>(&hh);
+                        lw[p2] = *reinterpret_cast<const uint32_t*>(&ll);
+                    }
+                    uint8_t* pe = img + band::gc_offset(t, 8 * q8, P.g16);
+                    *reinterpret_cast<uint4*>(pe) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(pe + band::gc_plane_bytes(P.g16)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+            // the row's maximum m_i and the band and globals' part of its sum
+            // (score_finalize_kernel adds the extras)
             xch[rtid] = lsum;
             ptx::named_barrier_sync(pair_bar, 64);
             if (hcol == 0 && row_ok) {
@@ -525,61 +574,58 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 }
 
 // ---------------------------------------------------------------- global rows' weights
-// One CTA per (unit, 128-key tile): A_gr = exp(s - max) / sum with the global
-// rows' (max, 1/sum) from score_sparse_kernel, in place, and the tile's
-// global-row operand image (hi / lo bf16; keys past n are 0).
-__global__ void __launch_bounds__(256)
+// One CTA per (unit, global row s): the row's max and sum of exp over all n
+// keys (fixed-order tree reductions), then A_gr = exp(s - max) / sum in place
+// and row s of every tile's global-row operand image (hi / lo bf16; keys past
+// n are 0).
+constexpr int kNormThreads = 256;
+
+__global__ void __launch_bounds__(kNormThreads)
 score_global_norm_kernel(ScoreArgs a) {
-    __shared__ float2 st[kBandMaxGlobals];        // (max, 1 / sum) of each global row
+    __shared__ float red[kNormThreads / 32];
     const BandPlan& P = a.plan;
-    const int64_t u = blockIdx.x / P.tiles;
-    const int64_t tile = blockIdx.x - u * P.tiles;
-    const int64_t i0 = tile * kTileRows;
-    // merge the per-tile (max, sum of exp) of every global row: 16 lanes per row,
-    // each lane over tiles l, l + 16, ..., in a fixed order
-    for (int s0 = 0; s0 < P.g; s0 += 16) {
-        const int sl = s0 + (threadIdx.x >> 4), l = threadIdx.x & 15;
-        const bool ok = sl < P.g;
-        float M = -INFINITY;
-        for (int tt = l; ok && tt < P.tiles; tt += 16)
-            M = fmaxf(M, __ldg(a.w.sstat + (((size_t)u * P.tiles + tt) * P.g + sl) * 2));
+    const int64_t u = blockIdx.x / P.g;
+    const int sl = (int)(blockIdx.x - u * P.g);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float* row = a.w.A_gr + ((size_t)u * P.g + sl) * P.n;
+    float mx = -INFINITY;
+    for (int64_t j = tid; j < P.n; j += kNormThreads) mx = fmaxf(mx, row[j]);
 #pragma unroll
-        for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off, 16));
-        float L = 0.f;
-        for (int tt = l; ok && tt < P.tiles; tt += 16) {
-            const float* sp = a.w.sstat + (((size_t)u * P.tiles + tt) * P.g + sl) * 2;
-            const float mt = __ldg(sp);
-            if (mt != -INFINITY) L += __ldg(sp + 1) * expf(mt - M);
-        }
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off, 16);
-        if (ok && l == 0) {
-            st[sl] = make_float2(M, 1.f / L);
-            if (tile == 0) {
-                a.w.gstat[((size_t)u * P.g + sl) * 2] = M;
-                a.w.gstat[((size_t)u * P.g + sl) * 2 + 1] = 1.f / L;
-            }
-        }
-    }
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[warp] = mx;
     __syncthreads();
-    uint8_t* gimg = a.w.A_gimg + (size_t)blockIdx.x * band::kGImgBytes;
-    for (int e = threadIdx.x; e < P.g * kTileRows; e += blockDim.x) {
-        const int sl = e / kTileRows, jj = e % kTileRows;
+    mx = red[0];
+#pragma unroll
+    for (int w = 1; w < kNormThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+    __syncthreads();
+    float l = 0.f;
+    for (int64_t j = tid; j < P.n; j += kNormThreads) l += expf(row[j] - mx);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    if (lane == 0) red[warp] = l;
+    __syncthreads();
+    l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kNormThreads / 32; ++w) l += red[w];
+    const float inv = 1.f / l;
+    if (tid == 0) {
+        a.w.gstat[((size_t)u * P.g + sl) * 2] = mx;
+        a.w.gstat[((size_t)u * P.g + sl) * 2 + 1] = inv;
+    }
+    const int64_t nkeys = (int64_t)P.tiles * kTileRows;
+    for (int64_t j = tid; j < nkeys; j += kNormThreads) {
         float w = 0.f;
-        if (i0 + jj < P.n) {
-            const float gm = st[sl].x;
-            const float ginv = st[sl].y;
-            float* v = a.w.A_gr + ((size_t)u * P.g + sl) * P.n + i0 + jj;
-            w = expf(*v - gm) * ginv;
-            *v = w;
+        if (j < P.n) {
+            w = expf(row[j] - mx) * inv;
+            row[j] = w;
         }
-        const int h = jj >> 6, k = jj & 63;
+        const int64_t tile = j / kTileRows;
+        const int jj = (int)(j - tile * kTileRows), h = jj >> 6, k = jj & 63;
+        uint8_t* pe = a.w.A_gimg + (size_t)(u * P.tiles + tile) * band::kGImgBytes + h * 2 * band::kGImgPlaneBytes +
+                      (sl >> 3) * 1024 + (sl & 7) * 128 + ((((k >> 3) ^ (sl & 7))) << 4) + (k & 7) * 2;
         const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
-        uint8_t* pe = gimg + h * 2 * band::kGImgPlaneBytes + (sl >> 3) * 1024 + (sl & 7) * 128 +
-                      ((((k >> 3) ^ (sl & 7))) << 4) + (k & 7) * 2;
         *reinterpret_cast<__nv_bfloat16*>(pe) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(pe + band::kGImgPlaneBytes) = lo;
+        *reinterpret_cast<__nv_bfloat16*>(pe + band::kGImgPlaneBytes) = __float2bfloat16_rn(w - __bfloat162float(hi));
     }
 }
 
@@ -661,6 +707,8 @@ ScoreArgs make_args(const diffuser_graph* g, const BandPlan& p, int64_t units, c
     s.gr = band_graph_refs(g);
     s.w = band_weights(ws, L);
     s.counters = reinterpret_cast<int*>(ws + L.counters);
+    s.Q = nullptr;
+    s.K = nullptr;
     return s;
 }
 
@@ -681,17 +729,14 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
     ScoreArgs a = make_args(g, p, units, ws, L);
     const auto* Qb = static_cast<const __nv_bfloat16*>(Q);
     const auto* Kb = static_cast<const __nv_bfloat16*>(K);
+    a.Q = Qb;
+    a.K = Kb;
     const unsigned grid = (unsigned)(units * p.tiles);
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
         score_sparse_kernel<<<grid, kSparseThreads, 0, stream>>>(a, Qb, Kb);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_sparse_kernel");
-    if (p.g > 0) {
-        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
-        score_global_norm_kernel<<<grid, 256, 0, stream>>>(a);
-    }
-    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_global_norm_kernel");
 
     auto fn = encode_fn();
     if (!fn) return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
@@ -723,6 +768,11 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
         score_band_tc_kernel<<<pgrid, kBThreads, kBSmemBytes, stream>>>(tmQ, tmK, a, g->d_status);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_band_tc_kernel");
+    if (p.g > 0) {
+        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
+        score_global_norm_kernel<<<(unsigned)(units * p.g), kNormThreads, 0, stream>>>(a);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_global_norm_kernel");
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
         score_finalize_kernel<<<(unsigned)((units * p.n + 7) / 8), 256, 0, stream>>>(a);
