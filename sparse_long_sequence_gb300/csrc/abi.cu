@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -30,6 +31,13 @@ std::mutex g_prof_mu;
 bool g_prof_on = false;
 std::vector<ProfileRecord> g_prof_records;
 std::vector<cudaEvent_t> g_event_pool;
+
+// ---- CUDA-graph capture: launches made while a capture context is set are
+// counted there (and credited at each replay) instead of in the counters ----
+struct CaptureCtx {
+    int64_t launches[DIFFUSER_KERNEL_KINDS] = {0};
+};
+thread_local CaptureCtx* t_capture = nullptr;
 
 cudaEvent_t take_event() {
     if (!g_event_pool.empty()) {
@@ -63,6 +71,11 @@ int cuda_fail(cudaError_t err, const char* what) {
 }
 
 LaunchScope::LaunchScope(diffuser_kernel_kind kind, cudaStream_t stream) : stream_(stream) {
+    if (t_capture) {
+        t_capture->launches[kind] += 1;    // counted at each replay
+        capture_slot_ = 0;
+        return;
+    }
     g_launches[kind].fetch_add(1, std::memory_order_relaxed);
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if (!g_prof_on) return;
@@ -74,6 +87,7 @@ LaunchScope::LaunchScope(diffuser_kernel_kind kind, cudaStream_t stream) : strea
 }
 
 LaunchScope::~LaunchScope() {
+    if (capture_slot_ >= 0) return;
     if (slot_ < 0) return;
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if (slot_ < (int)g_prof_records.size()) cudaEventRecord(g_prof_records[slot_].stop, stream_);
@@ -190,6 +204,141 @@ int run_hops_csr(const diffuser_graph* g, const CsrArgs& a, const float* A, cons
     return DIFFUSER_OK;
 }
 
+// ---- replay of captured band-path forwards ---------------------------------
+// The second forward with the same pointers, shape, hops, alpha and path is
+// captured on an internal stream into a CUDA graph; later ones replay it on
+// the caller's stream (launch counts are credited per replay).  While a
+// profile is open, and while the caller's stream is capturing its own graph,
+// forwards launch their kernels directly.
+struct ReplayKey {
+    const void *Q, *K, *V, *out, *ws;
+    size_t ws_bytes;
+    int64_t B, H;
+    int32_t dtype, hops;
+    float alpha;
+    int path;
+    bool operator==(const ReplayKey& o) const {
+        return Q == o.Q && K == o.K && V == o.V && out == o.out && ws == o.ws && ws_bytes == o.ws_bytes &&
+               B == o.B && H == o.H && dtype == o.dtype && hops == o.hops &&
+               std::memcmp(&alpha, &o.alpha, sizeof(float)) == 0 && path == o.path;
+    }
+};
+
+struct ReplayEntry {
+    ReplayKey key{};
+    uint64_t stamp = 0;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int64_t launches[DIFFUSER_KERNEL_KINDS] = {0};
+};
+
+struct ReplayCache {
+    std::mutex mu;
+    std::vector<ReplayEntry> entries;
+    uint64_t clock = 0;
+};
+
+namespace {
+constexpr size_t kReplayEntries = 4;
+constexpr int kMaxReplayDevices = 64;
+std::mutex g_capture_mu;
+cudaStream_t g_capture_stream[kMaxReplayDevices] = {nullptr};
+
+void destroy_entry(ReplayEntry& e) {
+    if (e.exec) cudaGraphExecDestroy(e.exec);
+    if (e.graph) cudaGraphDestroy(e.graph);
+    e = ReplayEntry{};
+}
+
+cudaStream_t capture_stream(int dev) {
+    if (dev < 0 || dev >= kMaxReplayDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_capture_mu);
+    if (!g_capture_stream[dev] &&
+        cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking) != cudaSuccess)
+        g_capture_stream[dev] = nullptr;
+    return g_capture_stream[dev];
+}
+
+int replay(ReplayEntry& e, cudaStream_t stream) {
+    for (int k = 0; k < DIFFUSER_KERNEL_KINDS; ++k)
+        g_launches[k].fetch_add(e.launches[k], std::memory_order_relaxed);
+    cudaError_t err = cudaGraphLaunch(e.exec, stream);
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "cudaGraphLaunch(forward)");
+}
+
+// Captures `launch` (which enqueues the forward on the stream it is given) into
+// e; false when capture or instantiation is not possible (nothing is kept).
+template <class Launch>
+bool capture(ReplayEntry& e, int dev, Launch&& launch) {
+    cudaStream_t cs = capture_stream(dev);
+    if (!cs) return false;
+    CaptureCtx ctx;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return false;
+    t_capture = &ctx;
+    const int st = launch(cs);
+    t_capture = nullptr;
+    cudaGraph_t graph = nullptr;
+    const cudaError_t cerr = cudaStreamEndCapture(cs, &graph);
+    auto drop = [&]() {
+        if (graph) cudaGraphDestroy(graph);
+        cudaGetLastError();
+        return false;
+    };
+    if (st != DIFFUSER_OK || cerr != cudaSuccess || !graph) return drop();
+    cudaGraphExec_t exec = nullptr;
+    if (cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) return drop();
+    e.graph = graph;
+    e.exec = exec;
+    for (int k = 0; k < DIFFUSER_KERNEL_KINDS; ++k) e.launches[k] = ctx.launches[k];
+    return true;
+}
+}  // namespace
+
+void destroy_replay_cache(ReplayCache* c) {
+    if (!c) return;
+    for (auto& e : c->entries) destroy_entry(e);
+    delete c;
+}
+
+// The band-path forward through the replay cache of g.
+template <class Launch>
+int band_forward(const diffuser_graph* g, const ReplayKey& key, cudaStream_t stream, Launch&& launch) {
+    ReplayCache* c = g->replay;
+    // a caller capturing its own graph on this stream records the kernels themselves
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (!c || cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+        return launch(stream);
+    bool profiling;
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        profiling = g_prof_on;
+    }
+    if (profiling) return launch(stream);          // per-kernel events need direct launches
+    std::lock_guard<std::mutex> lk(c->mu);
+    ++c->clock;
+    for (auto& e : c->entries) {
+        if (!(e.key == key)) continue;
+        e.stamp = c->clock;
+        if (e.exec) return replay(e, stream);
+        // seen once before: capture this time (launches fall back to direct on failure)
+        if (capture(e, g->device, launch)) return replay(e, stream);
+        return launch(stream);
+    }
+    // first sighting: run directly and remember the key
+    if (c->entries.size() >= kReplayEntries) {
+        size_t old = 0;
+        for (size_t k = 1; k < c->entries.size(); ++k)
+            if (c->entries[k].stamp < c->entries[old].stamp) old = k;
+        destroy_entry(c->entries[old]);
+        c->entries.erase(c->entries.begin() + old);
+    }
+    ReplayEntry e;
+    e.key = key;
+    e.stamp = c->clock;
+    c->entries.push_back(std::move(e));
+    return launch(stream);
+}
+
 int forward_device(const void* Q, const void* K, const void* V, int32_t dtype, int64_t B,
                    int64_t H, int32_t d, const diffuser_graph* g, int32_t hops, float alpha,
                    void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -220,8 +369,12 @@ int forward_device(const void* Q, const void* K, const void* V, int32_t dtype, i
     if (use_band(g, dtype, &bp)) {
         BandLayout BL;
         if ((st = plan_band_layout(g, bp, B * H, &BL))) return st;
-        if ((st = launch_band_scores(g, bp, B * H, Q, K, ws, BL, stream))) return st;
-        return launch_band_hops(g, bp, B * H, V, hops, alpha, out, ws, BL, stream);
+        const ReplayKey key{Q, K, V, out, workspace, workspace_bytes, B, H, dtype, hops, alpha, g_path.load()};
+        return band_forward(g, key, stream, [&](cudaStream_t s) {
+            int r = launch_band_scores(g, bp, B * H, Q, K, ws, BL, s);
+            if (!r) r = launch_band_hops(g, bp, B * H, V, hops, alpha, out, ws, BL, s);
+            return r;
+        });
     }
     float* A = reinterpret_cast<float*>(ws + L.a_off);
     if ((st = launch_score_csr(a, Q, K, dtype, A, stream))) return st;
@@ -233,11 +386,13 @@ int new_graph(diffuser_graph** out, diffuser_graph** g) {
     *out = nullptr;
     *g = new (std::nothrow) diffuser_graph();
     if (!*g) return fail(DIFFUSER_ERR_ALLOC, "host allocation failed");
+    (*g)->replay = new (std::nothrow) ReplayCache();   // without it, forwards launch directly
     cudaError_t err = cudaGetDevice(&(*g)->device);
     if (err == cudaSuccess) err = cudaMalloc(&(*g)->d_status, sizeof(int));
     if (err == cudaSuccess) err = cudaMemset((*g)->d_status, 0, sizeof(int));
     if (err != cudaSuccess) {
         cudaFree((*g)->d_status);
+        delete (*g)->replay;
         delete *g;
         *g = nullptr;
         return cuda_fail(err, "graph set-up");
@@ -374,6 +529,7 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_x_ptr);
     cudaFree(g->d_x_col);
     cudaFree(g->d_status);
+    dfs::destroy_replay_cache(g->replay);
     delete g;
 }
 

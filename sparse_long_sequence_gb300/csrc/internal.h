@@ -44,6 +44,10 @@ struct BandLayout {
 
 }  // namespace dfs
 
+namespace dfs {
+struct ReplayCache;
+}
+
 struct diffuser_graph {
     int kind = dfs::kTokenGraph;
     int device = 0;
@@ -65,6 +69,7 @@ struct diffuser_graph {
     int64_t* d_x_ptr = nullptr;       // [n+1]
     int32_t* d_x_col = nullptr;       // [nx], ascending within a row
     int* d_status = nullptr;          // device status word written by kernels (0 = ok)
+    dfs::ReplayCache* replay = nullptr;   // captured band-path forwards (see abi.cu)
     // host copy of the CSR
     std::vector<int64_t> h_row_ptr;
     std::vector<int32_t> h_col;
@@ -89,6 +94,7 @@ class LaunchScope {
 
   private:
     int slot_ = -1;
+    int capture_slot_ = -1;
     cudaStream_t stream_;
 };
 

@@ -252,6 +252,42 @@ def test_band_path_repeatable_under_load(dl):
     assert dl.diffuser_graph_status(g) == 0
 
 
+def test_replayed_forward_matches_direct(dl):
+    # The same forward five times: the first runs its kernels directly, the
+    # second is captured into a CUDA graph, the next ones replay it, and the
+    # last (inside an open profile) launches directly again.  Every output must
+    # be bit-identical, every call must count the same launches, and the
+    # profile must see each kernel.
+    import torch
+    B, H, n = 2, 3, 1536
+    g = dl.diffuser_build_graph(n, 64, 4, rand_per_row=8)
+    Q, K, V = synthetic.qkv(B, H, n, 64, "bf16", seed=11)
+    Qd, Kd, Vd = (to_device(x, "bf16") for x in (Q, K, V))
+    ws = dl.alloc_workspace(dl.diffuser_workspace_size(g, B, H, 64, dl.DIFFUSER_DTYPE_BF16))
+    out = torch.empty_like(Vd)
+    ref, counts, prof = None, [], None
+    for call in range(5):
+        out.zero_()
+        torch.cuda.synchronize()
+        before, _ = dl.diffuser_launch_count()
+        if call == 4:
+            dl.diffuser_profile_begin()
+        dl.diffuser_forward(Qd, Kd, Vd, g, 3, 0.1, out=out, workspace=ws)
+        if call == 4:
+            prof = dl.diffuser_profile_end()
+        torch.cuda.synchronize()
+        after, _ = dl.diffuser_launch_count()
+        counts.append(after - before)
+        if ref is None:
+            ref = out.clone()
+        else:
+            assert torch.equal(out, ref), f"call {call} differs from the first"
+    assert counts[0] > 0 and len(set(counts)) == 1, counts
+    assert sum(v[1] for v in prof.values()) == counts[0]
+    assert all(v[0] > 0 for v in prof.values() if v[1])
+    assert dl.diffuser_graph_status(g) == 0
+
+
 def test_bad_workspace_launches_nothing(dl):
     import torch
     g = dl.diffuser_build_graph(256, 8, 1, rand_per_row=2)
