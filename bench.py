@@ -345,7 +345,7 @@ def run_ours(args, w) -> None:
             "config": {**w.describe(), "nnz": g.nnz, "units_per_gpu": w.units,
                        "parallelism": f"dp{world}" if world > 1 else "single GPU",
                        "l2": "flushed between steps (256 MB write outside the timed events)",
-                       "arith": "A and Z_k fp32, fp32 accumulate"},
+                       "arith": "A and Z_k as bf16 hi + lo pairs on the tensor cores (window, globals), fp32 gathers and accumulation"},
             "e2e": {"value": world * edge_hops / (t_e2e / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": 3 * io_bytes, "d2h_bytes_per_step": io_bytes},
             "roofline": roofline,

@@ -24,14 +24,15 @@
 //   extra  [nx]        e of the random edges outside window and G, CSR order
 //   inv_l  [n]         per-row normalizer of the rows not in G
 //   grow   [g][n]      the global rows' weights A_ij (raw scores until the
-//                      band score kernel normalizes them with
+//                      global-row norm kernel normalizes them with
 //   gstat  [g][2]      their (row max, 1 / row sum of exp(s - max)))
 //   gimg   [tiles][2][hi | lo][32 rows x 64 keys] bf16: the normalized
 //                      global-row weights of tile T's own keys 128 T .. +127
 //                      (two 64-key halves), as the tensor-core A operand
 //                      image (rows s < g; keys past n are 0)
-// The hop state Z_k is kept as [n][hi 64 | lo 64] bf16 rows (Z = hi + lo),
-// the B operand of the band MMA and the source of the row gathers alike.
+// The hop state Z_k is kept twice: as [n][hi 64 | lo 64] bf16 rows (Z = hi +
+// lo), the B operand of the band MMA, and as [n][64] fp32 rows, the source of
+// the random-edge row gathers.
 #pragma once
 
 #include <cuda.h>
@@ -61,9 +62,6 @@ __host__ __device__ constexpr int gc_offset(int t, int s, int g16) {
     return (t >> 3) * (16 * g16) + (t & 7) * 16 + (s >> 3) * 128 + (s & 7) * 2;
 }
 
-__device__ __forceinline__ float tf32_trunc(float x) {
-    return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-}
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
