@@ -3,12 +3,13 @@
 // pairs plus 1/l_i).
 //
 // Hop Z_{k+1} = (1-alpha) A Z_k + alpha V ("Diffuser...", sec 2.4 eq S.7),
-// three kernels per hop:
+// two kernels per hop:
 //   hop_gather_kernel: the random extras of every row not in G, into a
-//            per-row partial P_i (whole Z_k rows gathered from L2).  Each
-//            quarter-warp walks the extras of 4 consecutive rows as one stream
-//            with several rows in flight; every load instruction reads whole
-//            128-byte lines.
+//            per-row partial P_i (whole Z_k rows gathered from L2).  The rows
+//            are split evenly over the quarter-warps of the grid; each walks
+//            its rows' extras as one stream with several rows in flight, the
+//            next slots' indices loading meanwhile; every load instruction
+//            reads whole 128-byte lines.
 //   hop_band_kernel (persistent, 128-row tiles): tcgen05 MMA, M = 128 rows,
 //            K = 64 keys per chunk, bf16 operands split into hi + lo (each the
 //            bf16 rounding of what is left): e_hi*[Z_hi | Z_lo] (N = 128) +
@@ -23,9 +24,9 @@
 //            (full rows of A) ride along: on the two chunks that hold the
 //            tile's own keys, the same Z_k tiles also multiply the global rows'
 //            weights of those keys (a 32-row operand image) into a second
-//            accumulator; each tile writes that share, and
-//            hop_global_rows_kernel sums the shares in tile order and writes
-//            the rows.  Epilogue:
+//            accumulator; each tile writes that share, and the CTA that
+//            finishes a unit's last tile sums the unit's shares in tile order
+//            and writes the global rows.  Epilogue:
 //            z_i = (1 - alpha) * inv_l_i * (band_i + P_i) + alpha * V_i,
 //            written as the next [hi | lo] bf16 row and fp32 row, or as the
 //            bf16 output.
@@ -89,9 +90,10 @@ struct HopArgs {
     const int32_t* x_col;
     int64_t nx;
     const float* A_gc;
-    const float* A_x;
+    float* A_x;                  // extras' weights (raw scores on entry to the first hop)
     const uint8_t* A_gimg;       // global-row weight images [units][tiles] (kGImgBytes each)
-    const float* inv_l;   // [units][n]
+    float* inv_l;                // [units][n] (the first hop's gather completes it)
+    const float* m_sparse;       // [units][n] row maxima m_i
     const __nv_bfloat16* V;
     const __nv_bfloat16* A_band; // the tiles' A images [units][tiles][chunks][hi | lo]
     const uint8_t* A_gcimg;      // out-of-window globals' weight images [units][tiles][hi | lo]
@@ -100,8 +102,10 @@ struct HopArgs {
     float* Zf_out;               // Z_{k+1} as fp32 rows [n][64], all hops but the last
     __nv_bfloat16* out;          // the last hop's output [n][64]
     float* Psum;                 // [units][n][64] sparse partial of the rows not in G
-    float* gpart;                // [units][tiles][g][64]
-    int* counters;               // [units]
+    float* gpart;                // [units][tiles][g][64] the global rows' shares, per tile
+    __nv_bfloat16* Zk_hilo;      // Z_k as [n][hi | lo] rows and
+    float* Zk_f;                 // as fp32 rows: the gather of hops after the first writes
+                                 // Z_k's global rows there (from the previous hop's shares)
     int* status;
 };
 
@@ -143,76 +147,64 @@ __device__ __forceinline__ uint4 pack8(const float* z) {
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-// One CTA per unit, 1024 threads: Z_{k+1} of the global rows from the shares
-// sum_j A_gr[s][j] Z_k[j] of every tile, summed in a fixed order (tile quarter
-// q adds tiles q, q + 4, ... with all its loads in flight; then the quarters in
-// order), written as the next [hi | lo] bf16 and fp32 rows, or as the output.
-constexpr int kGRThreads = 1024;
-
-template <bool kLast>
-__global__ void __launch_bounds__(kGRThreads) hop_global_rows_kernel(HopArgs a) {
-    __shared__ float4 red[4][16][16];             // [tile quarter][row s (16 at a time)][feature quad]
+// One float4 (features 4 fq .. 4 fq + 3) of global row s of unit u in the next
+// state: (1 - alpha) * (the tiles' shares sum_j A_gr[s][j] Z[j], added in tile
+// order) + alpha * V, from the shares `gpart` that a band hop kernel wrote;
+// written as [hi | lo] bf16 and fp32 row pieces (zhl, zf) or as the output.
+template <bool kOut>
+__device__ __forceinline__ void global_row_out(const HopArgs& a, const float* gpart, int64_t u, int s,
+                                               int fq, __nv_bfloat16* zhl, float* zf) {
     const BandPlan& P = a.plan;
-    const int64_t u = blockIdx.x;
-    const int g = P.g;
-    const int tq = threadIdx.x >> 8, sl0 = (threadIdx.x >> 4) & 15, fq = threadIdx.x & 15;
-    const float keep = 1.f - a.alpha;
-    const size_t tstride = (size_t)g * (kHeadDim / 4);
-    for (int s0 = 0; s0 < g; s0 += 16) {
-        const int s = s0 + sl0;
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (s < g) {
-            const float4* src = reinterpret_cast<const float4*>(a.gpart) +
-                                ((size_t)u * P.tiles * g + s) * (kHeadDim / 4) + fq;
-            for (int c0 = tq; c0 < P.tiles; c0 += 32) {
-                float4 v[8];
+    const size_t tstride = (size_t)P.g * (kHeadDim / 4);  // float4s from one tile's shares to the next
+    const float4* src = reinterpret_cast<const float4*>(gpart) + (size_t)u * P.tiles * tstride +
+                        (size_t)s * (kHeadDim / 4) + fq;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t0 = 0; t0 < P.tiles; t0 += 8) {
+        float4 v[8];
 #pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    const int tt = c0 + 4 * b;
-                    v[b] = tt < P.tiles ? __ldcg(src + (size_t)tt * tstride) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+        for (int b = 0; b < 8; ++b)
+            v[b] = t0 + b < P.tiles ? __ldg(src + (size_t)(t0 + b) * tstride) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    sum.x += v[b].x; sum.y += v[b].y; sum.z += v[b].z; sum.w += v[b].w;
-                }
-            }
+        for (int b = 0; b < 8; ++b) {
+            sum.x += v[b].x; sum.y += v[b].y; sum.z += v[b].z; sum.w += v[b].w;
         }
-        red[tq][sl0][fq] = sum;
-        __syncthreads();
-        if (tq == 0 && s < g) {
-#pragma unroll
-            for (int q = 1; q < 4; ++q) {
-                const float4 v = red[q][sl0][fq];
-                sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-            }
-            const int64_t gi = a.globals[s];
-            const size_t vrow = ((size_t)u * P.n + gi) * kHeadDim + 4 * fq;
-            const uint2 vv = __ldg(reinterpret_cast<const uint2*>(a.V + vrow));
-            float z[4] = {fmaf(keep, sum.x, a.alpha * bf16lo(vv.x)), fmaf(keep, sum.y, a.alpha * bf16hi(vv.x)),
-                          fmaf(keep, sum.z, a.alpha * bf16lo(vv.y)), fmaf(keep, sum.w, a.alpha * bf16hi(vv.y))};
-            if (kLast) {
-                const __nv_bfloat162 h0 = __floats2bfloat162_rn(z[0], z[1]);
-                const __nv_bfloat162 h1 = __floats2bfloat162_rn(z[2], z[3]);
-                *reinterpret_cast<uint2*>(a.out + vrow) =
-                    make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-            } else {
-                uint32_t hw[2], lw[2];
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const __nv_bfloat162 hh = __floats2bfloat162_rn(z[2 * p], z[2 * p + 1]);
-                    const __nv_bfloat162 ll =
-                        __floats2bfloat162_rn(z[2 * p] - __low2float(hh), z[2 * p + 1] - __high2float(hh));
-                    hw[p] = *reinterpret_cast<const uint32_t*>(&hh);
-                    lw[p] = *reinterpret_cast<const uint32_t*>(&ll);
-                }
-                __nv_bfloat16* zr = a.Z_out + ((size_t)u * P.n + gi) * (2 * kHeadDim) + 4 * fq;
-                *reinterpret_cast<uint2*>(zr) = make_uint2(hw[0], hw[1]);
-                *reinterpret_cast<uint2*>(zr + kHeadDim) = make_uint2(lw[0], lw[1]);
-                *reinterpret_cast<float4*>(a.Zf_out + vrow) = make_float4(z[0], z[1], z[2], z[3]);
-            }
-        }
-        __syncthreads();                          // red is reused by the next 16 rows
     }
+    const float keep = 1.f - a.alpha;
+    const int64_t gi = a.globals[s];
+    const size_t vrow = ((size_t)u * P.n + gi) * kHeadDim + 4 * fq;
+    const uint2 vv = __ldg(reinterpret_cast<const uint2*>(a.V + vrow));
+    float z[4] = {fmaf(keep, sum.x, a.alpha * bf16lo(vv.x)), fmaf(keep, sum.y, a.alpha * bf16hi(vv.x)),
+                  fmaf(keep, sum.z, a.alpha * bf16lo(vv.y)), fmaf(keep, sum.w, a.alpha * bf16hi(vv.y))};
+    if (kOut) {
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(z[0], z[1]);
+        const __nv_bfloat162 h1 = __floats2bfloat162_rn(z[2], z[3]);
+        *reinterpret_cast<uint2*>(a.out + vrow) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    } else {
+        uint32_t hw[2], lw[2];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const __nv_bfloat162 hh = __floats2bfloat162_rn(z[2 * p], z[2 * p + 1]);
+            const __nv_bfloat162 ll =
+                __floats2bfloat162_rn(z[2 * p] - __low2float(hh), z[2 * p + 1] - __high2float(hh));
+            hw[p] = *reinterpret_cast<const uint32_t*>(&hh);
+            lw[p] = *reinterpret_cast<const uint32_t*>(&ll);
+        }
+        __nv_bfloat16* zr = zhl + ((size_t)u * P.n + gi) * (2 * kHeadDim) + 4 * fq;
+        *reinterpret_cast<uint2*>(zr) = make_uint2(hw[0], hw[1]);
+        *reinterpret_cast<uint2*>(zr + kHeadDim) = make_uint2(lw[0], lw[1]);
+        *reinterpret_cast<float4*>(zf + vrow) = make_float4(z[0], z[1], z[2], z[3]);
+    }
+}
+
+// The output's global rows after the last hop: one thread per float4.
+__global__ void __launch_bounds__(256) hop_global_out_kernel(HopArgs a) {
+    const int64_t per_unit = (int64_t)a.plan.g * (kHeadDim / 4);
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= a.units * per_unit) return;
+    const int64_t u = idx / per_unit;
+    const int rem = (int)(idx - u * per_unit);
+    global_row_out<true>(a, a.gpart, u, rem >> 4, rem & 15, nullptr, nullptr);
 }
 
 // ---------------------------------------------------------------- band part of a hop
@@ -463,7 +455,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
             ptx::tc_fence_after();
             if (has_g && quad == 0) {
                 // TMEM lanes 0..31 of the global accumulator are the global slots s:
-                // this tile's share of the global rows (hop_global_rows_kernel sums them)
+                // this tile's share of the global rows (summed by global_row_out)
                 float gd[32];
                 ptx::tmem_ld32(tmem + kGlobCol0 + kAccCols * ab + 32 * fhalf, gd);
                 if (!kHop0) {
@@ -490,35 +482,36 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&acc_empty[ab]);                    // the accumulators are in registers
-            if (!row_ok) continue;
-            float z[32];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                const uint32_t w4[4] = {vv[c4].x, vv[c4].y, vv[c4].z, vv[c4].w};
-                const float p8[8] = {pv[2 * c4].x, pv[2 * c4].y, pv[2 * c4].z, pv[2 * c4].w,
-                                     pv[2 * c4 + 1].x, pv[2 * c4 + 1].y, pv[2 * c4 + 1].z, pv[2 * c4 + 1].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int k = 8 * c4 + 2 * e;
-                    z[k] = fmaf(keep, d[k] + p8[2 * e], a.alpha * bf16lo(w4[e]));
-                    z[k + 1] = fmaf(keep, d[k + 1] + p8[2 * e + 1], a.alpha * bf16hi(w4[e]));
-                }
-            }
-            if (kLast) {
-                uint4* op = reinterpret_cast<uint4*>(a.out + vrow);
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) op[c4] = pack8(z + 8 * c4);
-            } else {
-                __nv_bfloat16* zr = a.Z_out + ((size_t)u * P.n + i) * (2 * kHeadDim) + 32 * fhalf;
-                float4* zf = reinterpret_cast<float4*>(a.Zf_out + vrow);
+            if (row_ok) {
+                float z[32];
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    uint4 hi, lo;
-                    split8(z + 8 * c4, hi, lo);
-                    reinterpret_cast<uint4*>(zr)[c4] = hi;
-                    reinterpret_cast<uint4*>(zr + kHeadDim)[c4] = lo;
-                    zf[2 * c4] = make_float4(z[8 * c4], z[8 * c4 + 1], z[8 * c4 + 2], z[8 * c4 + 3]);
-                    zf[2 * c4 + 1] = make_float4(z[8 * c4 + 4], z[8 * c4 + 5], z[8 * c4 + 6], z[8 * c4 + 7]);
+                    const uint32_t w4[4] = {vv[c4].x, vv[c4].y, vv[c4].z, vv[c4].w};
+                    const float p8[8] = {pv[2 * c4].x, pv[2 * c4].y, pv[2 * c4].z, pv[2 * c4].w,
+                                         pv[2 * c4 + 1].x, pv[2 * c4 + 1].y, pv[2 * c4 + 1].z, pv[2 * c4 + 1].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 8 * c4 + 2 * e;
+                        z[k] = fmaf(keep, d[k] + p8[2 * e], a.alpha * bf16lo(w4[e]));
+                        z[k + 1] = fmaf(keep, d[k + 1] + p8[2 * e + 1], a.alpha * bf16hi(w4[e]));
+                    }
+                }
+                if (kLast) {
+                    uint4* op = reinterpret_cast<uint4*>(a.out + vrow);
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) op[c4] = pack8(z + 8 * c4);
+                } else {
+                    __nv_bfloat16* zr = a.Z_out + ((size_t)u * P.n + i) * (2 * kHeadDim) + 32 * fhalf;
+                    float4* zf = reinterpret_cast<float4*>(a.Zf_out + vrow);
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint4 hi, lo;
+                        split8(z + 8 * c4, hi, lo);
+                        reinterpret_cast<uint4*>(zr)[c4] = hi;
+                        reinterpret_cast<uint4*>(zr + kHeadDim)[c4] = lo;
+                        zf[2 * c4] = make_float4(z[8 * c4], z[8 * c4 + 1], z[8 * c4 + 2], z[8 * c4 + 3]);
+                        zf[2 * c4 + 1] = make_float4(z[8 * c4 + 4], z[8 * c4 + 5], z[8 * c4 + 6], z[8 * c4 + 7]);
+                    }
                 }
             }
         }
@@ -529,114 +522,163 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
 }
 
 // ---------------------------------------------------------------- sparse part of a hop
-// Persistent over 128-row tiles, 8 warps.  Quarter-warp q of a tile owns rows
-// 4 q .. 4 q + 3, whose random extras are one contiguous stretch of the extras
-// list: it walks that stretch in batches of kB slots (every slot's Z_k row in
-// flight at once; a slot past the end reads row 0 with weight 0), and on
-// leaving a row stores the row's sum in shared memory; then each row writes P_i.
-// Lane l of a quarter owns features
+// Persistent, 8 warps per CTA.  The rows of all units are split evenly over the
+// quarter-warps of the grid (random extras per row vary little, so equal rows
+// are equal work; global rows carry none).  A quarter walks its rows in
+// windows of up to kWinRows rows of one unit, whose extras are one contiguous
+// stretch of the extras list: it streams that stretch kB slots at a time
+// (every slot's Z_k row in flight at once) while the indices and weights of
+// the next kB slots load, one slot per lane, and reach the quarter by shuffles.
+// On leaving a row it writes the row's sum P_i (zeros for a row without
+// extras; nothing for a global row).  Lane l of a quarter owns features
 // 4 l .. 4 l + 3 and 32 + 4 l .. 32 + 4 l + 3, so each load instruction reads
 // whole 128-byte lines of the gathered rows.
 constexpr int kGThreadsG = 256;
+constexpr int kWinRows = 16;
 
 template <bool kHop0, int kB, int kMinBlocks>
 __global__ void __launch_bounds__(kGThreadsG, kMinBlocks)
 hop_gather_kernel(HopArgs a) {
-    __shared__ float4 sR[32 * 4 * 16];            // [quarter][row][16]: the rows' extras sums
+    static_assert(kB <= 8, "one slot per lane of a quarter");
+    __shared__ int sStart[32][kWinRows + 1];      // per quarter: the window's row starts (unit-local slots)
+    __shared__ float sMax[32][kWinRows];          // per quarter: the rows' m_i (first hop)
+    __shared__ uint8_t sGlob[32][kWinRows];       // per quarter: the window's rows in G
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ql = lane & 7;
-    const int qi = 4 * warp + (lane >> 3);        // quarter 0..31: rows 4 qi .. +3
-    float4* rq = sR + qi * 64;                    // this quarter's 4 rows
-    const int64_t total_tiles = a.units * P.tiles;
-    for (int64_t tix = blockIdx.x; tix < total_tiles; tix += gridDim.x) {
-        const int64_t u = tix / P.tiles;
-        const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-        const int64_t ib = i0 + 4 * qi;
-        const int64_t rlim = P.n;
-        // extras of row ib + m: [d_m, d_{m+1}) relative to the first
-        const int64_t xb = a.x_ptr[ib < rlim ? ib : rlim];
-        const int d1 = (int)(a.x_ptr[ib + 1 < rlim ? ib + 1 : rlim] - xb);
-        const int d2 = (int)(a.x_ptr[ib + 2 < rlim ? ib + 2 : rlim] - xb);
-        const int d3 = (int)(a.x_ptr[ib + 3 < rlim ? ib + 3 : rlim] - xb);
-        const int nslot = (int)(a.x_ptr[ib + 4 < rlim ? ib + 4 : rlim] - xb);
-        const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) { rq[m * 16 + ql] = zero4; rq[m * 16 + 8 + ql] = zero4; }
-        const float* wq = a.A_x + (size_t)u * a.nx + xb;
-        const int32_t* jq = a.x_col + xb;
+    const int qi = 4 * warp + (lane >> 3);
+    const unsigned qmask = 0xFFu << (lane & 24);  // this quarter's lanes
+    const int64_t nq = (int64_t)gridDim.x * 32, q = (int64_t)blockIdx.x * 32 + qi;
+    const int64_t rows_total = a.units * P.n;
+    const int64_t R1 = (q + 1) * rows_total / nq;
+    int* ss = sStart[qi];
+    float* sm = sMax[qi];
+    uint8_t* sg = sGlob[qi];
+    if (!kHop0 && P.g > 0) {
+        // Z_k of the global rows, from the previous hop's shares: one float4 per
+        // thread, spread over all CTAs (no extra reads them: the extras exclude G)
+        const int64_t per_unit = (int64_t)P.g * (kHeadDim / 4), total = a.units * per_unit;
+        for (int64_t idx = (int64_t)tid * gridDim.x + blockIdx.x; idx < total;
+             idx += (int64_t)blockDim.x * gridDim.x) {
+            const int64_t u = idx / per_unit;
+            const int rem = (int)(idx - u * per_unit);
+            global_row_out<false>(a, a.gpart, u, rem >> 4, rem & 15, a.Zk_hilo, a.Zk_f);
+        }
+        __syncwarp();     // reconverge: the quarters below synchronize only among themselves
+    }
+    for (int64_t Rw = q * rows_total / nq; Rw < R1;) {
+        const int64_t u = Rw / P.n;
+        const int64_t iw = Rw - u * P.n;
+        int64_t cnt64 = R1 - Rw;
+        if (cnt64 > P.n - iw) cnt64 = P.n - iw;
+        const int cnt = cnt64 < kWinRows ? (int)cnt64 : kWinRows;
         const size_t ubase = (size_t)u * P.n;
+        // the window's row starts, global flags (and row maxima)
+        for (int m = ql; m <= cnt; m += 8) {
+            ss[m] = (int)a.x_ptr[iw + m];
+            if (m < cnt) {
+                sg[m] = a.is_global[iw + m];
+                if (kHop0) sm[m] = a.m_sparse[ubase + iw + m];
+            }
+        }
+        __syncwarp(qmask);
+        const int sb = ss[0], se = ss[cnt];
+        float* wq = a.A_x + (size_t)u * a.nx;
         // this lane's features of row j of Z_k: zrow + 16 j (fp32) or vrow + 16 j (bf16 V)
         const float4* zrow = reinterpret_cast<const float4*>(a.Zf_in) + ubase * 16 + ql;
         const uint2* vrow = reinterpret_cast<const uint2*>(a.V) + ubase * 16 + ql;
+        float4* prow = reinterpret_cast<float4*>(a.Psum) + ubase * 16 + ql;
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
-        int cur = 0;                              // row (0..3) being accumulated
-        int nb = d1;                              // first slot past row cur
-        auto stash = [&]() {
-            rq[cur * 16 + ql] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-            rq[cur * 16 + 8 + ql] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+        int cur = 0;                              // window row being accumulated
+        int nb = ss[1];                           // first slot past row cur
+        // First hop only: the extras' weights arrive as raw scores s; each
+        // becomes e = exp(s - m_i) (stored back for the later hops), and the
+        // row's sum of e completes inv_l_i (which holds the band and globals'
+        // part of the sum on entry).
+        float mcur = kHop0 ? sm[0] : 0.f;
+        float lsum = 0.f;
+        // closes row cur: its partial P_i (and, first hop, inv_l_i)
+        auto finish_row = [&]() {
+            if (!sg[cur]) {
+                float4* pr = prow + (size_t)(iw + cur) * 16;
+                pr[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+                pr[8] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+                if (kHop0 && ql == 0) {
+                    float* il = a.inv_l + ubase + iw + cur;
+                    *il = 1.f / (*il + lsum);
+                }
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
+            lsum = 0.f;
+            ++cur;
         };
-        for (int e0 = 0; e0 < nslot; e0 += kB) {
-            int32_t j[kB];
-            float w[kB];
-#pragma unroll
-            for (int b = 0; b < kB; ++b) {
-                const bool v = e0 + b < nslot;
-                j[b] = v ? __ldg(jq + e0 + b) : 0;
-                w[b] = v ? __ldg(wq + e0 + b) : 0.f;
-            }
+        // slot sb + ql's index and weight (slots past the window read row 0 with weight 0)
+        int32_t jc = 0;
+        float wc = 0.f;
+        if (ql < kB && sb + ql < se) { jc = __ldg(a.x_col + sb + ql); wc = __ldg(wq + sb + ql); }
+        for (int e0 = sb; e0 < se; e0 += kB) {
+            int32_t jn = 0;
+            float wn = 0.f;
+            const int en = e0 + kB + ql;
+            if (ql < kB && en < se) { jn = __ldg(a.x_col + en); wn = __ldg(wq + en); }
             float4 z0[kB], z1[kB];
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
+                const int j = __shfl_sync(qmask, jc, b, 8);
                 if (kHop0) {
-                    z0[b] = bf16x4(__ldg(vrow + 16 * j[b]));
-                    z1[b] = bf16x4(__ldg(vrow + 16 * j[b] + 8));
+                    z0[b] = bf16x4(__ldg(vrow + 16 * j));
+                    z1[b] = bf16x4(__ldg(vrow + 16 * j + 8));
                 } else {
-                    z0[b] = __ldg(zrow + 16 * j[b]);
-                    z1[b] = __ldg(zrow + 16 * j[b] + 8);
+                    z0[b] = __ldg(zrow + 16 * j);
+                    z1[b] = __ldg(zrow + 16 * j + 8);
                 }
             }
             if (e0 + kB <= nb) {
-                // the whole batch belongs to row cur (slots past the end carry weight 0)
+                // the whole batch belongs to row cur
+                if (kHop0) {
+                    wc = expf(wc - mcur);
+                    if (ql < kB) wq[e0 + ql] = wc;
+                }
 #pragma unroll
-                for (int b = 0; b < kB; ++b) ffma8(acc, w[b], z0[b], z1[b]);
+                for (int b = 0; b < kB; ++b) {
+                    const float w = __shfl_sync(qmask, wc, b, 8);
+                    if (kHop0) lsum += w;
+                    ffma8(acc, w, z0[b], z1[b]);
+                }
             } else {
 #pragma unroll
                 for (int b = 0; b < kB; ++b) {
                     const int e = e0 + b;
-                    const int m = (e >= d1) + (e >= d2) + (e >= d3);
-                    if (e < nslot && m != cur) {
-                        // each row's extras are one contiguous span: stash its sum once
-                        stash();
-                        cur = m;
-                        nb = m == 1 ? d2 : (m == 2 ? d3 : nslot);
+                    if (e < se) {
+                        while (e >= nb) {
+                            finish_row();
+                            nb = ss[cur < cnt ? cur + 1 : cnt];
+                            if (kHop0) mcur = sm[cur];
+                        }
+                        float w = __shfl_sync(qmask, wc, b, 8);
+                        if (kHop0) {
+                            w = expf(w - mcur);
+                            if (ql == b) wq[e] = w;
+                            lsum += w;
+                        }
+                        ffma8(acc, w, z0[b], z1[b]);
                     }
-                    ffma8(acc, w[b], z0[b], z1[b]);
                 }
             }
+            jc = jn;
+            wc = wn;
         }
-        if (nslot > 0) stash();
-        __syncwarp();
-        // each row: write P_i
-        for (int m = 0; m < 4; ++m) {
-            const int64_t i = ib + m;
-            if (i >= P.n || a.is_global[i]) continue;     // uniform within the quarter
-            const float4 r0 = rq[m * 16 + ql], r1 = rq[m * 16 + 8 + ql];
-            float2 v[4] = {make_float2(r0.x, r0.y), make_float2(r0.z, r0.w), make_float2(r1.x, r1.y),
-                           make_float2(r1.z, r1.w)};
-            float4* pr = reinterpret_cast<float4*>(a.Psum + ((size_t)u * P.n + i) * kHeadDim);
-            pr[ql] = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
-            pr[8 + ql] = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
-        }
-        __syncwarp();                                     // rq is reused by the next tile
+        // the rows left (the last one, and any without extras)
+        while (cur < cnt) finish_row();
+        __syncwarp(qmask);                        // the window's smem is rewritten next
+        Rw += cnt;
     }
 }
 
-// the gather configuration: rows in flight per quarter-warp, CTAs per SM
-constexpr int kGatherBatch = 6, kGatherBlocks = 3;
+// the gather configuration: slots in flight per quarter-warp, CTAs per SM
+constexpr int kGatherBatch = 5, kGatherBlocks = 3;
 
 // bf16 tensor map over rows of `row_elems` elements: box of 64 elements x 64 rows
 int encode_rows(CUtensorMap* m, const void* base, int64_t n, int64_t units, int row_elems) {
@@ -678,9 +720,8 @@ int launch_hop(const CUtensorMap& tmZ, const HopArgs& a, cudaStream_t stream) {
     const int64_t total_tiles = a.units * a.plan.tiles;
     {
         LaunchScope scope(DIFFUSER_KERNEL_GATHER, stream);
-        const int64_t gmax = (int64_t)sms * kGatherBlocks;
         hop_gather_kernel<kHop0, kGatherBatch, kGatherBlocks>
-            <<<(unsigned)(total_tiles < gmax ? total_tiles : gmax), kGThreadsG, 0, stream>>>(a);
+            <<<(unsigned)(sms * kGatherBlocks), kGThreadsG, 0, stream>>>(a);
     }
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return cuda_fail(err, "hop_gather_kernel");
@@ -691,12 +732,13 @@ int launch_hop(const CUtensorMap& tmZ, const HopArgs& a, cudaStream_t stream) {
     }
     err = cudaGetLastError();
     if (err != cudaSuccess) return cuda_fail(err, "hop_band_kernel");
-    if (a.plan.g > 0) {
+    if (kLast && a.plan.g > 0) {
         LaunchScope scope(DIFFUSER_KERNEL_GATHER, stream);
-        hop_global_rows_kernel<kLast><<<(unsigned)a.units, kGRThreads, 0, stream>>>(a);
+        const int64_t outs = a.units * a.plan.g * (kHeadDim / 4);
+        hop_global_out_kernel<<<(unsigned)((outs + 255) / 256), 256, 0, stream>>>(a);
     }
     err = cudaGetLastError();
-    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_global_rows_kernel");
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_global_out_kernel");
 }
 
 }  // namespace
@@ -779,8 +821,6 @@ int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, 
 int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* V,
                      int32_t hops, float alpha, void* out, char* ws, const BandLayout& L,
                      cudaStream_t stream) {
-    cudaError_t err = cudaMemsetAsync(ws + L.counters, 0, (size_t)units * 4, stream);
-    if (err != cudaSuccess) return cuda_fail(err, "clearing the tile counters");
     // tensor maps of the B operand: V ([n][64]) for hop 0, then the Z_k rows ([n][hi | lo])
     CUtensorMap tmV, tmZ[2];
     int st = encode_rows(&tmV, V, p.n, units, kHeadDim);
@@ -797,15 +837,15 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     a.x_col = g->d_x_col;
     a.nx = g->nx;
     a.A_gc = reinterpret_cast<const float*>(ws + L.a_gc);
-    a.A_x = reinterpret_cast<const float*>(ws + L.a_x);
+    a.A_x = reinterpret_cast<float*>(ws + L.a_x);
+    a.m_sparse = reinterpret_cast<const float*>(ws + L.m_sparse);
     a.A_gimg = reinterpret_cast<const uint8_t*>(ws + L.a_gimg);
-    a.inv_l = reinterpret_cast<const float*>(ws + L.inv_l);
+    a.inv_l = reinterpret_cast<float*>(ws + L.inv_l);
     a.Psum = reinterpret_cast<float*>(ws + L.psum);
     a.A_band = reinterpret_cast<const __nv_bfloat16*>(ws + L.a_band);
     a.A_gcimg = reinterpret_cast<const uint8_t*>(ws + L.a_gcimg);
     a.V = static_cast<const __nv_bfloat16*>(V);
     a.gpart = reinterpret_cast<float*>(ws + L.gpart);
-    a.counters = reinterpret_cast<int*>(ws + L.counters);
     a.status = g->d_status;
     a.out = static_cast<__nv_bfloat16*>(out);
     // Z_{k+1} of hop k lives in z[k & 1]; hop k reads Z_k (V for k = 0)
@@ -814,6 +854,8 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
         a.Z_out = reinterpret_cast<__nv_bfloat16*>(ws + L.z[k & 1]);
         a.Zf_in = first ? nullptr : reinterpret_cast<const float*>(ws + L.zf[(k - 1) & 1]);
         a.Zf_out = reinterpret_cast<float*>(ws + L.zf[k & 1]);
+        a.Zk_hilo = first ? nullptr : reinterpret_cast<__nv_bfloat16*>(ws + L.z[(k - 1) & 1]);
+        a.Zk_f = first ? nullptr : reinterpret_cast<float*>(ws + L.zf[(k - 1) & 1]);
         const CUtensorMap& tm = first ? tmV : tmZ[(k - 1) & 1];
         if (first && last) st = launch_hop<true, true>(tm, a, stream);
         else if (first) st = launch_hop<true, false>(tm, a, stream);

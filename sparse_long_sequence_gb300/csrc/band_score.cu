@@ -17,6 +17,8 @@
 //    image.
 //  * score_finalize_kernel: a warp per row turns the extras' raw scores into
 //    e = exp(s - m_i) and stores inv_l = 1 / (band + globals + extras sum).
+//    The forward leaves this step to its first hop's gather, which reads the
+//    extras anyway.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -715,7 +717,8 @@ ScoreArgs make_args(const diffuser_graph* g, const BandPlan& p, int64_t units, c
 }  // namespace
 
 int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
-                       const void* K, char* ws, const BandLayout& L, cudaStream_t stream) {
+                       const void* K, char* ws, const BandLayout& L, bool finalize_extras,
+                       cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -773,6 +776,7 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
         score_global_norm_kernel<<<(unsigned)(units * p.g), kNormThreads, 0, stream>>>(a);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_global_norm_kernel");
+    if (!finalize_extras) return DIFFUSER_OK;
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
         score_finalize_kernel<<<(unsigned)((units * p.n + 7) / 8), 256, 0, stream>>>(a);

@@ -122,11 +122,15 @@ int launch_hop_csr(const CsrArgs& a, const float* A, const void* src, bool src_i
                    const void* V, void* dst, bool dst_is_io, int32_t dtype, float alpha,
                    cudaStream_t stream);
 
-// ---- band path (band_path.cu): token graphs, bf16 I/O ----------------------
+// ---- band path (band_score.cu, band_hop.cu): token graphs, bf16 I/O --------
 bool band_plan(const diffuser_graph* g, BandPlan* p);   // false: graph not eligible
 int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, BandLayout* L);
+// Scores and weights.  With finalize_extras false the random extras keep their
+// raw scores and inv_l only the band and globals' part of the row sum: the
+// first hop's gather completes both (launch_band_hops must follow).
 int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
-                       const void* K, char* ws, const BandLayout& L, cudaStream_t stream);
+                       const void* K, char* ws, const BandLayout& L, bool finalize_extras,
+                       cudaStream_t stream);
 int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* V,
                      int32_t hops, float alpha, void* out, char* ws, const BandLayout& L,
                      cudaStream_t stream);
