@@ -76,7 +76,6 @@ struct Weights {
     float* inv_l;      // [units][n]
     float* m_sparse;   // [units][n] max raw score over a row's gcol + extras
     float* gstat;      // [units][g][2]
-    float* sstat;      // [units][tiles][g][2] per-tile (max, sum) of the global rows
 };
 
 struct GraphRefs {

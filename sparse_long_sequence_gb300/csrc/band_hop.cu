@@ -774,7 +774,6 @@ band::Weights band_weights(char* ws, const BandLayout& L) {
     w.inv_l = reinterpret_cast<float*>(ws + L.inv_l);
     w.m_sparse = reinterpret_cast<float*>(ws + L.m_sparse);
     w.gstat = reinterpret_cast<float*>(ws + L.gstat);
-    w.sstat = reinterpret_cast<float*>(ws + L.sstat);
     return w;
 }
 
@@ -812,8 +811,6 @@ int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     L->inv_l = take(U * (size_t)p.n * 4);
     L->m_sparse = take(U * (size_t)p.n * 4);
     L->gstat = take(U * gg * 2 * 4);
-    L->sstat = take(U * (size_t)p.tiles * gg * 2 * 4);
-    L->counters = take(U * 4);
     L->total = off;
     return DIFFUSER_OK;
 }

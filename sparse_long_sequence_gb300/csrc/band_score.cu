@@ -45,13 +45,24 @@ struct ScoreArgs {
     int64_t units;
     band::GraphRefs gr;
     band::Weights w;
-    int* counters;      // [units] tile tickets
     const __nv_bfloat16* Q;
     const __nv_bfloat16* K;
 };
 
 // ---------------------------------------------------------------- sparse scores
+int sm_count_scores() {
+    static int num_sms = 0;
+    if (num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms < 1)
+            num_sms = 1;
+    }
+    return num_sms;
+}
+
 constexpr int kSparseThreads = 256;
+constexpr int kSparseBlocks = 2;         // CTAs per SM of the persistent sparse kernel
 
 // v[b] (b < 8) are this lane's partial sums of slot b; afterwards v[0] on
 // lane l of the 8-lane group is the full sum of slot l (butterfly transpose).
@@ -81,69 +92,116 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
     x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
 }
 
-__global__ void __launch_bounds__(kSparseThreads, 2)
+// Persistent, 8 warps per CTA.  The rows of all units are split evenly over the
+// quarter-warps of the grid; a quarter walks its rows in windows of up to
+// kSWinRows rows of one unit, as a sequence of batches of up to 8 slots of one
+// row.  Batch b + 1's k rows (and q, if its row differs) load while batch b's
+// dot products run, and batch b + 2's columns load meanwhile.  Lane l holds
+// features 8 l .. 8 l + 7 of q and reads the same 16 bytes of each k row, so a
+// load instruction reads whole 128-byte lines; the 8 partial dot products of a
+// batch are reduced across the quarter at once.
+constexpr int kSWinRows = 16;
+
+__global__ void __launch_bounds__(kSparseThreads, kSparseBlocks)
 score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
                     const __nv_bfloat16* __restrict__ K) {
+    __shared__ int sStart[32][kSWinRows + 1];     // per quarter: the window's row starts (unit-local slots)
     const BandPlan& P = a.plan;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t u = blockIdx.x / P.tiles;
-    const int tile = (int)(blockIdx.x - u * P.tiles);
-    const int64_t i0 = (int64_t)tile * kTileRows;
-    const __nv_bfloat16* Qu = Q + (size_t)u * P.n * kHeadDim;
-    const __nv_bfloat16* Ku = K + (size_t)u * P.n * kHeadDim;
-    // quarter-warp qi owns rows 4 qi .. +3; lane ql holds features 8 ql .. +7 of
-    // q_i and reads the same 16 bytes of each k row (whole 128-byte lines)
     const int ql = lane & 7, qi = 4 * warp + (lane >> 3);
     const unsigned qmask = 0xffu << (lane & 24);
-    for (int mrow = 0; mrow < 4; ++mrow) {
-        const int64_t i = i0 + 4 * qi + mrow;
-        if (i >= P.n || a.gr.is_global[i]) continue;      // uniform within the quarter
-        float q[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(Qu + (size_t)i * kHeadDim) + ql), q);
-        float m = -INFINITY;
-        const int64_t e0 = a.gr.x_ptr[i], e1 = a.gr.x_ptr[i + 1];
+    const int64_t nq = (int64_t)gridDim.x * 32, qg = (int64_t)blockIdx.x * 32 + qi;
+    const int64_t rows_total = a.units * P.n;
+    const int64_t R1 = (qg + 1) * rows_total / nq;
+    int* ss = sStart[qi];
+    for (int64_t Rw = qg * rows_total / nq; Rw < R1;) {
+        const int64_t u = Rw / P.n;
+        const int64_t iw = Rw - u * P.n;
+        int64_t cnt64 = R1 - Rw;
+        if (cnt64 > P.n - iw) cnt64 = P.n - iw;
+        const int cnt = cnt64 < kSWinRows ? (int)cnt64 : kSWinRows;
+        for (int m = ql; m <= cnt; m += 8) ss[m] = (int)a.gr.x_ptr[iw + m];
+        __syncwarp(qmask);
+        const uint4* Qu = reinterpret_cast<const uint4*>(Q + ((size_t)u * P.n + iw) * kHeadDim) + ql;
+        const uint4* Ku = reinterpret_cast<const uint4*>(K + (size_t)u * P.n * kHeadDim) + ql;
         float* wx = a.w.A_x + (size_t)u * a.gr.nx;
-        // 32 slots at a time: their columns loaded together (4 per lane), then four
-        // batches of 8 k rows with the next batch's rows in flight during this one's math
-        for (int64_t base = e0; base < e1; base += 32) {
-            const int cnt = e1 - base < 32 ? (int)(e1 - base) : 32;
-            int32_t jv[4];
+        float* mx = a.w.m_sparse + (size_t)u * P.n + iw;
+        // rows without extras (the global rows among them) have no maximum
+        for (int m = ql; m < cnt; m += 8)
+            if (ss[m + 1] == ss[m]) mx[m] = -INFINITY;
+        // batch cursor: row r, first slot e; r == cnt past the end
+        auto next = [&](int r, int e, int& r2, int& e2) {
+            e2 = e + 8;
+            r2 = r;
+            if (e2 >= ss[r + 1]) {
+                r2 = r + 1;
+                while (r2 < cnt && ss[r2 + 1] == ss[r2]) ++r2;
+                e2 = r2 < cnt ? ss[r2] : 0;
+            }
+        };
+        int rA = 0;                               // the first row with extras
+        while (rA < cnt && ss[rA + 1] == ss[rA]) ++rA;
+        int eA = rA < cnt ? ss[rA] : 0;
+        if (rA < cnt) {
+            int rB, eB;
+            next(rA, eA, rB, eB);
+            auto cols = [&](int r, int e) -> int32_t {       // this lane's column of batch (r, e)
+                return (r < cnt && e + ql < ss[r + 1]) ? __ldg(a.gr.x_col + e + ql) : 0;
+            };
+            const int32_t jA = cols(rA, eA);
+            int32_t jB = cols(rB, eB);
+            uint4 qA = __ldg(Qu + (size_t)rA * 8);
+            uint4 qB = rB < cnt ? __ldg(Qu + (size_t)rB * 8) : qA;
+            uint4 kA[8], kB[8];
+            const int nA0 = ss[rA + 1] - eA;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) jv[k] = 8 * k + ql < cnt ? __ldg(a.gr.x_col + base + 8 * k + ql) : (int32_t)i;
-            uint4 kr[2][8];
+            for (int b = 0; b < 8; ++b) {
+                const int j = __shfl_sync(qmask, jA, b, 8);
+                kA[b] = b < nA0 ? __ldg(Ku + (size_t)j * 8) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            float mrow = -INFINITY;               // this lane's running max of row rA
+            while (rA < cnt) {
+                int rC, eC;
+                if (rB < cnt) next(rB, eB, rC, eC); else { rC = cnt; eC = 0; }
+                const int32_t jC = cols(rC, eC);
+                const uint4 qC = (rC < cnt && rC != rB) ? __ldg(Qu + (size_t)rC * 8) : qB;
+                const int nB = rB < cnt ? min(8, ss[rB + 1] - eB) : 0;
 #pragma unroll
-            for (int b = 0; b < 8; ++b)
-                kr[0][b] = __ldg(reinterpret_cast<const uint4*>(
-                                     Ku + (size_t)__shfl_sync(qmask, jv[0], b, 8) * kHeadDim) + ql);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (k < 3 && 8 * (k + 1) < cnt) {
-#pragma unroll
-                    for (int b = 0; b < 8; ++b)
-                        kr[(k + 1) & 1][b] = __ldg(reinterpret_cast<const uint4*>(
-                                                 Ku + (size_t)__shfl_sync(qmask, jv[k + 1], b, 8) * kHeadDim) + ql);
+                for (int b = 0; b < 8; ++b) {
+                    const int j = __shfl_sync(qmask, jB, b, 8);
+                    kB[b] = b < nB ? __ldg(Ku + (size_t)j * 8) : make_uint4(0u, 0u, 0u, 0u);
                 }
-                if (8 * k < cnt) {
-                    float v[8];
+                // batch A: 8 partial dot products, reduced across the quarter
+                float qf[8], v[8];
+                unpack8(qA, qf);
 #pragma unroll
-                    for (int b = 0; b < 8; ++b) {
-                        float kx[8];
-                        unpack8(kr[k & 1][b], kx);
-                        v[b] = q[0] * kx[0] + q[1] * kx[1] + q[2] * kx[2] + q[3] * kx[3] +
-                               q[4] * kx[4] + q[5] * kx[5] + q[6] * kx[6] + q[7] * kx[7];
-                    }
-                    const float dot = reduce8_transpose(v, ql, qmask);   // slot base + 8 k + ql
-                    if (8 * k + ql < cnt) {
-                        const float sc = dot * kScale;
-                        wx[base + 8 * k + ql] = sc;
-                        m = fmaxf(m, sc);
-                    }
+                for (int b = 0; b < 8; ++b) {
+                    float kx[8];
+                    unpack8(kA[b], kx);
+                    v[b] = qf[0] * kx[0] + qf[1] * kx[1] + qf[2] * kx[2] + qf[3] * kx[3] +
+                           qf[4] * kx[4] + qf[5] * kx[5] + qf[6] * kx[6] + qf[7] * kx[7];
                 }
+                const float dot = reduce8_transpose(v, ql, qmask);   // slot eA + ql
+                if (eA + ql < ss[rA + 1]) {
+                    const float sc = dot * kScale;
+                    wx[eA + ql] = sc;
+                    mrow = fmaxf(mrow, sc);
+                }
+                if (rB != rA) {
+                    // row rA ends with this batch
+#pragma unroll
+                    for (int off = 4; off > 0; off >>= 1) mrow = fmaxf(mrow, __shfl_xor_sync(qmask, mrow, off, 8));
+                    if (ql == 0) mx[rA] = mrow;
+                    mrow = -INFINITY;
+                }
+                rA = rB; eA = eB; qA = qB;
+#pragma unroll
+                for (int b = 0; b < 8; ++b) kA[b] = kB[b];
+                rB = rC; eB = eC; qB = qC; jB = jC;
             }
         }
-#pragma unroll
-        for (int off = 4; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(qmask, m, off, 8));
-        if (ql == 0) a.w.m_sparse[(size_t)u * P.n + i] = m;
+        __syncwarp(qmask);                        // the window's smem is rewritten next
+        Rw += cnt;
     }
 }
 
@@ -708,7 +766,6 @@ ScoreArgs make_args(const diffuser_graph* g, const BandPlan& p, int64_t units, c
     s.units = units;
     s.gr = band_graph_refs(g);
     s.w = band_weights(ws, L);
-    s.counters = reinterpret_cast<int*>(ws + L.counters);
     s.Q = nullptr;
     s.K = nullptr;
     return s;
@@ -727,8 +784,7 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
 
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(scores)");
-    cudaError_t err = cudaMemsetAsync(ws + L.counters, 0, (size_t)units * 4, stream);
-    if (err != cudaSuccess) return cuda_fail(err, "clearing the tile counters");
+    cudaError_t err;
     ScoreArgs a = make_args(g, p, units, ws, L);
     const auto* Qb = static_cast<const __nv_bfloat16*>(Q);
     const auto* Kb = static_cast<const __nv_bfloat16*>(K);
@@ -737,7 +793,7 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
     const unsigned grid = (unsigned)(units * p.tiles);
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
-        score_sparse_kernel<<<grid, kSparseThreads, 0, stream>>>(a, Qb, Kb);
+        score_sparse_kernel<<<(unsigned)(sm_count_scores() * kSparseBlocks), kSparseThreads, 0, stream>>>(a, Qb, Kb);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_sparse_kernel");
 
@@ -758,13 +814,7 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled (Q/K) failed: " + std::to_string((int)r));
-    static int num_sms = 0;
-    if (num_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms < 1)
-            num_sms = 1;
-    }
+    const int num_sms = sm_count_scores();
     const unsigned pgrid = grid < (unsigned)num_sms ? grid : (unsigned)num_sms;
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);

@@ -39,7 +39,7 @@ struct BandLayout {
     size_t z[2];        // hop state Z_k, [units][n][hi 64 | lo 64] bf16, ping-pong
     size_t zf[2];       // the same Z_k as fp32 rows [units][n][64] (row gathers)
     size_t psum;        // sparse partial of the rows not in G, [units][n][64] fp32
-    size_t gpart, inv_l, m_sparse, gstat, sstat, counters, total;
+    size_t gpart, inv_l, m_sparse, gstat, total;
 };
 
 }  // namespace dfs
