@@ -372,7 +372,7 @@ int forward_device(const void* Q, const void* K, const void* V, int32_t dtype, i
         const ReplayKey key{Q, K, V, out, workspace, workspace_bytes, B, H, dtype, hops, alpha, g_path.load()};
         return band_forward(g, key, stream, [&](cudaStream_t s) {
             int r = launch_band_scores(g, bp, B * H, Q, K, ws, BL, false, s);
-            if (!r) r = launch_band_hops(g, bp, B * H, V, hops, alpha, out, ws, BL, s);
+            if (!r) r = launch_band_hops(g, bp, B * H, Q, K, V, hops, alpha, out, ws, BL, s);
             return r;
         });
     }

@@ -1,6 +1,4 @@
-// Diffusion hops of the band path (token graphs, bf16 I/O), over the weight
-// layout described in band_common.cuh (unnormalized e_ij as bf16 hi / lo
-// pairs plus 1/l_i).
+// Diffusion hops of the band path (token graphs, bf16 I/O).
 //
 // Hop Z_{k+1} = (1-alpha) A Z_k + alpha V ("Diffuser...", sec 2.4 eq S.7),
 // two kernels per hop:
@@ -9,27 +7,30 @@
 //            are split evenly over the quarter-warps of the grid; each walks
 //            its rows' extras as one stream with several rows in flight, the
 //            next slots' indices loading meanwhile; every load instruction
-//            reads whole 128-byte lines.
-//   hop_band_kernel (persistent, 128-row tiles): tcgen05 MMA, M = 128 rows,
-//            K = 64 keys per chunk, bf16 operands split into hi + lo (each the
-//            bf16 rounding of what is left): e_hi*[Z_hi | Z_lo] (N = 128) +
-//            e_lo*Z_hi (N = 64), fp32 accumulation in TMEM; the e_lo*Z_lo term
-//            (below 2^-16 of the product) is the only one left out.  The
-//            score kernel stores each chunk's A tile as the exact shared-memory
-//            image of the operand, so a chunk is two 16 KB bulk copies; the
-//            Z_k rows come by TMA as the MN-major B operand.  The globals
+//            reads whole 128-byte lines.  Hops after the first also sum the
+//            global rows of Z_k from the previous hop's tile shares.
+//   hop_band_kernel (persistent, 128-row tiles): the window part, on tcgen05
+//            tensor cores.  The band weights are not stored: per 64-key chunk
+//            the kernel recomputes S = Q_tile K_chunk^T (bf16 operands, fp32 in
+//            TMEM), turns it into e_ij = exp(s_ij - m_i) with the row maxima of
+//            the score pass (0 outside the window), and writes e as bf16 hi + lo
+//            (each the bf16 rounding of what is left) straight into the shared-
+//            memory operand image of the second MMA: e_hi*[Z_hi | Z_lo] (N = 128)
+//            + e_lo*Z_hi (N = 64), fp32 accumulation in TMEM; the e_lo*Z_lo term
+//            (below 2^-16 of the product) is the only one left out.  Re-reading
+//            the weights from HBM on every hop would cost 4 bytes per edge; the
+//            recomputation costs one exp per edge and a small MMA.  The globals
 //            outside each row's window are one more K step into the same
-//            accumulator: their weights' operand image [128 x g16] against the
-//            global keys' Z_k rows (staged by warp 2).  The global rows
-//            (full rows of A) ride along: on the two chunks that hold the
+//            accumulator (their stored weights' operand image [128 x g16]
+//            against the global keys' Z_k rows, staged by warp 2).  The global
+//            rows (full rows of A) ride along: on the two chunks that hold the
 //            tile's own keys, the same Z_k tiles also multiply the global rows'
 //            weights of those keys (a 32-row operand image) into a second
-//            accumulator; each tile writes that share, and the CTA that
-//            finishes a unit's last tile sums the unit's shares in tile order
-//            and writes the global rows.  Epilogue:
+//            accumulator, and each tile writes that share.  Epilogue:
 //            z_i = (1 - alpha) * inv_l_i * (band_i + P_i) + alpha * V_i,
 //            written as the next [hi | lo] bf16 row and fp32 row, or as the
-//            bf16 output.
+//            bf16 output.  The first hop also adds up the band part of each
+//            row sum and completes inv_l.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,35 +50,45 @@ using band::bf16hi;
 using band::bf16lo;
 using band::kChunkKeys;
 using band::kTileRows;
-// warp 0: TMA producer (A and Z), warp 1: MMA, warp 2: stages the global keys'
-// Z_k rows, warps 4-11: epilogue (warp w
-// reads TMEM lane quadrant w % 4, features 32 ((w - 4) / 4) .. +31).
-// One CTA per SM (its shared memory alone rules out a second one).
-constexpr int kThreads = 384;
-constexpr int kTmaWarp = 0, kMmaWarp = 1, kEpiWarp0 = 4, kEpiThreads = 256;
-constexpr int kAStages = 4;              // A ring: hi tile + lo tile, 32 KB per stage
-constexpr int kZStagesMax = 4;           // Z ring: hi tile + lo tile, 16 KB per stage (3 when g > 16)
-constexpr int kAccCols = 128;            // one accumulator: columns [0,64) A Z_hi, [64,128) A_hi Z_lo
-constexpr int kGlobCol0 = 256;           // the global rows' accumulators: columns 256 + 128 (lt & 1)
-constexpr int kTmemCols = 512;           // band and global accumulators, double-buffered tiles
-constexpr int kATileBytes = band::kChunkPlaneBytes;
-constexpr int kAStageBytes = 2 * kATileBytes;
+// warp 0: TMA producer of Q and K, warp 1: score MMAs, warp 2: the weights'
+// MMAs, warp 3: producer of Z_k, the globals' weight images and the global
+// keys' Z_k rows, warps 4-19: the band weights of each chunk and the tile's
+// epilogue (warp w serves TMEM lane quadrant w % 4 and keys / features
+// 16 ((w - 4) / 4) .. +15).  One CTA per SM.
+constexpr int kThreads = 640;
+constexpr int kTmaWarp = 0, kSMmaWarp = 1, kPvMmaWarp = 2, kZWarp = 3, kEpiWarp0 = 4, kEpiThreads = 512;
+constexpr int kEpiWarps = kEpiThreads / 32;
+constexpr int kQBytes = kTileRows * kHeadDim * 2;     // a Q tile, bf16 [128][64]
+constexpr int kKBytes = kChunkKeys * kHeadDim * 2;    // a K chunk, bf16 [64][64]
+constexpr int kKStagesMax = 5;           // K ring
+constexpr int kZStagesMax = 6;           // Z ring: hi tile + lo tile, 16 KB per stage (5 when g > 16)
+constexpr int kPStages = 2;              // weight operands in TMEM (hi, lo: 32 columns each)
+constexpr int kSBufs = 2;                // TMEM score buffers of 64 columns
+// TMEM: the accumulator D in columns [0, 128) ([0,64) P Z_hi, [64,128) P_hi Z_lo)
+constexpr int kGlobCol0 = 128;           // the global rows' accumulator, columns [128, 256)
+constexpr int kSCol0 = 256;              // score buffers, columns 256 + 64 b
+constexpr int kPCol0 = 384;              // weight operands, columns 384 + 64 p (hi; lo 32 on)
+constexpr int kTmemCols = 512;
 constexpr int kZTileBytes = kChunkKeys * 128;
 constexpr int kZStageBytes = 2 * kZTileBytes;
-// the global rows' operand image comes first: its descriptors span 16 KB past
-// their start (rows 32..127 read whatever follows; those rows are not used)
-// the out-of-window globals: their weights' operand image (hi, lo; g16 slots)
-// and the Z_k rows of the global keys as an MN-major B tile (hi, lo)
-// Shared memory of a launch: the Z ring gets 4 stages when the globals' tiles
-// are small enough (g16 <= 16), else 3.
-__host__ __device__ constexpr int z_stages(int g16) { return g16 > 16 ? 3 : 4; }
+constexpr float kScale = 0.125f;         // 1/sqrt(64)
+constexpr float kLog2e = 1.4426950408889634f;
+// Shared memory of a launch.  The global rows' operand image comes first: its
+// descriptors span 16 KB past their start (rows 32..127 read whatever
+// follows; those rows are not used).  Then 2 Q tiles, the K, Z and weight-image
+// rings, the out-of-window globals' weight image (hi, lo; g16 slots) and their
+// Z_k rows as an MN-major B tile (hi, lo), the row-sum exchange, barriers.
+// The Z ring gets 4 stages when the globals' tiles are small (g16 <= 16), else 3.
+__host__ __device__ constexpr int z_stages(int g16) { return g16 > 16 ? kZStagesMax - 1 : kZStagesMax; }
+__host__ __device__ constexpr int k_stages(int) { return kKStagesMax; }
 __host__ __device__ constexpr int band_smem_bytes(int g16) {
-    return 1024 + band::kGImgBytes + kAStages * kAStageBytes + z_stages(g16) * kZStageBytes +
-           2 * kTileRows * (g16 > 0 ? g16 : 16) * 2 + 2 * (g16 > 0 ? g16 : 16) * 128 + 256;
+    return 1024 + band::kGImgBytes + 2 * kQBytes + k_stages(g16) * kKBytes + z_stages(g16) * kZStageBytes +
+           2 * kTileRows * (g16 > 0 ? g16 : 16) * 2 + 2 * (g16 > 0 ? g16 : 16) * 128 +
+           kEpiThreads * 4 + 512;
 }
 constexpr int kSmemBytesMax = band_smem_bytes(16) > band_smem_bytes(kBandMaxGlobals)
                                   ? band_smem_bytes(16) : band_smem_bytes(kBandMaxGlobals);
-static_assert(band_smem_bytes(16) <= 227 * 1024 && kSmemBytesMax <= 227 * 1024, "shared memory per CTA");
+static_assert(kSmemBytesMax <= 227 * 1024, "shared memory per CTA");
 static_assert(band_smem_bytes(0) > 116 * 1024, "must exclude a second CTA per SM");
 
 struct HopArgs {
@@ -95,7 +106,6 @@ struct HopArgs {
     float* inv_l;                // [units][n] (the first hop's gather completes it)
     const float* m_sparse;       // [units][n] row maxima m_i
     const __nv_bfloat16* V;
-    const __nv_bfloat16* A_band; // the tiles' A images [units][tiles][chunks][hi | lo]
     const uint8_t* A_gcimg;      // out-of-window globals' weight images [units][tiles][hi | lo]
     const float* Zf_in;          // Z_k as fp32 rows [n][64] (hops after the first)
     __nv_bfloat16* Z_out;        // Z_{k+1} ([n][hi 64 | lo 64]), all hops but the last
@@ -208,27 +218,42 @@ __global__ void __launch_bounds__(256) hop_global_out_kernel(HopArgs a) {
 }
 
 // ---------------------------------------------------------------- band part of a hop
+// The band weights are recomputed here on every hop from Q and K rather than
+// read back: per 64-key chunk, S = Q_tile K_chunk^T on the tensor cores (the
+// same MMA as the score kernel, so the same values), e = exp(s - m_i) with the
+// row maxima the score kernel stored (0 outside the window), written as the
+// bf16 hi / lo operand image in shared memory, then D += P Z_k as before.  The
+// first hop also adds up each row's band sum and completes inv_l.
 template <bool kHop0, bool kLast>
 __global__ void __launch_bounds__(kThreads, 1)
-hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
+hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint8_t* sGA = smem;                                         // global rows: 2 halves x (hi, lo) 4 KB
-    uint8_t* sA = sGA + band::kGImgBytes;                        // kAStages x (hi 16 KB, lo 16 KB)
     const int g16 = a.plan.g16, g16s = g16 > 0 ? g16 : 16;
-    const int zstages = z_stages(g16);
-    uint8_t* sZ = sA + kAStages * kAStageBytes;                  // zstages x (hi 8 KB, lo 8 KB)
-    uint8_t* sGC = sZ + zstages * kZStageBytes;                 // out-of-window globals' weights
+    const int zstages = z_stages(g16), kstages = k_stages(g16);
+    uint8_t* sGA = smem;                                         // global rows: 2 halves x (hi, lo) 4 KB
+    uint8_t* sQ = sGA + band::kGImgBytes;                        // 2 x 16 KB
+    uint8_t* sK = sQ + 2 * kQBytes;                              // kstages x 8 KB
+    uint8_t* sZ = sK + kstages * kKBytes;                        // zstages x (hi 8 KB, lo 8 KB)
+    uint8_t* sGC = sZ + zstages * kZStageBytes;                  // out-of-window globals' weights
     uint8_t* sZG = sGC + 2 * kTileRows * g16s * 2;               // Z_k rows of the global keys
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sZG + 2 * g16s * 128);
-    uint64_t* full_A = bars;
-    uint64_t* empty_A = full_A + kAStages;
-    uint64_t* full_Z = empty_A + kAStages;
+    float* xch = reinterpret_cast<float*>(sZG + 2 * g16s * 128);  // [256] row-sum halves
+    uint64_t* bars = reinterpret_cast<uint64_t*>(xch + kEpiThreads);
+    uint64_t* full_Q = bars;                                     // [2]
+    uint64_t* empty_Q = full_Q + 2;                              // [2]
+    uint64_t* full_K = empty_Q + 2;                              // [kKStagesMax]
+    uint64_t* empty_K = full_K + kKStagesMax;
+    uint64_t* full_Z = empty_K + kKStagesMax;                    // [kZStagesMax]
     uint64_t* empty_Z = full_Z + kZStagesMax;
-    uint64_t* acc_full = empty_Z + kZStagesMax;                  // [2]
-    uint64_t* acc_empty = acc_full + 2;                          // [2]
-    uint64_t* full_G = acc_empty + 2;
+    uint64_t* full_S = empty_Z + kZStagesMax;                    // [kSBufs]
+    uint64_t* empty_S = full_S + kSBufs;
+    uint64_t* full_P = empty_S + kSBufs;                         // [kPStages]
+    uint64_t* empty_P = full_P + kPStages;
+    uint64_t* acc_full = empty_P + kPStages;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* full_G = acc_empty + 1;
     uint64_t* empty_G = full_G + 1;
     uint64_t* full_GC = empty_G + 1;       // the image by bulk copy + the staged Z rows
     uint64_t* empty_GC = full_GC + 1;
@@ -236,7 +261,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int chunks = P.chunks;
+    const int nc = P.chunks;
     const int c0 = P.r64 / kChunkKeys;           // chunks c0 and c0 + 1 hold the tile's own keys
     const bool has_g = P.g > 0;
     const int gc_plane = band::gc_plane_bytes(g16);
@@ -244,158 +269,78 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
     // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
     const int my_tiles = blockIdx.x < total_tiles
         ? (int)((total_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+    const int total = my_tiles * nc;             // chunks of this CTA
 
-    if (warp == kMmaWarp) ptx::tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kSMmaWarp) ptx::tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
-        for (int s = 0; s < kAStages; ++s) { ptx::mbar_init(&full_A[s], 1); ptx::mbar_init(&empty_A[s], 1); }
+        for (int s = 0; s < 2; ++s) { ptx::mbar_init(&full_Q[s], 1); ptx::mbar_init(&empty_Q[s], 1); }
+        for (int s = 0; s < kstages; ++s) { ptx::mbar_init(&full_K[s], 1); ptx::mbar_init(&empty_K[s], 1); }
         for (int s = 0; s < zstages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
-        for (int s = 0; s < 2; ++s) { ptx::mbar_init(&acc_full[s], 1); ptx::mbar_init(&acc_empty[s], kEpiThreads); }
+        // the weight warps arrive once per warp (lane 0, after the warp has synced)
+        for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], kEpiWarps); }
+        for (int s = 0; s < kPStages; ++s) { ptx::mbar_init(&full_P[s], kEpiWarps); ptx::mbar_init(&empty_P[s], 1); }
+        ptx::mbar_init(acc_full, 1);
+        ptx::mbar_init(acc_empty, kEpiWarps);
         ptx::mbar_init(full_G, 1);
         ptx::mbar_init(empty_G, 1);
         ptx::mbar_init(full_GC, 2);
         ptx::mbar_init(empty_GC, 1);
         ptx::fence_mbar_init();
     }
-    if (warp == kTmaWarp && lane == 0) ptx::prefetch_tensormap(&tmZ);
+    if (warp == kTmaWarp && lane == 0) {
+        ptx::prefetch_tensormap(&tmQ);
+        ptx::prefetch_tensormap(&tmK);
+        ptx::prefetch_tensormap(&tmZ);
+    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kTmaWarp) {
-        // ---------------- TMA producer.  The chunk grid of a tile starts at key
-        // jb = i0 - r64; chunk c's A tile is one contiguous image (hi, lo).
+        // ---------------- TMA producer of the score operands: the Q tile and the K
+        // chunks (keys of the chunk grid jb = i0 - r64 ..; outside 0..n-1 they load
+        // as zeros), in the order the score MMAs use them.
         if (lane == 0) {
-            // the weights are read once per hop; Z_k is re-read by neighbouring tiles
-            const uint64_t pol_a = ptx::l2_evict_first(), pol_z = ptx::l2_evict_last();
-            for (int lt = 0; lt < my_tiles; ++lt) {
+            const uint64_t pol_keep = ptx::l2_evict_last();      // re-read by neighbouring tiles
+            for (int g = 0; g < total; ++g) {
+                const int lt = g / nc, c = g - lt * nc, qb = lt & 1;
                 const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
                 const int64_t u = tix / P.tiles;
                 const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-                const int64_t jb = i0 - P.r64;
-                const uint8_t* timg = reinterpret_cast<const uint8_t*>(a.A_band) +
-                                      (size_t)tix * chunks * band::kChunkImageBytes;
-                if (has_g) {
-                    if (lt >= 1) ptx::mbar_wait(empty_GC, (lt - 1) & 1, a.status);
+                if (c == 0) {
+                    if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, a.status);
+                    ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
+                    ptx::tma_load_3d_hint(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, (int)i0, (int)u, pol_keep);
+                }
+                const int sk = g % kstages;
+                if (g >= kstages) ptx::mbar_wait(&empty_K[sk], ((g / kstages) - 1) & 1, a.status);
+                ptx::mbar_arrive_expect_tx(&full_K[sk], kKBytes);
+                ptx::tma_load_3d_hint(sK + sk * kKBytes, &tmK, &full_K[sk], 0,
+                                      (int)(i0 - P.r64 + kChunkKeys * c), (int)u, pol_keep);
+            }
+        }
+    } else if (warp == kZWarp) {
+        // ---------------- producer of the weights' MMA operands (whole warp; lane 0
+        // issues the copies): per tile the globals' images and the global keys'
+        // Z_k rows, per chunk the Z_k rows, in the order the MMAs use them.
+        const uint64_t pol_once = ptx::l2_evict_first(), pol_keep = ptx::l2_evict_last();
+        for (int g = 0; g < total; ++g) {
+            const int lt = g / nc, c = g - lt * nc;
+            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+            const int64_t u = tix / P.tiles;
+            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+            if (has_g && c == 0) {
+                // the out-of-window globals: their weights' image by bulk copy, and the
+                // global keys' Z_k rows as an MN-major B tile (key row s: hi 128 bytes,
+                // lo g16 * 128 bytes on; 16-byte chunk c at (c ^ (s % 8)) * 16; rows
+                // past g are zero)
+                if (lt >= 1) ptx::mbar_wait(empty_GC, (lt - 1) & 1, a.status);
+                if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(full_GC, 2 * gc_plane);
                     ptx::bulk_load_hint(sGC, a.A_gcimg + (size_t)tix * 2 * gc_plane, 2 * gc_plane, full_GC,
-                                        pol_a);
-                    if (lt >= 1) ptx::mbar_wait(empty_G, (lt - 1) & 1, a.status);
-                    ptx::mbar_arrive_expect_tx(full_G, band::kGImgBytes);
-                    ptx::bulk_load_hint(sGA, a.A_gimg + (size_t)tix * band::kGImgBytes, band::kGImgBytes,
-                                        full_G, pol_a);
+                                        pol_once);
                 }
-                for (int c = 0; c < chunks; ++c) {
-                    const int gc = lt * chunks + c;
-                    const int sa = gc % kAStages;
-                    if (gc >= kAStages) ptx::mbar_wait(&empty_A[sa], ((gc / kAStages) - 1) & 1, a.status);
-                    ptx::mbar_arrive_expect_tx(&full_A[sa], kAStageBytes);
-                    uint8_t* adst = sA + sa * kAStageBytes;
-                    const uint8_t* asrc = timg + (size_t)c * band::kChunkImageBytes;
-                    ptx::bulk_load_hint(adst, asrc, kATileBytes, &full_A[sa], pol_a);
-                    ptx::bulk_load_hint(adst + kATileBytes, asrc + kATileBytes, kATileBytes, &full_A[sa], pol_a);
-                    const int sz = gc % zstages;
-                    if (gc >= zstages) ptx::mbar_wait(&empty_Z[sz], ((gc / zstages) - 1) & 1, a.status);
-                    uint8_t* zdst = sZ + sz * kZStageBytes;
-                    ptx::mbar_arrive_expect_tx(&full_Z[sz], kHop0 ? kZTileBytes : 2 * kZTileBytes);
-                    const int key = (int)(jb + kChunkKeys * c);
-                    ptx::tma_load_3d_hint(zdst, &tmZ, &full_Z[sz], 0, key, (int)u, pol_z);
-                    if (!kHop0)
-                        ptx::tma_load_3d_hint(zdst + kZTileBytes, &tmZ, &full_Z[sz], kHeadDim, key, (int)u, pol_z);
-                }
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer: accumulator lt & 1 of TMEM columns [128 (lt & 1), +128)
-        if (lane == 0) {
-            constexpr uint32_t idesc64 = ptx::mma_idesc_bf16_bmn(64);
-            constexpr uint32_t idesc128 = ptx::mma_idesc_bf16_bmn(128);
-            for (int lt = 0; lt < my_tiles; ++lt) {
-                const int ab = lt & 1;
-                if (lt >= 2) ptx::mbar_wait(&acc_empty[ab], ((lt / 2) - 1) & 1, a.status);
-                ptx::tc_fence_after();
-                const uint32_t dacc = tmem + kAccCols * ab;
-                if (has_g) {
-                    // the globals outside each row's window: [128 x g16] x [g16 x (hi | lo)]
-                    ptx::mbar_wait(full_GC, lt & 1, a.status);
-                    ptx::tc_fence_after();
-                    const uint32_t gch = ptx::smem_u32(sGC), gcl = gch + gc_plane;
-                    const uint32_t zg = ptx::smem_u32(sZG);
-                    for (int ks = 0; ks < g16 / 16; ++ks) {
-                        const uint64_t bdesc = ptx::sw128_mnmajor_desc(zg + 2048 * ks, g16 * 128);
-                        ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gch + 256 * ks, 128, 16 * g16), bdesc,
-                                         kHop0 ? idesc64 : idesc128, ks != 0);
-                        ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gcl + 256 * ks, 128, 16 * g16), bdesc,
-                                         idesc64, 1);
-                    }
-                    ptx::mma_commit(empty_GC);
-                }
-                for (int c = 0; c < chunks; ++c) {
-                    const int gc = lt * chunks + c;
-                    const int sa = gc % kAStages, sz = gc % zstages;
-                    ptx::mbar_wait(&full_A[sa], (gc / kAStages) & 1, a.status);
-                    ptx::mbar_wait(&full_Z[sz], (gc / zstages) & 1, a.status);
-                    ptx::tc_fence_after();
-                    const uint32_t ahi = ptx::smem_u32(sA + sa * kAStageBytes);
-                    const uint32_t alo = ahi + kATileBytes;
-                    const uint32_t zb = ptx::smem_u32(sZ + sz * kZStageBytes);
-#pragma unroll
-                    for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
-                        const uint64_t bdesc = ptx::sw128_mnmajor_desc(zb + 2048 * ks, kZTileBytes);
-                        ptx::mma_bf16_ss(dacc, ptx::sw128_kmajor_desc(ahi + 32 * ks), bdesc,
-                                         kHop0 ? idesc64 : idesc128, has_g || (c | ks) != 0);
-                        ptx::mma_bf16_ss(dacc, ptx::sw128_kmajor_desc(alo + 32 * ks), bdesc, idesc64, 1);
-                    }
-                    const int h = c - c0;
-                    if (has_g && (h == 0 || h == 1)) {
-                        // the global rows x this tile's own keys (same Z_k tile)
-                        if (h == 0) {
-                            ptx::mbar_wait(full_G, lt & 1, a.status);
-                            ptx::tc_fence_after();
-                        }
-                        const uint32_t dglob = tmem + kGlobCol0 + kAccCols * ab;
-                        const uint32_t ghi = ptx::smem_u32(sGA + h * 2 * band::kGImgPlaneBytes);
-                        const uint32_t glo = ghi + band::kGImgPlaneBytes;
-#pragma unroll
-                        for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
-                            const uint64_t bdesc = ptx::sw128_mnmajor_desc(zb + 2048 * ks, kZTileBytes);
-                            ptx::mma_bf16_ss(dglob, ptx::sw128_kmajor_desc(ghi + 32 * ks), bdesc,
-                                             kHop0 ? idesc64 : idesc128, (h | ks) != 0);
-                            ptx::mma_bf16_ss(dglob, ptx::sw128_kmajor_desc(glo + 32 * ks), bdesc, idesc64, 1);
-                        }
-                        if (h == 1) ptx::mma_commit(empty_G);
-                    }
-                    ptx::mma_commit(&empty_A[sa]);
-                    ptx::mma_commit(&empty_Z[sz]);
-                }
-                ptx::mma_commit(&acc_full[ab]);
-            }
-            // Drain: the commits arrive asynchronously when the MMAs finish.  Wait
-            // for the last phase of every empty barrier so that no arrival can land
-            // in this shared memory after the CTA exits.
-            const int total = my_tiles * chunks;
-            for (int s = 0; s < kAStages; ++s) {
-                const int uses = (total - s + kAStages - 1) / kAStages;
-                if (uses > 0) ptx::mbar_wait(&empty_A[s], (uses - 1) & 1, a.status);
-            }
-            for (int s = 0; s < zstages; ++s) {
-                const int uses = (total - s + zstages - 1) / zstages;
-                if (uses > 0) ptx::mbar_wait(&empty_Z[s], (uses - 1) & 1, a.status);
-            }
-            if (has_g && my_tiles > 0) {
-                ptx::mbar_wait(empty_G, (my_tiles - 1) & 1, a.status);
-                ptx::mbar_wait(empty_GC, (my_tiles - 1) & 1, a.status);
-            }
-        }
-    } else if (warp == 2) {
-        // ---------------- the global keys' Z_k rows as the B tile of the out-of-window
-        // globals' MMA: key row s (hi 128 bytes; lo g16 * 128 bytes on), 16-byte chunk
-        // c at (c ^ (s % 8)) * 16; rows past g are zero
-        if (has_g) {
-            for (int lt = 0; lt < my_tiles; ++lt) {
-                const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
-                const int64_t u = tix / P.tiles;
-                if (lt >= 1) ptx::mbar_wait(empty_GC, (lt - 1) & 1, a.status);
                 for (int e = lane; e < g16 * 8; e += 32) {
                     const int sl = e >> 3, cch = e & 7;
                     float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -423,69 +368,276 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(full_GC);
             }
+            if (has_g && c == c0) {
+                if (lt >= 1) ptx::mbar_wait(empty_G, (lt - 1) & 1, a.status);
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(full_G, band::kGImgBytes);
+                    ptx::bulk_load_hint(sGA, a.A_gimg + (size_t)tix * band::kGImgBytes, band::kGImgBytes,
+                                        full_G, pol_once);
+                }
+            }
+            const int key = (int)(i0 - P.r64 + kChunkKeys * c);
+            const int sz = g % zstages;
+            if (g >= zstages) ptx::mbar_wait(&empty_Z[sz], ((g / zstages) - 1) & 1, a.status);
+            if (lane == 0) {
+                uint8_t* zdst = sZ + sz * kZStageBytes;
+                ptx::mbar_arrive_expect_tx(&full_Z[sz], kHop0 ? kZTileBytes : 2 * kZTileBytes);
+                ptx::tma_load_3d_hint(zdst, &tmZ, &full_Z[sz], 0, key, (int)u, pol_keep);
+                if (!kHop0)
+                    ptx::tma_load_3d_hint(zdst + kZTileBytes, &tmZ, &full_Z[sz], kHeadDim, key, (int)u, pol_keep);
+            }
+            __syncwarp();
+        }
+    } else if (warp == kSMmaWarp) {
+        // ---------------- score MMAs: S[b] = Q_tile K_chunk^T (both K-major,
+        // 128-byte swizzle), as far ahead of the weights as the TMEM buffers allow
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = ptx::mma_idesc(1, kChunkKeys);
+            for (int g = 0; g < total; ++g) {
+                const int lt = g / nc, c = g - lt * nc, qb = lt & 1;
+                if (c == 0) ptx::mbar_wait(&full_Q[qb], (lt / 2) & 1, a.status);
+                const int sk = g % kstages, b = g % kSBufs;
+                ptx::mbar_wait(&full_K[sk], (g / kstages) & 1, a.status);
+                if (g >= kSBufs) ptx::mbar_wait(&empty_S[b], ((g / kSBufs) - 1) & 1, a.status);
+                ptx::tc_fence_after();
+                const uint32_t qa = ptx::smem_u32(sQ + qb * kQBytes);
+                const uint32_t kb = ptx::smem_u32(sK + sk * kKBytes);
+#pragma unroll
+                for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                    ptx::mma_bf16_ss(tmem + kSCol0 + kChunkKeys * b, ptx::sw128_kmajor_desc(qa + 32 * ks),
+                                     ptx::sw128_kmajor_desc(kb + 32 * ks), idesc_s, ks > 0);
+                ptx::mma_commit(&empty_K[sk]);
+                ptx::mma_commit(&full_S[b]);
+                if (c == nc - 1) ptx::mma_commit(&empty_Q[qb]);
+            }
+            // Drain: the commits arrive asynchronously when the MMAs finish; wait for
+            // the last phase of each so that none lands in shared memory after exit.
+            for (int s = 0; s < kstages; ++s) {
+                const int uses = (total - s + kstages - 1) / kstages;
+                if (uses > 0) ptx::mbar_wait(&empty_K[s], (uses - 1) & 1, a.status);
+            }
+            for (int s = 0; s < 2; ++s) {
+                const int uses = (my_tiles - s + 1) / 2;
+                if (uses > 0) ptx::mbar_wait(&empty_Q[s], (uses - 1) & 1, a.status);
+            }
+        }
+    } else if (warp == kPvMmaWarp) {
+        // ---------------- the weights' MMAs, chunk by chunk as the weight images are
+        // written: D += P_hi [Z_hi | Z_lo] + P_lo Z_hi, the globals and global rows
+        if (lane == 0) {
+            constexpr uint32_t idesc64 = ptx::mma_idesc_bf16_bmn(64);
+            constexpr uint32_t idesc128 = ptx::mma_idesc_bf16_bmn(128);
+            const uint32_t dacc = tmem;
+            for (int g = 0; g < total; ++g) {
+                const int lt = g / nc, c = g - lt * nc;
+                if (c == 0) {
+                    // the previous tile's accumulators have been read
+                    if (lt >= 1) ptx::mbar_wait(acc_empty, (lt - 1) & 1, a.status);
+                    ptx::tc_fence_after();
+                    if (has_g) {
+                        // the globals outside each row's window: [128 x g16] x [g16 x (hi | lo)]
+                        ptx::mbar_wait(full_GC, lt & 1, a.status);
+                        ptx::tc_fence_after();
+                        const uint32_t gch = ptx::smem_u32(sGC), gcl = gch + gc_plane;
+                        const uint32_t zg = ptx::smem_u32(sZG);
+                        for (int ks = 0; ks < g16 / 16; ++ks) {
+                            const uint64_t bdesc = ptx::sw128_mnmajor_desc(zg + 2048 * ks, g16 * 128);
+                            ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gch + 256 * ks, 128, 16 * g16),
+                                             bdesc, kHop0 ? idesc64 : idesc128, ks != 0);
+                            ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gcl + 256 * ks, 128, 16 * g16),
+                                             bdesc, idesc64, 1);
+                        }
+                        ptx::mma_commit(empty_GC);
+                    }
+                }
+                const int sp = g % kPStages, sz = g % zstages;
+                ptx::mbar_wait(&full_P[sp], (g / kPStages) & 1, a.status);
+                ptx::mbar_wait(&full_Z[sz], (g / zstages) & 1, a.status);
+                ptx::tc_fence_after();
+                const uint32_t phi = tmem + kPCol0 + 64 * sp;      // 8 columns per 16 keys
+                const uint32_t plo = phi + 32;
+                const uint32_t zb = ptx::smem_u32(sZ + sz * kZStageBytes);
+#pragma unroll
+                for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
+                    const uint64_t bdesc = ptx::sw128_mnmajor_desc(zb + 2048 * ks, kZTileBytes);
+                    ptx::mma_bf16_ts(dacc, phi + 8 * ks, bdesc, kHop0 ? idesc64 : idesc128,
+                                     has_g || (c | ks) != 0);
+                    ptx::mma_bf16_ts(dacc, plo + 8 * ks, bdesc, idesc64, 1);
+                }
+                const int h = c - c0;
+                if (has_g && (h == 0 || h == 1)) {
+                    // the global rows x this tile's own keys (same Z_k tile)
+                    if (h == 0) {
+                        ptx::mbar_wait(full_G, lt & 1, a.status);
+                        ptx::tc_fence_after();
+                    }
+                    const uint32_t dglob = tmem + kGlobCol0;
+                    const uint32_t ghi = ptx::smem_u32(sGA + h * 2 * band::kGImgPlaneBytes);
+                    const uint32_t glo = ghi + band::kGImgPlaneBytes;
+#pragma unroll
+                    for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
+                        const uint64_t bdesc = ptx::sw128_mnmajor_desc(zb + 2048 * ks, kZTileBytes);
+                        ptx::mma_bf16_ss(dglob, ptx::sw128_kmajor_desc(ghi + 32 * ks), bdesc,
+                                         kHop0 ? idesc64 : idesc128, (h | ks) != 0);
+                        ptx::mma_bf16_ss(dglob, ptx::sw128_kmajor_desc(glo + 32 * ks), bdesc, idesc64, 1);
+                    }
+                    if (h == 1) ptx::mma_commit(empty_G);
+                }
+                ptx::mma_commit(&empty_P[sp]);
+                ptx::mma_commit(&empty_Z[sz]);
+                if (c == nc - 1) ptx::mma_commit(acc_full);
+            }
+            for (int s = 0; s < zstages; ++s) {
+                const int uses = (total - s + zstages - 1) / zstages;
+                if (uses > 0) ptx::mbar_wait(&empty_Z[s], (uses - 1) & 1, a.status);
+            }
+            for (int s = 0; s < kPStages; ++s) {
+                const int uses = (total - s + kPStages - 1) / kPStages;
+                if (uses > 0) ptx::mbar_wait(&empty_P[s], (uses - 1) & 1, a.status);
+            }
+            if (has_g && my_tiles > 0) {
+                ptx::mbar_wait(empty_G, (my_tiles - 1) & 1, a.status);
+                ptx::mbar_wait(empty_GC, (my_tiles - 1) & 1, a.status);
+            }
         }
     } else if (warp >= kEpiWarp0) {
-        // ---------------- epilogue: thread <-> row t = 32 quad + lane, features 32 fhalf .. +31
+        // ---------------- weights and epilogue: thread <-> row t = 32 quad + lane,
+        // keys (of each chunk) and features 16 slice .. +15; the four warps of a
+        // lane quadrant meet on named barrier 2 + quad
         const int quad = warp & 3;
-        const int fhalf = (warp - kEpiWarp0) >> 2;
+        const int slice = (warp - kEpiWarp0) >> 2;        // 0..3
+        const int etid = tid - kEpiWarp0 * 32;            // 0..511
+        const int quad_bar = 2 + quad;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int t = quad * 32 + lane;
+        const float a_sc = kLog2e * kScale;
         for (int lt = 0; lt < my_tiles; ++lt) {
             const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
             const int64_t u = tix / P.tiles;
             const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-            const int t = quad * 32 + lane;
+            const int64_t jb = i0 - P.r64;
             const int64_t i = i0 + t;
             const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
-            // the row's inputs, fetched while the MMAs of this tile run
-            const size_t vrow = ((size_t)u * P.n + (row_ok ? i : 0)) * kHeadDim + 32 * fhalf;
-            float keep = 0.f;
-            float4 pv[8];
-            uint4 vv[4];
+            const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
+            const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+            const size_t urow = (size_t)u * P.n + (row_ok ? i : 0);
+            // the row's inputs, fetched while the chunks are processed
+            const size_t vrow = urow * kHeadDim + 16 * slice;
+            const float b2 = row_ok ? __ldg(a.m_sparse + urow) * kLog2e : 0.f;
+            float lsum_in = 0.f;
+            float4 pv[4];
+            uint4 vv[2];
             if (row_ok) {
-                keep = (1.f - a.alpha) * __ldg(a.inv_l + (size_t)u * P.n + i);
+                lsum_in = __ldg(a.inv_l + urow);
                 const float4* pp = reinterpret_cast<const float4*>(a.Psum + vrow);
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) pv[c4] = __ldg(pp + c4);
+                for (int c4 = 0; c4 < 4; ++c4) pv[c4] = __ldg(pp + c4);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) vv[c4] = __ldg(reinterpret_cast<const uint4*>(a.V + vrow) + c4);
+                for (int c4 = 0; c4 < 2; ++c4) vv[c4] = __ldg(reinterpret_cast<const uint4*>(a.V + vrow) + c4);
             }
-            const int ab = lt & 1;
-            ptx::mbar_wait(&acc_full[ab], (lt / 2) & 1, a.status);
+            float lsum = 0.f;
+            for (int c = 0; c < nc; ++c) {
+                const int g = lt * nc + c;
+                const int b = g % kSBufs;
+                ptx::mbar_wait(&full_S[b], (g / kSBufs) & 1, a.status);
+                __syncwarp();       // reconverge before the warp-collective tcgen05.ld
+                ptx::tc_fence_after();
+                float sv[16];
+                ptx::tmem_ld16(tmem + lane_base + kSCol0 + kChunkKeys * b + 16 * slice, sv);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&empty_S[b]);
+                // e = exp(s - m_i) inside the row's window (keys lo..hi), else 0
+                const int64_t j0 = jb + kChunkKeys * c + 16 * slice;
+                const bool full_in = row_ok && j0 >= lo && j0 + 15 <= hi;
+                const bool none_in = !row_ok || j0 > hi || j0 + 15 < lo;
+                float e[16];
+                if (none_in) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) e[k] = 0.f;
+                } else if (full_in) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) e[k] = ptx::ex2_approx(fmaf(sv[k], a_sc, -b2));
+                } else {
+                    const int dlo = (int)(lo - j0), dhi = (int)(hi - j0);   // in-window keys k in [dlo, dhi]
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        e[k] = (k >= dlo && k <= dhi) ? ptx::ex2_approx(fmaf(sv[k], a_sc, -b2)) : 0.f;
+                }
+                if (kHop0) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) lsum += e[k];
+                }
+                // this row's 16 keys of the chunk's weight operand: hi and lo bf16,
+                // two keys per TMEM column (the k-step's 8 columns of this slice)
+                uint32_t hw[8], lw[8];
+#pragma unroll
+                for (int p2 = 0; p2 < 8; ++p2) {
+                    const float x0 = e[2 * p2], x1 = e[2 * p2 + 1];
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+                    hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
+                    lw[p2] = *reinterpret_cast<const uint32_t*>(&l);
+                }
+                const int sp = g % kPStages;
+                if (g >= kPStages) ptx::mbar_wait(&empty_P[sp], ((g / kPStages) - 1) & 1, a.status);
+                __syncwarp();       // reconverge before the warp-collective tcgen05.st
+                const uint32_t pcol = tmem + lane_base + kPCol0 + 64 * sp + 8 * slice;
+                ptx::tmem_st8x2(pcol, hw, pcol + 32, lw);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&full_P[sp]);
+            }
+            // the normalizer: the first hop completes the row sum with the band part
+            // (the four slices' partial sums added in slice order)
+            float inv = row_ok ? lsum_in : 0.f;
+            if (kHop0) {
+                xch[etid] = lsum;
+                ptx::named_barrier_sync(quad_bar, 128);
+                const int r0 = quad * 32 + lane;          // xch[128 s + 32 quad + lane] is slice s
+                const float lband = ((xch[r0] + xch[128 + r0]) + xch[256 + r0]) + xch[384 + r0];
+                ptx::named_barrier_sync(quad_bar, 128);   // xch is reused by the next tile
+                inv = row_ok ? 1.f / (lband + lsum_in) : 0.f;
+                if (slice == 0 && row_ok) a.inv_l[urow] = inv;
+            }
+            const float keep = (1.f - a.alpha) * inv;
+            ptx::mbar_wait(acc_full, lt & 1, a.status);
             __syncwarp();       // reconverge before the warp-collective tcgen05.ld
             ptx::tc_fence_after();
             if (has_g && quad == 0) {
                 // TMEM lanes 0..31 of the global accumulator are the global slots s:
                 // this tile's share of the global rows (summed by global_row_out)
-                float gd[32];
-                ptx::tmem_ld32(tmem + kGlobCol0 + kAccCols * ab + 32 * fhalf, gd);
+                float gd[16];
+                ptx::tmem_ld16(tmem + kGlobCol0 + 16 * slice, gd);
                 if (!kHop0) {
-                    float g2[32];
-                    ptx::tmem_ld32(tmem + kGlobCol0 + kAccCols * ab + kHeadDim + 32 * fhalf, g2);
+                    float g2[16];
+                    ptx::tmem_ld16(tmem + kGlobCol0 + kHeadDim + 16 * slice, g2);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) gd[k] += g2[k];
+                    for (int k = 0; k < 16; ++k) gd[k] += g2[k];
                 }
                 if (lane < P.g) {
                     float4* gp = reinterpret_cast<float4*>(
-                        a.gpart + (((size_t)u * P.tiles + (i0 / kTileRows)) * P.g + lane) * kHeadDim + 32 * fhalf);
+                        a.gpart + (((size_t)u * P.tiles + (i0 / kTileRows)) * P.g + lane) * kHeadDim + 16 * slice);
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4)
+                    for (int c4 = 0; c4 < 4; ++c4)
                         gp[c4] = make_float4(gd[4 * c4], gd[4 * c4 + 1], gd[4 * c4 + 2], gd[4 * c4 + 3]);
                 }
             }
-            float d[32];
-            ptx::tmem_ld32(tmem + lane_base + kAccCols * ab + 32 * fhalf, d);
+            float d[16];
+            ptx::tmem_ld16(tmem + lane_base + 16 * slice, d);
             if (!kHop0) {
-                float d2[32];
-                ptx::tmem_ld32(tmem + lane_base + kAccCols * ab + kHeadDim + 32 * fhalf, d2);
+                float d2[16];
+                ptx::tmem_ld16(tmem + lane_base + kHeadDim + 16 * slice, d2);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) d[k] += d2[k];
+                for (int k = 0; k < 16; ++k) d[k] += d2[k];
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&acc_empty[ab]);                    // the accumulators are in registers
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(acc_empty);          // the accumulators are in registers
             if (row_ok) {
-                float z[32];
+                float z[16];
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
+                for (int c4 = 0; c4 < 2; ++c4) {
                     const uint32_t w4[4] = {vv[c4].x, vv[c4].y, vv[c4].z, vv[c4].w};
                     const float p8[8] = {pv[2 * c4].x, pv[2 * c4].y, pv[2 * c4].z, pv[2 * c4].w,
                                          pv[2 * c4 + 1].x, pv[2 * c4 + 1].y, pv[2 * c4 + 1].z, pv[2 * c4 + 1].w};
@@ -499,16 +651,16 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
                 if (kLast) {
                     uint4* op = reinterpret_cast<uint4*>(a.out + vrow);
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) op[c4] = pack8(z + 8 * c4);
+                    for (int c4 = 0; c4 < 2; ++c4) op[c4] = pack8(z + 8 * c4);
                 } else {
-                    __nv_bfloat16* zr = a.Z_out + ((size_t)u * P.n + i) * (2 * kHeadDim) + 32 * fhalf;
+                    __nv_bfloat16* zr = a.Z_out + urow * (2 * kHeadDim) + 16 * slice;
                     float4* zf = reinterpret_cast<float4*>(a.Zf_out + vrow);
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        uint4 hi, lo;
-                        split8(z + 8 * c4, hi, lo);
-                        reinterpret_cast<uint4*>(zr)[c4] = hi;
-                        reinterpret_cast<uint4*>(zr + kHeadDim)[c4] = lo;
+                    for (int c4 = 0; c4 < 2; ++c4) {
+                        uint4 hi4, lo4;
+                        split8(z + 8 * c4, hi4, lo4);
+                        reinterpret_cast<uint4*>(zr)[c4] = hi4;
+                        reinterpret_cast<uint4*>(zr + kHeadDim)[c4] = lo4;
                         zf[2 * c4] = make_float4(z[8 * c4], z[8 * c4 + 1], z[8 * c4 + 2], z[8 * c4 + 3]);
                         zf[2 * c4 + 1] = make_float4(z[8 * c4 + 4], z[8 * c4 + 5], z[8 * c4 + 6], z[8 * c4 + 7]);
                     }
@@ -518,7 +670,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmZ, HopArgs a) {
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+    if (warp == kSMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------- sparse part of a hop
@@ -594,8 +746,8 @@ hop_gather_kernel(HopArgs a) {
         int nb = ss[1];                           // first slot past row cur
         // First hop only: the extras' weights arrive as raw scores s; each
         // becomes e = exp(s - m_i) (stored back for the later hops), and the
-        // row's sum of e completes inv_l_i (which holds the band and globals'
-        // part of the sum on entry).
+        // row's sum of e is added to inv_l_i (the globals' part of the sum on
+        // entry; the band kernel adds the band part and inverts it).
         float mcur = kHop0 ? sm[0] : 0.f;
         float lsum = 0.f;
         // closes row cur: its partial P_i (and, first hop, inv_l_i)
@@ -604,10 +756,7 @@ hop_gather_kernel(HopArgs a) {
                 float4* pr = prow + (size_t)(iw + cur) * 16;
                 pr[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
                 pr[8] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
-                if (kHop0 && ql == 0) {
-                    float* il = a.inv_l + ubase + iw + cur;
-                    *il = 1.f / (*il + lsum);
-                }
+                if (kHop0 && ql == 0) a.inv_l[ubase + iw + cur] += lsum;
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
@@ -680,13 +829,14 @@ hop_gather_kernel(HopArgs a) {
 // the gather configuration: slots in flight per quarter-warp, CTAs per SM
 constexpr int kGatherBatch = 5, kGatherBlocks = 3;
 
-// bf16 tensor map over rows of `row_elems` elements: box of 64 elements x 64 rows
-int encode_rows(CUtensorMap* m, const void* base, int64_t n, int64_t units, int row_elems) {
+// bf16 tensor map over rows of `row_elems` elements: box of 64 elements x box_rows rows
+int encode_rows(CUtensorMap* m, const void* base, int64_t n, int64_t units, int row_elems,
+                int box_rows = kChunkKeys) {
     auto fn = band::tensor_map_encoder();
     if (!fn) return fail(DIFFUSER_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     const cuuint64_t dims[3] = {(cuuint64_t)row_elems, (cuuint64_t)n, (cuuint64_t)units};
     const cuuint64_t strides[2] = {(cuuint64_t)row_elems * 2, (cuuint64_t)n * row_elems * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)kChunkKeys, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)box_rows, 1};
     const cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -708,7 +858,8 @@ int sm_count() {
 }
 
 template <bool kHop0, bool kLast>
-int launch_hop(const CUtensorMap& tmZ, const HopArgs& a, cudaStream_t stream) {
+int launch_hop(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmZ, const HopArgs& a,
+               cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -728,7 +879,7 @@ int launch_hop(const CUtensorMap& tmZ, const HopArgs& a, cudaStream_t stream) {
     dim3 grid((unsigned)(total_tiles < sms ? total_tiles : sms));
     {
         LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
-        hop_band_kernel<kHop0, kLast><<<grid, kThreads, band_smem_bytes(a.plan.g16), stream>>>(tmZ, a);
+        hop_band_kernel<kHop0, kLast><<<grid, kThreads, band_smem_bytes(a.plan.g16), stream>>>(tmQ, tmK, tmZ, a);
     }
     err = cudaGetLastError();
     if (err != cudaSuccess) return cuda_fail(err, "hop_band_kernel");
@@ -815,12 +966,15 @@ int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     return DIFFUSER_OK;
 }
 
-int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* V,
-                     int32_t hops, float alpha, void* out, char* ws, const BandLayout& L,
-                     cudaStream_t stream) {
-    // tensor maps of the B operand: V ([n][64]) for hop 0, then the Z_k rows ([n][hi | lo])
-    CUtensorMap tmV, tmZ[2];
-    int st = encode_rows(&tmV, V, p.n, units, kHeadDim);
+int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
+                     const void* K, const void* V, int32_t hops, float alpha, void* out, char* ws,
+                     const BandLayout& L, cudaStream_t stream) {
+    // tensor maps: Q tiles and K chunks (the scores), and the B operand of the
+    // weights' MMA: V ([n][64]) for hop 0, then the Z_k rows ([n][hi | lo])
+    CUtensorMap tmQ, tmK, tmV, tmZ[2];
+    int st = encode_rows(&tmQ, Q, p.n, units, kHeadDim, kTileRows);
+    if (!st) st = encode_rows(&tmK, K, p.n, units, kHeadDim);
+    if (!st) st = encode_rows(&tmV, V, p.n, units, kHeadDim);
     for (int s = 0; s < 2 && !st; ++s) st = encode_rows(&tmZ[s], ws + L.z[s], p.n, units, 2 * kHeadDim);
     if (st) return st;
 
@@ -839,7 +993,6 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     a.A_gimg = reinterpret_cast<const uint8_t*>(ws + L.a_gimg);
     a.inv_l = reinterpret_cast<float*>(ws + L.inv_l);
     a.Psum = reinterpret_cast<float*>(ws + L.psum);
-    a.A_band = reinterpret_cast<const __nv_bfloat16*>(ws + L.a_band);
     a.A_gcimg = reinterpret_cast<const uint8_t*>(ws + L.a_gcimg);
     a.V = static_cast<const __nv_bfloat16*>(V);
     a.gpart = reinterpret_cast<float*>(ws + L.gpart);
@@ -854,10 +1007,10 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
         a.Zk_hilo = first ? nullptr : reinterpret_cast<__nv_bfloat16*>(ws + L.z[(k - 1) & 1]);
         a.Zk_f = first ? nullptr : reinterpret_cast<float*>(ws + L.zf[(k - 1) & 1]);
         const CUtensorMap& tm = first ? tmV : tmZ[(k - 1) & 1];
-        if (first && last) st = launch_hop<true, true>(tm, a, stream);
-        else if (first) st = launch_hop<true, false>(tm, a, stream);
-        else if (last) st = launch_hop<false, true>(tm, a, stream);
-        else st = launch_hop<false, false>(tm, a, stream);
+        if (first && last) st = launch_hop<true, true>(tmQ, tmK, tm, a, stream);
+        else if (first) st = launch_hop<true, false>(tmQ, tmK, tm, a, stream);
+        else if (last) st = launch_hop<false, true>(tmQ, tmK, tm, a, stream);
+        else st = launch_hop<false, false>(tmQ, tmK, tm, a, stream);
         if (st) return st;
     }
     return DIFFUSER_OK;

@@ -7,18 +7,20 @@
 //    128-byte line, 8 dot products reduced across the quarter at once.
 //  * score_band_tc_kernel (tcgen05, persistent): S = Q K^T for a 128-row
 //    tile against 64-key chunks of its window on bf16 tensor cores (fp32
-//    accumulation in TMEM), in two passes over the chunks: the row maximum
-//    m_i, then e = exp(s - m_i) written as the tile's operand image, and the
-//    band part of the row sum.  On the same tensor cores: q_i.k_G for the
-//    globals outside each row's window (N = g16; their e as an operand image)
-//    and q_G.k_j for the global rows against the tile's own keys (raw scores).
+//    accumulation in TMEM): the row maximum m_i.  For the attention-weights
+//    export a second pass writes e = exp(s - m_i) as the tile's operand image
+//    and the band part of the row sum; the forward skips it (its hop kernels
+//    recompute the band weights from Q and K).  On the same tensor cores:
+//    q_i.k_G for the globals outside each row's window (N = g16; their e as an
+//    operand image) and q_G.k_j for the global rows against the tile's own
+//    keys (raw scores).
 //  * score_global_norm_kernel: per global row, its (max, 1/sum) over all keys,
 //    the normalized weights, and its row of each tile's global-row operand
 //    image.
-//  * score_finalize_kernel: a warp per row turns the extras' raw scores into
-//    e = exp(s - m_i) and stores inv_l = 1 / (band + globals + extras sum).
-//    The forward leaves this step to its first hop's gather, which reads the
-//    extras anyway.
+//  * score_finalize_kernel (export only): a warp per row turns the extras' raw
+//    scores into e = exp(s - m_i) and stores inv_l = 1 / (band + globals +
+//    extras sum).  In the forward the first hop does this: its gather kernel
+//    finishes the extras and its band kernel adds the band sum.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -294,6 +296,12 @@ __device__ __forceinline__ void global_row_scores(const ScoreArgs& a, int64_t u,
     }
 }
 
+// kImages: two passes over the chunks (the row maximum, then e = exp(s - m)
+// written as the tile's operand images, and the band part of the row sum).
+// Without: one pass, the row maximum alone (the hop kernels recompute the band
+// weights and the first hop adds up their sum).  The out-of-window globals'
+// weights and the global rows' raw scores are written either way.
+template <bool kImages>
 __global__ void __launch_bounds__(kBThreads, 1)
 score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      ScoreArgs a, int* status) {
@@ -323,7 +331,7 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nc = P.chunks;                              // the tile's key chunks (from i0 - r64)
-    const int per_tile = 2 * nc;                          // pass 1 (max), pass 2 (exp + write)
+    const int per_tile = kImages ? 2 * nc : nc;           // pass 1 (max) [, pass 2 (exp + write)]
     const int64_t total_tiles = a.units * P.tiles;
     const int my_tiles = blockIdx.x < total_tiles
         ? (int)((total_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
@@ -485,33 +493,34 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int trow = (t >> 3) * 1024 + (t & 7) * 128;
             float mraw = -INFINITY;               // max of the raw dot products q.k (unscaled)
             float m = 0.f, b2 = 0.f, lsum = 0.f;
+            // both column halves of a row agree on the row maximum (band, the
+            // out-of-window globals, and the extras from score_sparse_kernel)
+            auto transition = [&]() {
+                xch[rtid] = mraw;
+                ptx::named_barrier_sync(pair_bar, 64);
+                const float other = xch[(rtid + 128) & 255];
+                const float ms = row_ok ? a.w.m_sparse[(size_t)u * P.n + i] : 0.f;
+                m = fmaxf(ms, fmaxf(mraw, other) * kScale);
+                if (has_g) {
+                    float gs[32];
+                    ptx::tmem_ld32(tmem + lane_base + kGcCol0 + 32 * (lt & 1), gs);
+#pragma unroll
+                    for (int sl = 0; sl < kBandMaxGlobals; ++sl) {
+                        if (sl < P.g) {
+                            const int64_t j = sGpos[sl];
+                            if (row_ok && (j < lo || j > hi)) m = fmaxf(m, gs[sl] * kScale);
+                        }
+                    }
+                    if (quad == 0) global_row_scores(a, u, i0, lt, hcol, lane, tmem, full_GR, empty_GR, status);
+                }
+                b2 = m * kLog2e;
+                ptx::named_barrier_sync(pair_bar, 64);     // xch is reused below
+            };
             for (int it = 0; it < per_tile; ++it) {
                 const int gi = lt * per_tile + it;
                 const int b = gi % kSBufs, c = it % nc;
                 const bool pass2 = it >= nc;
-                if (it == nc) {
-                    // both column halves of a row agree on the row maximum (band, the
-                    // out-of-window globals, and the extras from score_sparse_kernel)
-                    xch[rtid] = mraw;
-                    ptx::named_barrier_sync(pair_bar, 64);
-                    const float other = xch[(rtid + 128) & 255];
-                    const float ms = row_ok ? a.w.m_sparse[(size_t)u * P.n + i] : 0.f;
-                    m = fmaxf(ms, fmaxf(mraw, other) * kScale);
-                    if (has_g) {
-                        float gs[32];
-                        ptx::tmem_ld32(tmem + lane_base + kGcCol0 + 32 * (lt & 1), gs);
-#pragma unroll
-                        for (int sl = 0; sl < kBandMaxGlobals; ++sl) {
-                            if (sl < P.g) {
-                                const int64_t j = sGpos[sl];
-                                if (row_ok && (j < lo || j > hi)) m = fmaxf(m, gs[sl] * kScale);
-                            }
-                        }
-                        if (quad == 0) global_row_scores(a, u, i0, lt, hcol, lane, tmem, full_GR, empty_GR, status);
-                    }
-                    b2 = m * kLog2e;
-                    ptx::named_barrier_sync(pair_bar, 64);     // xch is reused below
-                }
+                if (kImages && it == nc) transition();
                 ptx::mbar_wait(&full_S[b], (gi / kSBufs) & 1, status);
                 __syncwarp();
                 ptx::tc_fence_after();
@@ -584,6 +593,7 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     }
                 }
             }
+            if (!kImages) transition();
             if (has_g) {
                 // the out-of-window globals: e = exp(s - m) as the tile's operand image
                 // (this half's slots 8 hcol .. +7 and 16 + 8 hcol .. +7; 0 inside the window)
@@ -626,7 +636,7 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             ptx::named_barrier_sync(pair_bar, 64);     // xch is reused by the next tile
         }
-        if (pair_leader) ptx::bulk_wait<0>();     // the last images are written before exit
+        if (kImages && pair_leader) ptx::bulk_wait<0>();     // the last images are written before exit
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -774,14 +784,16 @@ ScoreArgs make_args(const diffuser_graph* g, const BandPlan& p, int64_t units, c
 }  // namespace
 
 int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
-                       const void* K, char* ws, const BandLayout& L, bool finalize_extras,
+                       const void* K, char* ws, const BandLayout& L, bool weights_out,
                        cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(score_band_tc_kernel,
+        attr_err = cudaFuncSetAttribute(score_band_tc_kernel<true>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmemBytes);
-
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(score_band_tc_kernel<false>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmemBytes);
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(scores)");
     cudaError_t err;
@@ -818,7 +830,10 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
     const unsigned pgrid = grid < (unsigned)num_sms ? grid : (unsigned)num_sms;
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
-        score_band_tc_kernel<<<pgrid, kBThreads, kBSmemBytes, stream>>>(tmQ, tmK, a, g->d_status);
+        if (weights_out)
+            score_band_tc_kernel<true><<<pgrid, kBThreads, kBSmemBytes, stream>>>(tmQ, tmK, a, g->d_status);
+        else
+            score_band_tc_kernel<false><<<pgrid, kBThreads, kBSmemBytes, stream>>>(tmQ, tmK, a, g->d_status);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_band_tc_kernel");
     if (p.g > 0) {
@@ -826,7 +841,7 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
         score_global_norm_kernel<<<(unsigned)(units * p.g), kNormThreads, 0, stream>>>(a);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, "score_global_norm_kernel");
-    if (!finalize_extras) return DIFFUSER_OK;
+    if (!weights_out) return DIFFUSER_OK;
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
         score_finalize_kernel<<<(unsigned)((units * p.n + 7) / 8), 256, 0, stream>>>(a);

@@ -125,15 +125,17 @@ int launch_hop_csr(const CsrArgs& a, const float* A, const void* src, bool src_i
 // ---- band path (band_score.cu, band_hop.cu): token graphs, bf16 I/O --------
 bool band_plan(const diffuser_graph* g, BandPlan* p);   // false: graph not eligible
 int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, BandLayout* L);
-// Scores and weights.  With finalize_extras false the random extras keep their
-// raw scores and inv_l only the band and globals' part of the row sum: the
-// first hop's gather completes both (launch_band_hops must follow).
+// Scores and softmax statistics.  weights_out: also the band weights as tile
+// images and the finished row sums (the attention-weights export).  Without,
+// the forward's state: row maxima, the out-of-window globals' weights and
+// their part of the row sum in inv_l, the extras' raw scores and the global
+// rows' weights; the first hop completes the rest (launch_band_hops follows).
 int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
-                       const void* K, char* ws, const BandLayout& L, bool finalize_extras,
+                       const void* K, char* ws, const BandLayout& L, bool weights_out,
                        cudaStream_t stream);
-int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* V,
-                     int32_t hops, float alpha, void* out, char* ws, const BandLayout& L,
-                     cudaStream_t stream);
+int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
+                     const void* K, const void* V, int32_t hops, float alpha, void* out, char* ws,
+                     const BandLayout& L, cudaStream_t stream);
 int launch_band_to_csr(const diffuser_graph* g, const BandPlan& p, int64_t units, char* ws,
                        const BandLayout& L, float* A_out, cudaStream_t stream);
 
