@@ -14,19 +14,19 @@
 //            the kernel recomputes S = Q_tile K_chunk^T (bf16 operands, fp32 in
 //            TMEM), turns it into e_ij = exp(s_ij - m_i) with the row maxima of
 //            the score pass (0 outside the window), and writes e as bf16 hi + lo
-//            (each the bf16 rounding of what is left) straight into the shared-
-//            memory operand image of the second MMA: e_hi*[Z_hi | Z_lo] (N = 128)
+//            (each the bf16 rounding of what is left) straight into tensor
+//            memory as the A operand of the second MMA: e_hi*[Z_hi | Z_lo] (N = 128)
 //            + e_lo*Z_hi (N = 64), fp32 accumulation in TMEM; the e_lo*Z_lo term
 //            (below 2^-16 of the product) is the only one left out.  Re-reading
 //            the weights from HBM on every hop would cost 4 bytes per edge; the
 //            recomputation costs one exp per edge and a small MMA.  The globals
 //            outside each row's window are one more K step into the same
 //            accumulator (their stored weights' operand image [128 x g16]
-//            against the global keys' Z_k rows, staged by warp 2).  The global
-//            rows (full rows of A) ride along: on the two chunks that hold the
-//            tile's own keys, the same Z_k tiles also multiply the global rows'
-//            weights of those keys (a 32-row operand image) into a second
-//            accumulator, and each tile writes that share.  Epilogue:
+//            against the global keys' Z_k rows).  The global rows (full rows
+//            of A) ride along: on the two chunks that hold the tile's own keys,
+//            the same Z_k tiles also multiply the global rows' weights of those
+//            keys (a 32-row operand image) into a second accumulator, and each
+//            tile writes that share.  Epilogue:
 //            z_i = (1 - alpha) * inv_l_i * (band_i + P_i) + alpha * V_i,
 //            written as the next [hi | lo] bf16 row and fp32 row, or as the
 //            bf16 output.  The first hop also adds up the band part of each
@@ -52,16 +52,19 @@ using band::kChunkKeys;
 using band::kTileRows;
 // warp 0: TMA producer of Q and K, warp 1: score MMAs, warp 2: the weights'
 // MMAs, warp 3: producer of Z_k, the globals' weight images and the global
-// keys' Z_k rows, warps 4-19: the band weights of each chunk and the tile's
-// epilogue (warp w serves TMEM lane quadrant w % 4 and keys / features
-// 16 ((w - 4) / 4) .. +15).  One CTA per SM.
-constexpr int kThreads = 640;
-constexpr int kTmaWarp = 0, kSMmaWarp = 1, kPvMmaWarp = 2, kZWarp = 3, kEpiWarp0 = 4, kEpiThreads = 512;
-constexpr int kEpiWarps = kEpiThreads / 32;
+// keys' Z_k rows, warps 4-19: the band weights of each chunk (warp w serves
+// TMEM lane quadrant w % 4 and keys 16 ((w - 4) / 4) .. +15), warps 20-23: the
+// tiles' epilogues (lane quadrant w % 4, all features).  One CTA per SM.
+constexpr int kThreads = 768;
+constexpr int kTmaWarp = 0, kSMmaWarp = 1, kPvMmaWarp = 2, kZWarp = 3;
+constexpr int kSoftWarp0 = 4, kSoftThreads = 512, kSoftWarps = kSoftThreads / 32;   // band weights
+constexpr int kEpiWarp0 = 20, kEpiWarps = 4;                                      // epilogue
+constexpr int kEpiRowFloats = 68;        // an epilogue staging row (64 features, padded against bank conflicts)
+constexpr int kSlices = kSoftWarps / 4;  // weight warps per TMEM lane quadrant (16 keys each)
 constexpr int kQBytes = kTileRows * kHeadDim * 2;     // a Q tile, bf16 [128][64]
 constexpr int kKBytes = kChunkKeys * kHeadDim * 2;    // a K chunk, bf16 [64][64]
 constexpr int kKStagesMax = 5;           // K ring
-constexpr int kZStagesMax = 6;           // Z ring: hi tile + lo tile, 16 KB per stage (5 when g > 16)
+constexpr int kZStagesMax = 5;           // Z ring: hi tile + lo tile, 16 KB per stage (4 when g > 16)
 constexpr int kPStages = 2;              // weight operands in TMEM (hi, lo: 32 columns each)
 constexpr int kSBufs = 2;                // TMEM score buffers of 64 columns
 // TMEM: the accumulator D in columns [0, 128) ([0,64) P Z_hi, [64,128) P_hi Z_lo)
@@ -84,7 +87,7 @@ __host__ __device__ constexpr int k_stages(int) { return kKStagesMax; }
 __host__ __device__ constexpr int band_smem_bytes(int g16) {
     return 1024 + band::kGImgBytes + 2 * kQBytes + k_stages(g16) * kKBytes + z_stages(g16) * kZStageBytes +
            2 * kTileRows * (g16 > 0 ? g16 : 16) * 2 + 2 * (g16 > 0 ? g16 : 16) * 128 +
-           kEpiThreads * 4 + 512;
+           2 * kSoftThreads * 4 + 4 * 32 * kEpiRowFloats * 4 + 4 * 32 * 4 + 1024;
 }
 constexpr int kSmemBytesMax = band_smem_bytes(16) > band_smem_bytes(kBandMaxGlobals)
                                   ? band_smem_bytes(16) : band_smem_bytes(kBandMaxGlobals);
@@ -147,16 +150,6 @@ __device__ __forceinline__ void split8(const float* z, uint4& hi, uint4& lo) {
     lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-__device__ __forceinline__ uint4 pack8(const float* z) {
-    uint32_t h[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const __nv_bfloat162 hh = __floats2bfloat162_rn(z[2 * p], z[2 * p + 1]);
-        h[p] = *reinterpret_cast<const uint32_t*>(&hh);
-    }
-    return make_uint4(h[0], h[1], h[2], h[3]);
-}
-
 // One float4 (features 4 fq .. 4 fq + 3) of global row s of unit u in the next
 // state: (1 - alpha) * (the tiles' shares sum_j A_gr[s][j] Z[j], added in tile
 // order) + alpha * V, from the shares `gpart` that a band hop kernel wrote;
@@ -165,15 +158,16 @@ template <bool kOut>
 __device__ __forceinline__ void global_row_out(const HopArgs& a, const float* gpart, int64_t u, int s,
                                                int fq, __nv_bfloat16* zhl, float* zf) {
     const BandPlan& P = a.plan;
-    const size_t tstride = (size_t)P.g * (kHeadDim / 4);  // float4s from one tile's shares to the next
-    const float4* src = reinterpret_cast<const float4*>(gpart) + (size_t)u * P.tiles * tstride +
+    const size_t tstride = (size_t)P.g * (kHeadDim / 4);  // float4s from one share to the next
+    const int nshares = P.tiles;                          // one per tile
+    const float4* src = reinterpret_cast<const float4*>(gpart) + (size_t)u * nshares * tstride +
                         (size_t)s * (kHeadDim / 4) + fq;
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t0 = 0; t0 < P.tiles; t0 += 8) {
+    for (int t0 = 0; t0 < nshares; t0 += 8) {
         float4 v[8];
 #pragma unroll
         for (int b = 0; b < 8; ++b)
-            v[b] = t0 + b < P.tiles ? __ldg(src + (size_t)(t0 + b) * tstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[b] = t0 + b < nshares ? __ldg(src + (size_t)(t0 + b) * tstride) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             sum.x += v[b].x; sum.y += v[b].y; sum.z += v[b].z; sum.w += v[b].w;
@@ -239,8 +233,10 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint8_t* sZ = sK + kstages * kKBytes;                        // zstages x (hi 8 KB, lo 8 KB)
     uint8_t* sGC = sZ + zstages * kZStageBytes;                  // out-of-window globals' weights
     uint8_t* sZG = sGC + 2 * kTileRows * g16s * 2;               // Z_k rows of the global keys
-    float* xch = reinterpret_cast<float*>(sZG + 2 * g16s * 128);  // [256] row-sum halves
-    uint64_t* bars = reinterpret_cast<uint64_t*>(xch + kEpiThreads);
+    float* xch = reinterpret_cast<float*>(sZG + 2 * g16s * 128);  // [2][256] row-sum halves
+    float* sEpi = xch + 2 * kSoftThreads;                        // [4][32][68] epilogue staging
+    float* sEpiKeep = sEpi + 4 * 32 * kEpiRowFloats;             // [4][32]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpiKeep + 4 * 32);
     uint64_t* full_Q = bars;                                     // [2]
     uint64_t* empty_Q = full_Q + 2;                              // [2]
     uint64_t* full_K = empty_Q + 2;                              // [kKStagesMax]
@@ -257,7 +253,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint64_t* empty_G = full_G + 1;
     uint64_t* full_GC = empty_G + 1;       // the image by bulk copy + the staged Z rows
     uint64_t* empty_GC = full_GC + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_GC + 1);
+    // first hop: the band sums of a quadrant's rows, from its weight warps to its
+    // epilogue warp, double-buffered by tile parity: [quad][parity]
+    uint64_t* xch_full = empty_GC + 1;                           // [4][2], kSlices arrivals
+    uint64_t* xch_empty = xch_full + 8;                          // [4][2], 1 arrival
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xch_empty + 8);
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -277,14 +277,15 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int s = 0; s < kstages; ++s) { ptx::mbar_init(&full_K[s], 1); ptx::mbar_init(&empty_K[s], 1); }
         for (int s = 0; s < zstages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
         // the weight warps arrive once per warp (lane 0, after the warp has synced)
-        for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], kEpiWarps); }
-        for (int s = 0; s < kPStages; ++s) { ptx::mbar_init(&full_P[s], kEpiWarps); ptx::mbar_init(&empty_P[s], 1); }
+        for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], kSoftWarps); }
+        for (int s = 0; s < kPStages; ++s) { ptx::mbar_init(&full_P[s], kSoftWarps); ptx::mbar_init(&empty_P[s], 1); }
         ptx::mbar_init(acc_full, 1);
         ptx::mbar_init(acc_empty, kEpiWarps);
         ptx::mbar_init(full_G, 1);
         ptx::mbar_init(empty_G, 1);
         ptx::mbar_init(full_GC, 2);
         ptx::mbar_init(empty_GC, 1);
+        for (int s = 0; s < 8; ++s) { ptx::mbar_init(&xch_full[s], kSlices); ptx::mbar_init(&xch_empty[s], 1); }
         ptx::fence_mbar_init();
     }
     if (warp == kTmaWarp && lane == 0) {
@@ -500,172 +501,238 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ptx::mbar_wait(empty_GC, (my_tiles - 1) & 1, a.status);
             }
         }
-    } else if (warp >= kEpiWarp0) {
-        // ---------------- weights and epilogue: thread <-> row t = 32 quad + lane,
-        // keys (of each chunk) and features 16 slice .. +15; the four warps of a
-        // lane quadrant meet on named barrier 2 + quad
+    } else if (warp >= kSoftWarp0 && warp < kEpiWarp0) {
+        // ---------------- band weights: thread <-> row t = 32 quad + lane of the tile,
+        // keys 16 slice .. +15 of each chunk.  The next chunk's scores load from
+        // TMEM while this chunk's weights are computed.
         const int quad = warp & 3;
-        const int slice = (warp - kEpiWarp0) >> 2;        // 0..3
-        const int etid = tid - kEpiWarp0 * 32;            // 0..511
-        const int quad_bar = 2 + quad;
+        const int slice = (warp - kSoftWarp0) >> 2;       // keys 16 slice .. +15 of each chunk
+        const int stid = tid - kSoftWarp0 * 32;           // 0..511
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int t = quad * 32 + lane;
         const float a_sc = kLog2e * kScale;
+        // this row of tile lt: validity, window lo..hi, and b2 = m_i log2(e)
+        struct Row { int64_t jb, lo, hi; size_t urow; bool ok; float b2; };
+        auto row_of = [&](int lt) {
+            Row w;
+            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+            const int64_t u = tix / P.tiles;
+            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+            const int64_t i = i0 + t;
+            w.jb = i0 - P.r64;
+            w.ok = i < P.n && !a.is_global[i < P.n ? i : 0];
+            w.lo = i - P.r < 0 ? 0 : i - P.r;
+            w.hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+            w.urow = (size_t)u * P.n + (w.ok ? i : 0);
+            w.b2 = w.ok ? __ldg(a.m_sparse + w.urow) * kLog2e : 0.f;
+            return w;
+        };
+        auto s_addr = [&](int g) { return tmem + lane_base + kSCol0 + kChunkKeys * (g % kSBufs) + 16 * slice; };
+        uint32_t ra[16], rb[16];
+        if (total > 0) {
+            ptx::mbar_wait(&full_S[0], 0, a.status);
+            __syncwarp();
+            ptx::tc_fence_after();
+            ptx::tmem_ld16_issue(s_addr(0), ra);
+            ptx::tmem_ld_wait16(ra);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty_S[0]);
+        }
+        Row row = my_tiles > 0 ? row_of(0) : Row{};
+        Row next_row = row;
+        float lsum = 0.f;
+        for (int g = 0; g < total; ++g) {
+            const int lt = g / nc, c = g - lt * nc;
+            if (c == 0 && lt > 0) { row = next_row; lsum = 0.f; }
+            if (c == nc - 1 && lt + 1 < my_tiles) next_row = row_of(lt + 1);
+            const bool more = g + 1 < total;
+            if (more) {
+                ptx::mbar_wait(&full_S[(g + 1) % kSBufs], ((g + 1) / kSBufs) & 1, a.status);
+                __syncwarp();
+                ptx::tc_fence_after();
+                ptx::tmem_ld16_issue(s_addr(g + 1), rb);
+            }
+            // e = exp(s - m_i) inside the row's window (keys lo..hi), else 0
+            const int64_t j0 = row.jb + kChunkKeys * c + 16 * slice;
+            const bool full_in = row.ok && j0 >= row.lo && j0 + 15 <= row.hi;
+            const bool none_in = !row.ok || j0 > row.hi || j0 + 15 < row.lo;
+            float e[16];
+            if (none_in) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) e[k] = 0.f;
+            } else if (full_in) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) e[k] = ptx::ex2_approx(fmaf(__uint_as_float(ra[k]), a_sc, -row.b2));
+            } else {
+                const int dlo = (int)(row.lo - j0), dhi = (int)(row.hi - j0);   // in-window keys k in [dlo, dhi]
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    e[k] = (k >= dlo && k <= dhi) ? ptx::ex2_approx(fmaf(__uint_as_float(ra[k]), a_sc, -row.b2)) : 0.f;
+            }
+            if (kHop0) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) lsum += e[k];
+            }
+            // this row's 16 keys of the chunk's weight operand: hi and lo bf16,
+            // two keys per TMEM column
+            uint32_t hw[8], lw[8];
+#pragma unroll
+            for (int p2 = 0; p2 < 8; ++p2) {
+                const float x0 = e[2 * p2], x1 = e[2 * p2 + 1];
+                const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+                hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
+                lw[p2] = *reinterpret_cast<const uint32_t*>(&l);
+            }
+            const int sp = g % kPStages;
+            if (g >= kPStages) ptx::mbar_wait(&empty_P[sp], ((g / kPStages) - 1) & 1, a.status);
+            __syncwarp();       // reconverge before the warp-collective tcgen05.st
+            const uint32_t pcol = tmem + lane_base + kPCol0 + 64 * sp + 8 * slice;
+            ptx::tmem_st8x2(pcol, hw, pcol + 32, lw);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&full_P[sp]);
+            if (kHop0 && c == nc - 1) {
+                // the row's band sum (this slice) for the epilogue warp of the quadrant;
+                // the buffer of this parity is free once that warp has read tile lt - 2's
+                const int xb = quad * 2 + (lt & 1);
+                if (lt >= 2) ptx::mbar_wait(&xch_empty[xb], ((lt / 2) - 1) & 1, a.status);
+                xch[(lt & 1) * kSoftThreads + stid] = lsum;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&xch_full[xb]);
+            }
+            if (more) {
+                ptx::tmem_ld_wait16(rb);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&empty_S[(g + 1) % kSBufs]);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) ra[k] = rb[k];
+            }
+        }
+    } else if (warp >= kEpiWarp0) {
+        // ---------------- epilogue: the warp of lane quadrant q reads rows 32 q .. +31
+        // of the accumulator (thread <-> row), stages them in shared memory, then
+        // walks the rows two at a time with half a warp per row (lane: 4
+        // features) so that every global load and store covers whole lines.
+        const int quad = warp & 3;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int t = quad * 32 + lane;
+        float* st = sEpi + quad * (32 * kEpiRowFloats);                    // [32 rows][68]
+        float* sk = sEpiKeep + quad * 32;                                  // keep of each row (< 0: skip)
+        const int hr = lane >> 4, f4 = lane & 15;                          // row of the pair, feature quad
         for (int lt = 0; lt < my_tiles; ++lt) {
             const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
             const int64_t u = tix / P.tiles;
             const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-            const int64_t jb = i0 - P.r64;
             const int64_t i = i0 + t;
             const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
-            const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
-            const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
             const size_t urow = (size_t)u * P.n + (row_ok ? i : 0);
-            // the row's inputs, fetched while the chunks are processed
-            const size_t vrow = urow * kHeadDim + 16 * slice;
-            const float b2 = row_ok ? __ldg(a.m_sparse + urow) * kLog2e : 0.f;
-            float lsum_in = 0.f;
-            float4 pv[4];
-            uint4 vv[2];
-            if (row_ok) {
-                lsum_in = __ldg(a.inv_l + urow);
-                const float4* pp = reinterpret_cast<const float4*>(a.Psum + vrow);
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) pv[c4] = __ldg(pp + c4);
-#pragma unroll
-                for (int c4 = 0; c4 < 2; ++c4) vv[c4] = __ldg(reinterpret_cast<const uint4*>(a.V + vrow) + c4);
-            }
-            float lsum = 0.f;
-            for (int c = 0; c < nc; ++c) {
-                const int g = lt * nc + c;
-                const int b = g % kSBufs;
-                ptx::mbar_wait(&full_S[b], (g / kSBufs) & 1, a.status);
-                __syncwarp();       // reconverge before the warp-collective tcgen05.ld
-                ptx::tc_fence_after();
-                float sv[16];
-                ptx::tmem_ld16(tmem + lane_base + kSCol0 + kChunkKeys * b + 16 * slice, sv);
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&empty_S[b]);
-                // e = exp(s - m_i) inside the row's window (keys lo..hi), else 0
-                const int64_t j0 = jb + kChunkKeys * c + 16 * slice;
-                const bool full_in = row_ok && j0 >= lo && j0 + 15 <= hi;
-                const bool none_in = !row_ok || j0 > hi || j0 + 15 < lo;
-                float e[16];
-                if (none_in) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) e[k] = 0.f;
-                } else if (full_in) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) e[k] = ptx::ex2_approx(fmaf(sv[k], a_sc, -b2));
-                } else {
-                    const int dlo = (int)(lo - j0), dhi = (int)(hi - j0);   // in-window keys k in [dlo, dhi]
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        e[k] = (k >= dlo && k <= dhi) ? ptx::ex2_approx(fmaf(sv[k], a_sc, -b2)) : 0.f;
-                }
-                if (kHop0) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) lsum += e[k];
-                }
-                // this row's 16 keys of the chunk's weight operand: hi and lo bf16,
-                // two keys per TMEM column (the k-step's 8 columns of this slice)
-                uint32_t hw[8], lw[8];
-#pragma unroll
-                for (int p2 = 0; p2 < 8; ++p2) {
-                    const float x0 = e[2 * p2], x1 = e[2 * p2 + 1];
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-                    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
-                    hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
-                    lw[p2] = *reinterpret_cast<const uint32_t*>(&l);
-                }
-                const int sp = g % kPStages;
-                if (g >= kPStages) ptx::mbar_wait(&empty_P[sp], ((g / kPStages) - 1) & 1, a.status);
-                __syncwarp();       // reconverge before the warp-collective tcgen05.st
-                const uint32_t pcol = tmem + lane_base + kPCol0 + 64 * sp + 8 * slice;
-                ptx::tmem_st8x2(pcol, hw, pcol + 32, lw);
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&full_P[sp]);
-            }
-            // the normalizer: the first hop completes the row sum with the band part
-            // (the four slices' partial sums added in slice order)
-            float inv = row_ok ? lsum_in : 0.f;
+            float inv = row_ok ? __ldg(a.inv_l + urow) : 0.f;
             if (kHop0) {
-                xch[etid] = lsum;
-                ptx::named_barrier_sync(quad_bar, 128);
-                const int r0 = quad * 32 + lane;          // xch[128 s + 32 quad + lane] is slice s
-                const float lband = ((xch[r0] + xch[128 + r0]) + xch[256 + r0]) + xch[384 + r0];
-                ptx::named_barrier_sync(quad_bar, 128);   // xch is reused by the next tile
-                inv = row_ok ? 1.f / (lband + lsum_in) : 0.f;
-                if (slice == 0 && row_ok) a.inv_l[urow] = inv;
+                // the first hop completes the row sum: band halves (from the weight
+                // warps) + the globals' and extras' part already in inv_l
+                const int xb = quad * 2 + (lt & 1);
+                ptx::mbar_wait(&xch_full[xb], (lt / 2) & 1, a.status);
+                const float* xr = xch + (lt & 1) * kSoftThreads + t;        // slice s at xr[128 s]
+                const float lband = ((xr[0] + xr[128]) + xr[256]) + xr[384];
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&xch_empty[xb]);
+                inv = row_ok ? 1.f / (lband + inv) : 0.f;
+                if (row_ok) a.inv_l[urow] = inv;
             }
-            const float keep = (1.f - a.alpha) * inv;
             ptx::mbar_wait(acc_full, lt & 1, a.status);
             __syncwarp();       // reconverge before the warp-collective tcgen05.ld
             ptx::tc_fence_after();
             if (has_g && quad == 0) {
                 // TMEM lanes 0..31 of the global accumulator are the global slots s:
                 // this tile's share of the global rows (summed by global_row_out)
-                float gd[16];
-                ptx::tmem_ld16(tmem + kGlobCol0 + 16 * slice, gd);
-                if (!kHop0) {
-                    float g2[16];
-                    ptx::tmem_ld16(tmem + kGlobCol0 + kHeadDim + 16 * slice, g2);
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) gd[k] += g2[k];
-                }
-                if (lane < P.g) {
-                    float4* gp = reinterpret_cast<float4*>(
-                        a.gpart + (((size_t)u * P.tiles + (i0 / kTileRows)) * P.g + lane) * kHeadDim + 16 * slice);
+                for (int f = 0; f < 4; ++f) {
+                    float gd[16];
+                    ptx::tmem_ld16(tmem + kGlobCol0 + 16 * f, gd);
+                    if (!kHop0) {
+                        float g2[16];
+                        ptx::tmem_ld16(tmem + kGlobCol0 + kHeadDim + 16 * f, g2);
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-                        gp[c4] = make_float4(gd[4 * c4], gd[4 * c4 + 1], gd[4 * c4 + 2], gd[4 * c4 + 3]);
+                        for (int k = 0; k < 16; ++k) gd[k] += g2[k];
+                    }
+                    if (lane < P.g) {
+                        float4* gp = reinterpret_cast<float4*>(
+                            a.gpart + (((size_t)u * P.tiles + (i0 / kTileRows)) * P.g + lane) * kHeadDim + 16 * f);
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4)
+                            gp[c4] = make_float4(gd[4 * c4], gd[4 * c4 + 1], gd[4 * c4 + 2], gd[4 * c4 + 3]);
+                    }
                 }
             }
-            float d[16];
-            ptx::tmem_ld16(tmem + lane_base + 16 * slice, d);
-            if (!kHop0) {
-                float d2[16];
-                ptx::tmem_ld16(tmem + lane_base + kHeadDim + 16 * slice, d2);
+            // the accumulator rows (D[0:64) + D[64:128)) into shared memory
 #pragma unroll
-                for (int k = 0; k < 16; ++k) d[k] += d2[k];
+            for (int h = 0; h < 4; ++h) {
+                float dh[16];
+                ptx::tmem_ld16(tmem + lane_base + 16 * h, dh);
+                if (!kHop0) {
+                    float d2[16];
+                    ptx::tmem_ld16(tmem + lane_base + kHeadDim + 16 * h, d2);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) dh[k] += d2[k];
+                }
+                float4* dst = reinterpret_cast<float4*>(st + lane * kEpiRowFloats + 16 * h);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+                    dst[c4] = make_float4(dh[4 * c4], dh[4 * c4 + 1], dh[4 * c4 + 2], dh[4 * c4 + 3]);
             }
             ptx::tc_fence_before();
+            sk[lane] = row_ok ? (1.f - a.alpha) * inv : -1.f;
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(acc_empty);          // the accumulators are in registers
-            if (row_ok) {
-                float z[16];
+            if (lane == 0) ptx::mbar_arrive(acc_empty);          // the accumulators are read
+            // rows r = 2 it + hr; this lane's features 4 f4 .. +3
+            const size_t ubase = (size_t)u * P.n;
+#pragma unroll 1
+            for (int it0 = 0; it0 < 16; it0 += 4) {
+                float4 pv[4];
+                uint2 vv[4];
+                float keep[4];
+                size_t rr[4];
 #pragma unroll
-                for (int c4 = 0; c4 < 2; ++c4) {
-                    const uint32_t w4[4] = {vv[c4].x, vv[c4].y, vv[c4].z, vv[c4].w};
-                    const float p8[8] = {pv[2 * c4].x, pv[2 * c4].y, pv[2 * c4].z, pv[2 * c4].w,
-                                         pv[2 * c4 + 1].x, pv[2 * c4 + 1].y, pv[2 * c4 + 1].z, pv[2 * c4 + 1].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = 8 * c4 + 2 * e;
-                        z[k] = fmaf(keep, d[k] + p8[2 * e], a.alpha * bf16lo(w4[e]));
-                        z[k + 1] = fmaf(keep, d[k + 1] + p8[2 * e + 1], a.alpha * bf16hi(w4[e]));
+                for (int q = 0; q < 4; ++q) {
+                    const int r = 2 * (it0 + q) + hr;
+                    keep[q] = sk[r];
+                    rr[q] = ubase + (size_t)(i0 + quad * 32 + r);
+                    if (keep[q] >= 0.f) {
+                        pv[q] = __ldg(reinterpret_cast<const float4*>(a.Psum + rr[q] * kHeadDim) + f4);
+                        vv[q] = __ldg(reinterpret_cast<const uint2*>(a.V + rr[q] * kHeadDim) + f4);
                     }
                 }
-                if (kLast) {
-                    uint4* op = reinterpret_cast<uint4*>(a.out + vrow);
 #pragma unroll
-                    for (int c4 = 0; c4 < 2; ++c4) op[c4] = pack8(z + 8 * c4);
-                } else {
-                    __nv_bfloat16* zr = a.Z_out + urow * (2 * kHeadDim) + 16 * slice;
-                    float4* zf = reinterpret_cast<float4*>(a.Zf_out + vrow);
-#pragma unroll
-                    for (int c4 = 0; c4 < 2; ++c4) {
-                        uint4 hi4, lo4;
-                        split8(z + 8 * c4, hi4, lo4);
-                        reinterpret_cast<uint4*>(zr)[c4] = hi4;
-                        reinterpret_cast<uint4*>(zr + kHeadDim)[c4] = lo4;
-                        zf[2 * c4] = make_float4(z[8 * c4], z[8 * c4 + 1], z[8 * c4 + 2], z[8 * c4 + 3]);
-                        zf[2 * c4 + 1] = make_float4(z[8 * c4 + 4], z[8 * c4 + 5], z[8 * c4 + 6], z[8 * c4 + 7]);
+                for (int q = 0; q < 4; ++q) {
+                    if (keep[q] < 0.f) continue;
+                    const int r = 2 * (it0 + q) + hr;
+                    const float4 dv = *reinterpret_cast<const float4*>(st + r * kEpiRowFloats + 4 * f4);
+                    float z[4] = {fmaf(keep[q], dv.x + pv[q].x, a.alpha * bf16lo(vv[q].x)),
+                                  fmaf(keep[q], dv.y + pv[q].y, a.alpha * bf16hi(vv[q].x)),
+                                  fmaf(keep[q], dv.z + pv[q].z, a.alpha * bf16lo(vv[q].y)),
+                                  fmaf(keep[q], dv.w + pv[q].w, a.alpha * bf16hi(vv[q].y))};
+                    const __nv_bfloat162 h0 = __floats2bfloat162_rn(z[0], z[1]);
+                    const __nv_bfloat162 h1 = __floats2bfloat162_rn(z[2], z[3]);
+                    const uint2 hv = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
+                                                *reinterpret_cast<const uint32_t*>(&h1));
+                    if (kLast) {
+                        reinterpret_cast<uint2*>(a.out + rr[q] * kHeadDim)[f4] = hv;
+                    } else {
+                        const __nv_bfloat162 l0 = __floats2bfloat162_rn(z[0] - __low2float(h0), z[1] - __high2float(h0));
+                        const __nv_bfloat162 l1 = __floats2bfloat162_rn(z[2] - __low2float(h1), z[3] - __high2float(h1));
+                        __nv_bfloat16* zr = a.Z_out + rr[q] * (2 * kHeadDim);
+                        reinterpret_cast<uint2*>(zr)[f4] = hv;
+                        reinterpret_cast<uint2*>(zr + kHeadDim)[f4] =
+                            make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
+                        reinterpret_cast<float4*>(a.Zf_out + rr[q] * kHeadDim)[f4] =
+                            make_float4(z[0], z[1], z[2], z[3]);
                     }
                 }
             }
+            __syncwarp();       // the staging rows are rewritten by the next tile
         }
     }
     ptx::tc_fence_before();
