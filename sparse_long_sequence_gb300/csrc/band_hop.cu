@@ -65,12 +65,13 @@ constexpr int kQBytes = kTileRows * kHeadDim * 2;     // a Q tile, bf16 [128][64
 constexpr int kKBytes = kChunkKeys * kHeadDim * 2;    // a K chunk, bf16 [64][64]
 constexpr int kKStagesMax = 5;           // K ring
 constexpr int kZStagesMax = 5;           // Z ring: hi tile + lo tile, 16 KB per stage (4 when g > 16)
-constexpr int kPStages = 2;              // weight operands in TMEM (hi, lo: 32 columns each)
-constexpr int kSBufs = 2;                // TMEM score buffers of 64 columns
+constexpr int kSBufs = 4;                // TMEM buffers of 64 columns: a chunk's scores, then its weights
 // TMEM: the accumulator D in columns [0, 128) ([0,64) P Z_hi, [64,128) P_hi Z_lo)
 constexpr int kGlobCol0 = 128;           // the global rows' accumulator, columns [128, 256)
-constexpr int kSCol0 = 256;              // score buffers, columns 256 + 64 b
-constexpr int kPCol0 = 384;              // weight operands, columns 384 + 64 p (hi; lo 32 on)
+constexpr int kSCol0 = 256;              // score / weight buffers, columns 256 + 64 b
+// In buffer b, keys 16 s .. +15 of the chunk hold fp32 scores in columns 16 s .. +15;
+// the weight warp of slice s overwrites them with the bf16 pairs of its weights,
+// hi in columns 16 s .. +7 and lo in 16 s + 8 .. +15 (the A operand of K step s).
 constexpr int kTmemCols = 512;
 constexpr int kZTileBytes = kChunkKeys * 128;
 constexpr int kZStageBytes = 2 * kZTileBytes;
@@ -243,13 +244,13 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint64_t* empty_K = full_K + kKStagesMax;
     uint64_t* full_Z = empty_K + kKStagesMax;                    // [kZStagesMax]
     uint64_t* empty_Z = full_Z + kZStagesMax;
-    uint64_t* full_S = empty_Z + kZStagesMax;                    // [kSBufs]
-    uint64_t* empty_S = full_S + kSBufs;
-    uint64_t* full_P = empty_S + kSBufs;                         // [kPStages]
-    uint64_t* empty_P = full_P + kPStages;
-    uint64_t* acc_full = empty_P + kPStages;
+    uint64_t* full_S = empty_Z + kZStagesMax;                    // [kSBufs] scores written
+    uint64_t* full_P = full_S + kSBufs;                          // [kSBufs] weights written
+    uint64_t* empty_P = full_P + kSBufs;                         // [kSBufs] weights consumed
+    uint64_t* acc_full = empty_P + kSBufs;
     uint64_t* acc_empty = acc_full + 1;
-    uint64_t* full_G = acc_empty + 1;
+    uint64_t* glob_empty = acc_empty + 1;  // the global rows' accumulator has been read
+    uint64_t* full_G = glob_empty + 1;
     uint64_t* empty_G = full_G + 1;
     uint64_t* full_GC = empty_G + 1;       // the image by bulk copy + the staged Z rows
     uint64_t* empty_GC = full_GC + 1;
@@ -277,10 +278,14 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int s = 0; s < kstages; ++s) { ptx::mbar_init(&full_K[s], 1); ptx::mbar_init(&empty_K[s], 1); }
         for (int s = 0; s < zstages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
         // the weight warps arrive once per warp (lane 0, after the warp has synced)
-        for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], kSoftWarps); }
-        for (int s = 0; s < kPStages; ++s) { ptx::mbar_init(&full_P[s], kSoftWarps); ptx::mbar_init(&empty_P[s], 1); }
+        for (int s = 0; s < kSBufs; ++s) {
+            ptx::mbar_init(&full_S[s], 1);
+            ptx::mbar_init(&full_P[s], kSoftWarps);
+            ptx::mbar_init(&empty_P[s], 1);
+        }
         ptx::mbar_init(acc_full, 1);
         ptx::mbar_init(acc_empty, kEpiWarps);
+        ptx::mbar_init(glob_empty, 1);
         ptx::mbar_init(full_G, 1);
         ptx::mbar_init(empty_G, 1);
         ptx::mbar_init(full_GC, 2);
@@ -391,25 +396,32 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else if (warp == kSMmaWarp) {
         // ---------------- score MMAs: S[b] = Q_tile K_chunk^T (both K-major,
-        // 128-byte swizzle), as far ahead of the weights as the TMEM buffers allow
+        // 128-byte swizzle), as far ahead of the weights as the TMEM buffers allow:
+        // buffer b is free once the weights' MMAs of its previous chunk are done
         if (lane == 0) {
             constexpr uint32_t idesc_s = ptx::mma_idesc(1, kChunkKeys);
+            // descriptors advance by (byte offset >> 4) in their address field
+            const uint64_t qdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sQ));
+            const uint64_t kdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sK));
+            int c = 0, lt = 0, sk = 0, kph = 0, b = 0, bph = 0;   // running chunk, tile, ring slots and phases
             for (int g = 0; g < total; ++g) {
-                const int lt = g / nc, c = g - lt * nc, qb = lt & 1;
-                if (c == 0) ptx::mbar_wait(&full_Q[qb], (lt / 2) & 1, a.status);
-                const int sk = g % kstages, b = g % kSBufs;
-                ptx::mbar_wait(&full_K[sk], (g / kstages) & 1, a.status);
-                if (g >= kSBufs) ptx::mbar_wait(&empty_S[b], ((g / kSBufs) - 1) & 1, a.status);
+                const int qb = lt & 1;
+                if (c == 0) ptx::mbar_wait(&full_Q[qb], (lt >> 1) & 1, a.status);
+                ptx::mbar_wait(&full_K[sk], kph, a.status);
+                if (g >= kSBufs) ptx::mbar_wait(&empty_P[b], bph ^ 1, a.status);
                 ptx::tc_fence_after();
-                const uint32_t qa = ptx::smem_u32(sQ + qb * kQBytes);
-                const uint32_t kb = ptx::smem_u32(sK + sk * kKBytes);
+                const uint64_t qd = qdesc0 + (uint64_t)(qb * (kQBytes >> 4));
+                const uint64_t kd = kdesc0 + (uint64_t)(sk * (kKBytes >> 4));
+                const uint32_t dS = tmem + kSCol0 + kChunkKeys * b;
 #pragma unroll
                 for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                    ptx::mma_bf16_ss(tmem + kSCol0 + kChunkKeys * b, ptx::sw128_kmajor_desc(qa + 32 * ks),
-                                     ptx::sw128_kmajor_desc(kb + 32 * ks), idesc_s, ks > 0);
+                    ptx::mma_bf16_ss(dS, qd + 2 * ks, kd + 2 * ks, idesc_s, ks > 0);
                 ptx::mma_commit(&empty_K[sk]);
                 ptx::mma_commit(&full_S[b]);
                 if (c == nc - 1) ptx::mma_commit(&empty_Q[qb]);
+                if (++sk == kstages) { sk = 0; kph ^= 1; }
+                if (++b == kSBufs) { b = 0; bph ^= 1; }
+                if (++c == nc) { c = 0; ++lt; }
             }
             // Drain: the commits arrive asynchronously when the MMAs finish; wait for
             // the last phase of each so that none lands in shared memory after exit.
@@ -429,8 +441,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             constexpr uint32_t idesc64 = ptx::mma_idesc_bf16_bmn(64);
             constexpr uint32_t idesc128 = ptx::mma_idesc_bf16_bmn(128);
             const uint32_t dacc = tmem;
+            // descriptors advance by (byte offset >> 4) in their address field
+            const uint64_t zdesc0 = ptx::sw128_mnmajor_desc(ptx::smem_u32(sZ), kZTileBytes);
+            const uint64_t gdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sGA));
+            int c = 0, lt = 0, sp = 0, pph = 0, sz = 0, zph = 0;   // running chunk, tile, ring slots and phases
             for (int g = 0; g < total; ++g) {
-                const int lt = g / nc, c = g - lt * nc;
                 if (c == 0) {
                     // the previous tile's accumulators have been read
                     if (lt >= 1) ptx::mbar_wait(acc_empty, (lt - 1) & 1, a.status);
@@ -451,49 +466,52 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         ptx::mma_commit(empty_GC);
                     }
                 }
-                const int sp = g % kPStages, sz = g % zstages;
-                ptx::mbar_wait(&full_P[sp], (g / kPStages) & 1, a.status);
-                ptx::mbar_wait(&full_Z[sz], (g / zstages) & 1, a.status);
+                ptx::mbar_wait(&full_P[sp], pph, a.status);
+                ptx::mbar_wait(&full_Z[sz], zph, a.status);
                 ptx::tc_fence_after();
-                const uint32_t phi = tmem + kPCol0 + 64 * sp;      // 8 columns per 16 keys
-                const uint32_t plo = phi + 32;
-                const uint32_t zb = ptx::smem_u32(sZ + sz * kZStageBytes);
+                const uint32_t pbuf = tmem + kSCol0 + kChunkKeys * sp;   // K step ks: hi 16 ks, lo 16 ks + 8
+                const uint64_t zd = zdesc0 + (uint64_t)(sz * (kZStageBytes >> 4));
 #pragma unroll
                 for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
-                    const uint64_t bdesc = ptx::sw128_mnmajor_desc(zb + 2048 * ks, kZTileBytes);
-                    ptx::mma_bf16_ts(dacc, phi + 8 * ks, bdesc, kHop0 ? idesc64 : idesc128,
+                    const uint64_t bdesc = zd + (uint64_t)(128 * ks);     // 16 keys = 2048 bytes on
+                    ptx::mma_bf16_ts(dacc, pbuf + 16 * ks, bdesc, kHop0 ? idesc64 : idesc128,
                                      has_g || (c | ks) != 0);
-                    ptx::mma_bf16_ts(dacc, plo + 8 * ks, bdesc, idesc64, 1);
+                    ptx::mma_bf16_ts(dacc, pbuf + 16 * ks + 8, bdesc, idesc64, 1);
                 }
                 const int h = c - c0;
                 if (has_g && (h == 0 || h == 1)) {
                     // the global rows x this tile's own keys (same Z_k tile)
                     if (h == 0) {
+                        // the image is in shared memory and the previous tile's
+                        // accumulator has been read
                         ptx::mbar_wait(full_G, lt & 1, a.status);
+                        if (lt >= 1) ptx::mbar_wait(glob_empty, (lt - 1) & 1, a.status);
                         ptx::tc_fence_after();
                     }
                     const uint32_t dglob = tmem + kGlobCol0;
-                    const uint32_t ghi = ptx::smem_u32(sGA + h * 2 * band::kGImgPlaneBytes);
-                    const uint32_t glo = ghi + band::kGImgPlaneBytes;
+                    const uint64_t ghi = gdesc0 + (uint64_t)(h * ((2 * band::kGImgPlaneBytes) >> 4));
+                    const uint64_t glo = ghi + (uint64_t)(band::kGImgPlaneBytes >> 4);
 #pragma unroll
                     for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
-                        const uint64_t bdesc = ptx::sw128_mnmajor_desc(zb + 2048 * ks, kZTileBytes);
-                        ptx::mma_bf16_ss(dglob, ptx::sw128_kmajor_desc(ghi + 32 * ks), bdesc,
-                                         kHop0 ? idesc64 : idesc128, (h | ks) != 0);
-                        ptx::mma_bf16_ss(dglob, ptx::sw128_kmajor_desc(glo + 32 * ks), bdesc, idesc64, 1);
+                        const uint64_t bdesc = zd + (uint64_t)(128 * ks);
+                        ptx::mma_bf16_ss(dglob, ghi + 2 * ks, bdesc, kHop0 ? idesc64 : idesc128, (h | ks) != 0);
+                        ptx::mma_bf16_ss(dglob, glo + 2 * ks, bdesc, idesc64, 1);
                     }
                     if (h == 1) ptx::mma_commit(empty_G);
                 }
                 ptx::mma_commit(&empty_P[sp]);
                 ptx::mma_commit(&empty_Z[sz]);
                 if (c == nc - 1) ptx::mma_commit(acc_full);
+                if (++sp == kSBufs) { sp = 0; pph ^= 1; }
+                if (++sz == zstages) { sz = 0; zph ^= 1; }
+                if (++c == nc) { c = 0; ++lt; }
             }
             for (int s = 0; s < zstages; ++s) {
                 const int uses = (total - s + zstages - 1) / zstages;
                 if (uses > 0) ptx::mbar_wait(&empty_Z[s], (uses - 1) & 1, a.status);
             }
-            for (int s = 0; s < kPStages; ++s) {
-                const int uses = (total - s + kPStages - 1) / kPStages;
+            for (int s = 0; s < kSBufs; ++s) {
+                const int uses = (total - s + kSBufs - 1) / kSBufs;
                 if (uses > 0) ptx::mbar_wait(&empty_P[s], (uses - 1) & 1, a.status);
             }
             if (has_g && my_tiles > 0) {
@@ -527,6 +545,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             w.b2 = w.ok ? __ldg(a.m_sparse + w.urow) * kLog2e : 0.f;
             return w;
         };
+        // this warp's 16 columns of buffer g % kSBufs: the scores, then the weights
         auto s_addr = [&](int g) { return tmem + lane_base + kSCol0 + kChunkKeys * (g % kSBufs) + 16 * slice; };
         uint32_t ra[16], rb[16];
         if (total > 0) {
@@ -535,15 +554,14 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::tc_fence_after();
             ptx::tmem_ld16_issue(s_addr(0), ra);
             ptx::tmem_ld_wait16(ra);
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&empty_S[0]);
         }
         Row row = my_tiles > 0 ? row_of(0) : Row{};
         Row next_row = row;
         float lsum = 0.f;
+        int lt_run = 0, c_run = 0;
         for (int g = 0; g < total; ++g) {
-            const int lt = g / nc, c = g - lt * nc;
+            const int lt = lt_run, c = c_run;
+            if (++c_run == nc) { c_run = 0; ++lt_run; }
             if (c == 0 && lt > 0) { row = next_row; lsum = 0.f; }
             if (c == nc - 1 && lt + 1 < my_tiles) next_row = row_of(lt + 1);
             const bool more = g + 1 < total;
@@ -585,14 +603,13 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
                 lw[p2] = *reinterpret_cast<const uint32_t*>(&l);
             }
-            const int sp = g % kPStages;
-            if (g >= kPStages) ptx::mbar_wait(&empty_P[sp], ((g / kPStages) - 1) & 1, a.status);
+            // over this warp's own scores of the chunk (already in registers)
             __syncwarp();       // reconverge before the warp-collective tcgen05.st
-            const uint32_t pcol = tmem + lane_base + kPCol0 + 64 * sp + 8 * slice;
-            ptx::tmem_st8x2(pcol, hw, pcol + 32, lw);
+            const uint32_t pcol = s_addr(g);
+            ptx::tmem_st8x2(pcol, hw, pcol + 8, lw);
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&full_P[sp]);
+            if (lane == 0) ptx::mbar_arrive(&full_P[g % kSBufs]);
             if (kHop0 && c == nc - 1) {
                 // the row's band sum (this slice) for the epilogue warp of the quadrant;
                 // the buffer of this parity is free once that warp has read tile lt - 2's
@@ -604,9 +621,6 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             if (more) {
                 ptx::tmem_ld_wait16(rb);
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&empty_S[(g + 1) % kSBufs]);
 #pragma unroll
                 for (int k = 0; k < 16; ++k) ra[k] = rb[k];
             }
@@ -645,48 +659,62 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::mbar_wait(acc_full, lt & 1, a.status);
             __syncwarp();       // reconverge before the warp-collective tcgen05.ld
             ptx::tc_fence_after();
-            if (has_g && quad == 0) {
-                // TMEM lanes 0..31 of the global accumulator are the global slots s:
-                // this tile's share of the global rows (summed by global_row_out)
+            // the accumulator rows (D[0:64) + D[64:128)) into shared memory, two
+            // loads in flight per wait
 #pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    float gd[16];
-                    ptx::tmem_ld16(tmem + kGlobCol0 + 16 * f, gd);
-                    if (!kHop0) {
-                        float g2[16];
-                        ptx::tmem_ld16(tmem + kGlobCol0 + kHeadDim + 16 * f, g2);
+            for (int h = 0; h < 4; h += (kHop0 ? 2 : 1)) {
+                uint32_t dr[32];
+                if (kHop0) ptx::tmem_ld32_issue(tmem + lane_base + 16 * h, dr);
+                else ptx::tmem_ld16x2_issue(tmem + lane_base + 16 * h, tmem + lane_base + kHeadDim + 16 * h, dr);
+                ptx::tmem_ld_wait32(dr);
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) gd[k] += g2[k];
-                    }
-                    if (lane < P.g) {
-                        float4* gp = reinterpret_cast<float4*>(
-                            a.gpart + (((size_t)u * P.tiles + (i0 / kTileRows)) * P.g + lane) * kHeadDim + 16 * f);
+                for (int hh = 0; hh < (kHop0 ? 2 : 1); ++hh) {
+                    float dh[16];
 #pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4)
-                            gp[c4] = make_float4(gd[4 * c4], gd[4 * c4 + 1], gd[4 * c4 + 2], gd[4 * c4 + 3]);
-                    }
+                    for (int k = 0; k < 16; ++k)
+                        dh[k] = kHop0 ? __uint_as_float(dr[16 * hh + k])
+                                      : __uint_as_float(dr[k]) + __uint_as_float(dr[16 + k]);
+                    float4* dst = reinterpret_cast<float4*>(st + lane * kEpiRowFloats + 16 * (h + hh));
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        dst[c4] = make_float4(dh[4 * c4], dh[4 * c4 + 1], dh[4 * c4 + 2], dh[4 * c4 + 3]);
                 }
-            }
-            // the accumulator rows (D[0:64) + D[64:128)) into shared memory
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                float dh[16];
-                ptx::tmem_ld16(tmem + lane_base + 16 * h, dh);
-                if (!kHop0) {
-                    float d2[16];
-                    ptx::tmem_ld16(tmem + lane_base + kHeadDim + 16 * h, d2);
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) dh[k] += d2[k];
-                }
-                float4* dst = reinterpret_cast<float4*>(st + lane * kEpiRowFloats + 16 * h);
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-                    dst[c4] = make_float4(dh[4 * c4], dh[4 * c4 + 1], dh[4 * c4 + 2], dh[4 * c4 + 3]);
             }
             ptx::tc_fence_before();
             sk[lane] = row_ok ? (1.f - a.alpha) * inv : -1.f;
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(acc_empty);          // the accumulators are read
+            if (lane == 0) ptx::mbar_arrive(acc_empty);          // the accumulator D is read
+            if (has_g && quad == 0) {
+                // TMEM lanes 0..31 of the global accumulator are the global slots s:
+                // this tile's share of the global rows (summed by global_row_out)
+#pragma unroll
+                for (int f = 0; f < 4; f += (kHop0 ? 2 : 1)) {
+                    uint32_t gr[32];
+                    if (kHop0) ptx::tmem_ld32_issue(tmem + kGlobCol0 + 16 * f, gr);
+                    else ptx::tmem_ld16x2_issue(tmem + kGlobCol0 + 16 * f, tmem + kGlobCol0 + kHeadDim + 16 * f, gr);
+                    ptx::tmem_ld_wait32(gr);
+                    if (lane < P.g) {
+#pragma unroll
+                        for (int ff = 0; ff < (kHop0 ? 2 : 1); ++ff) {
+                            float4* gp = reinterpret_cast<float4*>(
+                                a.gpart + (((size_t)u * P.tiles + (i0 / kTileRows)) * P.g + lane) * kHeadDim +
+                                16 * (f + ff));
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4) {
+                                float v[4];
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    v[k] = kHop0 ? __uint_as_float(gr[16 * ff + 4 * c4 + k])
+                                                 : __uint_as_float(gr[4 * c4 + k]) + __uint_as_float(gr[16 + 4 * c4 + k]);
+                                gp[c4] = make_float4(v[0], v[1], v[2], v[3]);
+                            }
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(glob_empty);
+            }
             // rows r = 2 it + hr; this lane's features 4 f4 .. +3
             const size_t ubase = (size_t)u * P.n;
 #pragma unroll 1
