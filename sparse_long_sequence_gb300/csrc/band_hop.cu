@@ -63,9 +63,12 @@ constexpr int kEpiRowFloats = 68;        // an epilogue staging row (64 features
 constexpr int kSlices = kSoftWarps / 4;  // weight warps per TMEM lane quadrant (16 keys each)
 constexpr int kQBytes = kTileRows * kHeadDim * 2;     // a Q tile, bf16 [128][64]
 constexpr int kKBytes = kChunkKeys * kHeadDim * 2;    // a K chunk, bf16 [64][64]
-constexpr int kKStagesMax = 5;           // K ring
-constexpr int kZStagesMax = 5;           // Z ring: hi tile + lo tile, 16 KB per stage (4 when g > 16)
 constexpr int kSBufs = 4;                // TMEM buffers of 64 columns: a chunk's scores, then its weights
+// Chunk g uses slot b = g % kSBufs of everything: its K stage (8 KB), its score /
+// weight buffer and its Z stage (hi tile + lo tile, 16 KB), so that one barrier
+// per slot and event does: full_K (K landed), full_S (scores written, K read),
+// full_P (weights written by the 16 weight warps and Z landed), pv_done (the
+// weights' MMAs are done: buffer and Z stage free).
 // TMEM: the accumulator D in columns [0, 128) ([0,64) P Z_hi, [64,128) P_hi Z_lo)
 constexpr int kGlobCol0 = 128;           // the global rows' accumulator, columns [128, 256)
 constexpr int kSCol0 = 256;              // score / weight buffers, columns 256 + 64 b
@@ -82,11 +85,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // follows; those rows are not used).  Then 2 Q tiles, the K, Z and weight-image
 // rings, the out-of-window globals' weight image (hi, lo; g16 slots) and their
 // Z_k rows as an MN-major B tile (hi, lo), the row-sum exchange, barriers.
-// The Z ring gets 4 stages when the globals' tiles are small (g16 <= 16), else 3.
-__host__ __device__ constexpr int z_stages(int g16) { return g16 > 16 ? kZStagesMax - 1 : kZStagesMax; }
-__host__ __device__ constexpr int k_stages(int) { return kKStagesMax; }
 __host__ __device__ constexpr int band_smem_bytes(int g16) {
-    return 1024 + band::kGImgBytes + 2 * kQBytes + k_stages(g16) * kKBytes + z_stages(g16) * kZStageBytes +
+    return 1024 + band::kGImgBytes + 2 * kQBytes + kSBufs * (kKBytes + kZStageBytes) +
            2 * kTileRows * (g16 > 0 ? g16 : 16) * 2 + 2 * (g16 > 0 ? g16 : 16) * 128 +
            2 * kSoftThreads * 4 + 4 * 32 * kEpiRowFloats * 4 + 4 * 32 * 4 + 1024;
 }
@@ -227,12 +227,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     const int g16 = a.plan.g16, g16s = g16 > 0 ? g16 : 16;
-    const int zstages = z_stages(g16), kstages = k_stages(g16);
     uint8_t* sGA = smem;                                         // global rows: 2 halves x (hi, lo) 4 KB
     uint8_t* sQ = sGA + band::kGImgBytes;                        // 2 x 16 KB
-    uint8_t* sK = sQ + 2 * kQBytes;                              // kstages x 8 KB
-    uint8_t* sZ = sK + kstages * kKBytes;                        // zstages x (hi 8 KB, lo 8 KB)
-    uint8_t* sGC = sZ + zstages * kZStageBytes;                  // out-of-window globals' weights
+    uint8_t* sK = sQ + 2 * kQBytes;                              // kSBufs x 8 KB
+    uint8_t* sZ = sK + kSBufs * kKBytes;                         // kSBufs x (hi 8 KB, lo 8 KB)
+    uint8_t* sGC = sZ + kSBufs * kZStageBytes;                   // out-of-window globals' weights
     uint8_t* sZG = sGC + 2 * kTileRows * g16s * 2;               // Z_k rows of the global keys
     float* xch = reinterpret_cast<float*>(sZG + 2 * g16s * 128);  // [2][256] row-sum halves
     float* sEpi = xch + 2 * kSoftThreads;                        // [4][32][68] epilogue staging
@@ -240,14 +239,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint64_t* bars = reinterpret_cast<uint64_t*>(sEpiKeep + 4 * 32);
     uint64_t* full_Q = bars;                                     // [2]
     uint64_t* empty_Q = full_Q + 2;                              // [2]
-    uint64_t* full_K = empty_Q + 2;                              // [kKStagesMax]
-    uint64_t* empty_K = full_K + kKStagesMax;
-    uint64_t* full_Z = empty_K + kKStagesMax;                    // [kZStagesMax]
-    uint64_t* empty_Z = full_Z + kZStagesMax;
-    uint64_t* full_S = empty_Z + kZStagesMax;                    // [kSBufs] scores written
-    uint64_t* full_P = full_S + kSBufs;                          // [kSBufs] weights written
-    uint64_t* empty_P = full_P + kSBufs;                         // [kSBufs] weights consumed
-    uint64_t* acc_full = empty_P + kSBufs;
+    uint64_t* full_K = empty_Q + 2;                              // [kSBufs]
+    uint64_t* full_S = full_K + kSBufs;                          // [kSBufs]
+    uint64_t* full_P = full_S + kSBufs;                          // [kSBufs]
+    uint64_t* pv_done = full_P + kSBufs;                         // [kSBufs]
+    uint64_t* acc_full = pv_done + kSBufs;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* glob_empty = acc_empty + 1;  // the global rows' accumulator has been read
     uint64_t* full_G = glob_empty + 1;
@@ -275,13 +271,12 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (warp == kSMmaWarp) ptx::tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) { ptx::mbar_init(&full_Q[s], 1); ptx::mbar_init(&empty_Q[s], 1); }
-        for (int s = 0; s < kstages; ++s) { ptx::mbar_init(&full_K[s], 1); ptx::mbar_init(&empty_K[s], 1); }
-        for (int s = 0; s < zstages; ++s) { ptx::mbar_init(&full_Z[s], 1); ptx::mbar_init(&empty_Z[s], 1); }
         // the weight warps arrive once per warp (lane 0, after the warp has synced)
         for (int s = 0; s < kSBufs; ++s) {
+            ptx::mbar_init(&full_K[s], 1);
             ptx::mbar_init(&full_S[s], 1);
-            ptx::mbar_init(&full_P[s], kSoftWarps);
-            ptx::mbar_init(&empty_P[s], 1);
+            ptx::mbar_init(&full_P[s], kSoftWarps + 1);          // + the Z producer's arrival (with its bytes)
+            ptx::mbar_init(&pv_done[s], 1);
         }
         ptx::mbar_init(acc_full, 1);
         ptx::mbar_init(acc_empty, kEpiWarps);
@@ -309,21 +304,25 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // as zeros), in the order the score MMAs use them.
         if (lane == 0) {
             const uint64_t pol_keep = ptx::l2_evict_last();      // re-read by neighbouring tiles
+            int c = 0, lt = 0, b = 0, ph = 0;                     // running chunk, tile, slot, phase
+            int64_t u = 0, i0 = 0;
             for (int g = 0; g < total; ++g) {
-                const int lt = g / nc, c = g - lt * nc, qb = lt & 1;
-                const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
-                const int64_t u = tix / P.tiles;
-                const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+                const int qb = lt & 1;
                 if (c == 0) {
+                    const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+                    u = tix / P.tiles;
+                    i0 = (tix - u * P.tiles) * kTileRows;
                     if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, a.status);
                     ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
                     ptx::tma_load_3d_hint(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, (int)i0, (int)u, pol_keep);
                 }
-                const int sk = g % kstages;
-                if (g >= kstages) ptx::mbar_wait(&empty_K[sk], ((g / kstages) - 1) & 1, a.status);
-                ptx::mbar_arrive_expect_tx(&full_K[sk], kKBytes);
-                ptx::tma_load_3d_hint(sK + sk * kKBytes, &tmK, &full_K[sk], 0,
+                // stage b is free once the scores of chunk g - kSBufs are written
+                if (g >= kSBufs) ptx::mbar_wait(&full_S[b], ph ^ 1, a.status);
+                ptx::mbar_arrive_expect_tx(&full_K[b], kKBytes);
+                ptx::tma_load_3d_hint(sK + b * kKBytes, &tmK, &full_K[b], 0,
                                       (int)(i0 - P.r64 + kChunkKeys * c), (int)u, pol_keep);
+                if (++b == kSBufs) { b = 0; ph ^= 1; }
+                if (++c == nc) { c = 0; ++lt; }
             }
         }
     } else if (warp == kZWarp) {
@@ -383,14 +382,16 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
             }
             const int key = (int)(i0 - P.r64 + kChunkKeys * c);
-            const int sz = g % zstages;
-            if (g >= zstages) ptx::mbar_wait(&empty_Z[sz], ((g / zstages) - 1) & 1, a.status);
+            const int b = g % kSBufs;
+            // stage b is free once the weights' MMAs of chunk g - kSBufs are done; the
+            // copy completes on the chunk's full_P barrier
+            if (g >= kSBufs) ptx::mbar_wait(&pv_done[b], ((g / kSBufs) - 1) & 1, a.status);
             if (lane == 0) {
-                uint8_t* zdst = sZ + sz * kZStageBytes;
-                ptx::mbar_arrive_expect_tx(&full_Z[sz], kHop0 ? kZTileBytes : 2 * kZTileBytes);
-                ptx::tma_load_3d_hint(zdst, &tmZ, &full_Z[sz], 0, key, (int)u, pol_keep);
+                uint8_t* zdst = sZ + b * kZStageBytes;
+                ptx::mbar_arrive_expect_tx(&full_P[b], kHop0 ? kZTileBytes : 2 * kZTileBytes);
+                ptx::tma_load_3d_hint(zdst, &tmZ, &full_P[b], 0, key, (int)u, pol_keep);
                 if (!kHop0)
-                    ptx::tma_load_3d_hint(zdst + kZTileBytes, &tmZ, &full_Z[sz], kHeadDim, key, (int)u, pol_keep);
+                    ptx::tma_load_3d_hint(zdst + kZTileBytes, &tmZ, &full_P[b], kHeadDim, key, (int)u, pol_keep);
             }
             __syncwarp();
         }
@@ -403,31 +404,29 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // descriptors advance by (byte offset >> 4) in their address field
             const uint64_t qdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sQ));
             const uint64_t kdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sK));
-            int c = 0, lt = 0, sk = 0, kph = 0, b = 0, bph = 0;   // running chunk, tile, ring slots and phases
+            int c = 0, lt = 0, b = 0, ph = 0;                     // running chunk, tile, slot, phase
             for (int g = 0; g < total; ++g) {
                 const int qb = lt & 1;
                 if (c == 0) ptx::mbar_wait(&full_Q[qb], (lt >> 1) & 1, a.status);
-                ptx::mbar_wait(&full_K[sk], kph, a.status);
-                if (g >= kSBufs) ptx::mbar_wait(&empty_P[b], bph ^ 1, a.status);
+                ptx::mbar_wait(&full_K[b], ph, a.status);
+                if (g >= kSBufs) ptx::mbar_wait(&pv_done[b], ph ^ 1, a.status);
                 ptx::tc_fence_after();
                 const uint64_t qd = qdesc0 + (uint64_t)(qb * (kQBytes >> 4));
-                const uint64_t kd = kdesc0 + (uint64_t)(sk * (kKBytes >> 4));
+                const uint64_t kd = kdesc0 + (uint64_t)(b * (kKBytes >> 4));
                 const uint32_t dS = tmem + kSCol0 + kChunkKeys * b;
 #pragma unroll
                 for (int ks = 0; ks < kHeadDim / 16; ++ks)
                     ptx::mma_bf16_ss(dS, qd + 2 * ks, kd + 2 * ks, idesc_s, ks > 0);
-                ptx::mma_commit(&empty_K[sk]);
-                ptx::mma_commit(&full_S[b]);
+                ptx::mma_commit(&full_S[b]);                      // also frees K stage b
                 if (c == nc - 1) ptx::mma_commit(&empty_Q[qb]);
-                if (++sk == kstages) { sk = 0; kph ^= 1; }
-                if (++b == kSBufs) { b = 0; bph ^= 1; }
+                if (++b == kSBufs) { b = 0; ph ^= 1; }
                 if (++c == nc) { c = 0; ++lt; }
             }
             // Drain: the commits arrive asynchronously when the MMAs finish; wait for
             // the last phase of each so that none lands in shared memory after exit.
-            for (int s = 0; s < kstages; ++s) {
-                const int uses = (total - s + kstages - 1) / kstages;
-                if (uses > 0) ptx::mbar_wait(&empty_K[s], (uses - 1) & 1, a.status);
+            for (int s = 0; s < kSBufs; ++s) {
+                const int uses = (total - s + kSBufs - 1) / kSBufs;
+                if (uses > 0) ptx::mbar_wait(&full_S[s], (uses - 1) & 1, a.status);
             }
             for (int s = 0; s < 2; ++s) {
                 const int uses = (my_tiles - s + 1) / 2;
@@ -444,7 +443,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // descriptors advance by (byte offset >> 4) in their address field
             const uint64_t zdesc0 = ptx::sw128_mnmajor_desc(ptx::smem_u32(sZ), kZTileBytes);
             const uint64_t gdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sGA));
-            int c = 0, lt = 0, sp = 0, pph = 0, sz = 0, zph = 0;   // running chunk, tile, ring slots and phases
+            int c = 0, lt = 0, sp = 0, pph = 0;                   // running chunk, tile, slot, phase
             for (int g = 0; g < total; ++g) {
                 if (c == 0) {
                     // the previous tile's accumulators have been read
@@ -466,11 +465,10 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         ptx::mma_commit(empty_GC);
                     }
                 }
-                ptx::mbar_wait(&full_P[sp], pph, a.status);
-                ptx::mbar_wait(&full_Z[sz], zph, a.status);
+                ptx::mbar_wait(&full_P[sp], pph, a.status);          // weights and Z stage
                 ptx::tc_fence_after();
                 const uint32_t pbuf = tmem + kSCol0 + kChunkKeys * sp;   // K step ks: hi 16 ks, lo 16 ks + 8
-                const uint64_t zd = zdesc0 + (uint64_t)(sz * (kZStageBytes >> 4));
+                const uint64_t zd = zdesc0 + (uint64_t)(sp * (kZStageBytes >> 4));
 #pragma unroll
                 for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
                     const uint64_t bdesc = zd + (uint64_t)(128 * ks);     // 16 keys = 2048 bytes on
@@ -499,20 +497,14 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                     if (h == 1) ptx::mma_commit(empty_G);
                 }
-                ptx::mma_commit(&empty_P[sp]);
-                ptx::mma_commit(&empty_Z[sz]);
+                ptx::mma_commit(&pv_done[sp]);
                 if (c == nc - 1) ptx::mma_commit(acc_full);
                 if (++sp == kSBufs) { sp = 0; pph ^= 1; }
-                if (++sz == zstages) { sz = 0; zph ^= 1; }
                 if (++c == nc) { c = 0; ++lt; }
-            }
-            for (int s = 0; s < zstages; ++s) {
-                const int uses = (total - s + zstages - 1) / zstages;
-                if (uses > 0) ptx::mbar_wait(&empty_Z[s], (uses - 1) & 1, a.status);
             }
             for (int s = 0; s < kSBufs; ++s) {
                 const int uses = (total - s + kSBufs - 1) / kSBufs;
-                if (uses > 0) ptx::mbar_wait(&empty_P[s], (uses - 1) & 1, a.status);
+                if (uses > 0) ptx::mbar_wait(&pv_done[s], (uses - 1) & 1, a.status);
             }
             if (has_g && my_tiles > 0) {
                 ptx::mbar_wait(empty_G, (my_tiles - 1) & 1, a.status);
@@ -606,7 +598,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // over this warp's own scores of the chunk (already in registers)
             __syncwarp();       // reconverge before the warp-collective tcgen05.st
             const uint32_t pcol = s_addr(g);
-            ptx::tmem_st8x2(pcol, hw, pcol + 8, lw);
+            ptx::tmem_st16_hilo(pcol, hw, lw);     // hi in columns +0..7, lo in +8..15
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&full_P[g % kSBufs]);

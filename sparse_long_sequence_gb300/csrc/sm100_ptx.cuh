@@ -365,6 +365,17 @@ __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]) : : "memory");
 }
 
+// One 16-column store of this warp's lanes (thread i -> lane i): a[0..7] into
+// columns taddr .. +7, b[0..7] into taddr + 8 .. +15, then the wait.
+__device__ __forceinline__ void tmem_st16_hilo(uint32_t taddr, const uint32_t (&a)[8], const uint32_t (&b)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+        "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7])
+        : "memory");
+}
+
 // Two 16-column stores of this warp's lanes (thread i -> lane i), then one wait.
 __device__ __forceinline__ void tmem_st16x2(uint32_t taddr_a, const uint32_t (&a)[16], uint32_t taddr_b,
                                             const uint32_t (&b)[16]) {
