@@ -62,21 +62,22 @@ constexpr int kEpiWarp0 = 20, kEpiWarps = 4;                                    
 constexpr int kEpiRowFloats = 68;        // an epilogue staging row (64 features, padded against bank conflicts)
 constexpr int kSlices = kSoftWarps / 4;  // weight warps per TMEM lane quadrant (16 keys each)
 constexpr int kQBytes = kTileRows * kHeadDim * 2;     // a Q tile, bf16 [128][64]
-constexpr int kKBytes = kChunkKeys * kHeadDim * 2;    // a K chunk, bf16 [64][64]
-constexpr int kSBufs = 4;                // TMEM buffers of 64 columns: a chunk's scores, then its weights
-// Chunk g uses slot b = g % kSBufs of everything: its K stage (8 KB), its score /
-// weight buffer and its Z stage (hi tile + lo tile, 16 KB), so that one barrier
-// per slot and event does: full_K (K landed), full_S (scores written, K read),
-// full_P (weights written by the 16 weight warps and Z landed), pv_done (the
-// weights' MMAs are done: buffer and Z stage free).
+constexpr int kCK = 2 * kChunkKeys;    // keys per pipeline chunk (two 64-key halves of the key grid)
+constexpr int kKBytes = kCK * kHeadDim * 2;           // a K chunk, bf16 [128][64]
+constexpr int kSBufs = 2;                // pipeline slots (chunk g uses slot g % 2)
+// Chunk g uses slot b = g % kSBufs of everything: its K stage (16 KB), its score /
+// weight buffer (128 TMEM columns) and its Z stage (hi tile + lo tile, 32 KB),
+// with one barrier per slot and event: full_K (K landed), full_S (scores
+// written, K read), full_P (weights written by the 16 weight warps and Z
+// landed), pv_done (the weights' MMAs are done: buffer and Z stage free).
 // TMEM: the accumulator D in columns [0, 128) ([0,64) P Z_hi, [64,128) P_hi Z_lo)
 constexpr int kGlobCol0 = 128;           // the global rows' accumulator, columns [128, 256)
-constexpr int kSCol0 = 256;              // score / weight buffers, columns 256 + 64 b
+constexpr int kSCol0 = 256;              // score / weight buffers, columns 256 + 128 b
 // In buffer b, keys 16 s .. +15 of the chunk hold fp32 scores in columns 16 s .. +15;
-// the weight warp of slice s overwrites them with the bf16 pairs of its weights,
+// the weight warp of those keys overwrites them with the bf16 pairs of its weights,
 // hi in columns 16 s .. +7 and lo in 16 s + 8 .. +15 (the A operand of K step s).
 constexpr int kTmemCols = 512;
-constexpr int kZTileBytes = kChunkKeys * 128;
+constexpr int kZTileBytes = kCK * 128;   // a chunk's Z_k rows, one 64-feature half (hi or lo)
 constexpr int kZStageBytes = 2 * kZTileBytes;
 constexpr float kScale = 0.125f;         // 1/sqrt(64)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -229,8 +230,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int g16 = a.plan.g16, g16s = g16 > 0 ? g16 : 16;
     uint8_t* sGA = smem;                                         // global rows: 2 halves x (hi, lo) 4 KB
     uint8_t* sQ = sGA + band::kGImgBytes;                        // 2 x 16 KB
-    uint8_t* sK = sQ + 2 * kQBytes;                              // kSBufs x 8 KB
-    uint8_t* sZ = sK + kSBufs * kKBytes;                         // kSBufs x (hi 8 KB, lo 8 KB)
+    uint8_t* sK = sQ + 2 * kQBytes;                              // kSBufs x 16 KB
+    uint8_t* sZ = sK + kSBufs * kKBytes;                         // kSBufs x (hi 16 KB, lo 16 KB)
     uint8_t* sGC = sZ + kSBufs * kZStageBytes;                   // out-of-window globals' weights
     uint8_t* sZG = sGC + 2 * kTileRows * g16s * 2;               // Z_k rows of the global keys
     float* xch = reinterpret_cast<float*>(sZG + 2 * g16s * 128);  // [2][256] row-sum halves
@@ -258,8 +259,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nc = P.chunks;
-    const int c0 = P.r64 / kChunkKeys;           // chunks c0 and c0 + 1 hold the tile's own keys
+    const int nc = P.chunks / 2;                 // 128-key chunks of a tile (the key grid has an even count)
+    const int c0 = P.r64 / kCK;                  // the chunk of the tile's first own key
     const bool has_g = P.g > 0;
     const int gc_plane = band::gc_plane_bytes(g16);
     const int64_t total_tiles = a.units * P.tiles;
@@ -320,7 +321,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (g >= kSBufs) ptx::mbar_wait(&full_S[b], ph ^ 1, a.status);
                 ptx::mbar_arrive_expect_tx(&full_K[b], kKBytes);
                 ptx::tma_load_3d_hint(sK + b * kKBytes, &tmK, &full_K[b], 0,
-                                      (int)(i0 - P.r64 + kChunkKeys * c), (int)u, pol_keep);
+                                      (int)(i0 - P.r64 + kCK * c), (int)u, pol_keep);
                 if (++b == kSBufs) { b = 0; ph ^= 1; }
                 if (++c == nc) { c = 0; ++lt; }
             }
@@ -374,6 +375,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (lane == 0) ptx::mbar_arrive(full_GC);
             }
             if (has_g && c == c0) {
+                // the global rows' image of this tile's keys (used from this chunk on)
                 if (lt >= 1) ptx::mbar_wait(empty_G, (lt - 1) & 1, a.status);
                 if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(full_G, band::kGImgBytes);
@@ -381,7 +383,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                         full_G, pol_once);
                 }
             }
-            const int key = (int)(i0 - P.r64 + kChunkKeys * c);
+            const int key = (int)(i0 - P.r64 + kCK * c);
             const int b = g % kSBufs;
             // stage b is free once the weights' MMAs of chunk g - kSBufs are done; the
             // copy completes on the chunk's full_P barrier
@@ -400,7 +402,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // 128-byte swizzle), as far ahead of the weights as the TMEM buffers allow:
         // buffer b is free once the weights' MMAs of its previous chunk are done
         if (lane == 0) {
-            constexpr uint32_t idesc_s = ptx::mma_idesc(1, kChunkKeys);
+            constexpr uint32_t idesc_s = ptx::mma_idesc(1, kCK);
             // descriptors advance by (byte offset >> 4) in their address field
             const uint64_t qdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sQ));
             const uint64_t kdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sK));
@@ -413,7 +415,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ptx::tc_fence_after();
                 const uint64_t qd = qdesc0 + (uint64_t)(qb * (kQBytes >> 4));
                 const uint64_t kd = kdesc0 + (uint64_t)(b * (kKBytes >> 4));
-                const uint32_t dS = tmem + kSCol0 + kChunkKeys * b;
+                const uint32_t dS = tmem + kSCol0 + kCK * b;
 #pragma unroll
                 for (int ks = 0; ks < kHeadDim / 16; ++ks)
                     ptx::mma_bf16_ss(dS, qd + 2 * ks, kd + 2 * ks, idesc_s, ks > 0);
@@ -467,35 +469,40 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 ptx::mbar_wait(&full_P[sp], pph, a.status);          // weights and Z stage
                 ptx::tc_fence_after();
-                const uint32_t pbuf = tmem + kSCol0 + kChunkKeys * sp;   // K step ks: hi 16 ks, lo 16 ks + 8
+                const uint32_t pbuf = tmem + kSCol0 + kCK * sp;   // K step ks: hi 16 ks, lo 16 ks + 8
                 const uint64_t zd = zdesc0 + (uint64_t)(sp * (kZStageBytes >> 4));
 #pragma unroll
-                for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
+                for (int ks = 0; ks < kCK / 16; ++ks) {
                     const uint64_t bdesc = zd + (uint64_t)(128 * ks);     // 16 keys = 2048 bytes on
                     ptx::mma_bf16_ts(dacc, pbuf + 16 * ks, bdesc, kHop0 ? idesc64 : idesc128,
                                      has_g || (c | ks) != 0);
                     ptx::mma_bf16_ts(dacc, pbuf + 16 * ks + 8, bdesc, idesc64, 1);
                 }
-                const int h = c - c0;
-                if (has_g && (h == 0 || h == 1)) {
-                    // the global rows x this tile's own keys (same Z_k tile)
-                    if (h == 0) {
-                        // the image is in shared memory and the previous tile's
-                        // accumulator has been read
-                        ptx::mbar_wait(full_G, lt & 1, a.status);
-                        if (lt >= 1) ptx::mbar_wait(glob_empty, (lt - 1) & 1, a.status);
-                        ptx::tc_fence_after();
-                    }
+                if (has_g && (c == c0 || (c == c0 + 1 && (P.r64 % kCK) != 0))) {
+                    // the global rows x this tile's own keys i0 .. i0 + 127 (same Z_k
+                    // stage): K step ks of this chunk holds keys 128 c + 16 ks - r64 on
+                    // from i0, in 64-key half h of the image at its K step kk
                     const uint32_t dglob = tmem + kGlobCol0;
-                    const uint64_t ghi = gdesc0 + (uint64_t)(h * ((2 * band::kGImgPlaneBytes) >> 4));
-                    const uint64_t glo = ghi + (uint64_t)(band::kGImgPlaneBytes >> 4);
-#pragma unroll
-                    for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
+                    const int rel0 = kCK * c - P.r64;
+#pragma unroll 1
+                    for (int ks = 0; ks < kCK / 16; ++ks) {
+                        const int rel = rel0 + 16 * ks;
+                        if (rel < 0 || rel >= kTileRows) continue;
+                        if (rel == 0) {
+                            // the image is in shared memory and the previous tile's
+                            // accumulator has been read
+                            ptx::mbar_wait(full_G, lt & 1, a.status);
+                            if (lt >= 1) ptx::mbar_wait(glob_empty, (lt - 1) & 1, a.status);
+                            ptx::tc_fence_after();
+                        }
+                        const int h = rel >> 6, kk = (rel & 63) >> 4;
+                        const uint64_t ghi = gdesc0 + (uint64_t)(h * ((2 * band::kGImgPlaneBytes) >> 4) + 2 * kk);
+                        const uint64_t glo = ghi + (uint64_t)(band::kGImgPlaneBytes >> 4);
                         const uint64_t bdesc = zd + (uint64_t)(128 * ks);
-                        ptx::mma_bf16_ss(dglob, ghi + 2 * ks, bdesc, kHop0 ? idesc64 : idesc128, (h | ks) != 0);
-                        ptx::mma_bf16_ss(dglob, glo + 2 * ks, bdesc, idesc64, 1);
+                        ptx::mma_bf16_ss(dglob, ghi, bdesc, kHop0 ? idesc64 : idesc128, rel != 0);
+                        ptx::mma_bf16_ss(dglob, glo, bdesc, idesc64, 1);
+                        if (rel == kTileRows - 16) ptx::mma_commit(empty_G);
                     }
-                    if (h == 1) ptx::mma_commit(empty_G);
                 }
                 ptx::mma_commit(&pv_done[sp]);
                 if (c == nc - 1) ptx::mma_commit(acc_full);
@@ -513,10 +520,9 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else if (warp >= kSoftWarp0 && warp < kEpiWarp0) {
         // ---------------- band weights: thread <-> row t = 32 quad + lane of the tile,
-        // keys 16 slice .. +15 of each chunk.  The next chunk's scores load from
-        // TMEM while this chunk's weights are computed.
+        // keys 16 slice .. +15 of both 64-key halves of each chunk.
         const int quad = warp & 3;
-        const int slice = (warp - kSoftWarp0) >> 2;       // keys 16 slice .. +15 of each chunk
+        const int slice = (warp - kSoftWarp0) >> 2;       // keys 16 slice .. +15 of each half
         const int stid = tid - kSoftWarp0 * 32;           // 0..511
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int t = quad * 32 + lane;
@@ -537,34 +543,10 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             w.b2 = w.ok ? __ldg(a.m_sparse + w.urow) * kLog2e : 0.f;
             return w;
         };
-        // this warp's 16 columns of buffer g % kSBufs: the scores, then the weights
-        auto s_addr = [&](int g) { return tmem + lane_base + kSCol0 + kChunkKeys * (g % kSBufs) + 16 * slice; };
-        uint32_t ra[16], rb[16];
-        if (total > 0) {
-            ptx::mbar_wait(&full_S[0], 0, a.status);
-            __syncwarp();
-            ptx::tc_fence_after();
-            ptx::tmem_ld16_issue(s_addr(0), ra);
-            ptx::tmem_ld_wait16(ra);
-        }
-        Row row = my_tiles > 0 ? row_of(0) : Row{};
-        Row next_row = row;
-        float lsum = 0.f;
-        int lt_run = 0, c_run = 0;
-        for (int g = 0; g < total; ++g) {
-            const int lt = lt_run, c = c_run;
-            if (++c_run == nc) { c_run = 0; ++lt_run; }
-            if (c == 0 && lt > 0) { row = next_row; lsum = 0.f; }
-            if (c == nc - 1 && lt + 1 < my_tiles) next_row = row_of(lt + 1);
-            const bool more = g + 1 < total;
-            if (more) {
-                ptx::mbar_wait(&full_S[(g + 1) % kSBufs], ((g + 1) / kSBufs) & 1, a.status);
-                __syncwarp();
-                ptx::tc_fence_after();
-                ptx::tmem_ld16_issue(s_addr(g + 1), rb);
-            }
-            // e = exp(s - m_i) inside the row's window (keys lo..hi), else 0
-            const int64_t j0 = row.jb + kChunkKeys * c + 16 * slice;
+        // e = exp(s - m_i) for this row's 16 keys j0 .. j0 + 15 inside its window
+        // (keys lo..hi), else 0, as hi and lo bf16 pairs (two keys per TMEM column)
+        auto weights16 = [&](const uint32_t (&r)[16], const Row& row, int64_t j0, float& lsum,
+                             uint32_t (&hw)[8], uint32_t (&lw)[8]) {
             const bool full_in = row.ok && j0 >= row.lo && j0 + 15 <= row.hi;
             const bool none_in = !row.ok || j0 > row.hi || j0 + 15 < row.lo;
             float e[16];
@@ -573,20 +555,17 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int k = 0; k < 16; ++k) e[k] = 0.f;
             } else if (full_in) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) e[k] = ptx::ex2_approx(fmaf(__uint_as_float(ra[k]), a_sc, -row.b2));
+                for (int k = 0; k < 16; ++k) e[k] = ptx::ex2_approx(fmaf(__uint_as_float(r[k]), a_sc, -row.b2));
             } else {
                 const int dlo = (int)(row.lo - j0), dhi = (int)(row.hi - j0);   // in-window keys k in [dlo, dhi]
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
-                    e[k] = (k >= dlo && k <= dhi) ? ptx::ex2_approx(fmaf(__uint_as_float(ra[k]), a_sc, -row.b2)) : 0.f;
+                    e[k] = (k >= dlo && k <= dhi) ? ptx::ex2_approx(fmaf(__uint_as_float(r[k]), a_sc, -row.b2)) : 0.f;
             }
             if (kHop0) {
 #pragma unroll
                 for (int k = 0; k < 16; ++k) lsum += e[k];
             }
-            // this row's 16 keys of the chunk's weight operand: hi and lo bf16,
-            // two keys per TMEM column
-            uint32_t hw[8], lw[8];
 #pragma unroll
             for (int p2 = 0; p2 < 8; ++p2) {
                 const float x0 = e[2 * p2], x1 = e[2 * p2 + 1];
@@ -595,13 +574,41 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
                 lw[p2] = *reinterpret_cast<const uint32_t*>(&l);
             }
-            // over this warp's own scores of the chunk (already in registers)
-            __syncwarp();       // reconverge before the warp-collective tcgen05.st
-            const uint32_t pcol = s_addr(g);
-            ptx::tmem_st16_hilo(pcol, hw, lw);     // hi in columns +0..7, lo in +8..15
+        };
+        Row row = my_tiles > 0 ? row_of(0) : Row{};
+        Row next_row = row;
+        float lsum = 0.f;
+        int lt = 0, c = 0, sb = 0, sph = 0;                // running tile, chunk, slot, phase
+        for (int g = 0; g < total; ++g) {
+            if (c == 0 && lt > 0) { row = next_row; lsum = 0.f; }
+            if (c == nc - 1 && lt + 1 < my_tiles) next_row = row_of(lt + 1);
+            // this warp's columns of buffer sb: keys 16 slice .. +15 of both 64-key
+            // halves, the scores, then (in place) the weights
+            ptx::mbar_wait(&full_S[sb], sph, a.status);
+            __syncwarp();
+            ptx::tc_fence_after();
+            const uint32_t col = tmem + lane_base + kSCol0 + kCK * sb + 16 * slice;
+            uint32_t ra[16], rb[16];
+            ptx::tmem_ld16_issue(col, ra);
+            ptx::tmem_ld16_issue(col + kChunkKeys, rb);
+            ptx::tmem_ld_wait16(ra);
+            ptx::tmem_ld_wait16(rb);
+            const int64_t j0 = row.jb + kCK * c + 16 * slice;
+            {
+                uint32_t hw[8], lw[8];
+                weights16(ra, row, j0, lsum, hw, lw);
+                __syncwarp();   // reconverge before the warp-collective tcgen05.st
+                ptx::tmem_st16_hilo(col, hw, lw);                 // hi in columns +0..7, lo in +8..15
+            }
+            {
+                uint32_t hw[8], lw[8];
+                weights16(rb, row, j0 + kChunkKeys, lsum, hw, lw);
+                __syncwarp();
+                ptx::tmem_st16_hilo(col + kChunkKeys, hw, lw);
+            }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&full_P[g % kSBufs]);
+            if (lane == 0) ptx::mbar_arrive(&full_P[sb]);
             if (kHop0 && c == nc - 1) {
                 // the row's band sum (this slice) for the epilogue warp of the quadrant;
                 // the buffer of this parity is free once that warp has read tile lt - 2's
@@ -611,11 +618,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&xch_full[xb]);
             }
-            if (more) {
-                ptx::tmem_ld_wait16(rb);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) ra[k] = rb[k];
-            }
+            if (++sb == kSBufs) { sb = 0; sph ^= 1; }
+            if (++c == nc) { c = 0; ++lt; }
         }
     } else if (warp >= kEpiWarp0) {
         // ---------------- epilogue: the warp of lane quadrant q reads rows 32 q .. +31
@@ -1060,9 +1064,9 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     // weights' MMA: V ([n][64]) for hop 0, then the Z_k rows ([n][hi | lo])
     CUtensorMap tmQ, tmK, tmV, tmZ[2];
     int st = encode_rows(&tmQ, Q, p.n, units, kHeadDim, kTileRows);
-    if (!st) st = encode_rows(&tmK, K, p.n, units, kHeadDim);
-    if (!st) st = encode_rows(&tmV, V, p.n, units, kHeadDim);
-    for (int s = 0; s < 2 && !st; ++s) st = encode_rows(&tmZ[s], ws + L.z[s], p.n, units, 2 * kHeadDim);
+    if (!st) st = encode_rows(&tmK, K, p.n, units, kHeadDim, kCK);
+    if (!st) st = encode_rows(&tmV, V, p.n, units, kHeadDim, kCK);
+    for (int s = 0; s < 2 && !st; ++s) st = encode_rows(&tmZ[s], ws + L.z[s], p.n, units, 2 * kHeadDim, kCK);
     if (st) return st;
 
     HopArgs a;
