@@ -284,7 +284,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ptx::mbar_init(glob_empty, 1);
         ptx::mbar_init(full_G, 1);
         ptx::mbar_init(empty_G, 1);
-        ptx::mbar_init(full_GC, 2);
+        ptx::mbar_init(full_GC, 1 + kEpiWarps);  // the image's bytes + each epilogue warp's staged rows
         ptx::mbar_init(empty_GC, 1);
         for (int s = 0; s < 8; ++s) { ptx::mbar_init(&xch_full[s], kSlices); ptx::mbar_init(&xch_empty[s], 1); }
         ptx::fence_mbar_init();
@@ -337,45 +337,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int64_t u = tix / P.tiles;
             const int64_t i0 = (tix - u * P.tiles) * kTileRows;
             if (has_g && c == 0) {
-                // the out-of-window globals: their weights' image by bulk copy, and the
-                // global keys' Z_k rows as an MN-major B tile (key row s: hi 128 bytes,
-                // lo g16 * 128 bytes on; 16-byte chunk c at (c ^ (s % 8)) * 16; rows
-                // past g are zero)
-                if (lt >= 1) ptx::mbar_wait(empty_GC, (lt - 1) & 1, a.status);
-                if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(full_GC, 2 * gc_plane);
-                    ptx::bulk_load_hint(sGC, a.A_gcimg + (size_t)tix * 2 * gc_plane, 2 * gc_plane, full_GC,
-                                        pol_once);
-                }
-                for (int e = lane; e < g16 * 8; e += 32) {
-                    const int sl = e >> 3, cch = e & 7;
-                    float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    if (sl < P.g) {
-                        const size_t row = (size_t)u * P.n + a.globals[sl];
-                        if (kHop0) {
-                            const uint4 h = __ldg(reinterpret_cast<const uint4*>(a.V + row * kHeadDim) + cch);
-                            const uint32_t w4[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) { z[2 * q] = bf16lo(w4[q]); z[2 * q + 1] = bf16hi(w4[q]); }
-                        } else {
-                            const float4* zp = reinterpret_cast<const float4*>(a.Zf_in + row * kHeadDim) + 2 * cch;
-                            const float4 z0 = __ldg(zp), z1 = __ldg(zp + 1);
-                            z[0] = z0.x; z[1] = z0.y; z[2] = z0.z; z[3] = z0.w;
-                            z[4] = z1.x; z[5] = z1.y; z[6] = z1.z; z[7] = z1.w;
-                        }
-                    }
-                    uint4 hi, lo;
-                    split8(z, hi, lo);
-                    const int off = sl * 128 + ((cch ^ (sl & 7)) << 4);
-                    *reinterpret_cast<uint4*>(sZG + off) = hi;
-                    *reinterpret_cast<uint4*>(sZG + g16 * 128 + off) = lo;
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(full_GC);
-            }
-            if (has_g && c == c0) {
-                // the global rows' image of this tile's keys (used from this chunk on)
+                // the global rows' image of this tile's keys, needed from chunk c0 on
                 if (lt >= 1) ptx::mbar_wait(empty_G, (lt - 1) & 1, a.status);
                 if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(full_G, band::kGImgBytes);
@@ -632,7 +594,51 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         float* st = sEpi + quad * (32 * kEpiRowFloats);                    // [32 rows][68]
         float* sk = sEpiKeep + quad * 32;                                  // keep of each row (< 0: skip)
         const int hr = lane >> 4, f4 = lane & 15;                          // row of the pair, feature quad
+        // The out-of-window globals of tile lt: their weights' image by bulk copy, and
+        // the global keys' Z_k rows as an MN-major B tile (key row s: hi 128 bytes,
+        // lo g16 * 128 bytes on; 16-byte chunk c at (c ^ (s % 8)) * 16; rows past g
+        // are zero), staged a tile ahead of the MMAs that read them.
+        auto stage_gc = [&](int lt) {
+            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+            const int64_t u = tix / P.tiles;
+            if (quad == 0 && lane == 0) {
+                ptx::mbar_arrive_expect_tx(full_GC, 2 * gc_plane);
+                ptx::bulk_load_hint(sGC, a.A_gcimg + (size_t)tix * 2 * gc_plane, 2 * gc_plane, full_GC,
+                                    ptx::l2_evict_first());
+            }
+            for (int e = t; e < g16 * 8; e += kEpiWarps * 32) {
+                const int sl = e >> 3, cch = e & 7;
+                float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (sl < P.g) {
+                    const size_t row = (size_t)u * P.n + a.globals[sl];
+                    if (kHop0) {
+                        const uint4 h = __ldg(reinterpret_cast<const uint4*>(a.V + row * kHeadDim) + cch);
+                        const uint32_t w4[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) { z[2 * q] = bf16lo(w4[q]); z[2 * q + 1] = bf16hi(w4[q]); }
+                    } else {
+                        const float4* zp = reinterpret_cast<const float4*>(a.Zf_in + row * kHeadDim) + 2 * cch;
+                        const float4 z0 = __ldg(zp), z1 = __ldg(zp + 1);
+                        z[0] = z0.x; z[1] = z0.y; z[2] = z0.z; z[3] = z0.w;
+                        z[4] = z1.x; z[5] = z1.y; z[6] = z1.z; z[7] = z1.w;
+                    }
+                }
+                uint4 hi, lo;
+                split8(z, hi, lo);
+                const int off = sl * 128 + ((cch ^ (sl & 7)) << 4);
+                *reinterpret_cast<uint4*>(sZG + off) = hi;
+                *reinterpret_cast<uint4*>(sZG + g16 * 128 + off) = lo;
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(full_GC);
+        };
+        if (has_g && my_tiles > 0) stage_gc(0);
         for (int lt = 0; lt < my_tiles; ++lt) {
+            if (has_g && lt + 1 < my_tiles) {
+                ptx::mbar_wait(empty_GC, lt & 1, a.status);      // tile lt's globals' MMAs are done
+                stage_gc(lt + 1);
+            }
             const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
             const int64_t u = tix / P.tiles;
             const int64_t i0 = (tix - u * P.tiles) * kTileRows;
