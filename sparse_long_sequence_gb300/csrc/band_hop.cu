@@ -10,11 +10,11 @@
 //            reads whole 128-byte lines.  Hops after the first also sum the
 //            global rows of Z_k from the previous hop's tile shares.
 //   hop_band_kernel (persistent, 128-row tiles): the window part, on tcgen05
-//            tensor cores.  The band weights are not stored: per 64-key chunk
+//            tensor cores.  The band weights are not stored: per 128-key chunk
 //            the kernel recomputes S = Q_tile K_chunk^T (bf16 operands, fp32 in
 //            TMEM), turns it into e_ij = exp(s_ij - m_i) with the row maxima of
 //            the score pass (0 outside the window), and writes e as bf16 hi + lo
-//            (each the bf16 rounding of what is left) straight into tensor
+//            (each the bf16 rounding of what is left) over the scores in tensor
 //            memory as the A operand of the second MMA: e_hi*[Z_hi | Z_lo] (N = 128)
 //            + e_lo*Z_hi (N = 64), fp32 accumulation in TMEM; the e_lo*Z_lo term
 //            (below 2^-16 of the product) is the only one left out.  Re-reading
@@ -23,7 +23,7 @@
 //            outside each row's window are one more K step into the same
 //            accumulator (their stored weights' operand image [128 x g16]
 //            against the global keys' Z_k rows).  The global rows (full rows
-//            of A) ride along: on the two chunks that hold the tile's own keys,
+//            of A) ride along: on the chunk(s) that hold the tile's own keys,
 //            the same Z_k tiles also multiply the global rows' weights of those
 //            keys (a 32-row operand image) into a second accumulator, and each
 //            tile writes that share.  Epilogue:
