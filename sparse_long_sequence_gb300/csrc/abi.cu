@@ -381,6 +381,83 @@ int forward_device(const void* Q, const void* K, const void* V, int32_t dtype, i
     return run_hops_csr(g, a, A, V, dtype, hops, alpha, out, ws, L, stream);
 }
 
+// The side stream of the host-buffer forward that uploads V (one per device,
+// created on first use and kept for the life of the process).
+int upload_stream(int device, cudaStream_t* s) {
+    static std::mutex mu;
+    static cudaStream_t pool[16] = {};
+    if (device < 0 || device >= 16) return fail(DIFFUSER_ERR_CUDA, "device index out of range");
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pool[device]) {
+        cudaError_t err = cudaStreamCreateWithFlags(&pool[device], cudaStreamNonBlocking);
+        if (err != cudaSuccess) {
+            pool[device] = nullptr;
+            return cuda_fail(err, "upload stream");
+        }
+    }
+    *s = pool[device];
+    return DIFFUSER_OK;
+}
+
+// The device address of a pinned host buffer mapped into this device's address
+// space, or nullptr.
+void* mapped_host(void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+// Band-path forward from host buffers: Q and K upload on `stream` and the score
+// kernels start as soon as they are in; V uploads meanwhile on a side stream,
+// and the hops wait for it.  When `out` is pinned and mapped, the last hop
+// writes it in place (no download after the kernels); else it lands in dO and
+// is copied back.  Launches directly (no replay graph: the uploads leave the
+// CPU time to queue them).
+int forward_host_band(const void* Q, const void* K, const void* V, int64_t B, int64_t H,
+                      const diffuser_graph* g, const BandPlan& bp, int32_t hops, float alpha,
+                      void* out, char* dQ, char* dK, char* dV, char* dO, char* ws, size_t ws_bytes,
+                      size_t bytes, cudaStream_t stream) {
+    const int64_t units = B * H;
+    size_t need = 0;
+    int st = workspace_need(g, B, H, DIFFUSER_DTYPE_BF16, &need);
+    if (st) return st;
+    if ((st = check_workspace_bytes(need, ws, ws_bytes))) return st;
+    BandLayout BL;
+    if ((st = plan_band_layout(g, bp, units, &BL))) return st;
+    cudaStream_t up;
+    if ((st = upload_stream(g->device, &up))) return st;
+    void* out_dev = mapped_host(out);
+    if (out_dev && !aligned16(out_dev)) out_dev = nullptr;
+    cudaEvent_t ev[2] = {};
+    cudaError_t err = cudaEventCreateWithFlags(&ev[0], cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ev[1], cudaEventDisableTiming);
+    // ev[0]: entry on `stream` (the uploads follow earlier work there); ev[1]: V is in
+    if (err == cudaSuccess) err = cudaEventRecord(ev[0], stream);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(up, ev[0], 0);
+    if (err == cudaSuccess) err = cudaMemcpyAsync(dQ, Q, bytes, cudaMemcpyHostToDevice, stream);
+    if (err == cudaSuccess) err = cudaMemcpyAsync(dK, K, bytes, cudaMemcpyHostToDevice, stream);
+    if (err == cudaSuccess) err = cudaMemcpyAsync(dV, V, bytes, cudaMemcpyHostToDevice, up);
+    if (err == cudaSuccess) err = cudaEventRecord(ev[1], up);
+    if (err == cudaSuccess) {
+        st = launch_band_scores(g, bp, units, dQ, dK, ws, BL, false, stream);
+        if (!st) {
+            err = cudaStreamWaitEvent(stream, ev[1], 0);
+            if (err == cudaSuccess)
+                st = launch_band_hops(g, bp, units, dQ, dK, dV, hops, alpha, out_dev ? out_dev : dO, ws, BL,
+                                      stream);
+        }
+        if (!st && err == cudaSuccess && !out_dev)
+            err = cudaMemcpyAsync(out, dO, bytes, cudaMemcpyDeviceToHost, stream);
+    }
+    for (int i = 0; i < 2; ++i)
+        if (ev[i]) cudaEventDestroy(ev[i]);      // released once their work completes
+    if (st) return st;
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "host-buffer forward (copies)");
+}
+
 int new_graph(diffuser_graph** out, diffuser_graph** g) {
     if (!out) return fail(DIFFUSER_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
@@ -583,6 +660,10 @@ int diffuser_forward_host(const void* Q, const void* K, const void* V, int32_t d
         char* dK = ws + slot;
         char* dV = ws + 2 * slot;
         char* dO = ws + 3 * slot;
+        BandPlan bp;
+        if (hops > 0 && use_band(g, dtype, &bp))
+            return forward_host_band(Q, K, V, B, H, g, bp, hops, alpha, out, dQ, dK, dV, dO, ws + 4 * slot,
+                                     workspace_bytes - 4 * slot, bytes, stream);
         cudaError_t err = cudaMemcpyAsync(dQ, Q, bytes, cudaMemcpyHostToDevice, stream);
         if (err == cudaSuccess) err = cudaMemcpyAsync(dK, K, bytes, cudaMemcpyHostToDevice, stream);
         if (err == cudaSuccess) err = cudaMemcpyAsync(dV, V, bytes, cudaMemcpyHostToDevice, stream);

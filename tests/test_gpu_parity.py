@@ -305,14 +305,16 @@ def test_bad_workspace_launches_nothing(dl):
     assert after == before
 
 
-def test_forward_host_buffers(dl):
-    # the end-to-end entry point: host buffers in, host buffer out
+@pytest.mark.parametrize("pinned_out", [True, False], ids=["pinned-out", "pageable-out"])
+def test_forward_host_buffers(dl, pinned_out):
+    # the end-to-end entry point: host buffers in, host buffer out (a pinned,
+    # mapped `out` is written in place by the last hop; a pageable one is copied back)
     import torch
     B, H, n = 1, 2, 513
     g = dl.diffuser_build_graph(n, 16, 2, rand_per_row=4)
     Q, K, V = synthetic.qkv(B, H, n, 64, "bf16", seed=8)
     Qh, Kh, Vh = (torch.from_numpy(x).view(torch.bfloat16).pin_memory() for x in (Q, K, V))
-    out = torch.empty_like(Vh).pin_memory()
+    out = torch.empty_like(Vh).pin_memory() if pinned_out else torch.empty(Vh.shape, dtype=Vh.dtype)
     ws = dl.alloc_workspace(dl.diffuser_host_workspace_size(g, B, H, 64, dl.DIFFUSER_DTYPE_BF16))
     dl.diffuser_forward_host(Qh, Kh, Vh, g, 5, 0.1, out, ws)
     torch.cuda.synchronize()
