@@ -342,7 +342,8 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) { ptx::mbar_init(&full_Q[s], 1); ptx::mbar_init(&empty_Q[s], 1); }
         for (int s = 0; s < kKStages; ++s) { ptx::mbar_init(&full_K[s], 1); ptx::mbar_init(&empty_K[s], 1); }
-        for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], kRowThreads); }
+        // the row warps release an S buffer once per warp (lane 0, after the warp has synced)
+        for (int s = 0; s < kSBufs; ++s) { ptx::mbar_init(&full_S[s], 1); ptx::mbar_init(&empty_S[s], kRowThreads / 32); }
         for (int s = 0; s < 2; ++s) { ptx::mbar_init(&full_G[s], 1); ptx::mbar_init(&empty_G[s], 1); }
         ptx::mbar_init(full_GR, 1);
         ptx::mbar_init(empty_GR, 64);
@@ -527,7 +528,8 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 float sv[32];
                 ptx::tmem_ld32(tmem + lane_base + kSChunk * b + 32 * hcol, sv);
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(&empty_S[b]);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&empty_S[b]);
                 const int64_t j0 = jb + kSChunk * c + 32 * hcol;
                 const bool full_in = row_ok && j0 >= lo && j0 + 31 <= hi;
                 const bool none_in = !row_ok || j0 > hi || j0 + 31 < lo;
