@@ -371,7 +371,7 @@ int forward_device(const void* Q, const void* K, const void* V, int32_t dtype, i
         if ((st = plan_band_layout(g, bp, B * H, &BL))) return st;
         const ReplayKey key{Q, K, V, out, workspace, workspace_bytes, B, H, dtype, hops, alpha, g_path.load()};
         return band_forward(g, key, stream, [&](cudaStream_t s) {
-            int r = launch_band_scores(g, bp, B * H, Q, K, ws, BL, false, s);
+            int r = launch_band_scores(g, bp, B * H, Q, K, V, ws, BL, false, s);
             if (!r) r = launch_band_hops(g, bp, B * H, Q, K, V, hops, alpha, out, ws, BL, s);
             return r;
         });
@@ -442,7 +442,7 @@ int forward_host_band(const void* Q, const void* K, const void* V, int64_t B, in
     if (err == cudaSuccess) err = cudaMemcpyAsync(dV, V, bytes, cudaMemcpyHostToDevice, up);
     if (err == cudaSuccess) err = cudaEventRecord(ev[1], up);
     if (err == cudaSuccess) {
-        st = launch_band_scores(g, bp, units, dQ, dK, ws, BL, false, stream);
+        st = launch_band_scores(g, bp, units, dQ, dK, nullptr, ws, BL, false, stream);
         if (!st) {
             err = cudaStreamWaitEvent(stream, ev[1], 0);
             if (err == cudaSuccess)
@@ -696,7 +696,7 @@ int diffuser_attention_weights(const void* Q, const void* K, int32_t dtype, int6
             BandLayout BL;
             char* ws = static_cast<char*>(workspace);
             if ((st = plan_band_layout(g, bp, B * H, &BL))) return st;
-            if ((st = launch_band_scores(g, bp, B * H, Q, K, ws, BL, true, stream))) return st;
+            if ((st = launch_band_scores(g, bp, B * H, Q, K, nullptr, ws, BL, true, stream))) return st;
             return launch_band_to_csr(g, bp, B * H, ws, BL, A_out, stream);
         }
         CsrArgs a{g->d_row_ptr, g->d_col, g->n, g->nnz, B * H};

@@ -49,6 +49,8 @@ struct ScoreArgs {
     band::Weights w;
     const __nv_bfloat16* Q;
     const __nv_bfloat16* K;
+    const uint8_t* Vpre;    // V, pulled into L2 for the first hop (null: not needed)
+    size_t vbytes;
 };
 
 // ---------------------------------------------------------------- sparse scores
@@ -465,7 +467,15 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
         }
     } else if (warp < kRowWarp0) {
-        // warp 3 has no role
+        // warp 3: pull V into L2 (32 KB pieces round-robin over the CTAs) for the
+        // first hop's gathers and band tiles, which read it right after this kernel
+        if (a.Vpre && lane == 0) {
+            constexpr size_t kPiece = 32768;
+            for (size_t off = (size_t)blockIdx.x * kPiece; off < a.vbytes; off += (size_t)gridDim.x * kPiece) {
+                const size_t len = a.vbytes - off < kPiece ? a.vbytes - off : kPiece;
+                ptx::bulk_prefetch_l2(a.Vpre + off, (uint32_t)len);
+            }
+        }
     } else {
         const int rw = warp - kRowWarp0;          // 0..7
         const int quad = warp & 3, hcol = rw >> 2;
@@ -780,13 +790,15 @@ ScoreArgs make_args(const diffuser_graph* g, const BandPlan& p, int64_t units, c
     s.w = band_weights(ws, L);
     s.Q = nullptr;
     s.K = nullptr;
+    s.Vpre = nullptr;
+    s.vbytes = 0;
     return s;
 }
 
 }  // namespace
 
 int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
-                       const void* K, char* ws, const BandLayout& L, bool weights_out,
+                       const void* K, const void* V, char* ws, const BandLayout& L, bool weights_out,
                        cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -804,6 +816,8 @@ int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units
     const auto* Kb = static_cast<const __nv_bfloat16*>(K);
     a.Q = Qb;
     a.K = Kb;
+    a.Vpre = static_cast<const uint8_t*>(V);
+    a.vbytes = V ? (size_t)units * p.n * kHeadDim * 2 : 0;
     const unsigned grid = (unsigned)(units * p.tiles);
     {
         LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);

@@ -130,8 +130,9 @@ int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, 
 // the forward's state: row maxima, the out-of-window globals' weights and
 // their part of the row sum in inv_l, the extras' raw scores and the global
 // rows' weights; the first hop completes the rest (launch_band_hops follows).
+// V (may be null) is only pulled into L2 for the first hop, under the score kernels.
 int launch_band_scores(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
-                       const void* K, char* ws, const BandLayout& L, bool weights_out,
+                       const void* K, const void* V, char* ws, const BandLayout& L, bool weights_out,
                        cudaStream_t stream);
 int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, const void* Q,
                      const void* K, const void* V, int32_t hops, float alpha, void* out, char* ws,
