@@ -86,10 +86,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 // follows; those rows are not used).  Then 2 Q tiles, the K, Z and weight-image
 // rings, the out-of-window globals' weight image (hi, lo; g16 slots) and their
 // Z_k rows as an MN-major B tile (hi, lo), the row-sum exchange, barriers.
+// The CTA's tiles as a shared-memory table (filled once, read by every role).
+constexpr int kMaxCtaTiles = 256;         // the launch keeps each CTA at or below this many tiles
+struct TileEntry { int32_t u, t; int16_t c_lo, c_hi; };
 __host__ __device__ constexpr int band_smem_bytes(int g16) {
     return 1024 + band::kGImgBytes + 2 * kQBytes + kSBufs * (kKBytes + kZStageBytes) +
            2 * kTileRows * (g16 > 0 ? g16 : 16) * 2 + 2 * (g16 > 0 ? g16 : 16) * 128 +
-           2 * kSoftThreads * 4 + 4 * 32 * kEpiRowFloats * 4 + 4 * 32 * 4 + 1024;
+           2 * kSoftThreads * 4 + 4 * 32 * kEpiRowFloats * 4 + 4 * 32 * 4 +
+           kMaxCtaTiles * (int)sizeof(TileEntry) + 16 + 1024;
 }
 constexpr int kSmemBytesMax = band_smem_bytes(16) > band_smem_bytes(kBandMaxGlobals)
                                   ? band_smem_bytes(16) : band_smem_bytes(kBandMaxGlobals);
@@ -213,6 +217,62 @@ __global__ void __launch_bounds__(256) hop_global_out_kernel(HopArgs a) {
     global_row_out<true>(a, a.gpart, u, rem >> 4, rem & 15, nullptr, nullptr);
 }
 
+// ---------------------------------------------------------------- the CTAs' tiles
+// A tile's 128-key chunks c (keys i0 - r64 + 128 c .. +127) that hold at least one
+// key in 0 .. n-1: c_lo .. c_hi (the others would only add zeros).
+__device__ __forceinline__ void chunk_range(const BandPlan& P, int nc, int64_t i0, int& c_lo, int& c_hi) {
+    const int64_t below = (int64_t)P.r64 - i0 - (kCK - 1);     // chunk c lies below key 0 iff 128 c < below
+    c_lo = below > 0 ? (int)((below + kCK - 1) / kCK) : 0;
+    const int64_t last = (P.n - (i0 - P.r64) - 1) / kCK;       // the last chunk with a key below n
+    c_hi = last < nc - 1 ? (int)last : nc - 1;
+}
+
+// The tile position (0 .. tiles-1) of rank p when the positions are ordered by
+// falling chunk count: the interior positions (all nc chunks in range) in order,
+// then the edge positions (the first and last few of a unit), heavier first.
+__device__ int tile_position(const BandPlan& P, int nc, int p) {
+    const int64_t tl = P.r64 > kCK - 1 ? ((int64_t)P.r64 - (kCK - 1) + kCK - 1) / kCK : 0;
+    const int64_t rnum = P.n + P.r64 - 1 - (int64_t)kCK * (nc - 1);
+    int64_t tr = rnum >= 0 ? rnum / kCK : -1;
+    if (tr > P.tiles - 1) tr = P.tiles - 1;
+    if (tl > tr) return p;                                      // no interior: natural order
+    const int ni = (int)(tr - tl + 1);
+    if (p < ni) return (int)tl + p;
+    // merge the left edge (tl - 1 down to 0) and the right edge (tr + 1 up) by
+    // falling chunk count, left first on ties
+    auto count = [&](int64_t t) { int lo, hi; chunk_range(P, nc, t * kTileRows, lo, hi); return hi - lo; };
+    int64_t li = tl - 1, ri = tr + 1;
+    for (int q = p - ni;; --q) {
+        const bool has_l = li >= 0, has_r = ri < P.tiles;
+        const bool take_l = has_l && (!has_r || count(li) >= count(ri));
+        const int64_t t = take_l ? li : ri;
+        if (q == 0 || (!has_l && !has_r)) return (int)t;
+        if (take_l) --li; else ++ri;
+    }
+}
+
+// The CTAs take the units' tiles heaviest first, in snake order over the rounds
+// (round r: CTA b gets item r G + b, or r G + G - 1 - b when r is odd), so that the
+// light edge tiles fill the last rounds.  Item k is tile position tile_position(k /
+// units) of unit k % units.
+struct TileInfo { int64_t tix, u, i0; int c_lo, c_hi; };
+__device__ __forceinline__ int cta_tile_count(int64_t total_tiles) {
+    const int64_t G = gridDim.x, b = blockIdx.x, R = total_tiles / G, rem = total_tiles - R * G;
+    return (int)(R + ((R & 1) == 0 ? (b < rem ? 1 : 0) : (b >= G - rem ? 1 : 0)));
+}
+__device__ __forceinline__ TileInfo cta_tile(const BandPlan& P, int64_t units, int nc, int lt) {
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    const int64_t k = (int64_t)lt * G + ((lt & 1) ? G - 1 - b : b);
+    const int64_t pr = k / units;
+    TileInfo ti;
+    ti.u = k - pr * units;
+    const int t = tile_position(P, nc, (int)pr);
+    ti.tix = ti.u * P.tiles + t;
+    ti.i0 = (int64_t)t * kTileRows;
+    chunk_range(P, nc, ti.i0, ti.c_lo, ti.c_hi);
+    return ti;
+}
+
 // ---------------------------------------------------------------- band part of a hop
 // The band weights are recomputed here on every hop from Q and K rather than
 // read back: per 64-key chunk, S = Q_tile K_chunk^T on the tensor cores (the
@@ -237,7 +297,9 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     float* xch = reinterpret_cast<float*>(sZG + 2 * g16s * 128);  // [2][256] row-sum halves
     float* sEpi = xch + 2 * kSoftThreads;                        // [4][32][68] epilogue staging
     float* sEpiKeep = sEpi + 4 * 32 * kEpiRowFloats;             // [4][32]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpiKeep + 4 * 32);
+    TileEntry* sTile = reinterpret_cast<TileEntry*>(sEpiKeep + 4 * 32);   // [kMaxCtaTiles]
+    int* sTotal = reinterpret_cast<int*>(sTile + kMaxCtaTiles);         // this CTA's chunk count
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sTotal + 4);
     uint64_t* full_Q = bars;                                     // [2]
     uint64_t* empty_Q = full_Q + 2;                              // [2]
     uint64_t* full_K = empty_Q + 2;                              // [kSBufs]
@@ -264,10 +326,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const bool has_g = P.g > 0;
     const int gc_plane = band::gc_plane_bytes(g16);
     const int64_t total_tiles = a.units * P.tiles;
-    // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
-    const int my_tiles = blockIdx.x < total_tiles
-        ? (int)((total_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
-    const int total = my_tiles * nc;             // chunks of this CTA
+    const int my_tiles = cta_tile_count(total_tiles);           // this CTA's tiles (cta_tile)
+    for (int lt = tid; lt < my_tiles && lt < kMaxCtaTiles; lt += kThreads) {
+        const TileInfo ti = cta_tile(P, a.units, nc, lt);
+        sTile[lt] = TileEntry{(int32_t)ti.u, (int32_t)(ti.i0 / kTileRows), (int16_t)ti.c_lo, (int16_t)ti.c_hi};
+    }
 
     if (warp == kSMmaWarp) ptx::tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
@@ -298,6 +361,20 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // this CTA's chunk count (for the drains), summed from the table by every thread
+    int total = 0;
+    for (int lt = 0; lt < my_tiles; ++lt) total += sTile[lt].c_hi - sTile[lt].c_lo + 1;
+    // tile lt of this CTA from the table
+    auto tile = [&](int lt) {
+        const TileEntry e = sTile[lt];
+        TileInfo ti;
+        ti.u = e.u;
+        ti.tix = (int64_t)e.u * P.tiles + e.t;
+        ti.i0 = (int64_t)e.t * kTileRows;
+        ti.c_lo = e.c_lo;
+        ti.c_hi = e.c_hi;
+        return ti;
+    };
 
     if (warp == kTmaWarp) {
         // ---------------- TMA producer of the score operands: the Q tile and the K
@@ -305,25 +382,21 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // as zeros), in the order the score MMAs use them.
         if (lane == 0) {
             const uint64_t pol_keep = ptx::l2_evict_last();      // re-read by neighbouring tiles
-            int c = 0, lt = 0, b = 0, ph = 0;                     // running chunk, tile, slot, phase
-            int64_t u = 0, i0 = 0;
-            for (int g = 0; g < total; ++g) {
+            int g = 0, b = 0, ph = 0;                             // running chunk, slot, phase
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const TileInfo ti = tile(lt);
                 const int qb = lt & 1;
-                if (c == 0) {
-                    const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
-                    u = tix / P.tiles;
-                    i0 = (tix - u * P.tiles) * kTileRows;
-                    if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, a.status);
-                    ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
-                    ptx::tma_load_3d_hint(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, (int)i0, (int)u, pol_keep);
+                if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, a.status);
+                ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
+                ptx::tma_load_3d_hint(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, (int)ti.i0, (int)ti.u, pol_keep);
+                for (int c = ti.c_lo; c <= ti.c_hi; ++c, ++g) {
+                    // stage b is free once the scores of chunk g - kSBufs are written
+                    if (g >= kSBufs) ptx::mbar_wait(&full_S[b], ph ^ 1, a.status);
+                    ptx::mbar_arrive_expect_tx(&full_K[b], kKBytes);
+                    ptx::tma_load_3d_hint(sK + b * kKBytes, &tmK, &full_K[b], 0,
+                                          (int)(ti.i0 - P.r64 + kCK * c), (int)ti.u, pol_keep);
+                    if (++b == kSBufs) { b = 0; ph ^= 1; }
                 }
-                // stage b is free once the scores of chunk g - kSBufs are written
-                if (g >= kSBufs) ptx::mbar_wait(&full_S[b], ph ^ 1, a.status);
-                ptx::mbar_arrive_expect_tx(&full_K[b], kKBytes);
-                ptx::tma_load_3d_hint(sK + b * kKBytes, &tmK, &full_K[b], 0,
-                                      (int)(i0 - P.r64 + kCK * c), (int)u, pol_keep);
-                if (++b == kSBufs) { b = 0; ph ^= 1; }
-                if (++c == nc) { c = 0; ++lt; }
             }
         }
     } else if (warp == kZWarp) {
@@ -331,33 +404,34 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // issues the copies): per tile the globals' images and the global keys'
         // Z_k rows, per chunk the Z_k rows, in the order the MMAs use them.
         const uint64_t pol_once = ptx::l2_evict_first(), pol_keep = ptx::l2_evict_last();
-        for (int g = 0; g < total; ++g) {
-            const int lt = g / nc, c = g - lt * nc;
-            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
-            const int64_t u = tix / P.tiles;
-            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-            if (has_g && c == 0) {
+        int g = 0;                                                // running chunk
+        for (int lt = 0; lt < my_tiles; ++lt) {
+            const TileInfo ti = tile(lt);
+            if (has_g) {
                 // the global rows' image of this tile's keys, needed from chunk c0 on
                 if (lt >= 1) ptx::mbar_wait(empty_G, (lt - 1) & 1, a.status);
                 if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(full_G, band::kGImgBytes);
-                    ptx::bulk_load_hint(sGA, a.A_gimg + (size_t)tix * band::kGImgBytes, band::kGImgBytes,
+                    ptx::bulk_load_hint(sGA, a.A_gimg + (size_t)ti.tix * band::kGImgBytes, band::kGImgBytes,
                                         full_G, pol_once);
                 }
             }
-            const int key = (int)(i0 - P.r64 + kCK * c);
-            const int b = g % kSBufs;
-            // stage b is free once the weights' MMAs of chunk g - kSBufs are done; the
-            // copy completes on the chunk's full_P barrier
-            if (g >= kSBufs) ptx::mbar_wait(&pv_done[b], ((g / kSBufs) - 1) & 1, a.status);
-            if (lane == 0) {
-                uint8_t* zdst = sZ + b * kZStageBytes;
-                ptx::mbar_arrive_expect_tx(&full_P[b], kHop0 ? kZTileBytes : 2 * kZTileBytes);
-                ptx::tma_load_3d_hint(zdst, &tmZ, &full_P[b], 0, key, (int)u, pol_keep);
-                if (!kHop0)
-                    ptx::tma_load_3d_hint(zdst + kZTileBytes, &tmZ, &full_P[b], kHeadDim, key, (int)u, pol_keep);
+            for (int c = ti.c_lo; c <= ti.c_hi; ++c, ++g) {
+                const int key = (int)(ti.i0 - P.r64 + kCK * c);
+                const int b = g % kSBufs;
+                // stage b is free once the weights' MMAs of chunk g - kSBufs are done; the
+                // copy completes on the chunk's full_P barrier
+                if (g >= kSBufs) ptx::mbar_wait(&pv_done[b], ((g / kSBufs) - 1) & 1, a.status);
+                if (lane == 0) {
+                    uint8_t* zdst = sZ + b * kZStageBytes;
+                    ptx::mbar_arrive_expect_tx(&full_P[b], kHop0 ? kZTileBytes : 2 * kZTileBytes);
+                    ptx::tma_load_3d_hint(zdst, &tmZ, &full_P[b], 0, key, (int)ti.u, pol_keep);
+                    if (!kHop0)
+                        ptx::tma_load_3d_hint(zdst + kZTileBytes, &tmZ, &full_P[b], kHeadDim, key, (int)ti.u,
+                                              pol_keep);
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
     } else if (warp == kSMmaWarp) {
         // ---------------- score MMAs: S[b] = Q_tile K_chunk^T (both K-major,
@@ -368,23 +442,25 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // descriptors advance by (byte offset >> 4) in their address field
             const uint64_t qdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sQ));
             const uint64_t kdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sK));
-            int c = 0, lt = 0, b = 0, ph = 0;                     // running chunk, tile, slot, phase
-            for (int g = 0; g < total; ++g) {
+            int g = 0, b = 0, ph = 0;                             // running chunk, slot, phase
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const TileInfo ti = tile(lt);
                 const int qb = lt & 1;
-                if (c == 0) ptx::mbar_wait(&full_Q[qb], (lt >> 1) & 1, a.status);
-                ptx::mbar_wait(&full_K[b], ph, a.status);
-                if (g >= kSBufs) ptx::mbar_wait(&pv_done[b], ph ^ 1, a.status);
-                ptx::tc_fence_after();
+                ptx::mbar_wait(&full_Q[qb], (lt >> 1) & 1, a.status);
                 const uint64_t qd = qdesc0 + (uint64_t)(qb * (kQBytes >> 4));
-                const uint64_t kd = kdesc0 + (uint64_t)(b * (kKBytes >> 4));
-                const uint32_t dS = tmem + kSCol0 + kCK * b;
+                for (int c = ti.c_lo; c <= ti.c_hi; ++c, ++g) {
+                    ptx::mbar_wait(&full_K[b], ph, a.status);
+                    if (g >= kSBufs) ptx::mbar_wait(&pv_done[b], ph ^ 1, a.status);
+                    ptx::tc_fence_after();
+                    const uint64_t kd = kdesc0 + (uint64_t)(b * (kKBytes >> 4));
+                    const uint32_t dS = tmem + kSCol0 + kCK * b;
 #pragma unroll
-                for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                    ptx::mma_bf16_ss(dS, qd + 2 * ks, kd + 2 * ks, idesc_s, ks > 0);
-                ptx::mma_commit(&full_S[b]);                      // also frees K stage b
-                if (c == nc - 1) ptx::mma_commit(&empty_Q[qb]);
-                if (++b == kSBufs) { b = 0; ph ^= 1; }
-                if (++c == nc) { c = 0; ++lt; }
+                    for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                        ptx::mma_bf16_ss(dS, qd + 2 * ks, kd + 2 * ks, idesc_s, ks > 0);
+                    ptx::mma_commit(&full_S[b]);                  // also frees K stage b
+                    if (c == ti.c_hi) ptx::mma_commit(&empty_Q[qb]);
+                    if (++b == kSBufs) { b = 0; ph ^= 1; }
+                }
             }
             // Drain: the commits arrive asynchronously when the MMAs finish; wait for
             // the last phase of each so that none lands in shared memory after exit.
@@ -407,9 +483,10 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // descriptors advance by (byte offset >> 4) in their address field
             const uint64_t zdesc0 = ptx::sw128_mnmajor_desc(ptx::smem_u32(sZ), kZTileBytes);
             const uint64_t gdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sGA));
-            int c = 0, lt = 0, sp = 0, pph = 0;                   // running chunk, tile, slot, phase
-            for (int g = 0; g < total; ++g) {
-                if (c == 0) {
+            int sp = 0, pph = 0;                                  // running slot, phase
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const TileInfo ti = tile(lt);
+                {
                     // the previous tile's accumulators have been read
                     if (lt >= 1) ptx::mbar_wait(acc_empty, (lt - 1) & 1, a.status);
                     ptx::tc_fence_after();
@@ -429,6 +506,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         ptx::mma_commit(empty_GC);
                     }
                 }
+              for (int c = ti.c_lo; c <= ti.c_hi; ++c) {
                 ptx::mbar_wait(&full_P[sp], pph, a.status);          // weights and Z stage
                 ptx::tc_fence_after();
                 const uint32_t pbuf = tmem + kSCol0 + kCK * sp;   // K step ks: hi 16 ks, lo 16 ks + 8
@@ -437,10 +515,14 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int ks = 0; ks < kCK / 16; ++ks) {
                     const uint64_t bdesc = zd + (uint64_t)(128 * ks);     // 16 keys = 2048 bytes on
                     ptx::mma_bf16_ts(dacc, pbuf + 16 * ks, bdesc, kHop0 ? idesc64 : idesc128,
-                                     has_g || (c | ks) != 0);
+                                     has_g || c != ti.c_lo || ks != 0);
                     ptx::mma_bf16_ts(dacc, pbuf + 16 * ks + 8, bdesc, idesc64, 1);
                 }
-                if (has_g && (c == c0 || (c == c0 + 1 && (P.r64 % kCK) != 0))) {
+                // the chunk(s) holding the tile's own keys: c0, and c0 + 1 when r64 is an
+                // odd multiple of 64 and that chunk is in range (a ragged last tile may end
+                // before it); the image is released after the last of them
+                const int glob_last = ((P.r64 % kCK) != 0 && c0 + 1 <= ti.c_hi) ? c0 + 1 : c0;
+                if (has_g && (c == c0 || c == glob_last)) {
                     // the global rows x this tile's own keys i0 .. i0 + 127 (same Z_k
                     // stage): K step ks of this chunk holds keys 128 c + 16 ks - r64 on
                     // from i0, in 64-key half h of the image at its K step kk
@@ -463,13 +545,13 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         const uint64_t bdesc = zd + (uint64_t)(128 * ks);
                         ptx::mma_bf16_ss(dglob, ghi, bdesc, kHop0 ? idesc64 : idesc128, rel != 0);
                         ptx::mma_bf16_ss(dglob, glo, bdesc, idesc64, 1);
-                        if (rel == kTileRows - 16) ptx::mma_commit(empty_G);
                     }
+                    if (c == glob_last) ptx::mma_commit(empty_G);
                 }
                 ptx::mma_commit(&pv_done[sp]);
-                if (c == nc - 1) ptx::mma_commit(acc_full);
+                if (c == ti.c_hi) ptx::mma_commit(acc_full);
                 if (++sp == kSBufs) { sp = 0; pph ^= 1; }
-                if (++c == nc) { c = 0; ++lt; }
+              }
             }
             for (int s = 0; s < kSBufs; ++s) {
                 const int uses = (total - s + kSBufs - 1) / kSBufs;
@@ -490,12 +572,13 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int t = quad * 32 + lane;
         const float a_sc = kLog2e * kScale;
         // this row of tile lt: validity, window lo..hi, and b2 = m_i log2(e)
-        struct Row { int64_t jb, lo, hi; size_t urow; bool ok; float b2; };
+        struct Row { int64_t jb, lo, hi; size_t urow; bool ok; float b2; int c_lo, c_hi; };
         auto row_of = [&](int lt) {
             Row w;
-            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
-            const int64_t u = tix / P.tiles;
-            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+            const TileInfo ti = tile(lt);
+            const int64_t u = ti.u, i0 = ti.i0;
+            w.c_lo = ti.c_lo;
+            w.c_hi = ti.c_hi;
             const int64_t i = i0 + t;
             w.jb = i0 - P.r64;
             w.ok = i < P.n && !a.is_global[i < P.n ? i : 0];
@@ -540,10 +623,9 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         Row row = my_tiles > 0 ? row_of(0) : Row{};
         Row next_row = row;
         float lsum = 0.f;
-        int lt = 0, c = 0, sb = 0, sph = 0;                // running tile, chunk, slot, phase
+        int lt = 0, c = row.c_lo, sb = 0, sph = 0;         // running tile, chunk, slot, phase
         for (int g = 0; g < total; ++g) {
-            if (c == 0 && lt > 0) { row = next_row; lsum = 0.f; }
-            if (c == nc - 1 && lt + 1 < my_tiles) next_row = row_of(lt + 1);
+            if (c == row.c_hi && lt + 1 < my_tiles) next_row = row_of(lt + 1);
             // this warp's columns of buffer sb: keys 16 slice .. +15 of both 64-key
             // halves, the scores, then (in place) the weights
             ptx::mbar_wait(&full_S[sb], sph, a.status);
@@ -571,7 +653,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&full_P[sb]);
-            if (kHop0 && c == nc - 1) {
+            if (kHop0 && c == row.c_hi) {
                 // the row's band sum (this slice) for the epilogue warp of the quadrant;
                 // the buffer of this parity is free once that warp has read tile lt - 2's
                 const int xb = quad * 2 + (lt & 1);
@@ -581,7 +663,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (lane == 0) ptx::mbar_arrive(&xch_full[xb]);
             }
             if (++sb == kSBufs) { sb = 0; sph ^= 1; }
-            if (++c == nc) { c = 0; ++lt; }
+            if (++c > row.c_hi && ++lt < my_tiles) {
+                row = next_row;
+                c = row.c_lo;
+                lsum = 0.f;
+            }
         }
     } else if (warp >= kEpiWarp0) {
         // ---------------- epilogue: the warp of lane quadrant q reads rows 32 q .. +31
@@ -599,8 +685,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // lo g16 * 128 bytes on; 16-byte chunk c at (c ^ (s % 8)) * 16; rows past g
         // are zero), staged a tile ahead of the MMAs that read them.
         auto stage_gc = [&](int lt) {
-            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
-            const int64_t u = tix / P.tiles;
+            const TileInfo ti = tile(lt);
+            const int64_t tix = ti.tix, u = ti.u;
             if (quad == 0 && lane == 0) {
                 ptx::mbar_arrive_expect_tx(full_GC, 2 * gc_plane);
                 ptx::bulk_load_hint(sGC, a.A_gcimg + (size_t)tix * 2 * gc_plane, 2 * gc_plane, full_GC,
@@ -639,9 +725,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ptx::mbar_wait(empty_GC, lt & 1, a.status);      // tile lt's globals' MMAs are done
                 stage_gc(lt + 1);
             }
-            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
-            const int64_t u = tix / P.tiles;
-            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+            const TileInfo ti = tile(lt);
+            const int64_t u = ti.u, i0 = ti.i0;
             const int64_t i = i0 + t;
             const bool row_ok = i < P.n && !a.is_global[i < P.n ? i : 0];
             const size_t urow = (size_t)u * P.n + (row_ok ? i : 0);
@@ -973,7 +1058,10 @@ int launch_hop(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap
     }
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return cuda_fail(err, "hop_gather_kernel");
-    dim3 grid((unsigned)(total_tiles < sms ? total_tiles : sms));
+    // one CTA per SM, or more (in waves) when an SM's share would exceed the tile table
+    int64_t ctas = total_tiles < sms ? total_tiles : sms;
+    if ((total_tiles + ctas - 1) / ctas > kMaxCtaTiles) ctas = (total_tiles + kMaxCtaTiles - 1) / kMaxCtaTiles;
+    dim3 grid((unsigned)ctas);
     {
         LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
         hop_band_kernel<kHop0, kLast><<<grid, kThreads, band_smem_bytes(a.plan.g16), stream>>>(tmQ, tmK, tmZ, a);
