@@ -253,8 +253,10 @@ __device__ int tile_position(const BandPlan& P, int nc, int p) {
 
 // The CTAs take the units' tiles heaviest first, in snake order over the rounds
 // (round r: CTA b gets item r G + b, or r G + G - 1 - b when r is odd), so that the
-// light edge tiles fill the last rounds.  Item k is tile position tile_position(k /
-// units) of unit k % units.
+// light edge tiles fill the last rounds.  The items: first every unit's interior
+// tiles, unit by unit (so that CTAs running at the same time mostly hold
+// neighbouring tiles, which share K and Z_k chunks in L2), then the edge tiles,
+// heavier positions first (tile_position), unit by unit within a position.
 struct TileInfo { int64_t tix, u, i0; int c_lo, c_hi; };
 __device__ __forceinline__ int cta_tile_count(int64_t total_tiles) {
     const int64_t G = gridDim.x, b = blockIdx.x, R = total_tiles / G, rem = total_tiles - R * G;
@@ -263,10 +265,16 @@ __device__ __forceinline__ int cta_tile_count(int64_t total_tiles) {
 __device__ __forceinline__ TileInfo cta_tile(const BandPlan& P, int64_t units, int nc, int lt) {
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t k = (int64_t)lt * G + ((lt & 1) ? G - 1 - b : b);
-    const int64_t pr = k / units;
+    // interior tiles first, unit-major (neighbouring tiles run together), then the edge tiles
+    const int64_t tl = P.r64 > kCK - 1 ? ((int64_t)P.r64 - (kCK - 1) + kCK - 1) / kCK : 0;
+    const int64_t rnum = P.n + P.r64 - 1 - (int64_t)kCK * (nc - 1);
+    int64_t tr = rnum >= 0 ? rnum / kCK : -1;
+    if (tr > P.tiles - 1) tr = P.tiles - 1;
     TileInfo ti;
-    ti.u = k - pr * units;
-    const int t = tile_position(P, nc, (int)pr);
+    int t;
+    const int64_t ni = tl <= tr ? tr - tl + 1 : 0;
+    if (k < units * ni) { ti.u = k / ni; t = (int)(tl + (k - ti.u * ni)); }
+    else { const int64_t k2 = k - units * ni, pr = ni + k2 / units; ti.u = k2 - (k2 / units) * units; t = tile_position(P, nc, (int)pr); }
     ti.tix = ti.u * P.tiles + t;
     ti.i0 = (int64_t)t * kTileRows;
     chunk_range(P, nc, ti.i0, ti.c_lo, ti.c_hi);
