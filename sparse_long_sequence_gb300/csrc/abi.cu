@@ -210,6 +210,9 @@ int run_hops_csr(const diffuser_graph* g, const CsrArgs& a, const float* A, cons
 // the caller's stream (launch counts are credited per replay).  While a
 // profile is open, and while the caller's stream is capturing its own graph,
 // forwards launch their kernels directly.
+// marks the keys of host-buffer forwards (whose replays include the copies)
+constexpr int kHostPathKey = 1 << 8;
+
 struct ReplayKey {
     const void *Q, *K, *V, *out, *ws;
     size_t ws_bytes;
@@ -410,12 +413,13 @@ void* mapped_host(void* p) {
     return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
-// Band-path forward from host buffers: Q and K upload on `stream` and the score
-// kernels start as soon as they are in; V uploads meanwhile on a side stream,
-// and the hops wait for it.  When `out` is pinned and mapped, the last hop
-// writes it in place (no download after the kernels); else it lands in dO and
-// is copied back.  Launches directly (no replay graph: the uploads leave the
-// CPU time to queue them).
+// Band-path forward from host buffers: Q and K upload side by side (on the
+// forward's stream and a side stream) and the score kernels start as soon as both
+// are in; V then uploads on the side stream under the score kernels, and the hops
+// wait for it.  When `out` is pinned and mapped, the last hop writes it in place
+// (no download after the kernels); else it lands in dO and is copied back.  With
+// all four host buffers pinned, repeated calls replay the whole sequence (copies
+// and kernels) as one captured graph, like the device-buffer forward.
 int forward_host_band(const void* Q, const void* K, const void* V, int64_t B, int64_t H,
                       const diffuser_graph* g, const BandPlan& bp, int32_t hops, float alpha,
                       void* out, char* dQ, char* dK, char* dV, char* dO, char* ws, size_t ws_bytes,
@@ -431,31 +435,47 @@ int forward_host_band(const void* Q, const void* K, const void* V, int64_t B, in
     if ((st = upload_stream(g->device, &up))) return st;
     void* out_dev = mapped_host(out);
     if (out_dev && !aligned16(out_dev)) out_dev = nullptr;
-    cudaEvent_t ev[2] = {};
-    cudaError_t err = cudaEventCreateWithFlags(&ev[0], cudaEventDisableTiming);
-    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ev[1], cudaEventDisableTiming);
-    // ev[0]: entry on `stream` (the uploads follow earlier work there); ev[1]: V is in
-    if (err == cudaSuccess) err = cudaEventRecord(ev[0], stream);
-    if (err == cudaSuccess) err = cudaStreamWaitEvent(up, ev[0], 0);
-    if (err == cudaSuccess) err = cudaMemcpyAsync(dQ, Q, bytes, cudaMemcpyHostToDevice, stream);
-    if (err == cudaSuccess) err = cudaMemcpyAsync(dK, K, bytes, cudaMemcpyHostToDevice, stream);
-    if (err == cudaSuccess) err = cudaMemcpyAsync(dV, V, bytes, cudaMemcpyHostToDevice, up);
-    if (err == cudaSuccess) err = cudaEventRecord(ev[1], up);
-    if (err == cudaSuccess) {
-        st = launch_band_scores(g, bp, units, dQ, dK, nullptr, ws, BL, false, stream);
-        if (!st) {
-            err = cudaStreamWaitEvent(stream, ev[1], 0);
-            if (err == cudaSuccess)
-                st = launch_band_hops(g, bp, units, dQ, dK, dV, hops, alpha, out_dev ? out_dev : dO, ws, BL,
-                                      stream);
-        }
-        if (!st && err == cudaSuccess && !out_dev)
-            err = cudaMemcpyAsync(out, dO, bytes, cudaMemcpyDeviceToHost, stream);
+    const bool pinned = out_dev && mapped_host(const_cast<void*>(Q)) && mapped_host(const_cast<void*>(K)) &&
+                        mapped_host(const_cast<void*>(V));
+    cudaEvent_t ev[4] = {};
+    cudaError_t err = cudaSuccess;
+    for (int i = 0; i < 4 && err == cudaSuccess; ++i) err = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    // ev[0]: entry on the stream (the uploads follow earlier work there); ev[1]: K is
+    // in; ev[2]: Q and K are in; ev[3]: V is in.  V uploads after Q and K so that it
+    // does not share the link with the uploads the score kernels wait for.
+    auto enqueue = [&](cudaStream_t s) -> int {
+        cudaError_t e = cudaEventRecord(ev[0], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(up, ev[0], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dQ, Q, bytes, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dK, K, bytes, cudaMemcpyHostToDevice, up);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[1], up);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev[1], 0);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[2], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(up, ev[2], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dV, V, bytes, cudaMemcpyHostToDevice, up);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[3], up);
+        if (e != cudaSuccess) return cuda_fail(e, "host-buffer forward (uploads)");
+        int r = launch_band_scores(g, bp, units, dQ, dK, nullptr, ws, BL, false, s);
+        if (r) return r;
+        if ((e = cudaStreamWaitEvent(s, ev[3], 0)) != cudaSuccess) return cuda_fail(e, "host-buffer forward");
+        r = launch_band_hops(g, bp, units, dQ, dK, dV, hops, alpha, out_dev ? out_dev : dO, ws, BL, s);
+        if (r) return r;
+        if (!out_dev && (e = cudaMemcpyAsync(out, dO, bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+            return cuda_fail(e, "device-to-host copy");
+        return DIFFUSER_OK;
+    };
+    if (err != cudaSuccess) {
+        st = cuda_fail(err, "host-buffer forward (events)");
+    } else if (pinned) {
+        const ReplayKey key{Q, K, V, out, ws, ws_bytes, B, H, DIFFUSER_DTYPE_BF16, hops, alpha,
+                            g_path.load() | kHostPathKey};
+        st = band_forward(g, key, stream, enqueue);
+    } else {
+        st = enqueue(stream);
     }
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < 4; ++i)
         if (ev[i]) cudaEventDestroy(ev[i]);      // released once their work completes
-    if (st) return st;
-    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "host-buffer forward (copies)");
+    return st;
 }
 
 int new_graph(diffuser_graph** out, diffuser_graph** g) {
