@@ -182,11 +182,16 @@ DIFFUSER_API int diffuser_host_workspace_size(const diffuser_graph* g, int64_t B
 
 /*
  * diffuser_forward on HOST buffers: enqueues the host-to-device copies of Q,
- * K and V, the forward, and the device-to-host copy of out, all on `stream`.
+ * K and V, the forward, and the transfer of out back to the host, ordered
+ * after earlier work on `stream` and complete when `stream` is.
  * Q, K, V, out are host [B][H][n][d] buffers (page-locked memory makes the
  * copies asynchronous; pageable memory works but the copies then block).
- * The caller must synchronize `stream` before reading `out`.
- * Errors: as diffuser_forward.
+ * On the band path V uploads on an internal side stream while the score
+ * kernels run, and a page-locked `out` that is mapped into the device's
+ * address space is written directly by the last hop (no separate copy); the
+ * host buffers must therefore stay valid and untouched until `stream` has
+ * been synchronized.  The caller must synchronize `stream` before reading
+ * `out`.  Errors: as diffuser_forward.
  */
 DIFFUSER_API int diffuser_forward_host(const void* Q, const void* K, const void* V, int32_t dtype, int64_t B,
                           int64_t H, int32_t d, const diffuser_graph* g, int32_t hops,
