@@ -142,6 +142,10 @@ SMALL = [
     (2, 2, 513, 20, 2, 4, 2, 1.0),       # alpha 1 returns V
     (1, 4, 700, 17, 5, 3, 0, 0.1),       # hops 0 returns V
     (1, 1, 389, 128, 2, 32, 5, 0.1),     # ragged tail against 128-row tiles
+    # window radius padded to an odd multiple of 64 (a tile's own keys span two key
+    # chunks) and a last tile of fewer than 64 rows (the second one is out of range)
+    (1, 2, 650, 150, 3, 8, 5, 0.1),
+    (1, 3, 1034, 150, 5, 8, 3, 0.1),
 ]
 
 
