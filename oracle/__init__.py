@@ -67,6 +67,8 @@ def _load():
         lib.oracle_token_graph.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _i32p,
                                            ctypes.c_int32, ctypes.c_uint64, _i64p, _i32p,
                                            ctypes.c_int64, _i64p]
+        lib.oracle_token_graph_causal.restype = ctypes.c_int
+        lib.oracle_token_graph_causal.argtypes = lib.oracle_token_graph.argtypes
         lib.oracle_block_graph.restype = ctypes.c_int
         lib.oracle_block_graph.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64, _i64p,
@@ -100,21 +102,26 @@ def _check(status: int, what: str) -> None:
 
 
 def token_graph(n: int, r: int, n_globals: int, rand_per_row: int, seed: int = 0,
-                globals_idx=None) -> tuple[np.ndarray, np.ndarray]:
-    """CSR (row_ptr int64[n+1], col int32[nnz]) of window u globals u random draws."""
+                globals_idx=None, causal: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """CSR (row_ptr int64[n+1], col int32[nnz]) of window u globals u random draws.
+
+    ``causal``: the same edge set with the mask j <= i applied to every edge
+    kind (Diffuser notes sec 2.6; window of the r+1 history positions).
+    """
     lib = _load()
+    fn = lib.oracle_token_graph_causal if causal else lib.oracle_token_graph
     g = None
     if globals_idx is not None:
         g = np.ascontiguousarray(np.asarray(globals_idx, dtype=np.int32))
         n_globals = int(g.size)
     gp = _p(g, _i32p) if g is not None else None
     nnz = ctypes.c_int64(0)
-    _check(lib.oracle_token_graph(n, r, n_globals, gp, rand_per_row, seed, None, None, 0,
-                                  ctypes.byref(nnz)), "token_graph(count)")
+    _check(fn(n, r, n_globals, gp, rand_per_row, seed, None, None, 0, ctypes.byref(nnz)),
+           "token_graph(count)")
     row_ptr = np.zeros(n + 1, dtype=np.int64)
     col = np.zeros(max(nnz.value, 1), dtype=np.int32)
-    _check(lib.oracle_token_graph(n, r, n_globals, gp, rand_per_row, seed, _p(row_ptr, _i64p),
-                                  _p(col, _i32p), col.size, ctypes.byref(nnz)), "token_graph")
+    _check(fn(n, r, n_globals, gp, rand_per_row, seed, _p(row_ptr, _i64p), _p(col, _i32p),
+              col.size, ctypes.byref(nnz)), "token_graph")
     return row_ptr, col[: nnz.value]
 
 

@@ -14,10 +14,12 @@
  *   [D]  "Diffuser: modelling long sequences with multi-hop attention
  *        diffusion" (reading notes on arXiv 2210.11794v2):
  *        sec 2.1 eq S.1-S.5 (masked softmax weights), sec 2.2 (three edge
- *        kinds), sec 2.4 eq S.7 (PPR recursion), sec 2.5 (finite-K form).
+ *        kinds), sec 2.4 eq S.7 (PPR recursion), sec 2.5 (finite-K form),
+ *        sec 2.6 (causal use: A lower-triangular).
  *   [S]  "1.2.1 Static sparsity: Longformer, BigBird and sliding windows":
  *        sec 1 eq 1-4 (scores, mask, softmax, output), sec 1.1 eq 5-6
- *        (window), sec 1.2 eq 12 (symmetric global tokens), sec 2 eq 13 and
+ *        (window; causal window of r+1 history positions), sec 1.2 eq 12
+ *        (symmetric global tokens), sec 2 eq 13 and
  *        the 12-block example (BigBird block pattern), sec 2.1 (duplicate
  *        edges must not enter the denominator twice).
  *   [B]  "038 BigBird: keeping long-sequence information paths with sparse
@@ -40,6 +42,10 @@
  *     pair is an edge iff its block pair is allowed; the last block may be
  *     ragged ([S] sec 2, eq 13).
  *   - Scale 1/sqrt(d) with d the head width ([S] eq 1, [D] eq S.1).
+ *   - Causal graph: the token graph with the mask j <= i applied to all
+ *     three edge kinds ([D] sec 2.6; [S] sec 1.1 for the causal window):
+ *     window [i-r, i], globals g <= i, a global row reads 0..i, and a random
+ *     draw that lands after i is dropped, not redrawn.
  *
  * Everything is computed in double precision, in the plainest loop order.
  */
@@ -88,9 +94,9 @@ static int64_t emit_row(const unsigned char* mark, int64_t n, int32_t* col,
  * `globals` NULL means G = {0..n_globals-1}; otherwise it must be strictly
  * increasing inside [0, n).
  */
-int oracle_token_graph(int64_t n, int32_t r, int32_t n_globals,
+static int token_graph(int64_t n, int32_t r, int32_t n_globals,
                        const int32_t* globals, int32_t rand_per_row,
-                       uint64_t seed, int64_t* row_ptr, int32_t* col,
+                       uint64_t seed, int causal, int64_t* row_ptr, int32_t* col,
                        int64_t col_capacity, int64_t* nnz_out) {
     if (n < 1 || n > INT32_MAX || r < 0 || n_globals < 0 || n_globals > n ||
         rand_per_row < 0 || !nnz_out)
@@ -123,6 +129,8 @@ int oracle_token_graph(int64_t n, int32_t r, int32_t n_globals,
                 mark[j] = 1;
             }
         }
+        if (causal)                                      /* causal mask, [D] sec 2.6 */
+            for (int64_t j = i + 1; j < n; ++j) mark[j] = 0;
         nnz += emit_row(mark, n, col, nnz, col_capacity, &overflow);
         if (overflow) { free(is_global); free(mark); return ORACLE_CAPACITY; }
         if (row_ptr) row_ptr[i + 1] = nnz;
@@ -131,6 +139,32 @@ int oracle_token_graph(int64_t n, int32_t r, int32_t n_globals,
     free(is_global);
     free(mark);
     return ORACLE_OK;
+}
+
+int oracle_token_graph(int64_t n, int32_t r, int32_t n_globals,
+                       const int32_t* globals, int32_t rand_per_row,
+                       uint64_t seed, int64_t* row_ptr, int32_t* col,
+                       int64_t col_capacity, int64_t* nnz_out) {
+    return token_graph(n, r, n_globals, globals, rand_per_row, seed, 0, row_ptr,
+                       col, col_capacity, nnz_out);
+}
+
+/*
+ * Causal token graph ([D] sec 2.6: A lower-triangular, so every window,
+ * random and global edge must satisfy j <= i; [S] sec 1.1: the causal window
+ * is the r+1 nearest history positions).  The edge set is the token graph
+ * above with the mask j <= i applied to every row:
+ *   N(i) = {0..i}                                           if i in G
+ *   N(i) = ({j : i-r <= j <= i} u G u {random draws}) n [0, i]  otherwise
+ * The random draws are the same draws as the bidirectional graph's; those
+ * that land in the future are dropped, not redrawn.
+ */
+int oracle_token_graph_causal(int64_t n, int32_t r, int32_t n_globals,
+                              const int32_t* globals, int32_t rand_per_row,
+                              uint64_t seed, int64_t* row_ptr, int32_t* col,
+                              int64_t col_capacity, int64_t* nnz_out) {
+    return token_graph(n, r, n_globals, globals, rand_per_row, seed, 1, row_ptr,
+                       col, col_capacity, nnz_out);
 }
 
 /*

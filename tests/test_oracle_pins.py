@@ -44,6 +44,24 @@ def brute_token_graph(n, r, G, R, seed):
     return rows
 
 
+def brute_causal_token_graph(n, r, G, R, seed):
+    """Causal neighbour sets from the text: [S] sec 1.1 window of the r+1 history
+    positions; [D] sec 2.6 every global and random edge obeys j <= i."""
+    rows = []
+    for i in range(n):
+        if i in G:
+            s = set(range(i + 1))
+        else:
+            s = set(range(max(0, i - r), i + 1))
+            s |= {g for g in G if g <= i}
+            for t in range(R):
+                j = sm64_py(seed ^ (i * R + t)) % n
+                if j <= i:
+                    s.add(j)
+        rows.append(sorted(s))
+    return rows
+
+
 def brute_block_graph(n, b, c, s, gb, seed):
     nb = -(-n // b)
     half = (c - 1) // 2
@@ -358,3 +376,74 @@ def test_bf16_rounding_nearest_even():
     np.testing.assert_array_equal(back, np.array([1.0, 1.0, 1.0 + 2 ** -6, 1.0, -2.5, 0.0],
                                                  dtype=np.float32))
     np.testing.assert_array_equal(oracle.widen(bits, "bf16"), back.astype(np.float64))
+
+
+# ---------------------------------------------------------------- causal graph
+@pytest.mark.parametrize("n,r", [(1, 0), (8, 1), (9, 4), (64, 3), (513, 32), (1000, 99)])
+def test_causal_window_count_closed_form(n, r):
+    # [S] sec 1.1: a causal window row holds at most r+1 history positions;
+    # rows i < r hold i+1, so |E| = n(r+1) - r(r+1)/2 for n > r
+    assert n > r
+    row_ptr, _ = oracle.token_graph(n, r, 0, 0, causal=True)
+    assert row_ptr[-1] == n * (r + 1) - r * (r + 1) // 2
+
+
+@pytest.mark.parametrize("n,r,G,R,seed", [
+    (1, 0, [], 0, 0), (1, 3, [0], 5, 0), (2, 0, [], 3, 7), (17, 2, [0, 1], 4, 0),
+    (33, 1, [5, 20], 6, 123), (40, 0, [], 8, 99), (64, 5, [0, 31, 63], 16, 2**63 + 5),
+    (50, 30, [10], 3, 1), (96, 4, [], 40, 42),
+])
+def test_causal_token_graph_brute_force(n, r, G, R, seed):
+    row_ptr, col = oracle.token_graph(n, r, len(G), R, seed=seed, globals_idx=G, causal=True)
+    assert csr_rows(row_ptr, col) == brute_causal_token_graph(n, r, G, R, seed)
+
+
+def test_causal_graph_is_masked_bidirectional_graph():
+    # [D] sec 2.6: the causal graph is the lower triangle of the same edge set;
+    # every row keeps its self edge, so no softmax row is empty
+    n = 200
+    rp_b, col_b = oracle.token_graph(n, 6, 4, 5, seed=3, globals_idx=[0, 50, 120, 199])
+    rp_c, col_c = oracle.token_graph(n, 6, 4, 5, seed=3, globals_idx=[0, 50, 120, 199],
+                                     causal=True)
+    for i, (rb, rc) in enumerate(zip(csr_rows(rp_b, col_b), csr_rows(rp_c, col_c))):
+        assert rc == [j for j in rb if j <= i]
+        assert rc[-1] == i
+    # position 4 cannot read the future global 8 ([S] sec 1.2, causal remark)
+    rp, col = oracle.token_graph(16, 1, 0, 0, causal=True, globals_idx=[8])
+    assert 8 not in csr_rows(rp, col)[4] and 8 in csr_rows(rp, col)[9]
+
+
+def test_causal_full_graph_one_hop_is_dense_causal_attention():
+    # r >= n: every row reads all of its history; hops=1, alpha=0 is textbook
+    # causal softmax(Q K^T / sqrt(d) + upper-triangular -inf) V
+    n, d = 37, 64
+    Q, K, V = random_qkv(n, d, 19)
+    row_ptr, col = oracle.token_graph(n, n, 0, 0, causal=True)
+    out = oracle.forward(Q[None], K[None], V[None], row_ptr, col, hops=1, alpha=0.0)[0]
+    S = Q @ K.T / np.sqrt(d)
+    S[np.triu_indices(n, 1)] = -np.inf
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(out, P @ V, rtol=1e-12, atol=1e-13)
+
+
+def test_causal_diffusion_never_reads_the_future():
+    # [D] sec 2.6: A lower-triangular => every A^k and the PPR sum are too, so
+    # changing position p's Q, K or V leaves output rows < p exactly unchanged
+    n, d, p = 96, 16, 40
+    Q, K, V = random_qkv(n, d, 21)
+    row_ptr, col = oracle.token_graph(n, 5, 2, 6, seed=4, globals_idx=[10, 70], causal=True)
+    base = oracle.forward(Q[None], K[None], V[None], row_ptr, col, hops=5, alpha=0.1)[0]
+    for X in (Q, K, V):
+        Xp = X.copy()
+        Xp[p] += 1.0
+        args = [Q, K, V]
+        args[[id(Q), id(K), id(V)].index(id(X))] = Xp
+        pert = oracle.forward(*(a[None] for a in args), row_ptr, col, hops=5, alpha=0.1)[0]
+        np.testing.assert_array_equal(pert[:p], base[:p])
+        assert np.abs(pert[p:] - base[p:]).max() > 1e-6
+    # row 0 reads only itself: A_00 = 1, so Z_k row 0 is V row 0 for every K
+    np.testing.assert_allclose(base[0], V[0], rtol=0, atol=1e-15)
+    A = oracle.attention_weights(Q, K, row_ptr, col)
+    M = dense_from_csr(A, row_ptr, col, n)
+    assert not np.triu(np.linalg.matrix_power(M, 5), 1).any()
