@@ -109,6 +109,22 @@ DIFFUSER_API int diffuser_build_graph(int64_t n, int32_t r, int32_t n_globals, c
                          int32_t rand_per_row, uint64_t seed, diffuser_graph** out);
 
 /*
+ * Causal token graph ([D] sec 2.6: for autoregressive use A must be
+ * lower-triangular, so every window, global and random edge obeys j <= i;
+ * [S] sec 1.1: the causal window is the r+1 history positions).  The edge
+ * set of diffuser_build_graph with the same arguments, cut to j <= i:
+ *   N(i) = {0..i}                                               if i in G
+ *   N(i) = ({j : i-r <= j <= i} u G u {random draws}) n [0, i]  otherwise
+ * with the same draws as diffuser_build_graph; a draw that lands after i is
+ * dropped, not redrawn.  Every row holds its own position, so no softmax row
+ * is empty.  Arguments, ownership and errors: as diffuser_build_graph.  The
+ * forward over a causal graph takes the general CSR path.
+ */
+DIFFUSER_API int diffuser_build_causal_graph(int64_t n, int32_t r, int32_t n_globals,
+                                const int32_t* global_idx, int32_t rand_per_row,
+                                uint64_t seed, diffuser_graph** out);
+
+/*
  * BigBird ITC block graph ([S] sec 2 eq 13 and its 12-block example; [B]
  * sec 2).  N = ceil(n/block) blocks (the last one may be ragged).  Block row
  * J < global_blocks reads every block.  Any other block row J reads the

@@ -530,8 +530,10 @@ const char* diffuser_last_error(void) { return g_last_error.c_str(); }
 
 int diffuser_version(void) { return 100; }
 
-int diffuser_build_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* global_idx,
-                         int32_t rand_per_row, uint64_t seed, diffuser_graph** out) {
+namespace {
+
+int build_token_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* global_idx,
+                      int32_t rand_per_row, uint64_t seed, bool causal, diffuser_graph** out) {
     try {
         if (n < 1 || n > INT32_MAX) return fail(DIFFUSER_ERR_INVALID_ARG, "n out of range");
         if (r < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "r must be >= 0");
@@ -559,6 +561,7 @@ int diffuser_build_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t*
         g->r = r;
         g->n_globals = n_globals;
         g->rand_per_row = rand_per_row;
+        g->causal = causal;
         g->seed = seed;
         g->h_globals = std::move(G);
         st = build_token_graph_device(g, nullptr);
@@ -568,6 +571,19 @@ int diffuser_build_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t*
     } catch (...) {
         return fail(DIFFUSER_ERR_INVALID_ARG, "unexpected exception");
     }
+}
+
+}  // namespace
+
+int diffuser_build_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* global_idx,
+                         int32_t rand_per_row, uint64_t seed, diffuser_graph** out) {
+    return build_token_graph(n, r, n_globals, global_idx, rand_per_row, seed, false, out);
+}
+
+int diffuser_build_causal_graph(int64_t n, int32_t r, int32_t n_globals,
+                                const int32_t* global_idx, int32_t rand_per_row, uint64_t seed,
+                                diffuser_graph** out) {
+    return build_token_graph(n, r, n_globals, global_idx, rand_per_row, seed, true, out);
 }
 
 int diffuser_build_block_graph(int64_t n, int32_t block, int32_t window_blocks,

@@ -11,6 +11,11 @@
 // that fall outside the window and outside G, sorted and deduplicated.  The
 // three parts are disjoint, so a row is a merge of three sorted lists.
 //
+// Causal token graph (Diffuser notes sec 2.6: A lower-triangular, every edge
+// obeys j <= i; sliding-window page sec 1.1: the causal window holds the r+1
+// history positions): the same sets cut to [0, i].  Each row's upper limit
+// `last` is i instead of n-1; draws that land after i are dropped.
+//
 // Block graph (same page, sec 2 eq 13; "038 BigBird", sec 2): allowed blocks
 // of block row J are all blocks for J < gb, else [0, gb) u (window blocks u
 // random blocks); the tokens of the allowed blocks, ascending.
@@ -48,7 +53,21 @@ struct TokenParams {
     uint64_t seed;
     const int32_t* globals;
     const uint8_t* is_global;
+    int32_t causal;
 };
+
+// last column row i may read: i for the causal graph, else n-1
+__device__ __forceinline__ int64_t row_last(const TokenParams& p, int64_t i) {
+    return p.causal ? i : p.n - 1;
+}
+
+// window [lo, hi] of row i, cut to [0, last]
+__device__ __forceinline__ void row_window(const TokenParams& p, int64_t i, int64_t& lo,
+                                           int64_t& hi) {
+    const int64_t last = row_last(p, i);
+    lo = i - p.r < 0 ? 0 : i - p.r;
+    hi = i + p.r > last ? last : i + p.r;
+}
 
 // Sorted, deduplicated random draws of row i that fall outside its window
 // and outside G.  Returns their number; xs must hold R entries.
@@ -58,7 +77,7 @@ __device__ int32_t row_extras(const TokenParams& p, int64_t i, int64_t lo, int64
     for (int32_t t = 0; t < p.R; ++t) {
         uint64_t key = (uint64_t)i * (uint64_t)p.R + (uint64_t)t;
         int64_t j = (int64_t)(splitmix64(p.seed ^ key) % (uint64_t)p.n);
-        if ((j >= lo && j <= hi) || p.is_global[j]) continue;
+        if (j > row_last(p, i) || (j >= lo && j <= hi) || p.is_global[j]) continue;
         // insertion into the sorted prefix, dropping duplicates
         int32_t pos = cnt;
         while (pos > 0 && xs[pos - 1] > j) --pos;
@@ -74,11 +93,13 @@ __global__ void token_count_kernel(TokenParams p, int64_t* counts) {
     extern __shared__ int32_t smem_xs[];
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.n) return;
-    if (p.is_global[i]) { counts[i] = p.n; return; }
-    int64_t lo = i - p.r < 0 ? 0 : i - p.r;
-    int64_t hi = i + p.r > p.n - 1 ? p.n - 1 : i + p.r;
+    const int64_t last = row_last(p, i);
+    if (p.is_global[i]) { counts[i] = last + 1; return; }
+    int64_t lo, hi;
+    row_window(p, i, lo, hi);
     int64_t c = hi - lo + 1;
-    c += count_less(p.globals, p.g, lo) + (p.g - count_less(p.globals, p.g, hi + 1));
+    c += count_less(p.globals, p.g, lo) +
+         (count_less(p.globals, p.g, last + 1) - count_less(p.globals, p.g, hi + 1));
     int32_t* xs = smem_xs + (size_t)threadIdx.x * p.R;
     c += row_extras(p, i, lo, hi, xs);
     counts[i] = c;
@@ -102,8 +123,8 @@ __global__ void extras_count_kernel(TokenParams p, int64_t* counts) {
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.n) return;
     if (p.is_global[i]) { counts[i] = 0; return; }
-    int64_t lo = i - p.r < 0 ? 0 : i - p.r;
-    int64_t hi = i + p.r > p.n - 1 ? p.n - 1 : i + p.r;
+    int64_t lo, hi;
+    row_window(p, i, lo, hi);
     counts[i] = row_extras(p, i, lo, hi, smem_xs + (size_t)threadIdx.x * p.R);
 }
 
@@ -111,8 +132,8 @@ __global__ void extras_fill_kernel(TokenParams p, const int64_t* x_ptr, int32_t*
     extern __shared__ int32_t smem_xs[];
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.n || p.is_global[i]) return;
-    int64_t lo = i - p.r < 0 ? 0 : i - p.r;
-    int64_t hi = i + p.r > p.n - 1 ? p.n - 1 : i + p.r;
+    int64_t lo, hi;
+    row_window(p, i, lo, hi);
     int32_t* xs = smem_xs + (size_t)threadIdx.x * p.R;
     int32_t nx = row_extras(p, i, lo, hi, xs);
     for (int32_t q = 0; q < nx; ++q) x_col[x_ptr[i] + q] = xs[q];
@@ -123,17 +144,18 @@ __global__ void token_fill_kernel(TokenParams p, const int64_t* row_ptr, int32_t
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.n) return;
     int32_t* out = col + row_ptr[i];
+    const int64_t last = row_last(p, i);
     if (p.is_global[i]) {
-        for (int64_t j = 0; j < p.n; ++j) out[j] = (int32_t)j;
+        for (int64_t j = 0; j <= last; ++j) out[j] = (int32_t)j;
         return;
     }
-    int64_t lo = i - p.r < 0 ? 0 : i - p.r;
-    int64_t hi = i + p.r > p.n - 1 ? p.n - 1 : i + p.r;
+    int64_t lo, hi;
+    row_window(p, i, lo, hi);
     int32_t* xs = smem_xs + (size_t)threadIdx.x * p.R;
     int32_t nx = row_extras(p, i, lo, hi, xs);
     int64_t w = merge_range(p.globals, p.g, xs, nx, 0, lo - 1, out);
     for (int64_t j = lo; j <= hi; ++j) out[w++] = (int32_t)j;
-    merge_range(p.globals, p.g, xs, nx, hi + 1, p.n - 1, out + w);
+    merge_range(p.globals, p.g, xs, nx, hi + 1, last, out + w);
 }
 
 struct BlockParams {
@@ -336,7 +358,8 @@ int build_token_graph_device(diffuser_graph* g, cudaStream_t stream) {
     err = cudaMalloc(&d_counts, sizeof(int64_t) * n);
     if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(counts) failed");
 
-    TokenParams p{n, g->r, g->n_globals, g->rand_per_row, g->seed, g->d_globals, g->d_is_global};
+    TokenParams p{n,        g->r,           g->n_globals,   g->rand_per_row,
+                  g->seed,  g->d_globals,   g->d_is_global, g->causal ? 1 : 0};
     // per-thread scratch for the extras lives in shared memory; keep it <= 48 KB
     int threads = 128;
     while (threads > 1 && (size_t)threads * p.R * sizeof(int32_t) > 48 * 1024) threads >>= 1;

@@ -55,6 +55,7 @@ struct diffuser_graph {
     int64_t nnz = 0;
     // token graph parameters
     int32_t r = 0, n_globals = 0, rand_per_row = 0;
+    bool causal = false;              // token graph cut to j <= i
     // block graph parameters
     int32_t block = 0, window_blocks = 0, rand_blocks = 0, global_blocks = 0;
     uint64_t seed = 0;

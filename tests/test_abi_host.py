@@ -29,7 +29,8 @@ def declared_entry_points():
 
 def test_header_declares_the_boundary():
     names = declared_entry_points()
-    for must in ("diffuser_build_graph", "diffuser_build_block_graph", "diffuser_forward",
+    for must in ("diffuser_build_graph", "diffuser_build_causal_graph",
+                 "diffuser_build_block_graph", "diffuser_forward",
                  "diffuser_workspace_size", "diffuser_graph_copy_csr", "diffuser_graph_free"):
         assert must in names
 
@@ -68,6 +69,11 @@ def test_invalid_arguments_rejected_on_host(lib):
     bad = (i32 * 2)(5, 3)                                          # not increasing
     assert f(10, 1, 2, bad, 0, 0, ctypes.byref(out)) == 1
     assert f(10, 1, 0, None, 0, 0, None) == 1                      # null out
+    fc = lib.diffuser_build_causal_graph
+    fc.argtypes = f.argtypes
+    assert fc(0, 1, 0, None, 0, 0, ctypes.byref(out)) == 1         # n < 1
+    assert fc(10, -1, 0, None, 0, 0, ctypes.byref(out)) == 1       # r < 0
+    assert fc(10, 1, 2, bad, 0, 0, ctypes.byref(out)) == 1         # not increasing
     fb = lib.diffuser_build_block_graph
     fb.argtypes = [i64, i32, i32, i32, i32, u64, ctypes.POINTER(vp)]
     assert fb(100, 16, 2, 1, 1, 0, ctypes.byref(out)) == 1         # even window

@@ -327,6 +327,104 @@ def test_forward_host_buffers(dl, pinned_out):
     assert torch.equal(out, ref_dev.cpu())
 
 
+# ---------------------------------------------------------------- causal graph
+def build_causal(dl, args):
+    a = dict(args)
+    gi = a.pop("globals_idx", None)
+    return dl.diffuser_build_causal_graph(a["n"], a["r"], a["n_globals"], global_idx=gi,
+                                          rand_per_row=a["rand_per_row"], seed=a["seed"])
+
+
+@pytest.mark.parametrize("args", TOKEN_CASES)
+def test_causal_graph_bit_exact(dl, args):
+    g = build_causal(dl, args)
+    row_ptr, col = dl.diffuser_graph_copy_csr(g)
+    o_ptr, o_col = oracle.token_graph(**args, causal=True)
+    np.testing.assert_array_equal(row_ptr, o_ptr)
+    np.testing.assert_array_equal(col, o_col)
+
+
+CAUSAL_SMALL = [  # (B, H, n, r, |G|, R, K, alpha)
+    (2, 3, 300, 8, 3, 5, 5, 0.1),
+    (1, 2, 1000, 64, 8, 16, 5, 0.1),
+    (1, 1, 640, 640, 0, 0, 1, 0.0),      # full causal graph, one hop: dense causal attention
+    (1, 2, 389, 256, 2, 32, 5, 0.1),     # the text workload's r, |G| and R on a ragged n
+    (1, 2, 513, 20, 2, 4, 2, 1.0),       # alpha 1 returns V
+]
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("case", CAUSAL_SMALL, ids=lambda c: "B%dH%dn%dr%dg%dR%dK%da%s" % c)
+def test_causal_forward_small(dl, case, dtype):
+    import torch
+    B, H, n, r, gn, R, hops, alpha = case
+    g = dl.diffuser_build_causal_graph(n, r, gn, rand_per_row=R, seed=0)
+    o_ptr, o_col = oracle.token_graph(n, r, gn, R, seed=0, causal=True)
+    Q, K, V = synthetic.qkv(B, H, n, 64, dtype, seed=n + 1)
+    out = dl.diffuser_forward(to_device(Q, dtype), to_device(K, dtype), to_device(V, dtype), g,
+                              hops, alpha)
+    torch.cuda.synchronize()
+    ref = oracle.forward(oracle.widen(Q, dtype), oracle.widen(K, dtype), oracle.widen(V, dtype),
+                         o_ptr, o_col, hops, alpha, nthreads=4)
+    check_output(to_f64(out), ref, dtype)
+    if alpha == 1.0:
+        np.testing.assert_array_equal(to_f64(out), oracle.widen(V, dtype))
+
+
+def test_causal_forward_never_reads_the_future(dl):
+    # A lower-triangular: changing position p's V leaves every output row < p
+    # bit-identical on the device; row 0 reads only itself, so it returns V_0
+    import torch
+    B, H, n, p = 1, 4, 1500, 700
+    g = dl.diffuser_build_causal_graph(n, 64, 4, global_idx=[3, 650, 900, 1400],
+                                       rand_per_row=8, seed=5)
+    Q, K, V = (to_device(x, "bf16") for x in synthetic.qkv(B, H, n, 64, "bf16", seed=12))
+    base = dl.diffuser_forward(Q, K, V, g, 5, 0.1)
+    V2 = V.clone()
+    V2[:, :, p] += 1.0
+    pert = dl.diffuser_forward(Q, K, V2, g, 5, 0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(base[:, :, :p], pert[:, :, :p])
+    assert not torch.equal(base[:, :, p:], pert[:, :, p:])
+    assert torch.equal(base[:, :, 0], V[:, :, 0])
+
+
+def test_causal_text_workload_sampled_units(dl):
+    # the text workload's sizes (B2 H12 n4096 r256 |G|16 R32) on the causal graph,
+    # whole units sampled against the oracle
+    import torch
+    B, H, n, r, gn, R = 2, 12, 4096, 256, 16, 32
+    dtype = "bf16"
+    g = dl.diffuser_build_causal_graph(n, r, gn, rand_per_row=R, seed=1)
+    o_ptr, o_col = oracle.token_graph(n, r, gn, R, seed=1, causal=True)
+    assert g.nnz == o_ptr[-1]
+    Q, K, V = synthetic.qkv(B, H, n, 64, dtype, seed=4)
+    out = dl.diffuser_forward(to_device(Q, dtype), to_device(K, dtype), to_device(V, dtype), g,
+                              5, 0.1)
+    torch.cuda.synchronize()
+    got = to_f64(out).reshape(B * H, n, 64)
+    Qw, Kw, Vw = (oracle.widen(x, dtype).reshape(B * H, n, 64) for x in (Q, K, V))
+    units = _sample_units(B * H)
+    ref = oracle.forward(Qw[units], Kw[units], Vw[units], o_ptr, o_col, 5, 0.1, nthreads=3)
+    check_output(got[units], ref, dtype)
+
+
+def test_causal_forward_host_buffers(dl):
+    # host buffers through the end-to-end entry point take the same CSR path
+    import torch
+    B, H, n = 1, 2, 513
+    g = dl.diffuser_build_causal_graph(n, 16, 2, rand_per_row=4)
+    Q, K, V = synthetic.qkv(B, H, n, 64, "bf16", seed=9)
+    Qh, Kh, Vh = (torch.from_numpy(x).view(torch.bfloat16).pin_memory() for x in (Q, K, V))
+    out = torch.empty_like(Vh).pin_memory()
+    ws = dl.alloc_workspace(dl.diffuser_host_workspace_size(g, B, H, 64, dl.DIFFUSER_DTYPE_BF16))
+    dl.diffuser_forward_host(Qh, Kh, Vh, g, 5, 0.1, out, ws)
+    torch.cuda.synchronize()
+    ref_dev = dl.diffuser_forward(Qh.cuda(), Kh.cuda(), Vh.cuda(), g, 5, 0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_dev.cpu())
+
+
 # ---------------------------------------------------------------- full-size workloads
 def _sample_units(units: int):
     return sorted({0, units // 2, units - 1})
