@@ -152,8 +152,10 @@ def oracle_sample(w: workloads.Workload, units: int, nthreads: int) -> tuple[flo
     edge-hops, nnz)."""
     import oracle
     gargs = w.graph_args()
-    row_ptr, col = (oracle.token_graph(**gargs) if w.kind == "token"
-                    else oracle.block_graph(**gargs))
+    if w.kind == "block":
+        row_ptr, col = oracle.block_graph(**gargs)
+    else:
+        row_ptr, col = oracle.token_graph(**gargs, causal=w.kind == "causal")
     nnz = int(row_ptr[-1])
     Q, K, V = synthetic.qkv(1, units, w.n, w.d, w.dtype, seed=w.seed)
     Qw, Kw, Vw = (oracle.widen(x, w.dtype) for x in (Q, K, V))
@@ -213,9 +215,9 @@ def run_ours(args, w) -> None:
     from sparse_long_sequence_gb300 import binding as dl
 
     # graph + inputs (each rank its own copy of the workload: weak scaling)
-    if w.kind == "token":
-        g = dl.diffuser_build_graph(w.n, w.r, w.n_globals, rand_per_row=w.rand_per_row,
-                                    seed=w.seed)
+    if w.kind in ("token", "causal"):
+        build = dl.diffuser_build_causal_graph if w.kind == "causal" else dl.diffuser_build_graph
+        g = build(w.n, w.r, w.n_globals, rand_per_row=w.rand_per_row, seed=w.seed)
     else:
         g = dl.diffuser_build_block_graph(w.n, w.block, w.window_blocks, w.rand_blocks,
                                           w.global_blocks, seed=w.seed)
@@ -313,6 +315,7 @@ def run_ours(args, w) -> None:
     # launches (the tensor-core window kernel and the gather kernel), so the
     # hop's device time is their sum, per hop
     hop_ms = prof["hop"][0] + prof.get("gather", (0.0, 0))[0]
+    band = prof.get("gather", (0.0, 0))[1] > 0
     n_hops = args.steps * w.hops
     peak, peak_kind = measured_peaks()
     roofline = None
@@ -322,7 +325,8 @@ def run_ours(args, w) -> None:
         traffic = hop_kernel_traffic(w.name)
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "traffic": traffic,
-                    "kernel": "diffusion hop (window tcgen05 kernel + gather kernel)",
+                    "kernel": ("diffusion hop (window tcgen05 kernel + gather kernel)" if band
+                               else "diffusion hop (CSR SIMT kernel)"),
                     "peak_kind": peak_kind,
                     "algorithmic_bytes_per_hop": model["per_hop_launch"],
                     "mean_hop_ms": hop_ms / n_hops}
@@ -345,7 +349,8 @@ def run_ours(args, w) -> None:
             "config": {**w.describe(), "nnz": g.nnz, "units_per_gpu": w.units,
                        "parallelism": f"dp{world}" if world > 1 else "single GPU",
                        "l2": "flushed between steps (256 MB write outside the timed events)",
-                       "arith": "A and Z_k as bf16 hi + lo pairs on the tensor cores (window, globals), fp32 gathers and accumulation"},
+                       "arith": ("A and Z_k as bf16 hi + lo pairs on the tensor cores (window, globals), "
+                                 "fp32 gathers and accumulation" if band else "fp32 SIMT (CSR path)")},
             "e2e": {"value": world * edge_hops / (t_e2e / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": 3 * io_bytes, "d2h_bytes_per_step": io_bytes},
             "roofline": roofline,

@@ -118,7 +118,8 @@ DIFFUSER_API int diffuser_build_graph(int64_t n, int32_t r, int32_t n_globals, c
  * with the same draws as diffuser_build_graph; a draw that lands after i is
  * dropped, not redrawn.  Every row holds its own position, so no softmax row
  * is empty.  Arguments, ownership and errors: as diffuser_build_graph.  The
- * forward over a causal graph takes the general CSR path.
+ * forward picks its path as for diffuser_build_graph; on the band path a
+ * tile reads only the key chunks up to its last row.
  */
 DIFFUSER_API int diffuser_build_causal_graph(int64_t n, int32_t r, int32_t n_globals,
                                 const int32_t* global_idx, int32_t rand_per_row,
@@ -283,7 +284,7 @@ typedef enum {
  * default is DIFFUSER_PATH_AUTO).  The band path serves token graphs with
  * bf16 I/O, window radius >= 8 and at most 32 globals; it stores the weights
  * in a decomposed window/global/extra layout and runs the window part of
- * every hop on tcgen05 tensor cores (3xTF32 split, fp32 accumulation).
+ * every hop on tcgen05 tensor cores (bf16 hi + lo split, fp32 accumulation).
  * The workspace size depends on the path: query diffuser_workspace_size
  * after changing it.  Errors: INVALID_ARG for an unknown path.
  */

@@ -65,6 +65,22 @@ __host__ __device__ constexpr int gc_offset(int t, int s, int g16) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Window [lo, hi] of row i: [i - r, i + r] cut to [0, n), or [i - r, i] on the
+// causal graph (the r+1 history positions; "1.2.1 Static sparsity", sec 1.1).
+__device__ __forceinline__ void window_of(const BandPlan& P, int64_t i, int64_t& lo, int64_t& hi) {
+    const int64_t up = P.causal ? 0 : P.r;
+    lo = i - P.r < 0 ? 0 : i - P.r;
+    hi = i + up > P.n - 1 ? P.n - 1 : i + up;
+}
+
+// Whether a non-global row with window [lo, hi] reads the global at j through
+// the out-of-window globals' weights: j outside the window and, on the causal
+// graph, not after the row (Diffuser notes sec 2.6: A lower-triangular).
+__device__ __forceinline__ bool reads_global_outside(const BandPlan& P, int64_t j, int64_t lo,
+                                                     int64_t hi) {
+    return j < lo || (j > hi && !P.causal);
+}
+
 // Pointers into the band layout of the workspace (see plan_band_layout).
 struct Weights {
     __nv_bfloat16* A_band;   // units x band_unit bytes

@@ -590,8 +590,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int64_t i = i0 + t;
             w.jb = i0 - P.r64;
             w.ok = i < P.n && !a.is_global[i < P.n ? i : 0];
-            w.lo = i - P.r < 0 ? 0 : i - P.r;
-            w.hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+            band::window_of(P, i, w.lo, w.hi);
             w.urow = (size_t)u * P.n + (w.ok ? i : 0);
             w.b2 = w.ok ? __ldg(a.m_sparse + w.urow) * kLog2e : 0.f;
             return w;
@@ -1122,17 +1121,21 @@ band::Weights band_weights(char* ws, const BandLayout& L) {
 }
 
 bool band_plan(const diffuser_graph* g, BandPlan* p) {
-    if (g->kind != kTokenGraph || g->causal || g->r < 8 || g->n_globals > kBandMaxGlobals)
-        return false;
+    if (g->kind != kTokenGraph || g->r < 8 || g->n_globals > kBandMaxGlobals) return false;
     p->n = g->n;
     p->r = g->r;
+    p->causal = g->causal ? 1 : 0;
     p->r64 = (g->r + kChunkKeys - 1) / kChunkKeys * kChunkKeys;
     p->g = g->n_globals;
     p->g_pad = (g->n_globals + 3) / 4 * 4;
     if (p->g_pad == 0) p->g_pad = 4;
     p->g16 = (g->n_globals + 15) / 16 * 16;
     p->tiles = (int32_t)((g->n + kTileRows - 1) / kTileRows);
-    p->chunks = (int32_t)((p->r64 + kTileRows + g->r + kChunkKeys - 1) / kChunkKeys);
+    // keys i0 - r64 .. i0 + 127 + (the window's upper radius: r, or 0 when causal),
+    // in an even number of 64-key chunks (the hop kernel takes them in pairs)
+    const int64_t up = g->causal ? 0 : g->r;
+    p->chunks = (int32_t)((p->r64 + kTileRows + up + kChunkKeys - 1) / kChunkKeys);
+    p->chunks += p->chunks & 1;
     p->band_unit = (size_t)p->tiles * p->chunks * band::kChunkImageBytes;
     return true;
 }

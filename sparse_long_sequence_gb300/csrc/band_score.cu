@@ -494,8 +494,8 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int64_t jb = i0 - P.r64;
             const int64_t i = i0 + t;
             const bool row_ok = i < P.n && !a.gr.is_global[i < P.n ? i : 0];
-            const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
-            const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+            int64_t lo, hi;
+            band::window_of(P, i, lo, hi);
             // this tile's weight image in global memory; a chunk's image is built
             // in shared memory (row t of a plane at 1024 (t / 8) + 128 (t % 8),
             // 16-byte slot q of the row at q ^ (t % 8)) and written by one bulk copy
@@ -519,7 +519,8 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     for (int sl = 0; sl < kBandMaxGlobals; ++sl) {
                         if (sl < P.g) {
                             const int64_t j = sGpos[sl];
-                            if (row_ok && (j < lo || j > hi)) m = fmaxf(m, gs[sl] * kScale);
+                            if (row_ok && band::reads_global_outside(P, j, lo, hi))
+                                m = fmaxf(m, gs[sl] * kScale);
                         }
                     }
                     if (quad == 0) global_row_scores(a, u, i0, lt, hcol, lane, tmem, full_GR, empty_GR, status);
@@ -623,7 +624,7 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         for (int h2 = 0; h2 < 2; ++h2) {
                             const int sl = 8 * q8 + 2 * p2 + h2;
                             const int64_t j = sGpos[sl < P.g ? sl : 0];
-                            x[h2] = (row_ok && sl < P.g && (j < lo || j > hi))
+                            x[h2] = (row_ok && sl < P.g && band::reads_global_outside(P, j, lo, hi))
                                         ? ptx::ex2_approx(fmaf(gs[sl], a_sc, -b2)) : 0.f;
                             lsum += x[h2];
                         }
@@ -656,10 +657,10 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 }
 
 // ---------------------------------------------------------------- global rows' weights
-// One CTA per (unit, global row s): the row's max and sum of exp over all n
-// keys (fixed-order tree reductions), then A_gr = exp(s - max) / sum in place
-// and row s of every tile's global-row operand image (hi / lo bf16; keys past
-// n are 0).
+// One CTA per (unit, global row s): the row's max and sum of exp over the keys
+// it reads (all n; on the causal graph 0 .. its own position), by fixed-order
+// tree reductions, then A_gr = exp(s - max) / sum in place and row s of every
+// tile's global-row operand image (hi / lo bf16; keys it does not read are 0).
 constexpr int kNormThreads = 256;
 
 __global__ void __launch_bounds__(kNormThreads)
@@ -670,8 +671,9 @@ score_global_norm_kernel(ScoreArgs a) {
     const int sl = (int)(blockIdx.x - u * P.g);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float* row = a.w.A_gr + ((size_t)u * P.g + sl) * P.n;
+    const int64_t nread = P.causal ? (int64_t)a.gr.globals[sl] + 1 : P.n;   // keys 0 .. nread-1
     float mx = -INFINITY;
-    for (int64_t j = tid; j < P.n; j += kNormThreads) mx = fmaxf(mx, row[j]);
+    for (int64_t j = tid; j < nread; j += kNormThreads) mx = fmaxf(mx, row[j]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if (lane == 0) red[warp] = mx;
@@ -681,7 +683,7 @@ score_global_norm_kernel(ScoreArgs a) {
     for (int w = 1; w < kNormThreads / 32; ++w) mx = fmaxf(mx, red[w]);
     __syncthreads();
     float l = 0.f;
-    for (int64_t j = tid; j < P.n; j += kNormThreads) l += expf(row[j] - mx);
+    for (int64_t j = tid; j < nread; j += kNormThreads) l += expf(row[j] - mx);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
     if (lane == 0) red[warp] = l;
@@ -697,10 +699,8 @@ score_global_norm_kernel(ScoreArgs a) {
     const int64_t nkeys = (int64_t)P.tiles * kTileRows;
     for (int64_t j = tid; j < nkeys; j += kNormThreads) {
         float w = 0.f;
-        if (j < P.n) {
-            w = expf(row[j] - mx) * inv;
-            row[j] = w;
-        }
+        if (j < nread) w = expf(row[j] - mx) * inv;
+        if (j < P.n) row[j] = w;
         const int64_t tile = j / kTileRows;
         const int jj = (int)(j - tile * kTileRows), h = jj >> 6, k = jj & 63;
         uint8_t* pe = a.w.A_gimg + (size_t)(u * P.tiles + tile) * band::kGImgBytes + h * 2 * band::kGImgPlaneBytes +
@@ -728,8 +728,8 @@ band_to_csr_kernel(ScoreArgs a, const int64_t* __restrict__ row_ptr,
         for (int64_t e = e0 + lane; e < e1; e += 32) o[e] = Ag[col[e]];
         return;
     }
-    const int64_t lo = i - P.r < 0 ? 0 : i - P.r;
-    const int64_t hi = i + P.r > P.n - 1 ? P.n - 1 : i + P.r;
+    int64_t lo, hi;
+    band::window_of(P, i, lo, hi);
     const int64_t tile = i / kTileRows, t = i - tile * kTileRows;
     const int64_t jb = tile * kTileRows - P.r64;       // first key of the tile's chunk grid
     const float inv = a.w.inv_l[(size_t)u * P.n + i];

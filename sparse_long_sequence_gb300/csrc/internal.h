@@ -25,11 +25,12 @@ enum GraphKind { kTokenGraph = 0, kBlockGraph = 1 };
 struct BandPlan {
     int64_t n;          // sequence length
     int32_t r;          // window radius
+    int32_t causal;     // 1: causal graph (window [i - r, i]; a row reads globals g <= i only)
     int32_t r64;        // the radius rounded up to a multiple of 64 (start of a tile's key chunks)
     int32_t g, g_pad;   // number of globals, padded to a multiple of 4
     int32_t g16;        // g rounded up to 16 (the K of the out-of-window globals' MMA), 0 if g = 0
     int32_t tiles;      // 128-row tiles per unit
-    int32_t chunks;     // 64-key chunks per tile
+    int32_t chunks;     // 64-key chunks per tile (even)
     size_t band_unit;   // bytes of one unit's band weights (tiles x chunks x 32 KB)
 };
 

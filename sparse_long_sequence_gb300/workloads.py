@@ -18,7 +18,7 @@ class Workload:
     n: int
     d: int
     dtype: str                    # "fp32" | "bf16"
-    kind: str                     # "token" | "block"
+    kind: str                     # "token" | "causal" (token graph cut to j <= i) | "block"
     r: int = 0                    # token graph: window radius
     n_globals: int = 0            # token graph: globals at positions 0..g-1
     rand_per_row: int = 0         # token graph: random draws per row
@@ -36,7 +36,7 @@ class Workload:
         return self.B * self.H
 
     def graph_args(self) -> dict:
-        if self.kind == "token":
+        if self.kind in ("token", "causal"):
             return dict(n=self.n, r=self.r, n_globals=self.n_globals,
                         rand_per_row=self.rand_per_row, seed=self.seed)
         return dict(n=self.n, block=self.block, window_blocks=self.window_blocks,
@@ -62,4 +62,10 @@ LONG = Workload("long_bf16_b1h16_n16384", 1, 16, 16384, 64, "bf16", "token", r=2
                 n_globals=32, rand_per_row=32)
 
 ALL = (TINY, TEXT, LRA, BIGBIRD, LONG)
-BY_NAME = {w.name: w for w in ALL}
+
+# The causal variant of the text workload: the same sizes on the lower-triangular
+# graph that autoregressive use needs (Diffuser notes sec 2.6).
+CAUSAL_TEXT = Workload("causal_text_bf16_b2h12_n4096", 2, 12, 4096, 64, "bf16", "causal", r=256,
+                       n_globals=16, rand_per_row=32)
+VARIANTS = (CAUSAL_TEXT,)
+BY_NAME = {w.name: w for w in ALL + VARIANTS}

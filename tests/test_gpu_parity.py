@@ -183,12 +183,14 @@ def test_forward_block_graph_small(dl, args, dtype):
     check_output(to_f64(out), ref, dtype)
 
 
+@pytest.mark.parametrize("causal", [False, True], ids=["bidirectional", "causal"])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-def test_attention_weights_parity(dl, dtype):
+def test_attention_weights_parity(dl, dtype, causal):
     import torch
     B, H, n = 1, 3, 600
-    g = dl.diffuser_build_graph(n, 40, 4, rand_per_row=12, seed=0)
-    o_ptr, o_col = oracle.token_graph(n, 40, 4, 12, seed=0)
+    build = dl.diffuser_build_causal_graph if causal else dl.diffuser_build_graph
+    g = build(n, 40, 4, rand_per_row=12, seed=0)
+    o_ptr, o_col = oracle.token_graph(n, 40, 4, 12, seed=0, causal=causal)
     Q, K, _ = synthetic.qkv(B, H, n, 64, dtype, seed=2)
     A = dl.diffuser_attention_weights(to_device(Q, dtype), to_device(K, dtype), g)
     torch.cuda.synchronize()
@@ -199,14 +201,17 @@ def test_attention_weights_parity(dl, dtype):
         np.testing.assert_allclose(A[u], ref, rtol=2e-5, atol=1e-8)
 
 
+@pytest.mark.parametrize("causal", [False, True], ids=["bidirectional", "causal"])
 @pytest.mark.parametrize("case", [(1, 2, 300, 8, 3, 5), (2, 3, 1000, 64, 8, 16),
-                                  (1, 2, 777, 33, 0, 7), (1, 1, 4096, 256, 16, 32)],
+                                  (1, 2, 777, 33, 0, 7), (1, 1, 4096, 256, 16, 32),
+                                  (1, 2, 650, 150, 3, 8)],
                          ids=lambda c: "B%dH%dn%dr%dg%dR%d" % c)
-def test_band_path_matches_csr_path(dl, case):
+def test_band_path_matches_csr_path(dl, case, causal):
     # the tensor-core band path and the general CSR path on the same inputs
     import torch
     B, H, n, r, gn, R = case
-    g = dl.diffuser_build_graph(n, r, gn, rand_per_row=R, seed=3)
+    build = dl.diffuser_build_causal_graph if causal else dl.diffuser_build_graph
+    g = build(n, r, gn, rand_per_row=R, seed=3)
     Q, K, V = synthetic.qkv(B, H, n, 64, "bf16", seed=11)
     Qd, Kd, Vd = (to_device(x, "bf16") for x in (Q, K, V))
     try:
@@ -217,7 +222,7 @@ def test_band_path_matches_csr_path(dl, case):
     out = to_f64(dl.diffuser_forward(Qd, Kd, Vd, g, 5, 0.1))
     torch.cuda.synchronize()
     assert dl.diffuser_graph_status(g) == 0
-    o_ptr, o_col = oracle.token_graph(n, r, gn, R, seed=3)
+    o_ptr, o_col = oracle.token_graph(n, r, gn, R, seed=3, causal=causal)
     oref = oracle.forward(oracle.widen(Q, "bf16"), oracle.widen(K, "bf16"),
                           oracle.widen(V, "bf16"), o_ptr, o_col, 5, 0.1, nthreads=4)
     check_output(out, oref, "bf16")
@@ -366,6 +371,7 @@ def test_causal_forward_small(dl, case, dtype):
     torch.cuda.synchronize()
     ref = oracle.forward(oracle.widen(Q, dtype), oracle.widen(K, dtype), oracle.widen(V, dtype),
                          o_ptr, o_col, hops, alpha, nthreads=4)
+    assert dl.diffuser_graph_status(g) == 0
     check_output(to_f64(out), ref, dtype)
     if alpha == 1.0:
         np.testing.assert_array_equal(to_f64(out), oracle.widen(V, dtype))
@@ -384,6 +390,7 @@ def test_causal_forward_never_reads_the_future(dl):
     V2[:, :, p] += 1.0
     pert = dl.diffuser_forward(Q, K, V2, g, 5, 0.1)
     torch.cuda.synchronize()
+    assert dl.diffuser_graph_status(g) == 0
     assert torch.equal(base[:, :, :p], pert[:, :, :p])
     assert not torch.equal(base[:, :, p:], pert[:, :, p:])
     assert torch.equal(base[:, :, 0], V[:, :, 0])
