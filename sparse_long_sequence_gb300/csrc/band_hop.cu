@@ -863,9 +863,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }
 
 // ---------------------------------------------------------------- sparse part of a hop
-// Persistent, 8 warps per CTA.  The rows of all units are split evenly over the
-// quarter-warps of the grid (random extras per row vary little, so equal rows
-// are equal work; global rows carry none).  A quarter walks its rows in
+// Persistent, 8 warps per CTA.  The rows of all units are split over the
+// quarter-warps of the grid in contiguous ranges of equal cost, a row costing
+// kRowCost plus its number of extras (on the causal graph a row keeps only the
+// draws that land before it, so late rows carry far more than early ones;
+// global rows carry none).  A quarter walks its rows in
 // windows of up to kWinRows rows of one unit, whose extras are one contiguous
 // stretch of the extras list: it streams that stretch kB slots at a time
 // (every slot's Z_k row in flight at once) while the indices and weights of
@@ -876,6 +878,24 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // whole 128-byte lines of the gathered rows.
 constexpr int kGThreadsG = 256;
 constexpr int kWinRows = 16;
+constexpr int64_t kRowCost = 2;      // a row's fixed work (its P_i store, its window slots), in extras
+
+// First row (over all units, u n + i) of quarter q of nq: the smallest row
+// whose cost prefix  u (kRowCost n + nx) + kRowCost i + x_ptr[i]  reaches
+// q / nq of the total.  Monotone in q; q = nq gives units * n.  (The products
+// stay far inside int64: nq < 2^15 and the total cost < 2^40.)
+__device__ __forceinline__ int64_t gather_first_row(const HopArgs& a, int64_t q, int64_t nq) {
+    const int64_t n = a.plan.n;
+    const int64_t per_unit = kRowCost * n + a.nx;
+    const int64_t target = q * (a.units * per_unit) / nq;
+    const int64_t u = target / per_unit, rem = target - u * per_unit;
+    int64_t lo = 0, hi = n;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (kRowCost * mid + __ldg(a.x_ptr + mid) < rem) lo = mid + 1; else hi = mid;
+    }
+    return u * n + lo;
+}
 
 template <bool kHop0, int kB, int kMinBlocks>
 __global__ void __launch_bounds__(kGThreadsG, kMinBlocks)
@@ -890,8 +910,7 @@ hop_gather_kernel(HopArgs a) {
     const int qi = 4 * warp + (lane >> 3);
     const unsigned qmask = 0xFFu << (lane & 24);  // this quarter's lanes
     const int64_t nq = (int64_t)gridDim.x * 32, q = (int64_t)blockIdx.x * 32 + qi;
-    const int64_t rows_total = a.units * P.n;
-    const int64_t R1 = (q + 1) * rows_total / nq;
+    const int64_t R1 = gather_first_row(a, q + 1, nq);
     int* ss = sStart[qi];
     float* sm = sMax[qi];
     uint8_t* sg = sGlob[qi];
@@ -907,7 +926,7 @@ hop_gather_kernel(HopArgs a) {
         }
         __syncwarp();     // reconverge: the quarters below synchronize only among themselves
     }
-    for (int64_t Rw = q * rows_total / nq; Rw < R1;) {
+    for (int64_t Rw = gather_first_row(a, q, nq); Rw < R1;) {
         const int64_t u = Rw / P.n;
         const int64_t iw = Rw - u * P.n;
         int64_t cnt64 = R1 - Rw;
