@@ -864,14 +864,16 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
 // ---------------------------------------------------------------- sparse part of a hop
 // Persistent, 8 warps per CTA.  The rows of all units are split over the
-// quarter-warps of the grid in contiguous ranges of equal cost, a row costing
-// kRowCost plus its number of extras (on the causal graph a row keeps only the
-// draws that land before it, so late rows carry far more than early ones;
-// global rows carry none).  A quarter walks its rows in
-// windows of up to kWinRows rows of one unit, whose extras are one contiguous
-// stretch of the extras list: it streams that stretch kB slots at a time
-// (every slot's Z_k row in flight at once) while the indices and weights of
-// the next kB slots load, one slot per lane, and reach the quarter by shuffles.
+// quarter-warps of the grid in contiguous ranges: of equal row count on the
+// bidirectional graph (random extras per row vary little, so equal rows are
+// equal work; global rows carry none), and of equal cost on the causal graph,
+// where a row keeps only the draws that land before it, so late rows carry
+// far more extras than early ones (a row costs kRowCost plus its extras).
+// A quarter walks its rows in windows of up to kWinRows rows of one unit,
+// whose extras are one contiguous stretch of the extras list: it streams that
+// stretch kB slots at a time (every slot's Z_k row in flight at once) while the
+// indices and weights of the next kB slots load, one slot per lane, and reach
+// the quarter by shuffles.
 // On leaving a row it writes the row's sum P_i (zeros for a row without
 // extras; nothing for a global row).  Lane l of a quarter owns features
 // 4 l .. 4 l + 3 and 32 + 4 l .. 32 + 4 l + 3, so each load instruction reads
@@ -880,21 +882,47 @@ constexpr int kGThreadsG = 256;
 constexpr int kWinRows = 16;
 constexpr int64_t kRowCost = 2;      // a row's fixed work (its P_i store, its window slots), in extras
 
-// First row (over all units, u n + i) of quarter q of nq: the smallest row
-// whose cost prefix  u (kRowCost n + nx) + kRowCost i + x_ptr[i]  reaches
-// q / nq of the total.  Monotone in q; q = nq gives units * n.  (The products
+// Causal graph: the first rows (over all units, u n + i) of quarters q and q + 1
+// of nq, each the smallest row whose cost prefix u (kRowCost n + nx) +
+// kRowCost i + x_ptr[i] reaches q / nq (resp. (q + 1) / nq) of the total.
+// Monotone in q; q = nq gives units * n.  The quarter's 8 lanes run both
+// searches together, 8 probes a round (about log9 n rounds of one load
+// each).  All 8 lanes of the quarter must be converged here.  (The products
 // stay far inside int64: nq < 2^15 and the total cost < 2^40.)
-__device__ __forceinline__ int64_t gather_first_row(const HopArgs& a, int64_t q, int64_t nq) {
+__device__ __forceinline__ void causal_row_range(const HopArgs& a, int64_t q, int64_t nq, int ql,
+                                                 unsigned qmask, int shift, int64_t& R0,
+                                                 int64_t& R1) {
     const int64_t n = a.plan.n;
-    const int64_t per_unit = kRowCost * n + a.nx;
-    const int64_t target = q * (a.units * per_unit) / nq;
-    const int64_t u = target / per_unit, rem = target - u * per_unit;
-    int64_t lo = 0, hi = n;
-    while (lo < hi) {
-        const int64_t mid = (lo + hi) >> 1;
-        if (kRowCost * mid + __ldg(a.x_ptr + mid) < rem) lo = mid + 1; else hi = mid;
+    const int64_t per_unit = kRowCost * n + a.nx, total = a.units * per_unit;
+    const int64_t t0 = q * total / nq, t1 = (q + 1) * total / nq;
+    const int64_t u0 = t0 / per_unit, rem0 = t0 - u0 * per_unit;
+    const int64_t u1 = t1 / per_unit, rem1 = t1 - u1 * per_unit;
+    // the answer i lies in [lo, hi]; cost(i) >= rem is false below it, true from it on
+    int64_t lo0 = 0, hi0 = n, lo1 = 0, hi1 = n;
+    while (lo0 < hi0 || lo1 < hi1) {
+        const int64_t p0 = lo0 + (hi0 - lo0) * (ql + 1) / 9;   // < hi0 while lo0 < hi0
+        const int64_t p1 = lo1 + (hi1 - lo1) * (ql + 1) / 9;
+        const bool f0 = lo0 < hi0 && kRowCost * p0 + __ldg(a.x_ptr + p0) >= rem0;
+        const bool f1 = lo1 < hi1 && kRowCost * p1 + __ldg(a.x_ptr + p1) >= rem1;
+        const unsigned b0 = (__ballot_sync(qmask, f0) >> shift) & 0xFFu;
+        const unsigned b1 = (__ballot_sync(qmask, f1) >> shift) & 0xFFu;
+        if (lo0 < hi0) {
+            const int k = 8 - __popc(b0);                          // probes below the answer
+            const int64_t plo = lo0 + (hi0 - lo0) * k / 9;         // probe k - 1 (if k > 0)
+            const int64_t phi = lo0 + (hi0 - lo0) * (k + 1) / 9;   // probe k (if k < 8)
+            if (k > 0) lo0 = plo + 1;
+            if (k < 8) hi0 = phi;
+        }
+        if (lo1 < hi1) {
+            const int k = 8 - __popc(b1);
+            const int64_t plo = lo1 + (hi1 - lo1) * k / 9;
+            const int64_t phi = lo1 + (hi1 - lo1) * (k + 1) / 9;
+            if (k > 0) lo1 = plo + 1;
+            if (k < 8) hi1 = phi;
+        }
     }
-    return u * n + lo;
+    R0 = u0 * n + lo0;
+    R1 = u1 * n + lo1;
 }
 
 template <bool kHop0, int kB, int kMinBlocks>
@@ -910,7 +938,14 @@ hop_gather_kernel(HopArgs a) {
     const int qi = 4 * warp + (lane >> 3);
     const unsigned qmask = 0xFFu << (lane & 24);  // this quarter's lanes
     const int64_t nq = (int64_t)gridDim.x * 32, q = (int64_t)blockIdx.x * 32 + qi;
-    const int64_t R1 = gather_first_row(a, q + 1, nq);
+    int64_t R0, R1;
+    if (P.causal) {
+        causal_row_range(a, q, nq, ql, qmask, lane & 24, R0, R1);
+    } else {
+        const int64_t rows_total = a.units * P.n;
+        R0 = q * rows_total / nq;
+        R1 = (q + 1) * rows_total / nq;
+    }
     int* ss = sStart[qi];
     float* sm = sMax[qi];
     uint8_t* sg = sGlob[qi];
@@ -926,7 +961,7 @@ hop_gather_kernel(HopArgs a) {
         }
         __syncwarp();     // reconverge: the quarters below synchronize only among themselves
     }
-    for (int64_t Rw = gather_first_row(a, q, nq); Rw < R1;) {
+    for (int64_t Rw = R0; Rw < R1;) {
         const int64_t u = Rw / P.n;
         const int64_t iw = Rw - u * P.n;
         int64_t cnt64 = R1 - Rw;
