@@ -83,6 +83,10 @@ def _load():
         lib.oracle_forward.argtypes = [_f64p, _f64p, _f64p, ctypes.c_int64, ctypes.c_int64,
                                        ctypes.c_int32, _i64p, _i32p, ctypes.c_int32, ctypes.c_double,
                                        _f64p, ctypes.c_int32]
+        lib.oracle_backward.restype = ctypes.c_int
+        lib.oracle_backward.argtypes = [_f64p, _f64p, _f64p, _f64p, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int32, _i64p, _i32p, ctypes.c_int32,
+                                        ctypes.c_double, _f64p, _f64p, _f64p]
         _lib = lib
         return lib
 
@@ -198,3 +202,19 @@ def forward(Q: np.ndarray, K: np.ndarray, V: np.ndarray, row_ptr: np.ndarray, co
                                   _p(np.ascontiguousarray(col, dtype=np.int32), _i32p),
                                   hops, alpha, _p(out, _f64p), max(1, int(nthreads))), "forward")
     return out
+
+
+def backward(Q: np.ndarray, K: np.ndarray, V: np.ndarray, dOut: np.ndarray, row_ptr: np.ndarray,
+             col: np.ndarray, hops: int, alpha: float):
+    """Gradients (dQ, dK, dV) of <dOut, Z_hops> over [units][n][d] float64 inputs (or [n][d])."""
+    Q, K, V, dOut = (np.ascontiguousarray(x, dtype=np.float64) for x in (Q, K, V, dOut))
+    units = int(np.prod(Q.shape[:-2])) if Q.ndim > 2 else 1
+    n, d = Q.shape[-2], Q.shape[-1]
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    _check(_load().oracle_backward(_p(Q, _f64p), _p(K, _f64p), _p(V, _f64p), _p(dOut, _f64p),
+                                   units, n, d,
+                                   _p(np.ascontiguousarray(row_ptr, dtype=np.int64), _i64p),
+                                   _p(np.ascontiguousarray(col, dtype=np.int32), _i32p),
+                                   hops, alpha, _p(dQ, _f64p), _p(dK, _f64p), _p(dV, _f64p)),
+           "backward")
+    return dQ, dK, dV

@@ -4,7 +4,8 @@
  * A plain, slow, fp64 CPU statement of what the Diffuser hot path computes:
  * the fixed sparse edge set (local window, global tokens, random edges, or the
  * BigBird block pattern), the row softmax over each row's allowed set, and K
- * personalized-PageRank (PPR) diffusion hops over those weights.
+ * personalized-PageRank (PPR) diffusion hops over those weights; and the
+ * gradient of that forward with respect to Q, K and V (the backward pass).
  *
  * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
  * load this library.  It shares no code, header, table or helper with the
@@ -15,7 +16,8 @@
  *        diffusion" (reading notes on arXiv 2210.11794v2):
  *        sec 2.1 eq S.1-S.5 (masked softmax weights), sec 2.2 (three edge
  *        kinds), sec 2.4 eq S.7 (PPR recursion), sec 2.5 (finite-K form),
- *        sec 2.6 (causal use: A lower-triangular).
+ *        sec 2.6 (training through the unrolled recursion; causal use: A
+ *        lower-triangular).
  *   [S]  "1.2.1 Static sparsity: Longformer, BigBird and sliding windows":
  *        sec 1 eq 1-4 (scores, mask, softmax, output), sec 1.1 eq 5-6
  *        (window; causal window of r+1 history positions), sec 1.2 eq 12
@@ -346,5 +348,91 @@ int oracle_forward(const double* Q, const double* K, const double* V,
         if (jobs[t].status != ORACLE_OK) status = jobs[t].status;
     free(jobs);
     free(th);
+    return status;
+}
+
+/*
+ * Backward pass through the unrolled recursion ([D] sec 2.6: training runs the
+ * same unrolled K-hop recursion, and the gradient flows back through every
+ * round of aggregation into the attention weights and from there into the
+ * scores).  For one unit, given dOut = dL/dZ_hops, the chain rule taken step
+ * by step in reverse order:
+ *   Z_{k+1} = (1 - alpha) A Z_k + alpha V:
+ *       dV   += alpha G_{k+1}
+ *       dA_e += (1 - alpha) G_{k+1}[i] . Z_k[j]         for each edge e = (i, j)
+ *       G_k   = (1 - alpha) A^T G_{k+1}
+ *   Z_0 = V:  dV += G_0
+ *   softmax over row i:  dS_e = A_e (dA_e - sum_{t in row i} A_t dA_t)
+ *   s_ij = q_i . k_j / sqrt(d):  dQ_i += dS_e k_j / sqrt(d),  dK_j += dS_e q_i / sqrt(d)
+ * with G_hops = dOut.  The forward states Z_0 .. Z_{hops-1} are kept (the
+ * plain store-everything form of automatic differentiation).
+ * Q, K, V, dOut, dQ, dK, dV: [units][n][d] contiguous; dQ, dK, dV are written.
+ */
+int oracle_backward(const double* Q, const double* K, const double* V,
+                    const double* dOut, int64_t units, int64_t n, int32_t d,
+                    const int64_t* row_ptr, const int32_t* col, int32_t hops,
+                    double alpha, double* dQ, double* dK, double* dV) {
+    if (units < 0 || n < 1 || d < 1 || hops < 0) return ORACLE_BAD_ARG;
+    const int64_t nnz = row_ptr[n];
+    const size_t nd = (size_t)n * (size_t)d;
+    const double scale = 1.0 / sqrt((double)d);
+    double* A = (double*)malloc(sizeof(double) * (size_t)(nnz > 0 ? nnz : 1));
+    double* dA = (double*)malloc(sizeof(double) * (size_t)(nnz > 0 ? nnz : 1));
+    double* Z = (double*)malloc(sizeof(double) * nd * (size_t)(hops > 0 ? hops : 1));
+    double* G = (double*)malloc(sizeof(double) * nd);
+    double* Gn = (double*)malloc(sizeof(double) * nd);
+    if (!A || !dA || !Z || !G || !Gn) {
+        free(A); free(dA); free(Z); free(G); free(Gn);
+        return ORACLE_NO_MEM;
+    }
+    int status = ORACLE_OK;
+    for (int64_t u = 0; u < units && status == ORACLE_OK; ++u) {
+        const double* q = Q + (size_t)u * nd;
+        const double* k = K + (size_t)u * nd;
+        const double* v = V + (size_t)u * nd;
+        double* dq = dQ + (size_t)u * nd;
+        double* dk = dK + (size_t)u * nd;
+        double* dv = dV + (size_t)u * nd;
+        oracle_attention_weights(q, k, n, d, row_ptr, col, A);
+        /* forward states Z_0 .. Z_{hops-1} */
+        for (int32_t h = 0; h < hops && status == ORACLE_OK; ++h)
+            status = oracle_diffuse(A, row_ptr, col, v, n, d, h, alpha, Z + (size_t)h * nd);
+        if (status != ORACLE_OK) break;
+        memcpy(G, dOut + (size_t)u * nd, sizeof(double) * nd);
+        memset(dv, 0, sizeof(double) * nd);
+        memset(dA, 0, sizeof(double) * (size_t)(nnz > 0 ? nnz : 1));
+        for (int32_t h = hops - 1; h >= 0; --h) {
+            const double* z = Z + (size_t)h * nd;          /* Z_h; G holds G_{h+1} */
+            for (size_t x = 0; x < nd; ++x) dv[x] += alpha * G[x];
+            memset(Gn, 0, sizeof(double) * nd);
+            for (int64_t i = 0; i < n; ++i) {
+                for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) {
+                    const int64_t j = col[e];
+                    double dot = 0.0;
+                    for (int32_t c = 0; c < d; ++c) dot += G[i * d + c] * z[j * d + c];
+                    dA[e] += (1.0 - alpha) * dot;
+                    for (int32_t c = 0; c < d; ++c)
+                        Gn[j * d + c] += (1.0 - alpha) * A[e] * G[i * d + c];
+                }
+            }
+            memcpy(G, Gn, sizeof(double) * nd);
+        }
+        for (size_t x = 0; x < nd; ++x) dv[x] += G[x];    /* Z_0 = V */
+        memset(dq, 0, sizeof(double) * nd);
+        memset(dk, 0, sizeof(double) * nd);
+        for (int64_t i = 0; i < n; ++i) {
+            double dot = 0.0;                               /* sum_t A_t dA_t over row i */
+            for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) dot += A[e] * dA[e];
+            for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) {
+                const int64_t j = col[e];
+                const double ds = A[e] * (dA[e] - dot) * scale;
+                for (int32_t c = 0; c < d; ++c) {
+                    dq[i * d + c] += ds * k[j * d + c];
+                    dk[j * d + c] += ds * q[i * d + c];
+                }
+            }
+        }
+    }
+    free(A); free(dA); free(Z); free(G); free(Gn);
     return status;
 }
