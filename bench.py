@@ -198,6 +198,25 @@ def run_reference(args, w) -> None:
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of x over the ranks of the default process group (x itself
+    with no group or one rank): every rank's replica must have finished."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, nnz: int, hops: int, world: int, ms: float) -> float:
+    """Edge-hops per second over all ranks: each rank runs its own replica of the
+    workload (weak scaling), and the job takes the slowest rank's time."""
+    return world * units_per_rank * nnz * hops / (ms / 1e3)
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_ours(args, w) -> None:
     import torch
@@ -280,11 +299,7 @@ def run_ours(args, w) -> None:
     torch.cuda.synchronize()
     prof = dl.diffuser_profile_end()
     prof_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    t_step = statistics.mean(step_ms)
-    if world > 1:
-        tt = torch.tensor([t_step], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = float(tt.item())
+    t_step = max_over_ranks(statistics.mean(step_ms), device="cuda")
 
     # ---- end to end through the host-buffer entry point
     Oh = torch.empty_like(Vp).pin_memory()
@@ -300,15 +315,10 @@ def run_ours(args, w) -> None:
         dl.diffuser_forward_host(Qp, Kp, Vp, g, w.hops, w.alpha, Oh, ws_h, stream=stream)
         stream.synchronize()
         e2e_ms.append(1e3 * (time.perf_counter() - t0))
-    t_e2e = statistics.mean(e2e_ms)
-    if world > 1:
-        tt = torch.tensor([t_e2e], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = max_over_ranks(statistics.mean(e2e_ms), device="cuda")
     assert torch.equal(Oh, out.cpu()), "end-to-end output differs from the device forward"
 
-    edge_hops = w.units * g.nnz * w.hops
-    value = world * edge_hops / (t_step / 1e3)
+    value = whole_job_rate(w.units, g.nnz, w.hops, world, t_step)
     io_bytes = w.units * w.n * w.d * (2 if w.dtype == "bf16" else 4)
     model = algorithmic_bytes(w, g.nnz)
     # the dominant kernel is the diffusion hop; on the band path one hop is two
@@ -351,7 +361,7 @@ def run_ours(args, w) -> None:
                        "l2": "flushed between steps (256 MB write outside the timed events)",
                        "arith": ("A and Z_k as bf16 hi + lo pairs on the tensor cores (window, globals), "
                                  "fp32 gathers and accumulation" if band else "fp32 SIMT (CSR path)")},
-            "e2e": {"value": world * edge_hops / (t_e2e / 1e3), "unit": UNIT,
+            "e2e": {"value": whole_job_rate(w.units, g.nnz, w.hops, world, t_e2e), "unit": UNIT,
                     "h2d_bytes_per_step": 3 * io_bytes, "d2h_bytes_per_step": io_bytes},
             "roofline": roofline,
             "whole_forward_hbm_frac": whole_frac,
