@@ -67,5 +67,9 @@ ALL = (TINY, TEXT, LRA, BIGBIRD, LONG)
 # graph that autoregressive use needs (Diffuser notes sec 2.6).
 CAUSAL_TEXT = Workload("causal_text_bf16_b2h12_n4096", 2, 12, 4096, 64, "bf16", "causal", r=256,
                        n_globals=16, rand_per_row=32)
-VARIANTS = (CAUSAL_TEXT,)
+# The text workload's pattern (r 256, 16 globals, 32 draws per row) over a length sweep
+# (n = 4096 is TEXT itself).
+SWEEP = tuple(Workload(f"text_bf16_b2h12_n{n}", 2, 12, n, 64, "bf16", "token", r=256,
+                       n_globals=16, rand_per_row=32) for n in (1024, 2048, 8192, 16384))
+VARIANTS = (CAUSAL_TEXT,) + SWEEP
 BY_NAME = {w.name: w for w in ALL + VARIANTS}

@@ -80,3 +80,22 @@ def test_reference_arm_line():
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "tiny_fp32_n512"
+
+
+def test_workload_registry():
+    sys.path.insert(0, ROOT)
+    from sparse_long_sequence_gb300 import workloads
+    import oracle
+    names = [w.name for w in workloads.ALL + workloads.VARIANTS]
+    assert len(names) == len(set(names)) == len(workloads.BY_NAME)
+    for w in workloads.BY_NAME.values():
+        assert w.kind in ("token", "causal", "block") and w.d == 64 and w.units >= 1
+        assert w.describe()["workload"] == w.name
+    # the sweep keeps the text pattern; its window part is the [S] eq 6 closed form
+    for w in workloads.SWEEP[:2]:
+        assert (w.r, w.n_globals, w.rand_per_row, w.B, w.H) == (256, 16, 32, 2, 12)
+        row_ptr, _ = oracle.token_graph(w.n, w.r, 0, 0)
+        assert row_ptr[-1] == w.n * (2 * w.r + 1) - w.r * (w.r + 1)
+    c = workloads.CAUSAL_TEXT
+    row_ptr, _ = oracle.token_graph(c.n, c.r, 0, 0, causal=True)
+    assert row_ptr[-1] == c.n * (c.r + 1) - c.r * (c.r + 1) // 2
