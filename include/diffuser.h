@@ -215,6 +215,38 @@ DIFFUSER_API int diffuser_forward_host(const void* Q, const void* K, const void*
                           float alpha, void* out, void* workspace, size_t workspace_bytes,
                           diffuser_stream stream);
 
+/*
+ * Backward pass ([D] sec 2.6: training runs the same unrolled K-hop
+ * recursion and the gradient flows back through every round of aggregation
+ * into the weights and the scores).  Given dOut = dL/dout of the forward with
+ * the same Q, K, V, graph, hops and alpha, writes the exact gradients
+ *   dV = sum over the hops of alpha G_{k+1}, plus G_0, where G_K = dOut and
+ *        G_k = (1 - alpha) A^T G_{k+1};
+ *   dA_ij = (1 - alpha) sum_k G_{k+1}[i] . Z_k[j];
+ *   dS_ij = A_ij (dA_ij - sum_t A_it dA_it);
+ *   dQ_i = sum_j dS_ij k_j / sqrt(d),  dK_j = sum_i dS_ij q_i / sqrt(d).
+ * The forward's weights and states Z_1 .. Z_{K-1} are recomputed inside the
+ * call.  The first backward on a graph also builds its transposed edge list
+ * (on the host, then a synchronous upload: 12 bytes per edge of device memory,
+ * held with the graph), so make that first call outside any stream capture.  All arithmetic is fp32 (the CSR kernels, for any graph); dQ, dK, dV
+ * are written in the I/O dtype.  Sums run in a fixed order: repeated calls
+ * give identical bits.  Launches count as SCORE (the recomputed weights, the
+ * softmax and score gradients) and HOP (the recomputed and reversed hops).
+ *
+ *   Q, K, V, dOut   device [B][H][n][d] in dtype, 16-byte aligned
+ *   dQ, dK, dV      device [B][H][n][d] in dtype, written; they may not overlap
+ *                   the inputs or each other
+ *   workspace       diffuser_backward_workspace_size bytes, 256-byte aligned:
+ *                   2 units nnz + (2 + max(K, 1)) units n 64 fp32 values
+ * Asynchronous on `stream`.  Errors: as diffuser_forward.
+ */
+DIFFUSER_API int diffuser_backward_workspace_size(const diffuser_graph* g, int64_t B, int64_t H,
+                                     int32_t d, int32_t dtype, int32_t hops, size_t* bytes);
+DIFFUSER_API int diffuser_backward(const void* Q, const void* K, const void* V, const void* dOut,
+                      int32_t dtype, int64_t B, int64_t H, int32_t d, const diffuser_graph* g,
+                      int32_t hops, float alpha, void* dQ, void* dK, void* dV, void* workspace,
+                      size_t workspace_bytes, diffuser_stream stream);
+
 /* ---------------------------------------------------------------- no-allocation forward */
 
 /*

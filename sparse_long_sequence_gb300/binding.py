@@ -57,6 +57,10 @@ def _load() -> ctypes.CDLL:
                                                    c.POINTER(c.c_size_t)]),
         "diffuser_forward_host": (c.c_int, [vp, vp, vp, i32, i64, i64, i32, vp, i32, f32, vp,
                                             vp, c.c_size_t, vp]),
+        "diffuser_backward_workspace_size": (c.c_int, [vp, i64, i64, i32, i32, i32,
+                                                       c.POINTER(c.c_size_t)]),
+        "diffuser_backward": (c.c_int, [vp, vp, vp, vp, i32, i64, i64, i32, vp, i32, f32, vp, vp,
+                                        vp, vp, c.c_size_t, vp]),
         "diffuser_attention_weights": (c.c_int, [vp, vp, i32, i64, i64, i32, vp, vp, vp,
                                                  c.c_size_t, vp]),
         "diffuser_diffuse_csr": (c.c_int, [vp, vp, vp, i32, i64, i64, i32, i32, f32, vp, vp,
@@ -225,6 +229,33 @@ def diffuser_forward(Q, K, V, g: Graph, hops: int, alpha: float, out=None, works
                                  g.handle, hops, alpha, out.data_ptr(), workspace.data_ptr(),
                                  workspace.numel(), _stream(stream)), "diffuser_forward")
     return out
+
+
+def diffuser_backward_workspace_size(g: Graph, B: int, H: int, d: int, dtype: int,
+                                     hops: int) -> int:
+    b = ctypes.c_size_t()
+    _check(_lib.diffuser_backward_workspace_size(g.handle, B, H, d, dtype, hops, ctypes.byref(b)),
+           "diffuser_backward_workspace_size")
+    return b.value
+
+
+def diffuser_backward(Q, K, V, dOut, g: Graph, hops: int, alpha: float, dQ=None, dK=None, dV=None,
+                      workspace=None, stream=None):
+    """Gradients (dQ, dK, dV) of <dOut, forward(Q, K, V)>; device tensors in one dtype."""
+    import torch
+    B, H, d = _shape(Q, g)
+    code = _dtype_code(Q)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    if workspace is None:
+        workspace = alloc_workspace(diffuser_backward_workspace_size(g, B, H, d, code, hops),
+                                    Q.device)
+    _check(_lib.diffuser_backward(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dOut.data_ptr(), code,
+                                  B, H, d, g.handle, hops, alpha, dQ.data_ptr(), dK.data_ptr(),
+                                  dV.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                  _stream(stream)), "diffuser_backward")
+    return dQ, dK, dV
 
 
 def diffuser_forward_host(Q, K, V, g: Graph, hops: int, alpha: float, out, workspace,

@@ -641,6 +641,9 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_gslot);
     cudaFree(g->d_x_ptr);
     cudaFree(g->d_x_col);
+    cudaFree(g->d_t_ptr);
+    cudaFree(g->d_t_row);
+    cudaFree(g->d_t_edge);
     cudaFree(g->d_status);
     dfs::destroy_replay_cache(g->replay);
     delete g;
@@ -660,6 +663,63 @@ int diffuser_forward(const void* Q, const void* K, const void* V, int32_t dtype,
     try {
         return forward_device(Q, K, V, dtype, B, H, d, g, hops, alpha, out, workspace,
                               workspace_bytes, stream);
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+int diffuser_backward_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32_t d,
+                                     int32_t dtype, int32_t hops, size_t* bytes) {
+    int st = check_shape(g, B, H, d, dtype);
+    if (st) return st;
+    if (!bytes) return fail(DIFFUSER_ERR_INVALID_ARG, "bytes is NULL");
+    if (hops < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "hops must be >= 0");
+    BwdLayout L;
+    if ((st = plan_backward_layout(g, B * H, hops, &L))) return st;
+    *bytes = L.total;
+    return DIFFUSER_OK;
+}
+
+int diffuser_backward(const void* Q, const void* K, const void* V, const void* dOut, int32_t dtype,
+                      int64_t B, int64_t H, int32_t d, const diffuser_graph* g, int32_t hops,
+                      float alpha, void* dQ, void* dK, void* dV, void* workspace,
+                      size_t workspace_bytes, diffuser_stream stream) {
+    try {
+        int st = check_shape(g, B, H, d, dtype);
+        if (st) return st;
+        if (!Q || !K || !V || !dOut || !dQ || !dK || !dV)
+            return fail(DIFFUSER_ERR_INVALID_ARG, "a tensor pointer is NULL");
+        if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dOut) || !aligned16(dQ) ||
+            !aligned16(dK) || !aligned16(dV))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+        if (hops < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "hops must be >= 0");
+        if (!(alpha >= 0.f && alpha <= 1.f))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "alpha must lie in [0, 1]");
+        const size_t bytes = io_bytes(g, B, H, dtype);
+        const void* in[4] = {Q, K, V, dOut};
+        void* grads[3] = {dQ, dK, dV};
+        for (int x = 0; x < 3; ++x) {
+            for (int y = 0; y < 4; ++y)
+                if (overlaps(grads[x], bytes, in[y], bytes))
+                    return fail(DIFFUSER_ERR_INVALID_ARG, "a gradient overlaps an input");
+            for (int y = x + 1; y < 3; ++y)
+                if (overlaps(grads[x], bytes, grads[y], bytes))
+                    return fail(DIFFUSER_ERR_INVALID_ARG, "the gradients overlap");
+        }
+        BwdLayout L;
+        if ((st = plan_backward_layout(g, B * H, hops, &L))) return st;
+        if ((st = check_workspace_bytes(L.total, workspace, workspace_bytes))) return st;
+        if ((st = check_device(g))) return st;
+        {
+            // the transposed graph, built by the first backward on this graph; the
+            // graph stays logically immutable (the lock orders the one-time build)
+            static std::mutex mu;
+            std::lock_guard<std::mutex> lock(mu);
+            if (!g->d_t_ptr && (st = build_transposed_graph(const_cast<diffuser_graph*>(g)))) return st;
+        }
+        return launch_backward_csr(g, B * H, Q, K, V, dOut, dtype, hops, alpha, dQ, dK, dV,
+                                   static_cast<char*>(workspace), L,
+                                   static_cast<cudaStream_t>(stream));
     } catch (...) {
         return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
     }

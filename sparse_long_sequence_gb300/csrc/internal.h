@@ -43,6 +43,15 @@ struct BandLayout {
     size_t gpart, inv_l, m_sparse, gstat, total;
 };
 
+// Byte offsets of the backward pass's workspace regions (fp32 throughout).
+struct BwdLayout {
+    size_t a, da;       // weights A and their gradient dA (then dS), [units][nnz]
+    size_t dv;          // the dV accumulator, [units][n][64]
+    size_t g[2];        // G_k, the gradient reaching Z_k, ping-pong, [units][n][64]
+    size_t z, z_stride; // Z_1 .. Z_{K-1}, each [units][n][64]
+    size_t total;
+};
+
 }  // namespace dfs
 
 namespace dfs {
@@ -70,6 +79,10 @@ struct diffuser_graph {
     int64_t nx = 0;                   // number of such "extra" edges
     int64_t* d_x_ptr = nullptr;       // [n+1]
     int32_t* d_x_col = nullptr;       // [nx], ascending within a row
+    // transposed graph (the backward pass): incoming edges of each key, rows ascending
+    int64_t* d_t_ptr = nullptr;       // [n+1]
+    int32_t* d_t_row = nullptr;       // [nnz] row i of each incoming edge
+    int64_t* d_t_edge = nullptr;      // [nnz] its CSR edge id
     int* d_status = nullptr;          // device status word written by kernels (0 = ok)
     dfs::ReplayCache* replay = nullptr;   // captured band-path forwards (see abi.cu)
     // host copy of the CSR
@@ -123,6 +136,14 @@ int launch_score_csr(const CsrArgs& a, const void* Q, const void* K, int32_t dty
 int launch_hop_csr(const CsrArgs& a, const float* A, const void* src, bool src_is_io,
                    const void* V, void* dst, bool dst_is_io, int32_t dtype, float alpha,
                    cudaStream_t stream);
+
+// ---- backward pass (backward.cu): CSR path, either I/O dtype ----------------
+int build_transposed_graph(diffuser_graph* g);   // from the host CSR copy
+int plan_backward_layout(const diffuser_graph* g, int64_t units, int32_t hops, BwdLayout* L);
+int launch_backward_csr(const diffuser_graph* g, int64_t units, const void* Q, const void* K,
+                        const void* V, const void* dOut, int32_t dtype, int32_t hops, float alpha,
+                        void* dQ, void* dK, void* dV, char* ws, const BwdLayout& L,
+                        cudaStream_t stream);
 
 // ---- band path (band_score.cu, band_hop.cu): token graphs, bf16 I/O --------
 bool band_plan(const diffuser_graph* g, BandPlan* p);   // false: graph not eligible

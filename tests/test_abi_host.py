@@ -87,6 +87,14 @@ def test_invalid_arguments_rejected_on_host(lib):
     fw.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, i32, ctypes.c_float, vp, vp,
                    ctypes.c_size_t, vp]
     assert fw(None, None, None, 1, 1, 1, 64, None, 5, 0.1, None, None, 0, None) == 1
+    bws = lib.diffuser_backward_workspace_size
+    bws.argtypes = [vp, i64, i64, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)]
+    assert bws(None, 1, 1, 64, 1, 5, ctypes.byref(nbytes)) == 1   # null graph
+    bw = lib.diffuser_backward
+    bw.argtypes = [vp, vp, vp, vp, i32, i64, i64, i32, vp, i32, ctypes.c_float, vp, vp, vp, vp,
+                   ctypes.c_size_t, vp]
+    assert bw(None, None, None, None, 1, 1, 1, 64, None, 5, 0.1, None, None, None, None, 0,
+              None) == 1
     lib.diffuser_last_error.restype = ctypes.c_char_p
     assert lib.diffuser_last_error() != b""
 
