@@ -69,6 +69,11 @@ def _load():
                                            ctypes.c_int64, _i64p]
         lib.oracle_token_graph_causal.restype = ctypes.c_int
         lib.oracle_token_graph_causal.argtypes = lib.oracle_token_graph.argtypes
+        lib.oracle_token_graph_dilated.restype = ctypes.c_int
+        lib.oracle_token_graph_dilated.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                   ctypes.c_int32, _i32p, ctypes.c_int32,
+                                                   ctypes.c_uint64, ctypes.c_int32, _i64p, _i32p,
+                                                   ctypes.c_int64, _i64p]
         lib.oracle_block_graph.restype = ctypes.c_int
         lib.oracle_block_graph.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64, _i64p,
@@ -126,6 +131,28 @@ def token_graph(n: int, r: int, n_globals: int, rand_per_row: int, seed: int = 0
     col = np.zeros(max(nnz.value, 1), dtype=np.int32)
     _check(fn(n, r, n_globals, gp, rand_per_row, seed, _p(row_ptr, _i64p), _p(col, _i32p),
               col.size, ctypes.byref(nnz)), "token_graph")
+    return row_ptr, col[: nnz.value]
+
+
+def dilated_graph(n: int, r: int, dilation: int, n_globals: int, rand_per_row: int, seed: int = 0,
+                  globals_idx=None, causal: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """CSR of the token graph whose window is {i + k dilation : |k| <= r} (sliding-window
+    page, sec 1.2 eq 11)."""
+    lib = _load()
+    g = None
+    if globals_idx is not None:
+        g = np.ascontiguousarray(np.asarray(globals_idx, dtype=np.int32))
+        n_globals = int(g.size)
+    gp = _p(g, _i32p) if g is not None else None
+    nnz = ctypes.c_int64(0)
+    _check(lib.oracle_token_graph_dilated(n, r, dilation, n_globals, gp, rand_per_row, seed,
+                                          int(causal), None, None, 0, ctypes.byref(nnz)),
+           "dilated_graph(count)")
+    row_ptr = np.zeros(n + 1, dtype=np.int64)
+    col = np.zeros(max(nnz.value, 1), dtype=np.int32)
+    _check(lib.oracle_token_graph_dilated(n, r, dilation, n_globals, gp, rand_per_row, seed,
+                                          int(causal), _p(row_ptr, _i64p), _p(col, _i32p),
+                                          col.size, ctypes.byref(nnz)), "dilated_graph")
     return row_ptr, col[: nnz.value]
 
 

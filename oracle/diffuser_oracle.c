@@ -88,7 +88,8 @@ static int64_t emit_row(const unsigned char* mark, int64_t n, int32_t* col,
 }
 
 /*
- * Token-level graph ([D] sec 2.2; [S] eq 5, eq 12; [B] sec 2).
+ * Token-level graph ([D] sec 2.2; [S] eq 5, eq 12; [B] sec 2); `dilation`
+ * spaces the window's positions ([S] eq 11), 1 for the plain window.
  *   N(i) = {0..n-1}                                   if i in G
  *   N(i) = {j : |i-j| <= r} u G u {random draws}      otherwise
  * The set is held as a 0/1 mark per column, so duplicates collapse and the
@@ -96,11 +97,11 @@ static int64_t emit_row(const unsigned char* mark, int64_t n, int32_t* col,
  * `globals` NULL means G = {0..n_globals-1}; otherwise it must be strictly
  * increasing inside [0, n).
  */
-static int token_graph(int64_t n, int32_t r, int32_t n_globals,
+static int token_graph(int64_t n, int32_t r, int32_t dilation, int32_t n_globals,
                        const int32_t* globals, int32_t rand_per_row,
                        uint64_t seed, int causal, int64_t* row_ptr, int32_t* col,
                        int64_t col_capacity, int64_t* nnz_out) {
-    if (n < 1 || n > INT32_MAX || r < 0 || n_globals < 0 || n_globals > n ||
+    if (n < 1 || n > INT32_MAX || r < 0 || dilation < 1 || n_globals < 0 || n_globals > n ||
         rand_per_row < 0 || !nnz_out)
         return ORACLE_BAD_ARG;
     unsigned char* is_global = (unsigned char*)calloc((size_t)n, 1);
@@ -121,8 +122,9 @@ static int token_graph(int64_t n, int32_t r, int32_t n_globals,
             memset(mark, 1, (size_t)n);                 /* a global row reads all */
         } else {
             memset(mark, 0, (size_t)n);
-            for (int64_t j = 0; j < n; ++j)              /* window, eq 5 */
-                if (llabs(i - j) <= (int64_t)r) mark[j] = 1;
+            for (int64_t j = 0; j < n; ++j)              /* window, eq 5 (eq 11 when dilated) */
+                if (llabs(i - j) <= (int64_t)r * dilation && llabs(i - j) % dilation == 0)
+                    mark[j] = 1;
             for (int64_t j = 0; j < n; ++j)              /* every row reads G, eq 12 */
                 if (is_global[j]) mark[j] = 1;
             for (int32_t t = 0; t < rand_per_row; ++t) { /* random draws */
@@ -147,7 +149,7 @@ int oracle_token_graph(int64_t n, int32_t r, int32_t n_globals,
                        const int32_t* globals, int32_t rand_per_row,
                        uint64_t seed, int64_t* row_ptr, int32_t* col,
                        int64_t col_capacity, int64_t* nnz_out) {
-    return token_graph(n, r, n_globals, globals, rand_per_row, seed, 0, row_ptr,
+    return token_graph(n, r, 1, n_globals, globals, rand_per_row, seed, 0, row_ptr,
                        col, col_capacity, nnz_out);
 }
 
@@ -165,8 +167,23 @@ int oracle_token_graph_causal(int64_t n, int32_t r, int32_t n_globals,
                               const int32_t* globals, int32_t rand_per_row,
                               uint64_t seed, int64_t* row_ptr, int32_t* col,
                               int64_t col_capacity, int64_t* nnz_out) {
-    return token_graph(n, r, n_globals, globals, rand_per_row, seed, 1, row_ptr,
+    return token_graph(n, r, 1, n_globals, globals, rand_per_row, seed, 1, row_ptr,
                        col, col_capacity, nnz_out);
+}
+
+/*
+ * Dilated token graph ([S] sec 1.2 eq 11): the window of row i becomes
+ *   {i + k * dilation : -r <= k <= r} cut to the sequence,
+ * which is the sliding window for dilation 1; globals and random draws as in
+ * the token graph (one that falls on a window position enters once).
+ * `causal` applies the mask j <= i as for oracle_token_graph_causal.
+ */
+int oracle_token_graph_dilated(int64_t n, int32_t r, int32_t dilation, int32_t n_globals,
+                               const int32_t* globals, int32_t rand_per_row, uint64_t seed,
+                               int32_t causal, int64_t* row_ptr, int32_t* col,
+                               int64_t col_capacity, int64_t* nnz_out) {
+    return token_graph(n, r, dilation, n_globals, globals, rand_per_row, seed, causal != 0,
+                       row_ptr, col, col_capacity, nnz_out);
 }
 
 /*

@@ -447,3 +447,59 @@ def test_causal_diffusion_never_reads_the_future():
     A = oracle.attention_weights(Q, K, row_ptr, col)
     M = dense_from_csr(A, row_ptr, col, n)
     assert not np.triu(np.linalg.matrix_power(M, 5), 1).any()
+
+
+# ---------------------------------------------------------------- dilated window
+def test_dilated_window_page_example():
+    # [S] sec 1.2 eq 11: r = 2, dilation 3 - position 10 reads 4, 7, 10, 13, 16 and not 9 or 11
+    row_ptr, col = oracle.dilated_graph(40, 2, 3, 0, 0)
+    assert list(col[row_ptr[10]:row_ptr[11]]) == [4, 7, 10, 13, 16]
+
+
+@pytest.mark.parametrize("n,r,dl,G,R,seed,causal", [
+    (50, 2, 3, [], 0, 0, False), (97, 4, 5, [0, 60], 6, 3, False), (64, 3, 7, [5], 4, 1, True),
+    (20, 9, 4, [], 3, 2, False), (33, 1, 1, [2, 20], 5, 9, True),
+])
+def test_dilated_graph_brute_force(n, r, dl, G, R, seed, causal):
+    rows = []
+    for i in range(n):
+        if i in G:
+            s = set(range(n))
+        else:
+            s = {i + k * dl for k in range(-r, r + 1) if 0 <= i + k * dl < n}
+            s |= set(G)
+            s |= {sm64_py(seed ^ (i * R + t)) % n for t in range(R)}
+        if causal:
+            s = {j for j in s if j <= i}
+        rows.append(sorted(s))
+    row_ptr, col = oracle.dilated_graph(n, r, dl, len(G), R, seed=seed, globals_idx=G, causal=causal)
+    assert csr_rows(row_ptr, col) == rows
+
+
+def test_dilation_one_is_the_sliding_window():
+    for causal in (False, True):
+        a = oracle.dilated_graph(300, 7, 1, 3, 5, seed=4, causal=causal)
+        b = oracle.token_graph(300, 7, 3, 5, seed=4, causal=causal)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+
+
+def _components(row_ptr, col, n):
+    parent = list(range(n))
+
+    def find(x):
+        while parent[x] != x:
+            parent[x] = parent[parent[x]]
+            x = parent[x]
+        return x
+    for i in range(n):
+        for j in col[row_ptr[i]:row_ptr[i + 1]]:
+            parent[find(i)] = find(int(j))
+    return len({find(i) for i in range(n)})
+
+
+def test_dilation_splits_the_graph_by_residue():
+    # [S] sec 1.2: with one dilation 3 and nothing else, edges join only positions that
+    # agree mod 3 - three components; one global token reconnects them
+    assert _components(*oracle.dilated_graph(60, 2, 3, 0, 0), 60) == 3
+    assert _components(*oracle.dilated_graph(60, 2, 3, 1, 0), 60) == 1
