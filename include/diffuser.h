@@ -126,6 +126,20 @@ DIFFUSER_API int diffuser_build_causal_graph(int64_t n, int32_t r, int32_t n_glo
                                 uint64_t seed, diffuser_graph** out);
 
 /*
+ * Dilated token graph ([S] sec 1.2 eq 11): as diffuser_build_graph (or, with
+ * causal != 0, diffuser_build_causal_graph) with the window of row i replaced
+ * by the positions {i + k * dilation : -r <= k <= r} inside the sequence
+ * (dilation 1 is the sliding window and builds exactly that graph).  Globals
+ * and random draws as there; a global or draw that falls on a window position
+ * enters once.  dilation >= 1.  A graph with dilation > 1 takes the CSR path.
+ * Errors: as diffuser_build_graph.
+ */
+DIFFUSER_API int diffuser_build_dilated_graph(int64_t n, int32_t r, int32_t dilation,
+                                 int32_t n_globals, const int32_t* global_idx,
+                                 int32_t rand_per_row, uint64_t seed, int32_t causal,
+                                 diffuser_graph** out);
+
+/*
  * BigBird ITC block graph ([S] sec 2 eq 13 and its 12-block example; [B]
  * sec 2).  N = ceil(n/block) blocks (the last one may be ragged).  Block row
  * J < global_blocks reads every block.  Any other block row J reads the

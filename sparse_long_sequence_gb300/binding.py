@@ -46,6 +46,8 @@ def _load() -> ctypes.CDLL:
         "diffuser_version": (c.c_int, []),
         "diffuser_build_graph": (c.c_int, [i64, i32, i32, i32p, i32, u64, c.POINTER(vp)]),
         "diffuser_build_causal_graph": (c.c_int, [i64, i32, i32, i32p, i32, u64, c.POINTER(vp)]),
+        "diffuser_build_dilated_graph": (c.c_int, [i64, i32, i32, i32, i32p, i32, u64, i32,
+                                                   c.POINTER(vp)]),
         "diffuser_build_block_graph": (c.c_int, [i64, i32, i32, i32, i32, u64, c.POINTER(vp)]),
         "diffuser_graph_info": (c.c_int, [vp, i64p, i64p]),
         "diffuser_graph_copy_csr": (c.c_int, [vp, i64p, i32p]),
@@ -143,6 +145,20 @@ def diffuser_build_causal_graph(n: int, r: int, n_globals: int, global_idx=None,
                                 rand_per_row: int = 0, seed: int = 0) -> Graph:
     return _build_token(_lib.diffuser_build_causal_graph, "diffuser_build_causal_graph", n, r,
                         n_globals, global_idx, rand_per_row, seed)
+
+
+def diffuser_build_dilated_graph(n: int, r: int, dilation: int, n_globals: int, global_idx=None,
+                                 rand_per_row: int = 0, seed: int = 0, causal: bool = False) -> Graph:
+    gp = None
+    if global_idx is not None:
+        gl = np.ascontiguousarray(np.asarray(global_idx, dtype=np.int32))
+        n_globals = int(gl.size)
+        gp = gl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    out = ctypes.c_void_p()
+    _check(_lib.diffuser_build_dilated_graph(n, r, dilation, n_globals, gp, rand_per_row,
+                                             seed & 0xFFFFFFFFFFFFFFFF, int(causal),
+                                             ctypes.byref(out)), "diffuser_build_dilated_graph")
+    return Graph(out.value)
 
 
 def diffuser_build_block_graph(n: int, block: int, window_blocks: int, rand_blocks: int,

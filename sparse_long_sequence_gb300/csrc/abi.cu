@@ -532,11 +532,13 @@ int diffuser_version(void) { return 100; }
 
 namespace {
 
-int build_token_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* global_idx,
-                      int32_t rand_per_row, uint64_t seed, bool causal, diffuser_graph** out) {
+int build_token_graph(int64_t n, int32_t r, int32_t dilation, int32_t n_globals,
+                      const int32_t* global_idx, int32_t rand_per_row, uint64_t seed, bool causal,
+                      diffuser_graph** out) {
     try {
         if (n < 1 || n > INT32_MAX) return fail(DIFFUSER_ERR_INVALID_ARG, "n out of range");
         if (r < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "r must be >= 0");
+        if (dilation < 1) return fail(DIFFUSER_ERR_INVALID_ARG, "dilation must be >= 1");
         if (n_globals < 0 || n_globals > n)
             return fail(DIFFUSER_ERR_INVALID_ARG, "n_globals out of range");
         if (rand_per_row < 0 || rand_per_row > kMaxRandPerRow)
@@ -562,9 +564,10 @@ int build_token_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* gl
         g->n_globals = n_globals;
         g->rand_per_row = rand_per_row;
         g->causal = causal;
+        g->dilation = dilation;
         g->seed = seed;
         g->h_globals = std::move(G);
-        st = build_token_graph_device(g, nullptr);
+        st = dilation > 1 ? build_dilated_graph_device(g, nullptr) : build_token_graph_device(g, nullptr);
         return finish_graph(st, g, out);
     } catch (const std::bad_alloc&) {
         return fail(DIFFUSER_ERR_ALLOC, "host allocation failed");
@@ -577,13 +580,20 @@ int build_token_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* gl
 
 int diffuser_build_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* global_idx,
                          int32_t rand_per_row, uint64_t seed, diffuser_graph** out) {
-    return build_token_graph(n, r, n_globals, global_idx, rand_per_row, seed, false, out);
+    return build_token_graph(n, r, 1, n_globals, global_idx, rand_per_row, seed, false, out);
 }
 
 int diffuser_build_causal_graph(int64_t n, int32_t r, int32_t n_globals,
                                 const int32_t* global_idx, int32_t rand_per_row, uint64_t seed,
                                 diffuser_graph** out) {
-    return build_token_graph(n, r, n_globals, global_idx, rand_per_row, seed, true, out);
+    return build_token_graph(n, r, 1, n_globals, global_idx, rand_per_row, seed, true, out);
+}
+
+int diffuser_build_dilated_graph(int64_t n, int32_t r, int32_t dilation, int32_t n_globals,
+                                 const int32_t* global_idx, int32_t rand_per_row, uint64_t seed,
+                                 int32_t causal, diffuser_graph** out) {
+    return build_token_graph(n, r, dilation, n_globals, global_idx, rand_per_row, seed,
+                             causal != 0, out);
 }
 
 int diffuser_build_block_graph(int64_t n, int32_t block, int32_t window_blocks,

@@ -1175,7 +1175,8 @@ band::Weights band_weights(char* ws, const BandLayout& L) {
 }
 
 bool band_plan(const diffuser_graph* g, BandPlan* p) {
-    if (g->kind != kTokenGraph || g->r < 8 || g->n_globals > kBandMaxGlobals) return false;
+    if (g->kind != kTokenGraph || g->dilation != 1 || g->r < 8 || g->n_globals > kBandMaxGlobals)
+        return false;
     p->n = g->n;
     p->r = g->r;
     p->causal = g->causal ? 1 : 0;

@@ -158,6 +158,82 @@ __global__ void token_fill_kernel(TokenParams p, const int64_t* row_ptr, int32_t
     merge_range(p.globals, p.g, xs, nx, hi + 1, last, out + w);
 }
 
+// ---- dilated token graph (sliding-window page, sec 1.2 eq 11) ----
+// Row i's window is the progression i + k dil, |k| <= r, cut to [0, last]; a
+// row is the merge of that progression, the globals up to last and the row's
+// own draws up to last, each value entering once.  (dil = 1 graphs take the
+// token kernels above.)
+
+// Sorted, deduplicated random draws of row i that do not lie after `last`.
+__device__ int32_t row_draws(const TokenParams& p, int64_t i, int64_t last, int32_t* xs) {
+    int32_t cnt = 0;
+    for (int32_t t = 0; t < p.R; ++t) {
+        uint64_t key = (uint64_t)i * (uint64_t)p.R + (uint64_t)t;
+        int64_t j = (int64_t)(splitmix64(p.seed ^ key) % (uint64_t)p.n);
+        if (j > last) continue;
+        int32_t pos = cnt;
+        while (pos > 0 && xs[pos - 1] > j) --pos;
+        if (pos > 0 && xs[pos - 1] == j) continue;
+        for (int32_t q = cnt; q > pos; --q) xs[q] = xs[q - 1];
+        xs[pos] = (int32_t)j;
+        ++cnt;
+    }
+    return cnt;
+}
+
+// The merged row (written to out unless it is null); returns its length.
+__device__ int64_t dilated_row(const TokenParams& p, int32_t dil, int64_t i, const int32_t* xs,
+                               int32_t nx, int32_t* out) {
+    const int64_t last = row_last(p, i);
+    const int64_t kmin = -(i / dil < p.r ? i / dil : (int64_t)p.r);          // i + k dil >= 0
+    const int64_t kmax = (last - i) / dil < p.r ? (last - i) / dil : (int64_t)p.r;   // <= last
+    const int32_t a_end = count_less(p.globals, p.g, last + 1);
+    const int64_t none = INT64_MAX;
+    int64_t k = kmin, w = 0;
+    int32_t a = 0, b = 0;
+    for (;;) {
+        const int64_t vw = k <= kmax ? i + k * dil : none;
+        const int64_t vg = a < a_end ? (int64_t)p.globals[a] : none;
+        const int64_t vx = b < nx ? (int64_t)xs[b] : none;
+        int64_t v = vw < vg ? vw : vg;
+        if (vx < v) v = vx;
+        if (v == none) break;
+        if (out) out[w] = (int32_t)v;
+        ++w;
+        if (vw == v) ++k;
+        if (vg == v) ++a;
+        if (vx == v) ++b;
+    }
+    return w;
+}
+
+__global__ void dilated_count_kernel(TokenParams p, int32_t dil, int64_t* counts) {
+    extern __shared__ int32_t smem_xs[];
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n) return;
+    const int64_t last = row_last(p, i);
+    if (p.is_global[i]) { counts[i] = last + 1; return; }
+    int32_t* xs = smem_xs + (size_t)threadIdx.x * p.R;
+    const int32_t nx = row_draws(p, i, last, xs);
+    counts[i] = dilated_row(p, dil, i, xs, nx, nullptr);
+}
+
+__global__ void dilated_fill_kernel(TokenParams p, int32_t dil, const int64_t* row_ptr,
+                                    int32_t* col) {
+    extern __shared__ int32_t smem_xs[];
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n) return;
+    int32_t* out = col + row_ptr[i];
+    const int64_t last = row_last(p, i);
+    if (p.is_global[i]) {
+        for (int64_t j = 0; j <= last; ++j) out[j] = (int32_t)j;
+        return;
+    }
+    int32_t* xs = smem_xs + (size_t)threadIdx.x * p.R;
+    const int32_t nx = row_draws(p, i, last, xs);
+    dilated_row(p, dil, i, xs, nx, out);
+}
+
 struct BlockParams {
     int64_t n, nb;
     int32_t block, half, s, gb;
@@ -380,6 +456,50 @@ int build_token_graph_device(diffuser_graph* g, cudaStream_t stream) {
         if ((err = cudaGetLastError()) != cudaSuccess) status = cuda_fail(err, "token_fill_kernel");
     }
     if (status == DIFFUSER_OK) status = build_extras(g, p, blocks, threads, shmem, d_counts, stream);
+    if (status == DIFFUSER_OK) status = copy_csr_to_host(g, stream);
+    cudaFree(d_counts);
+    return status;
+}
+
+int build_dilated_graph_device(diffuser_graph* g, cudaStream_t stream) {
+    const int64_t n = g->n;
+    cudaError_t err;
+    std::vector<uint8_t> flags(n, 0);
+    for (int32_t s : g->h_globals) flags[s] = 1;
+    err = cudaMalloc(&g->d_is_global, n);
+    if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(is_global) failed");
+    err = cudaMalloc(&g->d_globals, sizeof(int32_t) * (g->n_globals > 0 ? g->n_globals : 1));
+    if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(globals) failed");
+    err = cudaMemcpyAsync(g->d_is_global, flags.data(), n, cudaMemcpyHostToDevice, stream);
+    if (err == cudaSuccess && g->n_globals > 0)
+        err = cudaMemcpyAsync(g->d_globals, g->h_globals.data(), sizeof(int32_t) * g->n_globals,
+                              cudaMemcpyHostToDevice, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "uploading the global positions");
+    int64_t* d_counts = nullptr;
+    err = cudaMalloc(&d_counts, sizeof(int64_t) * n);
+    if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(counts) failed");
+    TokenParams p{n,       g->r,         g->n_globals,   g->rand_per_row,
+                  g->seed, g->d_globals, g->d_is_global, g->causal ? 1 : 0};
+    // per-thread scratch for the draws lives in shared memory; keep it <= 48 KB
+    int threads = 128;
+    while (threads > 1 && (size_t)threads * p.R * sizeof(int32_t) > 48 * 1024) threads >>= 1;
+    const size_t shmem = (size_t)threads * p.R * sizeof(int32_t);
+    const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+    int status = DIFFUSER_OK;
+    {
+        LaunchScope scope(DIFFUSER_KERNEL_BUILD, stream);
+        dilated_count_kernel<<<blocks, threads, shmem, stream>>>(p, g->dilation, d_counts);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) status = cuda_fail(err, "dilated_count_kernel");
+    if (status == DIFFUSER_OK) status = scan_and_alloc(g, d_counts, stream);
+    if (status == DIFFUSER_OK) {
+        {
+            LaunchScope scope(DIFFUSER_KERNEL_BUILD, stream);
+            dilated_fill_kernel<<<blocks, threads, shmem, stream>>>(p, g->dilation, g->d_row_ptr,
+                                                                     g->d_col);
+        }
+        if ((err = cudaGetLastError()) != cudaSuccess) status = cuda_fail(err, "dilated_fill_kernel");
+    }
     if (status == DIFFUSER_OK) status = copy_csr_to_host(g, stream);
     cudaFree(d_counts);
     return status;

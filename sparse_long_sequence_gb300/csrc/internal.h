@@ -66,6 +66,7 @@ struct diffuser_graph {
     // token graph parameters
     int32_t r = 0, n_globals = 0, rand_per_row = 0;
     bool causal = false;              // token graph cut to j <= i
+    int32_t dilation = 1;             // token graph: spacing of the window's positions
     // block graph parameters
     int32_t block = 0, window_blocks = 0, rand_blocks = 0, global_blocks = 0;
     uint64_t seed = 0;
@@ -116,6 +117,7 @@ class LaunchScope {
 // ---- graph construction kernels (graph_build.cu) ---------------------------
 int build_token_graph_device(diffuser_graph* g, cudaStream_t stream);
 int build_block_graph_device(diffuser_graph* g, cudaStream_t stream);
+int build_dilated_graph_device(diffuser_graph* g, cudaStream_t stream);   // dilation > 1
 
 // ---- CSR SIMT path (simt_path.cu) ------------------------------------------
 struct CsrArgs {

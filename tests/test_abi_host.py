@@ -74,6 +74,10 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert fc(0, 1, 0, None, 0, 0, ctypes.byref(out)) == 1         # n < 1
     assert fc(10, -1, 0, None, 0, 0, ctypes.byref(out)) == 1       # r < 0
     assert fc(10, 1, 2, bad, 0, 0, ctypes.byref(out)) == 1         # not increasing
+    fd = lib.diffuser_build_dilated_graph
+    fd.argtypes = [i64, i32, i32, i32, ctypes.POINTER(i32), i32, u64, i32, ctypes.POINTER(vp)]
+    assert fd(10, 1, 0, 0, None, 0, 0, 0, ctypes.byref(out)) == 1   # dilation < 1
+    assert fd(10, -1, 2, 0, None, 0, 0, 0, ctypes.byref(out)) == 1  # r < 0
     fb = lib.diffuser_build_block_graph
     fb.argtypes = [i64, i32, i32, i32, i32, u64, ctypes.POINTER(vp)]
     assert fb(100, 16, 2, 1, 1, 0, ctypes.byref(out)) == 1         # even window
