@@ -245,3 +245,22 @@ def backward(Q: np.ndarray, K: np.ndarray, V: np.ndarray, dOut: np.ndarray, row_
                                    hops, alpha, _p(dQ, _f64p), _p(dK, _f64p), _p(dV, _f64p)),
            "backward")
     return dQ, dK, dV
+
+
+def layer_forward(X: np.ndarray, Wq: np.ndarray, Wk: np.ndarray, Wv: np.ndarray, Wo: np.ndarray,
+                  row_ptr: np.ndarray, col: np.ndarray, hops: int, alpha: float) -> np.ndarray:
+    """The diffusion module with its projections (Diffuser notes sec 2.1: per head
+    Q = X W_Q, K = X W_K, V = X W_V; the heads' outputs are concatenated and
+    projected by W_O; sec 2.4: residual and feed-forward lie outside the module).
+
+    X [B][n][D]; Wq, Wk, Wv [H][D][d]; Wo [H*d][D]; all float64.  Returns [B][n][D].
+    """
+    X = np.asarray(X, dtype=np.float64)
+    B, n, _ = X.shape
+    H, _, d = Wq.shape
+    Q = np.einsum("bnD,hDd->bhnd", X, Wq)
+    K = np.einsum("bnD,hDd->bhnd", X, Wk)
+    V = np.einsum("bnD,hDd->bhnd", X, Wv)
+    Z = forward(Q, K, V, row_ptr, col, hops, alpha)                 # [B][H][n][d]
+    heads = np.transpose(Z, (0, 2, 1, 3)).reshape(B, n, H * d)      # concatenation
+    return heads @ Wo
