@@ -237,3 +237,40 @@ def test_model_detects_a_missing_arrival():
     tl = cta_tiles(300, 8, False, 1, 1, 0)
     assert simulate(tl, r64 // CK, r64, True, True)
     assert not simulate(tl, r64 // CK, r64, True, True, fp_arrivals=3)
+
+
+# ---------------------------------------------------------------- the gather's row split
+def quarter_rows(q, nq, n, units, x_ptr, row_cost=2):
+    """causal_row_range in csrc/band_hop.cu: rows [R0, R1) of quarter q, found by the
+    quarter's 8 lanes probing 8 points a round (both boundaries together)."""
+    per_unit = row_cost * n + x_ptr[n]
+    total = units * per_unit
+
+    def first_row(t):
+        u, rem = divmod(t, per_unit)
+        lo, hi = 0, n
+        while lo < hi:
+            probes = [lo + (hi - lo) * (l + 1) // 9 for l in range(8)]
+            k = sum(1 for p in probes if row_cost * p + x_ptr[p] < rem)   # probes below
+            new_lo = lo + (hi - lo) * k // 9 + 1 if k > 0 else lo
+            new_hi = lo + (hi - lo) * (k + 1) // 9 if k < 8 else hi
+            lo, hi = new_lo, new_hi
+        return u * n + lo
+    return first_row(q * total // nq), first_row((q + 1) * total // nq)
+
+
+@pytest.mark.parametrize("n,units,nq", [(4096, 24, 14592), (389, 2, 64), (1, 3, 32), (1000, 7, 448)])
+def test_causal_gather_split_covers_rows_once_in_balanced_ranges(n, units, nq):
+    import random
+    rng = random.Random(n)
+    counts = [rng.randint(0, 32 * (i + 1) // n) for i in range(n)]   # late rows keep more draws
+    x_ptr = [0]
+    for c in counts:
+        x_ptr.append(x_ptr[-1] + c)
+    bounds = [quarter_rows(q, nq, n, units, x_ptr) for q in range(nq)]
+    assert bounds[0][0] == 0 and bounds[-1][1] == units * n
+    for (a0, a1), (b0, _) in zip(bounds, bounds[1:]):
+        assert a0 <= a1 == b0
+    ideal = units * (2 * n + x_ptr[n]) / nq
+    worst = max(sum(2 + counts[R % n] for R in range(r0, r1)) for r0, r1 in bounds)
+    assert worst <= ideal + 2 + max(counts)
