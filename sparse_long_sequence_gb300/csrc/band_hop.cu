@@ -4,7 +4,7 @@
 // two kernels per hop:
 //   hop_gather_kernel: the random extras of every row not in G, into a
 //            per-row partial P_i (whole Z_k rows gathered from L2).  The rows
-//            are split evenly over the quarter-warps of the grid; each walks
+//            are split over the quarter-warps of the grid; each walks
 //            its rows' extras as one stream with several rows in flight, the
 //            next slots' indices loading meanwhile; every load instruction
 //            reads whole 128-byte lines.  Hops after the first also sum the
@@ -31,6 +31,9 @@
 //            written as the next [hi | lo] bf16 row and fp32 row, or as the
 //            bf16 output.  The first hop also adds up the band part of each
 //            row sum and completes inv_l.
+// On the causal graph ("Diffuser...", sec 2.6) the window is [i - r, i], a
+// tile's key chunks end at its last row, and the gather splits its rows by
+// cost (late rows keep more draws) instead of by count.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

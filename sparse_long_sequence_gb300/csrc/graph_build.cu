@@ -16,6 +16,10 @@
 // history positions): the same sets cut to [0, i].  Each row's upper limit
 // `last` is i instead of n-1; draws that land after i are dropped.
 //
+// Dilated token graph (sliding-window page, sec 1.2 eq 11): the window of row
+// i is the progression i + k * dilation, |k| <= r; its rows are built by
+// separate kernels that merge that progression, G and the row's draws.
+//
 // Block graph (same page, sec 2 eq 13; "038 BigBird", sec 2): allowed blocks
 // of block row J are all blocks for J < gb, else [0, gb) u (window blocks u
 // random blocks); the tokens of the allowed blocks, ascending.
