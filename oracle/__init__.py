@@ -10,14 +10,18 @@ this module compiles it with gcc on first use and marshals numpy arrays.
 
 Sources, cited by page title and section/equation:
   * "Diffuser: modelling long sequences with multi-hop attention diffusion"
-    (reading notes, arXiv 2210.11794v2): sec 2.1 eq S.1-S.5 (weights A),
-    sec 2.4 eq S.7 (PPR recursion).
+    (reading notes, arXiv 2210.11794v2): sec 2.1 eq S.1-S.5 (weights A; the
+    per-head projections and W_O), sec 2.4 eq S.7 (PPR recursion), sec 2.6
+    (training through the unrolled recursion; causal use, A lower-triangular).
   * "1.2.1 Static sparsity: Longformer, BigBird and sliding windows":
-    eq 1-6 (scores, softmax, window), eq 12 (globals), sec 2 eq 13 (blocks).
+    eq 1-6 (scores, softmax, window; the causal window), eq 11 (dilated
+    window), eq 12 (globals), sec 2 eq 13 (blocks).
   * "038 BigBird": sec 2 (window u random u global; global rows read all).
 
-Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
-values the pages print, closed forms and brute force.  The random-edge draws
+Pins: every function here is checked against values the pages print, closed
+forms, brute force, finite differences and invariants, in
+``tests/test_oracle_pins.py``, ``tests/test_oracle_backward_pins.py`` and
+``tests/test_oracle_layer_pins.py``.  The random-edge draws
 themselves are a definition (SplitMix64 keyed by row and draw index), pinned
 only through the published SplitMix64 test vector: parity unpinned beyond it.
 """
