@@ -217,6 +217,13 @@ def whole_job_rate(units_per_rank: int, nnz: int, hops: int, world: int, ms: flo
     return world * units_per_rank * nnz * hops / (ms / 1e3)
 
 
+def step_stats(ms: list[float]) -> dict:
+    """Median, 10th and 90th percentile of the per-step times (any count >= 1)."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "n": int(a.size)}
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_ours(args, w) -> None:
     import torch
@@ -355,6 +362,7 @@ def run_ours(args, w) -> None:
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "step_ms": step_stats(step_ms),
             "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
             "config": {**w.describe(), "nnz": g.nnz, "units_per_gpu": w.units,
                        "parallelism": f"dp{world}" if world > 1 else "single GPU",

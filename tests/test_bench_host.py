@@ -99,3 +99,12 @@ def test_workload_registry():
     c = workloads.CAUSAL_TEXT
     row_ptr, _ = oracle.token_graph(c.n, c.r, 0, 0, causal=True)
     assert row_ptr[-1] == c.n * (c.r + 1) - c.r * (c.r + 1) // 2
+
+
+def test_step_stats():
+    sys.path.insert(0, ROOT)
+    import bench
+    one = bench.step_stats([2.0])
+    assert one == {"median": 2.0, "p10": 2.0, "p90": 2.0, "n": 1}
+    st = bench.step_stats([float(x) for x in range(1, 12)])
+    assert st["median"] == 6.0 and st["p10"] == 2.0 and st["p90"] == 10.0 and st["n"] == 11
