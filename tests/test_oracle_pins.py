@@ -503,3 +503,16 @@ def test_dilation_splits_the_graph_by_residue():
     # agree mod 3 - three components; one global token reconnects them
     assert _components(*oracle.dilated_graph(60, 2, 3, 0, 0), 60) == 3
     assert _components(*oracle.dilated_graph(60, 2, 3, 1, 0), 60) == 1
+
+
+def test_twelve_layer_reach_example():
+    # [S] sec 2.1: 12 layers reaching distance 900 need r >= 75 (12 * 75 = 900); for
+    # n = 8192 the page counts 8192 * 151 = 1,236,992 local edges ignoring the ends,
+    # against 8192^2 = 67,108,864 for full attention (about 1.84 %); the ends remove
+    # r(r+1) = 5,700 of them ([S] eq 6)
+    r = -(-900 // 12)
+    assert r == 75
+    nominal = 8192 * (2 * r + 1)
+    assert nominal == 1_236_992 and round(100 * nominal / 8192 ** 2, 2) == 1.84
+    row_ptr, _ = oracle.token_graph(8192, r, 0, 0)
+    assert row_ptr[-1] == nominal - r * (r + 1) == 1_231_292
