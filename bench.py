@@ -146,6 +146,70 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- shared pieces
+def bench_config(w: workloads.Workload, world: int) -> dict:
+    """The `config` object of the JSON line, identical for both arms."""
+    return {**w.describe(), "parallelism": f"dp{world}" if world > 1 else "single GPU",
+            "l2": "GPU arm: flushed between steps (256 MB write outside the timed events)"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU legs."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+class BenchCheckFailed(RuntimeError):
+    """A timed forward did not complete correctly: the line must not be printed."""
+
+
+def check_graph_status(dl, g, where: str) -> None:
+    """Fail when a kernel on graph g reported a failure (a bounded wait that gave
+    up): every result since the last reset, timed ones included, is invalid."""
+    st = dl.diffuser_graph_status(g)
+    if st != 0:
+        raise BenchCheckFailed(f"device status word {st:#x} set after {where}")
+
+
+def check_sampled_unit(w: workloads.Workload, out_unit, Qh, Kh, Vh, unit: int) -> dict:
+    """Compare one (batch, head) unit of a timed forward's output with the fp64
+    oracle on the same inputs: fp32 max-abs <= 1e-5, bf16 per-row max error over
+    the row's max-norm <= 4e-3."""
+    import oracle
+    b, h = divmod(unit, w.H)
+    gargs = w.graph_args()
+    if w.kind == "block":
+        row_ptr, col = oracle.block_graph(**gargs)
+    else:
+        row_ptr, col = oracle.token_graph(**gargs, causal=w.kind == "causal")
+    one = [oracle.widen(x[b:b + 1, h:h + 1], w.dtype) for x in (Qh, Kh, Vh)]
+    ref = oracle.forward(*one, row_ptr, col, w.hops, w.alpha, nthreads=os.cpu_count() or 1)[0, 0]
+    got = np.asarray(out_unit, dtype=np.float64)
+    if w.dtype == "fp32":
+        err, tol = float(np.abs(got - ref).max()), 1e-5
+    else:
+        den = np.abs(ref).max(axis=-1)
+        err = float((np.abs(got - ref).max(axis=-1) / np.where(den > 0, den, 1.0)).max())
+        tol = 4e-3
+    if not err <= tol:
+        raise BenchCheckFailed(f"unit {unit} differs from the oracle: error {err:.3e} > {tol}")
+    return {"unit": unit, "error": err, "tolerance": tol,
+            "metric": "max-abs" if w.dtype == "fp32" else "per-row max error / row max-norm"}
+
+
 # ---------------------------------------------------------------- CPU oracle arm
 def oracle_sample(w: workloads.Workload, units: int, nthreads: int) -> tuple[float, int, int]:
     """Run the fp64 oracle on `units` units of the workload; returns (seconds,
@@ -166,8 +230,10 @@ def oracle_sample(w: workloads.Workload, units: int, nthreads: int) -> tuple[flo
 
 
 def cpu_sample_units(w) -> tuple[int, int]:
+    """All units of the workload (the oracle takes well under a minute for any of
+    them on a 16-core host), threads over units."""
     cores = os.cpu_count() or 1
-    return min(w.units, cores), cores
+    return w.units, cores
 
 
 def run_reference(args, w) -> None:
@@ -184,14 +250,15 @@ def run_reference(args, w) -> None:
     value = eh / statistics.mean(times)
     sample = (f"{units} of {w.units} (batch, head) units of {w.name} per step, "
               f"fp64 oracle, {cores} threads over units")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {**w.describe(), "parallelism": "host threads"},
+        "config": bench_config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -265,6 +332,7 @@ def run_ours(args, w) -> None:
     def step():
         dl.diffuser_forward(Q, K, V, g, w.hops, w.alpha, out=out, workspace=ws, stream=stream)
 
+    dl.diffuser_graph_status(g, reset=True)     # every later check covers all of this run
     for _ in range(max(args.warmup, 0)):
         flush.fill_(1)
         step()
@@ -291,6 +359,12 @@ def run_ours(args, w) -> None:
         dist.barrier()
     clock_info = clocks.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    check_graph_status(dl, g, "the warm-up and timed steps")
+    # the last timed forward's output, one sampled (batch, head) unit against the oracle
+    # (outside the timed region; the unit differs per rank)
+    sample_unit = (w.units - 1 - rank) % w.units
+    sb, sh = divmod(sample_unit, w.H)
+    checked = check_sampled_unit(w, out[sb, sh].float().cpu().numpy(), Qh, Kh, Vh, sample_unit)
 
     # ---- the same K steps again with per-kernel CUDA events (the library
     # launches each kernel directly while its profile is open): the device time
@@ -323,7 +397,9 @@ def run_ours(args, w) -> None:
         stream.synchronize()
         e2e_ms.append(1e3 * (time.perf_counter() - t0))
     t_e2e = max_over_ranks(statistics.mean(e2e_ms), device="cuda")
-    assert torch.equal(Oh, out.cpu()), "end-to-end output differs from the device forward"
+    check_graph_status(dl, g, "the kernel-timing and end-to-end passes")
+    if not torch.equal(Oh, out.cpu()):
+        raise BenchCheckFailed("end-to-end output differs from the device forward")
 
     value = whole_job_rate(w.units, g.nnz, w.hops, world, t_step)
     io_bytes = w.units * w.n * w.d * (2 if w.dtype == "bf16" else 4)
@@ -340,8 +416,9 @@ def run_ours(args, w) -> None:
         per_hop_s = hop_ms / n_hops / 1e3
         achieved = model["per_hop_launch"] / per_hop_s / 1e9
         traffic = hop_kernel_traffic(w.name)
+        measured_frac = traffic / per_hop_s / 1e9 / peak if traffic else None
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "traffic": traffic,
+                    "frac": achieved / peak, "traffic": traffic, "measured_frac": measured_frac,
                     "kernel": ("diffusion hop (window tcgen05 kernel + gather kernel)" if band
                                else "diffusion hop (CSR SIMT kernel)"),
                     "peak_kind": peak_kind,
@@ -353,9 +430,13 @@ def run_ours(args, w) -> None:
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         units, cores = cpu_sample_units(w)
         dt, eh, _ = oracle_sample(w, units, cores)
+        dt1, eh1, _ = oracle_sample(w, 1, 1)
         cpu = {"value": eh / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{units} of {w.units} (batch, head) units of {w.name}, fp64 oracle, "
-                         f"{cores} threads over units, {dt:.1f} s"}
+                         f"{cores} threads over units, {dt:.1f} s",
+               "cpu_model": cpu_model(),
+               "single_thread": {"value": eh1 / dt1, "unit": UNIT, "cores": 1,
+                                 "sample": f"1 (batch, head) unit of {w.name}, {dt1:.1f} s"}}
 
     if rank == 0:
         line = {
@@ -364,11 +445,14 @@ def run_ours(args, w) -> None:
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "step_ms": step_stats(step_ms),
             "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
-            "config": {**w.describe(), "nnz": g.nnz, "units_per_gpu": w.units,
-                       "parallelism": f"dp{world}" if world > 1 else "single GPU",
-                       "l2": "flushed between steps (256 MB write outside the timed events)",
-                       "arith": ("A and Z_k as bf16 hi + lo pairs on the tensor cores (window, globals), "
-                                 "fp32 gathers and accumulation" if band else "fp32 SIMT (CSR path)")},
+            "config": bench_config(w, world),
+            "details": {"nnz": g.nnz, "units_per_gpu": w.units,
+                        "arith": ("A and Z_k as bf16 hi + lo pairs on the tensor cores (window, globals), "
+                                  "fp32 gathers and accumulation" if band else "fp32 SIMT (CSR path)")},
+            "checked": {**checked, "device_status": 0,
+                        "what": "graph status word read after the warm-up + timed steps and after the "
+                                "later passes (a bounded wait that gave up would set it); one sampled "
+                                "unit of the last timed forward against the fp64 oracle"},
             "e2e": {"value": whole_job_rate(w.units, g.nnz, w.hops, world, t_e2e), "unit": UNIT,
                     "h2d_bytes_per_step": 3 * io_bytes, "d2h_bytes_per_step": io_bytes},
             "roofline": roofline,
@@ -401,7 +485,12 @@ def main():
     if args.impl == "reference":
         run_reference(args, w)
     else:
-        run_ours(args, w)
+        try:
+            run_ours(args, w)
+        except BenchCheckFailed as e:
+            print(json.dumps({"metric": METRIC, "value": None, "unit": UNIT, "error": str(e)}),
+                  flush=True)
+            raise SystemExit(3)
 
 
 if __name__ == "__main__":

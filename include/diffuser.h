@@ -172,9 +172,14 @@ DIFFUSER_API void diffuser_graph_free(diffuser_graph* g);
 
 /*
  * Bytes of device workspace diffuser_forward needs for this graph and shape,
- * whichever kernel path is selected.  The workspace holds the stored weights
- * A (fp32, "score once, aggregate K times", [D] sec 2.4 / 2.6) and the fp32
- * hop state Z_k.
+ * whichever kernel path is selected.  On the CSR path the workspace holds
+ * the stored weights A (fp32, "score once, aggregate K times", [D] sec 2.4 /
+ * 2.6) and the fp32 hop state Z_k.  On the band path it holds the row
+ * statistics (maxima, inverse sums), the weights of the edges outside the
+ * window (globals, random extras, the global rows), the hop state Z_k (as
+ * fp32 rows and as bf16 hi/lo operand rows) and the per-hop partial sums;
+ * the window's weights are recomputed from Q and K in every hop and never
+ * stored.
  *   B, H >= 1; d == 64; dtype a diffuser_dtype.
  */
 DIFFUSER_API int diffuser_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32_t d,
@@ -198,7 +203,11 @@ DIFFUSER_API int diffuser_workspace_size(const diffuser_graph* g, int64_t B, int
  *   stream      stream on which everything is enqueued
  * Precision: A and Z_k are fp32; bf16 outputs are rounded to nearest-even
  * once, from fp32.  Errors: INVALID_ARG, UNSUPPORTED (d != 64, dtype),
- * WORKSPACE, CUDA.
+ * WORKSPACE, CUDA, and DEVICE when a kernel of an earlier call on g has
+ * reported a failure through the graph's status word (see
+ * diffuser_graph_status): the check reads a host mirror of the word, so it
+ * costs no synchronization and sees failures of calls that have completed;
+ * nothing is launched until the word is reset.
  */
 DIFFUSER_API int diffuser_forward(const void* Q, const void* K, const void* V, int32_t dtype, int64_t B,
                      int64_t H, int32_t d, const diffuser_graph* g, int32_t hops, float alpha,
@@ -265,21 +274,26 @@ DIFFUSER_API int diffuser_backward(const void* Q, const void* K, const void* V, 
 
 /*
  * diffuser_forward without any device allocation, for callers that cannot
- * call cudaMalloc while the forward runs: code recording a CUDA stream
- * capture, serving loops whose device memory is fixed at start-up, or host
- * frameworks that own every allocation and forbid allocating calls on their
- * hot path.  (The pages have no counterpart: this is a library convenience,
- * not part of the method.)
+ * call cudaMalloc while the forward runs: serving loops whose device memory
+ * is fixed at start-up, or host frameworks that own every allocation and
+ * forbid allocating calls on their hot path (cudaMalloc may synchronize the
+ * device and fail under memory pressure at an unpredictable moment).  (The
+ * pages have no counterpart: this is a library convenience, not part of the
+ * method.)
  *
  * Same arguments and results as diffuser_forward, without the workspace: the
  * weights A and the hop state live in one fixed array in device global
  * memory defined by the library (diffuser_no_alloc_scratch_bytes() bytes,
  * 32 MiB), which every GPU that loads the library holds until the process
- * exits.  It runs the general CSR kernels.  The graph must be built
- * beforehand (diffuser_build_graph allocates).
+ * exits.  It runs the general CSR kernels, with diffuser_forward's CSR-path
+ * argument checks, workspace layout and hop sequence.  The graph must be
+ * built beforehand (diffuser_build_graph allocates).
  *   - Problems whose weights and hop state need more than the array holds
  *     (units * nnz * 4 + 2 * units * n * 64 * 4 bytes, each part rounded up
  *     to 256) are rejected with DIFFUSER_ERR_WORKSPACE before anything runs.
+ *   - Every call overwrites the part of the array it uses; nothing in it has
+ *     to start at zero (the weights and each hop's state are written before
+ *     they are read).
  *   - The first call on a device looks up the array's device address on that
  *     device (make it before any stream capture); later calls only launch
  *     kernels.  No cudaMalloc, cudaFree or allocating library routine is
@@ -339,10 +353,20 @@ DIFFUSER_API int diffuser_get_path(void);
 
 /*
  * Read (synchronously) the device status word that the graph's kernels set
- * when a bounded internal wait gives up (0 = no error); reset != 0 clears it.
- * A nonzero word means results computed since the last reset are invalid.
+ * when a bounded internal wait gives up (0 = no error); reset != 0 clears it
+ * and its host mirror.  A nonzero word means results computed since the last
+ * reset are invalid, and every forward or backward on g returns
+ * DIFFUSER_ERR_DEVICE without launching anything until it is reset.
  */
 DIFFUSER_API int diffuser_graph_status(const diffuser_graph* g, int* status, int reset);
+
+/*
+ * Test export: write `status` into the graph's status word and its host
+ * mirror with plain copies (no kernel), as a kernel does when one of its
+ * bounded waits gives up.  Lets a test check the error path of the entry
+ * points and of the caller's own checks without making any kernel fail.
+ */
+DIFFUSER_API int diffuser_graph_set_status(const diffuser_graph* g, int status);
 
 /* ---------------------------------------------------------------- measurement */
 

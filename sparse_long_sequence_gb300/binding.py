@@ -73,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "diffuser_set_path": (c.c_int, [c.c_int]),
         "diffuser_get_path": (c.c_int, []),
         "diffuser_graph_status": (c.c_int, [vp, c.POINTER(c.c_int), c.c_int]),
+        "diffuser_graph_set_status": (c.c_int, [vp, c.c_int]),
         "diffuser_launch_count": (c.c_int64, [i64p]),
         "diffuser_profile_begin": (c.c_int, []),
         "diffuser_profile_end": (c.c_int, [c.POINTER(c.c_double), i64p]),
@@ -345,6 +346,10 @@ def diffuser_graph_status(g: Graph, reset: bool = False) -> int:
     _check(_lib.diffuser_graph_status(g.handle, ctypes.byref(st), int(reset)),
            "diffuser_graph_status")
     return st.value
+
+
+def diffuser_graph_set_status(g: Graph, status: int) -> None:
+    _check(_lib.diffuser_graph_set_status(g.handle, int(status)), "diffuser_graph_set_status")
 
 
 def diffuser_launch_count() -> tuple[int, dict]:

@@ -94,11 +94,6 @@ LaunchScope::~LaunchScope() {
 }
 
 // ---- workspace layout ---------------------------------------------------------
-// [A: units*nnz fp32][Z ping: units*n*64 fp32][Z pong: units*n*64 fp32]
-struct Layout {
-    size_t a_off, z0_off, z1_off, total;
-};
-
 int plan_layout(const diffuser_graph* g, int64_t B, int64_t H, Layout* L) {
     size_t units = (size_t)B * (size_t)H;
     size_t a_bytes, z_elems, z_bytes;
@@ -121,6 +116,14 @@ int check_shape(const diffuser_graph* g, int64_t B, int64_t H, int32_t d, int32_
     if (dtype != DIFFUSER_DTYPE_FP32 && dtype != DIFFUSER_DTYPE_BF16)
         return fail(DIFFUSER_ERR_UNSUPPORTED, "dtype must be FP32 or BF16");
     return DIFFUSER_OK;
+}
+
+int check_status_word(const diffuser_graph* g) {
+    const int word = g->h_status ? *reinterpret_cast<const volatile int*>(g->h_status) : 0;
+    if (word == 0) return DIFFUSER_OK;
+    return fail(DIFFUSER_ERR_DEVICE, "a kernel on this graph reported status " + std::to_string(word) +
+                                         " (results since the last reset are invalid; "
+                                         "clear it with diffuser_graph_status(reset = 1))");
 }
 
 int check_device(const diffuser_graph* g) {
@@ -362,6 +365,7 @@ int forward_device(const void* Q, const void* K, const void* V, int32_t dtype, i
     if ((st = workspace_need(g, B, H, dtype, &need))) return st;
     if ((st = check_workspace_bytes(need, workspace, workspace_bytes))) return st;
     if ((st = check_device(g))) return st;
+    if ((st = check_status_word(g))) return st;
 
     char* ws = static_cast<char*>(workspace);
     CsrArgs a{g->d_row_ptr, g->d_col, g->n, g->nnz, B * H};
@@ -478,17 +482,31 @@ int forward_host_band(const void* Q, const void* K, const void* V, int64_t B, in
     return st;
 }
 
+constexpr size_t kStatusBlockBytes = 16;
+
 int new_graph(diffuser_graph** out, diffuser_graph** g) {
     if (!out) return fail(DIFFUSER_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     *g = new (std::nothrow) diffuser_graph();
     if (!*g) return fail(DIFFUSER_ERR_ALLOC, "host allocation failed");
     (*g)->replay = new (std::nothrow) ReplayCache();   // without it, forwards launch directly
+    // status block: word, padding, then the device address of the host mirror
     cudaError_t err = cudaGetDevice(&(*g)->device);
-    if (err == cudaSuccess) err = cudaMalloc(&(*g)->d_status, sizeof(int));
-    if (err == cudaSuccess) err = cudaMemset((*g)->d_status, 0, sizeof(int));
+    int* mirror_dev = nullptr;
+    if (err == cudaSuccess) err = cudaMalloc(&(*g)->d_status, kStatusBlockBytes);
+    if (err == cudaSuccess) err = cudaHostAlloc(&(*g)->h_status, sizeof(int), cudaHostAllocMapped);
+    if (err == cudaSuccess) {
+        *(*g)->h_status = 0;
+        err = cudaHostGetDevicePointer(&mirror_dev, (*g)->h_status, 0);
+    }
+    if (err == cudaSuccess) {
+        unsigned char block[kStatusBlockBytes] = {0};
+        std::memcpy(block + 8, &mirror_dev, sizeof(mirror_dev));
+        err = cudaMemcpy((*g)->d_status, block, kStatusBlockBytes, cudaMemcpyHostToDevice);
+    }
     if (err != cudaSuccess) {
         cudaFree((*g)->d_status);
+        if ((*g)->h_status) cudaFreeHost((*g)->h_status);
         delete (*g)->replay;
         delete *g;
         *g = nullptr;
@@ -655,6 +673,7 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_t_row);
     cudaFree(g->d_t_edge);
     cudaFree(g->d_status);
+    if (g->h_status) cudaFreeHost(g->h_status);
     dfs::destroy_replay_cache(g->replay);
     delete g;
 }
@@ -720,6 +739,7 @@ int diffuser_backward(const void* Q, const void* K, const void* V, const void* d
         if ((st = plan_backward_layout(g, B * H, hops, &L))) return st;
         if ((st = check_workspace_bytes(L.total, workspace, workspace_bytes))) return st;
         if ((st = check_device(g))) return st;
+        if ((st = check_status_word(g))) return st;
         {
             // the transposed graph, built by the first backward on this graph; the
             // graph stays logically immutable (the lock orders the one-time build)
@@ -760,6 +780,7 @@ int diffuser_forward_host(const void* Q, const void* K, const void* V, int32_t d
             return fail(DIFFUSER_ERR_WORKSPACE, "workspace too small: need " +
                                                     std::to_string(need) + " bytes");
         if ((st = check_device(g))) return st;
+        if ((st = check_status_word(g))) return st;
         const size_t bytes = io_bytes(g, B, H, dtype), slot = align_up(bytes);
         char* ws = static_cast<char*>(workspace);
         char* dQ = ws;
@@ -797,6 +818,7 @@ int diffuser_attention_weights(const void* Q, const void* K, int32_t dtype, int6
         if ((st = workspace_need(g, B, H, dtype, &need))) return st;
         if ((st = check_workspace_bytes(need, workspace, workspace_bytes))) return st;
         if ((st = check_device(g))) return st;
+        if ((st = check_status_word(g))) return st;
         BandPlan bp;
         if (use_band(g, dtype, &bp)) {
             BandLayout BL;
@@ -831,6 +853,7 @@ int diffuser_diffuse_csr(const diffuser_graph* g, const float* A, const void* V,
         if ((st = plan_layout(g, B, H, &L))) return st;
         if ((st = check_workspace(L, workspace, workspace_bytes))) return st;
         if ((st = check_device(g))) return st;
+        if ((st = check_status_word(g))) return st;
         CsrArgs a{g->d_row_ptr, g->d_col, g->n, g->nnz, B * H};
         return run_hops_csr(g, a, A, V, dtype, hops, alpha, out, static_cast<char*>(workspace),
                             L, stream);
@@ -855,8 +878,25 @@ int diffuser_graph_status(const diffuser_graph* g, int* status, int reset) {
     if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
     if (dev != g->device) return fail(DIFFUSER_ERR_INVALID_ARG, "not the graph's device");
     err = cudaMemcpy(status, g->d_status, sizeof(int), cudaMemcpyDeviceToHost);
-    if (err == cudaSuccess && reset) err = cudaMemset(g->d_status, 0, sizeof(int));
+    if (err == cudaSuccess && *status == 0 && g->h_status)
+        *status = *reinterpret_cast<volatile int*>(g->h_status);
+    if (err == cudaSuccess && reset) {
+        err = cudaMemset(g->d_status, 0, sizeof(int));
+        if (g->h_status) *reinterpret_cast<volatile int*>(g->h_status) = 0;
+    }
     if (err != cudaSuccess) return cuda_fail(err, "reading the device status word");
+    return DIFFUSER_OK;
+}
+
+int diffuser_graph_set_status(const diffuser_graph* g, int status) {
+    if (!g) return fail(DIFFUSER_ERR_INVALID_ARG, "NULL argument");
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+    if (dev != g->device) return fail(DIFFUSER_ERR_INVALID_ARG, "not the graph's device");
+    err = cudaMemcpy(g->d_status, &status, sizeof(int), cudaMemcpyHostToDevice);
+    if (err != cudaSuccess) return cuda_fail(err, "writing the device status word");
+    if (g->h_status) *reinterpret_cast<volatile int*>(g->h_status) = status;
     return DIFFUSER_OK;
 }
 

@@ -84,7 +84,10 @@ struct diffuser_graph {
     int64_t* d_t_ptr = nullptr;       // [n+1]
     int32_t* d_t_row = nullptr;       // [nnz] row i of each incoming edge
     int64_t* d_t_edge = nullptr;      // [nnz] its CSR edge id
-    int* d_status = nullptr;          // device status word written by kernels (0 = ok)
+    // status block written by kernels: the word (0 = ok) at [0], the device
+    // address of h_status at byte 8 (a bounded wait that gives up writes both)
+    int* d_status = nullptr;
+    int* h_status = nullptr;          // page-locked, mapped host mirror of the word
     dfs::ReplayCache* replay = nullptr;   // captured band-path forwards (see abi.cu)
     // host copy of the CSR
     std::vector<int64_t> h_row_ptr;
@@ -97,6 +100,29 @@ namespace dfs {
 // ---- status plumbing (abi.cu) -------------------------------------------------
 int fail(int status, const std::string& msg);
 int cuda_fail(cudaError_t err, const char* what);
+
+// DIFFUSER_ERR_DEVICE when a kernel has reported a failure on g since the last
+// reset (read from the host mirror of the status word: no synchronization).
+int check_status_word(const diffuser_graph* g);
+
+// ---- argument checks and the CSR path's workspace (abi.cu) ------------------
+// CSR-path workspace: [A: units*nnz fp32][Z ping: units*n*64 fp32][Z pong: same],
+// each region 256-byte aligned.
+struct Layout {
+    size_t a_off, z0_off, z1_off, total;
+};
+int plan_layout(const diffuser_graph* g, int64_t B, int64_t H, Layout* L);   // OVERFLOW-checked
+int check_shape(const diffuser_graph* g, int64_t B, int64_t H, int32_t d, int32_t dtype);
+int check_device(const diffuser_graph* g);
+bool aligned16(const void* p);
+size_t io_bytes(const diffuser_graph* g, int64_t B, int64_t H, int32_t dtype);
+bool overlaps(const void* a, size_t na, const void* b, size_t nb);
+struct CsrArgs;
+// The hops over weights already in A (CSR order): Z_0 = V, the last hop writes
+// out; hops = 0 copies V to out.  The hop state lives in ws at L's offsets.
+int run_hops_csr(const diffuser_graph* g, const CsrArgs& a, const float* A, const void* V,
+                 int32_t dtype, int32_t hops, float alpha, void* out, char* ws, const Layout& L,
+                 cudaStream_t stream);
 
 // ---- launch accounting and profiling (abi.cu) ------------------------------
 // Brackets one kernel launch: counts it and, while a profile is open, records

@@ -72,10 +72,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
+// The status block of a graph: the status word at status[0] and, at byte
+// offset 8, the device address of a page-locked host mirror of it (or null).
+// A wait that gives up writes both, so that the host can see the failure
+// without synchronizing (the next forward then refuses to run).
+__device__ __forceinline__ void record_status(int* status, int code) {
+    atomicExch(status, code);
+    int* mirror = *reinterpret_cast<int* const volatile*>(status + 2);
+    if (mirror) *reinterpret_cast<volatile int*>(mirror) = code;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after about
 // two seconds (or at once when another wait has already given up), records
-// kStatusTimeout in *status and returns false; callers carry on so that the
-// kernel always terminates.
+// kStatusTimeout in the status block and returns false; callers carry on so
+// that the kernel always terminates.
 // The common case (already complete) costs one non-blocking test; after that
 // the thread sleeps in the barrier unit instead of polling it, so that waiting
 // warps do not slow down the barrier operations of the others.  The status
@@ -87,7 +97,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 15) == 0 &&
             (*reinterpret_cast<volatile int*>(status) != 0 || globaltimer() - t0 > kWaitLimitNs)) {
-            atomicExch(status, kStatusTimeout);
+            record_status(status, kStatusTimeout);
             return false;
         }
     }

@@ -85,3 +85,23 @@ def test_backward_special_cases_and_repeatability(dl):
     b = dl.diffuser_backward(Q, K, V, dO, g, 5, 0.1)
     torch.cuda.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(a, b))
+
+
+def test_backward_full_text_sampled_unit(dl):
+    """The text workload at full size (2 x 12 units, n = 4096, E = 2,271,946, K = 5),
+    bf16: one sampled (batch, head) unit of every gradient against the oracle's
+    backward on that unit alone (the units are independent)."""
+    import torch
+    from sparse_long_sequence_gb300 import workloads
+    w = workloads.TEXT
+    g = dl.diffuser_build_graph(w.n, w.r, w.n_globals, rand_per_row=w.rand_per_row, seed=w.seed)
+    o_ptr, o_col = oracle.token_graph(w.n, w.r, w.n_globals, w.rand_per_row, seed=w.seed)
+    Q, K, V = synthetic.qkv(w.B, w.H, w.n, w.d, w.dtype, seed=w.seed)
+    dO = synthetic.qkv(w.B, w.H, w.n, w.d, w.dtype, seed=w.seed + 1)[0]
+    grads = dl.diffuser_backward(*(to_device(x, w.dtype) for x in (Q, K, V, dO)), g, w.hops, w.alpha)
+    torch.cuda.synchronize()
+    b, h = 1, 7
+    ref = oracle.backward(*(oracle.widen(x[b, h], w.dtype) for x in (Q, K, V, dO)), o_ptr, o_col,
+                          w.hops, w.alpha)
+    for got, want in zip(grads, ref):
+        check_grad(to_f64(got[b, h]), want, w.dtype)
