@@ -78,6 +78,10 @@ def _load():
                                                    ctypes.c_int32, _i32p, ctypes.c_int32,
                                                    ctypes.c_uint64, ctypes.c_int32, _i64p, _i32p,
                                                    ctypes.c_int64, _i64p]
+        lib.oracle_token_graph_uniform.restype = ctypes.c_int
+        lib.oracle_token_graph_uniform.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                   _i32p, ctypes.c_int32, ctypes.c_int32, _i64p,
+                                                   _i32p, ctypes.c_int64, _i64p]
         lib.oracle_block_graph.restype = ctypes.c_int
         lib.oracle_block_graph.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64, _i64p,
@@ -158,6 +162,40 @@ def dilated_graph(n: int, r: int, dilation: int, n_globals: int, rand_per_row: i
                                           int(causal), _p(row_ptr, _i64p), _p(col, _i32p),
                                           col.size, ctypes.byref(nnz)), "dilated_graph")
     return row_ptr, col[: nnz.value]
+
+
+def uniform_graph(n: int, r: int, n_globals: int, rand_per_row: int, globals_idx=None,
+                  causal: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """CSR of the token graph whose R extras of row i sit on the uniform grid
+    j_t = (i + floor((2t + 1) n / (2R))) mod n ("w uni.", Diffuser notes sec 4.5,
+    Tab S.7), with the causal mask when ``causal``."""
+    lib = _load()
+    g = None
+    if globals_idx is not None:
+        g = np.ascontiguousarray(np.asarray(globals_idx, dtype=np.int32))
+        n_globals = int(g.size)
+    gp = _p(g, _i32p) if g is not None else None
+    nnz = ctypes.c_int64(0)
+    _check(lib.oracle_token_graph_uniform(n, r, n_globals, gp, rand_per_row, int(causal), None,
+                                          None, 0, ctypes.byref(nnz)), "uniform_graph(count)")
+    row_ptr = np.zeros(n + 1, dtype=np.int64)
+    col = np.zeros(max(nnz.value, 1), dtype=np.int32)
+    _check(lib.oracle_token_graph_uniform(n, r, n_globals, gp, rand_per_row, int(causal),
+                                          _p(row_ptr, _i64p), _p(col, _i32p), col.size,
+                                          ctypes.byref(nnz)), "uniform_graph")
+    return row_ptr, col[: nnz.value]
+
+
+def forward_per_head(Q: np.ndarray, K: np.ndarray, V: np.ndarray, graphs, hops: int,
+                     alpha: float, nthreads: int = 1) -> np.ndarray:
+    """The forward with one graph per head (Diffuser notes sec 2.2: the random
+    sets may differ per layer and per head): head h of every batch item runs on
+    graphs[h] = (row_ptr, col).  Q, K, V float64 [B][H][n][d]."""
+    Q, K, V = (np.asarray(x, dtype=np.float64) for x in (Q, K, V))
+    out = np.zeros_like(V)
+    for h, (row_ptr, col) in enumerate(graphs):
+        out[:, h] = forward(Q[:, h], K[:, h], V[:, h], row_ptr, col, hops, alpha, nthreads=nthreads)
+    return out
 
 
 def block_graph(n: int, block: int, window_blocks: int, rand_blocks: int, global_blocks: int,

@@ -48,6 +48,11 @@
  *     three edge kinds ([D] sec 2.6; [S] sec 1.1 for the causal window):
  *     window [i-r, i], globals g <= i, a global row reads 0..i, and a random
  *     draw that lands after i is dropped, not redrawn.
+ *   - Uniform-spaced extras ("w uni." of [D] sec 4.5, Tab S.7: the random
+ *     edges' positions are taken at uniform spacing instead of at random;
+ *     the spacing rule is not given): the R positions of row i are the
+ *     uniform grid of spacing n/R on the ring of positions, offset by half a
+ *     spacing from i:  j_t = (i + floor((2t + 1) n / (2R))) mod n,  t < R.
  *
  * Everything is computed in double precision, in the plainest loop order.
  */
@@ -99,7 +104,7 @@ static int64_t emit_row(const unsigned char* mark, int64_t n, int32_t* col,
  */
 static int token_graph(int64_t n, int32_t r, int32_t dilation, int32_t n_globals,
                        const int32_t* globals, int32_t rand_per_row,
-                       uint64_t seed, int causal, int64_t* row_ptr, int32_t* col,
+                       uint64_t seed, int causal, int uniform, int64_t* row_ptr, int32_t* col,
                        int64_t col_capacity, int64_t* nnz_out) {
     if (n < 1 || n > INT32_MAX || r < 0 || dilation < 1 || n_globals < 0 || n_globals > n ||
         rand_per_row < 0 || !nnz_out)
@@ -128,8 +133,14 @@ static int token_graph(int64_t n, int32_t r, int32_t dilation, int32_t n_globals
             for (int64_t j = 0; j < n; ++j)              /* every row reads G, eq 12 */
                 if (is_global[j]) mark[j] = 1;
             for (int32_t t = 0; t < rand_per_row; ++t) { /* random draws */
-                uint64_t key = (uint64_t)i * (uint64_t)rand_per_row + (uint64_t)t;
-                uint64_t j = oracle_splitmix64(seed ^ key) % (uint64_t)n;
+                uint64_t j;
+                if (uniform) {                           /* "w uni.": uniform grid from i */
+                    int64_t off = ((int64_t)(2 * t + 1) * n) / (2 * (int64_t)rand_per_row);
+                    j = (uint64_t)((i + off) % n);
+                } else {
+                    uint64_t key = (uint64_t)i * (uint64_t)rand_per_row + (uint64_t)t;
+                    j = oracle_splitmix64(seed ^ key) % (uint64_t)n;
+                }
                 mark[j] = 1;
             }
         }
@@ -149,7 +160,7 @@ int oracle_token_graph(int64_t n, int32_t r, int32_t n_globals,
                        const int32_t* globals, int32_t rand_per_row,
                        uint64_t seed, int64_t* row_ptr, int32_t* col,
                        int64_t col_capacity, int64_t* nnz_out) {
-    return token_graph(n, r, 1, n_globals, globals, rand_per_row, seed, 0, row_ptr,
+    return token_graph(n, r, 1, n_globals, globals, rand_per_row, seed, 0, 0, row_ptr,
                        col, col_capacity, nnz_out);
 }
 
@@ -167,7 +178,7 @@ int oracle_token_graph_causal(int64_t n, int32_t r, int32_t n_globals,
                               const int32_t* globals, int32_t rand_per_row,
                               uint64_t seed, int64_t* row_ptr, int32_t* col,
                               int64_t col_capacity, int64_t* nnz_out) {
-    return token_graph(n, r, 1, n_globals, globals, rand_per_row, seed, 1, row_ptr,
+    return token_graph(n, r, 1, n_globals, globals, rand_per_row, seed, 1, 0, row_ptr,
                        col, col_capacity, nnz_out);
 }
 
@@ -182,8 +193,22 @@ int oracle_token_graph_dilated(int64_t n, int32_t r, int32_t dilation, int32_t n
                                const int32_t* globals, int32_t rand_per_row, uint64_t seed,
                                int32_t causal, int64_t* row_ptr, int32_t* col,
                                int64_t col_capacity, int64_t* nnz_out) {
-    return token_graph(n, r, dilation, n_globals, globals, rand_per_row, seed, causal != 0,
+    return token_graph(n, r, dilation, n_globals, globals, rand_per_row, seed, causal != 0, 0,
                        row_ptr, col, col_capacity, nnz_out);
+}
+
+/*
+ * Token graph with uniform-spaced extras ([D] sec 4.5, Tab S.7, "w uni."):
+ * the token graph (or, with causal != 0, the causal token graph) whose R
+ * random draws of row i are replaced by the positions
+ *   j_t = (i + floor((2t + 1) n / (2R))) mod n,  t < R
+ * (R >= 1 when used; R = 0 gives the plain window-and-globals graph).
+ */
+int oracle_token_graph_uniform(int64_t n, int32_t r, int32_t n_globals, const int32_t* globals,
+                               int32_t rand_per_row, int32_t causal, int64_t* row_ptr,
+                               int32_t* col, int64_t col_capacity, int64_t* nnz_out) {
+    return token_graph(n, r, 1, n_globals, globals, rand_per_row, 0, causal != 0, 1, row_ptr,
+                       col, col_capacity, nnz_out);
 }
 
 /*
