@@ -140,6 +140,22 @@ DIFFUSER_API int diffuser_build_dilated_graph(int64_t n, int32_t r, int32_t dila
                                  diffuser_graph** out);
 
 /*
+ * Token graph with uniform-spaced extras ([D] sec 4.5, Tab S.7, the "w uni."
+ * ablation: the positions of the random edges are taken at uniform spacing
+ * instead of at random; the pages do not give the spacing rule).  As
+ * diffuser_build_graph (causal != 0: diffuser_build_causal_graph) with the R
+ * draws of row i replaced by the uniform grid of spacing n / R on the ring of
+ * positions, half a spacing on from i:
+ *   j_t = (i + floor((2t + 1) n / (2R))) mod n,  t < R = positions_per_row,
+ * entering once where they fall on the window or a global.  No seed: the
+ * graph is deterministic.  positions_per_row 0..1024.  The forward picks its
+ * path as for diffuser_build_graph.  Errors: as diffuser_build_graph.
+ */
+DIFFUSER_API int diffuser_build_uniform_graph(int64_t n, int32_t r, int32_t n_globals,
+                                              const int32_t* global_idx, int32_t positions_per_row,
+                                              int32_t causal, diffuser_graph** out);
+
+/*
  * BigBird ITC block graph ([S] sec 2 eq 13 and its 12-block example; [B]
  * sec 2).  N = ceil(n/block) blocks (the last one may be ragged).  Block row
  * J < global_blocks reads every block.  Any other block row J reads the
@@ -269,6 +285,34 @@ DIFFUSER_API int diffuser_backward(const void* Q, const void* K, const void* V, 
                       int32_t dtype, int64_t B, int64_t H, int32_t d, const diffuser_graph* g,
                       int32_t hops, float alpha, void* dQ, void* dK, void* dV, void* workspace,
                       size_t workspace_bytes, diffuser_stream stream);
+
+/* ---------------------------------------------------------------- one graph per head */
+
+/*
+ * diffuser_forward with a graph of its own for every head ([D] sec 2.2 and
+ * [S] sec 2: the random connections may differ per layer and per head; a
+ * per-layer graph is one graph object per layer).  Head h of every batch item
+ * runs on graphs[h]; the heads' graphs must share n and the device.  Q, K, V,
+ * out, hops, alpha, stream and the aliasing rules are those of
+ * diffuser_forward.
+ *   graphs      host array of H graph pointers (may repeat a graph)
+ *   workspace   device, >= diffuser_per_head_workspace_size bytes, 256-byte
+ *               aligned: for B > 1, staging for one head's Q, K, V and out
+ *               (4 B n d elements; a head's slices are strided in BHSD, so each
+ *               head is gathered into it with one strided copy per tensor and
+ *               its output scattered back), then the largest per-head
+ *               diffuser_forward workspace for B units.  For B = 1 the heads
+ *               are contiguous and run in place (no staging).
+ * The heads run one after the other on `stream`.  Errors: as
+ * diffuser_forward (INVALID_ARG also for a NULL or mismatched graph).
+ */
+DIFFUSER_API int diffuser_per_head_workspace_size(const diffuser_graph* const* graphs, int64_t B,
+                                                  int64_t H, int32_t d, int32_t dtype, size_t* bytes);
+DIFFUSER_API int diffuser_forward_per_head(const void* Q, const void* K, const void* V, int32_t dtype,
+                                           int64_t B, int64_t H, int32_t d,
+                                           const diffuser_graph* const* graphs, int32_t hops,
+                                           float alpha, void* out, void* workspace,
+                                           size_t workspace_bytes, diffuser_stream stream);
 
 /* ---------------------------------------------------------------- no-allocation forward */
 

@@ -72,6 +72,12 @@ def _load() -> ctypes.CDLL:
         "diffuser_no_alloc_scratch_bytes": (c.c_size_t, []),
         "diffuser_set_path": (c.c_int, [c.c_int]),
         "diffuser_get_path": (c.c_int, []),
+        "diffuser_build_uniform_graph": (c.c_int, [i64, i32, i32, c.POINTER(c.c_int32), i32, i32,
+                                                   c.POINTER(vp)]),
+        "diffuser_per_head_workspace_size": (c.c_int, [c.POINTER(vp), i64, i64, i32, i32,
+                                                       c.POINTER(c.c_size_t)]),
+        "diffuser_forward_per_head": (c.c_int, [vp, vp, vp, i32, i64, i64, i32, c.POINTER(vp), i32,
+                                                c.c_float, vp, vp, c.c_size_t, vp]),
         "diffuser_graph_status": (c.c_int, [vp, c.POINTER(c.c_int), c.c_int]),
         "diffuser_graph_set_status": (c.c_int, [vp, c.c_int]),
         "diffuser_launch_count": (c.c_int64, [i64p]),
@@ -162,6 +168,20 @@ def diffuser_build_dilated_graph(n: int, r: int, dilation: int, n_globals: int, 
     return Graph(out.value)
 
 
+def diffuser_build_uniform_graph(n: int, r: int, n_globals: int, global_idx=None,
+                                 positions_per_row: int = 0, causal: bool = False) -> Graph:
+    """Token graph whose extras sit on a uniform grid ("w uni."), no seed."""
+    gp = None
+    if global_idx is not None:
+        gl = np.ascontiguousarray(np.asarray(global_idx, dtype=np.int32))
+        n_globals = int(gl.size)
+        gp = gl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    out = ctypes.c_void_p()
+    _check(_lib.diffuser_build_uniform_graph(n, r, n_globals, gp, positions_per_row, int(causal),
+                                             ctypes.byref(out)), "diffuser_build_uniform_graph")
+    return Graph(out.value)
+
+
 def diffuser_build_block_graph(n: int, block: int, window_blocks: int, rand_blocks: int,
                                global_blocks: int, seed: int = 0) -> Graph:
     out = ctypes.c_void_p()
@@ -245,6 +265,36 @@ def diffuser_forward(Q, K, V, g: Graph, hops: int, alpha: float, out=None, works
     _check(_lib.diffuser_forward(Q.data_ptr(), K.data_ptr(), V.data_ptr(), code, B, H, d,
                                  g.handle, hops, alpha, out.data_ptr(), workspace.data_ptr(),
                                  workspace.numel(), _stream(stream)), "diffuser_forward")
+    return out
+
+
+def _graph_array(graphs):
+    return (ctypes.c_void_p * len(graphs))(*[g.handle.value for g in graphs])
+
+
+def diffuser_per_head_workspace_size(graphs, B: int, H: int, d: int, dtype: int) -> int:
+    b = ctypes.c_size_t()
+    _check(_lib.diffuser_per_head_workspace_size(_graph_array(graphs), B, H, d, dtype,
+                                                 ctypes.byref(b)), "diffuser_per_head_workspace_size")
+    return b.value
+
+
+def diffuser_forward_per_head(Q, K, V, graphs, hops: int, alpha: float, out=None, workspace=None,
+                              stream=None):
+    """The forward with graphs[h] for head h (device tensors [B][H][n][d])."""
+    import torch
+    B, H, n, d = Q.shape
+    if len(graphs) != H:
+        raise ValueError("one graph per head is needed")
+    code = _dtype_code(Q)
+    if out is None:
+        out = torch.empty_like(V)
+    if workspace is None:
+        workspace = alloc_workspace(diffuser_per_head_workspace_size(graphs, B, H, d, code), Q.device)
+    _check(_lib.diffuser_forward_per_head(Q.data_ptr(), K.data_ptr(), V.data_ptr(), code, B, H, d,
+                                          _graph_array(graphs), hops, alpha, out.data_ptr(),
+                                          workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "diffuser_forward_per_head")
     return out
 
 

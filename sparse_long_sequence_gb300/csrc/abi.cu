@@ -552,7 +552,7 @@ namespace {
 
 int build_token_graph(int64_t n, int32_t r, int32_t dilation, int32_t n_globals,
                       const int32_t* global_idx, int32_t rand_per_row, uint64_t seed, bool causal,
-                      diffuser_graph** out) {
+                      diffuser_graph** out, bool uniform = false) {
     try {
         if (n < 1 || n > INT32_MAX) return fail(DIFFUSER_ERR_INVALID_ARG, "n out of range");
         if (r < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "r must be >= 0");
@@ -583,6 +583,7 @@ int build_token_graph(int64_t n, int32_t r, int32_t dilation, int32_t n_globals,
         g->rand_per_row = rand_per_row;
         g->causal = causal;
         g->dilation = dilation;
+        g->uniform = uniform ? 1 : 0;
         g->seed = seed;
         g->h_globals = std::move(G);
         st = dilation > 1 ? build_dilated_graph_device(g, nullptr) : build_token_graph_device(g, nullptr);
@@ -612,6 +613,12 @@ int diffuser_build_dilated_graph(int64_t n, int32_t r, int32_t dilation, int32_t
                                  int32_t causal, diffuser_graph** out) {
     return build_token_graph(n, r, dilation, n_globals, global_idx, rand_per_row, seed,
                              causal != 0, out);
+}
+
+int diffuser_build_uniform_graph(int64_t n, int32_t r, int32_t n_globals, const int32_t* global_idx,
+                                 int32_t positions_per_row, int32_t causal, diffuser_graph** out) {
+    return build_token_graph(n, r, 1, n_globals, global_idx, positions_per_row, 0, causal != 0, out,
+                             true);
 }
 
 int diffuser_build_block_graph(int64_t n, int32_t block, int32_t window_blocks,
@@ -750,6 +757,116 @@ int diffuser_backward(const void* Q, const void* K, const void* V, const void* d
         return launch_backward_csr(g, B * H, Q, K, V, dOut, dtype, hops, alpha, dQ, dK, dV,
                                    static_cast<char*>(workspace), L,
                                    static_cast<cudaStream_t>(stream));
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+namespace {
+
+// The per-head forward's workspace: device staging for one head's Q, K, V and
+// out slices when B > 1 (a head's [B][n][d] slice is strided in BHSD), then the
+// largest per-head forward workspace for B units.
+int per_head_need(const diffuser_graph* const* graphs, int64_t B, int64_t H, int32_t d,
+                  int32_t dtype, size_t* staging, size_t* need) {
+    if (!graphs) return fail(DIFFUSER_ERR_INVALID_ARG, "graphs is NULL");
+    int st = check_shape(graphs[0], B, H, d, dtype);
+    if (st) return st;
+    size_t fwd = 0;
+    for (int64_t h = 0; h < H; ++h) {
+        const diffuser_graph* g = graphs[h];
+        if (!g) return fail(DIFFUSER_ERR_INVALID_ARG, "a head's graph is NULL");
+        if (g->n != graphs[0]->n) return fail(DIFFUSER_ERR_INVALID_ARG, "the heads' graphs differ in n");
+        if (g->device != graphs[0]->device)
+            return fail(DIFFUSER_ERR_INVALID_ARG, "the heads' graphs live on different devices");
+        size_t one = 0;
+        if ((st = workspace_need(g, B, 1, dtype, &one))) return st;
+        if (one > fwd) fwd = one;
+    }
+    *staging = B > 1 ? 4 * align_up(io_bytes(graphs[0], B, 1, dtype)) : 0;
+    *need = *staging + fwd;
+    return DIFFUSER_OK;
+}
+
+}  // namespace
+
+int diffuser_per_head_workspace_size(const diffuser_graph* const* graphs, int64_t B, int64_t H,
+                                     int32_t d, int32_t dtype, size_t* bytes) {
+    try {
+        if (!bytes) return fail(DIFFUSER_ERR_INVALID_ARG, "bytes is NULL");
+        size_t staging = 0;
+        return per_head_need(graphs, B, H, d, dtype, &staging, bytes);
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+int diffuser_forward_per_head(const void* Q, const void* K, const void* V, int32_t dtype,
+                              int64_t B, int64_t H, int32_t d, const diffuser_graph* const* graphs,
+                              int32_t hops, float alpha, void* out, void* workspace,
+                              size_t workspace_bytes, diffuser_stream stream) {
+    try {
+        size_t staging = 0, need = 0;
+        int st = per_head_need(graphs, B, H, d, dtype, &staging, &need);
+        if (st) return st;
+        const diffuser_graph* g0 = graphs[0];
+        if (!Q || !K || !V || !out) return fail(DIFFUSER_ERR_INVALID_ARG, "a tensor pointer is NULL");
+        if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+        if (hops < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "hops must be >= 0");
+        if (!(alpha >= 0.f && alpha <= 1.f))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "alpha must lie in [0, 1]");
+        const size_t bytes = io_bytes(g0, B, H, dtype);
+        if (overlaps(out, bytes, Q, bytes) || overlaps(out, bytes, K, bytes))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "out overlaps Q or K");
+        if (hops > 0 && overlaps(out, bytes, V, bytes))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "out may alias V only when hops == 0");
+        if ((st = check_workspace_bytes(need, workspace, workspace_bytes))) return st;
+        for (int64_t h = 0; h < H; ++h) {
+            if ((st = check_device(graphs[h]))) return st;
+            if ((st = check_status_word(graphs[h]))) return st;
+        }
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if (hops == 0) {
+            if (out == V) return DIFFUSER_OK;
+            cudaError_t err = cudaMemcpyAsync(out, V, bytes, cudaMemcpyDeviceToDevice, s);
+            return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "copying V to out (hops = 0)");
+        }
+        const size_t slice = io_bytes(g0, 1, 1, dtype);         // one [n][d] head slice
+        const char* q = static_cast<const char*>(Q);
+        const char* k = static_cast<const char*>(K);
+        const char* v = static_cast<const char*>(V);
+        char* o = static_cast<char*>(out);
+        char* ws = static_cast<char*>(workspace);
+        for (int64_t h = 0; h < H; ++h) {
+            const size_t at = (size_t)h * slice;
+            if (B == 1) {
+                // head h's slices are contiguous: run it in place
+                st = forward_device(q + at, k + at, v + at, dtype, 1, 1, d, graphs[h], hops, alpha,
+                                    o + at, ws, workspace_bytes, s);
+                if (st) return st;
+                continue;
+            }
+            // gather head h of every batch item (B rows of `slice` bytes, H slices apart),
+            // run the B units, scatter the output back
+            const size_t seg = staging / 4, pitch = (size_t)H * slice;
+            char* sq = ws;
+            char* sk = ws + seg;
+            char* sv = ws + 2 * seg;
+            char* so = ws + 3 * seg;
+            cudaError_t err = cudaMemcpy2DAsync(sq, slice, q + at, pitch, slice, B, cudaMemcpyDeviceToDevice, s);
+            if (err == cudaSuccess)
+                err = cudaMemcpy2DAsync(sk, slice, k + at, pitch, slice, B, cudaMemcpyDeviceToDevice, s);
+            if (err == cudaSuccess)
+                err = cudaMemcpy2DAsync(sv, slice, v + at, pitch, slice, B, cudaMemcpyDeviceToDevice, s);
+            if (err != cudaSuccess) return cuda_fail(err, "gathering a head's slices");
+            st = forward_device(sq, sk, sv, dtype, B, 1, d, graphs[h], hops, alpha, so, ws + staging,
+                                workspace_bytes - staging, s);
+            if (st) return st;
+            err = cudaMemcpy2DAsync(o + at, pitch, so, slice, slice, B, cudaMemcpyDeviceToDevice, s);
+            if (err != cudaSuccess) return cuda_fail(err, "scattering a head's output");
+        }
+        return DIFFUSER_OK;
     } catch (...) {
         return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
     }

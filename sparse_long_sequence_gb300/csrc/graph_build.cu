@@ -8,8 +8,9 @@
 //   i in G:  N(i) = {0..n-1}
 //   else:    N(i) = window [i-r, i+r] cut to [0,n)  u  G  u  extras(i)
 // where extras(i) are the random draws splitmix64(seed ^ (i*R + t)) mod n
-// that fall outside the window and outside G, sorted and deduplicated.  The
-// three parts are disjoint, so a row is a merge of three sorted lists.
+// (or, for the uniform-spaced variant, the grid positions of row_draw) that
+// fall outside the window and outside G, sorted and deduplicated.  The three
+// parts are disjoint, so a row is a merge of three sorted lists.
 //
 // Causal token graph (Diffuser notes sec 2.6: A lower-triangular, every edge
 // obeys j <= i; sliding-window page sec 1.1: the causal window holds the r+1
@@ -58,7 +59,18 @@ struct TokenParams {
     const int32_t* globals;
     const uint8_t* is_global;
     int32_t causal;
+    int32_t uniform;     // 1: the R extras of a row sit on a uniform grid instead of random draws
 };
+
+// Extra t of row i: the random draw splitmix64(seed ^ (i R + t)) mod n, or on
+// the uniform grid ("w uni.", Diffuser notes sec 4.5, Tab S.7; the spacing
+// rule is not given): i + floor((2t + 1) n / (2R)) mod n, half a spacing on
+// from i, spacing n / R around the ring of positions.
+__device__ __forceinline__ int64_t row_draw(const TokenParams& p, int64_t i, int32_t t) {
+    if (p.uniform) return (i + ((int64_t)(2 * t + 1) * p.n) / (2 * (int64_t)p.R)) % p.n;
+    const uint64_t key = (uint64_t)i * (uint64_t)p.R + (uint64_t)t;
+    return (int64_t)(splitmix64(p.seed ^ key) % (uint64_t)p.n);
+}
 
 // last column row i may read: i for the causal graph, else n-1
 __device__ __forceinline__ int64_t row_last(const TokenParams& p, int64_t i) {
@@ -79,8 +91,7 @@ __device__ int32_t row_extras(const TokenParams& p, int64_t i, int64_t lo, int64
                               int32_t* xs) {
     int32_t cnt = 0;
     for (int32_t t = 0; t < p.R; ++t) {
-        uint64_t key = (uint64_t)i * (uint64_t)p.R + (uint64_t)t;
-        int64_t j = (int64_t)(splitmix64(p.seed ^ key) % (uint64_t)p.n);
+        const int64_t j = row_draw(p, i, t);
         if (j > row_last(p, i) || (j >= lo && j <= hi) || p.is_global[j]) continue;
         // insertion into the sorted prefix, dropping duplicates
         int32_t pos = cnt;
@@ -172,8 +183,7 @@ __global__ void token_fill_kernel(TokenParams p, const int64_t* row_ptr, int32_t
 __device__ int32_t row_draws(const TokenParams& p, int64_t i, int64_t last, int32_t* xs) {
     int32_t cnt = 0;
     for (int32_t t = 0; t < p.R; ++t) {
-        uint64_t key = (uint64_t)i * (uint64_t)p.R + (uint64_t)t;
-        int64_t j = (int64_t)(splitmix64(p.seed ^ key) % (uint64_t)p.n);
+        const int64_t j = row_draw(p, i, t);
         if (j > last) continue;
         int32_t pos = cnt;
         while (pos > 0 && xs[pos - 1] > j) --pos;
@@ -439,7 +449,7 @@ int build_token_graph_device(diffuser_graph* g, cudaStream_t stream) {
     if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(counts) failed");
 
     TokenParams p{n,        g->r,           g->n_globals,   g->rand_per_row,
-                  g->seed,  g->d_globals,   g->d_is_global, g->causal ? 1 : 0};
+                  g->seed,  g->d_globals,   g->d_is_global, g->causal ? 1 : 0, g->uniform};
     // per-thread scratch for the extras lives in shared memory; keep it <= 48 KB
     int threads = 128;
     while (threads > 1 && (size_t)threads * p.R * sizeof(int32_t) > 48 * 1024) threads >>= 1;
@@ -483,7 +493,7 @@ int build_dilated_graph_device(diffuser_graph* g, cudaStream_t stream) {
     err = cudaMalloc(&d_counts, sizeof(int64_t) * n);
     if (err != cudaSuccess) return fail(DIFFUSER_ERR_ALLOC, "cudaMalloc(counts) failed");
     TokenParams p{n,       g->r,         g->n_globals,   g->rand_per_row,
-                  g->seed, g->d_globals, g->d_is_global, g->causal ? 1 : 0};
+                  g->seed, g->d_globals, g->d_is_global, g->causal ? 1 : 0, g->uniform};
     // per-thread scratch for the draws lives in shared memory; keep it <= 48 KB
     int threads = 128;
     while (threads > 1 && (size_t)threads * p.R * sizeof(int32_t) > 48 * 1024) threads >>= 1;

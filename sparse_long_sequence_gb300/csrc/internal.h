@@ -67,6 +67,7 @@ struct diffuser_graph {
     int32_t r = 0, n_globals = 0, rand_per_row = 0;
     bool causal = false;              // token graph cut to j <= i
     int32_t dilation = 1;             // token graph: spacing of the window's positions
+    int32_t uniform = 0;              // token graph: extras on a uniform grid, not random draws
     // block graph parameters
     int32_t block = 0, window_blocks = 0, rand_blocks = 0, global_blocks = 0;
     uint64_t seed = 0;
