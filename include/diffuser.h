@@ -395,6 +395,22 @@ typedef enum {
 DIFFUSER_API int diffuser_set_path(int path);
 DIFFUSER_API int diffuser_get_path(void);
 
+/* Kernel families a forward can run on. */
+typedef enum {
+    DIFFUSER_KERNELS_CSR = 1,     /* general CSR SIMT kernels (fp32 arithmetic) */
+    DIFFUSER_KERNELS_BAND = 2,    /* token graphs: tcgen05 window tiles + random-edge gathers */
+    DIFFUSER_KERNELS_BLOCK = 3    /* block graphs of 64-token blocks: tcgen05 block-sparse tiles */
+} diffuser_kernels;
+
+/*
+ * The kernel family diffuser_forward would run for graph g and this dtype
+ * under the current path selection (a diffuser_kernels value in *kernels).
+ * The band family serves token graphs with bf16 I/O, window radius >= 8,
+ * dilation 1 and at most 32 globals; the block family serves block graphs of
+ * 64-token blocks with bf16 I/O; everything else runs the CSR family.
+ */
+DIFFUSER_API int diffuser_kernels_for(const diffuser_graph* g, int32_t dtype, int* kernels);
+
 /*
  * Read (synchronously) the device status word that the graph's kernels set
  * when a bounded internal wait gives up (0 = no error); reset != 0 clears it

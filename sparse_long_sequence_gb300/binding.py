@@ -78,6 +78,7 @@ def _load() -> ctypes.CDLL:
                                                        c.POINTER(c.c_size_t)]),
         "diffuser_forward_per_head": (c.c_int, [vp, vp, vp, i32, i64, i64, i32, c.POINTER(vp), i32,
                                                 c.c_float, vp, vp, c.c_size_t, vp]),
+        "diffuser_kernels_for": (c.c_int, [vp, i32, c.POINTER(c.c_int)]),
         "diffuser_graph_status": (c.c_int, [vp, c.POINTER(c.c_int), c.c_int]),
         "diffuser_graph_set_status": (c.c_int, [vp, c.c_int]),
         "diffuser_launch_count": (c.c_int64, [i64p]),
@@ -389,6 +390,16 @@ def diffuser_set_path(path: int) -> None:
 
 def diffuser_get_path() -> int:
     return int(_lib.diffuser_get_path())
+
+
+DIFFUSER_KERNELS_CSR, DIFFUSER_KERNELS_BAND, DIFFUSER_KERNELS_BLOCK = 1, 2, 3
+
+
+def diffuser_kernels_for(g: Graph, dtype: int) -> int:
+    """The kernel family a forward on g with this dtype runs (DIFFUSER_KERNELS_*)."""
+    k = ctypes.c_int()
+    _check(_lib.diffuser_kernels_for(g.handle, dtype, ctypes.byref(k)), "diffuser_kernels_for")
+    return k.value
 
 
 def diffuser_graph_status(g: Graph, reset: bool = False) -> int:

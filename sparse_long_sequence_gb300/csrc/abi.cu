@@ -182,7 +182,19 @@ int workspace_need(const diffuser_graph* g, int64_t B, int64_t H, int32_t dtype,
         if ((st = plan_band_layout(g, bp, B * H, &BL))) return st;
         if (BL.total > *need) *need = BL.total;
     }
+    if (dtype == DIFFUSER_DTYPE_BF16 && block_eligible(g)) {
+        BlockLayout KL;
+        if ((st = plan_block_layout(g, B * H, &KL))) return st;
+        if (KL.total > *need) *need = KL.total;
+    }
     return DIFFUSER_OK;
+}
+
+// The block-sparse tensor-core path serves block graphs of 64-token blocks with
+// bf16 I/O (the general CSR path runs everything else).
+bool use_block(const diffuser_graph* g, int32_t dtype) {
+    if (g_path.load() == DIFFUSER_PATH_CSR) return false;
+    return dtype == DIFFUSER_DTYPE_BF16 && block_eligible(g);
 }
 
 // The hops over weights already in A (CSR order): Z_0 = V, last hop -> out.
@@ -381,6 +393,14 @@ int forward_device(const void* Q, const void* K, const void* V, int32_t dtype, i
             int r = launch_band_scores(g, bp, B * H, Q, K, V, ws, BL, false, s);
             if (!r) r = launch_band_hops(g, bp, B * H, Q, K, V, hops, alpha, out, ws, BL, s);
             return r;
+        });
+    }
+    if (use_block(g, dtype)) {
+        BlockLayout KL;
+        if ((st = plan_block_layout(g, B * H, &KL))) return st;
+        const ReplayKey key{Q, K, V, out, workspace, workspace_bytes, B, H, dtype, hops, alpha, g_path.load()};
+        return band_forward(g, key, stream, [&](cudaStream_t s) {
+            return launch_block_forward(g, B * H, Q, K, V, hops, alpha, out, ws, KL, s);
         });
     }
     float* A = reinterpret_cast<float*>(ws + L.a_off);
@@ -645,6 +665,7 @@ int diffuser_build_block_graph(int64_t n, int32_t block, int32_t window_blocks,
         g->global_blocks = global_blocks;
         g->seed = seed;
         st = build_block_graph_device(g, nullptr);
+        if (st == DIFFUSER_OK) st = build_block_tiles(g);
         return finish_graph(st, g, out);
     } catch (const std::bad_alloc&) {
         return fail(DIFFUSER_ERR_ALLOC, "host allocation failed");
@@ -679,6 +700,9 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_t_ptr);
     cudaFree(g->d_t_row);
     cudaFree(g->d_t_edge);
+    cudaFree(g->d_blk_chunks);
+    cudaFree(g->d_blk_tile_ptr);
+    cudaFree(g->d_blk_order);
     cudaFree(g->d_status);
     if (g->h_status) cudaFreeHost(g->h_status);
     dfs::destroy_replay_cache(g->replay);
@@ -987,6 +1011,17 @@ int diffuser_set_path(int path) {
 }
 
 int diffuser_get_path(void) { return g_path.load(); }
+
+int diffuser_kernels_for(const diffuser_graph* g, int32_t dtype, int* kernels) {
+    if (!g || !kernels) return fail(DIFFUSER_ERR_INVALID_ARG, "NULL argument");
+    if (dtype != DIFFUSER_DTYPE_FP32 && dtype != DIFFUSER_DTYPE_BF16)
+        return fail(DIFFUSER_ERR_UNSUPPORTED, "dtype must be FP32 or BF16");
+    BandPlan bp;
+    *kernels = use_band(g, dtype, &bp) ? DIFFUSER_KERNELS_BAND
+               : use_block(g, dtype)   ? DIFFUSER_KERNELS_BLOCK
+                                       : DIFFUSER_KERNELS_CSR;
+    return DIFFUSER_OK;
+}
 
 int diffuser_graph_status(const diffuser_graph* g, int* status, int reset) {
     if (!g || !status) return fail(DIFFUSER_ERR_INVALID_ARG, "NULL argument");

@@ -87,6 +87,13 @@ struct diffuser_graph {
     int64_t* d_t_edge = nullptr;      // [nnz] its CSR edge id
     // status block written by kernels: the word (0 = ok) at [0], the device
     // address of h_status at byte 8 (a bounded wait that gives up writes both)
+    // block graph with 64-token blocks: each 128-row tile's key blocks, paired into
+    // 128-key chunks (block_path.cu)
+    int32_t* d_blk_chunks = nullptr;  // [blk_chunks][4]: key blocks kb0, kb1, mask bits, 0
+    int32_t* d_blk_tile_ptr = nullptr;   // [blk_tiles + 1]
+    int32_t* d_blk_order = nullptr;   // [blk_tiles] tile positions by falling chunk count
+    int32_t blk_tiles = 0;
+    int64_t blk_chunks = 0;
     int* d_status = nullptr;
     int* h_status = nullptr;          // page-locked, mapped host mirror of the word
     dfs::ReplayCache* replay = nullptr;   // captured band-path forwards (see abi.cu)
@@ -173,6 +180,19 @@ int launch_backward_csr(const diffuser_graph* g, int64_t units, const void* Q, c
                         const void* V, const void* dOut, int32_t dtype, int32_t hops, float alpha,
                         void* dQ, void* dK, void* dV, char* ws, const BwdLayout& L,
                         cudaStream_t stream);
+
+// ---- block-sparse path (block_path.cu): block graphs of 64-token blocks, bf16 I/O
+struct BlockLayout {
+    size_t z[2];        // hop state Z_k, [units][n][hi 64 | lo 64] bf16, ping-pong
+    size_t mb2, inv_l;  // per-row max (base-2 scale) and inverse sum, [units][n] fp32
+    size_t total;
+};
+bool block_eligible(const diffuser_graph* g);
+int build_block_tiles(diffuser_graph* g);      // from the host CSR copy; no-op for other graphs
+int plan_block_layout(const diffuser_graph* g, int64_t units, BlockLayout* L);
+int launch_block_forward(const diffuser_graph* g, int64_t units, const void* Q, const void* K,
+                         const void* V, int32_t hops, float alpha, void* out, char* ws,
+                         const BlockLayout& L, cudaStream_t stream);
 
 // ---- band path (band_score.cu, band_hop.cu): token graphs, bf16 I/O --------
 bool band_plan(const diffuser_graph* g, BandPlan* p);   // false: graph not eligible
