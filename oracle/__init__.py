@@ -289,20 +289,34 @@ def backward(Q: np.ndarray, K: np.ndarray, V: np.ndarray, dOut: np.ndarray, row_
     return dQ, dK, dV
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 value (8 significant bits), ties to even,
+    returned as float64: x = m 2^e with 0.5 <= |m| < 1, m rounded to a multiple
+    of 2^-8 (normal range; no overflow handling)."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+
+
 def layer_forward(X: np.ndarray, Wq: np.ndarray, Wk: np.ndarray, Wv: np.ndarray, Wo: np.ndarray,
-                  row_ptr: np.ndarray, col: np.ndarray, hops: int, alpha: float) -> np.ndarray:
+                  row_ptr: np.ndarray, col: np.ndarray, hops: int, alpha: float,
+                  bf16_interfaces: bool = False) -> np.ndarray:
     """The diffusion module with its projections (Diffuser notes sec 2.1: per head
     Q = X W_Q, K = X W_K, V = X W_V; the heads' outputs are concatenated and
     projected by W_O; sec 2.4: residual and feed-forward lie outside the module).
 
     X [B][n][D]; Wq, Wk, Wv [H][D][d]; Wo [H*d][D]; all float64.  Returns [B][n][D].
+    ``bf16_interfaces``: the tensors passed between the stages (Q, K, V, the heads'
+    outputs Z and the result) are bf16, each rounded once to nearest-even from the
+    exact value of its stage; the arithmetic inside every stage stays float64.
     """
+    r = round_bf16 if bf16_interfaces else (lambda t: t)
     X = np.asarray(X, dtype=np.float64)
     B, n, _ = X.shape
     H, _, d = Wq.shape
-    Q = np.einsum("bnD,hDd->bhnd", X, Wq)
-    K = np.einsum("bnD,hDd->bhnd", X, Wk)
-    V = np.einsum("bnD,hDd->bhnd", X, Wv)
-    Z = forward(Q, K, V, row_ptr, col, hops, alpha)                 # [B][H][n][d]
+    Q = r(np.einsum("bnD,hDd->bhnd", X, Wq))
+    K = r(np.einsum("bnD,hDd->bhnd", X, Wk))
+    V = r(np.einsum("bnD,hDd->bhnd", X, Wv))
+    Z = r(forward(Q, K, V, row_ptr, col, hops, alpha))              # [B][H][n][d]
     heads = np.transpose(Z, (0, 2, 1, 3)).reshape(B, n, H * d)      # concatenation
-    return heads @ Wo
+    return r(heads @ Wo)

@@ -90,3 +90,20 @@ def checksum(*arrays: np.ndarray) -> str:
     for a in arrays:
         h.update(np.ascontiguousarray(a).tobytes())
     return h.hexdigest()[:16]
+
+
+def layer_inputs(B: int, n: int, D: int, H: int, seed: int = 0):
+    """Input and synthetic weights of the module with its projections, as bf16
+    bit patterns: X [B][n][D] ~ N(0, 1); Wqkv [3 H 64][D] and Wo [D][H 64] ~
+    N(0, 1) scaled by the power of two nearest 1/sqrt(fan-in) (exact in bf16).
+    Drawn from one running pair counter: X, then Wqkv, then Wo."""
+    d = 64
+    sizes = (B * n * D, 3 * H * d * D, D * H * d)
+    scales = (1.0, 2.0 ** -round(np.log2(np.sqrt(D))), 2.0 ** -round(np.log2(np.sqrt(H * d))))
+    shapes = ((B, n, D), (3 * H * d, D), (D, H * d))
+    out, first = [], 0
+    for size, scale, shape in zip(sizes, scales, shapes):
+        z = (normals(seed, size, first_pair=first) * scale).astype(np.float32).reshape(shape)
+        first += (size + 1) // 2
+        out.append(to_bf16_bits(z))
+    return tuple(out)

@@ -63,3 +63,31 @@ def test_linear_in_the_value_and_output_projections():
                                2 * base, rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(oracle.layer_forward(X, Wq, Wk, Wv, -3 * Wo, row_ptr, col, 5, 0.1),
                                -3 * base, rtol=1e-13, atol=1e-14)
+
+
+def test_round_bf16_matches_torch_and_ties_to_even():
+    import torch
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(10000) * 10.0 ** rng.integers(-6, 6, 10000),
+                        [1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(2.0 + 2 ** -7), 0.0, 2 ** -100]])
+    want = torch.tensor(x, dtype=torch.float64).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(x), want)
+    # ties go to the even neighbour
+    assert oracle.round_bf16(np.array([1.0 + 2 ** -8]))[0] == 1.0
+    assert oracle.round_bf16(np.array([1.0 + 3 * 2 ** -8]))[0] == 1.0 + 2 ** -6
+
+
+def test_bf16_interfaces_with_no_hops_are_two_rounded_products():
+    # hops = 0: Z = V, so the module is round(round(round(X W_V) concatenated) W_O)
+    n, D, H, d = 20, 16, 2, 8
+    rng = np.random.default_rng(6)
+    X = rng.standard_normal((2, n, D))
+    Wq, Wk, Wv, Wo = weights(D, H, d, 7)
+    row_ptr, col = oracle.token_graph(n, 2, 1, 2, seed=1)
+    got = oracle.layer_forward(X, Wq, Wk, Wv, Wo, row_ptr, col, 0, 0.1, bf16_interfaces=True)
+    import torch
+    def rb(t):
+        return torch.tensor(t, dtype=torch.float64).to(torch.bfloat16).double().numpy()
+    V = rb(np.stack([X @ Wv[h] for h in range(H)], axis=1))          # [B][H][n][d]
+    heads = np.concatenate([V[:, h] for h in range(H)], axis=-1)
+    np.testing.assert_array_equal(got, rb(heads @ Wo))
