@@ -314,6 +314,55 @@ DIFFUSER_API int diffuser_forward_per_head(const void* Q, const void* K, const v
                                            float alpha, void* out, void* workspace,
                                            size_t workspace_bytes, diffuser_stream stream);
 
+/* ---------------------------------------------------------------- the surrounding layer */
+
+/*
+ * The projections around the diffusion module ([D] sec 2.1: per head
+ * Q = X W_Q, K = X W_K, V = X W_V; [D] sec 2.4, Fig S.3: the heads' outputs
+ * are concatenated and projected by W_O; residual and feed-forward lie
+ * outside the module), as dense GEMMs on the tcgen05 tensor cores: bf16
+ * operands, fp32 accumulation, bf16 results rounded to nearest-even once.
+ * Weights use the [out_features][in_features] layout:
+ *   X     device bf16 [B][n][D]   (tokens of batch item b, model width D)
+ *   Wqkv  device bf16 [3 H d][D]  row s H d + h d + f is feature f of head h
+ *                                 of Q (s = 0), K (s = 1) or V (s = 2)
+ *   Wo    device bf16 [D][H d]    column h d + f reads feature f of head h
+ *   Q, K, V, Z   device bf16 [B][H][n][d] (the forward's layout)
+ *   Y     device bf16 [B][n][D]
+ * d == 64; D a multiple of 8, at most 65536; H >= 1.  All pointers 16-byte
+ * aligned; outputs may not overlap inputs or each other.  Asynchronous on
+ * `stream`.  The first projection call on a device makes a 16-byte device
+ * status block and a page-locked host mirror of it (kept for the process);
+ * a projection kernel whose bounded wait gives up records a code there
+ * (diffuser_projection_status) and later projection calls return
+ * DIFFUSER_ERR_DEVICE until it is reset.
+ * Errors: INVALID_ARG, UNSUPPORTED, ALLOC, CUDA, DEVICE.
+ */
+DIFFUSER_API int diffuser_qkv_projection(const void* X, const void* Wqkv, int64_t B, int64_t n, int32_t D,
+                                         int32_t H, int32_t d, void* Q, void* K, void* V,
+                                         diffuser_stream stream);
+/* Y[b][i] = concat_h Z[b][h][i] . Wo^T (the heads' concatenation and W_O). */
+DIFFUSER_API int diffuser_output_projection(const void* Z, const void* Wo, int64_t B, int64_t n, int32_t D,
+                                            int32_t H, int32_t d, void* Y, diffuser_stream stream);
+/* Read (synchronously) the stand-alone projections' status word of the
+ * current device; reset != 0 clears it. */
+DIFFUSER_API int diffuser_projection_status(int* status, int reset);
+
+/*
+ * The whole module on one graph: Q, K, V = the projections of X, Z =
+ * diffuser_forward(Q, K, V) (bf16), Y = the output projection of Z.  n is the
+ * graph's n.  workspace: device, >= diffuser_layer_workspace_size bytes,
+ * 256-byte aligned (Q, K, V, Z, then the forward's workspace).  Kernel
+ * failures are recorded in the graph's status word.  Errors: as
+ * diffuser_forward and the projections.
+ */
+DIFFUSER_API int diffuser_layer_workspace_size(const diffuser_graph* g, int64_t B, int32_t D, int32_t H,
+                                               int32_t d, size_t* bytes);
+DIFFUSER_API int diffuser_layer_forward(const void* X, const void* Wqkv, const void* Wo, int64_t B,
+                                        int32_t D, int32_t H, int32_t d, const diffuser_graph* g,
+                                        int32_t hops, float alpha, void* Y, void* workspace,
+                                        size_t workspace_bytes, diffuser_stream stream);
+
 /* ---------------------------------------------------------------- no-allocation forward */
 
 /*

@@ -79,6 +79,12 @@ def _load() -> ctypes.CDLL:
         "diffuser_forward_per_head": (c.c_int, [vp, vp, vp, i32, i64, i64, i32, c.POINTER(vp), i32,
                                                 c.c_float, vp, vp, c.c_size_t, vp]),
         "diffuser_kernels_for": (c.c_int, [vp, i32, c.POINTER(c.c_int)]),
+        "diffuser_qkv_projection": (c.c_int, [vp, vp, i64, i64, i32, i32, i32, vp, vp, vp, vp]),
+        "diffuser_output_projection": (c.c_int, [vp, vp, i64, i64, i32, i32, i32, vp, vp]),
+        "diffuser_projection_status": (c.c_int, [c.POINTER(c.c_int), c.c_int]),
+        "diffuser_layer_workspace_size": (c.c_int, [vp, i64, i32, i32, i32, c.POINTER(c.c_size_t)]),
+        "diffuser_layer_forward": (c.c_int, [vp, vp, vp, i64, i32, i32, i32, vp, i32, c.c_float, vp,
+                                             vp, c.c_size_t, vp]),
         "diffuser_graph_status": (c.c_int, [vp, c.POINTER(c.c_int), c.c_int]),
         "diffuser_graph_set_status": (c.c_int, [vp, c.c_int]),
         "diffuser_launch_count": (c.c_int64, [i64p]),
@@ -297,6 +303,58 @@ def diffuser_forward_per_head(Q, K, V, graphs, hops: int, alpha: float, out=None
                                           workspace.data_ptr(), workspace.numel(), _stream(stream)),
            "diffuser_forward_per_head")
     return out
+
+
+def diffuser_qkv_projection(X, Wqkv, H: int, Q=None, K=None, V=None, stream=None):
+    """Per-head Q, K, V [B][H][n][64] of X [B][n][D] by Wqkv [3 H 64][D] (bf16 tensors)."""
+    import torch
+    B, n, D = X.shape
+    shape = (B, H, n, 64)
+    Q = torch.empty(shape, dtype=torch.bfloat16, device=X.device) if Q is None else Q
+    K = torch.empty(shape, dtype=torch.bfloat16, device=X.device) if K is None else K
+    V = torch.empty(shape, dtype=torch.bfloat16, device=X.device) if V is None else V
+    _check(_lib.diffuser_qkv_projection(X.data_ptr(), Wqkv.data_ptr(), B, n, D, H, 64, Q.data_ptr(),
+                                        K.data_ptr(), V.data_ptr(), _stream(stream)),
+           "diffuser_qkv_projection")
+    return Q, K, V
+
+
+def diffuser_output_projection(Z, Wo, Y=None, stream=None):
+    """Y [B][n][D] = the heads of Z [B][H][n][64] concatenated, times Wo^T (Wo [D][H 64])."""
+    import torch
+    B, H, n, d = Z.shape
+    D = Wo.shape[0]
+    Y = torch.empty((B, n, D), dtype=torch.bfloat16, device=Z.device) if Y is None else Y
+    _check(_lib.diffuser_output_projection(Z.data_ptr(), Wo.data_ptr(), B, n, D, H, d, Y.data_ptr(),
+                                           _stream(stream)), "diffuser_output_projection")
+    return Y
+
+
+def diffuser_projection_status(reset: bool = False) -> int:
+    st = ctypes.c_int()
+    _check(_lib.diffuser_projection_status(ctypes.byref(st), int(reset)), "diffuser_projection_status")
+    return st.value
+
+
+def diffuser_layer_workspace_size(g: Graph, B: int, D: int, H: int) -> int:
+    b = ctypes.c_size_t()
+    _check(_lib.diffuser_layer_workspace_size(g.handle, B, D, H, 64, ctypes.byref(b)),
+           "diffuser_layer_workspace_size")
+    return b.value
+
+
+def diffuser_layer_forward(X, Wqkv, Wo, g: Graph, H: int, hops: int, alpha: float, Y=None,
+                           workspace=None, stream=None):
+    """The module: projections, the forward on graph g, concatenation and W_O (bf16)."""
+    import torch
+    B, n, D = X.shape
+    Y = torch.empty_like(X) if Y is None else Y
+    if workspace is None:
+        workspace = alloc_workspace(diffuser_layer_workspace_size(g, B, D, H), X.device)
+    _check(_lib.diffuser_layer_forward(X.data_ptr(), Wqkv.data_ptr(), Wo.data_ptr(), B, D, H, 64,
+                                       g.handle, hops, alpha, Y.data_ptr(), workspace.data_ptr(),
+                                       workspace.numel(), _stream(stream)), "diffuser_layer_forward")
+    return Y
 
 
 def diffuser_backward_workspace_size(g: Graph, B: int, H: int, d: int, dtype: int,

@@ -896,6 +896,177 @@ int diffuser_forward_per_head(const void* Q, const void* K, const void* V, int32
     }
 }
 
+namespace {
+
+// Status block of the stand-alone projections on each device (the layout of a
+// graph's: word, padding, device address of a page-locked host mirror), made
+// on the first projection call on that device and kept for the process.
+struct ProjStatus {
+    int* d = nullptr;
+    int* h = nullptr;
+};
+std::mutex g_proj_mu;
+ProjStatus g_proj_status[kMaxReplayDevices];
+
+int projection_status(ProjStatus* out) {
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxReplayDevices) return fail(DIFFUSER_ERR_UNSUPPORTED, "device index out of range");
+    std::lock_guard<std::mutex> lk(g_proj_mu);
+    ProjStatus& ps = g_proj_status[dev];
+    if (!ps.d) {
+        int* d = nullptr;
+        int* h = nullptr;
+        int* mirror_dev = nullptr;
+        err = cudaMalloc(&d, kStatusBlockBytes);
+        if (err == cudaSuccess) err = cudaHostAlloc(&h, sizeof(int), cudaHostAllocMapped);
+        if (err == cudaSuccess) {
+            *h = 0;
+            err = cudaHostGetDevicePointer(&mirror_dev, h, 0);
+        }
+        if (err == cudaSuccess) {
+            unsigned char block[kStatusBlockBytes] = {0};
+            std::memcpy(block + 8, &mirror_dev, sizeof(mirror_dev));
+            err = cudaMemcpy(d, block, kStatusBlockBytes, cudaMemcpyHostToDevice);
+        }
+        if (err != cudaSuccess) {
+            cudaFree(d);
+            if (h) cudaFreeHost(h);
+            return cuda_fail(err, "projection status block");
+        }
+        ps.d = d;
+        ps.h = h;
+    }
+    *out = ps;
+    return DIFFUSER_OK;
+}
+
+int check_projection_pointers(const void* const* in, int nin, void* const* outs, int nout,
+                              const size_t* in_bytes, const size_t* out_bytes) {
+    for (int x = 0; x < nin; ++x)
+        if (!in[x] || !aligned16(in[x])) return fail(DIFFUSER_ERR_INVALID_ARG, "an input is NULL or not 16-byte aligned");
+    for (int x = 0; x < nout; ++x) {
+        if (!outs[x] || !aligned16(outs[x]))
+            return fail(DIFFUSER_ERR_INVALID_ARG, "an output is NULL or not 16-byte aligned");
+        for (int y = 0; y < nin; ++y)
+            if (overlaps(outs[x], out_bytes[x], in[y], in_bytes[y]))
+                return fail(DIFFUSER_ERR_INVALID_ARG, "an output overlaps an input");
+        for (int y = x + 1; y < nout; ++y)
+            if (overlaps(outs[x], out_bytes[x], outs[y], out_bytes[y]))
+                return fail(DIFFUSER_ERR_INVALID_ARG, "the outputs overlap");
+    }
+    return DIFFUSER_OK;
+}
+
+}  // namespace
+
+int diffuser_qkv_projection(const void* X, const void* Wqkv, int64_t B, int64_t n, int32_t D, int32_t H,
+                            int32_t d, void* Q, void* K, void* V, diffuser_stream stream) {
+    try {
+        int st = check_layer_shape(B, n, D, H, d);
+        if (st) return st;
+        const size_t xb = (size_t)B * n * D * 2, wb = (size_t)3 * H * kHeadDim * D * 2;
+        const size_t ob = (size_t)B * H * n * kHeadDim * 2;
+        const void* in[2] = {X, Wqkv};
+        void* outs[3] = {Q, K, V};
+        const size_t inb[2] = {xb, wb}, outb[3] = {ob, ob, ob};
+        if ((st = check_projection_pointers(in, 2, outs, 3, inb, outb))) return st;
+        ProjStatus ps;
+        if ((st = projection_status(&ps))) return st;
+        if (*reinterpret_cast<volatile int*>(ps.h) != 0)
+            return fail(DIFFUSER_ERR_DEVICE, "a projection kernel reported a failure (see diffuser_projection_status)");
+        return launch_qkv_projection(X, Wqkv, B, n, D, H, Q, K, V, ps.d, static_cast<cudaStream_t>(stream));
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+int diffuser_output_projection(const void* Z, const void* Wo, int64_t B, int64_t n, int32_t D, int32_t H,
+                               int32_t d, void* Y, diffuser_stream stream) {
+    try {
+        int st = check_layer_shape(B, n, D, H, d);
+        if (st) return st;
+        const size_t zb = (size_t)B * H * n * kHeadDim * 2, wb = (size_t)D * H * kHeadDim * 2;
+        const size_t yb = (size_t)B * n * D * 2;
+        const void* in[2] = {Z, Wo};
+        void* outs[1] = {Y};
+        const size_t inb[2] = {zb, wb}, outb[1] = {yb};
+        if ((st = check_projection_pointers(in, 2, outs, 1, inb, outb))) return st;
+        ProjStatus ps;
+        if ((st = projection_status(&ps))) return st;
+        if (*reinterpret_cast<volatile int*>(ps.h) != 0)
+            return fail(DIFFUSER_ERR_DEVICE, "a projection kernel reported a failure (see diffuser_projection_status)");
+        return launch_output_projection(Z, Wo, B, n, D, H, Y, ps.d, static_cast<cudaStream_t>(stream));
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+int diffuser_projection_status(int* status, int reset) {
+    if (!status) return fail(DIFFUSER_ERR_INVALID_ARG, "NULL argument");
+    ProjStatus ps;
+    int st = projection_status(&ps);
+    if (st) return st;
+    cudaError_t err = cudaMemcpy(status, ps.d, sizeof(int), cudaMemcpyDeviceToHost);
+    if (err == cudaSuccess && *status == 0) *status = *reinterpret_cast<volatile int*>(ps.h);
+    if (err == cudaSuccess && reset) {
+        err = cudaMemset(ps.d, 0, sizeof(int));
+        *reinterpret_cast<volatile int*>(ps.h) = 0;
+    }
+    return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "reading the projection status word");
+}
+
+int diffuser_layer_workspace_size(const diffuser_graph* g, int64_t B, int32_t D, int32_t H, int32_t d,
+                                  size_t* bytes) {
+    try {
+        if (!g || !bytes) return fail(DIFFUSER_ERR_INVALID_ARG, "NULL argument");
+        int st = check_layer_shape(B, g->n, D, H, d);
+        if (st) return st;
+        size_t fwd = 0;
+        if ((st = workspace_need(g, B, H, DIFFUSER_DTYPE_BF16, &fwd))) return st;
+        *bytes = 4 * align_up(io_bytes(g, B, H, DIFFUSER_DTYPE_BF16)) + fwd;
+        return DIFFUSER_OK;
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
+int diffuser_layer_forward(const void* X, const void* Wqkv, const void* Wo, int64_t B, int32_t D, int32_t H,
+                           int32_t d, const diffuser_graph* g, int32_t hops, float alpha, void* Y,
+                           void* workspace, size_t workspace_bytes, diffuser_stream stream) {
+    try {
+        if (!g) return fail(DIFFUSER_ERR_INVALID_ARG, "graph is NULL");
+        const int64_t n = g->n;
+        int st = check_layer_shape(B, n, D, H, d);
+        if (st) return st;
+        if (hops < 0) return fail(DIFFUSER_ERR_INVALID_ARG, "hops must be >= 0");
+        if (!(alpha >= 0.f && alpha <= 1.f)) return fail(DIFFUSER_ERR_INVALID_ARG, "alpha must lie in [0, 1]");
+        const size_t xb = (size_t)B * n * D * 2, wqb = (size_t)3 * H * kHeadDim * D * 2;
+        const size_t wob = (size_t)D * H * kHeadDim * 2;
+        const void* in[3] = {X, Wqkv, Wo};
+        void* outs[1] = {Y};
+        const size_t inb[3] = {xb, wqb, wob}, outb[1] = {xb};
+        if ((st = check_projection_pointers(in, 3, outs, 1, inb, outb))) return st;
+        size_t need = 0;
+        if ((st = diffuser_layer_workspace_size(g, B, D, H, d, &need))) return st;
+        if ((st = check_workspace_bytes(need, workspace, workspace_bytes))) return st;
+        if ((st = check_device(g))) return st;
+        if ((st = check_status_word(g))) return st;
+        const size_t slot = align_up(io_bytes(g, B, H, DIFFUSER_DTYPE_BF16));
+        char* ws = static_cast<char*>(workspace);
+        char *q = ws, *k = ws + slot, *v = ws + 2 * slot, *z = ws + 3 * slot;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if ((st = launch_qkv_projection(X, Wqkv, B, n, D, H, q, k, v, g->d_status, s))) return st;
+        if ((st = forward_device(q, k, v, DIFFUSER_DTYPE_BF16, B, H, d, g, hops, alpha, z, ws + 4 * slot,
+                                 workspace_bytes - 4 * slot, s)))
+            return st;
+        return launch_output_projection(z, Wo, B, n, D, H, Y, g->d_status, s);
+    } catch (...) {
+        return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");
+    }
+}
+
 int diffuser_host_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32_t d,
                                  int32_t dtype, size_t* bytes) {
     size_t base = 0;

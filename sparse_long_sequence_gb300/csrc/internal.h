@@ -194,6 +194,15 @@ int launch_block_forward(const diffuser_graph* g, int64_t units, const void* Q, 
                          const void* V, int32_t hops, float alpha, void* out, char* ws,
                          const BlockLayout& L, cudaStream_t stream);
 
+// ---- the projections around the module (layer_gemm.cu): tcgen05 GEMMs, bf16 --
+int check_layer_shape(int64_t B, int64_t n, int32_t D, int32_t H, int32_t d);
+// Q, K, V [B][H][n][64] = per-head projections of X [B][n][D] by Wqkv [3 H 64][D]
+int launch_qkv_projection(const void* X, const void* Wqkv, int64_t B, int64_t n, int32_t D, int32_t H,
+                          void* Q, void* K, void* V, int* status, cudaStream_t stream);
+// Y [B][n][D] = concat_h Z[b][h][i][:] projected by Wo [D][H 64]
+int launch_output_projection(const void* Z, const void* Wo, int64_t B, int64_t n, int32_t D, int32_t H,
+                             void* Y, int* status, cudaStream_t stream);
+
 // ---- band path (band_score.cu, band_hop.cu): token graphs, bf16 I/O --------
 bool band_plan(const diffuser_graph* g, BandPlan* p);   // false: graph not eligible
 int plan_band_layout(const diffuser_graph* g, const BandPlan& p, int64_t units, BandLayout* L);
