@@ -70,6 +70,87 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_bf16_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def time_events(fn, steps: int, stream, flush) -> list[float]:
+    """Device milliseconds of fn() per step: CUDA events on `stream`, L2 flushed
+    between steps outside the events."""
+    import torch
+    ms = []
+    for k in range(steps):
+        flush.fill_(k & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    return ms
+
+
+def measure_layer(dl, w, g, steps: int, stream, flush) -> dict:
+    """The module's projections at the workload's sizes (model width D = 64 H):
+    each GEMM's TFLOP/s (2 M N K flops over its median device time) against the
+    measured bf16 peak, and the whole module (projections + forward) per step."""
+    import torch
+    B, n, H = w.B, w.n, w.H
+    D = 64 * H
+    X, Wqkv, Wo = (torch.from_numpy(t).view(torch.bfloat16).cuda()
+                   for t in synthetic.layer_inputs(B, n, D, H, seed=w.seed))
+    Q, K, V = (torch.empty((B, H, n, 64), dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    Y = torch.empty_like(X)
+    ws = dl.alloc_workspace(dl.diffuser_layer_workspace_size(g, B, D, H))
+    for _ in range(3):
+        dl.diffuser_qkv_projection(X, Wqkv, H, Q=Q, K=K, V=V, stream=stream)
+        dl.diffuser_output_projection(Q, Wo, Y=Y, stream=stream)
+        dl.diffuser_layer_forward(X, Wqkv, Wo, g, H, w.hops, w.alpha, Y=Y, workspace=ws, stream=stream)
+    torch.cuda.synchronize()
+    t_qkv = statistics.median(time_events(
+        lambda: dl.diffuser_qkv_projection(X, Wqkv, H, Q=Q, K=K, V=V, stream=stream), steps, stream, flush))
+    t_out = statistics.median(time_events(
+        lambda: dl.diffuser_output_projection(Q, Wo, Y=Y, stream=stream), steps, stream, flush))
+    t_mod = statistics.median(time_events(
+        lambda: dl.diffuser_layer_forward(X, Wqkv, Wo, g, H, w.hops, w.alpha, Y=Y, workspace=ws,
+                                          stream=stream), steps, stream, flush))
+    peak, kind = measured_bf16_peak()
+    M = B * n
+    f_qkv, f_out = 2.0 * M * (3 * D) * D, 2.0 * M * D * D
+    tf_qkv, tf_out = f_qkv / (t_qkv / 1e3) / 1e12, f_out / (t_out / 1e3) / 1e12
+    return {"model_width": D, "tokens": M,
+            "qkv_projection": {"ms": t_qkv, "tflops": tf_qkv, "frac": tf_qkv / peak},
+            "output_projection": {"ms": t_out, "tflops": tf_out, "frac": tf_out / peak},
+            "module_ms": t_mod, "peak_tflops": peak, "peak_kind": kind,
+            "bound": "tensor", "timing": "median device time of the steps, L2 flushed between them"}
+
+
+def measure_backward(dl, w, g, Q, K, V, steps: int, stream, flush) -> dict:
+    """The backward pass (gradients of <dOut, forward>) on the workload: median
+    device time per step and edge-hops per second of the hops it reverses."""
+    import torch
+    dO = V.flip(-1).contiguous()
+    code = dl.DIFFUSER_DTYPE_BF16 if w.dtype == "bf16" else dl.DIFFUSER_DTYPE_FP32
+    ws = dl.alloc_workspace(dl.diffuser_backward_workspace_size(g, w.B, w.H, w.d, code, w.hops))
+    grads = [torch.empty_like(Q) for _ in range(3)]
+    for _ in range(2):
+        dl.diffuser_backward(Q, K, V, dO, g, w.hops, w.alpha, *grads, workspace=ws, stream=stream)
+    torch.cuda.synchronize()
+    t = statistics.median(time_events(
+        lambda: dl.diffuser_backward(Q, K, V, dO, g, w.hops, w.alpha, *grads, workspace=ws, stream=stream),
+        steps, stream, flush))
+    return {"ms": t, "value": w.units * g.nnz * w.hops / (t / 1e3), "unit": UNIT,
+            "kernels": "CSR SIMT (recompute, reversed hops over the transposed edge list)"}
+
+
 def hop_kernel_traffic(workload: str) -> float | None:
     """ncu DRAM bytes of one hop (window + gather kernels), if recorded for the
     current kernel source (profiles/traffic.json)."""
@@ -401,6 +482,12 @@ def run_ours(args, w) -> None:
     if not torch.equal(Oh, out.cpu()):
         raise BenchCheckFailed("end-to-end output differs from the device forward")
 
+    check_graph_status(dl, g, "the kernel-timing and end-to-end passes")
+    extra_steps = max(3, min(args.steps, 10))
+    layer = measure_layer(dl, w, g, extra_steps, stream, flush) if w.dtype == "bf16" else None
+    backward = measure_backward(dl, w, g, Q, K, V, extra_steps, stream, flush)
+    check_graph_status(dl, g, "the module and backward passes")
+
     value = whole_job_rate(w.units, g.nnz, w.hops, world, t_step)
     io_bytes = w.units * w.n * w.d * (2 if w.dtype == "bf16" else 4)
     model = algorithmic_bytes(w, g.nnz)
@@ -463,6 +550,9 @@ def run_ours(args, w) -> None:
                              "the timed steps replay the forward as a captured CUDA graph",
             "kernel_launches_per_step": {k: v[1] / args.steps for k, v in prof.items() if v[1]},
             "gpu_launches": int(launches1 - launches0),
+            "kernels": ["CSR", "band", "block"][dl.diffuser_kernels_for(g, code) - 1],
+            "layer": layer,
+            "backward": backward,
             "clocks": clock_info,
             "cpu_baseline": cpu,
         }
