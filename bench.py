@@ -463,6 +463,14 @@ def run_ours(args, w) -> None:
     prof_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     t_step = max_over_ranks(statistics.mean(step_ms), device="cuda")
 
+    if args.forward_only:
+        # profiling runs: the timed and kernel-timing passes only
+        check_graph_status(dl, g, "the kernel-timing pass")
+        print(json.dumps({"metric": METRIC, "value": whole_job_rate(w.units, g.nnz, w.hops, world, t_step),
+                          "unit": UNIT, "ms_per_step": t_step, "forward_only": True,
+                          "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]}}),
+              flush=True)
+        return
     # ---- end to end through the host-buffer entry point
     Oh = torch.empty_like(Vp).pin_memory()
     ws_h = dl.alloc_workspace(dl.diffuser_host_workspace_size(g, w.B, w.H, w.d, code))
@@ -569,6 +577,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.TEXT.name, choices=sorted(workloads.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time the forward only (no end-to-end, module or backward passes); for profiling")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
     w = workloads.BY_NAME[args.workload]

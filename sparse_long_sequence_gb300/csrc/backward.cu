@@ -146,13 +146,17 @@ bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ 
         const float w_l = t < t1 ? Au[a.t_edge[t]] : 0.f;
         const int32_t i_l = t < t1 ? a.t_row[t] : 0;
         const int cnt = (t1 - base) < 32 ? (int)(t1 - base) : 32;
-#pragma unroll 4
-        for (int s = 0; s < cnt; ++s) {
-            const float w = __shfl_sync(0xffffffffu, w_l, s);
+        float2 gv[32];        // all 32 rows requested before the first is used
+#pragma unroll
+        for (int s = 0; s < 32; ++s) {
             const int32_t i = __shfl_sync(0xffffffffu, i_l, s);
-            const float2 gv = load2(Gu + (size_t)i * kHeadDim);
-            acc.x = fmaf(w, gv.x, acc.x);
-            acc.y = fmaf(w, gv.y, acc.y);
+            gv[s] = s < cnt ? load2(Gu + (size_t)i * kHeadDim) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int s = 0; s < 32; ++s) {
+            const float w = __shfl_sync(0xffffffffu, w_l, s);
+            acc.x = fmaf(w, gv[s].x, acc.x);
+            acc.y = fmaf(w, gv[s].y, acc.y);
         }
     }
     const float keep = 1.f - alpha;
@@ -200,13 +204,17 @@ bwd_softmax_dq_kernel(BwdArgs a, const float* __restrict__ A, float* __restrict_
             j_l = a.col[e];
         }
         const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
-#pragma unroll 4
-        for (int s = 0; s < cnt; ++s) {
-            const float w = __shfl_sync(0xffffffffu, ds_l, s);
+        float2 kv[32];        // all 32 rows requested before the first is used
+#pragma unroll
+        for (int s = 0; s < 32; ++s) {
             const int32_t j = __shfl_sync(0xffffffffu, j_l, s);
-            const float2 kv = load2(Ku + (size_t)j * kHeadDim);
-            acc.x = fmaf(w, kv.x, acc.x);
-            acc.y = fmaf(w, kv.y, acc.y);
+            kv[s] = s < cnt ? load2(Ku + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int s = 0; s < 32; ++s) {
+            const float w = __shfl_sync(0xffffffffu, ds_l, s);
+            acc.x = fmaf(w, kv[s].x, acc.x);
+            acc.y = fmaf(w, kv[s].y, acc.y);
         }
     }
     store2(dQ + unit + (size_t)i * kHeadDim + 2 * lane, acc);
@@ -231,13 +239,17 @@ bwd_dk_kernel(BwdArgs a, const float* __restrict__ dS, const TIo* __restrict__ Q
         const float w_l = t < t1 ? dSu[a.t_edge[t]] : 0.f;
         const int32_t i_l = t < t1 ? a.t_row[t] : 0;
         const int cnt = (t1 - base) < 32 ? (int)(t1 - base) : 32;
-#pragma unroll 4
-        for (int s = 0; s < cnt; ++s) {
-            const float w = __shfl_sync(0xffffffffu, w_l, s);
+        float2 qv[32];        // all 32 rows requested before the first is used
+#pragma unroll
+        for (int s = 0; s < 32; ++s) {
             const int32_t i = __shfl_sync(0xffffffffu, i_l, s);
-            const float2 qv = load2(Qu + (size_t)i * kHeadDim);
-            acc.x = fmaf(w, qv.x, acc.x);
-            acc.y = fmaf(w, qv.y, acc.y);
+            qv[s] = s < cnt ? load2(Qu + (size_t)i * kHeadDim) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int s = 0; s < 32; ++s) {
+            const float w = __shfl_sync(0xffffffffu, w_l, s);
+            acc.x = fmaf(w, qv[s].x, acc.x);
+            acc.y = fmaf(w, qv[s].y, acc.y);
         }
     }
     store2(dK + unit + (size_t)j * kHeadDim + 2 * lane, acc);

@@ -151,19 +151,26 @@ hop_csr_kernel(CsrArgs a, const float* __restrict__ A, const TSrc* __restrict__ 
     const float* Au = A + (size_t)u * a.nnz;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
 
+    // 32 edges per round: all 32 rows of Z_k are requested before the first is
+    // used (a long row, such as a global row, is latency-bound otherwise); the
+    // sum still runs in edge order
     float2 acc = make_float2(0.f, 0.f);
     for (int64_t base = e0; base < e1; base += 32) {
         const int64_t e = base + lane;
         const float a_l = e < e1 ? Au[e] : 0.f;
         const int32_t j_l = e < e1 ? a.col[e] : 0;
         const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
-#pragma unroll 8
-        for (int t = 0; t < cnt; ++t) {
-            const float w = __shfl_sync(0xffffffffu, a_l, t);
+        float2 z[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
             const int32_t j = __shfl_sync(0xffffffffu, j_l, t);
-            const float2 z = Pair<TSrc>::load(Z + (size_t)j * kHeadDim);
-            acc.x = fmaf(w, z.x, acc.x);
-            acc.y = fmaf(w, z.y, acc.y);
+            z[t] = t < cnt ? Pair<TSrc>::load(Z + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            const float w = __shfl_sync(0xffffffffu, a_l, t);
+            acc.x = fmaf(w, z[t].x, acc.x);
+            acc.y = fmaf(w, z[t].y, acc.y);
         }
     }
     const float2 v = Pair<TV>::load(V + unit + (size_t)i * kHeadDim + 2 * lane);
