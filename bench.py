@@ -151,27 +151,40 @@ def measure_backward(dl, w, g, Q, K, V, steps: int, stream, flush) -> dict:
             "kernels": "CSR SIMT (recompute, reversed hops over the transposed edge list)"}
 
 
-def hop_kernel_traffic(workload: str) -> float | None:
-    """ncu DRAM bytes of one hop (window + gather kernels), if recorded for the
-    current kernel source (profiles/traffic.json)."""
+# the source files of each path's hop kernels (and what they include): a traffic
+# record holds while these are unchanged
+BAND_FILES = ("band_hop.cu", "band_score.cu", "band_common.cuh", "sm100_ptx.cuh", "internal.h")
+BLOCK_FILES = ("block_path.cu", "band_common.cuh", "sm100_ptx.cuh", "internal.h")
+CSR_FILES = ("simt_path.cu", "internal.h")
+
+
+def path_files(kernels: str) -> tuple:
+    return {"band": BAND_FILES, "block": BLOCK_FILES}.get(kernels, CSR_FILES)
+
+
+def hop_kernel_traffic(workload: str, kernels: str) -> float | None:
+    """ncu DRAM bytes of one middle hop (all its launches), if recorded for the
+    current source of that path's kernels (profiles/traffic.json)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f).get(workload)
     except Exception:
         return None
-    if not rec or rec.get("source_sha") != kernel_source_sha():
+    if not rec or rec.get("source_sha") != kernel_source_sha(path_files(kernels)):
         return None
     return float(rec["bytes_per_hop"])
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(files: tuple | None = None) -> str:
+    """sha256 prefix over the named files of sparse_long_sequence_gb300/csrc (all of
+    its sources when None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_long_sequence_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".h", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    names = sorted(files) if files else sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".h", ".cuh")))
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -510,11 +523,13 @@ def run_ours(args, w) -> None:
     if n_hops and prof["hop"][1]:
         per_hop_s = hop_ms / n_hops / 1e3
         achieved = model["per_hop_launch"] / per_hop_s / 1e9
-        traffic = hop_kernel_traffic(w.name)
+        traffic = hop_kernel_traffic(w.name, ["CSR", "band", "block"][dl.diffuser_kernels_for(g, code) - 1])
         measured_frac = traffic / per_hop_s / 1e9 / peak if traffic else None
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "traffic": traffic, "measured_frac": measured_frac,
                     "kernel": ("diffusion hop (window tcgen05 kernel + gather kernel)" if band
+                               else "diffusion hop (block-sparse tcgen05 kernel)"
+                               if dl.diffuser_kernels_for(g, code) == dl.DIFFUSER_KERNELS_BLOCK
                                else "diffusion hop (CSR SIMT kernel)"),
                     "peak_kind": peak_kind,
                     "algorithmic_bytes_per_hop": model["per_hop_launch"],
