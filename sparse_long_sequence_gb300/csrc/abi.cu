@@ -437,24 +437,23 @@ void* mapped_host(void* p) {
     return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
-// Band-path forward from host buffers: Q and K upload side by side (on the
-// forward's stream and a side stream) and the score kernels start as soon as both
-// are in; V then uploads on the side stream under the score kernels, and the hops
-// wait for it.  When `out` is pinned and mapped, the last hop writes it in place
-// (no download after the kernels); else it lands in dO and is copied back.  With
-// all four host buffers pinned, repeated calls replay the whole sequence (copies
-// and kernels) as one captured graph, like the device-buffer forward.
-int forward_host_band(const void* Q, const void* K, const void* V, int64_t B, int64_t H,
-                      const diffuser_graph* g, const BandPlan& bp, int32_t hops, float alpha,
-                      void* out, char* dQ, char* dK, char* dV, char* dO, char* ws, size_t ws_bytes,
-                      size_t bytes, cudaStream_t stream) {
-    const int64_t units = B * H;
+// Forward from host buffers on the band or block path: Q and K upload side by
+// side (on the forward's stream and a side stream) and the score kernels start as
+// soon as both are in; V then uploads on the side stream under the score kernels,
+// and the hops wait for it.  When `out` is pinned and mapped, the last hop writes it
+// in place (no download after the kernels); else it lands in dO and is copied back.
+// With all four host buffers pinned, repeated calls replay the whole sequence
+// (copies and kernels) as one captured graph, like the device-buffer forward.
+// scores(dQ, dK, s) and run_hops(dQ, dK, dV, out, s) enqueue the path's kernels.
+template <class Scores, class Hops>
+int forward_host_overlapped(const void* Q, const void* K, const void* V, int64_t B, int64_t H,
+                            const diffuser_graph* g, int32_t hops, float alpha, void* out, char* dQ,
+                            char* dK, char* dV, char* dO, char* ws, size_t ws_bytes, size_t bytes,
+                            cudaStream_t stream, Scores&& scores, Hops&& run_hops) {
     size_t need = 0;
     int st = workspace_need(g, B, H, DIFFUSER_DTYPE_BF16, &need);
     if (st) return st;
     if ((st = check_workspace_bytes(need, ws, ws_bytes))) return st;
-    BandLayout BL;
-    if ((st = plan_band_layout(g, bp, units, &BL))) return st;
     cudaStream_t up;
     if ((st = upload_stream(g->device, &up))) return st;
     void* out_dev = mapped_host(out);
@@ -479,10 +478,10 @@ int forward_host_band(const void* Q, const void* K, const void* V, int64_t B, in
         if (e == cudaSuccess) e = cudaMemcpyAsync(dV, V, bytes, cudaMemcpyHostToDevice, up);
         if (e == cudaSuccess) e = cudaEventRecord(ev[3], up);
         if (e != cudaSuccess) return cuda_fail(e, "host-buffer forward (uploads)");
-        int r = launch_band_scores(g, bp, units, dQ, dK, nullptr, ws, BL, false, s);
+        int r = scores(dQ, dK, s);
         if (r) return r;
         if ((e = cudaStreamWaitEvent(s, ev[3], 0)) != cudaSuccess) return cuda_fail(e, "host-buffer forward");
-        r = launch_band_hops(g, bp, units, dQ, dK, dV, hops, alpha, out_dev ? out_dev : dO, ws, BL, s);
+        r = run_hops(dQ, dK, dV, out_dev ? out_dev : static_cast<void*>(dO), s);
         if (r) return r;
         if (!out_dev && (e = cudaMemcpyAsync(out, dO, bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
             return cuda_fail(e, "device-to-host copy");
@@ -1100,9 +1099,33 @@ int diffuser_forward_host(const void* Q, const void* K, const void* V, int32_t d
         char* dV = ws + 2 * slot;
         char* dO = ws + 3 * slot;
         BandPlan bp;
-        if (hops > 0 && use_band(g, dtype, &bp))
-            return forward_host_band(Q, K, V, B, H, g, bp, hops, alpha, out, dQ, dK, dV, dO, ws + 4 * slot,
-                                     workspace_bytes - 4 * slot, bytes, stream);
+        char* fws = ws + 4 * slot;
+        const size_t fws_bytes = workspace_bytes - 4 * slot;
+        const int64_t units = B * H;
+        if (hops > 0 && use_band(g, dtype, &bp)) {
+            BandLayout BL;
+            if ((st = plan_band_layout(g, bp, units, &BL))) return st;
+            return forward_host_overlapped(
+                Q, K, V, B, H, g, hops, alpha, out, dQ, dK, dV, dO, fws, fws_bytes, bytes, stream,
+                [&](const void* q, const void* k, cudaStream_t s) {
+                    return launch_band_scores(g, bp, units, q, k, nullptr, fws, BL, false, s);
+                },
+                [&](const void* q, const void* k, const void* v, void* o, cudaStream_t s) {
+                    return launch_band_hops(g, bp, units, q, k, v, hops, alpha, o, fws, BL, s);
+                });
+        }
+        if (hops > 0 && use_block(g, dtype)) {
+            BlockLayout KL;
+            if ((st = plan_block_layout(g, units, &KL))) return st;
+            return forward_host_overlapped(
+                Q, K, V, B, H, g, hops, alpha, out, dQ, dK, dV, dO, fws, fws_bytes, bytes, stream,
+                [&](const void* q, const void* k, cudaStream_t s) {
+                    return launch_block_scores(g, units, q, k, fws, KL, s);
+                },
+                [&](const void* q, const void* k, const void* v, void* o, cudaStream_t s) {
+                    return launch_block_hops(g, units, q, k, v, hops, alpha, o, fws, KL, s);
+                });
+        }
         cudaError_t err = cudaMemcpyAsync(dQ, Q, bytes, cudaMemcpyHostToDevice, stream);
         if (err == cudaSuccess) err = cudaMemcpyAsync(dK, K, bytes, cudaMemcpyHostToDevice, stream);
         if (err == cudaSuccess) err = cudaMemcpyAsync(dV, V, bytes, cudaMemcpyHostToDevice, stream);

@@ -639,15 +639,9 @@ int plan_block_layout(const diffuser_graph* g, int64_t units, BlockLayout* L) {
     return DIFFUSER_OK;
 }
 
-int launch_block_forward(const diffuser_graph* g, int64_t units, const void* Q, const void* K,
-                         const void* V, int32_t hops, float alpha, void* out, char* ws,
-                         const BlockLayout& L, cudaStream_t stream) {
-    CUtensorMap tmQ, tmK, tmV, tmZ[2];
-    int st = encode_map(&tmQ, Q, g->n, units, kHeadDim, kTile);
-    if (!st) st = encode_map(&tmK, K, g->n, units, kHeadDim, kBlock);
-    if (!st) st = encode_map(&tmV, V, g->n, units, kHeadDim, kBlock);
-    for (int s = 0; s < 2 && !st; ++s) st = encode_map(&tmZ[s], ws + L.z[s], g->n, units, 2 * kHeadDim, kBlock);
-    if (st) return st;
+namespace {
+
+BlockArgs block_args(const diffuser_graph* g, int64_t units, char* ws, const BlockLayout& L) {
     BlockArgs a;
     a.n = g->n;
     a.units = units;
@@ -657,12 +651,39 @@ int launch_block_forward(const diffuser_graph* g, int64_t units, const void* Q, 
     a.order = g->d_blk_order;
     a.mb2 = reinterpret_cast<float*>(ws + L.mb2);
     a.inv_l = reinterpret_cast<float*>(ws + L.inv_l);
+    a.V = nullptr;
+    a.out = nullptr;
+    a.alpha = 0.f;
+    a.status = g->d_status;
+    a.Z_out = nullptr;
+    return a;
+}
+
+}  // namespace
+
+int launch_block_scores(const diffuser_graph* g, int64_t units, const void* Q, const void* K, char* ws,
+                        const BlockLayout& L, cudaStream_t stream) {
+    CUtensorMap tmQ, tmK;
+    int st = encode_map(&tmQ, Q, g->n, units, kHeadDim, kTile);
+    if (!st) st = encode_map(&tmK, K, g->n, units, kHeadDim, kBlock);
+    if (st) return st;
+    const BlockArgs a = block_args(g, units, ws, L);
+    return launch_block<kScore>(tmQ, tmK, tmK, a, stream);     // the score pass loads no Z
+}
+
+int launch_block_hops(const diffuser_graph* g, int64_t units, const void* Q, const void* K,
+                      const void* V, int32_t hops, float alpha, void* out, char* ws,
+                      const BlockLayout& L, cudaStream_t stream) {
+    CUtensorMap tmQ, tmK, tmV, tmZ[2];
+    int st = encode_map(&tmQ, Q, g->n, units, kHeadDim, kTile);
+    if (!st) st = encode_map(&tmK, K, g->n, units, kHeadDim, kBlock);
+    if (!st) st = encode_map(&tmV, V, g->n, units, kHeadDim, kBlock);
+    for (int s = 0; s < 2 && !st; ++s) st = encode_map(&tmZ[s], ws + L.z[s], g->n, units, 2 * kHeadDim, kBlock);
+    if (st) return st;
+    BlockArgs a = block_args(g, units, ws, L);
     a.V = static_cast<const __nv_bfloat16*>(V);
     a.out = static_cast<__nv_bfloat16*>(out);
     a.alpha = alpha;
-    a.status = g->d_status;
-    a.Z_out = nullptr;
-    if ((st = launch_block<kScore>(tmQ, tmK, tmV, a, stream))) return st;
     // Z_{k+1} of hop k lives in z[k & 1]; hop k reads Z_k (V for k = 0)
     for (int32_t k = 0; k < hops; ++k) {
         const bool first = k == 0, last = k == hops - 1;
@@ -675,6 +696,13 @@ int launch_block_forward(const diffuser_graph* g, int64_t units, const void* Q, 
         if (st) return st;
     }
     return DIFFUSER_OK;
+}
+
+int launch_block_forward(const diffuser_graph* g, int64_t units, const void* Q, const void* K,
+                         const void* V, int32_t hops, float alpha, void* out, char* ws,
+                         const BlockLayout& L, cudaStream_t stream) {
+    int st = launch_block_scores(g, units, Q, K, ws, L, stream);
+    return st ? st : launch_block_hops(g, units, Q, K, V, hops, alpha, out, ws, L, stream);
 }
 
 }  // namespace dfs

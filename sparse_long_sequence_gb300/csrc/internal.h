@@ -190,6 +190,12 @@ struct BlockLayout {
 bool block_eligible(const diffuser_graph* g);
 int build_block_tiles(diffuser_graph* g);      // from the host CSR copy; no-op for other graphs
 int plan_block_layout(const diffuser_graph* g, int64_t units, BlockLayout* L);
+// the score pass (row max and sum) and the hops; launch_block_forward runs both
+int launch_block_scores(const diffuser_graph* g, int64_t units, const void* Q, const void* K, char* ws,
+                        const BlockLayout& L, cudaStream_t stream);
+int launch_block_hops(const diffuser_graph* g, int64_t units, const void* Q, const void* K,
+                      const void* V, int32_t hops, float alpha, void* out, char* ws,
+                      const BlockLayout& L, cudaStream_t stream);
 int launch_block_forward(const diffuser_graph* g, int64_t units, const void* Q, const void* K,
                          const void* V, int32_t hops, float alpha, void* out, char* ws,
                          const BlockLayout& L, cudaStream_t stream);

@@ -104,3 +104,25 @@ def test_block_path_full_bigbird_workload_selected(dl):
     w = workloads.BIGBIRD
     g = dl.diffuser_build_block_graph(**w.graph_args())
     assert dl.diffuser_kernels_for(g, dl.DIFFUSER_DTYPE_BF16) == dl.DIFFUSER_KERNELS_BLOCK
+
+
+@pytest.mark.parametrize("pinned_out", [True, False], ids=["pinned_out", "pageable_out"])
+def test_block_path_host_buffers(dl, pinned_out):
+    # the end-to-end entry point on the block path: Q and K upload side by side, V under
+    # the score pass, a pinned mapped `out` written in place (a pageable one copied back);
+    # three calls so that the pinned sequence is also replayed as a captured graph
+    import torch
+    args = dict(n=1000, block=64, window_blocks=3, rand_blocks=3, global_blocks=2, seed=0)
+    g = dl.diffuser_build_block_graph(**args)
+    Q, K, V = synthetic.qkv(2, 2, 1000, 64, "bf16", seed=9)
+    Qh, Kh, Vh = (torch.from_numpy(x).view(torch.bfloat16).pin_memory() for x in (Q, K, V))
+    out = torch.empty_like(Vh).pin_memory() if pinned_out else torch.empty(Vh.shape, dtype=Vh.dtype)
+    ws = dl.alloc_workspace(dl.diffuser_host_workspace_size(g, 2, 2, 64, dl.DIFFUSER_DTYPE_BF16))
+    ref_dev = dl.diffuser_forward(Qh.cuda(), Kh.cuda(), Vh.cuda(), g, 5, 0.1)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        out.zero_()
+        dl.diffuser_forward_host(Qh, Kh, Vh, g, 5, 0.1, out, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_dev.cpu())
+    assert dl.diffuser_graph_status(g) == 0
