@@ -13,11 +13,11 @@
 //    block rows each key block is allowed for.  The lists are built once per
 //    graph on the host from the graph's own CSR (every token of a block row
 //    has the same neighbour set, so the first token's row gives the blocks).
-//  * block_score_kernel: S = Q_tile K_chunk^T per chunk (bf16 operands, fp32
-//    accumulation in tensor memory); each row's maximum and sum of exp(s - max)
-//    over its allowed keys, kept online in registers (the row softmax,
-//    "Diffuser: modelling long sequences with multi-hop attention diffusion",
-//    eq S.1-S.5): m_i (base-2 exponent scale) and inv_l_i = 1 / l_i.
+//  * the score pass: S = Q_tile K_chunk^T per chunk (bf16 operands, fp32
+//    accumulation in tensor memory); each row's maximum over its allowed keys
+//    (the row softmax, "Diffuser: modelling long sequences with multi-hop
+//    attention diffusion", eq S.1-S.5): m_i on the base-2 exponent scale.  The
+//    first hop adds up each row's weights and stores inv_l_i = 1 / l_i.
 //  * block_hop_kernel (one launch per hop, eq S.7): S again for every chunk
 //    (the same MMAs, so the same values), e_ij = 2^(s_ij log2(e) / 8 - m_i) on
 //    the allowed keys (0 elsewhere) written over the scores as bf16 hi + lo
@@ -27,14 +27,17 @@
 //    only one left out.  Epilogue: z_i = (1 - alpha) inv_l_i D_i + alpha V_i,
 //    written as the next [hi | lo] row, or as the bf16 output after the last
 //    hop.  Storing A instead would cost 4 bytes per edge per hop of HBM
-//    traffic; the recomputation costs one exp per edge and a K = 64 MMA.
+//    traffic; the recomputation costs one exp per edge and a K = 64 MMA.  The
+//    first hop's weight warps also add up each row's weights (fp32, before the
+//    split) and hand the four key slices' sums to the epilogue, which stores
+//    inv_l_i for the later hops.
 //
 // Roles (24 warps, one CTA per SM, persistent over a per-CTA tile table):
 // warp 0 loads Q tiles and K chunks (TMA), warp 1 issues the score MMAs,
 // warp 2 the weights' MMAs, warp 3 loads the Z_k chunks, warps 4-19 turn
 // scores into weights (warp w: TMEM lane quadrant w % 4, keys 16 ((w - 4) / 4)
 // .. +15 of both 64-key halves), warps 20-23 are the epilogue (hop) or merge
-// the four key slices' row statistics (score).  Every barrier wait is bounded
+// the four key slices' row maxima (score).  Every barrier wait is bounded
 // (ptx::mbar_wait) and records a status instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -87,7 +90,7 @@ struct BlockArgs {
     const int32_t* tile_ptr;       // [tiles + 1] chunk range of each position
     const int32_t* order;          // [tiles] positions by falling chunk count
     float* mb2;                    // [units][n] row max of s log2(e) / 8 over the allowed keys
-    float* inv_l;                  // [units][n] 1 / sum of 2^(s log2(e) / 8 - mb2)
+    float* inv_l;                  // [units][n] 1 / sum of 2^(s log2(e) / 8 - mb2) (first hop)
     const __nv_bfloat16* V;        // [units][n][64]
     __nv_bfloat16* Z_out;          // [units][n][hi 64 | lo 64], all hops but the last
     __nv_bfloat16* out;            // the last hop's output [units][n][64]
@@ -97,7 +100,7 @@ struct BlockArgs {
 
 __host__ __device__ constexpr int block_smem_bytes() {
     return 1024 + 2 * kQBytes + kSlots * (kKBytes + kZStageBytes) + 4 * 32 * kEpiRowFloats * 4 +
-           4 * 32 * 4 + 2 * kSlices * kTile * 2 * 4 + kMaxCtaTiles * (int)sizeof(TileEntry) + 256;
+           4 * 32 * 4 + 2 * kSlices * kTile * 4 + kMaxCtaTiles * (int)sizeof(TileEntry) + 256;
 }
 static_assert(block_smem_bytes() <= 227 * 1024, "shared memory per CTA");
 static_assert(block_smem_bytes() > 116 * 1024, "must exclude a second CTA per SM");
@@ -125,8 +128,8 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     uint8_t* sZ = sK + kSlots * kKBytes;                         // kSlots x (hi 16 KB, lo 16 KB)
     float* sEpi = reinterpret_cast<float*>(sZ + kSlots * kZStageBytes);   // [4][32][68]
     float* sKeep = sEpi + 4 * 32 * kEpiRowFloats;                // [4][32]
-    float* xch = sKeep + 4 * 32;                                 // [2][kSlices][128][2] row stats
-    TileEntry* sTile = reinterpret_cast<TileEntry*>(xch + 2 * kSlices * kTile * 2);
+    float* xch = sKeep + 4 * 32;                                 // [2][kSlices][128] row maxima / sums
+    TileEntry* sTile = reinterpret_cast<TileEntry*>(xch + 2 * kSlices * kTile);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sTile + kMaxCtaTiles);
     uint64_t* full_Q = bars;                  // [2]
     uint64_t* empty_Q = full_Q + 2;           // [2]
@@ -136,8 +139,9 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     uint64_t* slot_free = full_P + kSlots;    // [kSlots] hop: weights' MMAs done; score: S read
     uint64_t* acc_full = slot_free + kSlots;
     uint64_t* acc_empty = acc_full + 1;
-    uint64_t* xch_full = acc_empty + 1;       // [4][2] score: a quadrant's slices wrote their stats
-    uint64_t* xch_empty = xch_full + 8;       // [4][2] score: the merge has read them
+    uint64_t* xch_full = acc_empty + 1;       // [4][2] a quadrant's slices wrote their row maxima
+                                              // (score) or row sums (first hop)
+    uint64_t* xch_empty = xch_full + 8;       // [4][2] the epilogue warp has read them
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xch_empty + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -306,14 +310,25 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         int64_t urow = 0;
         bool row_ok = false;
         float b2 = 0.f;                              // hop: this row's m_i
-        float m = -INFINITY, l = 0.f;                // score: running max and sum
+        float m = -INFINITY;                         // score: running max
+        float lsum = 0.f;                            // first hop: this slice's part of the row sum
         auto enter_tile = [&]() {
             const int64_t i = (int64_t)te.t * kTile + t;
             row_ok = i < a.n;
             urow = (size_t)te.u * a.n + (row_ok ? i : 0);
             if (kHop) b2 = row_ok ? __ldg(a.mb2 + urow) : 0.f;
             m = -INFINITY;
-            l = 0.f;
+            lsum = 0.f;
+        };
+        // this slice's value of the row (max or sum) for the quadrant's epilogue warp at
+        // the tile's last chunk; the buffer of this parity is free once that warp has
+        // read tile lt - 2's
+        auto hand_over = [&](float v) {
+            const int xb = quad * 2 + (lt & 1);
+            if (lt >= 2) ptx::mbar_wait(&xch_empty[xb], ((lt / 2) - 1) & 1, a.status);
+            xch[((lt & 1) * kSlices + slice) * kTile + t] = v;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&xch_full[xb]);
         };
         if (my_tiles > 0) enter_tile();
         for (int g = 0; g < total; ++g) {
@@ -336,31 +351,12 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&slot_free[sb]);       // the scores are in registers
-                float gm = -INFINITY;
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    if (k < lim0) gm = fmaxf(gm, __uint_as_float(ra[k]) * kLog2eScale);
-                    if (k < lim1) gm = fmaxf(gm, __uint_as_float(rb[k]) * kLog2eScale);
+                    if (k < lim0) m = fmaxf(m, __uint_as_float(ra[k]) * kLog2eScale);
+                    if (k < lim1) m = fmaxf(m, __uint_as_float(rb[k]) * kLog2eScale);
                 }
-                if (gm > m) { l *= ptx::ex2_approx(m - gm); m = gm; }
-                float s = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    if (k < lim0) s += ptx::ex2_approx(fmaf(__uint_as_float(ra[k]), kLog2eScale, -m));
-                    if (k < lim1) s += ptx::ex2_approx(fmaf(__uint_as_float(rb[k]), kLog2eScale, -m));
-                }
-                l += s;
-                if (c == te.c1 - 1) {
-                    // this slice's (m, l) of the row for the quadrant's merge warp; the buffer
-                    // of this parity is free once that warp has read tile lt - 2's
-                    const int xb = quad * 2 + (lt & 1);
-                    if (lt >= 2) ptx::mbar_wait(&xch_empty[xb], ((lt / 2) - 1) & 1, a.status);
-                    float* xs = xch + (((lt & 1) * kSlices + slice) * kTile + t) * 2;
-                    xs[0] = m;
-                    xs[1] = l;
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&xch_full[xb]);
-                }
+                if (c == te.c1 - 1) hand_over(m);
             } else {
                 uint32_t hw[8], lw[8];
                 auto weights = [&](const uint32_t (&r)[16], int lim) {
@@ -369,6 +365,7 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                         const int k0 = 2 * p2, k1 = 2 * p2 + 1;
                         const float x0 = k0 < lim ? ptx::ex2_approx(fmaf(__uint_as_float(r[k0]), kLog2eScale, -b2)) : 0.f;
                         const float x1 = k1 < lim ? ptx::ex2_approx(fmaf(__uint_as_float(r[k1]), kLog2eScale, -b2)) : 0.f;
+                        if (kHop0) lsum += x0 + x1;
                         const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
                         const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
                         hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
@@ -384,6 +381,7 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&full_P[sb]);
+                if (kHop0 && c == te.c1 - 1) hand_over(lsum);
             }
             if (++sb == kSlots) { sb = 0; sph ^= 1; }
             if (++c == te.c1 && ++lt < my_tiles) {
@@ -395,32 +393,24 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     } else if (warp >= kEpiWarp0) {
         const int quad = warp & 3;
         const int t = quad * 32 + lane;
+        // the four key slices' values of row t of tile lt (max or sum), in slice order
+        auto take_over = [&](int lt, bool is_max) {
+            const int xb = quad * 2 + (lt & 1);
+            ptx::mbar_wait(&xch_full[xb], (lt / 2) & 1, a.status);
+            const float* xs = xch + (lt & 1) * kSlices * kTile + t;
+            const float v = is_max ? fmaxf(fmaxf(xs[0], xs[kTile]), fmaxf(xs[2 * kTile], xs[3 * kTile]))
+                                   : ((xs[0] + xs[kTile]) + xs[2 * kTile]) + xs[3 * kTile];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&xch_empty[xb]);
+            return v;
+        };
         if constexpr (!kHop) {
-            // ---------------- merge of the four slices' (m, l): the row's m_i and inv_l_i
+            // ---------------- merge of the four slices' maxima: the row's m_i
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const TileEntry te = sTile[lt];
-                const int xb = quad * 2 + (lt & 1);
-                ptx::mbar_wait(&xch_full[xb], (lt / 2) & 1, a.status);
-                float ms[kSlices], ls[kSlices], mm = -INFINITY;
-#pragma unroll
-                for (int s = 0; s < kSlices; ++s) {
-                    const float* xs = xch + (((lt & 1) * kSlices + s) * kTile + t) * 2;
-                    ms[s] = xs[0];
-                    ls[s] = xs[1];
-                    mm = fmaxf(mm, ms[s]);
-                }
-                float ll = 0.f;
-#pragma unroll
-                for (int s = 0; s < kSlices; ++s)
-                    if (ls[s] > 0.f) ll += ls[s] * ptx::ex2_approx(ms[s] - mm);
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&xch_empty[xb]);
+                const float mm = take_over(lt, true);
                 const int64_t i = (int64_t)te.t * kTile + t;
-                if (i < a.n) {
-                    const size_t urow = (size_t)te.u * a.n + i;
-                    a.mb2[urow] = mm;
-                    a.inv_l[urow] = 1.f / ll;
-                }
+                if (i < a.n) a.mb2[(size_t)te.u * a.n + i] = mm;
             }
         } else {
             // ---------------- epilogue: accumulator rows -> shared staging -> half a warp
@@ -435,7 +425,15 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 const int64_t i = i0 + t;
                 const bool row_ok = i < a.n;
                 const size_t urow = (size_t)te.u * a.n + (row_ok ? i : 0);
-                const float inv = row_ok ? __ldg(a.inv_l + urow) : 0.f;
+                float inv;
+                if (kHop0) {
+                    // the first hop completes the row sum from the four slices' parts
+                    const float l = take_over(lt, false);
+                    inv = row_ok ? 1.f / l : 0.f;
+                    if (row_ok) a.inv_l[urow] = inv;
+                } else {
+                    inv = row_ok ? __ldg(a.inv_l + urow) : 0.f;
+                }
                 ptx::mbar_wait(acc_full, lt & 1, a.status);
                 __syncwarp();
                 ptx::tc_fence_after();
