@@ -90,13 +90,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 // rings, the out-of-window globals' weight image (hi, lo; g16 slots) and their
 // Z_k rows as an MN-major B tile (hi, lo), the row-sum exchange, barriers.
 // The CTA's tiles as a shared-memory table (filled once, read by every role).
-constexpr int kMaxCtaTiles = 256;         // the launch keeps each CTA at or below this many tiles
+constexpr int kMaxCtaTiles = 192;         // the launch keeps each CTA at or below this many tiles
 struct TileEntry { int32_t u, t; int16_t c_lo, c_hi; };
 __host__ __device__ constexpr int band_smem_bytes(int g16) {
     return 1024 + band::kGImgBytes + 2 * kQBytes + kSBufs * (kKBytes + kZStageBytes) +
            2 * kTileRows * (g16 > 0 ? g16 : 16) * 2 + 2 * (g16 > 0 ? g16 : 16) * 128 +
-           2 * kSoftThreads * 4 + 4 * 32 * kEpiRowFloats * 4 + 4 * 32 * 4 +
-           kMaxCtaTiles * (int)sizeof(TileEntry) + 16 + 1024;
+           2 * kSoftThreads * 4 + 4 * 32 * kEpiRowFloats * 4 + 4 * 32 * 4 + 4 * 32 * kHeadDim * 2 +
+           kMaxCtaTiles * (int)sizeof(TileEntry) + 16 + 512;
 }
 constexpr int kSmemBytesMax = band_smem_bytes(16) > band_smem_bytes(kBandMaxGlobals)
                                   ? band_smem_bytes(16) : band_smem_bytes(kBandMaxGlobals);
@@ -308,7 +308,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     float* xch = reinterpret_cast<float*>(sZG + 2 * g16s * 128);  // [2][256] row-sum halves
     float* sEpi = xch + 2 * kSoftThreads;                        // [4][32][68] epilogue staging
     float* sEpiKeep = sEpi + 4 * 32 * kEpiRowFloats;             // [4][32]
-    TileEntry* sTile = reinterpret_cast<TileEntry*>(sEpiKeep + 4 * 32);   // [kMaxCtaTiles]
+    __nv_bfloat16* sEpiV = reinterpret_cast<__nv_bfloat16*>(sEpiKeep + 4 * 32);   // [4][32][64] V rows
+    TileEntry* sTile = reinterpret_cast<TileEntry*>(sEpiV + 4 * 32 * kHeadDim);   // [kMaxCtaTiles]
     int* sTotal = reinterpret_cast<int*>(sTile + kMaxCtaTiles);         // this CTA's chunk count
     uint64_t* bars = reinterpret_cast<uint64_t*>(sTotal + 4);
     uint64_t* full_Q = bars;                                     // [2]
@@ -689,6 +690,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int t = quad * 32 + lane;
         float* st = sEpi + quad * (32 * kEpiRowFloats);                    // [32 rows][68]
         float* sk = sEpiKeep + quad * 32;                                  // keep of each row (< 0: skip)
+        __nv_bfloat16* sv = sEpiV + quad * 32 * kHeadDim;                   // [32 rows][64] V
         const int hr = lane >> 4, f4 = lane & 15;                          // row of the pair, feature quad
         // The out-of-window globals of tile lt: their weights' image by bulk copy, and
         // the global keys' Z_k rows as an MN-major B tile (key row s: hi 128 bytes,
@@ -731,6 +733,30 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         };
         if (has_g && my_tiles > 0) stage_gc(0);
         for (int lt = 0; lt < my_tiles; ++lt) {
+            {
+                // this quadrant's rows of Psum into its staging rows and of V into its V
+                // rows, as asynchronous copies issued before the accumulator is waited
+                // for (the tile's MMAs hide their latency); the accumulator is added to
+                // the Psum rows below.  Lanes 0-15 copy one 256-byte Psum row, lanes
+                // 16-31 the next; a 128-byte V row takes 8 lanes.
+                const TileInfo tp = tile(lt);
+                const size_t ub = (size_t)tp.u * P.n;
+#pragma unroll
+                for (int it = 0; it < 16; ++it) {
+                    const int idx = it * 32 + lane, r = idx >> 4, c = idx & 15;
+                    const int64_t ir = tp.i0 + quad * 32 + r;
+                    if (ir < P.n)
+                        ptx::cp_async16(st + r * kEpiRowFloats + 4 * c, a.Psum + (ub + ir) * kHeadDim + 4 * c);
+                }
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int idx = it * 32 + lane, r = idx >> 3, c = idx & 7;
+                    const int64_t ir = tp.i0 + quad * 32 + r;
+                    if (ir < P.n)
+                        ptx::cp_async16(sv + r * kHeadDim + 8 * c, a.V + (ub + ir) * kHeadDim + 8 * c);
+                }
+                ptx::cp_async_commit();
+            }
             if (has_g && lt + 1 < my_tiles) {
                 ptx::mbar_wait(empty_GC, lt & 1, a.status);      // tile lt's globals' MMAs are done
                 stage_gc(lt + 1);
@@ -754,10 +780,12 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (row_ok) a.inv_l[urow] = inv;
             }
             ptx::mbar_wait(acc_full, lt & 1, a.status);
-            __syncwarp();       // reconverge before the warp-collective tcgen05.ld
+            ptx::cp_async_wait_all();
+            __syncwarp();       // reconverge before the warp-collective tcgen05.ld; the
+                                // quadrant's Psum and V rows are in shared memory
             ptx::tc_fence_after();
-            // the accumulator rows (D[0:64) + D[64:128)) into shared memory, two
-            // loads in flight per wait
+            // the accumulator rows (D[0:64) + D[64:128)) added to them, two loads in
+            // flight per wait
 #pragma unroll
             for (int h = 0; h < 4; h += (kHop0 ? 2 : 1)) {
                 uint32_t dr[32];
@@ -773,8 +801,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                       : __uint_as_float(dr[k]) + __uint_as_float(dr[16 + k]);
                     float4* dst = reinterpret_cast<float4*>(st + lane * kEpiRowFloats + 16 * (h + hh));
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-                        dst[c4] = make_float4(dh[4 * c4], dh[4 * c4 + 1], dh[4 * c4 + 2], dh[4 * c4 + 3]);
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const float4 p = dst[c4];
+                        dst[c4] = make_float4(dh[4 * c4] + p.x, dh[4 * c4 + 1] + p.y, dh[4 * c4 + 2] + p.z,
+                                              dh[4 * c4 + 3] + p.w);
+                    }
                 }
             }
             ptx::tc_fence_before();
@@ -816,7 +847,6 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const size_t ubase = (size_t)u * P.n;
 #pragma unroll 1
             for (int it0 = 0; it0 < 16; it0 += 4) {
-                float4 pv[4];
                 uint2 vv[4];
                 float keep[4];
                 size_t rr[4];
@@ -825,20 +855,17 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int r = 2 * (it0 + q) + hr;
                     keep[q] = sk[r];
                     rr[q] = ubase + (size_t)(i0 + quad * 32 + r);
-                    if (keep[q] >= 0.f) {
-                        pv[q] = __ldg(reinterpret_cast<const float4*>(a.Psum + rr[q] * kHeadDim) + f4);
-                        vv[q] = __ldg(reinterpret_cast<const uint2*>(a.V + rr[q] * kHeadDim) + f4);
-                    }
+                    if (keep[q] >= 0.f) vv[q] = reinterpret_cast<const uint2*>(sv + r * kHeadDim)[f4];
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     if (keep[q] < 0.f) continue;
                     const int r = 2 * (it0 + q) + hr;
-                    const float4 dv = *reinterpret_cast<const float4*>(st + r * kEpiRowFloats + 4 * f4);
-                    float z[4] = {fmaf(keep[q], dv.x + pv[q].x, a.alpha * bf16lo(vv[q].x)),
-                                  fmaf(keep[q], dv.y + pv[q].y, a.alpha * bf16hi(vv[q].x)),
-                                  fmaf(keep[q], dv.z + pv[q].z, a.alpha * bf16lo(vv[q].y)),
-                                  fmaf(keep[q], dv.w + pv[q].w, a.alpha * bf16hi(vv[q].y))};
+                    const float4 dv = *reinterpret_cast<const float4*>(st + r * kEpiRowFloats + 4 * f4);   // D + Psum
+                    float z[4] = {fmaf(keep[q], dv.x, a.alpha * bf16lo(vv[q].x)),
+                                  fmaf(keep[q], dv.y, a.alpha * bf16hi(vv[q].x)),
+                                  fmaf(keep[q], dv.z, a.alpha * bf16lo(vv[q].y)),
+                                  fmaf(keep[q], dv.w, a.alpha * bf16hi(vv[q].y))};
                     const __nv_bfloat162 h0 = __floats2bfloat162_rn(z[0], z[1]);
                     const __nv_bfloat162 h1 = __floats2bfloat162_rn(z[2], z[3]);
                     const uint2 hv = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),

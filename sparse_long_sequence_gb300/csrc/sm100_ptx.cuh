@@ -169,6 +169,15 @@ __device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// 16-byte global -> shared copy that completes asynchronously (L2 only, no L1
+// allocation); cp_async_wait_all waits for this thread's copies, after which a
+// __syncwarp (or __syncthreads) makes them visible to the other threads.
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Contiguous shared -> global copy by the bulk-copy engine (bulk_group
 // completion): addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
