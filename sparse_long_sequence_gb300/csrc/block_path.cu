@@ -100,7 +100,8 @@ struct BlockArgs {
 
 __host__ __device__ constexpr int block_smem_bytes() {
     return 1024 + 2 * kQBytes + kSlots * (kKBytes + kZStageBytes) + 4 * 32 * kEpiRowFloats * 4 +
-           4 * 32 * 4 + 2 * kSlices * kTile * 4 + kMaxCtaTiles * (int)sizeof(TileEntry) + 256;
+           4 * 32 * 4 + 4 * 32 * kHeadDim * 2 + 2 * kSlices * kTile * 4 +
+           kMaxCtaTiles * (int)sizeof(TileEntry) + 256;
 }
 static_assert(block_smem_bytes() <= 227 * 1024, "shared memory per CTA");
 static_assert(block_smem_bytes() > 116 * 1024, "must exclude a second CTA per SM");
@@ -128,7 +129,8 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     uint8_t* sZ = sK + kSlots * kKBytes;                         // kSlots x (hi 16 KB, lo 16 KB)
     float* sEpi = reinterpret_cast<float*>(sZ + kSlots * kZStageBytes);   // [4][32][68]
     float* sKeep = sEpi + 4 * 32 * kEpiRowFloats;                // [4][32]
-    float* xch = sKeep + 4 * 32;                                 // [2][kSlices][128] row maxima / sums
+    __nv_bfloat16* sEpiV = reinterpret_cast<__nv_bfloat16*>(sKeep + 4 * 32);   // [4][32][64] V rows
+    float* xch = reinterpret_cast<float*>(sEpiV + 4 * 32 * kHeadDim);   // [2][kSlices][128] row maxima / sums
     TileEntry* sTile = reinterpret_cast<TileEntry*>(xch + 2 * kSlices * kTile);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sTile + kMaxCtaTiles);
     uint64_t* full_Q = bars;                  // [2]
@@ -418,10 +420,24 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
             float* st = sEpi + quad * (32 * kEpiRowFloats);
             float* sk = sKeep + quad * 32;
+            __nv_bfloat16* sv = sEpiV + quad * 32 * kHeadDim;       // [32 rows][64] V
             const int hr = lane >> 4, f4 = lane & 15;
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const TileEntry te = sTile[lt];
                 const int64_t i0 = (int64_t)te.t * kTile;
+                {
+                    // this quadrant's V rows into shared memory, as asynchronous copies issued
+                    // before the accumulator is waited for (8 lanes per 128-byte row); the
+                    // previous tile's loop has finished reading them
+                    const size_t ub = (size_t)te.u * a.n;
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int idx = it * 32 + lane, r = idx >> 3, c = idx & 7;
+                        const int64_t ir = i0 + quad * 32 + r;
+                        if (ir < a.n) ptx::cp_async16(sv + r * kHeadDim + 8 * c, a.V + (ub + ir) * kHeadDim + 8 * c);
+                    }
+                    ptx::cp_async_commit();
+                }
                 const int64_t i = i0 + t;
                 const bool row_ok = i < a.n;
                 const size_t urow = (size_t)te.u * a.n + (row_ok ? i : 0);
@@ -435,7 +451,8 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     inv = row_ok ? __ldg(a.inv_l + urow) : 0.f;
                 }
                 ptx::mbar_wait(acc_full, lt & 1, a.status);
-                __syncwarp();
+                ptx::cp_async_wait_all();
+                __syncwarp();       // reconverge for tcgen05.ld; the V rows are in shared memory
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < 4; h += (kHop0 ? 2 : 1)) {
@@ -471,7 +488,7 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                         const int r = 2 * (it0 + q) + hr;
                         keep[q] = sk[r];
                         rr[q] = ubase + (size_t)(i0 + quad * 32 + r);
-                        if (keep[q] >= 0.f) vv[q] = __ldg(reinterpret_cast<const uint2*>(a.V + rr[q] * kHeadDim) + f4);
+                        if (keep[q] >= 0.f) vv[q] = reinterpret_cast<const uint2*>(sv + r * kHeadDim)[f4];
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
