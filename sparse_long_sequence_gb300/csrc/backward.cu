@@ -6,8 +6,11 @@
 // dtype.  With G_K = dOut, after recomputing A and Z_1 .. Z_{K-1} with the
 // forward's own kernels, for k = K-1 .. 0:
 //
-//  * bwd_weight_grad_kernel (warp per row i, lane per edge, G_{k+1}[i] held
-//    in registers):  dA_e += (1 - alpha) G_{k+1}[i] . Z_k[j]  for e = (i, j);
+//  * bwd_weight_grad_kernel (warp per row i, 32 edges per round; lane l holds
+//    features 2l, 2l+1 of G_{k+1}[i] and reads the same two features of every
+//    edge's Z_k row, one coalesced line per row; a butterfly over the lanes
+//    leaves edge t's dot product with lane t):
+//    dA_e += (1 - alpha) G_{k+1}[i] . Z_k[j]  for e = (i, j);
 //  * bwd_hop_t_kernel (warp per key j over its incoming edges, the transposed
 //    graph; lanes own feature pairs):  G_k[j] = (1 - alpha) sum_e A_e G_{k+1}[i],
 //    and dV_acc[j] += alpha G_{k+1}[j]; at k = 0 it writes dV = dV_acc + G_0
@@ -48,52 +51,6 @@ __device__ __forceinline__ void store2(__nv_bfloat16* p, float2 v) {
     *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
 }
 
-// A whole 64-wide row in 64 fp32 registers.
-__device__ __forceinline__ void load_row(const float* p, float (&x)[64]) {
-    const float4* q = reinterpret_cast<const float4*>(p);
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        const float4 v = __ldg(q + c);
-        x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
-    }
-}
-__device__ __forceinline__ void load_row(const __nv_bfloat16* p, float (&x)[64]) {
-    const uint4* q = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 v = __ldg(q + c);
-        x[8 * c] = bf16lo(v.x); x[8 * c + 1] = bf16hi(v.x); x[8 * c + 2] = bf16lo(v.y);
-        x[8 * c + 3] = bf16hi(v.y); x[8 * c + 4] = bf16lo(v.z); x[8 * c + 5] = bf16hi(v.z);
-        x[8 * c + 6] = bf16lo(v.w); x[8 * c + 7] = bf16hi(v.w);
-    }
-}
-
-// g . z over 64 features, z read from memory in 16-byte pieces.
-__device__ __forceinline__ float dot_row(const float (&g)[64], const float* z) {
-    const float4* q = reinterpret_cast<const float4*>(z);
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        const float4 v = __ldg(q + c);
-        acc = fmaf(g[4 * c], v.x, acc); acc = fmaf(g[4 * c + 1], v.y, acc);
-        acc = fmaf(g[4 * c + 2], v.z, acc); acc = fmaf(g[4 * c + 3], v.w, acc);
-    }
-    return acc;
-}
-__device__ __forceinline__ float dot_row(const float (&g)[64], const __nv_bfloat16* z) {
-    const uint4* q = reinterpret_cast<const uint4*>(z);
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 v = __ldg(q + c);
-        acc = fmaf(g[8 * c], bf16lo(v.x), acc); acc = fmaf(g[8 * c + 1], bf16hi(v.x), acc);
-        acc = fmaf(g[8 * c + 2], bf16lo(v.y), acc); acc = fmaf(g[8 * c + 3], bf16hi(v.y), acc);
-        acc = fmaf(g[8 * c + 4], bf16lo(v.z), acc); acc = fmaf(g[8 * c + 5], bf16hi(v.z), acc);
-        acc = fmaf(g[8 * c + 6], bf16lo(v.w), acc); acc = fmaf(g[8 * c + 7], bf16hi(v.w), acc);
-    }
-    return acc;
-}
-
 struct BwdArgs {
     const int64_t* row_ptr;   // CSR [n + 1]
     const int32_t* col;       // CSR [nnz]
@@ -114,13 +71,22 @@ bwd_weight_grad_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict
     const int64_t u = gw / a.n, i = gw - u * a.n;
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
-    if (e0 == e1) return;
-    float g[64];
-    load_row(G + unit + (size_t)i * kHeadDim, g);
+    const float2 g = load2(G + unit + (size_t)i * kHeadDim + 2 * lane);
+    const TZ* Zu = Z + unit + 2 * lane;
     float* dAu = dA + (size_t)u * a.nnz;
-    for (int64_t e = e0 + lane; e < e1; e += 32) {
-        const int64_t j = a.col[e];
-        dAu[e] += keep * dot_row(g, Z + unit + (size_t)j * kHeadDim);
+    for (int64_t base = e0; base < e1; base += 32) {
+        const int64_t e = base + lane;
+        const int32_t j_l = e < e1 ? a.col[e] : 0;
+        const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
+        float p[32];        // all 32 rows requested before the first is used
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            const int32_t j = __shfl_sync(0xffffffffu, j_l, t);
+            const float2 z = t < cnt ? load2(Zu + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
+            p[t] = fmaf(g.x, z.x, g.y * z.y);
+        }
+        const float dot = warp_transpose_sum32(p, lane);             // edge base + lane
+        if (e < e1) dAu[e] += keep * dot;
     }
 }
 

@@ -154,6 +154,27 @@ int build_block_graph_device(diffuser_graph* g, cudaStream_t stream);
 int build_dilated_graph_device(diffuser_graph* g, cudaStream_t stream);   // dilation > 1
 
 // ---- CSR SIMT path (simt_path.cu) ------------------------------------------
+#ifdef __CUDACC__
+// v[k] of every lane of a full warp is one lane's share of value k (k < 32); on
+// return, lane l holds the sum over the 32 lanes of value l.  A butterfly over the
+// lane bits: at each of the 5 steps a lane keeps the half of its values whose index
+// bit matches its own lane bit and adds its partner's copy of it (16 + 8 + 4 + 2 + 1
+// shuffles).  The order of the additions is fixed: repeated calls give identical bits.
+__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < off; ++k) {
+            const float send = upper ? v[k] : v[k + off];
+            const float keep = upper ? v[k + off] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return v[0];
+}
+#endif
+
 struct CsrArgs {
     const int64_t* row_ptr;
     const int32_t* col;

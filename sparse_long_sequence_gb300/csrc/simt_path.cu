@@ -3,10 +3,13 @@
 // for graphs without a fast layout, and the reference implementation the
 // tensor-core kernels are checked against on the device.
 //
-//  * score_csr_kernel: one warp per (unit, row).  Lanes take edges
-//    round-robin; each lane holds q_i (64 fp32 registers) and dots it with
-//    k_j, keeping an online (max, sum) pair; the pairs are merged across the
-//    warp, then each lane normalises the weights it wrote.
+//  * score_csr_kernel: one warp per (unit, row), 32 edges per round.  Lane l
+//    holds features 2l, 2l+1 of q_i; for each edge of the round the warp reads
+//    the key row k_j whole (each lane its two features, one coalesced line per
+//    row), every lane forms its two-feature part of each of the 32 dot
+//    products, and a butterfly over the lanes leaves edge t's score with lane t.
+//    Each lane keeps an online (max, sum) pair over its edges; the pairs are
+//    merged across the warp, then each lane normalises the weights it wrote.
 //    ("Diffuser: modelling long sequences with multi-hop attention
 //    diffusion", eq S.1-S.5; "1.2.1 Static sparsity", eq 1-3.)
 //  * hop_csr_kernel: one warp per (unit, row).  Lanes own two of the 64
@@ -18,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -29,80 +33,54 @@ constexpr int kWarpsPerBlock = 8;
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Load a 64-wide row (fp32 or bf16) into 64 fp32 registers.
-template <bool kBf16>
-__device__ __forceinline__ void load_row64(const void* base, float (&x)[64]) {
-    if constexpr (kBf16) {
-        const uint4* p = reinterpret_cast<const uint4*>(base);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 v = __ldg(p + c);
-            x[8 * c + 0] = bf16lo(v.x); x[8 * c + 1] = bf16hi(v.x);
-            x[8 * c + 2] = bf16lo(v.y); x[8 * c + 3] = bf16hi(v.y);
-            x[8 * c + 4] = bf16lo(v.z); x[8 * c + 5] = bf16hi(v.z);
-            x[8 * c + 6] = bf16lo(v.w); x[8 * c + 7] = bf16hi(v.w);
-        }
-    } else {
-        const float4* p = reinterpret_cast<const float4*>(base);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            float4 v = __ldg(p + c);
-            x[4 * c + 0] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
-        }
+template <typename T> struct Pair;
+template <> struct Pair<float> {
+    static __device__ __forceinline__ float2 load(const float* p) {
+        return *reinterpret_cast<const float2*>(p);
     }
-}
+};
+template <> struct Pair<__nv_bfloat16> {
+    static __device__ __forceinline__ float2 load(const __nv_bfloat16* p) {
+        uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+        return make_float2(bf16lo(w), bf16hi(w));
+    }
+};
 
-// q . k over 64 features, k streamed in 16-byte pieces.
-template <bool kBf16>
-__device__ __forceinline__ float dot64(const float (&q)[64], const void* kbase) {
-    float acc = 0.f;
-    if constexpr (kBf16) {
-        const uint4* p = reinterpret_cast<const uint4*>(kbase);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 v = __ldg(p + c);
-            acc = fmaf(q[8 * c + 0], bf16lo(v.x), acc); acc = fmaf(q[8 * c + 1], bf16hi(v.x), acc);
-            acc = fmaf(q[8 * c + 2], bf16lo(v.y), acc); acc = fmaf(q[8 * c + 3], bf16hi(v.y), acc);
-            acc = fmaf(q[8 * c + 4], bf16lo(v.z), acc); acc = fmaf(q[8 * c + 5], bf16hi(v.z), acc);
-            acc = fmaf(q[8 * c + 6], bf16lo(v.w), acc); acc = fmaf(q[8 * c + 7], bf16hi(v.w), acc);
-        }
-    } else {
-        const float4* p = reinterpret_cast<const float4*>(kbase);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            float4 v = __ldg(p + c);
-            acc = fmaf(q[4 * c + 0], v.x, acc); acc = fmaf(q[4 * c + 1], v.y, acc);
-            acc = fmaf(q[4 * c + 2], v.z, acc); acc = fmaf(q[4 * c + 3], v.w, acc);
-        }
-    }
-    return acc;
-}
 
 template <bool kBf16>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 score_csr_kernel(CsrArgs a, const void* __restrict__ Q, const void* __restrict__ K,
                  float* __restrict__ A) {
+    using T = typename std::conditional<kBf16, __nv_bfloat16, float>::type;
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
     const int64_t u = gw / a.n, i = gw - u * a.n;
-    const size_t esz = kBf16 ? 2 : 4;
-    const char* Qb = static_cast<const char*>(Q) + (size_t)u * a.n * kHeadDim * esz;
-    const char* Kb = static_cast<const char*>(K) + (size_t)u * a.n * kHeadDim * esz;
+    const size_t unit = (size_t)u * a.n * kHeadDim;
+    const T* Ku = static_cast<const T*>(K) + unit + 2 * lane;
     float* Au = A + (size_t)u * a.nnz;
-
-    float q[64];
-    load_row64<kBf16>(Qb + (size_t)i * kHeadDim * esz, q);
+    const float2 q = Pair<T>::load(static_cast<const T*>(Q) + unit + (size_t)i * kHeadDim + 2 * lane);
     const float scale = 0.125f;  // 1/sqrt(64), exact
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
 
     float m = -INFINITY, l = 0.f;
-    for (int64_t e = e0 + lane; e < e1; e += 32) {
-        const int64_t j = a.col[e];
-        float s = dot64<kBf16>(q, Kb + (size_t)j * kHeadDim * esz) * scale;
-        Au[e] = s;
-        if (s > m) { l = l * expf(m - s) + 1.f; m = s; }
-        else       { l += expf(s - m); }
+    for (int64_t base = e0; base < e1; base += 32) {
+        const int64_t e = base + lane;
+        const int32_t j_l = e < e1 ? a.col[e] : 0;
+        const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
+        float p[32];        // all 32 key rows requested before the first is used
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            const int32_t j = __shfl_sync(0xffffffffu, j_l, t);
+            const float2 kv = t < cnt ? Pair<T>::load(Ku + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
+            p[t] = fmaf(q.x, kv.x, q.y * kv.y);
+        }
+        const float s = warp_transpose_sum32(p, lane) * scale;     // edge base + lane
+        if (e < e1) {
+            Au[e] = s;
+            if (s > m) { l = l * expf(m - s) + 1.f; m = s; }
+            else       { l += expf(s - m); }
+        }
     }
     // merge the per-lane (max, sum) pairs
 #pragma unroll
@@ -117,19 +95,6 @@ score_csr_kernel(CsrArgs a, const void* __restrict__ Q, const void* __restrict__
     }
     for (int64_t e = e0 + lane; e < e1; e += 32) Au[e] = expf(Au[e] - m) / l;
 }
-
-template <typename T> struct Pair;
-template <> struct Pair<float> {
-    static __device__ __forceinline__ float2 load(const float* p) {
-        return *reinterpret_cast<const float2*>(p);
-    }
-};
-template <> struct Pair<__nv_bfloat16> {
-    static __device__ __forceinline__ float2 load(const __nv_bfloat16* p) {
-        uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-        return make_float2(bf16lo(w), bf16hi(w));
-    }
-};
 
 __device__ __forceinline__ void store_pair(float* p, float2 v) {
     *reinterpret_cast<float2*>(p) = v;
