@@ -392,21 +392,28 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // ---------------- TMA producer of the score operands: the Q tile and the K
         // chunks (keys of the chunk grid jb = i0 - r64 ..; outside 0..n-1 they load
         // as zeros), in the order the score MMAs use them.
-        if (lane == 0) {
+        // (the whole warp runs the loop; the elected lane issues the copies)
+        {
             const uint64_t pol_keep = ptx::l2_evict_last();      // re-read by neighbouring tiles
             int g = 0, b = 0, ph = 0;                             // running chunk, slot, phase
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const TileInfo ti = tile(lt);
                 const int qb = lt & 1;
                 if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, a.status);
-                ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
-                ptx::tma_load_3d_hint(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, (int)ti.i0, (int)ti.u, pol_keep);
+                __syncwarp();
+                if (ptx::elect_one()) {
+                    ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
+                    ptx::tma_load_3d_hint(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, (int)ti.i0, (int)ti.u, pol_keep);
+                }
                 for (int c = ti.c_lo; c <= ti.c_hi; ++c, ++g) {
                     // stage b is free once the scores of chunk g - kSBufs are written
                     if (g >= kSBufs) ptx::mbar_wait(&full_S[b], ph ^ 1, a.status);
-                    ptx::mbar_arrive_expect_tx(&full_K[b], kKBytes);
-                    ptx::tma_load_3d_hint(sK + b * kKBytes, &tmK, &full_K[b], 0,
-                                          (int)(ti.i0 - P.r64 + kCK * c), (int)ti.u, pol_keep);
+                    __syncwarp();
+                    if (ptx::elect_one()) {
+                        ptx::mbar_arrive_expect_tx(&full_K[b], kKBytes);
+                        ptx::tma_load_3d_hint(sK + b * kKBytes, &tmK, &full_K[b], 0,
+                                              (int)(ti.i0 - P.r64 + kCK * c), (int)ti.u, pol_keep);
+                    }
                     if (++b == kSBufs) { b = 0; ph ^= 1; }
                 }
             }
@@ -449,7 +456,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // ---------------- score MMAs: S[b] = Q_tile K_chunk^T (both K-major,
         // 128-byte swizzle), as far ahead of the weights as the TMEM buffers allow:
         // buffer b is free once the weights' MMAs of its previous chunk are done
-        if (lane == 0) {
+        // (the whole warp runs the loop; the elected lane issues each instruction)
+        {
             constexpr uint32_t idesc_s = ptx::mma_idesc(1, kCK);
             // descriptors advance by (byte offset >> 4) in their address field
             const uint64_t qdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sQ));
@@ -463,14 +471,15 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int c = ti.c_lo; c <= ti.c_hi; ++c, ++g) {
                     ptx::mbar_wait(&full_K[b], ph, a.status);
                     if (g >= kSBufs) ptx::mbar_wait(&pv_done[b], ph ^ 1, a.status);
+                    __syncwarp();
                     ptx::tc_fence_after();
                     const uint64_t kd = kdesc0 + (uint64_t)(b * (kKBytes >> 4));
                     const uint32_t dS = tmem + kSCol0 + kCK * b;
 #pragma unroll
                     for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                        ptx::mma_bf16_ss(dS, qd + 2 * ks, kd + 2 * ks, idesc_s, ks > 0);
-                    ptx::mma_commit(&full_S[b]);                  // also frees K stage b
-                    if (c == ti.c_hi) ptx::mma_commit(&empty_Q[qb]);
+                        if (ptx::elect_one()) ptx::mma_bf16_ss(dS, qd + 2 * ks, kd + 2 * ks, idesc_s, ks > 0);
+                    if (ptx::elect_one()) ptx::mma_commit(&full_S[b]);   // also frees K stage b
+                    if (c == ti.c_hi && ptx::elect_one()) ptx::mma_commit(&empty_Q[qb]);
                     if (++b == kSBufs) { b = 0; ph ^= 1; }
                 }
             }
@@ -488,7 +497,8 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else if (warp == kPvMmaWarp) {
         // ---------------- the weights' MMAs, chunk by chunk as the weight images are
         // written: D += P_hi [Z_hi | Z_lo] + P_lo Z_hi, the globals and global rows
-        if (lane == 0) {
+        // (the whole warp runs the loop; the elected lane issues each instruction)
+        {
             constexpr uint32_t idesc64 = ptx::mma_idesc_bf16_bmn(64);
             constexpr uint32_t idesc128 = ptx::mma_idesc_bf16_bmn(128);
             const uint32_t dacc = tmem;
@@ -501,34 +511,40 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 {
                     // the previous tile's accumulators have been read
                     if (lt >= 1) ptx::mbar_wait(acc_empty, (lt - 1) & 1, a.status);
+                    __syncwarp();
                     ptx::tc_fence_after();
                     if (has_g) {
                         // the globals outside each row's window: [128 x g16] x [g16 x (hi | lo)]
                         ptx::mbar_wait(full_GC, lt & 1, a.status);
+                        __syncwarp();
                         ptx::tc_fence_after();
                         const uint32_t gch = ptx::smem_u32(sGC), gcl = gch + gc_plane;
                         const uint32_t zg = ptx::smem_u32(sZG);
                         for (int ks = 0; ks < g16 / 16; ++ks) {
                             const uint64_t bdesc = ptx::sw128_mnmajor_desc(zg + 2048 * ks, g16 * 128);
-                            ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gch + 256 * ks, 128, 16 * g16),
-                                             bdesc, kHop0 ? idesc64 : idesc128, ks != 0);
-                            ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gcl + 256 * ks, 128, 16 * g16),
-                                             bdesc, idesc64, 1);
+                            if (ptx::elect_one())
+                                ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gch + 256 * ks, 128, 16 * g16),
+                                                 bdesc, kHop0 ? idesc64 : idesc128, ks != 0);
+                            if (ptx::elect_one())
+                                ptx::mma_bf16_ss(dacc, ptx::noswz_kmajor_desc(gcl + 256 * ks, 128, 16 * g16),
+                                                 bdesc, idesc64, 1);
                         }
-                        ptx::mma_commit(empty_GC);
+                        if (ptx::elect_one()) ptx::mma_commit(empty_GC);
                     }
                 }
               for (int c = ti.c_lo; c <= ti.c_hi; ++c) {
                 ptx::mbar_wait(&full_P[sp], pph, a.status);          // weights and Z stage
+                __syncwarp();
                 ptx::tc_fence_after();
                 const uint32_t pbuf = tmem + kSCol0 + kCK * sp;   // K step ks: hi 16 ks, lo 16 ks + 8
                 const uint64_t zd = zdesc0 + (uint64_t)(sp * (kZStageBytes >> 4));
 #pragma unroll
                 for (int ks = 0; ks < kCK / 16; ++ks) {
                     const uint64_t bdesc = zd + (uint64_t)(128 * ks);     // 16 keys = 2048 bytes on
-                    ptx::mma_bf16_ts(dacc, pbuf + 16 * ks, bdesc, kHop0 ? idesc64 : idesc128,
-                                     has_g || c != ti.c_lo || ks != 0);
-                    ptx::mma_bf16_ts(dacc, pbuf + 16 * ks + 8, bdesc, idesc64, 1);
+                    if (ptx::elect_one())
+                        ptx::mma_bf16_ts(dacc, pbuf + 16 * ks, bdesc, kHop0 ? idesc64 : idesc128,
+                                         has_g || c != ti.c_lo || ks != 0);
+                    if (ptx::elect_one()) ptx::mma_bf16_ts(dacc, pbuf + 16 * ks + 8, bdesc, idesc64, 1);
                 }
                 // the chunk(s) holding the tile's own keys: c0, and c0 + 1 when r64 is an
                 // odd multiple of 64 and that chunk is in range (a ragged last tile may end
@@ -549,19 +565,20 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                             // accumulator has been read
                             ptx::mbar_wait(full_G, lt & 1, a.status);
                             if (lt >= 1) ptx::mbar_wait(glob_empty, (lt - 1) & 1, a.status);
+                            __syncwarp();
                             ptx::tc_fence_after();
                         }
                         const int h = rel >> 6, kk = (rel & 63) >> 4;
                         const uint64_t ghi = gdesc0 + (uint64_t)(h * ((2 * band::kGImgPlaneBytes) >> 4) + 2 * kk);
                         const uint64_t glo = ghi + (uint64_t)(band::kGImgPlaneBytes >> 4);
                         const uint64_t bdesc = zd + (uint64_t)(128 * ks);
-                        ptx::mma_bf16_ss(dglob, ghi, bdesc, kHop0 ? idesc64 : idesc128, rel != 0);
-                        ptx::mma_bf16_ss(dglob, glo, bdesc, idesc64, 1);
+                        if (ptx::elect_one()) ptx::mma_bf16_ss(dglob, ghi, bdesc, kHop0 ? idesc64 : idesc128, rel != 0);
+                        if (ptx::elect_one()) ptx::mma_bf16_ss(dglob, glo, bdesc, idesc64, 1);
                     }
-                    if (c == glob_last) ptx::mma_commit(empty_G);
+                    if (c == glob_last && ptx::elect_one()) ptx::mma_commit(empty_G);
                 }
-                ptx::mma_commit(&pv_done[sp]);
-                if (c == ti.c_hi) ptx::mma_commit(acc_full);
+                if (ptx::elect_one()) ptx::mma_commit(&pv_done[sp]);
+                if (c == ti.c_hi && ptx::elect_one()) ptx::mma_commit(acc_full);
                 if (++sp == kSBufs) { sp = 0; pph ^= 1; }
               }
             }
@@ -610,8 +627,15 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                 for (int k = 0; k < 16; ++k) e[k] = 0.f;
             } else if (full_in) {
+                // the scaling as packed pairs (one fma each, the same roundings as fmaf)
+                const float2 sc = make_float2(a_sc, a_sc), nb = make_float2(-row.b2, -row.b2);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) e[k] = ptx::ex2_approx(fmaf(__uint_as_float(r[k]), a_sc, -row.b2));
+                for (int p2 = 0; p2 < 8; ++p2) {
+                    const float2 y = __ffma2_rn(make_float2(__uint_as_float(r[2 * p2]), __uint_as_float(r[2 * p2 + 1])),
+                                                sc, nb);
+                    e[2 * p2] = ptx::ex2_approx(y.x);
+                    e[2 * p2 + 1] = ptx::ex2_approx(y.y);
+                }
             } else {
                 const int dlo = (int)(row.lo - j0), dhi = (int)(row.hi - j0);   // in-window keys k in [dlo, dhi]
 #pragma unroll

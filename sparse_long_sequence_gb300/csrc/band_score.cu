@@ -358,27 +358,33 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            for (int lt = 0; lt < my_tiles; ++lt) {
-                const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
-                const int64_t u = tix / P.tiles;
-                const int64_t i0 = (tix - u * P.tiles) * kTileRows;
-                const int64_t jb = i0 - P.r64;
-                const int qb = lt & 1;
-                if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, status);
+        // (the whole warp runs the loop; the elected lane issues the copies)
+        for (int lt = 0; lt < my_tiles; ++lt) {
+            const int64_t tix = blockIdx.x + (int64_t)lt * gridDim.x;
+            const int64_t u = tix / P.tiles;
+            const int64_t i0 = (tix - u * P.tiles) * kTileRows;
+            const int64_t jb = i0 - P.r64;
+            const int qb = lt & 1;
+            if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, status);
+            __syncwarp();
+            if (ptx::elect_one()) {
                 ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
                 ptx::tma_load_3d(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, (int)i0, (int)u);
-                for (int it = 0; it < per_tile; ++it) {
-                    const int gi = lt * per_tile + it;
-                    const int c = it % nc, s = gi % kKStages;
-                    if (gi >= kKStages) ptx::mbar_wait(&empty_K[s], ((gi / kKStages) - 1) & 1, status);
+            }
+            for (int it = 0; it < per_tile; ++it) {
+                const int gi = lt * per_tile + it;
+                const int c = it % nc, s = gi % kKStages;
+                if (gi >= kKStages) ptx::mbar_wait(&empty_K[s], ((gi / kKStages) - 1) & 1, status);
+                __syncwarp();
+                if (ptx::elect_one()) {
                     ptx::mbar_arrive_expect_tx(&full_K[s], kKBytes);
                     ptx::tma_load_3d(sK + s * kKBytes, &tmK, &full_K[s], 0, (int)(jb + kSChunk * c), (int)u);
                 }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        // (the whole warp runs the loop; the elected lane issues each instruction)
+        {
             constexpr uint32_t idesc = ptx::mma_idesc(1, kSChunk);
             const uint32_t idesc_gc = ptx::mma_idesc(1, P.g16 > 0 ? P.g16 : 16);
             for (int lt = 0; lt < my_tiles; ++lt) {
@@ -389,43 +395,51 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (has_g) {
                     // q_i . k_G for the tile's rows (N = g16) into columns kGcCol0 + 32 (lt & 1)
                     ptx::mbar_wait(&full_G[qb], (lt / 2) & 1, status);
+                    __syncwarp();
                     ptx::tc_fence_after();
                     const uint32_t kg = ptx::smem_u32(sKG + qb * kGBufBytes);
 #pragma unroll
                     for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                        ptx::mma_bf16_ss(tmem + kGcCol0 + 32 * qb, ptx::sw128_kmajor_desc(qa + 32 * ks),
-                                         ptx::sw128_kmajor_desc(kg + 32 * ks), idesc_gc, ks > 0);
+                        if (ptx::elect_one())
+                            ptx::mma_bf16_ss(tmem + kGcCol0 + 32 * qb, ptx::sw128_kmajor_desc(qa + 32 * ks),
+                                             ptx::sw128_kmajor_desc(kg + 32 * ks), idesc_gc, ks > 0);
                 }
                 for (int it = 0; it < per_tile; ++it) {
                     const int gi = lt * per_tile + it;
                     const int s = gi % kKStages, b = gi % kSBufs;
                     ptx::mbar_wait(&full_K[s], (gi / kKStages) & 1, status);
                     if (gi >= kSBufs) ptx::mbar_wait(&empty_S[b], ((gi / kSBufs) - 1) & 1, status);
+                    __syncwarp();
                     ptx::tc_fence_after();
                     const uint32_t kb = ptx::smem_u32(sK + s * kKBytes);
 #pragma unroll
                     for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                        ptx::mma_bf16_ss(tmem + kSChunk * b, ptx::sw128_kmajor_desc(qa + 32 * ks),
-                                         ptx::sw128_kmajor_desc(kb + 32 * ks), idesc, ks > 0);
+                        if (ptx::elect_one())
+                            ptx::mma_bf16_ss(tmem + kSChunk * b, ptx::sw128_kmajor_desc(qa + 32 * ks),
+                                             ptx::sw128_kmajor_desc(kb + 32 * ks), idesc, ks > 0);
                     const int h = it - c0;
                     if (has_g && (h == 0 || h == 1)) {
                         // q_G . k_j for the tile's own keys (the global rows' scores):
                         // rows 0..g-1 of an M = 128 operand whose other rows are not used
                         if (h == 0 && lt >= 1) ptx::mbar_wait(empty_GR, (lt - 1) & 1, status);
+                        __syncwarp();
                         ptx::tc_fence_after();
 #pragma unroll
                         for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                            ptx::mma_bf16_ss(tmem + kGrCol0 + kSChunk * h, ptx::sw128_kmajor_desc(qg + 32 * ks),
-                                             ptx::sw128_kmajor_desc(kb + 32 * ks), idesc, ks > 0);
-                        if (h == 1) {
+                            if (ptx::elect_one())
+                                ptx::mma_bf16_ss(tmem + kGrCol0 + kSChunk * h, ptx::sw128_kmajor_desc(qg + 32 * ks),
+                                                 ptx::sw128_kmajor_desc(kb + 32 * ks), idesc, ks > 0);
+                        if (h == 1 && ptx::elect_one()) {
                             ptx::mma_commit(full_GR);
                             ptx::mma_commit(&empty_G[qb]);
                         }
                     }
-                    ptx::mma_commit(&empty_K[s]);
-                    ptx::mma_commit(&full_S[b]);
+                    if (ptx::elect_one()) {
+                        ptx::mma_commit(&empty_K[s]);
+                        ptx::mma_commit(&full_S[b]);
+                    }
                 }
-                ptx::mma_commit(&empty_Q[qb]);
+                if (ptx::elect_one()) ptx::mma_commit(&empty_Q[qb]);
             }
             // drain the asynchronous commit arrivals before the CTA can exit
             const int total = my_tiles * per_tile;

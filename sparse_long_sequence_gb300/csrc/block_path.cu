@@ -185,29 +185,37 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 
     if (warp == kTmaWarp) {
         // ---------------- Q tiles and K chunks (two 64-key boxes each), in MMA order
-        if (lane == 0) {
+        // (the whole warp runs the loop; the elected lane issues the copies)
+        {
             const uint64_t pol_keep = ptx::l2_evict_last();
             int g = 0, b = 0, ph = 0;
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const TileEntry te = sTile[lt];
                 const int qb = lt & 1;
                 if (lt >= 2) ptx::mbar_wait(&empty_Q[qb], ((lt / 2) - 1) & 1, a.status);
-                ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
-                ptx::tma_load_3d_hint(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, te.t * kTile, te.u, pol_keep);
+                __syncwarp();
+                if (ptx::elect_one()) {
+                    ptx::mbar_arrive_expect_tx(&full_Q[qb], kQBytes);
+                    ptx::tma_load_3d_hint(sQ + qb * kQBytes, &tmQ, &full_Q[qb], 0, te.t * kTile, te.u, pol_keep);
+                }
                 for (int c = te.c0; c < te.c1; ++c, ++g) {
                     const int4 ch = chunk(c);
                     if (g >= kSlots) ptx::mbar_wait(&full_S[b], ph ^ 1, a.status);
-                    ptx::mbar_arrive_expect_tx(&full_K[b], kKBytes);
-                    ptx::tma_load_3d_hint(sK + b * kKBytes, &tmK, &full_K[b], 0, ch.x * kBlock, te.u, pol_keep);
-                    ptx::tma_load_3d_hint(sK + b * kKBytes + kHalfBytes, &tmK, &full_K[b], 0, ch.y * kBlock,
-                                          te.u, pol_keep);
+                    __syncwarp();
+                    if (ptx::elect_one()) {
+                        ptx::mbar_arrive_expect_tx(&full_K[b], kKBytes);
+                        ptx::tma_load_3d_hint(sK + b * kKBytes, &tmK, &full_K[b], 0, ch.x * kBlock, te.u, pol_keep);
+                        ptx::tma_load_3d_hint(sK + b * kKBytes + kHalfBytes, &tmK, &full_K[b], 0, ch.y * kBlock,
+                                              te.u, pol_keep);
+                    }
                     if (++b == kSlots) { b = 0; ph ^= 1; }
                 }
             }
         }
     } else if (warp == kZWarp) {
         // ---------------- Z_k chunks (hop): the two key blocks' hi rows, and lo rows after hop 0
-        if (kHop && lane == 0) {
+        // (the whole warp runs the loop; the elected lane issues the copies)
+        if (kHop) {
             const uint64_t pol_keep = ptx::l2_evict_last();
             int g = 0;
             for (int lt = 0; lt < my_tiles; ++lt) {
@@ -216,22 +224,26 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     const int4 ch = chunk(c);
                     const int b = g % kSlots;
                     if (g >= kSlots) ptx::mbar_wait(&slot_free[b], ((g / kSlots) - 1) & 1, a.status);
-                    uint8_t* zdst = sZ + b * kZStageBytes;
-                    ptx::mbar_arrive_expect_tx(&full_P[b], kHop0 ? 2 * kHalfBytes : 4 * kHalfBytes);
-                    ptx::tma_load_3d_hint(zdst, &tmZ, &full_P[b], 0, ch.x * kBlock, te.u, pol_keep);
-                    ptx::tma_load_3d_hint(zdst + kHalfBytes, &tmZ, &full_P[b], 0, ch.y * kBlock, te.u, pol_keep);
-                    if (!kHop0) {
-                        ptx::tma_load_3d_hint(zdst + kZTileBytes, &tmZ, &full_P[b], kHeadDim, ch.x * kBlock,
-                                              te.u, pol_keep);
-                        ptx::tma_load_3d_hint(zdst + kZTileBytes + kHalfBytes, &tmZ, &full_P[b], kHeadDim,
-                                              ch.y * kBlock, te.u, pol_keep);
+                    __syncwarp();
+                    if (ptx::elect_one()) {
+                        uint8_t* zdst = sZ + b * kZStageBytes;
+                        ptx::mbar_arrive_expect_tx(&full_P[b], kHop0 ? 2 * kHalfBytes : 4 * kHalfBytes);
+                        ptx::tma_load_3d_hint(zdst, &tmZ, &full_P[b], 0, ch.x * kBlock, te.u, pol_keep);
+                        ptx::tma_load_3d_hint(zdst + kHalfBytes, &tmZ, &full_P[b], 0, ch.y * kBlock, te.u, pol_keep);
+                        if (!kHop0) {
+                            ptx::tma_load_3d_hint(zdst + kZTileBytes, &tmZ, &full_P[b], kHeadDim, ch.x * kBlock,
+                                                  te.u, pol_keep);
+                            ptx::tma_load_3d_hint(zdst + kZTileBytes + kHalfBytes, &tmZ, &full_P[b], kHeadDim,
+                                                  ch.y * kBlock, te.u, pol_keep);
+                        }
                     }
                 }
             }
         }
     } else if (warp == kSMmaWarp) {
         // ---------------- score MMAs S[b] = Q_tile K_chunk^T (K-major, 128-byte swizzle)
-        if (lane == 0) {
+        // (the whole warp runs the loop; the elected lane issues each instruction)
+        {
             constexpr uint32_t idesc_s = ptx::mma_idesc(1, kCK);
             const uint64_t qdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sQ));
             const uint64_t kdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sK));
@@ -244,14 +256,15 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 for (int c = te.c0; c < te.c1; ++c, ++g) {
                     ptx::mbar_wait(&full_K[b], ph, a.status);
                     if (g >= kSlots) ptx::mbar_wait(&slot_free[b], ph ^ 1, a.status);
+                    __syncwarp();
                     ptx::tc_fence_after();
                     const uint64_t kd = kdesc0 + (uint64_t)(b * (kKBytes >> 4));
                     const uint32_t dS = tmem + kSCol0 + kCK * b;
 #pragma unroll
                     for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                        ptx::mma_bf16_ss(dS, qd + 2 * ks, kd + 2 * ks, idesc_s, ks > 0);
-                    ptx::mma_commit(&full_S[b]);
-                    if (c == te.c1 - 1) ptx::mma_commit(&empty_Q[qb]);
+                        if (ptx::elect_one()) ptx::mma_bf16_ss(dS, qd + 2 * ks, kd + 2 * ks, idesc_s, ks > 0);
+                    if (ptx::elect_one()) ptx::mma_commit(&full_S[b]);
+                    if (c == te.c1 - 1 && ptx::elect_one()) ptx::mma_commit(&empty_Q[qb]);
                     if (++b == kSlots) { b = 0; ph ^= 1; }
                 }
             }
@@ -267,7 +280,8 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         }
     } else if (warp == kPvMmaWarp) {
         // ---------------- weights' MMAs (hop): D += e_hi [Z_hi | Z_lo] + e_lo Z_hi
-        if (kHop && lane == 0) {
+        // (the whole warp runs the loop; the elected lane issues each instruction)
+        if (kHop) {
             constexpr uint32_t idesc64 = ptx::mma_idesc_bf16_bmn(64);
             constexpr uint32_t idesc128 = ptx::mma_idesc_bf16_bmn(128);
             const uint64_t zdesc0 = ptx::sw128_mnmajor_desc(ptx::smem_u32(sZ), kZTileBytes);
@@ -275,21 +289,24 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const TileEntry te = sTile[lt];
                 if (lt >= 1) ptx::mbar_wait(acc_empty, (lt - 1) & 1, a.status);
+                __syncwarp();
                 ptx::tc_fence_after();
                 for (int c = te.c0; c < te.c1; ++c) {
                     ptx::mbar_wait(&full_P[sp], pph, a.status);
+                    __syncwarp();
                     ptx::tc_fence_after();
                     const uint32_t pbuf = tmem + kSCol0 + kCK * sp;   // K step ks: hi 16 ks, lo 16 ks + 8
                     const uint64_t zd = zdesc0 + (uint64_t)(sp * (kZStageBytes >> 4));
 #pragma unroll
                     for (int ks = 0; ks < kCK / 16; ++ks) {
                         const uint64_t bdesc = zd + (uint64_t)(128 * ks);   // 16 keys = 2048 bytes on
-                        ptx::mma_bf16_ts(tmem, pbuf + 16 * ks, bdesc, kHop0 ? idesc64 : idesc128,
-                                         c != te.c0 || ks != 0);
-                        ptx::mma_bf16_ts(tmem, pbuf + 16 * ks + 8, bdesc, idesc64, 1);
+                        if (ptx::elect_one())
+                            ptx::mma_bf16_ts(tmem, pbuf + 16 * ks, bdesc, kHop0 ? idesc64 : idesc128,
+                                             c != te.c0 || ks != 0);
+                        if (ptx::elect_one()) ptx::mma_bf16_ts(tmem, pbuf + 16 * ks + 8, bdesc, idesc64, 1);
                     }
-                    ptx::mma_commit(&slot_free[sp]);
-                    if (c == te.c1 - 1) ptx::mma_commit(acc_full);
+                    if (ptx::elect_one()) ptx::mma_commit(&slot_free[sp]);
+                    if (c == te.c1 - 1 && ptx::elect_one()) ptx::mma_commit(acc_full);
                     if (++sp == kSlots) { sp = 0; pph ^= 1; }
                 }
             }
@@ -361,17 +378,37 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 if (c == te.c1 - 1) hand_over(m);
             } else {
                 uint32_t hw[8], lw[8];
+                auto split = [&](float x0, float x1, int p2) {
+                    if (kHop0) lsum += x0 + x1;
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+                    hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
+                    lw[p2] = *reinterpret_cast<const uint32_t*>(&lo);
+                };
+                // lim is the same for the whole warp except in a ragged last tile: a key
+                // block is allowed for all 16 keys (no per-key select, the scaling as
+                // packed pairs) or for none (no exps), and only a block cut by the
+                // sequence end takes the general path
                 auto weights = [&](const uint32_t (&r)[16], int lim) {
+                    if (lim >= 16) {
+                        const float2 sc = make_float2(kLog2eScale, kLog2eScale), nb = make_float2(-b2, -b2);
 #pragma unroll
-                    for (int p2 = 0; p2 < 8; ++p2) {
-                        const int k0 = 2 * p2, k1 = 2 * p2 + 1;
-                        const float x0 = k0 < lim ? ptx::ex2_approx(fmaf(__uint_as_float(r[k0]), kLog2eScale, -b2)) : 0.f;
-                        const float x1 = k1 < lim ? ptx::ex2_approx(fmaf(__uint_as_float(r[k1]), kLog2eScale, -b2)) : 0.f;
-                        if (kHop0) lsum += x0 + x1;
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-                        const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
-                        hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
-                        lw[p2] = *reinterpret_cast<const uint32_t*>(&lo);
+                        for (int p2 = 0; p2 < 8; ++p2) {
+                            const float2 y = __ffma2_rn(make_float2(__uint_as_float(r[2 * p2]), __uint_as_float(r[2 * p2 + 1])),
+                                                        sc, nb);
+                            split(ptx::ex2_approx(y.x), ptx::ex2_approx(y.y), p2);
+                        }
+                    } else if (lim <= 0) {
+#pragma unroll
+                        for (int p2 = 0; p2 < 8; ++p2) { hw[p2] = 0u; lw[p2] = 0u; }
+                    } else {
+#pragma unroll
+                        for (int p2 = 0; p2 < 8; ++p2) {
+                            const int k0 = 2 * p2, k1 = 2 * p2 + 1;
+                            const float x0 = k0 < lim ? ptx::ex2_approx(fmaf(__uint_as_float(r[k0]), kLog2eScale, -b2)) : 0.f;
+                            const float x1 = k1 < lim ? ptx::ex2_approx(fmaf(__uint_as_float(r[k1]), kLog2eScale, -b2)) : 0.f;
+                            split(x0, x1, p2);
+                        }
                     }
                 };
                 weights(ra, lim0);

@@ -42,7 +42,8 @@ constexpr int kStages = 4;
 constexpr int kABytes = kTM * kTK * 2;             // 16 KB
 constexpr int kBBytes = kTN * kTK * 2;             // 32 KB
 constexpr int kGemmThreads = 192;
-constexpr int kEpiWarp0 = 2;
+constexpr int kEpiWarp0 = 2;                       // warps 0 TMA, 1 MMA, 2..5 epilogue
+static_assert(kGemmThreads == 32 * (kEpiWarp0 + 4), "four epilogue warps, one per lane quadrant");
 constexpr int kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256;   // + barriers
 static_assert(kGemmSmem <= 227 * 1024, "shared memory per CTA");
 
@@ -110,14 +111,16 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol_a = ptx::l2_evict_first(), pol_b = ptx::l2_evict_last();
-            int g = 0;                                       // running K step over this CTA's tiles
-            for (int lt = 0; lt < my_tiles; ++lt) {
-                const GemmTile tl = tile(lt);
-                for (int kb = 0; kb < a.k_blocks; ++kb, ++g) {
-                    const int s = g % kStages;
-                    if (g >= kStages) ptx::mbar_wait(&empty[s], ((g / kStages) - 1) & 1, a.status);
+        // (the whole warp runs the loop; the elected lane issues the copies)
+        const uint64_t pol_a = ptx::l2_evict_first(), pol_b = ptx::l2_evict_last();
+        int g = 0;                                           // running K step over this CTA's tiles
+        for (int lt = 0; lt < my_tiles; ++lt) {
+            const GemmTile tl = tile(lt);
+            for (int kb = 0; kb < a.k_blocks; ++kb, ++g) {
+                const int s = g % kStages;
+                if (g >= kStages) ptx::mbar_wait(&empty[s], ((g / kStages) - 1) & 1, a.status);
+                __syncwarp();
+                if (ptx::elect_one()) {
                     ptx::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
                     if constexpr (kMode == kQkv)
                         ptx::tma_load_3d_hint(sA + s * kABytes, &tmA, &full[s], kb * kTK, tl.i0, tl.b, pol_a);
@@ -128,7 +131,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        // (the whole warp runs the loop; the elected lane issues each instruction)
+        {
             constexpr uint32_t idesc = ptx::mma_idesc(1, kTN);
             const uint64_t adesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sA));
             const uint64_t bdesc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(sB));
@@ -137,20 +141,22 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int buf = lt & 1;
                 // the epilogue has read this accumulator's previous tile
                 if (lt >= 2) ptx::mbar_wait(&acc_empty[buf], ((lt / 2) - 1) & 1, a.status);
+                __syncwarp();
                 ptx::tc_fence_after();
                 const uint32_t dacc = tmem + buf * kTN;
                 for (int kb = 0; kb < a.k_blocks; ++kb, ++g) {
                     const int s = g % kStages;
                     ptx::mbar_wait(&full[s], (g / kStages) & 1, a.status);
+                    __syncwarp();
                     ptx::tc_fence_after();
                     const uint64_t ad = adesc0 + (uint64_t)(s * (kABytes >> 4));
                     const uint64_t bd = bdesc0 + (uint64_t)(s * (kBBytes >> 4));
 #pragma unroll
                     for (int ks = 0; ks < kTK / 16; ++ks)
-                        ptx::mma_bf16_ss(dacc, ad + 2 * ks, bd + 2 * ks, idesc, kb > 0 || ks > 0);
-                    ptx::mma_commit(&empty[s]);
+                        if (ptx::elect_one()) ptx::mma_bf16_ss(dacc, ad + 2 * ks, bd + 2 * ks, idesc, kb > 0 || ks > 0);
+                    if (ptx::elect_one()) ptx::mma_commit(&empty[s]);
                 }
-                ptx::mma_commit(&acc_full[buf]);
+                if (ptx::elect_one()) ptx::mma_commit(&acc_full[buf]);
             }
             // drain: the last commits land before the CTA exits
             for (int s = 0; s < kStages; ++s) {

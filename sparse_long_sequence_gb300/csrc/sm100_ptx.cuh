@@ -290,6 +290,22 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// True in exactly one lane (the lowest) of the fully converged calling warp.
+// The MMA-issuing warps run their loops with all 32 lanes and let the elected
+// lane issue each tcgen05 instruction: a loop run by one lane alone gets far
+// fewer scheduler turns beside busy softmax warps on the same SM sub-partition
+// (measured: 16 weight MMAs under three ALU-bound warps per sub-partition took
+// about 5200 cycles from a lone lane, about 1600 from a converged warp).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n.reg .pred P;\nelect.sync _|P, 0xffffffff;\nselp.u32 %0, 1, 0, P;\n}"
+        : "=r"(pred)
+        :
+        : "memory");
+    return pred != 0;
+}
+
 // D[tmem] (+)= A[tmem] * B[smem], kind::f16 (bf16 operands).  A is K-major in
 // tensor memory: row m in lane m, two consecutive K elements per 32-bit column
 // (the lower K index in the low half).
