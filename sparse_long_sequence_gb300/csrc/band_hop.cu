@@ -600,8 +600,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int t = quad * 32 + lane;
         const float a_sc = kLog2e * kScale;
-        // this row of tile lt: validity, window lo..hi, and b2 = m_i log2(e)
-        struct Row { int64_t jb, lo, hi; size_t urow; bool ok; float b2; int c_lo, c_hi; };
+        // this row of tile lt: its window lo..hi as offsets from the tile's key grid
+        // origin i0 - r64 (an empty window, hi < 0 <= lo, for a global row or a row
+        // past the end), b2 = m_i log2(e), and the tile's chunk range: few registers,
+        // as the weight code needs most of them
+        struct Row { int lo, hi; float b2; int c_lo, c_hi; };
         auto row_of = [&](int lt) {
             Row w;
             const TileInfo ti = tile(lt);
@@ -609,50 +612,54 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             w.c_lo = ti.c_lo;
             w.c_hi = ti.c_hi;
             const int64_t i = i0 + t;
-            w.jb = i0 - P.r64;
-            w.ok = i < P.n && !a.is_global[i < P.n ? i : 0];
-            band::window_of(P, i, w.lo, w.hi);
-            w.urow = (size_t)u * P.n + (w.ok ? i : 0);
-            w.b2 = w.ok ? __ldg(a.m_sparse + w.urow) * kLog2e : 0.f;
+            const bool ok = i < P.n && !a.is_global[i < P.n ? i : 0];
+            int64_t lo, hi;
+            band::window_of(P, i, lo, hi);
+            const int64_t jb = i0 - P.r64;
+            w.lo = ok ? (int)(lo - jb) : 1 << 30;
+            w.hi = ok ? (int)(hi - jb) : -1;
+            w.b2 = ok ? __ldg(a.m_sparse + (size_t)u * P.n + i) * kLog2e : 0.f;
             return w;
         };
-        // e = exp(s - m_i) for this row's 16 keys j0 .. j0 + 15 inside its window
-        // (keys lo..hi), else 0, as hi and lo bf16 pairs (two keys per TMEM column)
-        auto weights16 = [&](const uint32_t (&r)[16], const Row& row, int64_t j0, float& lsum,
+        // e = exp(s - m_i) for this row's 16 keys j0 .. j0 + 15 (offsets from the key
+        // grid origin) inside its window, else 0, as hi and lo bf16 pairs (two keys
+        // per TMEM column)
+        auto weights16 = [&](const uint32_t (&r)[16], const Row& row, int j0, float& lsum,
                              uint32_t (&hw)[8], uint32_t (&lw)[8]) {
-            const bool full_in = row.ok && j0 >= row.lo && j0 + 15 <= row.hi;
-            const bool none_in = !row.ok || j0 > row.hi || j0 + 15 < row.lo;
-            float e[16];
+            const bool full_in = j0 >= row.lo && j0 + 15 <= row.hi;
+            const bool none_in = j0 > row.hi || j0 + 15 < row.lo;
             if (none_in) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) e[k] = 0.f;
-            } else if (full_in) {
-                // the scaling as packed pairs (one fma each, the same roundings as fmaf)
-                const float2 sc = make_float2(a_sc, a_sc), nb = make_float2(-row.b2, -row.b2);
-#pragma unroll
-                for (int p2 = 0; p2 < 8; ++p2) {
-                    const float2 y = __ffma2_rn(make_float2(__uint_as_float(r[2 * p2]), __uint_as_float(r[2 * p2 + 1])),
-                                                sc, nb);
-                    e[2 * p2] = ptx::ex2_approx(y.x);
-                    e[2 * p2 + 1] = ptx::ex2_approx(y.y);
-                }
-            } else {
-                const int dlo = (int)(row.lo - j0), dhi = (int)(row.hi - j0);   // in-window keys k in [dlo, dhi]
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    e[k] = (k >= dlo && k <= dhi) ? ptx::ex2_approx(fmaf(__uint_as_float(r[k]), a_sc, -row.b2)) : 0.f;
+                for (int p2 = 0; p2 < 8; ++p2) { hw[p2] = 0u; lw[p2] = 0u; }
+                return;
             }
-            if (kHop0) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) lsum += e[k];
-            }
-#pragma unroll
-            for (int p2 = 0; p2 < 8; ++p2) {
-                const float x0 = e[2 * p2], x1 = e[2 * p2 + 1];
+            // pair by pair (few live registers): the scaling as one packed fma (the same
+            // roundings as fmaf); at a window edge the keys outside it are set to 0
+            const float2 sc = make_float2(a_sc, a_sc), nb = make_float2(-row.b2, -row.b2);
+            auto pair = [&](int p2, float x0, float x1) {
+                if (kHop0) { lsum += x0; lsum += x1; }
                 const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
                 const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
                 hw[p2] = *reinterpret_cast<const uint32_t*>(&h);
                 lw[p2] = *reinterpret_cast<const uint32_t*>(&l);
+            };
+            if (full_in) {
+#pragma unroll
+                for (int p2 = 0; p2 < 8; ++p2) {
+                    const float2 y = __ffma2_rn(make_float2(__uint_as_float(r[2 * p2]), __uint_as_float(r[2 * p2 + 1])),
+                                                sc, nb);
+                    pair(p2, ptx::ex2_approx(y.x), ptx::ex2_approx(y.y));
+                }
+            } else {
+                const int dlo = row.lo - j0, dhi = row.hi - j0;       // in-window keys k in [dlo, dhi]
+#pragma unroll
+                for (int p2 = 0; p2 < 8; ++p2) {
+                    const float2 y = __ffma2_rn(make_float2(__uint_as_float(r[2 * p2]), __uint_as_float(r[2 * p2 + 1])),
+                                                sc, nb);
+                    const float x0 = (2 * p2 >= dlo && 2 * p2 <= dhi) ? ptx::ex2_approx(y.x) : 0.f;
+                    const float x1 = (2 * p2 + 1 >= dlo && 2 * p2 + 1 <= dhi) ? ptx::ex2_approx(y.y) : 0.f;
+                    pair(p2, x0, x1);
+                }
             }
         };
         Row row = my_tiles > 0 ? row_of(0) : Row{};
@@ -672,7 +679,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::tmem_ld16_issue(col + kChunkKeys, rb);
             ptx::tmem_ld_wait16(ra);
             ptx::tmem_ld_wait16(rb);
-            const int64_t j0 = row.jb + kCK * c + 16 * slice;
+            const int j0 = kCK * c + 16 * slice;
             {
                 uint32_t hw[8], lw[8];
                 weights16(ra, row, j0, lsum, hw, lw);
