@@ -702,6 +702,7 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_blk_chunks);
     cudaFree(g->d_blk_tile_ptr);
     cudaFree(g->d_blk_order);
+    dfs::destroy_block_deals(g->blk_deals);
     cudaFree(g->d_status);
     if (g->h_status) cudaFreeHost(g->h_status);
     dfs::destroy_replay_cache(g->replay);

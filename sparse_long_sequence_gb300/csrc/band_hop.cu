@@ -316,8 +316,9 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint64_t* empty_Q = full_Q + 2;                              // [2]
     uint64_t* full_K = empty_Q + 2;                              // [kSBufs]
     uint64_t* full_S = full_K + kSBufs;                          // [kSBufs]
-    uint64_t* full_P = full_S + kSBufs;                          // [kSBufs]
-    uint64_t* pv_done = full_P + kSBufs;                         // [kSBufs]
+    uint64_t* full_P = full_S + kSBufs;                          // [kSBufs] keys 0-63 weighted + Z landed
+    uint64_t* full_P1 = full_P + kSBufs;                         // [kSBufs] keys 64-127 weighted
+    uint64_t* pv_done = full_P1 + kSBufs;                        // [kSBufs]
     uint64_t* acc_full = pv_done + kSBufs;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* glob_empty = acc_empty + 1;  // the global rows' accumulator has been read
@@ -352,6 +353,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::mbar_init(&full_K[s], 1);
             ptx::mbar_init(&full_S[s], 1);
             ptx::mbar_init(&full_P[s], kSoftWarps + 1);          // + the Z producer's arrival (with its bytes)
+            ptx::mbar_init(&full_P1[s], kSoftWarps);
             ptx::mbar_init(&pv_done[s], 1);
         }
         ptx::mbar_init(acc_full, 1);
@@ -533,13 +535,18 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                 }
               for (int c = ti.c_lo; c <= ti.c_hi; ++c) {
-                ptx::mbar_wait(&full_P[sp], pph, a.status);          // weights and Z stage
+                ptx::mbar_wait(&full_P[sp], pph, a.status);          // keys 0-63 weighted, Z stage landed
                 __syncwarp();
                 ptx::tc_fence_after();
                 const uint32_t pbuf = tmem + kSCol0 + kCK * sp;   // K step ks: hi 16 ks, lo 16 ks + 8
                 const uint64_t zd = zdesc0 + (uint64_t)(sp * (kZStageBytes >> 4));
 #pragma unroll
                 for (int ks = 0; ks < kCK / 16; ++ks) {
+                    if (ks == kCK / 32) {
+                        ptx::mbar_wait(&full_P1[sp], pph, a.status);    // keys 64-127 weighted
+                        __syncwarp();
+                        ptx::tc_fence_after();
+                    }
                     const uint64_t bdesc = zd + (uint64_t)(128 * ks);     // 16 keys = 2048 bytes on
                     if (ptx::elect_one())
                         ptx::mma_bf16_ts(dacc, pbuf + 16 * ks, bdesc, kHop0 ? idesc64 : idesc128,
@@ -686,6 +693,11 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 __syncwarp();   // reconverge before the warp-collective tcgen05.st
                 ptx::tmem_st16_hilo(col, hw, lw);                 // hi in columns +0..7, lo in +8..15
             }
+            // the first 64 keys' weights are in: their MMAs may start while the
+            // second half is computed
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&full_P[sb]);
             {
                 uint32_t hw[8], lw[8];
                 weights16(rb, row, j0 + kChunkKeys, lsum, hw, lw);
@@ -694,7 +706,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&full_P[sb]);
+            if (lane == 0) ptx::mbar_arrive(&full_P1[sb]);
             if (kHop0 && c == row.c_hi) {
                 // the row's band sum (this slice) for the epilogue warp of the quadrant;
                 // the buffer of this parity is free once that warp has read tile lt - 2's

@@ -47,7 +47,10 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <utility>
 #include <vector>
 
 #include "band_common.cuh"
@@ -70,8 +73,8 @@ constexpr int kKBytes = kCK * kHeadDim * 2;         // 16 KB (two 64-row boxes)
 constexpr int kHalfBytes = kBlock * kHeadDim * 2;   // 8 KB: one key block of K or of a Z half
 constexpr int kZTileBytes = kCK * 128;              // one 64-feature half (hi or lo) of a chunk
 constexpr int kZStageBytes = 2 * kZTileBytes;
-constexpr int kSlots = 2;                  // pipeline slots (chunk g uses slot g % 2)
-constexpr int kSCol0 = 256;                // score / weight buffers: columns 256 + 128 b
+constexpr int kSlots = 3;                  // pipeline slots (chunk g uses slot g % 3)
+constexpr int kSCol0 = 128;                // score / weight buffers: columns 128 + 128 b
 constexpr int kTmemCols = 512;             // D in [0, 128)
 constexpr int kMaxCtaTiles = 256;
 constexpr float kLog2eScale = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
@@ -89,6 +92,8 @@ struct BlockArgs {
     const int32_t* chunks;         // [total][4]: kb0, kb1, mask bits, 0
     const int32_t* tile_ptr;       // [tiles + 1] chunk range of each position
     const int32_t* order;          // [tiles] positions by falling chunk count
+    const int32_t* deal_ptr;       // [CTAs + 1] each CTA's range of deal_items (null: snake order)
+    const int32_t* deal_items;     // launch items k (position rank k / units, unit k % units)
     float* mb2;                    // [units][n] row max of s log2(e) / 8 over the allowed keys
     float* inv_l;                  // [units][n] 1 / sum of 2^(s log2(e) / 8 - mb2) (first hop)
     const __nv_bfloat16* V;        // [units][n][64]
@@ -100,15 +105,16 @@ struct BlockArgs {
 
 __host__ __device__ constexpr int block_smem_bytes() {
     return 1024 + 2 * kQBytes + kSlots * (kKBytes + kZStageBytes) + 4 * 32 * kEpiRowFloats * 4 +
-           4 * 32 * 4 + 4 * 32 * kHeadDim * 2 + 2 * kSlices * kTile * 4 +
-           kMaxCtaTiles * (int)sizeof(TileEntry) + 256;
+           4 * 32 * 4 + 2 * kSlices * kTile * 4 +
+           kMaxCtaTiles * (int)sizeof(TileEntry) + 512;
 }
 static_assert(block_smem_bytes() <= 227 * 1024, "shared memory per CTA");
 static_assert(block_smem_bytes() > 116 * 1024, "must exclude a second CTA per SM");
 
-// Item k of the launch (position rank k / units, unit k % units), dealt to the
-// CTAs heaviest first in snake order over the rounds (round r: CTA b gets item
-// r G + b, or r G + G - 1 - b when r is odd), so light tiles fill the last rounds.
+// Item k of the launch (position rank k / units, unit k % units).  With a deal
+// table (built on the host, see block_deal) each CTA takes its listed items;
+// without one the items go to the CTAs heaviest first in snake order over the
+// rounds (round r: CTA b gets item r G + b, or r G + G - 1 - b when r is odd).
 __device__ __forceinline__ int cta_tile_count(int64_t total) {
     const int64_t G = gridDim.x, b = blockIdx.x, R = total / G, rem = total - R * G;
     return (int)(R + ((R & 1) == 0 ? (b < rem ? 1 : 0) : (b >= G - rem ? 1 : 0)));
@@ -129,16 +135,16 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     uint8_t* sZ = sK + kSlots * kKBytes;                         // kSlots x (hi 16 KB, lo 16 KB)
     float* sEpi = reinterpret_cast<float*>(sZ + kSlots * kZStageBytes);   // [4][32][68]
     float* sKeep = sEpi + 4 * 32 * kEpiRowFloats;                // [4][32]
-    __nv_bfloat16* sEpiV = reinterpret_cast<__nv_bfloat16*>(sKeep + 4 * 32);   // [4][32][64] V rows
-    float* xch = reinterpret_cast<float*>(sEpiV + 4 * 32 * kHeadDim);   // [2][kSlices][128] row maxima / sums
+    float* xch = sKeep + 4 * 32;                                 // [2][kSlices][128] row maxima / sums
     TileEntry* sTile = reinterpret_cast<TileEntry*>(xch + 2 * kSlices * kTile);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sTile + kMaxCtaTiles);
     uint64_t* full_Q = bars;                  // [2]
     uint64_t* empty_Q = full_Q + 2;           // [2]
     uint64_t* full_K = empty_Q + 2;           // [kSlots]
     uint64_t* full_S = full_K + kSlots;       // [kSlots] scores written (also frees the K stage)
-    uint64_t* full_P = full_S + kSlots;       // [kSlots] hop: weights written + Z landed
-    uint64_t* slot_free = full_P + kSlots;    // [kSlots] hop: weights' MMAs done; score: S read
+    uint64_t* full_P = full_S + kSlots;       // [kSlots] hop: key block 0 weighted + Z landed
+    uint64_t* full_P1 = full_P + kSlots;      // [kSlots] hop: key block 1 weighted
+    uint64_t* slot_free = full_P1 + kSlots;   // [kSlots] hop: weights' MMAs done; score: S read
     uint64_t* acc_full = slot_free + kSlots;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* xch_full = acc_empty + 1;       // [4][2] a quadrant's slices wrote their row maxima
@@ -148,10 +154,12 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t total_items = a.units * a.tiles;
-    const int my_tiles = cta_tile_count(total_items);
+    const int my_tiles = a.deal_ptr ? a.deal_ptr[blockIdx.x + 1] - a.deal_ptr[blockIdx.x]
+                                    : cta_tile_count(total_items);
     for (int lt = tid; lt < my_tiles && lt < kMaxCtaTiles; lt += kThreads) {
         const int64_t G = gridDim.x, b = blockIdx.x;
-        const int64_t k = (int64_t)lt * G + ((lt & 1) ? G - 1 - b : b);
+        const int64_t k = a.deal_ptr ? (int64_t)a.deal_items[a.deal_ptr[b] + lt]
+                                     : (int64_t)lt * G + ((lt & 1) ? G - 1 - b : b);
         const int64_t rank = k / a.units, u = k - rank * a.units;
         const int t = a.order[rank];
         sTile[lt] = TileEntry{(int32_t)u, t, a.tile_ptr[t], a.tile_ptr[t + 1]};
@@ -163,6 +171,7 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             ptx::mbar_init(&full_K[s], 1);
             ptx::mbar_init(&full_S[s], 1);
             ptx::mbar_init(&full_P[s], kSoftWarps + 1);   // the weight warps + the Z copies' arrival
+            ptx::mbar_init(&full_P1[s], kSoftWarps);
             ptx::mbar_init(&slot_free[s], kHop ? 1 : kSoftWarps);
         }
         ptx::mbar_init(acc_full, 1);
@@ -299,6 +308,11 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     const uint64_t zd = zdesc0 + (uint64_t)(sp * (kZStageBytes >> 4));
 #pragma unroll
                     for (int ks = 0; ks < kCK / 16; ++ks) {
+                        if (ks == kCK / 32) {
+                            ptx::mbar_wait(&full_P1[sp], pph, a.status);    // key block 1 weighted
+                            __syncwarp();
+                            ptx::tc_fence_after();
+                        }
                         const uint64_t bdesc = zd + (uint64_t)(128 * ks);   // 16 keys = 2048 bytes on
                         if (ptx::elect_one())
                             ptx::mma_bf16_ts(tmem, pbuf + 16 * ks, bdesc, kHop0 ? idesc64 : idesc128,
@@ -414,12 +428,16 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 weights(ra, lim0);
                 __syncwarp();       // reconverge before the warp-collective tcgen05.st
                 ptx::tmem_st16_hilo(col, hw, lw);
+                // key block 0's weights are in: its MMAs may start while block 1's are computed
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&full_P[sb]);
                 weights(rb, lim1);
                 __syncwarp();
                 ptx::tmem_st16_hilo(col + kBlock, hw, lw);
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&full_P[sb]);
+                if (lane == 0) ptx::mbar_arrive(&full_P1[sb]);
                 if (kHop0 && c == te.c1 - 1) hand_over(lsum);
             }
             if (++sb == kSlots) { sb = 0; sph ^= 1; }
@@ -457,23 +475,18 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
             float* st = sEpi + quad * (32 * kEpiRowFloats);
             float* sk = sKeep + quad * 32;
-            __nv_bfloat16* sv = sEpiV + quad * 32 * kHeadDim;       // [32 rows][64] V
             const int hr = lane >> 4, f4 = lane & 15;
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const TileEntry te = sTile[lt];
                 const int64_t i0 = (int64_t)te.t * kTile;
                 {
-                    // this quadrant's V rows into shared memory, as asynchronous copies issued
-                    // before the accumulator is waited for (8 lanes per 128-byte row); the
-                    // previous tile's loop has finished reading them
-                    const size_t ub = (size_t)te.u * a.n;
-#pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int idx = it * 32 + lane, r = idx >> 3, c = idx & 7;
-                        const int64_t ir = i0 + quad * 32 + r;
-                        if (ir < a.n) ptx::cp_async16(sv + r * kHeadDim + 8 * c, a.V + (ub + ir) * kHeadDim + 8 * c);
-                    }
-                    ptx::cp_async_commit();
+                    // this quadrant's V rows (4 KB, contiguous) pulled into L2 now: the
+                    // write loop below reads them after the tile's MMAs
+                    const int64_t r0 = i0 + quad * 32;
+                    const int64_t nr = a.n - r0 < 32 ? a.n - r0 : 32;
+                    if (lane == 0 && nr > 0)
+                        ptx::bulk_prefetch_l2(a.V + ((size_t)te.u * a.n + r0) * kHeadDim,
+                                              (uint32_t)nr * kHeadDim * 2);
                 }
                 const int64_t i = i0 + t;
                 const bool row_ok = i < a.n;
@@ -488,8 +501,7 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     inv = row_ok ? __ldg(a.inv_l + urow) : 0.f;
                 }
                 ptx::mbar_wait(acc_full, lt & 1, a.status);
-                ptx::cp_async_wait_all();
-                __syncwarp();       // reconverge for tcgen05.ld; the V rows are in shared memory
+                __syncwarp();       // reconverge for tcgen05.ld
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < 4; h += (kHop0 ? 2 : 1)) {
@@ -525,7 +537,8 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                         const int r = 2 * (it0 + q) + hr;
                         keep[q] = sk[r];
                         rr[q] = ubase + (size_t)(i0 + quad * 32 + r);
-                        if (keep[q] >= 0.f) vv[q] = reinterpret_cast<const uint2*>(sv + r * kHeadDim)[f4];
+                        // V from global memory (L2): its latency is off the MMAs' path
+                        if (keep[q] >= 0.f) vv[q] = __ldg(reinterpret_cast<const uint2*>(a.V + rr[q] * kHeadDim) + f4);
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -588,6 +601,14 @@ int num_sms() {
     return sms;
 }
 
+// CTAs of a launch over `total` items: one per SM, more when the snake dealing
+// would give a CTA more items than its table holds
+int64_t block_ctas(int64_t total) {
+    int64_t ctas = total < num_sms() ? total : num_sms();
+    if ((total + ctas - 1) / ctas > kMaxCtaTiles) ctas = (total + kMaxCtaTiles - 1) / kMaxCtaTiles;
+    return ctas;
+}
+
 template <int kMode>
 int launch_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmZ,
                  const BlockArgs& a, cudaStream_t stream) {
@@ -598,9 +619,7 @@ int launch_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorM
                                         block_smem_bytes());
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(block kernel)");
-    const int64_t total = a.units * a.tiles;
-    int64_t ctas = total < num_sms() ? total : num_sms();
-    if ((total + ctas - 1) / ctas > kMaxCtaTiles) ctas = (total + kMaxCtaTiles - 1) / kMaxCtaTiles;
+    const int64_t ctas = block_ctas(a.units * a.tiles);
     {
         LaunchScope scope(kMode == kScore ? DIFFUSER_KERNEL_SCORE : DIFFUSER_KERNEL_HOP, stream);
         block_kernel<kMode><<<(unsigned)ctas, kThreads, block_smem_bytes(), stream>>>(tmQ, tmK, tmZ, a);
@@ -613,6 +632,28 @@ int launch_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorM
 
 bool block_eligible(const diffuser_graph* g) {
     return g->kind == kBlockGraph && g->block == kBlock && g->d_blk_chunks != nullptr;
+}
+
+// The deal tables of a graph, one per (units, CTAs); never evicted, as a captured
+// replay of a forward holds the pointers it was launched with.
+struct BlockDeals {
+    struct Entry {
+        int64_t units;
+        int64_t ctas;
+        int32_t* d_ptr;
+        int32_t* d_items;
+    };
+    std::mutex mu;
+    std::vector<Entry> entries;
+};
+
+void destroy_block_deals(BlockDeals* d) {
+    if (!d) return;
+    for (auto& e : d->entries) {
+        cudaFree(e.d_ptr);
+        cudaFree(e.d_items);
+    }
+    delete d;
 }
 
 // The tiles' key-block lists from the host CSR: block row J's allowed blocks are
@@ -674,11 +715,80 @@ int build_block_tiles(diffuser_graph* g) {
     }
     g->d_blk_tile_ptr = d_ptr;
     g->d_blk_order = d_order;
+    g->h_blk_tile_ptr = tile_ptr;
+    g->h_blk_order = order;
+    if (!g->blk_deals) g->blk_deals = new BlockDeals();
     g->blk_tiles = (int32_t)tiles;
     g->blk_chunks = (int64_t)(chunks.size() / 4);
     g->d_blk_chunks = d_chunks;            // set last: non-null means the lists are complete
     return DIFFUSER_OK;
 }
+
+namespace {
+
+constexpr size_t kMaxDeals = 4;
+
+// The launch's items dealt heaviest first, each to the CTA with the fewest chunks so
+// far (ties: the lowest index): a position with many more key blocks than the rest
+// (the global block rows read all of them) then shares its CTA with fewer light
+// tiles, where the snake order gives every CTA the same number of items.  Built on
+// the first launch for (units, CTAs), outside stream capture; while the caller's
+// stream is capturing, after kMaxDeals tables, or when a CTA's list would not fit
+// its table, the kernel deals in snake order instead.
+void block_deal(const diffuser_graph* g, int64_t units, int64_t ctas, cudaStream_t stream, BlockArgs& a) {
+    a.deal_ptr = nullptr;
+    a.deal_items = nullptr;
+    BlockDeals* D = g->blk_deals;
+    if (!D) return;
+    std::lock_guard<std::mutex> lk(D->mu);
+    for (const auto& e : D->entries)
+        if (e.units == units && e.ctas == ctas) {
+            a.deal_ptr = e.d_ptr;
+            a.deal_items = e.d_items;
+            return;
+        }
+    if (D->entries.size() >= kMaxDeals) return;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return;
+    const int64_t total = units * (int64_t)g->blk_tiles;
+    if (total > INT32_MAX || (int64_t)g->h_blk_order.size() != g->blk_tiles) return;
+    using Load = std::pair<int64_t, int64_t>;        // (chunks so far, CTA)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int64_t b = 0; b < ctas; ++b) heap.push({0, b});
+    std::vector<std::vector<int32_t>> lists((size_t)ctas);
+    for (int64_t k = 0; k < total; ++k) {            // chunk counts fall with k
+        const int32_t t = g->h_blk_order[(size_t)(k / units)];
+        const int64_t size = g->h_blk_tile_ptr[(size_t)t + 1] - g->h_blk_tile_ptr[(size_t)t];
+        const Load top = heap.top();
+        heap.pop();
+        lists[(size_t)top.second].push_back((int32_t)k);
+        heap.push({top.first + size, top.second});
+    }
+    std::vector<int32_t> ptr((size_t)ctas + 1, 0), items;
+    items.reserve((size_t)total);
+    for (int64_t b = 0; b < ctas; ++b) {
+        if (lists[(size_t)b].size() > (size_t)kMaxCtaTiles) return;
+        items.insert(items.end(), lists[(size_t)b].begin(), lists[(size_t)b].end());
+        ptr[(size_t)b + 1] = (int32_t)items.size();
+    }
+    int32_t *dp = nullptr, *di = nullptr;
+    cudaError_t err = cudaMalloc(&dp, sizeof(int32_t) * ptr.size());
+    if (err == cudaSuccess) err = cudaMalloc(&di, sizeof(int32_t) * items.size());
+    if (err == cudaSuccess) err = cudaMemcpy(dp, ptr.data(), sizeof(int32_t) * ptr.size(), cudaMemcpyHostToDevice);
+    if (err == cudaSuccess)
+        err = cudaMemcpy(di, items.data(), sizeof(int32_t) * items.size(), cudaMemcpyHostToDevice);
+    if (err != cudaSuccess) {
+        cudaFree(dp);
+        cudaFree(di);
+        cudaGetLastError();                           // the snake order serves instead
+        return;
+    }
+    D->entries.push_back({units, ctas, dp, di});
+    a.deal_ptr = dp;
+    a.deal_items = di;
+}
+
+}  // namespace
 
 int plan_block_layout(const diffuser_graph* g, int64_t units, BlockLayout* L) {
     auto al = [](size_t x) { return (x + 1023) / 1024 * 1024; };
@@ -701,6 +811,8 @@ BlockArgs block_args(const diffuser_graph* g, int64_t units, char* ws, const Blo
     a.chunks = g->d_blk_chunks;
     a.tile_ptr = g->d_blk_tile_ptr;
     a.order = g->d_blk_order;
+    a.deal_ptr = nullptr;
+    a.deal_items = nullptr;
     a.mb2 = reinterpret_cast<float*>(ws + L.mb2);
     a.inv_l = reinterpret_cast<float*>(ws + L.inv_l);
     a.V = nullptr;
@@ -719,7 +831,8 @@ int launch_block_scores(const diffuser_graph* g, int64_t units, const void* Q, c
     int st = encode_map(&tmQ, Q, g->n, units, kHeadDim, kTile);
     if (!st) st = encode_map(&tmK, K, g->n, units, kHeadDim, kBlock);
     if (st) return st;
-    const BlockArgs a = block_args(g, units, ws, L);
+    BlockArgs a = block_args(g, units, ws, L);
+    block_deal(g, units, block_ctas(units * g->blk_tiles), stream, a);
     return launch_block<kScore>(tmQ, tmK, tmK, a, stream);     // the score pass loads no Z
 }
 
@@ -733,6 +846,7 @@ int launch_block_hops(const diffuser_graph* g, int64_t units, const void* Q, con
     for (int s = 0; s < 2 && !st; ++s) st = encode_map(&tmZ[s], ws + L.z[s], g->n, units, 2 * kHeadDim, kBlock);
     if (st) return st;
     BlockArgs a = block_args(g, units, ws, L);
+    block_deal(g, units, block_ctas(units * g->blk_tiles), stream, a);
     a.V = static_cast<const __nv_bfloat16*>(V);
     a.out = static_cast<__nv_bfloat16*>(out);
     a.alpha = alpha;

@@ -56,6 +56,7 @@ struct BwdLayout {
 
 namespace dfs {
 struct ReplayCache;
+struct BlockDeals;
 }
 
 struct diffuser_graph {
@@ -94,6 +95,8 @@ struct diffuser_graph {
     int32_t* d_blk_order = nullptr;   // [blk_tiles] tile positions by falling chunk count
     int32_t blk_tiles = 0;
     int64_t blk_chunks = 0;
+    std::vector<int32_t> h_blk_tile_ptr, h_blk_order;   // host copies of the two lists above
+    dfs::BlockDeals* blk_deals = nullptr;   // per (B H, CTAs): the tiles dealt to the CTAs (block_path.cu)
     int* d_status = nullptr;
     int* h_status = nullptr;          // page-locked, mapped host mirror of the word
     dfs::ReplayCache* replay = nullptr;   // captured band-path forwards (see abi.cu)
@@ -210,6 +213,7 @@ struct BlockLayout {
 };
 bool block_eligible(const diffuser_graph* g);
 int build_block_tiles(diffuser_graph* g);      // from the host CSR copy; no-op for other graphs
+void destroy_block_deals(BlockDeals* d);
 int plan_block_layout(const diffuser_graph* g, int64_t units, BlockLayout* L);
 // the score pass (row max and sum) and the hops; launch_block_forward runs both
 int launch_block_scores(const diffuser_graph* g, int64_t units, const void* Q, const void* K, char* ws,
