@@ -126,3 +126,33 @@ def test_block_path_host_buffers(dl, pinned_out):
         torch.cuda.synchronize()
         assert torch.equal(out, ref_dev.cpu())
     assert dl.diffuser_graph_status(g) == 0
+
+
+def test_block_dealing_table_and_snake_order_agree(dl):
+    # The tiles of a launch go to the CTAs through a deal table (heaviest first to the
+    # least-loaded CTA), built on the first forward with a given B*H outside stream
+    # capture; a forward issued while the caller's stream is capturing deals them in
+    # snake order instead.  Each tile is computed by one CTA in a fixed order either
+    # way, so the two outputs agree bit for bit.
+    import torch
+    args = dict(n=4096, block=64, window_blocks=3, rand_blocks=3, global_blocks=2, seed=0)
+    g = dl.diffuser_build_block_graph(**args)
+    # a plain forward with another B*H first: the kernels' one-time set-up happens
+    # outside the capture below, and no table exists yet for B*H = 12
+    Q1, K1, V1 = (to_device(x, "bf16") for x in synthetic.qkv(1, 1, 4096, 64, "bf16", seed=10))
+    dl.diffuser_forward(Q1, K1, V1, g, 5, 0.1)
+    torch.cuda.synchronize()
+    B, H = 3, 4        # 12 global block-row tiles of 32 chunks among 372 of 6: the dealings differ
+    Q, K, V = (to_device(x, "bf16") for x in synthetic.qkv(B, H, 4096, 64, "bf16", seed=11))
+    ws = dl.alloc_workspace(dl.diffuser_workspace_size(g, B, H, 64, dl.DIFFUSER_DTYPE_BF16))
+    out_snake = torch.empty_like(V)
+    side = torch.cuda.Stream()
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cg, stream=side):
+        dl.diffuser_forward(Q, K, V, g, 5, 0.1, out=out_snake, workspace=ws)
+    cg.replay()
+    torch.cuda.synchronize()
+    out_deal = dl.diffuser_forward(Q, K, V, g, 5, 0.1)
+    torch.cuda.synchronize()
+    assert dl.diffuser_graph_status(g) == 0
+    assert torch.equal(out_snake, out_deal)
