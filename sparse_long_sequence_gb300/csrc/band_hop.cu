@@ -299,7 +299,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     const int g16 = a.plan.g16, g16s = g16 > 0 ? g16 : 16;
-    uint8_t* sGA = smem;                                         // global rows: 2 halves x (hi, lo) 4 KB
+    uint8_t* sGA = smem;                                         // global rows' image(s), 16 KB
     uint8_t* sQ = sGA + band::kGImgBytes;                        // 2 x 16 KB
     uint8_t* sK = sQ + 2 * kQBytes;                              // kSBufs x 16 KB
     uint8_t* sZ = sK + kSBufs * kKBytes;                         // kSBufs x (hi 16 KB, lo 16 KB)
@@ -322,9 +322,9 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint64_t* acc_full = pv_done + kSBufs;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* glob_empty = acc_empty + 1;  // the global rows' accumulator has been read
-    uint64_t* full_G = glob_empty + 1;
-    uint64_t* empty_G = full_G + 1;
-    uint64_t* full_GC = empty_G + 1;       // the image by bulk copy + the staged Z rows
+    uint64_t* full_G = glob_empty + 1;     // [gbufs] the global rows' image of tile lt, buffer lt % gbufs
+    uint64_t* empty_G = full_G + 2;        // [gbufs]
+    uint64_t* full_GC = empty_G + 2;       // the image by bulk copy + the staged Z rows
     uint64_t* empty_GC = full_GC + 1;
     // first hop: the band sums of a quadrant's rows, from its weight warps to its
     // epilogue warp, double-buffered by tile parity: [quad][parity]
@@ -334,6 +334,14 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     const BandPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The global rows' image of a tile: four planes (two 64-key halves x hi, lo) of 32
+    // rows in global memory.  With at most 16 global rows only the planes' first 16
+    // rows are copied, into two 8 KB buffers used by alternate tiles, so that a tile's
+    // image loads while the previous tile's global MMAs run; with more, one 16 KB
+    // buffer.  (The MMA reads 128 A rows: rows past the copied ones fall on other
+    // shared-memory data and reach only accumulator rows that are never read.)
+    const int gbufs = P.g <= 16 ? 2 : 1;
+    const int gplane = P.g <= 16 ? band::kGImgPlaneBytes / 2 : band::kGImgPlaneBytes;   // bytes per plane
     const int nc = P.chunks / 2;                 // 128-key chunks of a tile (the key grid has an even count)
     const int c0 = P.r64 / kCK;                  // the chunk of the tile's first own key
     const bool has_g = P.g > 0;
@@ -359,8 +367,7 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ptx::mbar_init(acc_full, 1);
         ptx::mbar_init(acc_empty, kEpiWarps);
         ptx::mbar_init(glob_empty, 1);
-        ptx::mbar_init(full_G, 1);
-        ptx::mbar_init(empty_G, 1);
+        for (int s = 0; s < 2; ++s) { ptx::mbar_init(&full_G[s], 1); ptx::mbar_init(&empty_G[s], 1); }
         ptx::mbar_init(full_GC, 1 + kEpiWarps);  // the image's bytes + each epilogue warp's staged rows
         ptx::mbar_init(empty_GC, 1);
         for (int s = 0; s < 8; ++s) { ptx::mbar_init(&xch_full[s], kSlices); ptx::mbar_init(&xch_empty[s], 1); }
@@ -430,11 +437,15 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const TileInfo ti = tile(lt);
             if (has_g) {
                 // the global rows' image of this tile's keys, needed from chunk c0 on
-                if (lt >= 1) ptx::mbar_wait(empty_G, (lt - 1) & 1, a.status);
+                const int gb = lt % gbufs, gk = lt / gbufs;
+                if (lt >= gbufs) ptx::mbar_wait(&empty_G[gb], (gk - 1) & 1, a.status);
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(full_G, band::kGImgBytes);
-                    ptx::bulk_load_hint(sGA, a.A_gimg + (size_t)ti.tix * band::kGImgBytes, band::kGImgBytes,
-                                        full_G, pol_once);
+                    uint8_t* gdst = sGA + gb * (band::kGImgBytes / 2);
+                    const uint8_t* gsrc = a.A_gimg + (size_t)ti.tix * band::kGImgBytes;
+                    ptx::mbar_arrive_expect_tx(&full_G[gb], 4 * gplane);
+                    for (int pl = 0; pl < 4; ++pl)
+                        ptx::bulk_load_hint(gdst + pl * gplane, gsrc + pl * band::kGImgPlaneBytes, gplane,
+                                            &full_G[gb], pol_once);
                 }
             }
             for (int c = ti.c_lo; c <= ti.c_hi; ++c, ++g) {
@@ -570,19 +581,20 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         if (rel == 0) {
                             // the image is in shared memory and the previous tile's
                             // accumulator has been read
-                            ptx::mbar_wait(full_G, lt & 1, a.status);
+                            ptx::mbar_wait(&full_G[lt % gbufs], (lt / gbufs) & 1, a.status);
                             if (lt >= 1) ptx::mbar_wait(glob_empty, (lt - 1) & 1, a.status);
                             __syncwarp();
                             ptx::tc_fence_after();
                         }
                         const int h = rel >> 6, kk = (rel & 63) >> 4;
-                        const uint64_t ghi = gdesc0 + (uint64_t)(h * ((2 * band::kGImgPlaneBytes) >> 4) + 2 * kk);
-                        const uint64_t glo = ghi + (uint64_t)(band::kGImgPlaneBytes >> 4);
+                        const uint64_t ghi = gdesc0 + (uint64_t)((((lt % gbufs) * (band::kGImgBytes / 2) + h * 2 * gplane) >> 4) +
+                                                                 2 * kk);
+                        const uint64_t glo = ghi + (uint64_t)(gplane >> 4);
                         const uint64_t bdesc = zd + (uint64_t)(128 * ks);
                         if (ptx::elect_one()) ptx::mma_bf16_ss(dglob, ghi, bdesc, kHop0 ? idesc64 : idesc128, rel != 0);
                         if (ptx::elect_one()) ptx::mma_bf16_ss(dglob, glo, bdesc, idesc64, 1);
                     }
-                    if (c == glob_last && ptx::elect_one()) ptx::mma_commit(empty_G);
+                    if (c == glob_last && ptx::elect_one()) ptx::mma_commit(&empty_G[lt % gbufs]);
                 }
                 if (ptx::elect_one()) ptx::mma_commit(&pv_done[sp]);
                 if (c == ti.c_hi && ptx::elect_one()) ptx::mma_commit(acc_full);
@@ -594,7 +606,10 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (uses > 0) ptx::mbar_wait(&pv_done[s], (uses - 1) & 1, a.status);
             }
             if (has_g && my_tiles > 0) {
-                ptx::mbar_wait(empty_G, (my_tiles - 1) & 1, a.status);
+                for (int gb = 0; gb < gbufs; ++gb) {
+                    const int uses = (my_tiles - gb + gbufs - 1) / gbufs;
+                    if (uses > 0) ptx::mbar_wait(&empty_G[gb], (uses - 1) & 1, a.status);
+                }
                 ptx::mbar_wait(empty_GC, (my_tiles - 1) & 1, a.status);
             }
         }
@@ -747,34 +762,32 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ptx::bulk_load_hint(sGC, a.A_gcimg + (size_t)tix * 2 * gc_plane, 2 * gc_plane, full_GC,
                                     ptx::l2_evict_first());
             }
-            for (int e = t; e < g16 * 8; e += kEpiWarps * 32) {
-                const int sl = e >> 3, cch = e & 7;
-                float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                if (sl < P.g) {
+            // the key rows' hi and lo halves, as asynchronous copies from Z_k's hi | lo
+            // rows (V, whose lo part is zero, on the first hop); 16 pieces per row
+            for (int e = t; e < g16 * 16; e += kEpiWarps * 32) {
+                const int sl = e >> 4, half = (e >> 3) & 1, cch = e & 7;
+                uint8_t* dst = sZG + half * g16 * 128 + sl * 128 + ((cch ^ (sl & 7)) << 4);
+                if (sl < P.g && !(kHop0 && half)) {
                     const size_t row = (size_t)u * P.n + a.globals[sl];
-                    if (kHop0) {
-                        const uint4 h = __ldg(reinterpret_cast<const uint4*>(a.V + row * kHeadDim) + cch);
-                        const uint32_t w4[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) { z[2 * q] = bf16lo(w4[q]); z[2 * q + 1] = bf16hi(w4[q]); }
-                    } else {
-                        const float4* zp = reinterpret_cast<const float4*>(a.Zf_in + row * kHeadDim) + 2 * cch;
-                        const float4 z0 = __ldg(zp), z1 = __ldg(zp + 1);
-                        z[0] = z0.x; z[1] = z0.y; z[2] = z0.z; z[3] = z0.w;
-                        z[4] = z1.x; z[5] = z1.y; z[6] = z1.z; z[7] = z1.w;
-                    }
+                    if (kHop0) ptx::cp_async16(dst, a.V + row * kHeadDim + 8 * cch);
+                    else ptx::cp_async16(dst, a.Zk_hilo + row * (2 * kHeadDim) + half * kHeadDim + 8 * cch);
+                } else {
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
                 }
-                uint4 hi, lo;
-                split8(z, hi, lo);
-                const int off = sl * 128 + ((cch ^ (sl & 7)) << 4);
-                *reinterpret_cast<uint4*>(sZG + off) = hi;
-                *reinterpret_cast<uint4*>(sZG + g16 * 128 + off) = lo;
             }
+            ptx::cp_async_commit();
+        };
+        // this thread's copies have landed: visible to the MMAs, and the warp signals
+        auto stage_gc_done = [&]() {
+            ptx::cp_async_wait_all();
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(full_GC);
         };
-        if (has_g && my_tiles > 0) stage_gc(0);
+        if (has_g && my_tiles > 0) {
+            stage_gc(0);
+            stage_gc_done();
+        }
         for (int lt = 0; lt < my_tiles; ++lt) {
             {
                 // this quadrant's rows of Psum into its staging rows and of V into its V
@@ -823,7 +836,12 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (row_ok) a.inv_l[urow] = inv;
             }
             ptx::mbar_wait(acc_full, lt & 1, a.status);
-            ptx::cp_async_wait_all();
+            ptx::cp_async_wait_all();       // also the next tile's global key rows (stage_gc)
+            if (has_g && lt + 1 < my_tiles) {
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(full_GC);
+            }
             __syncwarp();       // reconverge before the warp-collective tcgen05.ld; the
                                 // quadrant's Psum and V rows are in shared memory
             ptx::tc_fence_after();
