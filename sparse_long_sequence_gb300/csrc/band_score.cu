@@ -518,14 +518,17 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int trow = (t >> 3) * 1024 + (t & 7) * 128;
             float mraw = -INFINITY;               // max of the raw dot products q.k (unscaled)
             float m = 0.f, b2 = 0.f, lsum = 0.f;
+            // the extras' maximum from score_sparse_kernel, loaded now so that its
+            // latency passes under the tile's chunks (this row is rewritten only at the
+            // tile's end, by this thread)
+            const float ms_pre = row_ok ? a.w.m_sparse[(size_t)u * P.n + i] : 0.f;
             // both column halves of a row agree on the row maximum (band, the
             // out-of-window globals, and the extras from score_sparse_kernel)
             auto transition = [&]() {
                 xch[rtid] = mraw;
                 ptx::named_barrier_sync(pair_bar, 64);
                 const float other = xch[(rtid + 128) & 255];
-                const float ms = row_ok ? a.w.m_sparse[(size_t)u * P.n + i] : 0.f;
-                m = fmaxf(ms, fmaxf(mraw, other) * kScale);
+                m = fmaxf(ms_pre, fmaxf(mraw, other) * kScale);
                 if (has_g) {
                     float gs[32];
                     ptx::tmem_ld32(tmem + lane_base + kGcCol0 + 32 * (lt & 1), gs);
@@ -559,16 +562,18 @@ score_band_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 const bool full_in = row_ok && j0 >= lo && j0 + 31 <= hi;
                 const bool none_in = !row_ok || j0 > hi || j0 + 31 < lo;
                 if (!pass2) {
+                    // four independent maxima (the max is exact in any order), then combined
+                    float m4[4] = {mraw, -INFINITY, -INFINITY, -INFINITY};
                     if (full_in) {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) mraw = fmaxf(mraw, sv[k]);
+                        for (int k = 0; k < 32; ++k) m4[k & 3] = fmaxf(m4[k & 3], sv[k]);
                     } else if (!none_in) {
+                        const int dlo = (int)(lo - j0), dhi = (int)(hi - j0);   // in-window keys k in [dlo, dhi]
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const int64_t j = j0 + k;
-                            if (j >= lo && j <= hi) mraw = fmaxf(mraw, sv[k]);
-                        }
+                        for (int k = 0; k < 32; ++k)
+                            if (k >= dlo && k <= dhi) m4[k & 3] = fmaxf(m4[k & 3], sv[k]);
                     }
+                    mraw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 } else {
                     // the staging buffer of this chunk is free once its previous bulk copy has read it
                     const int gs = lt * nc + c;           // pass-2 chunk count of this CTA
