@@ -204,7 +204,12 @@ def test_attention_weights_parity(dl, dtype, causal):
 @pytest.mark.parametrize("causal", [False, True], ids=["bidirectional", "causal"])
 @pytest.mark.parametrize("case", [(1, 2, 300, 8, 3, 5), (2, 3, 1000, 64, 8, 16),
                                   (1, 2, 777, 33, 0, 7), (1, 1, 4096, 256, 16, 32),
-                                  (1, 2, 650, 150, 3, 8)],
+                                  (1, 2, 650, 150, 3, 8),
+                                  # 16 global rows (two 16-row global-row images, used by
+                                  # alternate tiles), 17 and 32 (one 32-row image); radii
+                                  # whose tiles meet their own keys in their first chunk
+                                  (1, 2, 1000, 32, 16, 16), (2, 1, 900, 40, 17, 8),
+                                  (1, 1, 1200, 64, 32, 8)],
                          ids=lambda c: "B%dH%dn%dr%dg%dR%d" % c)
 def test_band_path_matches_csr_path(dl, case, causal):
     # the tensor-core band path and the general CSR path on the same inputs
