@@ -144,21 +144,6 @@ __device__ __forceinline__ float4 bf16x4(const uint2& h) {
     return make_float4(bf16lo(h.x), bf16hi(h.x), bf16lo(h.y), bf16hi(h.y));
 }
 
-// hi / lo bf16 split of eight fp32 values
-__device__ __forceinline__ void split8(const float* z, uint4& hi, uint4& lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const __nv_bfloat162 hh = __floats2bfloat162_rn(z[2 * p], z[2 * p + 1]);
-        const __nv_bfloat162 ll =
-            __floats2bfloat162_rn(z[2 * p] - __low2float(hh), z[2 * p + 1] - __high2float(hh));
-        h[p] = *reinterpret_cast<const uint32_t*>(&hh);
-        l[p] = *reinterpret_cast<const uint32_t*>(&ll);
-    }
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
 // One float4 (features 4 fq .. 4 fq + 3) of global row s of unit u in the next
 // state: (1 - alpha) * (the tiles' shares sum_j A_gr[s][j] Z[j], added in tile
 // order) + alpha * V, from the shares `gpart` that a band hop kernel wrote;

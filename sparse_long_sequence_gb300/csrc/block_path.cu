@@ -188,6 +188,10 @@ block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the set-up above reads only the graph's lists; everything below may touch what
+    // the previous launch on the stream reads or writes
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     int total = 0;                                   // this CTA's chunks
     for (int lt = 0; lt < my_tiles; ++lt) total += sTile[lt].c1 - sTile[lt].c0;
     auto chunk = [&](int c) { return reinterpret_cast<const int4*>(a.chunks)[c]; };
@@ -622,7 +626,9 @@ int launch_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorM
     const int64_t ctas = block_ctas(a.units * a.tiles);
     {
         LaunchScope scope(kMode == kScore ? DIFFUSER_KERNEL_SCORE : DIFFUSER_KERNEL_HOP, stream);
-        block_kernel<kMode><<<(unsigned)ctas, kThreads, block_smem_bytes(), stream>>>(tmQ, tmK, tmZ, a);
+        const cudaError_t e = launch_pdl(block_kernel<kMode>, dim3((unsigned)ctas), dim3(kThreads),
+                                         (size_t)block_smem_bytes(), stream, tmQ, tmK, tmZ, a);
+        if (e != cudaSuccess) return cuda_fail(e, "block_kernel");
     }
     const cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "block_kernel");

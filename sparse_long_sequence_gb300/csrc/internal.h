@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 #include <string>
 #include <vector>
 
@@ -158,6 +159,25 @@ int build_dilated_graph_device(diffuser_graph* g, cudaStream_t stream);   // dil
 
 // ---- CSR SIMT path (simt_path.cu) ------------------------------------------
 #ifdef __CUDACC__
+// Launch with programmatic dependent launch allowed: the kernel may be scheduled
+// before the previous kernel on the stream completes, and must call
+// ptx::griddep_wait before it touches memory that kernel reads or writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // v[k] of every lane of a full warp is one lane's share of value k (k < 32); on
 // return, lane l holds the sum over the 32 lanes of value l.  A butterfly over the
 // lane bits: at each of the 5 steps a lane keeps the half of its values whose index

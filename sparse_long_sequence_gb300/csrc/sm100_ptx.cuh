@@ -290,6 +290,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch (the block-path kernels; measured on the band path's
+// gather/band/score chain it made graph-replayed forwards slower).  A kernel launched
+// with the programmatic stream serialization attribute (launch_pdl) may start while
+// the kernel before it on the stream is still running; griddep_wait blocks until that
+// kernel has completed and its memory operations are visible (at once when launched
+// without the attribute).  griddep_launch_dependents lets the next such kernel be
+// scheduled; it is issued only after this kernel's own wait, so everything before
+// this kernel is complete by the time a dependent starts.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // True in exactly one lane (the lowest) of the fully converged calling warp.
 // The MMA-issuing warps run their loops with all 32 lanes and let the elected
 // lane issue each tcgen05 instruction: a loop run by one lane alone gets far
