@@ -140,8 +140,20 @@ __device__ __forceinline__ void ffma8(float2 (&acc)[4], float w, const float4& z
     acc[3] = __ffma2_rn(ww, make_float2(z1.z, z1.w), acc[3]);
 }
 
-__device__ __forceinline__ float4 bf16x4(const uint2& h) {
-    return make_float4(bf16lo(h.x), bf16hi(h.x), bf16lo(h.y), bf16hi(h.y));
+// acc += w * one gathered row piece: 8 bf16 (kBf16) or 2 x 4 fp32 as raw words
+template <bool kBf16>
+__device__ __forceinline__ void ffma_row(float2 (&acc)[4], float w, const uint4 (&z)[kBf16 ? 1 : 2]) {
+    if constexpr (kBf16) {
+        const uint4 h = z[0];
+        ffma8(acc, w, make_float4(bf16lo(h.x), bf16hi(h.x), bf16lo(h.y), bf16hi(h.y)),
+              make_float4(bf16lo(h.z), bf16hi(h.z), bf16lo(h.w), bf16hi(h.w)));
+    } else {
+        ffma8(acc, w,
+              make_float4(__uint_as_float(z[0].x), __uint_as_float(z[0].y), __uint_as_float(z[0].z),
+                          __uint_as_float(z[0].w)),
+              make_float4(__uint_as_float(z[1].x), __uint_as_float(z[1].y), __uint_as_float(z[1].z),
+                          __uint_as_float(z[1].w)));
+    }
 }
 
 // One float4 (features 4 fq .. 4 fq + 3) of global row s of unit u in the next
@@ -1055,10 +1067,13 @@ hop_gather_kernel(HopArgs a) {
         __syncwarp(qmask);
         const int sb = ss[0], se = ss[cnt];
         float* wq = a.A_x + (size_t)u * a.nx;
-        // this lane's features of row j of Z_k: zrow + 16 j (fp32) or vrow + 16 j (bf16 V)
-        const float4* zrow = reinterpret_cast<const float4*>(a.Zf_in) + ubase * 16 + ql;
-        const uint2* vrow = reinterpret_cast<const uint2*>(a.V) + ubase * 16 + ql;
-        float4* prow = reinterpret_cast<float4*>(a.Psum) + ubase * 16 + ql;
+        // this lane's features of row j of Z_k: fp32 rows, features 4 ql .. +3 and
+        // 32 + 4 ql .. +3 at zrow + 16 j (two 128-byte lines per quarter); the first
+        // hop's bf16 V rows, features 8 ql .. +7 at vrow + 8 j (one line per quarter).
+        // The accumulators hold the same features, in the same order.
+        const uint4* zrow = reinterpret_cast<const uint4*>(a.Zf_in) + ubase * 16 + ql;
+        const uint4* vrow = reinterpret_cast<const uint4*>(a.V) + ubase * 8 + ql;
+        float4* prow = reinterpret_cast<float4*>(a.Psum) + ubase * 16 + (kHop0 ? 2 * ql : ql);
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
         int cur = 0;                              // window row being accumulated
@@ -1074,7 +1089,7 @@ hop_gather_kernel(HopArgs a) {
             if (!sg[cur]) {
                 float4* pr = prow + (size_t)(iw + cur) * 16;
                 pr[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-                pr[8] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+                pr[kHop0 ? 1 : 8] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
                 if (kHop0 && ql == 0) a.inv_l[ubase + iw + cur] += lsum;
             }
 #pragma unroll
@@ -1091,16 +1106,15 @@ hop_gather_kernel(HopArgs a) {
             float wn = 0.f;
             const int en = e0 + kB + ql;
             if (ql < kB && en < se) { jn = __ldg(a.x_col + en); wn = __ldg(wq + en); }
-            float4 z0[kB], z1[kB];
+            uint4 zr[kB][kHop0 ? 1 : 2];
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
                 const int j = __shfl_sync(qmask, jc, b, 8);
                 if (kHop0) {
-                    z0[b] = bf16x4(__ldg(vrow + 16 * j));
-                    z1[b] = bf16x4(__ldg(vrow + 16 * j + 8));
+                    zr[b][0] = __ldg(vrow + 8 * j);
                 } else {
-                    z0[b] = __ldg(zrow + 16 * j);
-                    z1[b] = __ldg(zrow + 16 * j + 8);
+                    zr[b][0] = __ldg(zrow + 16 * j);
+                    zr[b][kHop0 ? 0 : 1] = __ldg(zrow + 16 * j + 8);
                 }
             }
             if (e0 + kB <= nb) {
@@ -1113,7 +1127,7 @@ hop_gather_kernel(HopArgs a) {
                 for (int b = 0; b < kB; ++b) {
                     const float w = __shfl_sync(qmask, wc, b, 8);
                     if (kHop0) lsum += w;
-                    ffma8(acc, w, z0[b], z1[b]);
+                    ffma_row<kHop0>(acc, w, zr[b]);
                 }
             } else {
 #pragma unroll
@@ -1131,7 +1145,7 @@ hop_gather_kernel(HopArgs a) {
                             if (ql == b) wq[e] = w;
                             lsum += w;
                         }
-                        ffma8(acc, w, z0[b], z1[b]);
+                        ffma_row<kHop0>(acc, w, zr[b]);
                     }
                 }
             }
@@ -1145,8 +1159,9 @@ hop_gather_kernel(HopArgs a) {
     }
 }
 
-// the gather configuration: slots in flight per quarter-warp, CTAs per SM
-constexpr int kGatherBatch = 5, kGatherBlocks = 3;
+// the gather configuration: slots in flight per quarter-warp (hops after the
+// first, the first hop), CTAs per SM
+constexpr int kGatherBatch = 5, kGatherBatch0 = 8, kGatherBlocks = 3;
 
 // bf16 tensor map over rows of `row_elems` elements: box of 64 elements x box_rows rows
 int encode_rows(CUtensorMap* m, const void* base, int64_t n, int64_t units, int row_elems,
@@ -1190,7 +1205,7 @@ int launch_hop(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap
     const int64_t total_tiles = a.units * a.plan.tiles;
     {
         LaunchScope scope(DIFFUSER_KERNEL_GATHER, stream);
-        hop_gather_kernel<kHop0, kGatherBatch, kGatherBlocks>
+        hop_gather_kernel<kHop0, kHop0 ? kGatherBatch0 : kGatherBatch, kGatherBlocks>
             <<<(unsigned)(sms * kGatherBlocks), kGThreadsG, 0, stream>>>(a);
     }
     cudaError_t err = cudaGetLastError();
