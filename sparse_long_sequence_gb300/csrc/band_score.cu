@@ -91,11 +91,6 @@ __device__ __forceinline__ float reduce8_transpose(float (&v)[8], int ql, unsign
     return keep + __shfl_xor_sync(mask, send, 1, 8);
 }
 
-__device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
-    x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
-    x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
-}
-
 // Persistent, 8 warps per CTA.  The rows of all units are split evenly over the
 // quarter-warps of the grid; a quarter walks its rows in windows of up to
 // kSWinRows rows of one unit, as a sequence of batches of up to 8 slots of one
@@ -152,38 +147,40 @@ score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
             auto cols = [&](int r, int e) -> int32_t {       // this lane's column of batch (r, e)
                 return (r < cnt && e + ql < ss[r + 1]) ? __ldg(a.gr.x_col + e + ql) : 0;
             };
+            // Slots past a row's end (and the batch after the last) read k row 0 of
+            // the unit: their dot products land on lanes whose results are not stored.
             const int32_t jA = cols(rA, eA);
             int32_t jB = cols(rB, eB);
             uint4 qA = __ldg(Qu + (size_t)rA * 8);
             uint4 qB = rB < cnt ? __ldg(Qu + (size_t)rB * 8) : qA;
             uint4 kA[8], kB[8];
-            const int nA0 = ss[rA + 1] - eA;
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                const int j = __shfl_sync(qmask, jA, b, 8);
-                kA[b] = b < nA0 ? __ldg(Ku + (size_t)j * 8) : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int b = 0; b < 8; ++b) kA[b] = __ldg(Ku + (size_t)__shfl_sync(qmask, jA, b, 8) * 8);
             float mrow = -INFINITY;               // this lane's running max of row rA
-            while (rA < cnt) {
+            // one batch: batch B's k rows load into kn while batch A's (in kc) are
+            // used; the two arrays swap roles from one batch to the next
+            auto step = [&](uint4 (&kc)[8], uint4 (&kn)[8]) {
                 int rC, eC;
                 if (rB < cnt) next(rB, eB, rC, eC); else { rC = cnt; eC = 0; }
                 const int32_t jC = cols(rC, eC);
                 const uint4 qC = (rC < cnt && rC != rB) ? __ldg(Qu + (size_t)rC * 8) : qB;
-                const int nB = rB < cnt ? min(8, ss[rB + 1] - eB) : 0;
+#pragma unroll
+                for (int b = 0; b < 8; ++b) kn[b] = __ldg(Ku + (size_t)__shfl_sync(qmask, jB, b, 8) * 8);
+                // batch A: 8 partial dot products (pairs of features on packed FMAs;
+                // bf16 products are exact in fp32), reduced across the quarter
+                const float2 q01 = make_float2(bf16lo(qA.x), bf16hi(qA.x));
+                const float2 q23 = make_float2(bf16lo(qA.y), bf16hi(qA.y));
+                const float2 q45 = make_float2(bf16lo(qA.z), bf16hi(qA.z));
+                const float2 q67 = make_float2(bf16lo(qA.w), bf16hi(qA.w));
+                float v[8];
 #pragma unroll
                 for (int b = 0; b < 8; ++b) {
-                    const int j = __shfl_sync(qmask, jB, b, 8);
-                    kB[b] = b < nB ? __ldg(Ku + (size_t)j * 8) : make_uint4(0u, 0u, 0u, 0u);
-                }
-                // batch A: 8 partial dot products, reduced across the quarter
-                float qf[8], v[8];
-                unpack8(qA, qf);
-#pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    float kx[8];
-                    unpack8(kA[b], kx);
-                    v[b] = qf[0] * kx[0] + qf[1] * kx[1] + qf[2] * kx[2] + qf[3] * kx[3] +
-                           qf[4] * kx[4] + qf[5] * kx[5] + qf[6] * kx[6] + qf[7] * kx[7];
+                    const uint4 k = kc[b];
+                    float2 p = __fmul2_rn(q01, make_float2(bf16lo(k.x), bf16hi(k.x)));
+                    p = __ffma2_rn(q23, make_float2(bf16lo(k.y), bf16hi(k.y)), p);
+                    p = __ffma2_rn(q45, make_float2(bf16lo(k.z), bf16hi(k.z)), p);
+                    p = __ffma2_rn(q67, make_float2(bf16lo(k.w), bf16hi(k.w)), p);
+                    v[b] = p.x + p.y;
                 }
                 const float dot = reduce8_transpose(v, ql, qmask);   // slot eA + ql
                 if (eA + ql < ss[rA + 1]) {
@@ -199,9 +196,12 @@ score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
                     mrow = -INFINITY;
                 }
                 rA = rB; eA = eB; qA = qB;
-#pragma unroll
-                for (int b = 0; b < 8; ++b) kA[b] = kB[b];
                 rB = rC; eB = eC; qB = qC; jB = jC;
+            };
+            while (rA < cnt) {
+                step(kA, kB);
+                if (rA >= cnt) break;
+                step(kB, kA);
             }
         }
         __syncwarp(qmask);                        // the window's smem is rewritten next
