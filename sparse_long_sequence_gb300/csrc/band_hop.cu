@@ -157,28 +157,42 @@ __device__ __forceinline__ void ffma_row(float2 (&acc)[4], float w, const uint4 
 }
 
 // One float4 (features 4 fq .. 4 fq + 3) of global row s of unit u in the next
-// state: (1 - alpha) * (the tiles' shares sum_j A_gr[s][j] Z[j], added in tile
-// order) + alpha * V, from the shares `gpart` that a band hop kernel wrote;
-// written as [hi | lo] bf16 and fp32 row pieces (zhl, zf) or as the output.
+// state: (1 - alpha) * (the tiles' shares sum_j A_gr[s][j] Z[j]) + alpha * V,
+// from the shares `gpart` that a band hop kernel wrote; written as [hi | lo]
+// bf16 and fp32 row pieces (zhl, zf) or as the output.  L = 1 or 8 lanes
+// (ql = 0 .. L-1, converged, mask qmask) compute it together, in a fixed order:
+// lane ql adds the shares of tiles ql, ql + L, ... in turn, then the L partial
+// sums are added pairwise; lane 0 writes.  Eight lanes when a unit has at least
+// kCoopTiles tiles (more loads in flight per output), one lane otherwise.
+constexpr int kCoopTiles = 16;
 template <bool kOut>
 __device__ __forceinline__ void global_row_out(const HopArgs& a, const float* gpart, int64_t u, int s,
-                                               int fq, __nv_bfloat16* zhl, float* zf) {
+                                               int fq, int L, int ql, unsigned qmask,
+                                               __nv_bfloat16* zhl, float* zf) {
     const BandPlan& P = a.plan;
     const size_t tstride = (size_t)P.g * (kHeadDim / 4);  // float4s from one share to the next
     const int nshares = P.tiles;                          // one per tile
     const float4* src = reinterpret_cast<const float4*>(gpart) + (size_t)u * nshares * tstride +
                         (size_t)s * (kHeadDim / 4) + fq;
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t0 = 0; t0 < nshares; t0 += 8) {
+    for (int t0 = ql; t0 < nshares; t0 += 8 * L) {
         float4 v[8];
 #pragma unroll
         for (int b = 0; b < 8; ++b)
-            v[b] = t0 + b < nshares ? __ldg(src + (size_t)(t0 + b) * tstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[b] = t0 + L * b < nshares ? __ldg(src + (size_t)(t0 + L * b) * tstride)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             sum.x += v[b].x; sum.y += v[b].y; sum.z += v[b].z; sum.w += v[b].w;
         }
     }
+    for (int off = 1; off < L; off <<= 1) {
+        sum.x += __shfl_xor_sync(qmask, sum.x, off, 8);
+        sum.y += __shfl_xor_sync(qmask, sum.y, off, 8);
+        sum.z += __shfl_xor_sync(qmask, sum.z, off, 8);
+        sum.w += __shfl_xor_sync(qmask, sum.w, off, 8);
+    }
+    if (ql != 0) return;
     const float keep = 1.f - a.alpha;
     const int64_t gi = a.globals[s];
     const size_t vrow = ((size_t)u * P.n + gi) * kHeadDim + 4 * fq;
@@ -207,14 +221,17 @@ __device__ __forceinline__ void global_row_out(const HopArgs& a, const float* gp
     }
 }
 
-// The output's global rows after the last hop: one thread per float4.
+// The output's global rows after the last hop: L lanes per float4 (global_row_out).
 __global__ void __launch_bounds__(256) hop_global_out_kernel(HopArgs a) {
     const int64_t per_unit = (int64_t)a.plan.g * (kHeadDim / 4);
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int L = a.plan.tiles >= kCoopTiles ? 8 : 1;
+    const int64_t tix = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t idx = L == 8 ? tix >> 3 : tix;   // the same for the L lanes of an output
     if (idx >= a.units * per_unit) return;
     const int64_t u = idx / per_unit;
     const int rem = (int)(idx - u * per_unit);
-    global_row_out<true>(a, a.gpart, u, rem >> 4, rem & 15, nullptr, nullptr);
+    global_row_out<true>(a, a.gpart, u, rem >> 4, rem & 15, L, L == 8 ? (int)(threadIdx.x & 7) : 0,
+                         L == 8 ? 0xFFu << (threadIdx.x & 24) : 0u, nullptr, nullptr);
 }
 
 // ---------------------------------------------------------------- the CTAs' tiles
@@ -1039,13 +1056,23 @@ hop_gather_kernel(HopArgs a) {
     uint8_t* sg = sGlob[qi];
     if (!kHop0 && P.g > 0) {
         // Z_k of the global rows, from the previous hop's shares: one float4 per
-        // thread, spread over all CTAs (no extra reads them: the extras exclude G)
+        // quarter-warp (or per thread, global_row_out), spread over all CTAs (no
+        // extra reads them: the extras exclude G)
         const int64_t per_unit = (int64_t)P.g * (kHeadDim / 4), total = a.units * per_unit;
-        for (int64_t idx = (int64_t)tid * gridDim.x + blockIdx.x; idx < total;
-             idx += (int64_t)blockDim.x * gridDim.x) {
-            const int64_t u = idx / per_unit;
-            const int rem = (int)(idx - u * per_unit);
-            global_row_out<false>(a, a.gpart, u, rem >> 4, rem & 15, a.Zk_hilo, a.Zk_f);
+        if (P.tiles >= kCoopTiles) {
+            for (int64_t idx = (int64_t)qi * gridDim.x + blockIdx.x; idx < total;
+                 idx += (int64_t)(kGThreadsG / 8) * gridDim.x) {
+                const int64_t u = idx / per_unit;
+                const int rem = (int)(idx - u * per_unit);
+                global_row_out<false>(a, a.gpart, u, rem >> 4, rem & 15, 8, ql, qmask, a.Zk_hilo, a.Zk_f);
+            }
+        } else {
+            for (int64_t idx = (int64_t)tid * gridDim.x + blockIdx.x; idx < total;
+                 idx += (int64_t)blockDim.x * gridDim.x) {
+                const int64_t u = idx / per_unit;
+                const int rem = (int)(idx - u * per_unit);
+                global_row_out<false>(a, a.gpart, u, rem >> 4, rem & 15, 1, 0, 0u, a.Zk_hilo, a.Zk_f);
+            }
         }
         __syncwarp();     // reconverge: the quarters below synchronize only among themselves
     }
@@ -1223,7 +1250,8 @@ int launch_hop(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap
     if (kLast && a.plan.g > 0) {
         LaunchScope scope(DIFFUSER_KERNEL_GATHER, stream);
         const int64_t outs = a.units * a.plan.g * (kHeadDim / 4);
-        hop_global_out_kernel<<<(unsigned)((outs + 255) / 256), 256, 0, stream>>>(a);
+        const int64_t threads = a.plan.tiles >= kCoopTiles ? 8 * outs : outs;
+        hop_global_out_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(a);
     }
     err = cudaGetLastError();
     return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_global_out_kernel");
