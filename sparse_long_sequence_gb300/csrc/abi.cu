@@ -509,6 +509,7 @@ int new_graph(diffuser_graph** out, diffuser_graph** g) {
     *g = new (std::nothrow) diffuser_graph();
     if (!*g) return fail(DIFFUSER_ERR_ALLOC, "host allocation failed");
     (*g)->replay = new (std::nothrow) ReplayCache();   // without it, forwards launch directly
+    (*g)->band_deals = dfs::create_band_deals();        // without it, the band path deals in snake order
     // status block: word, padding, then the device address of the host mirror
     cudaError_t err = cudaGetDevice(&(*g)->device);
     int* mirror_dev = nullptr;
@@ -703,6 +704,7 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_blk_tile_ptr);
     cudaFree(g->d_blk_order);
     dfs::destroy_block_deals(g->blk_deals);
+    dfs::destroy_band_deals(g->band_deals);
     cudaFree(g->d_status);
     if (g->h_status) cudaFreeHost(g->h_status);
     dfs::destroy_replay_cache(g->replay);

@@ -39,8 +39,11 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <new>
+#include <vector>
 
 #include "band_common.cuh"
 #include "internal.h"
@@ -129,6 +132,8 @@ struct HopArgs {
     float* Zk_f;                 // as fp32 rows: the gather of hops after the first writes
                                  // Z_k's global rows there (from the previous hop's shares)
     int* status;
+    const int32_t* deal_ptr;     // [CTAs + 1] each CTA's range of deal_tiles (null: snake order)
+    const int32_t* deal_tiles;   // the dealt tiles, u * tiles + t
 };
 
 // acc[0..3] += w * (z0, z1) with packed pairs (the same rounding as fmaf per element)
@@ -237,7 +242,8 @@ __global__ void __launch_bounds__(256) hop_global_out_kernel(HopArgs a) {
 // ---------------------------------------------------------------- the CTAs' tiles
 // A tile's 128-key chunks c (keys i0 - r64 + 128 c .. +127) that hold at least one
 // key in 0 .. n-1: c_lo .. c_hi (the others would only add zeros).
-__device__ __forceinline__ void chunk_range(const BandPlan& P, int nc, int64_t i0, int& c_lo, int& c_hi) {
+__host__ __device__ __forceinline__ void chunk_range(const BandPlan& P, int nc, int64_t i0, int& c_lo,
+                                                     int& c_hi) {
     const int64_t below = (int64_t)P.r64 - i0 - (kCK - 1);     // chunk c lies below key 0 iff 128 c < below
     c_lo = below > 0 ? (int)((below + kCK - 1) / kCK) : 0;
     const int64_t last = (P.n - (i0 - P.r64) - 1) / kCK;       // the last chunk with a key below n
@@ -247,7 +253,7 @@ __device__ __forceinline__ void chunk_range(const BandPlan& P, int nc, int64_t i
 // The tile position (0 .. tiles-1) of rank p when the positions are ordered by
 // falling chunk count: the interior positions (all nc chunks in range) in order,
 // then the edge positions (the first and last few of a unit), heavier first.
-__device__ int tile_position(const BandPlan& P, int nc, int p) {
+__host__ __device__ int tile_position(const BandPlan& P, int nc, int p) {
     const int64_t tl = P.r64 > kCK - 1 ? ((int64_t)P.r64 - (kCK - 1) + kCK - 1) / kCK : 0;
     const int64_t rnum = P.n + P.r64 - 1 - (int64_t)kCK * (nc - 1);
     int64_t tr = rnum >= 0 ? rnum / kCK : -1;
@@ -268,12 +274,25 @@ __device__ int tile_position(const BandPlan& P, int nc, int p) {
     }
 }
 
-// The CTAs take the units' tiles heaviest first, in snake order over the rounds
-// (round r: CTA b gets item r G + b, or r G + G - 1 - b when r is odd), so that the
-// light edge tiles fill the last rounds.  The items: first every unit's interior
-// tiles, unit by unit (so that CTAs running at the same time mostly hold
+// The launch's items k = 0 .. units * tiles - 1, heaviest first: every unit's
+// interior tiles, unit by unit (so that CTAs running at the same time mostly hold
 // neighbouring tiles, which share K and Z_k chunks in L2), then the edge tiles,
 // heavier positions first (tile_position), unit by unit within a position.
+__host__ __device__ __forceinline__ void band_item(const BandPlan& P, int64_t units, int nc, int64_t k,
+                                                   int64_t& u, int& t) {
+    const int64_t tl = P.r64 > kCK - 1 ? ((int64_t)P.r64 - (kCK - 1) + kCK - 1) / kCK : 0;
+    const int64_t rnum = P.n + P.r64 - 1 - (int64_t)kCK * (nc - 1);
+    int64_t tr = rnum >= 0 ? rnum / kCK : -1;
+    if (tr > P.tiles - 1) tr = P.tiles - 1;
+    const int64_t ni = tl <= tr ? tr - tl + 1 : 0;
+    if (k < units * ni) { u = k / ni; t = (int)(tl + (k - u * ni)); }
+    else { const int64_t k2 = k - units * ni, pr = ni + k2 / units; u = k2 - (k2 / units) * units; t = tile_position(P, nc, (int)pr); }
+}
+
+// Without a deal table the CTAs take the items in snake order over the rounds
+// (round r: CTA b gets item r G + b, or r G + G - 1 - b when r is odd), so that the
+// light edge tiles fill the last rounds; with one (band_deal), CTA b takes the
+// tiles listed for it.
 struct TileInfo { int64_t tix, u, i0; int c_lo, c_hi; };
 __device__ __forceinline__ int cta_tile_count(int64_t total_tiles) {
     const int64_t G = gridDim.x, b = blockIdx.x, R = total_tiles / G, rem = total_tiles - R * G;
@@ -282,16 +301,9 @@ __device__ __forceinline__ int cta_tile_count(int64_t total_tiles) {
 __device__ __forceinline__ TileInfo cta_tile(const BandPlan& P, int64_t units, int nc, int lt) {
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t k = (int64_t)lt * G + ((lt & 1) ? G - 1 - b : b);
-    // interior tiles first, unit-major (neighbouring tiles run together), then the edge tiles
-    const int64_t tl = P.r64 > kCK - 1 ? ((int64_t)P.r64 - (kCK - 1) + kCK - 1) / kCK : 0;
-    const int64_t rnum = P.n + P.r64 - 1 - (int64_t)kCK * (nc - 1);
-    int64_t tr = rnum >= 0 ? rnum / kCK : -1;
-    if (tr > P.tiles - 1) tr = P.tiles - 1;
     TileInfo ti;
     int t;
-    const int64_t ni = tl <= tr ? tr - tl + 1 : 0;
-    if (k < units * ni) { ti.u = k / ni; t = (int)(tl + (k - ti.u * ni)); }
-    else { const int64_t k2 = k - units * ni, pr = ni + k2 / units; ti.u = k2 - (k2 / units) * units; t = tile_position(P, nc, (int)pr); }
+    band_item(P, units, nc, k, ti.u, t);
     ti.tix = ti.u * P.tiles + t;
     ti.i0 = (int64_t)t * kTileRows;
     chunk_range(P, nc, ti.i0, ti.c_lo, ti.c_hi);
@@ -361,10 +373,21 @@ hop_band_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const bool has_g = P.g > 0;
     const int gc_plane = band::gc_plane_bytes(g16);
     const int64_t total_tiles = a.units * P.tiles;
-    const int my_tiles = cta_tile_count(total_tiles);           // this CTA's tiles (cta_tile)
+    // this CTA's tiles: its list in the deal table, or the snake order (cta_tile)
+    const int my_tiles = a.deal_ptr ? a.deal_ptr[blockIdx.x + 1] - a.deal_ptr[blockIdx.x]
+                                    : cta_tile_count(total_tiles);
     for (int lt = tid; lt < my_tiles && lt < kMaxCtaTiles; lt += kThreads) {
-        const TileInfo ti = cta_tile(P, a.units, nc, lt);
-        sTile[lt] = TileEntry{(int32_t)ti.u, (int32_t)(ti.i0 / kTileRows), (int16_t)ti.c_lo, (int16_t)ti.c_hi};
+        if (a.deal_ptr) {
+            const int32_t tix = a.deal_tiles[a.deal_ptr[blockIdx.x] + lt];
+            const int32_t u = tix / P.tiles, t = tix - u * P.tiles;
+            int lo, hi;
+            chunk_range(P, nc, (int64_t)t * kTileRows, lo, hi);
+            sTile[lt] = TileEntry{u, t, (int16_t)lo, (int16_t)hi};
+        } else {
+            const TileInfo ti = cta_tile(P, a.units, nc, lt);
+            sTile[lt] = TileEntry{(int32_t)ti.u, (int32_t)(ti.i0 / kTileRows), (int16_t)ti.c_lo,
+                                  (int16_t)ti.c_hi};
+        }
     }
 
     if (warp == kSMmaWarp) ptx::tmem_alloc(tmem_slot, kTmemCols);
@@ -1218,6 +1241,14 @@ int sm_count() {
     return num_sms;
 }
 
+// One CTA per SM, or more (in waves) when an SM's share would exceed the tile table.
+int64_t band_ctas(int64_t total_tiles) {
+    const int64_t sms = sm_count();
+    int64_t ctas = total_tiles < sms ? total_tiles : sms;
+    if ((total_tiles + ctas - 1) / ctas > kMaxCtaTiles) ctas = (total_tiles + kMaxCtaTiles - 1) / kMaxCtaTiles;
+    return ctas;
+}
+
 template <bool kHop0, bool kLast>
 int launch_hop(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmZ, const HopArgs& a,
                cudaStream_t stream) {
@@ -1237,10 +1268,7 @@ int launch_hop(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap
     }
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return cuda_fail(err, "hop_gather_kernel");
-    // one CTA per SM, or more (in waves) when an SM's share would exceed the tile table
-    int64_t ctas = total_tiles < sms ? total_tiles : sms;
-    if ((total_tiles + ctas - 1) / ctas > kMaxCtaTiles) ctas = (total_tiles + kMaxCtaTiles - 1) / kMaxCtaTiles;
-    dim3 grid((unsigned)ctas);
+    dim3 grid((unsigned)band_ctas(total_tiles));
     {
         LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
         hop_band_kernel<kHop0, kLast><<<grid, kThreads, band_smem_bytes(a.plan.g16), stream>>>(tmQ, tmK, tmZ, a);
@@ -1255,6 +1283,155 @@ int launch_hop(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap
     }
     err = cudaGetLastError();
     return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "hop_global_out_kernel");
+}
+
+// A tile's cost in the deal: 2 per 128-key chunk and 1 for the tile's own
+// hand-offs (a tile boundary costs about half a chunk's period).
+int64_t band_tile_cost(const BandPlan& P, int nc, int t) {
+    int lo, hi;
+    chunk_range(P, nc, (int64_t)t * kTileRows, lo, hi);
+    return 2 * (int64_t)(hi - lo + 1) + 1;
+}
+
+}  // namespace
+
+// The deal tables of a graph's band path, one per (units, CTAs); never evicted, as
+// a captured replay of a forward holds the pointers it was launched with.
+struct BandDeals {
+    struct Entry {
+        int64_t units;
+        int64_t ctas;
+        int32_t* d_ptr;
+        int32_t* d_tiles;
+    };
+    std::mutex mu;
+    std::vector<Entry> entries;
+};
+
+BandDeals* create_band_deals() { return new (std::nothrow) BandDeals(); }
+
+void destroy_band_deals(BandDeals* d) {
+    if (!d) return;
+    for (auto& e : d->entries) {
+        cudaFree(e.d_ptr);
+        cudaFree(e.d_tiles);
+    }
+    delete d;
+}
+
+namespace {
+
+constexpr size_t kMaxBandDeals = 4;
+
+// The snake order over the rounds gives every CTA ceil or floor of tiles / CTAs
+// tiles; when that does not divide, the CTAs with one tile more get their share
+// of heavy tiles as well (4 interior tiles and 2 edge tiles, where 3 and 3 would
+// do).  Starting from the snake deal, the busiest CTA repeatedly trades a tile for
+// a lighter one of the least busy CTA (or hands it one) while that lowers the
+// larger of the two loads.  Each CTA then takes its tiles in item order (heaviest
+// first, neighbouring tiles together).  Where no trade helps, the launch keeps the
+// snake order (a null table).  Built on the first launch for (units, CTAs), outside
+// stream capture; while the caller's stream is capturing, after
+// kMaxBandDeals tables, or when a CTA's list would not fit its table, the kernel
+// deals in snake order instead.
+void band_deal(const diffuser_graph* g, const BandPlan& P, int64_t units, int64_t ctas,
+               cudaStream_t stream, HopArgs& a) {
+    a.deal_ptr = nullptr;
+    a.deal_tiles = nullptr;
+    BandDeals* D = g->band_deals;
+    if (!D || ctas < 2) return;
+    std::lock_guard<std::mutex> lk(D->mu);
+    for (const auto& e : D->entries)
+        if (e.units == units && e.ctas == ctas) {
+            a.deal_ptr = e.d_ptr;
+            a.deal_tiles = e.d_tiles;
+            return;
+        }
+    if (D->entries.size() >= kMaxBandDeals) return;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return;
+    const int64_t total = units * (int64_t)P.tiles;
+    if (total > INT32_MAX) return;
+    const int nc = P.chunks / 2;
+    std::vector<int64_t> pos_cost((size_t)P.tiles);
+    for (int t = 0; t < P.tiles; ++t) pos_cost[(size_t)t] = band_tile_cost(P, nc, t);
+    std::vector<int32_t> tile_of((size_t)total);
+    std::vector<int64_t> cost((size_t)total);
+    std::vector<std::vector<int64_t>> lists((size_t)ctas);   // items k per CTA
+    std::vector<int64_t> load((size_t)ctas, 0);
+    for (int64_t k = 0; k < total; ++k) {
+        int64_t u;
+        int t;
+        band_item(P, units, nc, k, u, t);
+        tile_of[(size_t)k] = (int32_t)(u * P.tiles + t);
+        cost[(size_t)k] = pos_cost[(size_t)t];
+        const int64_t r = k / ctas, q = k - r * ctas, b = (r & 1) ? ctas - 1 - q : q;
+        lists[(size_t)b].push_back(k);
+        load[(size_t)b] += cost[(size_t)k];
+    }
+    int64_t trades = 0;
+    for (int64_t iter = 0; iter < 4 * ctas; ++iter, ++trades) {
+        const size_t M = (size_t)(std::max_element(load.begin(), load.end()) - load.begin());
+        const size_t B = (size_t)(std::min_element(load.begin(), load.end()) - load.begin());
+        if (M == B) break;
+        // the best trade: hand over x (y = none) or swap x for a lighter y
+        int64_t best = load[M];
+        long bx = -1, by = -1;
+        for (size_t ix = 0; ix < lists[M].size(); ++ix) {
+            const int64_t cx = cost[(size_t)lists[M][ix]];
+            if (lists[B].size() < (size_t)kMaxCtaTiles) {
+                const int64_t worst = std::max(load[M] - cx, load[B] + cx);
+                if (worst < best) { best = worst; bx = (long)ix; by = -1; }
+            }
+            for (size_t iy = 0; iy < lists[B].size(); ++iy) {
+                const int64_t d = cx - cost[(size_t)lists[B][iy]];
+                if (d <= 0) continue;
+                const int64_t worst = std::max(load[M] - d, load[B] + d);
+                if (worst < best) { best = worst; bx = (long)ix; by = (long)iy; }
+            }
+        }
+        if (bx < 0) break;
+        const int64_t kx = lists[M][(size_t)bx];
+        lists[M].erase(lists[M].begin() + bx);
+        load[M] -= cost[(size_t)kx];
+        if (by >= 0) {
+            const int64_t ky = lists[B][(size_t)by];
+            lists[B].erase(lists[B].begin() + by);
+            load[B] -= cost[(size_t)ky];
+            lists[M].push_back(ky);
+            load[M] += cost[(size_t)ky];
+        }
+        lists[B].push_back(kx);
+        load[B] += cost[(size_t)kx];
+    }
+    if (trades == 0) {                                // the snake order itself: no table
+        D->entries.push_back({units, ctas, nullptr, nullptr});
+        return;
+    }
+    std::vector<int32_t> ptr((size_t)ctas + 1, 0), tiles;
+    tiles.reserve((size_t)total);
+    for (int64_t b = 0; b < ctas; ++b) {
+        auto& l = lists[(size_t)b];
+        if (l.size() > (size_t)kMaxCtaTiles) return;
+        std::sort(l.begin(), l.end());
+        for (int64_t k : l) tiles.push_back(tile_of[(size_t)k]);
+        ptr[(size_t)b + 1] = (int32_t)tiles.size();
+    }
+    int32_t *dp = nullptr, *dt = nullptr;
+    cudaError_t err = cudaMalloc(&dp, sizeof(int32_t) * ptr.size());
+    if (err == cudaSuccess) err = cudaMalloc(&dt, sizeof(int32_t) * tiles.size());
+    if (err == cudaSuccess) err = cudaMemcpy(dp, ptr.data(), sizeof(int32_t) * ptr.size(), cudaMemcpyHostToDevice);
+    if (err == cudaSuccess)
+        err = cudaMemcpy(dt, tiles.data(), sizeof(int32_t) * tiles.size(), cudaMemcpyHostToDevice);
+    if (err != cudaSuccess) {
+        cudaFree(dp);
+        cudaFree(dt);
+        cudaGetLastError();                           // the snake order serves instead
+        return;
+    }
+    D->entries.push_back({units, ctas, dp, dt});
+    a.deal_ptr = dp;
+    a.deal_tiles = dt;
 }
 
 }  // namespace
@@ -1369,6 +1546,7 @@ int launch_band_hops(const diffuser_graph* g, const BandPlan& p, int64_t units, 
     a.gpart = reinterpret_cast<float*>(ws + L.gpart);
     a.status = g->d_status;
     a.out = static_cast<__nv_bfloat16*>(out);
+    band_deal(g, p, units, band_ctas(units * p.tiles), stream, a);
     // Z_{k+1} of hop k lives in z[k & 1]; hop k reads Z_k (V for k = 0)
     for (int32_t k = 0; k < hops; ++k) {
         const bool first = k == 0, last = k == hops - 1;

@@ -58,6 +58,7 @@ struct BwdLayout {
 namespace dfs {
 struct ReplayCache;
 struct BlockDeals;
+struct BandDeals;
 }
 
 struct diffuser_graph {
@@ -98,6 +99,7 @@ struct diffuser_graph {
     int64_t blk_chunks = 0;
     std::vector<int32_t> h_blk_tile_ptr, h_blk_order;   // host copies of the two lists above
     dfs::BlockDeals* blk_deals = nullptr;   // per (B H, CTAs): the tiles dealt to the CTAs (block_path.cu)
+    dfs::BandDeals* band_deals = nullptr;   // the same for the band path's hop kernel (band_hop.cu)
     int* d_status = nullptr;
     int* h_status = nullptr;          // page-locked, mapped host mirror of the word
     dfs::ReplayCache* replay = nullptr;   // captured band-path forwards (see abi.cu)
@@ -234,6 +236,8 @@ struct BlockLayout {
 bool block_eligible(const diffuser_graph* g);
 int build_block_tiles(diffuser_graph* g);      // from the host CSR copy; no-op for other graphs
 void destroy_block_deals(BlockDeals* d);
+BandDeals* create_band_deals();                // null on allocation failure (snake order then)
+void destroy_band_deals(BandDeals* d);
 int plan_block_layout(const diffuser_graph* g, int64_t units, BlockLayout* L);
 // the score pass (row max and sum) and the hops; launch_block_forward runs both
 int launch_block_scores(const diffuser_graph* g, int64_t units, const void* Q, const void* K, char* ws,

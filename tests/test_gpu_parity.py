@@ -302,6 +302,38 @@ def test_replayed_forward_matches_direct(dl):
     assert dl.diffuser_graph_status(g) == 0
 
 
+def test_band_dealing_table_and_snake_order_agree(dl):
+    # The band hop kernel's tiles go to the CTAs through a deal table (the snake
+    # order, then trades between the busiest and the least busy CTA), built on the
+    # first forward with a given B*H outside stream capture; a forward issued while
+    # the caller's stream is capturing deals them in snake order.  Each tile is
+    # computed by one CTA in a fixed order either way (the global rows' shares are
+    # added in tile order), so the two outputs agree bit for bit.  The text-like
+    # shape (24 units of 32 tiles on 152 CTAs) is one where the two dealings differ.
+    import torch
+    g = dl.diffuser_build_graph(4096, 256, 16, rand_per_row=32)
+    assert dl.diffuser_kernels_for(g, dl.DIFFUSER_DTYPE_BF16) == dl.DIFFUSER_KERNELS_BAND
+    # a plain forward with another B*H first: the one-time set-up happens outside
+    # the capture below, and no table exists yet for B*H = 24
+    Q1, K1, V1 = (to_device(x, "bf16") for x in synthetic.qkv(1, 1, 4096, 64, "bf16", seed=10))
+    dl.diffuser_forward(Q1, K1, V1, g, 5, 0.1)
+    torch.cuda.synchronize()
+    B, H = 2, 12
+    Q, K, V = (to_device(x, "bf16") for x in synthetic.qkv(B, H, 4096, 64, "bf16", seed=12))
+    ws = dl.alloc_workspace(dl.diffuser_workspace_size(g, B, H, 64, dl.DIFFUSER_DTYPE_BF16))
+    out_snake = torch.empty_like(V)
+    side = torch.cuda.Stream()
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cg, stream=side):
+        dl.diffuser_forward(Q, K, V, g, 5, 0.1, out=out_snake, workspace=ws)
+    cg.replay()
+    torch.cuda.synchronize()
+    out_deal = dl.diffuser_forward(Q, K, V, g, 5, 0.1)
+    torch.cuda.synchronize()
+    assert dl.diffuser_graph_status(g) == 0
+    assert torch.equal(out_snake, out_deal)
+
+
 def test_bad_workspace_launches_nothing(dl):
     import torch
     g = dl.diffuser_build_graph(256, 8, 1, rand_per_row=2)
