@@ -1120,7 +1120,8 @@ hop_gather_kernel(HopArgs a) {
         // this lane's features of row j of Z_k: fp32 rows, features 4 ql .. +3 and
         // 32 + 4 ql .. +3 at zrow + 16 j (two 128-byte lines per quarter); the first
         // hop's bf16 V rows, features 8 ql .. +7 at vrow + 8 j (one line per quarter).
-        // The accumulators hold the same features, in the same order.
+        // The accumulators hold the same features, in the same order.  The rows are
+        // read past L1 (.cg): few of them are read twice by one SM.
         const uint4* zrow = reinterpret_cast<const uint4*>(a.Zf_in) + ubase * 16 + ql;
         const uint4* vrow = reinterpret_cast<const uint4*>(a.V) + ubase * 8 + ql;
         float4* prow = reinterpret_cast<float4*>(a.Psum) + ubase * 16 + (kHop0 ? 2 * ql : ql);
@@ -1161,10 +1162,10 @@ hop_gather_kernel(HopArgs a) {
             for (int b = 0; b < kB; ++b) {
                 const int j = __shfl_sync(qmask, jc, b, 8);
                 if (kHop0) {
-                    zr[b][0] = __ldg(vrow + 8 * j);
+                    zr[b][0] = __ldcg(vrow + 8 * j);
                 } else {
-                    zr[b][0] = __ldg(zrow + 16 * j);
-                    zr[b][kHop0 ? 0 : 1] = __ldg(zrow + 16 * j + 8);
+                    zr[b][0] = __ldcg(zrow + 16 * j);
+                    zr[b][kHop0 ? 0 : 1] = __ldcg(zrow + 16 * j + 8);
                 }
             }
             if (e0 + kB <= nb) {
