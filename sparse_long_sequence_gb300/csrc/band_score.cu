@@ -155,7 +155,7 @@ score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
             uint4 qB = rB < cnt ? __ldg(Qu + (size_t)rB * 8) : qA;
             uint4 kA[8], kB[8];
 #pragma unroll
-            for (int b = 0; b < 8; ++b) kA[b] = __ldg(Ku + (size_t)__shfl_sync(qmask, jA, b, 8) * 8);
+            for (int b = 0; b < 8; ++b) kA[b] = __ldcg(Ku + (size_t)__shfl_sync(qmask, jA, b, 8) * 8);
             float mrow = -INFINITY;               // this lane's running max of row rA
             // one batch: batch B's k rows load into kn while batch A's (in kc) are
             // used; the two arrays swap roles from one batch to the next
@@ -165,7 +165,7 @@ score_sparse_kernel(ScoreArgs a, const __nv_bfloat16* __restrict__ Q,
                 const int32_t jC = cols(rC, eC);
                 const uint4 qC = (rC < cnt && rC != rB) ? __ldg(Qu + (size_t)rC * 8) : qB;
 #pragma unroll
-                for (int b = 0; b < 8; ++b) kn[b] = __ldg(Ku + (size_t)__shfl_sync(qmask, jB, b, 8) * 8);
+                for (int b = 0; b < 8; ++b) kn[b] = __ldcg(Ku + (size_t)__shfl_sync(qmask, jB, b, 8) * 8);
                 // batch A: 8 partial dot products (pairs of features on packed FMAs;
                 // bf16 products are exact in fp32), reduced across the quarter
                 const float2 q01 = make_float2(bf16lo(qA.x), bf16hi(qA.x));
