@@ -38,6 +38,10 @@ sys.path.insert(0, ROOT)
 from sparse_long_sequence_gb300 import synthetic, workloads  # noqa: E402
 
 METRIC = "edge-hops/sec for diffuser_forward (n=4096, K=5); % of GB300 HBM roofline"
+# the arithmetic of each kernel family (diffuser_kernels_for: CSR, band, block)
+ARITH = ("fp32 SIMT (CSR path)",
+         "A and Z_k as bf16 hi + lo pairs on the tensor cores (window, globals), fp32 gathers and accumulation",
+         "A and Z_k as bf16 hi + lo pairs on the tensor cores (every 64 x 64 block)")
 UNIT = "edge-hops/s"
 L2_FLUSH_BYTES = 256 << 20          # > 129 MB of L2
 FALLBACK_HBM_GBS = 6800.0
@@ -557,8 +561,7 @@ def run_ours(args, w) -> None:
             "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
             "config": bench_config(w, world),
             "details": {"nnz": g.nnz, "units_per_gpu": w.units,
-                        "arith": ("A and Z_k as bf16 hi + lo pairs on the tensor cores (window, globals), "
-                                  "fp32 gathers and accumulation" if band else "fp32 SIMT (CSR path)")},
+                        "arith": ARITH[dl.diffuser_kernels_for(g, code) - 1]},
             "checked": {**checked, "device_status": 0,
                         "what": "graph status word read after the warm-up + timed steps and after the "
                                 "later passes (a bounded wait that gave up would set it); one sampled "
