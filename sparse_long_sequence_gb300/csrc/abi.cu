@@ -700,6 +700,8 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_t_ptr);
     cudaFree(g->d_t_row);
     cudaFree(g->d_t_edge);
+    cudaFree(g->d_wp0);
+    cudaFree(g->d_tw0);
     cudaFree(g->d_blk_chunks);
     cudaFree(g->d_blk_tile_ptr);
     cudaFree(g->d_blk_order);
@@ -782,6 +784,7 @@ int diffuser_backward(const void* Q, const void* K, const void* V, const void* d
         }
         return launch_backward_csr(g, B * H, Q, K, V, dOut, dtype, hops, alpha, dQ, dK, dV,
                                    static_cast<char*>(workspace), L,
+                                   g_path.load() != DIFFUSER_PATH_CSR,
                                    static_cast<cudaStream_t>(stream));
     } catch (...) {
         return fail(DIFFUSER_ERR_ALLOC, "unexpected exception");

@@ -1,33 +1,37 @@
-// Backward pass on the CSR path: the gradients dQ, dK, dV of <dOut, Z_K>
-// ("Diffuser: modelling long sequences with multi-hop attention diffusion",
-// sec 2.6: training runs the same unrolled K-hop recursion, and the gradient
-// flows back through every round of aggregation into the weights and from
-// there into the scores).  fp32 arithmetic throughout; any graph, either I/O
-// dtype.  With G_K = dOut, after recomputing A and Z_1 .. Z_{K-1} with the
-// forward's own kernels, for k = K-1 .. 0:
+// Backward pass: the gradients dQ, dK, dV of <dOut, Z_K> ("Diffuser:
+// modelling long sequences with multi-hop attention diffusion", sec 2.6:
+// training runs the same unrolled K-hop recursion, and the gradient flows back
+// through every round of aggregation into the weights and from there into the
+// scores).  fp32 arithmetic throughout; any graph, either I/O dtype.  With
+// G_K = dOut, after recomputing A and Z_1 .. Z_{K-1}, for k = K-1 .. 0:
 //
-//  * bwd_weight_grad_kernel (warp per row i, 32 edges per round; lane l holds
-//    features 2l, 2l+1 of G_{k+1}[i] and reads the same two features of every
-//    edge's Z_k row, one coalesced line per row; a butterfly over the lanes
-//    leaves edge t's dot product with lane t):
-//    dA_e += (1 - alpha) G_{k+1}[i] . Z_k[j]  for e = (i, j);
-//  * bwd_hop_t_kernel (warp per key j over its incoming edges, the transposed
-//    graph; lanes own feature pairs):  G_k[j] = (1 - alpha) sum_e A_e G_{k+1}[i],
-//    and dV_acc[j] += alpha G_{k+1}[j]; at k = 0 it writes dV = dV_acc + G_0
-//    instead of G_0 (Z_0 = V).
+//    dA_e += (1 - alpha) G_{k+1}[i] . Z_k[j]          for every edge e = (i, j);
+//    G_k[j] = (1 - alpha) sum_e A_e G_{k+1}[i]         (the transposed graph),
+//    dV_acc[j] += alpha G_{k+1}[j]                     (dV = dV_acc + G_0 at k = 0);
 //
-// then the softmax and the scores:
+// then the softmax and the scores: dS_e = A_e (dA_e - sum_t A_t dA_t) / sqrt(64)
+// (in place over dA), dQ_i = sum_e dS_e k_j and dK_j = sum_e dS_e q_i.
 //
-//  * bwd_softmax_dq_kernel (warp per row i):  dS_e = A_e (dA_e - sum_t A_t dA_t)
-//    / sqrt(64), stored over dA, and dQ_i = sum_e dS_e k_j;
-//  * bwd_dk_kernel (warp per key j over its incoming edges):  dK_j = sum_e dS_e q_i.
-//
-// Every sum runs in a fixed order (edges ascending within a row; incoming
-// edges by ascending row within a key), so the result is deterministic.
+// Two kinds of kernels share the edges.  On a token graph with a plain window
+// (dilation 1) row i holds the keys lo(i) .. hi(i) of its window as one run of
+// its CSR row (at wp0[i]), and key j the rows whose windows hold it as one run
+// of its transposed list (at tw0[j]).  The band kernels take those runs as
+// dense tiles: a CTA stages 64 rows of the operand and the weights of a 64 x 64
+// block of the window in shared memory, and each thread accumulates a register
+// tile (products A Z and A^T G: 8 rows x 2 features per lane; dA: 4 rows x 4
+// keys per thread).  The CSR kernels (a warp per row or key, lanes own two
+// features, one coalesced operand row per edge) take the other edges -- the
+// globals outside the window, the random extras, the global rows' other keys
+// -- and add the band kernels' partial sums before their epilogue; on other
+// graphs (and with the CSR path forced) they take every edge.  Every sum runs
+// in a fixed order (window keys ascending, then the other edges in CSR or
+// transposed order), so the result is deterministic.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
+#include <vector>
 
 #include "internal.h"
 
@@ -46,6 +50,12 @@ __device__ __forceinline__ float2 load2(const __nv_bfloat16* p) {
     const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
     return make_float2(bf16lo(w), bf16hi(w));
 }
+// Four adjacent features of a row, widened to fp32.
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    return make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
+}
 __device__ __forceinline__ void store2(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
 __device__ __forceinline__ void store2(__nv_bfloat16* p, float2 v) {
     *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
@@ -57,10 +67,351 @@ struct BwdArgs {
     const int64_t* t_ptr;     // transposed graph: incoming edges of key j at t_ptr[j] .. t_ptr[j+1]-1
     const int32_t* t_row;     // their rows i, ascending
     const int64_t* t_edge;    // their CSR edge ids e
+    const int64_t* wp0;       // [n] CSR position of row i's window run; null: no band kernels
+    const int64_t* tw0;       // [n] transposed-list position of key j's window run
     int64_t n, nnz, units;
+    int32_t r, causal;        // the window: keys i - r .. i + r (.. i when causal), clipped
 };
 
-// dA_e += keep * G[i] . Z[j] over the edges of row i (G: G_{k+1}, Z: Z_k).
+// The keys lo .. hi of row i's window, and the rows lo .. hi whose windows hold key j.
+__device__ __forceinline__ void win_row(const BwdArgs& a, int64_t i, int64_t& lo, int64_t& hi) {
+    lo = i - a.r > 0 ? i - a.r : 0;
+    hi = a.causal ? i : (i + a.r < a.n - 1 ? i + a.r : a.n - 1);
+}
+__device__ __forceinline__ void win_key(const BwdArgs& a, int64_t j, int64_t& lo, int64_t& hi) {
+    lo = a.causal ? j : (j - a.r > 0 ? j - a.r : 0);
+    hi = j + a.r < a.n - 1 ? j + a.r : a.n - 1;
+}
+// The window run [s0, s1) of row i's CSR edges (key j's transposed list) that the
+// band kernels take; empty without them.
+__device__ __forceinline__ void row_run(const BwdArgs& a, int64_t i, int64_t e0, int64_t& s0, int64_t& s1) {
+    if (!a.wp0) { s0 = s1 = e0; return; }
+    int64_t lo, hi;
+    win_row(a, i, lo, hi);
+    s0 = a.wp0[i];
+    s1 = s0 + (hi - lo + 1);
+}
+__device__ __forceinline__ void key_run(const BwdArgs& a, int64_t j, int64_t t0, int64_t& s0, int64_t& s1) {
+    if (!a.tw0) { s0 = s1 = t0; return; }
+    int64_t lo, hi;
+    win_key(a, j, lo, hi);
+    s0 = a.tw0[j];
+    s1 = s0 + (hi - lo + 1);
+}
+// position v of the edges e0 .. e1-1 outside the run [s0, s1)
+__device__ __forceinline__ int64_t rest_pos(int64_t e0, int64_t v, int64_t s0, int64_t s1) {
+    const int64_t e = e0 + v;
+    return e >= s0 ? e + (s1 - s0) : e;
+}
+
+// ---------------------------------------------------------------- band kernels
+constexpr int kTile = 64;              // rows (keys) of a band tile
+constexpr int kChunk = 64;             // keys (rows) of a staged chunk
+constexpr int kBandThreads = 256;
+constexpr int kWStride = kChunk + 4;   // a staged weight row (float4-aligned)
+constexpr int kMaxRange = 1088;        // rows of a key tile whose runs are staged in shared memory
+constexpr int kXPer = kChunk * (kHeadDim / 4) / kBandThreads;   // float4s of X a thread stages (dA)
+static_assert(kXPer * kBandThreads == kChunk * (kHeadDim / 4), "staging shares");
+
+// A chunk's 64 operand rows (first .. first + 63, zero past last) as fp32 in xs:
+// every load issued before the first store.
+template <int kThreads, typename TX>
+__device__ __forceinline__ void stage_rows(float (*xs)[kHeadDim], const TX* Xu, int64_t first, int64_t last,
+                                           int tid) {
+    constexpr int kPer = kChunk * (kHeadDim / 4) / kThreads;
+    float4 v[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int idx = tid + kThreads * q, rr = idx >> 4, f4 = idx & 15;
+        const int64_t j = first + rr;
+        v[q] = j <= last ? load4(Xu + j * kHeadDim + 4 * f4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int idx = tid + kThreads * q, rr = idx >> 4, f4 = idx & 15;
+        *reinterpret_cast<float4*>(&xs[rr][4 * f4]) = v[q];
+    }
+}
+
+// P[i] = sum over the keys j of row i's window of W[e(i, j)] X[j], e(i, j) =
+// wp0[i] + j - lo(i).  A CTA: 64 rows of one unit; warp w rows 8w .. 8w+7, lane l
+// features 2l, 2l+1; the tile's keys in chunks of 64, ascending.
+template <typename TX>
+__global__ void __launch_bounds__(kBandThreads)
+bwd_band_rows_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restrict__ X, float* __restrict__ P) {
+    __shared__ __align__(16) float xs[kChunk][kHeadDim];
+    __shared__ __align__(16) float ws[kTile][kWStride];
+    __shared__ int64_t s_lo[kTile], s_hi[kTile], s_wp[kTile];   // the tile rows' windows and runs
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t tiles = (a.n + kTile - 1) / kTile;
+    const int64_t u = blockIdx.x / tiles, i0 = (blockIdx.x - u * tiles) * kTile;
+    const int64_t ilast = i0 + kTile - 1 < a.n - 1 ? i0 + kTile - 1 : a.n - 1;
+    int64_t klo, khi, tmp;
+    win_row(a, i0, klo, tmp);
+    win_row(a, ilast, tmp, khi);
+    if (tid < kTile) {
+        const int64_t i = i0 + tid;
+        int64_t lo = 1, hi = 0, wp = 0;            // rows past n: an empty window
+        if (i <= ilast) { win_row(a, i, lo, hi); wp = a.wp0[i]; }
+        s_lo[tid] = lo; s_hi[tid] = hi; s_wp[tid] = wp;
+    }
+    const float* Wu = W + (size_t)u * a.nnz;
+    const TX* Xu = X + (size_t)u * a.n * kHeadDim;
+    float2 acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = make_float2(0.f, 0.f);
+    constexpr int kWPer = kTile * kChunk / kBandThreads;
+    for (int64_t k0 = klo; k0 <= khi; k0 += kChunk) {
+        __syncthreads();                          // the previous chunk has been used
+        stage_rows<kBandThreads>(xs, Xu, k0, khi, tid);
+        {
+            const int kk = tid & (kChunk - 1);
+            const int64_t j = k0 + kk;
+            float wv[kWPer];
+#pragma unroll
+            for (int q = 0; q < kWPer; ++q) {
+                const int rr = (tid >> 6) + (kBandThreads / kChunk) * q;
+                const int64_t lo = s_lo[rr];
+                wv[q] = (j >= lo && j <= s_hi[rr]) ? Wu[s_wp[rr] + (j - lo)] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < kWPer; ++q) ws[(tid >> 6) + (kBandThreads / kChunk) * q][kk] = wv[q];
+        }
+        __syncthreads();
+#pragma unroll 2
+        for (int kk = 0; kk < kChunk; kk += 4) {
+            float2 z[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) z[q] = *reinterpret_cast<const float2*>(&xs[kk + q][2 * lane]);
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+                const float4 w4 = *reinterpret_cast<const float4*>(&ws[8 * warp + rr][kk]);
+                acc[rr] = __ffma2_rn(make_float2(w4.x, w4.x), z[0], acc[rr]);
+                acc[rr] = __ffma2_rn(make_float2(w4.y, w4.y), z[1], acc[rr]);
+                acc[rr] = __ffma2_rn(make_float2(w4.z, w4.z), z[2], acc[rr]);
+                acc[rr] = __ffma2_rn(make_float2(w4.w, w4.w), z[3], acc[rr]);
+            }
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+        const int64_t i = i0 + 8 * warp + rr;
+        if (i < a.n) store2(P + ((size_t)u * a.n + i) * kHeadDim + 2 * lane, acc[rr]);
+    }
+}
+
+// P[j] = sum over the rows i whose windows hold key j of W[e(i, j)] X[i].  A CTA:
+// 64 keys of one unit; warp w keys 8w .. 8w+7, lane l features 2l, 2l+1; the rows
+// in chunks of 64, ascending.  The runs wp0 of the tile's rows are staged once
+// when there are at most kMaxRange of them.
+template <typename TX>
+__global__ void __launch_bounds__(kBandThreads)
+bwd_band_keys_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restrict__ X, float* __restrict__ P) {
+    __shared__ __align__(16) float xs[kChunk][kHeadDim];
+    __shared__ __align__(16) float ws[kChunk][kWStride];   // [row of the chunk][key of the tile]
+    __shared__ int64_t s_wp[kMaxRange];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t tiles = (a.n + kTile - 1) / kTile;
+    const int64_t u = blockIdx.x / tiles, j0 = (blockIdx.x - u * tiles) * kTile;
+    const int64_t jlast = j0 + kTile - 1 < a.n - 1 ? j0 + kTile - 1 : a.n - 1;
+    int64_t rlo, rhi, tmp;
+    win_key(a, j0, rlo, tmp);
+    win_key(a, jlast, tmp, rhi);
+    const bool staged = rhi - rlo + 1 <= kMaxRange;
+    if (staged)
+        for (int64_t i = rlo + tid; i <= rhi; i += kBandThreads) s_wp[i - rlo] = a.wp0[i];
+    const float* Wu = W + (size_t)u * a.nnz;
+    const TX* Xu = X + (size_t)u * a.n * kHeadDim;
+    float2 acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = make_float2(0.f, 0.f);
+    constexpr int kWPer = kChunk * kTile / kBandThreads;
+    for (int64_t r0 = rlo; r0 <= rhi; r0 += kChunk) {
+        __syncthreads();
+        stage_rows<kBandThreads>(xs, Xu, r0, rhi, tid);
+        {
+            const int kk = tid & (kTile - 1);
+            const int64_t j = j0 + kk;
+            float wv[kWPer];
+#pragma unroll
+            for (int q = 0; q < kWPer; ++q) {
+                const int64_t i = r0 + (tid >> 6) + (kBandThreads / kTile) * q;
+                int64_t lo, hi;
+                win_row(a, i, lo, hi);
+                const bool in = i <= rhi && j < a.n && j >= lo && j <= hi;
+                wv[q] = in ? Wu[(staged ? s_wp[i - rlo] : a.wp0[i]) + (j - lo)] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < kWPer; ++q) ws[(tid >> 6) + (kBandThreads / kTile) * q][kk] = wv[q];
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int rr = 0; rr < kChunk; ++rr) {
+            const float2 x = *reinterpret_cast<const float2*>(&xs[rr][2 * lane]);
+            const float4 wa = *reinterpret_cast<const float4*>(&ws[rr][8 * warp]);
+            const float4 wb = *reinterpret_cast<const float4*>(&ws[rr][8 * warp + 4]);
+            acc[0] = __ffma2_rn(make_float2(wa.x, wa.x), x, acc[0]);
+            acc[1] = __ffma2_rn(make_float2(wa.y, wa.y), x, acc[1]);
+            acc[2] = __ffma2_rn(make_float2(wa.z, wa.z), x, acc[2]);
+            acc[3] = __ffma2_rn(make_float2(wa.w, wa.w), x, acc[3]);
+            acc[4] = __ffma2_rn(make_float2(wb.x, wb.x), x, acc[4]);
+            acc[5] = __ffma2_rn(make_float2(wb.y, wb.y), x, acc[5]);
+            acc[6] = __ffma2_rn(make_float2(wb.z, wb.z), x, acc[6]);
+            acc[7] = __ffma2_rn(make_float2(wb.w, wb.w), x, acc[7]);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int64_t j = j0 + 8 * warp + q;
+        if (j < a.n) store2(P + ((size_t)u * a.n + j) * kHeadDim + 2 * lane, acc[q]);
+    }
+}
+
+// A chunk's 64 operand rows, feature-major (xt[f][r]; rows fastest across the
+// threads, so the transposing stores are conflict-free), zero past last.
+template <typename TX>
+__device__ __forceinline__ void stage_rows_t(float (*xt)[kWStride], const TX* Xu, int64_t first, int64_t last,
+                                             int tid) {
+    float4 v[kXPer];
+#pragma unroll
+    for (int q = 0; q < kXPer; ++q) {
+        const int idx = tid + kBandThreads * q, rr = idx & (kChunk - 1), f4 = idx / kChunk;
+        const int64_t j = first + rr;
+        v[q] = j <= last ? load4(Xu + j * kHeadDim + 4 * f4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < kXPer; ++q) {
+        const int idx = tid + kBandThreads * q, rr = idx & (kChunk - 1), f4 = idx / kChunk;
+        xt[4 * f4][rr] = v[q].x; xt[4 * f4 + 1][rr] = v[q].y; xt[4 * f4 + 2][rr] = v[q].z; xt[4 * f4 + 3][rr] = v[q].w;
+    }
+}
+
+// dA[e(i, j)] += keep * G[i] . Z[j] over the windows of 64 rows of one unit: the
+// rows' G staged once (feature-major), the keys' Z in chunks of 64 (feature-major);
+// thread (ty, tx) computes rows 4ty .. +3 x keys 4tx .. +3 of each chunk.
+template <typename TG, typename TZ>
+__global__ void __launch_bounds__(kBandThreads)
+bwd_band_sddmm_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict__ Z, float* __restrict__ dA,
+                      float keep) {
+    __shared__ __align__(16) float gs[kHeadDim][kWStride];  // [feature][row]
+    __shared__ __align__(16) float zs[kHeadDim][kWStride];  // [feature][key]
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int64_t tiles = (a.n + kTile - 1) / kTile;
+    const int64_t u = blockIdx.x / tiles, i0 = (blockIdx.x - u * tiles) * kTile;
+    const int64_t ilast = i0 + kTile - 1 < a.n - 1 ? i0 + kTile - 1 : a.n - 1;
+    int64_t klo, khi, tmp;
+    win_row(a, i0, klo, tmp);
+    win_row(a, ilast, tmp, khi);
+    const TG* Gu = G + (size_t)u * a.n * kHeadDim;
+    const TZ* Zu = Z + (size_t)u * a.n * kHeadDim;
+    float* dAu = dA + (size_t)u * a.nnz;
+    stage_rows_t(gs, Gu, i0, ilast, tid);
+    // this thread's rows: window bounds and runs
+    int64_t rlo[4], rhi[4], rp0[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int64_t i = i0 + 4 * ty + q;
+        rlo[q] = 1; rhi[q] = 0; rp0[q] = 0;
+        if (i <= ilast) { win_row(a, i, rlo[q], rhi[q]); rp0[q] = a.wp0[i]; }
+    }
+    for (int64_t k0 = klo; k0 <= khi; k0 += kChunk) {
+        __syncthreads();
+        stage_rows_t(zs, Zu, k0, khi, tid);
+        __syncthreads();
+        float acc[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[q][c] = 0.f;
+#pragma unroll 8
+        for (int f = 0; f < kHeadDim; ++f) {
+            const float4 g4 = *reinterpret_cast<const float4*>(&gs[f][4 * ty]);
+            const float4 z4 = *reinterpret_cast<const float4*>(&zs[f][4 * tx]);
+            const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 gg = make_float2(gv[q], gv[q]);
+                float2 lo2 = make_float2(acc[q][0], acc[q][1]), hi2 = make_float2(acc[q][2], acc[q][3]);
+                lo2 = __ffma2_rn(gg, make_float2(z4.x, z4.y), lo2);
+                hi2 = __ffma2_rn(gg, make_float2(z4.z, z4.w), hi2);
+                acc[q][0] = lo2.x; acc[q][1] = lo2.y; acc[q][2] = hi2.x; acc[q][3] = hi2.y;
+            }
+        }
+        // the 16 read-modify-writes: every load issued before the first store (the
+        // positions are distinct)
+        float old[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int64_t j = k0 + 4 * tx + c;
+                old[q][c] = (j >= rlo[q] && j <= rhi[q]) ? dAu[rp0[q] + (j - rlo[q])] : 0.f;
+            }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int64_t j = k0 + 4 * tx + c;
+                if (j >= rlo[q] && j <= rhi[q]) dAu[rp0[q] + (j - rlo[q])] = fmaf(keep, acc[q][c], old[q][c]);
+            }
+    }
+}
+
+// ---------------------------------------------------------------- CSR kernels
+// (the edges outside the window runs; all edges without band kernels).  32 edges
+// a round: the round's 32 operand rows are requested before the first is used, and
+// the next round's edge indices and weights load while they are in flight.
+
+// Recomputed hop: Y[i] = (1 - alpha) (P[i] + sum_e A_e X[j]) + alpha V[i] (P: the
+// band kernel's window sum, or null).
+template <typename TX, typename TV>
+__global__ void __launch_bounds__(kBwdWarps * 32)
+bwd_hop_rows_kernel(BwdArgs a, const float* __restrict__ A, const TX* __restrict__ X,
+                    const float* __restrict__ P, const TV* __restrict__ V, float* __restrict__ Y, float alpha) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
+    if (gw >= a.units * a.n) return;
+    const int64_t u = gw / a.n, i = gw - u * a.n;
+    const size_t unit = (size_t)u * a.n * kHeadDim;
+    const TX* Xu = X + unit + 2 * lane;
+    const float* Au = A + (size_t)u * a.nnz;
+    const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+    int64_t s0, s1;
+    row_run(a, i, e0, s0, s1);
+    const int64_t len = (e1 - e0) - (s1 - s0);
+    const size_t at = unit + (size_t)i * kHeadDim + 2 * lane;
+    float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
+    bool ok = lane < len;
+    int64_t e = rest_pos(e0, lane, s0, s1);
+    float w_l = ok ? Au[e] : 0.f;
+    int32_t j_l = ok ? a.col[e] : 0;
+    for (int64_t vb = 0; vb < len; vb += 32) {
+        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
+        float2 z[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            const int32_t j = __shfl_sync(0xffffffffu, j_l, t);
+            z[t] = t < cnt ? load2(Xu + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
+        }
+        const float w_c = w_l;
+        ok = vb + 32 + lane < len;
+        e = rest_pos(e0, vb + 32 + lane, s0, s1);
+        w_l = ok ? Au[e] : 0.f;
+        j_l = ok ? a.col[e] : 0;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            const float w = __shfl_sync(0xffffffffu, w_c, t);
+            acc.x = fmaf(w, z[t].x, acc.x);
+            acc.y = fmaf(w, z[t].y, acc.y);
+        }
+    }
+    const float keep = 1.f - alpha;
+    const float2 v = load2(V + at);
+    store2(Y + at, make_float2(fmaf(keep, acc.x, alpha * v.x), fmaf(keep, acc.y, alpha * v.y)));
+}
+
+// dA_e += keep * G[i] . Z[j] over the edges of row i (G: G_{k+1}, Z: Z_k; and, for
+// the recomputed raw scores, G = Q, Z = K, keep = 1/8 on a zeroed A).
 template <typename TG, typename TZ>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 bwd_weight_grad_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict__ Z,
@@ -71,33 +422,42 @@ bwd_weight_grad_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict
     const int64_t u = gw / a.n, i = gw - u * a.n;
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+    int64_t s0, s1;
+    row_run(a, i, e0, s0, s1);
+    const int64_t len = (e1 - e0) - (s1 - s0);
     const float2 g = load2(G + unit + (size_t)i * kHeadDim + 2 * lane);
     const TZ* Zu = Z + unit + 2 * lane;
     float* dAu = dA + (size_t)u * a.nnz;
-    for (int64_t base = e0; base < e1; base += 32) {
-        const int64_t e = base + lane;
-        const int32_t j_l = e < e1 ? a.col[e] : 0;
-        const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
-        float p[32];        // all 32 rows requested before the first is used
+    bool ok = lane < len;
+    int64_t e = rest_pos(e0, lane, s0, s1);
+    int32_t j_l = ok ? a.col[e] : 0;
+    for (int64_t vb = 0; vb < len; vb += 32) {
+        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
+        float p[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
             const int32_t j = __shfl_sync(0xffffffffu, j_l, t);
             const float2 z = t < cnt ? load2(Zu + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
             p[t] = fmaf(g.x, z.x, g.y * z.y);
         }
-        const float dot = warp_transpose_sum32(p, lane);             // edge base + lane
-        if (e < e1) dAu[e] += keep * dot;
+        const bool ok_c = ok;
+        const int64_t e_c = e;
+        ok = vb + 32 + lane < len;
+        e = rest_pos(e0, vb + 32 + lane, s0, s1);
+        j_l = ok ? a.col[e] : 0;
+        const float dot = warp_transpose_sum32(p, lane);             // edge vb + lane
+        if (ok_c) dAu[e_c] += keep * dot;
     }
 }
 
-// Key j of the transposed hop: Gn[j] = keep * sum_{e = (i, j)} A_e G[i]; and
-// dV_acc[j] = (first ? 0 : dV_acc[j]) + alpha G[j].  With dV_out set (k = 0),
+// Key j of the transposed hop: Gn[j] = keep * (P[j] + sum_{e = (i, j)} A_e G[i]);
+// and dV_acc[j] = (first ? 0 : dV_acc[j]) + alpha G[j].  With dV_out set (k = 0),
 // dV_out[j] = dV_acc[j] + alpha G[j] + Gn[j] in the I/O dtype and Gn is not written.
 template <typename TG, typename TIo>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ G,
-                 float* __restrict__ Gn, float* __restrict__ dV_acc, TIo* __restrict__ dV_out,
-                 float alpha, bool first) {
+                 const float* __restrict__ P, float* __restrict__ Gn, float* __restrict__ dV_acc,
+                 TIo* __restrict__ dV_out, float alpha, bool first) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
@@ -106,27 +466,36 @@ bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ 
     const TG* Gu = G + unit + 2 * lane;
     const float* Au = A + (size_t)u * a.nnz;
     const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
-    float2 acc = make_float2(0.f, 0.f);
-    for (int64_t base = t0; base < t1; base += 32) {
-        const int64_t t = base + lane;
-        const float w_l = t < t1 ? Au[a.t_edge[t]] : 0.f;
-        const int32_t i_l = t < t1 ? a.t_row[t] : 0;
-        const int cnt = (t1 - base) < 32 ? (int)(t1 - base) : 32;
-        float2 gv[32];        // all 32 rows requested before the first is used
+    int64_t s0, s1;
+    key_run(a, j, t0, s0, s1);
+    const int64_t len = (t1 - t0) - (s1 - s0);
+    const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
+    float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
+    bool ok = lane < len;
+    int64_t t = rest_pos(t0, lane, s0, s1);
+    float w_l = ok ? Au[a.t_edge[t]] : 0.f;
+    int32_t i_l = ok ? a.t_row[t] : 0;
+    for (int64_t vb = 0; vb < len; vb += 32) {
+        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
+        float2 gv[32];
 #pragma unroll
         for (int s = 0; s < 32; ++s) {
             const int32_t i = __shfl_sync(0xffffffffu, i_l, s);
             gv[s] = s < cnt ? load2(Gu + (size_t)i * kHeadDim) : make_float2(0.f, 0.f);
         }
+        const float w_c = w_l;
+        ok = vb + 32 + lane < len;
+        t = rest_pos(t0, vb + 32 + lane, s0, s1);
+        w_l = ok ? Au[a.t_edge[t]] : 0.f;
+        i_l = ok ? a.t_row[t] : 0;
 #pragma unroll
         for (int s = 0; s < 32; ++s) {
-            const float w = __shfl_sync(0xffffffffu, w_l, s);
+            const float w = __shfl_sync(0xffffffffu, w_c, s);
             acc.x = fmaf(w, gv[s].x, acc.x);
             acc.y = fmaf(w, gv[s].y, acc.y);
         }
     }
     const float keep = 1.f - alpha;
-    const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
     const float2 gj = load2(G + at);
     float2 dv = first ? make_float2(0.f, 0.f) : load2(dV_acc + at);
     dv.x = fmaf(alpha, gj.x, dv.x);
@@ -140,17 +509,34 @@ bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ 
     }
 }
 
-// Row i: dS_e = A_e (dA_e - sum_t A_t dA_t) * scale in place over dA, then
-// dQ_i = sum_e dS_e K[j] in the I/O dtype.
-template <typename TIo>
+// Row i: the recomputed weights A_e = exp(s_e - m_i) / sum_t exp(s_t - m_i) from
+// the raw scores s in A (in place), m_i the row's largest score.
 __global__ void __launch_bounds__(kBwdWarps * 32)
-bwd_softmax_dq_kernel(BwdArgs a, const float* __restrict__ A, float* __restrict__ dA,
-                      const TIo* __restrict__ K, TIo* __restrict__ dQ) {
+bwd_scores_softmax_kernel(BwdArgs a, float* __restrict__ A) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
     const int64_t u = gw / a.n, i = gw - u * a.n;
-    const size_t unit = (size_t)u * a.n * kHeadDim;
+    float* Au = A + (size_t)u * a.nnz;
+    const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+    float m = -INFINITY;
+    for (int64_t e = e0 + lane; e < e1; e += 32) m = fmaxf(m, Au[e]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float l = 0.f;
+    for (int64_t e = e0 + lane; e < e1; e += 32) l += expf(Au[e] - m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    for (int64_t e = e0 + lane; e < e1; e += 32) Au[e] = expf(Au[e] - m) / l;
+}
+
+// Row i: dS_e = A_e (dA_e - sum_t A_t dA_t) * scale, in place over dA.
+__global__ void __launch_bounds__(kBwdWarps * 32)
+bwd_softmax_kernel(BwdArgs a, const float* __restrict__ A, float* __restrict__ dA) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
+    if (gw >= a.units * a.n) return;
+    const int64_t u = gw / a.n, i = gw - u * a.n;
     const float* Au = A + (size_t)u * a.nnz;
     float* dAu = dA + (size_t)u * a.nnz;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
@@ -158,39 +544,59 @@ bwd_softmax_dq_kernel(BwdArgs a, const float* __restrict__ A, float* __restrict_
     for (int64_t e = e0 + lane; e < e1; e += 32) dot = fmaf(Au[e], dAu[e], dot);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    const TIo* Ku = K + unit + 2 * lane;
-    float2 acc = make_float2(0.f, 0.f);
-    for (int64_t base = e0; base < e1; base += 32) {
-        const int64_t e = base + lane;
-        float ds_l = 0.f;
-        int32_t j_l = 0;
-        if (e < e1) {
-            ds_l = Au[e] * (dAu[e] - dot) * kScale;
-            dAu[e] = ds_l;
-            j_l = a.col[e];
-        }
-        const int cnt = (e1 - base) < 32 ? (int)(e1 - base) : 32;
-        float2 kv[32];        // all 32 rows requested before the first is used
+    for (int64_t e = e0 + lane; e < e1; e += 32) dAu[e] = Au[e] * (dAu[e] - dot) * kScale;
+}
+
+// Row i: out[i] = P[i] + sum_e W_e X[j] in the I/O dtype (dQ = dS K).
+template <typename TIo>
+__global__ void __launch_bounds__(kBwdWarps * 32)
+bwd_rows_out_kernel(BwdArgs a, const float* __restrict__ W, const TIo* __restrict__ X,
+                    const float* __restrict__ P, TIo* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
+    if (gw >= a.units * a.n) return;
+    const int64_t u = gw / a.n, i = gw - u * a.n;
+    const size_t unit = (size_t)u * a.n * kHeadDim;
+    const TIo* Xu = X + unit + 2 * lane;
+    const float* Wu = W + (size_t)u * a.nnz;
+    const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+    int64_t s0, s1;
+    row_run(a, i, e0, s0, s1);
+    const int64_t len = (e1 - e0) - (s1 - s0);
+    const size_t at = unit + (size_t)i * kHeadDim + 2 * lane;
+    float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
+    bool ok = lane < len;
+    int64_t e = rest_pos(e0, lane, s0, s1);
+    float w_l = ok ? Wu[e] : 0.f;
+    int32_t j_l = ok ? a.col[e] : 0;
+    for (int64_t vb = 0; vb < len; vb += 32) {
+        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
+        float2 xv[32];
 #pragma unroll
         for (int s = 0; s < 32; ++s) {
             const int32_t j = __shfl_sync(0xffffffffu, j_l, s);
-            kv[s] = s < cnt ? load2(Ku + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
+            xv[s] = s < cnt ? load2(Xu + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
         }
+        const float w_c = w_l;
+        ok = vb + 32 + lane < len;
+        e = rest_pos(e0, vb + 32 + lane, s0, s1);
+        w_l = ok ? Wu[e] : 0.f;
+        j_l = ok ? a.col[e] : 0;
 #pragma unroll
         for (int s = 0; s < 32; ++s) {
-            const float w = __shfl_sync(0xffffffffu, ds_l, s);
-            acc.x = fmaf(w, kv[s].x, acc.x);
-            acc.y = fmaf(w, kv[s].y, acc.y);
+            const float w = __shfl_sync(0xffffffffu, w_c, s);
+            acc.x = fmaf(w, xv[s].x, acc.x);
+            acc.y = fmaf(w, xv[s].y, acc.y);
         }
     }
-    store2(dQ + unit + (size_t)i * kHeadDim + 2 * lane, acc);
+    store2(out + at, acc);
 }
 
-// Key j: dK_j = sum_{e = (i, j)} dS_e Q[i] in the I/O dtype.
+// Key j: dK_j = P[j] + sum_{e = (i, j)} dS_e Q[i] in the I/O dtype.
 template <typename TIo>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 bwd_dk_kernel(BwdArgs a, const float* __restrict__ dS, const TIo* __restrict__ Q,
-              TIo* __restrict__ dK) {
+              const float* __restrict__ P, TIo* __restrict__ dK) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
@@ -199,26 +605,36 @@ bwd_dk_kernel(BwdArgs a, const float* __restrict__ dS, const TIo* __restrict__ Q
     const float* dSu = dS + (size_t)u * a.nnz;
     const TIo* Qu = Q + unit + 2 * lane;
     const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
-    float2 acc = make_float2(0.f, 0.f);
-    for (int64_t base = t0; base < t1; base += 32) {
-        const int64_t t = base + lane;
-        const float w_l = t < t1 ? dSu[a.t_edge[t]] : 0.f;
-        const int32_t i_l = t < t1 ? a.t_row[t] : 0;
-        const int cnt = (t1 - base) < 32 ? (int)(t1 - base) : 32;
-        float2 qv[32];        // all 32 rows requested before the first is used
+    int64_t s0, s1;
+    key_run(a, j, t0, s0, s1);
+    const int64_t len = (t1 - t0) - (s1 - s0);
+    const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
+    float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
+    bool ok = lane < len;
+    int64_t t = rest_pos(t0, lane, s0, s1);
+    float w_l = ok ? dSu[a.t_edge[t]] : 0.f;
+    int32_t i_l = ok ? a.t_row[t] : 0;
+    for (int64_t vb = 0; vb < len; vb += 32) {
+        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
+        float2 qv[32];
 #pragma unroll
         for (int s = 0; s < 32; ++s) {
             const int32_t i = __shfl_sync(0xffffffffu, i_l, s);
             qv[s] = s < cnt ? load2(Qu + (size_t)i * kHeadDim) : make_float2(0.f, 0.f);
         }
+        const float w_c = w_l;
+        ok = vb + 32 + lane < len;
+        t = rest_pos(t0, vb + 32 + lane, s0, s1);
+        w_l = ok ? dSu[a.t_edge[t]] : 0.f;
+        i_l = ok ? a.t_row[t] : 0;
 #pragma unroll
         for (int s = 0; s < 32; ++s) {
-            const float w = __shfl_sync(0xffffffffu, w_l, s);
+            const float w = __shfl_sync(0xffffffffu, w_c, s);
             acc.x = fmaf(w, qv[s].x, acc.x);
             acc.y = fmaf(w, qv[s].y, acc.y);
         }
     }
-    store2(dK + unit + (size_t)j * kHeadDim + 2 * lane, acc);
+    store2(dK + at, acc);
 }
 
 unsigned bwd_grid(const BwdArgs& a) {
@@ -236,13 +652,17 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
                    float alpha, TIo* dQ, TIo* dK, TIo* dV, char* ws, const BwdLayout& L,
                    cudaStream_t stream) {
     const dim3 grid(bwd_grid(a)), block(kBwdWarps * 32);
+    const bool band = a.wp0 != nullptr;
+    const dim3 bgrid((unsigned)(a.units * ((a.n + kTile - 1) / kTile))), bblock(kBandThreads);
     const size_t io = (size_t)a.units * a.n * kHeadDim * sizeof(TIo);
     float* A = reinterpret_cast<float*>(ws + L.a);
     float* dA = reinterpret_cast<float*>(ws + L.da);
     float* dVacc = reinterpret_cast<float*>(ws + L.dv);
+    float* P = band ? reinterpret_cast<float*>(ws + L.p) : nullptr;   // the band kernels' window sums
     float* Gbuf[2] = {reinterpret_cast<float*>(ws + L.g[0]), reinterpret_cast<float*>(ws + L.g[1])};
     auto zstate = [&](int32_t k) { return reinterpret_cast<float*>(ws + L.z + (size_t)(k - 1) * L.z_stride); };
     cudaError_t err;
+    int st;
     if (hops == 0) {
         // Z_K = V: dV = dOut, and nothing reaches the weights
         err = cudaMemcpyAsync(dV, dOut, io, cudaMemcpyDeviceToDevice, stream);
@@ -250,12 +670,34 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         if (err == cudaSuccess) err = cudaMemsetAsync(dK, 0, io, stream);
         return err == cudaSuccess ? DIFFUSER_OK : cuda_fail(err, "backward with hops = 0");
     }
-    // the forward's weights and states Z_1 .. Z_{K-1} (Z_0 is V)
-    int st = launch_score_csr(ca, Q, K, dtype, A, stream);
-    for (int32_t k = 1; k < hops && st == DIFFUSER_OK; ++k)
-        st = launch_hop_csr(ca, A, k == 1 ? static_cast<const void*>(V) : zstate(k - 1), k == 1, V,
-                            zstate(k), false, dtype, alpha, stream);
-    if (st != DIFFUSER_OK) return st;
+    // one launch scope per kernel (the launch counters and per-kernel events)
+    auto hop = [&](auto&& launch) { LaunchScope scope(DIFFUSER_KERNEL_HOP, stream); launch(); };
+    auto score = [&](auto&& launch) { LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream); launch(); };
+    // the forward's weights (on the band path: raw scores of the window runs as
+    // tiles, of the other edges by the CSR kernel, then each row's softmax) and
+    // states Z_1 .. Z_{K-1} (Z_0 is V)
+    if (band) {
+        err = cudaMemsetAsync(A, 0, (size_t)a.units * a.nnz * sizeof(float), stream);
+        if (err != cudaSuccess) return cuda_fail(err, "clearing A");
+        score([&] { bwd_band_sddmm_kernel<TIo, TIo><<<bgrid, bblock, 0, stream>>>(a, Q, K, A, kScale); });
+        score([&] { bwd_weight_grad_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, Q, K, A, kScale); });
+        score([&] { bwd_scores_softmax_kernel<<<grid, block, 0, stream>>>(a, A); });
+        if ((st = launched("bwd_scores_softmax_kernel"))) return st;
+    } else if ((st = launch_score_csr(ca, Q, K, dtype, A, stream))) {
+        return st;
+    }
+    for (int32_t k = 1; k < hops; ++k) {
+        if (k == 1) {
+            if (band) hop([&] { bwd_band_rows_kernel<TIo><<<bgrid, bblock, 0, stream>>>(a, A, V, P); });
+            hop([&] { bwd_hop_rows_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, A, V, P, V, zstate(k), alpha); });
+        } else {
+            if (band) hop([&] { bwd_band_rows_kernel<float><<<bgrid, bblock, 0, stream>>>(a, A, zstate(k - 1), P); });
+            hop([&] {
+                bwd_hop_rows_kernel<float, TIo><<<grid, block, 0, stream>>>(a, A, zstate(k - 1), P, V, zstate(k), alpha);
+            });
+        }
+        if ((st = launched("bwd_hop_rows_kernel"))) return st;
+    }
     err = cudaMemsetAsync(dA, 0, (size_t)a.units * a.nnz * sizeof(float), stream);
     if (err != cudaSuccess) return cuda_fail(err, "clearing dA");
     const float keep = 1.f - alpha;
@@ -263,45 +705,84 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         const bool top = (k == hops - 1);            // G_{k+1} is dOut itself
         float* Gn = Gbuf[k & 1];
         const float* Gf = Gbuf[(k + 1) & 1];         // G_{k+1} for k < hops - 1
-        {
-            LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
-            if (top && k == 0)
-                bwd_weight_grad_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, dOut, V, dA, keep);
-            else if (top)
-                bwd_weight_grad_kernel<TIo, float><<<grid, block, 0, stream>>>(a, dOut, zstate(k), dA, keep);
-            else if (k == 0)
-                bwd_weight_grad_kernel<float, TIo><<<grid, block, 0, stream>>>(a, Gf, V, dA, keep);
-            else
-                bwd_weight_grad_kernel<float, float><<<grid, block, 0, stream>>>(a, Gf, zstate(k), dA, keep);
+        if (top && k == 0) {
+            if (band) hop([&] { bwd_band_sddmm_kernel<TIo, TIo><<<bgrid, bblock, 0, stream>>>(a, dOut, V, dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, dOut, V, dA, keep); });
+        } else if (top) {
+            if (band)
+                hop([&] { bwd_band_sddmm_kernel<TIo, float><<<bgrid, bblock, 0, stream>>>(a, dOut, zstate(k), dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<TIo, float><<<grid, block, 0, stream>>>(a, dOut, zstate(k), dA, keep); });
+        } else if (k == 0) {
+            if (band) hop([&] { bwd_band_sddmm_kernel<float, TIo><<<bgrid, bblock, 0, stream>>>(a, Gf, V, dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<float, TIo><<<grid, block, 0, stream>>>(a, Gf, V, dA, keep); });
+        } else {
+            if (band)
+                hop([&] { bwd_band_sddmm_kernel<float, float><<<bgrid, bblock, 0, stream>>>(a, Gf, zstate(k), dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<float, float><<<grid, block, 0, stream>>>(a, Gf, zstate(k), dA, keep); });
         }
         if ((st = launched("bwd_weight_grad_kernel"))) return st;
-        {
-            LaunchScope scope(DIFFUSER_KERNEL_HOP, stream);
-            TIo* out = k == 0 ? dV : nullptr;
-            if (top)
-                bwd_hop_t_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, A, dOut, Gn, dVacc, out, alpha, true);
-            else
-                bwd_hop_t_kernel<float, TIo><<<grid, block, 0, stream>>>(a, A, Gf, Gn, dVacc, out, alpha, false);
+        TIo* out = k == 0 ? dV : nullptr;
+        if (top) {
+            if (band) hop([&] { bwd_band_keys_kernel<TIo><<<bgrid, bblock, 0, stream>>>(a, A, dOut, P); });
+            hop([&] {
+                bwd_hop_t_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, A, dOut, P, Gn, dVacc, out, alpha, true);
+            });
+        } else {
+            if (band) hop([&] { bwd_band_keys_kernel<float><<<bgrid, bblock, 0, stream>>>(a, A, Gf, P); });
+            hop([&] {
+                bwd_hop_t_kernel<float, TIo><<<grid, block, 0, stream>>>(a, A, Gf, P, Gn, dVacc, out, alpha, false);
+            });
         }
         if ((st = launched("bwd_hop_t_kernel"))) return st;
     }
-    {
-        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
-        bwd_softmax_dq_kernel<TIo><<<grid, block, 0, stream>>>(a, A, dA, K, dQ);
-    }
-    if ((st = launched("bwd_softmax_dq_kernel"))) return st;
-    {
-        LaunchScope scope(DIFFUSER_KERNEL_SCORE, stream);
-        bwd_dk_kernel<TIo><<<grid, block, 0, stream>>>(a, dA, Q, dK);
-    }
+    score([&] { bwd_softmax_kernel<<<grid, block, 0, stream>>>(a, A, dA); });
+    if (band) score([&] { bwd_band_rows_kernel<TIo><<<bgrid, bblock, 0, stream>>>(a, dA, K, P); });
+    score([&] { bwd_rows_out_kernel<TIo><<<grid, block, 0, stream>>>(a, dA, K, P, dQ); });
+    if ((st = launched("bwd_rows_out_kernel"))) return st;
+    if (band) score([&] { bwd_band_keys_kernel<TIo><<<bgrid, bblock, 0, stream>>>(a, dA, Q, P); });
+    score([&] { bwd_dk_kernel<TIo><<<grid, block, 0, stream>>>(a, dA, Q, P, dK); });
     return launched("bwd_dk_kernel");
 }
 
 }  // namespace
 
+// The window runs of a token graph with a plain window: wp0[i], the CSR position
+// of key lo(i) in row i, and tw0[j], the transposed-list position of row lo'(j)
+// in key j's list (the same bounds as win_row / win_key).  False, and nothing
+// kept, unless every run holds consecutive keys (rows).
+bool window_runs(const diffuser_graph* g, const std::vector<int64_t>& t_ptr,
+                 const std::vector<int32_t>& t_row, std::vector<int64_t>& wp0, std::vector<int64_t>& tw0) {
+    if (g->kind != kTokenGraph || g->dilation != 1 || g->n < 1) return false;
+    const int64_t n = g->n, r = g->r;
+    wp0.assign((size_t)n, 0);
+    tw0.assign((size_t)n, 0);
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t lo = i - r > 0 ? i - r : 0, hi = g->causal ? i : std::min(i + r, n - 1);
+        const int32_t* b = g->h_col.data() + g->h_row_ptr[i];
+        const int32_t* e = g->h_col.data() + g->h_row_ptr[i + 1];
+        const int32_t* at = std::lower_bound(b, e, (int32_t)lo);
+        if (e - at < hi - lo + 1) return false;
+        for (int64_t k = 0; k <= hi - lo; ++k)
+            if (at[k] != lo + k) return false;
+        wp0[(size_t)i] = at - g->h_col.data();
+    }
+    for (int64_t j = 0; j < n; ++j) {
+        const int64_t lo = g->causal ? j : (j - r > 0 ? j - r : 0), hi = std::min(j + r, n - 1);
+        const int32_t* b = t_row.data() + t_ptr[(size_t)j];
+        const int32_t* e = t_row.data() + t_ptr[(size_t)j + 1];
+        const int32_t* at = std::lower_bound(b, e, (int32_t)lo);
+        if (e - at < hi - lo + 1) return false;
+        for (int64_t k = 0; k <= hi - lo; ++k)
+            if (at[k] != lo + k) return false;
+        tw0[(size_t)j] = at - t_row.data();
+    }
+    return true;
+}
+
 // The transposed graph (incoming edges of every key, rows ascending), built on
-// the host from the CSR copy by a counting sort and uploaded (synchronously).
-// On failure the arrays allocated so far are freed and d_t_ptr stays null.
+// the host from the CSR copy by a counting sort and uploaded (synchronously),
+// with the window runs where the graph has them.  On failure the arrays
+// allocated so far are freed and d_t_ptr stays null.
 int build_transposed_graph(diffuser_graph* g) {
     const int64_t n = g->n, nnz = g->nnz;
     std::vector<int64_t> t_ptr(n + 1, 0);
@@ -317,9 +798,13 @@ int build_transposed_graph(diffuser_graph* g) {
             t_edge[at] = e;
         }
     }
+    std::vector<int64_t> wp0, tw0;
+    const bool runs = window_runs(g, t_ptr, t_row, wp0, tw0);
     int64_t* d_ptr = nullptr;
     int32_t* d_row = nullptr;
     int64_t* d_edge = nullptr;
+    int64_t* d_wp0 = nullptr;
+    int64_t* d_tw0 = nullptr;
     cudaError_t err = cudaMalloc(&d_ptr, sizeof(int64_t) * (n + 1));
     if (err == cudaSuccess) err = cudaMalloc(&d_row, sizeof(int32_t) * t_row.size());
     if (err == cudaSuccess) err = cudaMalloc(&d_edge, sizeof(int64_t) * t_edge.size());
@@ -329,12 +814,24 @@ int build_transposed_graph(diffuser_graph* g) {
         err = cudaMemcpy(d_row, t_row.data(), sizeof(int32_t) * t_row.size(), cudaMemcpyHostToDevice);
     if (err == cudaSuccess)
         err = cudaMemcpy(d_edge, t_edge.data(), sizeof(int64_t) * t_edge.size(), cudaMemcpyHostToDevice);
+    if (runs) {
+        if (err == cudaSuccess) err = cudaMalloc(&d_wp0, sizeof(int64_t) * (size_t)n);
+        if (err == cudaSuccess) err = cudaMalloc(&d_tw0, sizeof(int64_t) * (size_t)n);
+        if (err == cudaSuccess)
+            err = cudaMemcpy(d_wp0, wp0.data(), sizeof(int64_t) * (size_t)n, cudaMemcpyHostToDevice);
+        if (err == cudaSuccess)
+            err = cudaMemcpy(d_tw0, tw0.data(), sizeof(int64_t) * (size_t)n, cudaMemcpyHostToDevice);
+    }
     if (err != cudaSuccess) {
         cudaFree(d_ptr);
         cudaFree(d_row);
         cudaFree(d_edge);
+        cudaFree(d_wp0);
+        cudaFree(d_tw0);
         return cuda_fail(err, "building the transposed graph");
     }
+    g->d_wp0 = d_wp0;
+    g->d_tw0 = d_tw0;
     g->d_t_row = d_row;
     g->d_t_edge = d_edge;
     g->d_t_ptr = d_ptr;      // set last: non-null means the transposed graph is complete
@@ -342,8 +839,9 @@ int build_transposed_graph(diffuser_graph* g) {
 }
 
 int plan_backward_layout(const diffuser_graph* g, int64_t units, int32_t hops, BwdLayout* L) {
-    // A, dA: [units][nnz] fp32; dV_acc, G (x2), Z_1 .. Z_{K-1}: [units][n][64] fp32
-    const double states = 3.0 + (hops > 1 ? hops - 1 : 0);
+    // A, dA: [units][nnz] fp32; dV_acc, G (x2), the band kernels' window sums P,
+    // Z_1 .. Z_{K-1}: [units][n][64] fp32
+    const double states = 4.0 + (hops > 1 ? hops - 1 : 0);
     const double need = (double)units * (2.0 * 4.0 * (double)g->nnz +
                                          states * 4.0 * kHeadDim * (double)g->n);
     if (need > 4.0e18) return fail(DIFFUSER_ERR_OVERFLOW, "backward workspace size overflows size_t");
@@ -356,6 +854,7 @@ int plan_backward_layout(const diffuser_graph* g, int64_t units, int32_t hops, B
     L->dv = off; off += state;
     L->g[0] = off; off += state;
     L->g[1] = off; off += state;
+    L->p = off; off += state;
     L->z = off;
     L->z_stride = state;
     off += (hops > 1 ? (size_t)(hops - 1) : 0) * state;
@@ -365,9 +864,12 @@ int plan_backward_layout(const diffuser_graph* g, int64_t units, int32_t hops, B
 
 int launch_backward_csr(const diffuser_graph* g, int64_t units, const void* Q, const void* K,
                         const void* V, const void* dOut, int32_t dtype, int32_t hops, float alpha,
-                        void* dQ, void* dK, void* dV, char* ws, const BwdLayout& L,
+                        void* dQ, void* dK, void* dV, char* ws, const BwdLayout& L, bool band,
                         cudaStream_t stream) {
-    BwdArgs a{g->d_row_ptr, g->d_col, g->d_t_ptr, g->d_t_row, g->d_t_edge, g->n, g->nnz, units};
+    const bool runs = band && g->d_wp0 && g->d_tw0;
+    BwdArgs a{g->d_row_ptr, g->d_col, g->d_t_ptr, g->d_t_row, g->d_t_edge,
+              runs ? g->d_wp0 : nullptr, runs ? g->d_tw0 : nullptr, g->n, g->nnz, units,
+              g->r, g->causal ? 1 : 0};
     CsrArgs ca{g->d_row_ptr, g->d_col, g->n, g->nnz, units};
     if (dtype == DIFFUSER_DTYPE_BF16) {
         using T = __nv_bfloat16;

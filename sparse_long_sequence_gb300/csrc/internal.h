@@ -49,6 +49,7 @@ struct BwdLayout {
     size_t a, da;       // weights A and their gradient dA (then dS), [units][nnz]
     size_t dv;          // the dV accumulator, [units][n][64]
     size_t g[2];        // G_k, the gradient reaching Z_k, ping-pong, [units][n][64]
+    size_t p;           // the band kernels' window sums, [units][n][64]
     size_t z, z_stride; // Z_1 .. Z_{K-1}, each [units][n][64]
     size_t total;
 };
@@ -88,6 +89,8 @@ struct diffuser_graph {
     int64_t* d_t_ptr = nullptr;       // [n+1]
     int32_t* d_t_row = nullptr;       // [nnz] row i of each incoming edge
     int64_t* d_t_edge = nullptr;      // [nnz] its CSR edge id
+    int64_t* d_wp0 = nullptr;         // [n] token graph, plain window: CSR position of row i's window run
+    int64_t* d_tw0 = nullptr;         // [n] ... and transposed-list position of key j's (null otherwise)
     // status block written by kernels: the word (0 = ok) at [0], the device
     // address of h_status at byte 8 (a bounded wait that gives up writes both)
     // block graph with 64-token blocks: each 128-row tile's key blocks, paired into
@@ -224,7 +227,7 @@ int build_transposed_graph(diffuser_graph* g);   // from the host CSR copy
 int plan_backward_layout(const diffuser_graph* g, int64_t units, int32_t hops, BwdLayout* L);
 int launch_backward_csr(const diffuser_graph* g, int64_t units, const void* Q, const void* K,
                         const void* V, const void* dOut, int32_t dtype, int32_t hops, float alpha,
-                        void* dQ, void* dK, void* dV, char* ws, const BwdLayout& L,
+                        void* dQ, void* dK, void* dV, char* ws, const BwdLayout& L, bool band,
                         cudaStream_t stream);
 
 // ---- block-sparse path (block_path.cu): block graphs of 64-token blocks, bf16 I/O
