@@ -69,6 +69,9 @@ struct BwdArgs {
     const int64_t* t_edge;    // their CSR edge ids e
     const int64_t* wp0;       // [n] CSR position of row i's window run; null: no band kernels
     const int64_t* tw0;       // [n] transposed-list position of key j's window run
+    const int32_t* row_order; // [n] the heavy rows by falling edge count, then the others ascending
+    const int32_t* key_order; // [n] the same for the keys and their incoming edges
+    int64_t heavy_rows, heavy_keys;   // how many come first in each order
     int64_t n, nnz, units;
     int32_t r, causal;        // the window: keys i - r .. i + r (.. i when causal), clipped
 };
@@ -98,6 +101,22 @@ __device__ __forceinline__ void key_run(const BwdArgs& a, int64_t j, int64_t t0,
     s0 = a.tw0[j];
     s1 = s0 + (hi - lo + 1);
 }
+// The (unit, row) of CSR warp gw: the heavy rows (or keys) of every unit first,
+// heaviest first, every unit's copy in turn, so that their long lists start with
+// the launch; then the other rows unit by unit in order.
+__device__ __forceinline__ void warp_item(const BwdArgs& a, int64_t gw, const int32_t* order, int64_t heavy,
+                                          int64_t& u, int64_t& i) {
+    if (gw < a.units * heavy) {
+        const int64_t rk = gw / a.units;
+        u = gw - rk * a.units;
+        i = order[rk];
+    } else {
+        const int64_t g2 = gw - a.units * heavy, rest = a.n - heavy;
+        u = g2 / rest;
+        i = order[heavy + (g2 - u * rest)];
+    }
+}
+
 // position v of the edges e0 .. e1-1 outside the run [s0, s1)
 __device__ __forceinline__ int64_t rest_pos(int64_t e0, int64_t v, int64_t s0, int64_t s1) {
     const int64_t e = e0 + v;
@@ -360,7 +379,9 @@ bwd_band_sddmm_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict_
 // ---------------------------------------------------------------- CSR kernels
 // (the edges outside the window runs; all edges without band kernels).  32 edges
 // a round: the round's 32 operand rows are requested before the first is used, and
-// the next round's edge indices and weights load while they are in flight.
+// the next round's edge indices and weights load while they are in flight.  The
+// warps take the heavy rows (keys) first (warp_item), so that the global rows'
+// long lists start with the launch instead of ending it.
 
 // Recomputed hop: Y[i] = (1 - alpha) (P[i] + sum_e A_e X[j]) + alpha V[i] (P: the
 // band kernel's window sum, or null).
@@ -371,7 +392,8 @@ bwd_hop_rows_kernel(BwdArgs a, const float* __restrict__ A, const TX* __restrict
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
-    const int64_t u = gw / a.n, i = gw - u * a.n;
+    int64_t u, i;
+    warp_item(a, gw, a.row_order, a.heavy_rows, u, i);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const TX* Xu = X + unit + 2 * lane;
     const float* Au = A + (size_t)u * a.nnz;
@@ -419,7 +441,8 @@ bwd_weight_grad_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
-    const int64_t u = gw / a.n, i = gw - u * a.n;
+    int64_t u, i;
+    warp_item(a, gw, a.row_order, a.heavy_rows, u, i);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     int64_t s0, s1;
@@ -461,7 +484,8 @@ bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ 
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
-    const int64_t u = gw / a.n, j = gw - u * a.n;
+    int64_t u, j;
+    warp_item(a, gw, a.key_order, a.heavy_keys, u, j);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const TG* Gu = G + unit + 2 * lane;
     const float* Au = A + (size_t)u * a.nnz;
@@ -516,7 +540,8 @@ bwd_scores_softmax_kernel(BwdArgs a, float* __restrict__ A) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
-    const int64_t u = gw / a.n, i = gw - u * a.n;
+    int64_t u, i;
+    warp_item(a, gw, a.row_order, a.heavy_rows, u, i);
     float* Au = A + (size_t)u * a.nnz;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     float m = -INFINITY;
@@ -536,7 +561,8 @@ bwd_softmax_kernel(BwdArgs a, const float* __restrict__ A, float* __restrict__ d
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
-    const int64_t u = gw / a.n, i = gw - u * a.n;
+    int64_t u, i;
+    warp_item(a, gw, a.row_order, a.heavy_rows, u, i);
     const float* Au = A + (size_t)u * a.nnz;
     float* dAu = dA + (size_t)u * a.nnz;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
@@ -555,7 +581,8 @@ bwd_rows_out_kernel(BwdArgs a, const float* __restrict__ W, const TIo* __restric
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
-    const int64_t u = gw / a.n, i = gw - u * a.n;
+    int64_t u, i;
+    warp_item(a, gw, a.row_order, a.heavy_rows, u, i);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const TIo* Xu = X + unit + 2 * lane;
     const float* Wu = W + (size_t)u * a.nnz;
@@ -600,7 +627,8 @@ bwd_dk_kernel(BwdArgs a, const float* __restrict__ dS, const TIo* __restrict__ Q
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (gw >= a.units * a.n) return;
-    const int64_t u = gw / a.n, j = gw - u * a.n;
+    int64_t u, j;
+    warp_item(a, gw, a.key_order, a.heavy_keys, u, j);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const float* dSu = dS + (size_t)u * a.nnz;
     const TIo* Qu = Q + unit + 2 * lane;
@@ -800,12 +828,31 @@ int build_transposed_graph(diffuser_graph* g) {
     }
     std::vector<int64_t> wp0, tw0;
     const bool runs = window_runs(g, t_ptr, t_row, wp0, tw0);
+    // the heavy rows (keys): more than twice the mean edge count, heaviest first
+    // (ties: ascending index), then the others in ascending order
+    auto order_of = [&](auto len, std::vector<int32_t>& order) -> int64_t {
+        std::vector<int32_t> heavy, light;
+        for (int64_t i = 0; i < n; ++i) (len(i) * n > 2 * nnz ? heavy : light).push_back((int32_t)i);
+        std::stable_sort(heavy.begin(), heavy.end(), [&](int32_t x, int32_t y) { return len(x) > len(y); });
+        order = heavy;
+        order.insert(order.end(), light.begin(), light.end());
+        return (int64_t)heavy.size();
+    };
+    std::vector<int32_t> row_order, key_order;
+    const int64_t heavy_rows = order_of([&](int64_t i) { return g->h_row_ptr[i + 1] - g->h_row_ptr[i]; }, row_order);
+    const int64_t heavy_keys = order_of([&](int64_t j) { return t_ptr[(size_t)j + 1] - t_ptr[(size_t)j]; }, key_order);
     int64_t* d_ptr = nullptr;
     int32_t* d_row = nullptr;
     int64_t* d_edge = nullptr;
     int64_t* d_wp0 = nullptr;
     int64_t* d_tw0 = nullptr;
+    int32_t* d_orders = nullptr;             // [2][n]: row_order, key_order
     cudaError_t err = cudaMalloc(&d_ptr, sizeof(int64_t) * (n + 1));
+    if (err == cudaSuccess) err = cudaMalloc(&d_orders, sizeof(int32_t) * 2 * (size_t)n);
+    if (err == cudaSuccess)
+        err = cudaMemcpy(d_orders, row_order.data(), sizeof(int32_t) * (size_t)n, cudaMemcpyHostToDevice);
+    if (err == cudaSuccess)
+        err = cudaMemcpy(d_orders + n, key_order.data(), sizeof(int32_t) * (size_t)n, cudaMemcpyHostToDevice);
     if (err == cudaSuccess) err = cudaMalloc(&d_row, sizeof(int32_t) * t_row.size());
     if (err == cudaSuccess) err = cudaMalloc(&d_edge, sizeof(int64_t) * t_edge.size());
     if (err == cudaSuccess)
@@ -828,8 +875,12 @@ int build_transposed_graph(diffuser_graph* g) {
         cudaFree(d_edge);
         cudaFree(d_wp0);
         cudaFree(d_tw0);
+        cudaFree(d_orders);
         return cuda_fail(err, "building the transposed graph");
     }
+    g->d_orders = d_orders;
+    g->heavy_rows = heavy_rows;
+    g->heavy_keys = heavy_keys;
     g->d_wp0 = d_wp0;
     g->d_tw0 = d_tw0;
     g->d_t_row = d_row;
@@ -868,8 +919,8 @@ int launch_backward_csr(const diffuser_graph* g, int64_t units, const void* Q, c
                         cudaStream_t stream) {
     const bool runs = band && g->d_wp0 && g->d_tw0;
     BwdArgs a{g->d_row_ptr, g->d_col, g->d_t_ptr, g->d_t_row, g->d_t_edge,
-              runs ? g->d_wp0 : nullptr, runs ? g->d_tw0 : nullptr, g->n, g->nnz, units,
-              g->r, g->causal ? 1 : 0};
+              runs ? g->d_wp0 : nullptr, runs ? g->d_tw0 : nullptr, g->d_orders, g->d_orders + g->n,
+              g->heavy_rows, g->heavy_keys, g->n, g->nnz, units, g->r, g->causal ? 1 : 0};
     CsrArgs ca{g->d_row_ptr, g->d_col, g->n, g->nnz, units};
     if (dtype == DIFFUSER_DTYPE_BF16) {
         using T = __nv_bfloat16;
