@@ -151,8 +151,11 @@ def measure_backward(dl, w, g, Q, K, V, steps: int, stream, flush) -> dict:
     t = statistics.median(time_events(
         lambda: dl.diffuser_backward(Q, K, V, dO, g, w.hops, w.alpha, *grads, workspace=ws, stream=stream),
         steps, stream, flush))
-    return {"ms": t, "value": w.units * g.nnz * w.hops / (t / 1e3), "unit": UNIT,
-            "kernels": "CSR SIMT (recompute, reversed hops over the transposed edge list)"}
+    kernels = ("SIMT: the window's edges as 64 x 64 shared-memory tiles, the other edges on CSR "
+               "kernels (recompute, reversed hops over the transposed edge list)"
+               if w.kind in ("token", "causal") else
+               "CSR SIMT (recompute, reversed hops over the transposed edge list)")
+    return {"ms": t, "value": w.units * g.nnz * w.hops / (t / 1e3), "unit": UNIT, "kernels": kernels}
 
 
 # the source files of each path's hop kernels (and what they include): a traffic

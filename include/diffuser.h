@@ -266,17 +266,23 @@ DIFFUSER_API int diffuser_forward_host(const void* Q, const void* K, const void*
  *   dQ_i = sum_j dS_ij k_j / sqrt(d),  dK_j = sum_i dS_ij q_i / sqrt(d).
  * The forward's weights and states Z_1 .. Z_{K-1} are recomputed inside the
  * call.  The first backward on a graph also builds its transposed edge list
- * (on the host, then a synchronous upload: 12 bytes per edge of device memory,
- * held with the graph), so make that first call outside any stream capture.  All arithmetic is fp32 (the CSR kernels, for any graph); dQ, dK, dV
- * are written in the I/O dtype.  Sums run in a fixed order: repeated calls
- * give identical bits.  Launches count as SCORE (the recomputed weights, the
- * softmax and score gradients) and HOP (the recomputed and reversed hops).
+ * (on the host, then a synchronous upload: 12 bytes per edge and 8 per
+ * position of device memory, plus 16 per position on token graphs with a plain
+ * window, held with the graph), so make that first call outside any stream
+ * capture.  All arithmetic is fp32; dQ, dK, dV are written in the I/O dtype.
+ * On a token graph with a plain window (dilation 1) the window's edges run as
+ * 64 x 64 tiles in shared memory and the other edges (globals outside the
+ * window, random extras, the global rows' other keys) on CSR kernels; on other
+ * graphs, or with DIFFUSER_PATH_CSR selected, CSR kernels take every edge.
+ * Sums run in a fixed order: repeated calls give identical bits.  Launches
+ * count as SCORE (the recomputed weights, the softmax and score gradients) and
+ * HOP (the recomputed and reversed hops).
  *
  *   Q, K, V, dOut   device [B][H][n][d] in dtype, 16-byte aligned
  *   dQ, dK, dV      device [B][H][n][d] in dtype, written; they may not overlap
  *                   the inputs or each other
  *   workspace       diffuser_backward_workspace_size bytes, 256-byte aligned:
- *                   2 units nnz + (2 + max(K, 1)) units n 64 fp32 values
+ *                   2 units nnz + (3 + max(K, 1)) units n 64 fp32 values
  * Asynchronous on `stream`.  Errors: as diffuser_forward.
  */
 DIFFUSER_API int diffuser_backward_workspace_size(const diffuser_graph* g, int64_t B, int64_t H,
@@ -429,7 +435,7 @@ DIFFUSER_API int diffuser_diffuse_csr(const diffuser_graph* g, const float* A, c
 
 typedef enum {
     DIFFUSER_PATH_AUTO = 0,       /* band tensor-core path where eligible, else CSR */
-    DIFFUSER_PATH_CSR = 1         /* always the general CSR SIMT path */
+    DIFFUSER_PATH_CSR = 1         /* always the general CSR SIMT path (forward and backward) */
 } diffuser_path;
 
 /*
