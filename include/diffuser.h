@@ -268,12 +268,14 @@ DIFFUSER_API int diffuser_forward_host(const void* Q, const void* K, const void*
  * call.  The first backward on a graph also builds its transposed edge list
  * (on the host, then a synchronous upload: 12 bytes per edge and 8 per
  * position of device memory, plus 16 per position on token graphs with a plain
- * window, held with the graph), so make that first call outside any stream
- * capture.  All arithmetic is fp32; dQ, dK, dV are written in the I/O dtype.
+ * window or 12 per block pair on block graphs, held with the graph), so make
+ * that first call outside any stream capture.  All arithmetic is fp32; dQ, dK, dV are written in the I/O dtype.
  * On a token graph with a plain window (dilation 1) the window's edges run as
  * 64 x 64 tiles in shared memory and the other edges (globals outside the
- * window, random extras, the global rows' other keys) on CSR kernels; on other
- * graphs, or with DIFFUSER_PATH_CSR selected, CSR kernels take every edge.
+ * window, random extras, the global rows' other keys) on CSR kernels; on a
+ * block graph of 64-token blocks every edge runs as tiles, key block by key
+ * block; on other graphs, or with DIFFUSER_PATH_CSR selected, CSR kernels take
+ * every edge.
  * Sums run in a fixed order: repeated calls give identical bits.  Launches
  * count as SCORE (the recomputed weights, the softmax and score gradients) and
  * HOP (the recomputed and reversed hops).

@@ -703,6 +703,7 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_wp0);
     cudaFree(g->d_tw0);
     cudaFree(g->d_orders);
+    cudaFree(g->d_bruns);
     cudaFree(g->d_blk_chunks);
     cudaFree(g->d_blk_tile_ptr);
     cudaFree(g->d_blk_order);

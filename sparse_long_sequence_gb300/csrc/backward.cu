@@ -69,6 +69,11 @@ struct BwdArgs {
     const int64_t* t_edge;    // their CSR edge ids e
     const int64_t* wp0;       // [n] CSR position of row i's window run; null: no band kernels
     const int64_t* tw0;       // [n] transposed-list position of key j's window run
+    const int32_t* bptr;      // block graph (64-token blocks): key blocks of block row J at bcol[bptr[J] ..];
+    const int32_t* bcol;      //   null: no block runs
+    const int32_t* btptr;     // the row blocks holding key block KB at btrow[btptr[KB] ..], and the
+    const int32_t* btrow;     //   key block's place in each such row block's list
+    const int32_t* btpos;
     const int32_t* row_order; // [n] the heavy rows by falling edge count, then the others ascending
     const int32_t* key_order; // [n] the same for the keys and their incoming edges
     int64_t heavy_rows, heavy_keys;   // how many come first in each order
@@ -86,15 +91,19 @@ __device__ __forceinline__ void win_key(const BwdArgs& a, int64_t j, int64_t& lo
     hi = j + a.r < a.n - 1 ? j + a.r : a.n - 1;
 }
 // The window run [s0, s1) of row i's CSR edges (key j's transposed list) that the
-// band kernels take; empty without them.
-__device__ __forceinline__ void row_run(const BwdArgs& a, int64_t i, int64_t e0, int64_t& s0, int64_t& s1) {
+// band kernels take; empty without them, everything on a block graph.
+__device__ __forceinline__ void row_run(const BwdArgs& a, int64_t i, int64_t e0, int64_t e1, int64_t& s0,
+                                        int64_t& s1) {
+    if (a.bptr) { s0 = e0; s1 = e1; return; }
     if (!a.wp0) { s0 = s1 = e0; return; }
     int64_t lo, hi;
     win_row(a, i, lo, hi);
     s0 = a.wp0[i];
     s1 = s0 + (hi - lo + 1);
 }
-__device__ __forceinline__ void key_run(const BwdArgs& a, int64_t j, int64_t t0, int64_t& s0, int64_t& s1) {
+__device__ __forceinline__ void key_run(const BwdArgs& a, int64_t j, int64_t t0, int64_t t1, int64_t& s0,
+                                        int64_t& s1) {
+    if (a.bptr) { s0 = t0; s1 = t1; return; }
     if (!a.tw0) { s0 = s1 = t0; return; }
     int64_t lo, hi;
     win_key(a, j, lo, hi);
@@ -152,26 +161,48 @@ __device__ __forceinline__ void stage_rows(float (*xs)[kHeadDim], const TX* Xu, 
     }
 }
 
+// The tiles of a band launch: unit-major on token graphs (neighbouring tiles of a
+// unit run together); tile-major on block graphs, so that the heavy global block
+// rows (keys) of every unit start with the launch.
+__device__ __forceinline__ void tile_of(const BwdArgs& a, bool tile_major, int64_t& u, int64_t& t) {
+    const int64_t tiles = (a.n + kTile - 1) / kTile;
+    if (tile_major) { t = blockIdx.x / a.units; u = blockIdx.x - t * a.units; }
+    else { u = blockIdx.x / tiles; t = blockIdx.x - u * tiles; }
+}
+
 // P[i] = sum over the keys j of row i's window of W[e(i, j)] X[j], e(i, j) =
-// wp0[i] + j - lo(i).  A CTA: 64 rows of one unit; warp w rows 8w .. 8w+7, lane l
-// features 2l, 2l+1; the tile's keys in chunks of 64, ascending.
-template <typename TX>
+// wp0[i] + j - lo(i); on a block graph (kBlk) over the key blocks of row i's block,
+// e(i, j) = row_ptr[i] + 64 (place of j's block in the list) + j % 64.  A CTA: 64
+// rows of one unit; warp w rows 8w .. 8w+7, lane l features 2l, 2l+1; the keys in
+// chunks of 64 (the window's, or the key blocks), ascending.
+template <typename TX, bool kBlk>
 __global__ void __launch_bounds__(kBandThreads)
 bwd_band_rows_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restrict__ X, float* __restrict__ P) {
     __shared__ __align__(16) float xs[kChunk][kHeadDim];
     __shared__ __align__(16) float ws[kTile][kWStride];
     __shared__ int64_t s_lo[kTile], s_hi[kTile], s_wp[kTile];   // the tile rows' windows and runs
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t tiles = (a.n + kTile - 1) / kTile;
-    const int64_t u = blockIdx.x / tiles, i0 = (blockIdx.x - u * tiles) * kTile;
+    int64_t u, t;
+    tile_of(a, kBlk, u, t);
+    const int64_t i0 = t * kTile;
     const int64_t ilast = i0 + kTile - 1 < a.n - 1 ? i0 + kTile - 1 : a.n - 1;
-    int64_t klo, khi, tmp;
-    win_row(a, i0, klo, tmp);
-    win_row(a, ilast, tmp, khi);
+    int64_t klo = 0, khi = 0, c_begin = 0, c_end;
+    if (kBlk) {
+        c_begin = a.bptr[t];
+        c_end = a.bptr[t + 1];
+    } else {
+        int64_t tmp;
+        win_row(a, i0, klo, tmp);
+        win_row(a, ilast, tmp, khi);
+        c_end = (khi - klo) / kChunk + 1;
+    }
     if (tid < kTile) {
         const int64_t i = i0 + tid;
         int64_t lo = 1, hi = 0, wp = 0;            // rows past n: an empty window
-        if (i <= ilast) { win_row(a, i, lo, hi); wp = a.wp0[i]; }
+        if (i <= ilast) {
+            if (kBlk) { lo = 0; hi = a.n - 1; wp = a.row_ptr[i]; }
+            else { win_row(a, i, lo, hi); wp = a.wp0[i]; }
+        }
         s_lo[tid] = lo; s_hi[tid] = hi; s_wp[tid] = wp;
     }
     const float* Wu = W + (size_t)u * a.nnz;
@@ -180,9 +211,11 @@ bwd_band_rows_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restric
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = make_float2(0.f, 0.f);
     constexpr int kWPer = kTile * kChunk / kBandThreads;
-    for (int64_t k0 = klo; k0 <= khi; k0 += kChunk) {
+    for (int64_t c = c_begin; c < c_end; ++c) {
+        const int64_t k0 = kBlk ? (int64_t)a.bcol[c] * kChunk : klo + kChunk * c;
+        const int64_t kend = kBlk ? (k0 + kChunk - 1 < a.n - 1 ? k0 + kChunk - 1 : a.n - 1) : khi;
         __syncthreads();                          // the previous chunk has been used
-        stage_rows<kBandThreads>(xs, Xu, k0, khi, tid);
+        stage_rows<kBandThreads>(xs, Xu, k0, kend, tid);
         {
             const int kk = tid & (kChunk - 1);
             const int64_t j = k0 + kk;
@@ -191,7 +224,9 @@ bwd_band_rows_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restric
             for (int q = 0; q < kWPer; ++q) {
                 const int rr = (tid >> 6) + (kBandThreads / kChunk) * q;
                 const int64_t lo = s_lo[rr];
-                wv[q] = (j >= lo && j <= s_hi[rr]) ? Wu[s_wp[rr] + (j - lo)] : 0.f;
+                const bool in = j >= lo && j <= s_hi[rr] && j <= kend;
+                const int64_t at = kBlk ? s_wp[rr] + kChunk * (c - c_begin) + kk : s_wp[rr] + (j - lo);
+                wv[q] = in ? Wu[at] : 0.f;
             }
 #pragma unroll
             for (int q = 0; q < kWPer; ++q) ws[(tid >> 6) + (kBandThreads / kChunk) * q][kk] = wv[q];
@@ -219,35 +254,48 @@ bwd_band_rows_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restric
     }
 }
 
-// P[j] = sum over the rows i whose windows hold key j of W[e(i, j)] X[i].  A CTA:
-// 64 keys of one unit; warp w keys 8w .. 8w+7, lane l features 2l, 2l+1; the rows
-// in chunks of 64, ascending.  The runs wp0 of the tile's rows are staged once
-// when there are at most kMaxRange of them.
-template <typename TX>
+// P[j] = sum over the rows i whose windows (key-block lists, kBlk) hold key j of
+// W[e(i, j)] X[i].  A CTA: 64 keys of one unit; warp w keys 8w .. 8w+7, lane l
+// features 2l, 2l+1; the rows in chunks of 64 (the window rows', or the row blocks
+// holding the key block), ascending.  The runs wp0 of the tile's rows are staged
+// once when there are at most kMaxRange of them.
+template <typename TX, bool kBlk>
 __global__ void __launch_bounds__(kBandThreads)
 bwd_band_keys_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restrict__ X, float* __restrict__ P) {
     __shared__ __align__(16) float xs[kChunk][kHeadDim];
     __shared__ __align__(16) float ws[kChunk][kWStride];   // [row of the chunk][key of the tile]
     __shared__ int64_t s_wp[kMaxRange];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t tiles = (a.n + kTile - 1) / kTile;
-    const int64_t u = blockIdx.x / tiles, j0 = (blockIdx.x - u * tiles) * kTile;
+    int64_t u, t;
+    tile_of(a, kBlk, u, t);
+    const int64_t j0 = t * kTile;
     const int64_t jlast = j0 + kTile - 1 < a.n - 1 ? j0 + kTile - 1 : a.n - 1;
-    int64_t rlo, rhi, tmp;
-    win_key(a, j0, rlo, tmp);
-    win_key(a, jlast, tmp, rhi);
-    const bool staged = rhi - rlo + 1 <= kMaxRange;
-    if (staged)
-        for (int64_t i = rlo + tid; i <= rhi; i += kBandThreads) s_wp[i - rlo] = a.wp0[i];
+    int64_t rlo = 0, rhi = 0, c_begin = 0, c_end;
+    bool staged = false;
+    if (kBlk) {
+        c_begin = a.btptr[t];
+        c_end = a.btptr[t + 1];
+    } else {
+        int64_t tmp;
+        win_key(a, j0, rlo, tmp);
+        win_key(a, jlast, tmp, rhi);
+        c_end = (rhi - rlo) / kChunk + 1;
+        staged = rhi - rlo + 1 <= kMaxRange;
+        if (staged)
+            for (int64_t i = rlo + tid; i <= rhi; i += kBandThreads) s_wp[i - rlo] = a.wp0[i];
+    }
     const float* Wu = W + (size_t)u * a.nnz;
     const TX* Xu = X + (size_t)u * a.n * kHeadDim;
     float2 acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = make_float2(0.f, 0.f);
     constexpr int kWPer = kChunk * kTile / kBandThreads;
-    for (int64_t r0 = rlo; r0 <= rhi; r0 += kChunk) {
+    for (int64_t c = c_begin; c < c_end; ++c) {
+        const int64_t r0 = kBlk ? (int64_t)a.btrow[c] * kChunk : rlo + kChunk * c;
+        const int64_t rend = kBlk ? (r0 + kChunk - 1 < a.n - 1 ? r0 + kChunk - 1 : a.n - 1) : rhi;
+        const int64_t place = kBlk ? (int64_t)a.btpos[c] * kChunk : 0;
         __syncthreads();
-        stage_rows<kBandThreads>(xs, Xu, r0, rhi, tid);
+        stage_rows<kBandThreads>(xs, Xu, r0, rend, tid);
         {
             const int kk = tid & (kTile - 1);
             const int64_t j = j0 + kk;
@@ -255,10 +303,14 @@ bwd_band_keys_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restric
 #pragma unroll
             for (int q = 0; q < kWPer; ++q) {
                 const int64_t i = r0 + (tid >> 6) + (kBandThreads / kTile) * q;
-                int64_t lo, hi;
-                win_row(a, i, lo, hi);
-                const bool in = i <= rhi && j < a.n && j >= lo && j <= hi;
-                wv[q] = in ? Wu[(staged ? s_wp[i - rlo] : a.wp0[i]) + (j - lo)] : 0.f;
+                if (kBlk) {
+                    wv[q] = (i <= rend && j <= jlast) ? Wu[a.row_ptr[i] + place + kk] : 0.f;
+                } else {
+                    int64_t lo, hi;
+                    win_row(a, i, lo, hi);
+                    const bool in = i <= rend && j < a.n && j >= lo && j <= hi;
+                    wv[q] = in ? Wu[(staged ? s_wp[i - rlo] : a.wp0[i]) + (j - lo)] : 0.f;
+                }
             }
 #pragma unroll
             for (int q = 0; q < kWPer; ++q) ws[(tid >> 6) + (kBandThreads / kTile) * q][kk] = wv[q];
@@ -305,43 +357,58 @@ __device__ __forceinline__ void stage_rows_t(float (*xt)[kWStride], const TX* Xu
     }
 }
 
-// dA[e(i, j)] += keep * G[i] . Z[j] over the windows of 64 rows of one unit: the
-// rows' G staged once (feature-major), the keys' Z in chunks of 64 (feature-major);
-// thread (ty, tx) computes rows 4ty .. +3 x keys 4tx .. +3 of each chunk.
-template <typename TG, typename TZ>
+// dA[e(i, j)] += keep * G[i] . Z[j] over the windows (key-block lists, kBlk) of 64
+// rows of one unit: the rows' G staged once (feature-major), the keys' Z in chunks
+// of 64 (feature-major); thread (ty, tx) computes rows 4ty .. +3 x keys 4tx .. +3
+// of each chunk.
+template <typename TG, typename TZ, bool kBlk>
 __global__ void __launch_bounds__(kBandThreads)
 bwd_band_sddmm_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict__ Z, float* __restrict__ dA,
                       float keep) {
     __shared__ __align__(16) float gs[kHeadDim][kWStride];  // [feature][row]
     __shared__ __align__(16) float zs[kHeadDim][kWStride];  // [feature][key]
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int64_t tiles = (a.n + kTile - 1) / kTile;
-    const int64_t u = blockIdx.x / tiles, i0 = (blockIdx.x - u * tiles) * kTile;
+    int64_t u, t;
+    tile_of(a, kBlk, u, t);
+    const int64_t i0 = t * kTile;
     const int64_t ilast = i0 + kTile - 1 < a.n - 1 ? i0 + kTile - 1 : a.n - 1;
-    int64_t klo, khi, tmp;
-    win_row(a, i0, klo, tmp);
-    win_row(a, ilast, tmp, khi);
+    int64_t klo = 0, khi = 0, c_begin = 0, c_end;
+    if (kBlk) {
+        c_begin = a.bptr[t];
+        c_end = a.bptr[t + 1];
+    } else {
+        int64_t tmp;
+        win_row(a, i0, klo, tmp);
+        win_row(a, ilast, tmp, khi);
+        c_end = (khi - klo) / kChunk + 1;
+    }
     const TG* Gu = G + (size_t)u * a.n * kHeadDim;
     const TZ* Zu = Z + (size_t)u * a.n * kHeadDim;
     float* dAu = dA + (size_t)u * a.nnz;
     stage_rows_t(gs, Gu, i0, ilast, tid);
-    // this thread's rows: window bounds and runs
+    // this thread's rows: window bounds and runs (a block graph's rows take every key
+    // of their chunks)
     int64_t rlo[4], rhi[4], rp0[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int64_t i = i0 + 4 * ty + q;
         rlo[q] = 1; rhi[q] = 0; rp0[q] = 0;
-        if (i <= ilast) { win_row(a, i, rlo[q], rhi[q]); rp0[q] = a.wp0[i]; }
+        if (i <= ilast) {
+            if (kBlk) { rlo[q] = 0; rhi[q] = a.n - 1; rp0[q] = a.row_ptr[i]; }
+            else { win_row(a, i, rlo[q], rhi[q]); rp0[q] = a.wp0[i]; }
+        }
     }
-    for (int64_t k0 = klo; k0 <= khi; k0 += kChunk) {
+    for (int64_t c = c_begin; c < c_end; ++c) {
+        const int64_t k0 = kBlk ? (int64_t)a.bcol[c] * kChunk : klo + kChunk * c;
+        const int64_t kend = kBlk ? (k0 + kChunk - 1 < a.n - 1 ? k0 + kChunk - 1 : a.n - 1) : khi;
         __syncthreads();
-        stage_rows_t(zs, Zu, k0, khi, tid);
+        stage_rows_t(zs, Zu, k0, kend, tid);
         __syncthreads();
         float acc[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) acc[q][c] = 0.f;
+            for (int cc = 0; cc < 4; ++cc) acc[q][cc] = 0.f;
 #pragma unroll 8
         for (int f = 0; f < kHeadDim; ++f) {
             const float4 g4 = *reinterpret_cast<const float4*>(&gs[f][4 * ty]);
@@ -358,22 +425,44 @@ bwd_band_sddmm_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict_
         }
         // the 16 read-modify-writes: every load issued before the first store (the
         // positions are distinct)
+        int64_t at[4][4];
+        bool in[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int64_t j = k0 + 4 * tx + cc;
+                in[q][cc] = j >= rlo[q] && j <= rhi[q] && j <= kend;
+                at[q][cc] = kBlk ? rp0[q] + kChunk * (c - c_begin) + 4 * tx + cc : rp0[q] + (j - rlo[q]);
+            }
         float old[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int64_t j = k0 + 4 * tx + c;
-                old[q][c] = (j >= rlo[q] && j <= rhi[q]) ? dAu[rp0[q] + (j - rlo[q])] : 0.f;
-            }
+            for (int cc = 0; cc < 4; ++cc) old[q][cc] = in[q][cc] ? dAu[at[q][cc]] : 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int64_t j = k0 + 4 * tx + c;
-                if (j >= rlo[q] && j <= rhi[q]) dAu[rp0[q] + (j - rlo[q])] = fmaf(keep, acc[q][c], old[q][c]);
-            }
+            for (int cc = 0; cc < 4; ++cc)
+                if (in[q][cc]) dAu[at[q][cc]] = fmaf(keep, acc[q][cc], old[q][cc]);
     }
+}
+
+// The band kernels' launches: block-graph runs or window runs.
+template <typename TX>
+void band_rows(const BwdArgs& a, dim3 grid, cudaStream_t s, const float* W, const TX* X, float* P) {
+    if (a.bptr) bwd_band_rows_kernel<TX, true><<<grid, kBandThreads, 0, s>>>(a, W, X, P);
+    else bwd_band_rows_kernel<TX, false><<<grid, kBandThreads, 0, s>>>(a, W, X, P);
+}
+template <typename TX>
+void band_keys(const BwdArgs& a, dim3 grid, cudaStream_t s, const float* W, const TX* X, float* P) {
+    if (a.bptr) bwd_band_keys_kernel<TX, true><<<grid, kBandThreads, 0, s>>>(a, W, X, P);
+    else bwd_band_keys_kernel<TX, false><<<grid, kBandThreads, 0, s>>>(a, W, X, P);
+}
+template <typename TG, typename TZ>
+void band_sddmm(const BwdArgs& a, dim3 grid, cudaStream_t s, const TG* G, const TZ* Z, float* dA, float keep) {
+    if (a.bptr) bwd_band_sddmm_kernel<TG, TZ, true><<<grid, kBandThreads, 0, s>>>(a, G, Z, dA, keep);
+    else bwd_band_sddmm_kernel<TG, TZ, false><<<grid, kBandThreads, 0, s>>>(a, G, Z, dA, keep);
 }
 
 // ---------------------------------------------------------------- CSR kernels
@@ -399,7 +488,7 @@ bwd_hop_rows_kernel(BwdArgs a, const float* __restrict__ A, const TX* __restrict
     const float* Au = A + (size_t)u * a.nnz;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     int64_t s0, s1;
-    row_run(a, i, e0, s0, s1);
+    row_run(a, i, e0, e1, s0, s1);
     const int64_t len = (e1 - e0) - (s1 - s0);
     const size_t at = unit + (size_t)i * kHeadDim + 2 * lane;
     float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
@@ -446,7 +535,7 @@ bwd_weight_grad_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     int64_t s0, s1;
-    row_run(a, i, e0, s0, s1);
+    row_run(a, i, e0, e1, s0, s1);
     const int64_t len = (e1 - e0) - (s1 - s0);
     const float2 g = load2(G + unit + (size_t)i * kHeadDim + 2 * lane);
     const TZ* Zu = Z + unit + 2 * lane;
@@ -491,7 +580,7 @@ bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ 
     const float* Au = A + (size_t)u * a.nnz;
     const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
     int64_t s0, s1;
-    key_run(a, j, t0, s0, s1);
+    key_run(a, j, t0, t1, s0, s1);
     const int64_t len = (t1 - t0) - (s1 - s0);
     const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
     float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
@@ -588,7 +677,7 @@ bwd_rows_out_kernel(BwdArgs a, const float* __restrict__ W, const TIo* __restric
     const float* Wu = W + (size_t)u * a.nnz;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     int64_t s0, s1;
-    row_run(a, i, e0, s0, s1);
+    row_run(a, i, e0, e1, s0, s1);
     const int64_t len = (e1 - e0) - (s1 - s0);
     const size_t at = unit + (size_t)i * kHeadDim + 2 * lane;
     float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
@@ -634,7 +723,7 @@ bwd_dk_kernel(BwdArgs a, const float* __restrict__ dS, const TIo* __restrict__ Q
     const TIo* Qu = Q + unit + 2 * lane;
     const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
     int64_t s0, s1;
-    key_run(a, j, t0, s0, s1);
+    key_run(a, j, t0, t1, s0, s1);
     const int64_t len = (t1 - t0) - (s1 - s0);
     const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
     float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
@@ -680,8 +769,8 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
                    float alpha, TIo* dQ, TIo* dK, TIo* dV, char* ws, const BwdLayout& L,
                    cudaStream_t stream) {
     const dim3 grid(bwd_grid(a)), block(kBwdWarps * 32);
-    const bool band = a.wp0 != nullptr;
-    const dim3 bgrid((unsigned)(a.units * ((a.n + kTile - 1) / kTile))), bblock(kBandThreads);
+    const bool band = a.wp0 != nullptr || a.bptr != nullptr;
+    const dim3 bgrid((unsigned)(a.units * ((a.n + kTile - 1) / kTile)));
     const size_t io = (size_t)a.units * a.n * kHeadDim * sizeof(TIo);
     float* A = reinterpret_cast<float*>(ws + L.a);
     float* dA = reinterpret_cast<float*>(ws + L.da);
@@ -707,7 +796,7 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
     if (band) {
         err = cudaMemsetAsync(A, 0, (size_t)a.units * a.nnz * sizeof(float), stream);
         if (err != cudaSuccess) return cuda_fail(err, "clearing A");
-        score([&] { bwd_band_sddmm_kernel<TIo, TIo><<<bgrid, bblock, 0, stream>>>(a, Q, K, A, kScale); });
+        score([&] { band_sddmm<TIo, TIo>(a, bgrid, stream, Q, K, A, kScale); });
         score([&] { bwd_weight_grad_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, Q, K, A, kScale); });
         score([&] { bwd_scores_softmax_kernel<<<grid, block, 0, stream>>>(a, A); });
         if ((st = launched("bwd_scores_softmax_kernel"))) return st;
@@ -716,10 +805,10 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
     }
     for (int32_t k = 1; k < hops; ++k) {
         if (k == 1) {
-            if (band) hop([&] { bwd_band_rows_kernel<TIo><<<bgrid, bblock, 0, stream>>>(a, A, V, P); });
+            if (band) hop([&] { band_rows(a, bgrid, stream, A, V, P); });
             hop([&] { bwd_hop_rows_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, A, V, P, V, zstate(k), alpha); });
         } else {
-            if (band) hop([&] { bwd_band_rows_kernel<float><<<bgrid, bblock, 0, stream>>>(a, A, zstate(k - 1), P); });
+            if (band) hop([&] { band_rows(a, bgrid, stream, A, zstate(k - 1), P); });
             hop([&] {
                 bwd_hop_rows_kernel<float, TIo><<<grid, block, 0, stream>>>(a, A, zstate(k - 1), P, V, zstate(k), alpha);
             });
@@ -734,29 +823,29 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         float* Gn = Gbuf[k & 1];
         const float* Gf = Gbuf[(k + 1) & 1];         // G_{k+1} for k < hops - 1
         if (top && k == 0) {
-            if (band) hop([&] { bwd_band_sddmm_kernel<TIo, TIo><<<bgrid, bblock, 0, stream>>>(a, dOut, V, dA, keep); });
+            if (band) hop([&] { band_sddmm<TIo, TIo>(a, bgrid, stream, dOut, V, dA, keep); });
             hop([&] { bwd_weight_grad_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, dOut, V, dA, keep); });
         } else if (top) {
             if (band)
-                hop([&] { bwd_band_sddmm_kernel<TIo, float><<<bgrid, bblock, 0, stream>>>(a, dOut, zstate(k), dA, keep); });
+                hop([&] { band_sddmm<TIo, float>(a, bgrid, stream, dOut, zstate(k), dA, keep); });
             hop([&] { bwd_weight_grad_kernel<TIo, float><<<grid, block, 0, stream>>>(a, dOut, zstate(k), dA, keep); });
         } else if (k == 0) {
-            if (band) hop([&] { bwd_band_sddmm_kernel<float, TIo><<<bgrid, bblock, 0, stream>>>(a, Gf, V, dA, keep); });
+            if (band) hop([&] { band_sddmm<float, TIo>(a, bgrid, stream, Gf, V, dA, keep); });
             hop([&] { bwd_weight_grad_kernel<float, TIo><<<grid, block, 0, stream>>>(a, Gf, V, dA, keep); });
         } else {
             if (band)
-                hop([&] { bwd_band_sddmm_kernel<float, float><<<bgrid, bblock, 0, stream>>>(a, Gf, zstate(k), dA, keep); });
+                hop([&] { band_sddmm<float, float>(a, bgrid, stream, Gf, zstate(k), dA, keep); });
             hop([&] { bwd_weight_grad_kernel<float, float><<<grid, block, 0, stream>>>(a, Gf, zstate(k), dA, keep); });
         }
         if ((st = launched("bwd_weight_grad_kernel"))) return st;
         TIo* out = k == 0 ? dV : nullptr;
         if (top) {
-            if (band) hop([&] { bwd_band_keys_kernel<TIo><<<bgrid, bblock, 0, stream>>>(a, A, dOut, P); });
+            if (band) hop([&] { band_keys(a, bgrid, stream, A, dOut, P); });
             hop([&] {
                 bwd_hop_t_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, A, dOut, P, Gn, dVacc, out, alpha, true);
             });
         } else {
-            if (band) hop([&] { bwd_band_keys_kernel<float><<<bgrid, bblock, 0, stream>>>(a, A, Gf, P); });
+            if (band) hop([&] { band_keys(a, bgrid, stream, A, Gf, P); });
             hop([&] {
                 bwd_hop_t_kernel<float, TIo><<<grid, block, 0, stream>>>(a, A, Gf, P, Gn, dVacc, out, alpha, false);
             });
@@ -764,10 +853,10 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         if ((st = launched("bwd_hop_t_kernel"))) return st;
     }
     score([&] { bwd_softmax_kernel<<<grid, block, 0, stream>>>(a, A, dA); });
-    if (band) score([&] { bwd_band_rows_kernel<TIo><<<bgrid, bblock, 0, stream>>>(a, dA, K, P); });
+    if (band) score([&] { band_rows(a, bgrid, stream, dA, K, P); });
     score([&] { bwd_rows_out_kernel<TIo><<<grid, block, 0, stream>>>(a, dA, K, P, dQ); });
     if ((st = launched("bwd_rows_out_kernel"))) return st;
-    if (band) score([&] { bwd_band_keys_kernel<TIo><<<bgrid, bblock, 0, stream>>>(a, dA, Q, P); });
+    if (band) score([&] { band_keys(a, bgrid, stream, dA, Q, P); });
     score([&] { bwd_dk_kernel<TIo><<<grid, block, 0, stream>>>(a, dA, Q, P, dK); });
     return launched("bwd_dk_kernel");
 }
@@ -807,6 +896,52 @@ bool window_runs(const diffuser_graph* g, const std::vector<int64_t>& t_ptr,
     return true;
 }
 
+// The key-block runs of a block graph of 64-token blocks: every row of block row J
+// holds the keys of its key blocks, ascending, each block as one run of 64 (the
+// ragged last block fewer), the same for all its rows.  runs = [bptr (nb + 1) |
+// bcol | btptr (nb + 1) | btrow | btpos]: block row J's key blocks, and for key
+// block KB the row blocks holding it with its place in their lists.  False, and
+// nothing kept, unless every row has exactly that form.
+bool block_runs(const diffuser_graph* g, std::vector<int32_t>& runs) {
+    if (g->kind != kBlockGraph || g->block != kTile || g->n < 1) return false;
+    const int64_t n = g->n, nb = (n + kTile - 1) / kTile;
+    std::vector<std::vector<int32_t>> allowed((size_t)nb);
+    for (int64_t J = 0; J < nb; ++J) {
+        const int64_t i = J * kTile;
+        for (int64_t e = g->h_row_ptr[i]; e < g->h_row_ptr[i + 1]; ++e) {
+            const int32_t kb = g->h_col[e] / kTile;
+            if (allowed[(size_t)J].empty() || allowed[(size_t)J].back() != kb) allowed[(size_t)J].push_back(kb);
+        }
+        for (int64_t r = i; r < std::min(i + kTile, n); ++r) {
+            int64_t e = g->h_row_ptr[r];
+            for (int32_t kb : allowed[(size_t)J]) {
+                const int64_t k0 = (int64_t)kb * kTile, k1 = std::min(k0 + kTile, n);
+                for (int64_t j = k0; j < k1; ++j, ++e)
+                    if (e >= g->h_row_ptr[r + 1] || g->h_col[e] != j) return false;
+            }
+            if (e != g->h_row_ptr[r + 1]) return false;
+        }
+    }
+    std::vector<int32_t> bptr((size_t)nb + 1, 0), bcol, btptr((size_t)nb + 1, 0);
+    for (int64_t J = 0; J < nb; ++J) {
+        bcol.insert(bcol.end(), allowed[(size_t)J].begin(), allowed[(size_t)J].end());
+        bptr[(size_t)J + 1] = (int32_t)bcol.size();
+        for (int32_t kb : allowed[(size_t)J]) ++btptr[(size_t)kb + 1];
+    }
+    for (int64_t KB = 0; KB < nb; ++KB) btptr[(size_t)KB + 1] += btptr[(size_t)KB];
+    std::vector<int32_t> btrow(bcol.size()), btpos(bcol.size());
+    std::vector<int32_t> fill(btptr.begin(), btptr.end() - 1);
+    for (int64_t J = 0; J < nb; ++J)
+        for (size_t x = 0; x < allowed[(size_t)J].size(); ++x) {
+            const int32_t at = fill[(size_t)allowed[(size_t)J][x]]++;
+            btrow[(size_t)at] = (int32_t)J;
+            btpos[(size_t)at] = (int32_t)x;
+        }
+    runs.clear();
+    for (auto* v : {&bptr, &bcol, &btptr, &btrow, &btpos}) runs.insert(runs.end(), v->begin(), v->end());
+    return true;
+}
+
 // The transposed graph (incoming edges of every key, rows ascending), built on
 // the host from the CSR copy by a counting sort and uploaded (synchronously),
 // with the window runs where the graph has them.  On failure the arrays
@@ -828,6 +963,8 @@ int build_transposed_graph(diffuser_graph* g) {
     }
     std::vector<int64_t> wp0, tw0;
     const bool runs = window_runs(g, t_ptr, t_row, wp0, tw0);
+    std::vector<int32_t> bruns;
+    const bool blk = block_runs(g, bruns);
     // the heavy rows (keys): more than twice the mean edge count, heaviest first
     // (ties: ascending index), then the others in ascending order
     auto order_of = [&](auto len, std::vector<int32_t>& order) -> int64_t {
@@ -847,6 +984,7 @@ int build_transposed_graph(diffuser_graph* g) {
     int64_t* d_wp0 = nullptr;
     int64_t* d_tw0 = nullptr;
     int32_t* d_orders = nullptr;             // [2][n]: row_order, key_order
+    int32_t* d_bruns = nullptr;
     cudaError_t err = cudaMalloc(&d_ptr, sizeof(int64_t) * (n + 1));
     if (err == cudaSuccess) err = cudaMalloc(&d_orders, sizeof(int32_t) * 2 * (size_t)n);
     if (err == cudaSuccess)
@@ -869,6 +1007,11 @@ int build_transposed_graph(diffuser_graph* g) {
         if (err == cudaSuccess)
             err = cudaMemcpy(d_tw0, tw0.data(), sizeof(int64_t) * (size_t)n, cudaMemcpyHostToDevice);
     }
+    if (blk) {
+        if (err == cudaSuccess) err = cudaMalloc(&d_bruns, sizeof(int32_t) * bruns.size());
+        if (err == cudaSuccess)
+            err = cudaMemcpy(d_bruns, bruns.data(), sizeof(int32_t) * bruns.size(), cudaMemcpyHostToDevice);
+    }
     if (err != cudaSuccess) {
         cudaFree(d_ptr);
         cudaFree(d_row);
@@ -876,9 +1019,12 @@ int build_transposed_graph(diffuser_graph* g) {
         cudaFree(d_wp0);
         cudaFree(d_tw0);
         cudaFree(d_orders);
+        cudaFree(d_bruns);
         return cuda_fail(err, "building the transposed graph");
     }
     g->d_orders = d_orders;
+    g->d_bruns = d_bruns;
+    g->bruns_blocks = blk ? ((int64_t)bruns.size() - 2 * ((n + kTile - 1) / kTile + 1)) / 3 : 0;   // bcol entries
     g->heavy_rows = heavy_rows;
     g->heavy_keys = heavy_keys;
     g->d_wp0 = d_wp0;
@@ -918,8 +1064,14 @@ int launch_backward_csr(const diffuser_graph* g, int64_t units, const void* Q, c
                         void* dQ, void* dK, void* dV, char* ws, const BwdLayout& L, bool band,
                         cudaStream_t stream) {
     const bool runs = band && g->d_wp0 && g->d_tw0;
+    const bool blk = band && g->d_bruns;
+    const int64_t nb = (g->n + kTile - 1) / kTile, m = g->bruns_blocks;
+    const int32_t* br = g->d_bruns;
     BwdArgs a{g->d_row_ptr, g->d_col, g->d_t_ptr, g->d_t_row, g->d_t_edge,
-              runs ? g->d_wp0 : nullptr, runs ? g->d_tw0 : nullptr, g->d_orders, g->d_orders + g->n,
+              runs ? g->d_wp0 : nullptr, runs ? g->d_tw0 : nullptr,
+              blk ? br : nullptr, blk ? br + nb + 1 : nullptr, blk ? br + nb + 1 + m : nullptr,
+              blk ? br + 2 * (nb + 1) + m : nullptr, blk ? br + 2 * (nb + 1) + 2 * m : nullptr,
+              g->d_orders, g->d_orders + g->n,
               g->heavy_rows, g->heavy_keys, g->n, g->nnz, units, g->r, g->causal ? 1 : 0};
     CsrArgs ca{g->d_row_ptr, g->d_col, g->n, g->nnz, units};
     if (dtype == DIFFUSER_DTYPE_BF16) {

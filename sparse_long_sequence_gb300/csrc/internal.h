@@ -93,6 +93,8 @@ struct diffuser_graph {
     int64_t* d_tw0 = nullptr;         // [n] ... and transposed-list position of key j's (null otherwise)
     int32_t* d_orders = nullptr;      // [2][n] the backward's row and key orders (heavy ones first)
     int64_t heavy_rows = 0, heavy_keys = 0;
+    int32_t* d_bruns = nullptr;       // block graph, 64-token blocks: the backward's key-block runs
+    int64_t bruns_blocks = 0;         // their entries (key blocks over all block rows)
     // status block written by kernels: the word (0 = ok) at [0], the device
     // address of h_status at byte 8 (a bounded wait that gives up writes both)
     // block graph with 64-token blocks: each 128-row tile's key blocks, paired into

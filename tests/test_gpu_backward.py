@@ -57,18 +57,25 @@ def test_backward_small(dl, case, dtype):
         check_grad(to_f64(got), want, dtype)
 
 
-@pytest.mark.parametrize("causal", [False, True], ids=["bidirectional", "causal"])
-def test_backward_band_kernels_match_csr_kernels(dl, causal):
+@pytest.mark.parametrize("kind", ["bidirectional", "causal", "block"])
+def test_backward_band_kernels_match_csr_kernels(dl, kind):
     # On a token graph with a plain window the backward takes the window's edges with
     # band kernels (64 x 64 tiles in shared memory) and the other edges with CSR
-    # kernels; with the CSR path forced, CSR kernels take every edge.  Both sum in
-    # fp32, in fixed but different orders, so they agree to within fp32 rounding.
-    # The window (r = 100) is wider than a tile and n = 700 leaves a ragged last tile.
+    # kernels; on a block graph of 64-token blocks the band kernels take every edge,
+    # block by block.  With the CSR path forced, CSR kernels take every edge.  Both
+    # sum in fp32, in fixed but different orders, so they agree to within fp32
+    # rounding.  The window (r = 100) is wider than a tile; n = 700 and n = 1000
+    # leave a ragged last tile (block).
     import torch
-    build = dl.diffuser_build_causal_graph if causal else dl.diffuser_build_graph
-    g = build(700, 100, 3, rand_per_row=9, seed=2)
-    Q, K, V = (to_device(x, "fp32") for x in synthetic.qkv(1, 2, 700, 64, "fp32", seed=21))
-    dO = to_device(synthetic.qkv(1, 2, 700, 64, "fp32", seed=22)[0], "fp32")
+    if kind == "block":
+        n = 1000
+        g = dl.diffuser_build_block_graph(n=n, block=64, window_blocks=3, rand_blocks=3, global_blocks=2, seed=4)
+    else:
+        n = 700
+        build = dl.diffuser_build_causal_graph if kind == "causal" else dl.diffuser_build_graph
+        g = build(n, 100, 3, rand_per_row=9, seed=2)
+    Q, K, V = (to_device(x, "fp32") for x in synthetic.qkv(1, 2, n, 64, "fp32", seed=21))
+    dO = to_device(synthetic.qkv(1, 2, n, 64, "fp32", seed=22)[0], "fp32")
     band = dl.diffuser_backward(Q, K, V, dO, g, 5, 0.1)
     torch.cuda.synchronize()
     dl.diffuser_set_path(dl.DIFFUSER_PATH_CSR)
