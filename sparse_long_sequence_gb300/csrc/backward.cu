@@ -469,35 +469,48 @@ void band_sddmm(const BwdArgs& a, dim3 grid, cudaStream_t s, const TG* G, const 
 // (the edges outside the window runs; all edges without band kernels).  32 edges
 // a round: the round's 32 operand rows are requested before the first is used, and
 // the next round's edge indices and weights load while they are in flight.  The
-// warps take the heavy rows (keys) first (warp_item), so that the global rows'
-// long lists start with the launch instead of ending it.
+// heavy rows (keys) -- the global rows' 3,500 edges outside their window, say --
+// take a CTA each, its 8 warps an eighth of the edges each (partial sums added in
+// warp order), at the start of the launch; the other rows a warp each, unit by unit.
 
-// Recomputed hop: Y[i] = (1 - alpha) (P[i] + sum_e A_e X[j]) + alpha V[i] (P: the
-// band kernel's window sum, or null).
-template <typename TX, typename TV>
-__global__ void __launch_bounds__(kBwdWarps * 32)
-bwd_hop_rows_kernel(BwdArgs a, const float* __restrict__ A, const TX* __restrict__ X,
-                    const float* __restrict__ P, const TV* __restrict__ V, float* __restrict__ Y, float alpha) {
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
-    if (gw >= a.units * a.n) return;
-    int64_t u, i;
-    warp_item(a, gw, a.row_order, a.heavy_rows, u, i);
-    const size_t unit = (size_t)u * a.n * kHeadDim;
-    const TX* Xu = X + unit + 2 * lane;
-    const float* Au = A + (size_t)u * a.nnz;
-    const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
-    int64_t s0, s1;
-    row_run(a, i, e0, e1, s0, s1);
-    const int64_t len = (e1 - e0) - (s1 - s0);
-    const size_t at = unit + (size_t)i * kHeadDim + 2 * lane;
-    float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
-    bool ok = lane < len;
-    int64_t e = rest_pos(e0, lane, s0, s1);
-    float w_l = ok ? Au[e] : 0.f;
-    int32_t j_l = ok ? a.col[e] : 0;
-    for (int64_t vb = 0; vb < len; vb += 32) {
-        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
+// The item of CTA blockIdx.x (heavy) or of warp `warp` of it (light): unit u, row
+// (key) i, and whether it is heavy.
+__device__ __forceinline__ bool edge_item(const BwdArgs& a, const int32_t* order, int64_t heavy, int warp,
+                                          int64_t& u, int64_t& i) {
+    const int64_t hb = a.units * heavy;
+    if ((int64_t)blockIdx.x < hb) {
+        const int64_t rk = blockIdx.x / a.units;
+        u = blockIdx.x - rk * a.units;
+        i = order[rk];
+        return true;
+    }
+    const int64_t item = ((int64_t)blockIdx.x - hb) * kBwdWarps + warp, rest = a.n - heavy;
+    u = item / rest;
+    i = order[heavy + (item - u * rest)];
+    return false;
+}
+// the CTAs of an edge kernel launch
+unsigned edge_grid(const BwdArgs& a, int64_t heavy) {
+    return (unsigned)(a.units * heavy + (a.units * (a.n - heavy) + kBwdWarps - 1) / kBwdWarps);
+}
+// A heavy item's warp takes the edges [v0, v1) of the len outside the run.
+__device__ __forceinline__ void heavy_share(int64_t len, int warp, int64_t& v0, int64_t& v1) {
+    const int64_t per = (len + kBwdWarps - 1) / kBwdWarps;
+    v0 = per * warp < len ? per * warp : len;
+    v1 = v0 + per < len ? v0 + per : len;
+}
+
+// sum over the edges v0 .. v1-1 outside the run (edge ids from at(v)) of w * X[row],
+// lanes holding features 2l, 2l+1: ... row(v) / weight(v) give an edge's operand row
+// and weight.
+template <typename TX, class Row, class Weight>
+__device__ __forceinline__ float2 edge_sum(int lane, int64_t v0, int64_t v1, const TX* Xu, Row row, Weight weight,
+                                           float2 acc) {
+    bool ok = v0 + lane < v1;
+    float w_l = ok ? weight(v0 + lane) : 0.f;
+    int32_t j_l = ok ? row(v0 + lane) : 0;
+    for (int64_t vb = v0; vb < v1; vb += 32) {
+        const int cnt = (v1 - vb) < 32 ? (int)(v1 - vb) : 32;
         float2 z[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
@@ -505,10 +518,9 @@ bwd_hop_rows_kernel(BwdArgs a, const float* __restrict__ A, const TX* __restrict
             z[t] = t < cnt ? load2(Xu + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
         }
         const float w_c = w_l;
-        ok = vb + 32 + lane < len;
-        e = rest_pos(e0, vb + 32 + lane, s0, s1);
-        w_l = ok ? Au[e] : 0.f;
-        j_l = ok ? a.col[e] : 0;
+        ok = vb + 32 + lane < v1;
+        w_l = ok ? weight(vb + 32 + lane) : 0.f;
+        j_l = ok ? row(vb + 32 + lane) : 0;
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
             const float w = __shfl_sync(0xffffffffu, w_c, t);
@@ -516,6 +528,47 @@ bwd_hop_rows_kernel(BwdArgs a, const float* __restrict__ A, const TX* __restrict
             acc.y = fmaf(w, z[t].y, acc.y);
         }
     }
+    return acc;
+}
+
+// A heavy item's total: the 8 warps' partial sums (in shared memory) added in warp
+// order by warp 0, onto its initial value; false for the other warps.
+__device__ __forceinline__ bool heavy_total(float2 (*part)[32], int warp, int lane, float2& acc) {
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp != 0) return false;
+    float2 t = part[0][lane];
+#pragma unroll
+    for (int w = 1; w < kBwdWarps; ++w) { t.x += part[w][lane].x; t.y += part[w][lane].y; }
+    acc = t;
+    return true;
+}
+
+// Recomputed hop: Y[i] = (1 - alpha) (P[i] + sum_e A_e X[j]) + alpha V[i] (P: the
+// band kernel's window sum, or null).
+template <typename TX, typename TV>
+__global__ void __launch_bounds__(kBwdWarps * 32)
+bwd_hop_rows_kernel(BwdArgs a, const float* __restrict__ A, const TX* __restrict__ X,
+                    const float* __restrict__ P, const TV* __restrict__ V, float* __restrict__ Y, float alpha) {
+    __shared__ float2 part[kBwdWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t u, i;
+    const bool heavy = edge_item(a, a.row_order, a.heavy_rows, warp, u, i);
+    if (!heavy && u >= a.units) return;
+    const size_t unit = (size_t)u * a.n * kHeadDim;
+    const float* Au = A + (size_t)u * a.nnz;
+    const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+    int64_t s0, s1;
+    row_run(a, i, e0, e1, s0, s1);
+    const int64_t len = (e1 - e0) - (s1 - s0);
+    int64_t v0 = 0, v1 = len;
+    if (heavy) heavy_share(len, warp, v0, v1);
+    const size_t at = unit + (size_t)i * kHeadDim + 2 * lane;
+    float2 acc = (P && (!heavy || warp == 0)) ? load2(P + at) : make_float2(0.f, 0.f);
+    acc = edge_sum(lane, v0, v1, X + unit + 2 * lane,
+                   [&](int64_t v) { return a.col[rest_pos(e0, v, s0, s1)]; },
+                   [&](int64_t v) { return Au[rest_pos(e0, v, s0, s1)]; }, acc);
+    if (heavy && !heavy_total(part, warp, lane, acc)) return;
     const float keep = 1.f - alpha;
     const float2 v = load2(V + at);
     store2(Y + at, make_float2(fmaf(keep, acc.x, alpha * v.x), fmaf(keep, acc.y, alpha * v.y)));
@@ -527,24 +580,25 @@ template <typename TG, typename TZ>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 bwd_weight_grad_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict__ Z,
                        float* __restrict__ dA, float keep) {
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
-    if (gw >= a.units * a.n) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t u, i;
-    warp_item(a, gw, a.row_order, a.heavy_rows, u, i);
+    const bool heavy = edge_item(a, a.row_order, a.heavy_rows, warp, u, i);
+    if (!heavy && u >= a.units) return;
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     int64_t s0, s1;
     row_run(a, i, e0, e1, s0, s1);
     const int64_t len = (e1 - e0) - (s1 - s0);
+    int64_t v0 = 0, v1 = len;
+    if (heavy) heavy_share(len, warp, v0, v1);
     const float2 g = load2(G + unit + (size_t)i * kHeadDim + 2 * lane);
     const TZ* Zu = Z + unit + 2 * lane;
     float* dAu = dA + (size_t)u * a.nnz;
-    bool ok = lane < len;
-    int64_t e = rest_pos(e0, lane, s0, s1);
+    bool ok = v0 + lane < v1;
+    int64_t e = rest_pos(e0, v0 + lane, s0, s1);
     int32_t j_l = ok ? a.col[e] : 0;
-    for (int64_t vb = 0; vb < len; vb += 32) {
-        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
+    for (int64_t vb = v0; vb < v1; vb += 32) {
+        const int cnt = (v1 - vb) < 32 ? (int)(v1 - vb) : 32;
         float p[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
@@ -554,7 +608,7 @@ bwd_weight_grad_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict
         }
         const bool ok_c = ok;
         const int64_t e_c = e;
-        ok = vb + 32 + lane < len;
+        ok = vb + 32 + lane < v1;
         e = rest_pos(e0, vb + 32 + lane, s0, s1);
         j_l = ok ? a.col[e] : 0;
         const float dot = warp_transpose_sum32(p, lane);             // edge vb + lane
@@ -570,44 +624,25 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
 bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ G,
                  const float* __restrict__ P, float* __restrict__ Gn, float* __restrict__ dV_acc,
                  TIo* __restrict__ dV_out, float alpha, bool first) {
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
-    if (gw >= a.units * a.n) return;
+    __shared__ float2 part[kBwdWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t u, j;
-    warp_item(a, gw, a.key_order, a.heavy_keys, u, j);
+    const bool heavy = edge_item(a, a.key_order, a.heavy_keys, warp, u, j);
+    if (!heavy && u >= a.units) return;
     const size_t unit = (size_t)u * a.n * kHeadDim;
-    const TG* Gu = G + unit + 2 * lane;
     const float* Au = A + (size_t)u * a.nnz;
     const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
     int64_t s0, s1;
     key_run(a, j, t0, t1, s0, s1);
     const int64_t len = (t1 - t0) - (s1 - s0);
+    int64_t v0 = 0, v1 = len;
+    if (heavy) heavy_share(len, warp, v0, v1);
     const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
-    float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
-    bool ok = lane < len;
-    int64_t t = rest_pos(t0, lane, s0, s1);
-    float w_l = ok ? Au[a.t_edge[t]] : 0.f;
-    int32_t i_l = ok ? a.t_row[t] : 0;
-    for (int64_t vb = 0; vb < len; vb += 32) {
-        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
-        float2 gv[32];
-#pragma unroll
-        for (int s = 0; s < 32; ++s) {
-            const int32_t i = __shfl_sync(0xffffffffu, i_l, s);
-            gv[s] = s < cnt ? load2(Gu + (size_t)i * kHeadDim) : make_float2(0.f, 0.f);
-        }
-        const float w_c = w_l;
-        ok = vb + 32 + lane < len;
-        t = rest_pos(t0, vb + 32 + lane, s0, s1);
-        w_l = ok ? Au[a.t_edge[t]] : 0.f;
-        i_l = ok ? a.t_row[t] : 0;
-#pragma unroll
-        for (int s = 0; s < 32; ++s) {
-            const float w = __shfl_sync(0xffffffffu, w_c, s);
-            acc.x = fmaf(w, gv[s].x, acc.x);
-            acc.y = fmaf(w, gv[s].y, acc.y);
-        }
-    }
+    float2 acc = (P && (!heavy || warp == 0)) ? load2(P + at) : make_float2(0.f, 0.f);
+    acc = edge_sum(lane, v0, v1, G + unit + 2 * lane,
+                   [&](int64_t v) { return a.t_row[rest_pos(t0, v, s0, s1)]; },
+                   [&](int64_t v) { return Au[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
+    if (heavy && !heavy_total(part, warp, lane, acc)) return;
     const float keep = 1.f - alpha;
     const float2 gj = load2(G + at);
     float2 dv = first ? make_float2(0.f, 0.f) : load2(dV_acc + at);
@@ -667,44 +702,25 @@ template <typename TIo>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 bwd_rows_out_kernel(BwdArgs a, const float* __restrict__ W, const TIo* __restrict__ X,
                     const float* __restrict__ P, TIo* __restrict__ out) {
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
-    if (gw >= a.units * a.n) return;
+    __shared__ float2 part[kBwdWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t u, i;
-    warp_item(a, gw, a.row_order, a.heavy_rows, u, i);
+    const bool heavy = edge_item(a, a.row_order, a.heavy_rows, warp, u, i);
+    if (!heavy && u >= a.units) return;
     const size_t unit = (size_t)u * a.n * kHeadDim;
-    const TIo* Xu = X + unit + 2 * lane;
     const float* Wu = W + (size_t)u * a.nnz;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     int64_t s0, s1;
     row_run(a, i, e0, e1, s0, s1);
     const int64_t len = (e1 - e0) - (s1 - s0);
+    int64_t v0 = 0, v1 = len;
+    if (heavy) heavy_share(len, warp, v0, v1);
     const size_t at = unit + (size_t)i * kHeadDim + 2 * lane;
-    float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
-    bool ok = lane < len;
-    int64_t e = rest_pos(e0, lane, s0, s1);
-    float w_l = ok ? Wu[e] : 0.f;
-    int32_t j_l = ok ? a.col[e] : 0;
-    for (int64_t vb = 0; vb < len; vb += 32) {
-        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
-        float2 xv[32];
-#pragma unroll
-        for (int s = 0; s < 32; ++s) {
-            const int32_t j = __shfl_sync(0xffffffffu, j_l, s);
-            xv[s] = s < cnt ? load2(Xu + (size_t)j * kHeadDim) : make_float2(0.f, 0.f);
-        }
-        const float w_c = w_l;
-        ok = vb + 32 + lane < len;
-        e = rest_pos(e0, vb + 32 + lane, s0, s1);
-        w_l = ok ? Wu[e] : 0.f;
-        j_l = ok ? a.col[e] : 0;
-#pragma unroll
-        for (int s = 0; s < 32; ++s) {
-            const float w = __shfl_sync(0xffffffffu, w_c, s);
-            acc.x = fmaf(w, xv[s].x, acc.x);
-            acc.y = fmaf(w, xv[s].y, acc.y);
-        }
-    }
+    float2 acc = (P && (!heavy || warp == 0)) ? load2(P + at) : make_float2(0.f, 0.f);
+    acc = edge_sum(lane, v0, v1, X + unit + 2 * lane,
+                   [&](int64_t v) { return a.col[rest_pos(e0, v, s0, s1)]; },
+                   [&](int64_t v) { return Wu[rest_pos(e0, v, s0, s1)]; }, acc);
+    if (heavy && !heavy_total(part, warp, lane, acc)) return;
     store2(out + at, acc);
 }
 
@@ -713,44 +729,25 @@ template <typename TIo>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 bwd_dk_kernel(BwdArgs a, const float* __restrict__ dS, const TIo* __restrict__ Q,
               const float* __restrict__ P, TIo* __restrict__ dK) {
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
-    if (gw >= a.units * a.n) return;
+    __shared__ float2 part[kBwdWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t u, j;
-    warp_item(a, gw, a.key_order, a.heavy_keys, u, j);
+    const bool heavy = edge_item(a, a.key_order, a.heavy_keys, warp, u, j);
+    if (!heavy && u >= a.units) return;
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const float* dSu = dS + (size_t)u * a.nnz;
-    const TIo* Qu = Q + unit + 2 * lane;
     const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
     int64_t s0, s1;
     key_run(a, j, t0, t1, s0, s1);
     const int64_t len = (t1 - t0) - (s1 - s0);
+    int64_t v0 = 0, v1 = len;
+    if (heavy) heavy_share(len, warp, v0, v1);
     const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
-    float2 acc = P ? load2(P + at) : make_float2(0.f, 0.f);
-    bool ok = lane < len;
-    int64_t t = rest_pos(t0, lane, s0, s1);
-    float w_l = ok ? dSu[a.t_edge[t]] : 0.f;
-    int32_t i_l = ok ? a.t_row[t] : 0;
-    for (int64_t vb = 0; vb < len; vb += 32) {
-        const int cnt = (len - vb) < 32 ? (int)(len - vb) : 32;
-        float2 qv[32];
-#pragma unroll
-        for (int s = 0; s < 32; ++s) {
-            const int32_t i = __shfl_sync(0xffffffffu, i_l, s);
-            qv[s] = s < cnt ? load2(Qu + (size_t)i * kHeadDim) : make_float2(0.f, 0.f);
-        }
-        const float w_c = w_l;
-        ok = vb + 32 + lane < len;
-        t = rest_pos(t0, vb + 32 + lane, s0, s1);
-        w_l = ok ? dSu[a.t_edge[t]] : 0.f;
-        i_l = ok ? a.t_row[t] : 0;
-#pragma unroll
-        for (int s = 0; s < 32; ++s) {
-            const float w = __shfl_sync(0xffffffffu, w_c, s);
-            acc.x = fmaf(w, qv[s].x, acc.x);
-            acc.y = fmaf(w, qv[s].y, acc.y);
-        }
-    }
+    float2 acc = (P && (!heavy || warp == 0)) ? load2(P + at) : make_float2(0.f, 0.f);
+    acc = edge_sum(lane, v0, v1, Q + unit + 2 * lane,
+                   [&](int64_t v) { return a.t_row[rest_pos(t0, v, s0, s1)]; },
+                   [&](int64_t v) { return dSu[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
+    if (heavy && !heavy_total(part, warp, lane, acc)) return;
     store2(dK + at, acc);
 }
 
@@ -769,6 +766,7 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
                    float alpha, TIo* dQ, TIo* dK, TIo* dV, char* ws, const BwdLayout& L,
                    cudaStream_t stream) {
     const dim3 grid(bwd_grid(a)), block(kBwdWarps * 32);
+    const dim3 rgrid(edge_grid(a, a.heavy_rows)), kgrid(edge_grid(a, a.heavy_keys));   // the edge kernels
     const bool band = a.wp0 != nullptr || a.bptr != nullptr;
     const dim3 bgrid((unsigned)(a.units * ((a.n + kTile - 1) / kTile)));
     const size_t io = (size_t)a.units * a.n * kHeadDim * sizeof(TIo);
@@ -797,7 +795,7 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         err = cudaMemsetAsync(A, 0, (size_t)a.units * a.nnz * sizeof(float), stream);
         if (err != cudaSuccess) return cuda_fail(err, "clearing A");
         score([&] { band_sddmm<TIo, TIo>(a, bgrid, stream, Q, K, A, kScale); });
-        score([&] { bwd_weight_grad_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, Q, K, A, kScale); });
+        score([&] { bwd_weight_grad_kernel<TIo, TIo><<<rgrid, block, 0, stream>>>(a, Q, K, A, kScale); });
         score([&] { bwd_scores_softmax_kernel<<<grid, block, 0, stream>>>(a, A); });
         if ((st = launched("bwd_scores_softmax_kernel"))) return st;
     } else if ((st = launch_score_csr(ca, Q, K, dtype, A, stream))) {
@@ -806,11 +804,11 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
     for (int32_t k = 1; k < hops; ++k) {
         if (k == 1) {
             if (band) hop([&] { band_rows(a, bgrid, stream, A, V, P); });
-            hop([&] { bwd_hop_rows_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, A, V, P, V, zstate(k), alpha); });
+            hop([&] { bwd_hop_rows_kernel<TIo, TIo><<<rgrid, block, 0, stream>>>(a, A, V, P, V, zstate(k), alpha); });
         } else {
             if (band) hop([&] { band_rows(a, bgrid, stream, A, zstate(k - 1), P); });
             hop([&] {
-                bwd_hop_rows_kernel<float, TIo><<<grid, block, 0, stream>>>(a, A, zstate(k - 1), P, V, zstate(k), alpha);
+                bwd_hop_rows_kernel<float, TIo><<<rgrid, block, 0, stream>>>(a, A, zstate(k - 1), P, V, zstate(k), alpha);
             });
         }
         if ((st = launched("bwd_hop_rows_kernel"))) return st;
@@ -824,40 +822,40 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         const float* Gf = Gbuf[(k + 1) & 1];         // G_{k+1} for k < hops - 1
         if (top && k == 0) {
             if (band) hop([&] { band_sddmm<TIo, TIo>(a, bgrid, stream, dOut, V, dA, keep); });
-            hop([&] { bwd_weight_grad_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, dOut, V, dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<TIo, TIo><<<rgrid, block, 0, stream>>>(a, dOut, V, dA, keep); });
         } else if (top) {
             if (band)
                 hop([&] { band_sddmm<TIo, float>(a, bgrid, stream, dOut, zstate(k), dA, keep); });
-            hop([&] { bwd_weight_grad_kernel<TIo, float><<<grid, block, 0, stream>>>(a, dOut, zstate(k), dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<TIo, float><<<rgrid, block, 0, stream>>>(a, dOut, zstate(k), dA, keep); });
         } else if (k == 0) {
             if (band) hop([&] { band_sddmm<float, TIo>(a, bgrid, stream, Gf, V, dA, keep); });
-            hop([&] { bwd_weight_grad_kernel<float, TIo><<<grid, block, 0, stream>>>(a, Gf, V, dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<float, TIo><<<rgrid, block, 0, stream>>>(a, Gf, V, dA, keep); });
         } else {
             if (band)
                 hop([&] { band_sddmm<float, float>(a, bgrid, stream, Gf, zstate(k), dA, keep); });
-            hop([&] { bwd_weight_grad_kernel<float, float><<<grid, block, 0, stream>>>(a, Gf, zstate(k), dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<float, float><<<rgrid, block, 0, stream>>>(a, Gf, zstate(k), dA, keep); });
         }
         if ((st = launched("bwd_weight_grad_kernel"))) return st;
         TIo* out = k == 0 ? dV : nullptr;
         if (top) {
             if (band) hop([&] { band_keys(a, bgrid, stream, A, dOut, P); });
             hop([&] {
-                bwd_hop_t_kernel<TIo, TIo><<<grid, block, 0, stream>>>(a, A, dOut, P, Gn, dVacc, out, alpha, true);
+                bwd_hop_t_kernel<TIo, TIo><<<kgrid, block, 0, stream>>>(a, A, dOut, P, Gn, dVacc, out, alpha, true);
             });
         } else {
             if (band) hop([&] { band_keys(a, bgrid, stream, A, Gf, P); });
             hop([&] {
-                bwd_hop_t_kernel<float, TIo><<<grid, block, 0, stream>>>(a, A, Gf, P, Gn, dVacc, out, alpha, false);
+                bwd_hop_t_kernel<float, TIo><<<kgrid, block, 0, stream>>>(a, A, Gf, P, Gn, dVacc, out, alpha, false);
             });
         }
         if ((st = launched("bwd_hop_t_kernel"))) return st;
     }
     score([&] { bwd_softmax_kernel<<<grid, block, 0, stream>>>(a, A, dA); });
     if (band) score([&] { band_rows(a, bgrid, stream, dA, K, P); });
-    score([&] { bwd_rows_out_kernel<TIo><<<grid, block, 0, stream>>>(a, dA, K, P, dQ); });
+    score([&] { bwd_rows_out_kernel<TIo><<<rgrid, block, 0, stream>>>(a, dA, K, P, dQ); });
     if ((st = launched("bwd_rows_out_kernel"))) return st;
     if (band) score([&] { band_keys(a, bgrid, stream, dA, Q, P); });
-    score([&] { bwd_dk_kernel<TIo><<<grid, block, 0, stream>>>(a, dA, Q, P, dK); });
+    score([&] { bwd_dk_kernel<TIo><<<kgrid, block, 0, stream>>>(a, dA, Q, P, dK); });
     return launched("bwd_dk_kernel");
 }
 
