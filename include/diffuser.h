@@ -218,7 +218,14 @@ DIFFUSER_API int diffuser_workspace_size(const diffuser_graph* g, int64_t B, int
  *               workspace must not be used by two calls in flight at once
  *   stream      stream on which everything is enqueued
  * Precision: A and Z_k are fp32; bf16 outputs are rounded to nearest-even
- * once, from fp32.  Errors: INVALID_ARG, UNSUPPORTED (d != 64, dtype),
+ * once, from fp32.  On the band and block paths the first forward with a
+ * given B*H on a graph builds a table of each CTA's tiles on the host and
+ * uploads it (a few KB of device memory held with the graph, at most four
+ * tables per path); a forward issued while the caller's stream is capturing
+ * deals the tiles in a fixed snake order instead (the same results, bit for
+ * bit).  A forward repeated with the same arguments on an uncaptured stream
+ * is recorded once into a CUDA graph held with g and replayed afterwards.
+ * Errors: INVALID_ARG, UNSUPPORTED (d != 64, dtype),
  * WORKSPACE, CUDA, and DEVICE when a kernel of an earlier call on g has
  * reported a failure through the graph's status word (see
  * diffuser_graph_status): the check reads a host mirror of the word, so it
