@@ -31,6 +31,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 #include <vector>
 
 #include "internal.h"
@@ -170,17 +171,53 @@ __device__ __forceinline__ void tile_of(const BwdArgs& a, bool tile_major, int64
     else { u = blockIdx.x / tiles; t = blockIdx.x - u * tiles; }
 }
 
+// Asynchronous global -> shared copies (this thread's; cp_wait<N> leaves the N
+// newest groups in flight, a __syncthreads then shares the data): 16 or 4 bytes, or
+// zeros when `valid` is false (nothing is read then).
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void cp16(void* sdst, const void* gsrc, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(sdst)), "l"(gsrc),
+                 "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp4(void* sdst, const void* gsrc, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(sdst)), "l"(gsrc),
+                 "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kN>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(kN) : "memory"); }
+
+// A chunk's 64 operand rows (first .. first + 63, zeros past last) into xs, in X's
+// own type, as asynchronous 16-byte copies.
+template <typename TX>
+__device__ __forceinline__ void stage_rows_async(TX (*xs)[kHeadDim], const TX* Xu, int64_t first, int64_t last,
+                                                 int tid) {
+    constexpr int kPerRow = kHeadDim * (int)sizeof(TX) / 16;           // 16-byte pieces of a row
+    constexpr int kPer = kChunk * kPerRow / kBandThreads;
+    constexpr int kElems = 16 / (int)sizeof(TX);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int idx = tid + kBandThreads * q, rr = idx / kPerRow, c = idx - rr * kPerRow;
+        const int64_t j = first + rr;
+        cp16(&xs[rr][kElems * c], j <= last ? Xu + j * kHeadDim + kElems * c : Xu, j <= last);
+    }
+}
+
 // P[i] = sum over the keys j of row i's window of W[e(i, j)] X[j], e(i, j) =
 // wp0[i] + j - lo(i); on a block graph (kBlk) over the key blocks of row i's block,
 // e(i, j) = row_ptr[i] + 64 (place of j's block in the list) + j % 64.  A CTA: 64
 // rows of one unit; warp w rows 8w .. 8w+7, lane l features 2l, 2l+1; the keys in
-// chunks of 64 (the window's, or the key blocks), ascending.
+// chunks of 64 (the window's, or the key blocks), ascending, staged by
+// asynchronous copies one chunk ahead (two buffers).
 template <typename TX, bool kBlk>
 __global__ void __launch_bounds__(kBandThreads)
 bwd_band_rows_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restrict__ X, float* __restrict__ P) {
-    __shared__ __align__(16) float xs[kChunk][kHeadDim];
-    __shared__ __align__(16) float ws[kTile][kWStride];
-    __shared__ int64_t s_lo[kTile], s_hi[kTile], s_wp[kTile];   // the tile rows' windows and runs
+    extern __shared__ __align__(16) uint8_t band_smem[];
+    auto xs = reinterpret_cast<TX (*)[kChunk][kHeadDim]>(band_smem);                   // [2]
+    auto ws = reinterpret_cast<float (*)[kTile][kWStride]>(band_smem + 2 * kChunk * kHeadDim * sizeof(TX));
+    int64_t* s_lo = reinterpret_cast<int64_t*>(ws + 2);        // the tile rows' windows and runs
+    int64_t* s_hi = s_lo + kTile;
+    int64_t* s_wp = s_hi + kTile;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int64_t u, t;
     tile_of(a, kBlk, u, t);
@@ -205,47 +242,50 @@ bwd_band_rows_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restric
         }
         s_lo[tid] = lo; s_hi[tid] = hi; s_wp[tid] = wp;
     }
+    __syncthreads();                              // the row table, before the first staging
     const float* Wu = W + (size_t)u * a.nnz;
     const TX* Xu = X + (size_t)u * a.n * kHeadDim;
+    constexpr int kWPer = kTile * kChunk / kBandThreads;
+    auto stage = [&](int64_t c, int b) {
+        const int64_t k0 = kBlk ? (int64_t)a.bcol[c] * kChunk : klo + kChunk * c;
+        const int64_t kend = kBlk ? (k0 + kChunk - 1 < a.n - 1 ? k0 + kChunk - 1 : a.n - 1) : khi;
+        stage_rows_async(xs[b], Xu, k0, kend, tid);
+        const int kk = tid & (kChunk - 1);
+        const int64_t j = k0 + kk;
+#pragma unroll
+        for (int q = 0; q < kWPer; ++q) {
+            const int rr = (tid >> 6) + (kBandThreads / kChunk) * q;
+            const int64_t lo = s_lo[rr];
+            const bool in = j >= lo && j <= s_hi[rr] && j <= kend;
+            const int64_t at = kBlk ? s_wp[rr] + kChunk * (c - c_begin) + kk : s_wp[rr] + (j - lo);
+            cp4(&ws[b][rr][kk], in ? Wu + at : Wu, in);
+        }
+        cp_commit();
+    };
     float2 acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = make_float2(0.f, 0.f);
-    constexpr int kWPer = kTile * kChunk / kBandThreads;
+    if (c_begin < c_end) stage(c_begin, 0);
     for (int64_t c = c_begin; c < c_end; ++c) {
-        const int64_t k0 = kBlk ? (int64_t)a.bcol[c] * kChunk : klo + kChunk * c;
-        const int64_t kend = kBlk ? (k0 + kChunk - 1 < a.n - 1 ? k0 + kChunk - 1 : a.n - 1) : khi;
-        __syncthreads();                          // the previous chunk has been used
-        stage_rows<kBandThreads>(xs, Xu, k0, kend, tid);
-        {
-            const int kk = tid & (kChunk - 1);
-            const int64_t j = k0 + kk;
-            float wv[kWPer];
-#pragma unroll
-            for (int q = 0; q < kWPer; ++q) {
-                const int rr = (tid >> 6) + (kBandThreads / kChunk) * q;
-                const int64_t lo = s_lo[rr];
-                const bool in = j >= lo && j <= s_hi[rr] && j <= kend;
-                const int64_t at = kBlk ? s_wp[rr] + kChunk * (c - c_begin) + kk : s_wp[rr] + (j - lo);
-                wv[q] = in ? Wu[at] : 0.f;
-            }
-#pragma unroll
-            for (int q = 0; q < kWPer; ++q) ws[(tid >> 6) + (kBandThreads / kChunk) * q][kk] = wv[q];
-        }
-        __syncthreads();
+        const int b = (int)((c - c_begin) & 1);
+        if (c + 1 < c_end) { stage(c + 1, b ^ 1); cp_wait<1>(); }
+        else cp_wait<0>();
+        __syncthreads();                          // chunk c has landed for every thread
 #pragma unroll 2
         for (int kk = 0; kk < kChunk; kk += 4) {
             float2 z[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) z[q] = *reinterpret_cast<const float2*>(&xs[kk + q][2 * lane]);
+            for (int q = 0; q < 4; ++q) z[q] = load2(&xs[b][kk + q][2 * lane]);
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
-                const float4 w4 = *reinterpret_cast<const float4*>(&ws[8 * warp + rr][kk]);
+                const float4 w4 = *reinterpret_cast<const float4*>(&ws[b][8 * warp + rr][kk]);
                 acc[rr] = __ffma2_rn(make_float2(w4.x, w4.x), z[0], acc[rr]);
                 acc[rr] = __ffma2_rn(make_float2(w4.y, w4.y), z[1], acc[rr]);
                 acc[rr] = __ffma2_rn(make_float2(w4.z, w4.z), z[2], acc[rr]);
                 acc[rr] = __ffma2_rn(make_float2(w4.w, w4.w), z[3], acc[rr]);
             }
         }
+        __syncthreads();                          // buffer b is read before chunk c + 2 refills it
     }
 #pragma unroll
     for (int rr = 0; rr < 8; ++rr) {
@@ -257,14 +297,16 @@ bwd_band_rows_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restric
 // P[j] = sum over the rows i whose windows (key-block lists, kBlk) hold key j of
 // W[e(i, j)] X[i].  A CTA: 64 keys of one unit; warp w keys 8w .. 8w+7, lane l
 // features 2l, 2l+1; the rows in chunks of 64 (the window rows', or the row blocks
-// holding the key block), ascending.  The runs wp0 of the tile's rows are staged
-// once when there are at most kMaxRange of them.
+// holding the key block), ascending, staged one chunk ahead like the rows kernel.
+// The runs wp0 of the tile's rows are staged once when there are at most
+// kMaxRange of them.
 template <typename TX, bool kBlk>
 __global__ void __launch_bounds__(kBandThreads)
 bwd_band_keys_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restrict__ X, float* __restrict__ P) {
-    __shared__ __align__(16) float xs[kChunk][kHeadDim];
-    __shared__ __align__(16) float ws[kChunk][kWStride];   // [row of the chunk][key of the tile]
-    __shared__ int64_t s_wp[kMaxRange];
+    extern __shared__ __align__(16) uint8_t band_smem[];
+    auto xs = reinterpret_cast<TX (*)[kChunk][kHeadDim]>(band_smem);                   // [2]
+    auto ws = reinterpret_cast<float (*)[kChunk][kWStride]>(band_smem + 2 * kChunk * kHeadDim * sizeof(TX));
+    int64_t* s_wp = reinterpret_cast<int64_t*>(ws + 2);        // [kMaxRange] [row of the chunk][key of the tile]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int64_t u, t;
     tile_of(a, kBlk, u, t);
@@ -284,43 +326,50 @@ bwd_band_keys_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restric
         if (staged)
             for (int64_t i = rlo + tid; i <= rhi; i += kBandThreads) s_wp[i - rlo] = a.wp0[i];
     }
+    __syncthreads();                              // the run table, before the first staging
     const float* Wu = W + (size_t)u * a.nnz;
     const TX* Xu = X + (size_t)u * a.n * kHeadDim;
-    float2 acc[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = make_float2(0.f, 0.f);
     constexpr int kWPer = kChunk * kTile / kBandThreads;
-    for (int64_t c = c_begin; c < c_end; ++c) {
+    auto stage = [&](int64_t c, int b) {
         const int64_t r0 = kBlk ? (int64_t)a.btrow[c] * kChunk : rlo + kChunk * c;
         const int64_t rend = kBlk ? (r0 + kChunk - 1 < a.n - 1 ? r0 + kChunk - 1 : a.n - 1) : rhi;
         const int64_t place = kBlk ? (int64_t)a.btpos[c] * kChunk : 0;
-        __syncthreads();
-        stage_rows<kBandThreads>(xs, Xu, r0, rend, tid);
-        {
-            const int kk = tid & (kTile - 1);
-            const int64_t j = j0 + kk;
-            float wv[kWPer];
+        stage_rows_async(xs[b], Xu, r0, rend, tid);
+        const int kk = tid & (kTile - 1);
+        const int64_t j = j0 + kk;
 #pragma unroll
-            for (int q = 0; q < kWPer; ++q) {
-                const int64_t i = r0 + (tid >> 6) + (kBandThreads / kTile) * q;
-                if (kBlk) {
-                    wv[q] = (i <= rend && j <= jlast) ? Wu[a.row_ptr[i] + place + kk] : 0.f;
-                } else {
-                    int64_t lo, hi;
-                    win_row(a, i, lo, hi);
-                    const bool in = i <= rend && j < a.n && j >= lo && j <= hi;
-                    wv[q] = in ? Wu[(staged ? s_wp[i - rlo] : a.wp0[i]) + (j - lo)] : 0.f;
-                }
+        for (int q = 0; q < kWPer; ++q) {
+            const int rr = (tid >> 6) + (kBandThreads / kTile) * q;
+            const int64_t i = r0 + rr;
+            bool in;
+            int64_t at;
+            if (kBlk) {
+                in = i <= rend && j <= jlast;
+                at = in ? a.row_ptr[i] + place + kk : 0;
+            } else {
+                int64_t lo, hi;
+                win_row(a, i, lo, hi);
+                in = i <= rend && j < a.n && j >= lo && j <= hi;
+                at = in ? (staged ? s_wp[i - rlo] : a.wp0[i]) + (j - lo) : 0;
             }
-#pragma unroll
-            for (int q = 0; q < kWPer; ++q) ws[(tid >> 6) + (kBandThreads / kTile) * q][kk] = wv[q];
+            cp4(&ws[b][rr][kk], Wu + at, in);
         }
+        cp_commit();
+    };
+    float2 acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = make_float2(0.f, 0.f);
+    if (c_begin < c_end) stage(c_begin, 0);
+    for (int64_t c = c_begin; c < c_end; ++c) {
+        const int b = (int)((c - c_begin) & 1);
+        if (c + 1 < c_end) { stage(c + 1, b ^ 1); cp_wait<1>(); }
+        else cp_wait<0>();
         __syncthreads();
 #pragma unroll 4
         for (int rr = 0; rr < kChunk; ++rr) {
-            const float2 x = *reinterpret_cast<const float2*>(&xs[rr][2 * lane]);
-            const float4 wa = *reinterpret_cast<const float4*>(&ws[rr][8 * warp]);
-            const float4 wb = *reinterpret_cast<const float4*>(&ws[rr][8 * warp + 4]);
+            const float2 x = load2(&xs[b][rr][2 * lane]);
+            const float4 wa = *reinterpret_cast<const float4*>(&ws[b][rr][8 * warp]);
+            const float4 wb = *reinterpret_cast<const float4*>(&ws[b][rr][8 * warp + 4]);
             acc[0] = __ffma2_rn(make_float2(wa.x, wa.x), x, acc[0]);
             acc[1] = __ffma2_rn(make_float2(wa.y, wa.y), x, acc[1]);
             acc[2] = __ffma2_rn(make_float2(wa.z, wa.z), x, acc[2]);
@@ -330,6 +379,7 @@ bwd_band_keys_kernel(BwdArgs a, const float* __restrict__ W, const TX* __restric
             acc[6] = __ffma2_rn(make_float2(wb.z, wb.z), x, acc[6]);
             acc[7] = __ffma2_rn(make_float2(wb.w, wb.w), x, acc[7]);
         }
+        __syncthreads();
     }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -359,14 +409,23 @@ __device__ __forceinline__ void stage_rows_t(float (*xt)[kWStride], const TX* Xu
 
 // dA[e(i, j)] += keep * G[i] . Z[j] over the windows (key-block lists, kBlk) of 64
 // rows of one unit: the rows' G staged once (feature-major), the keys' Z in chunks
-// of 64 (feature-major); thread (ty, tx) computes rows 4ty .. +3 x keys 4tx .. +3
-// of each chunk.
+// of 64 (row-major, 65- or 66-element rows: conflict-free column reads), staged by
+// asynchronous copies one chunk ahead; thread (ty, tx) computes rows 4ty .. +3 x
+// keys tx + 16c (c < 4) of each chunk, the dA values it updates loaded before its
+// dot products.
+template <typename TZ>
+struct ZRow { static constexpr int kStride = sizeof(TZ) == 4 ? kChunk + 1 : kChunk + 2; };
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
 template <typename TG, typename TZ, bool kBlk>
 __global__ void __launch_bounds__(kBandThreads)
 bwd_band_sddmm_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict__ Z, float* __restrict__ dA,
                       float keep) {
-    __shared__ __align__(16) float gs[kHeadDim][kWStride];  // [feature][row]
-    __shared__ __align__(16) float zs[kHeadDim][kWStride];  // [feature][key]
+    constexpr int kZS = ZRow<TZ>::kStride;
+    extern __shared__ __align__(16) uint8_t band_smem[];
+    auto gs = reinterpret_cast<float (*)[kWStride]>(band_smem);                          // [feature][row]
+    auto zs = reinterpret_cast<TZ (*)[kChunk][kZS]>(band_smem + kHeadDim * kWStride * sizeof(float));   // [2][key][feature]
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     int64_t u, t;
     tile_of(a, kBlk, u, t);
@@ -385,6 +444,24 @@ bwd_band_sddmm_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict_
     const TG* Gu = G + (size_t)u * a.n * kHeadDim;
     const TZ* Zu = Z + (size_t)u * a.n * kHeadDim;
     float* dAu = dA + (size_t)u * a.nnz;
+    auto chunk_keys = [&](int64_t c, int64_t& k0, int64_t& kend) {
+        k0 = kBlk ? (int64_t)a.bcol[c] * kChunk : klo + kChunk * c;
+        kend = kBlk ? (k0 + kChunk - 1 < a.n - 1 ? k0 + kChunk - 1 : a.n - 1) : khi;
+    };
+    auto stage = [&](int64_t c, int b) {
+        int64_t k0, kend;
+        chunk_keys(c, k0, kend);
+        constexpr int kPairs = sizeof(TZ) == 4 ? 1 : 2;                 // elements per 4-byte copy
+        constexpr int kPer = kChunk * kHeadDim / kPairs / kBandThreads;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int idx = tid + kBandThreads * q, kk = idx / (kHeadDim / kPairs);
+            const int f = kPairs * (idx - kk * (kHeadDim / kPairs));
+            const int64_t j = k0 + kk;
+            cp4(&zs[b][kk][f], j <= kend ? Zu + j * kHeadDim + f : Zu, j <= kend);
+        }
+        cp_commit();
+    };
     stage_rows_t(gs, Gu, i0, ilast, tid);
     // this thread's rows: window bounds and runs (a block graph's rows take every key
     // of their chunks)
@@ -398,12 +475,28 @@ bwd_band_sddmm_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict_
             else { win_row(a, i, rlo[q], rhi[q]); rp0[q] = a.wp0[i]; }
         }
     }
+    if (c_begin < c_end) stage(c_begin, 0);
     for (int64_t c = c_begin; c < c_end; ++c) {
-        const int64_t k0 = kBlk ? (int64_t)a.bcol[c] * kChunk : klo + kChunk * c;
-        const int64_t kend = kBlk ? (k0 + kChunk - 1 < a.n - 1 ? k0 + kChunk - 1 : a.n - 1) : khi;
-        __syncthreads();
-        stage_rows_t(zs, Zu, k0, kend, tid);
-        __syncthreads();
+        const int b = (int)((c - c_begin) & 1);
+        int64_t k0, kend;
+        chunk_keys(c, k0, kend);
+        // the dA values this thread updates in chunk c (positions distinct)
+        int64_t at[4][4];
+        bool in[4][4];
+        float old[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int kk = tx + 16 * cc;
+                const int64_t j = k0 + kk;
+                in[q][cc] = j >= rlo[q] && j <= rhi[q] && j <= kend;
+                at[q][cc] = kBlk ? rp0[q] + kChunk * (c - c_begin) + kk : rp0[q] + (j - rlo[q]);
+                old[q][cc] = in[q][cc] ? dAu[at[q][cc]] : 0.f;
+            }
+        if (c + 1 < c_end) { stage(c + 1, b ^ 1); cp_wait<1>(); }
+        else cp_wait<0>();
+        __syncthreads();                          // chunk c (and, first, the rows' G) is in
         float acc[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -412,57 +505,71 @@ bwd_band_sddmm_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict_
 #pragma unroll 8
         for (int f = 0; f < kHeadDim; ++f) {
             const float4 g4 = *reinterpret_cast<const float4*>(&gs[f][4 * ty]);
-            const float4 z4 = *reinterpret_cast<const float4*>(&zs[f][4 * tx]);
             const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+            float zv[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 gg = make_float2(gv[q], gv[q]);
-                float2 lo2 = make_float2(acc[q][0], acc[q][1]), hi2 = make_float2(acc[q][2], acc[q][3]);
-                lo2 = __ffma2_rn(gg, make_float2(z4.x, z4.y), lo2);
-                hi2 = __ffma2_rn(gg, make_float2(z4.z, z4.w), hi2);
-                acc[q][0] = lo2.x; acc[q][1] = lo2.y; acc[q][2] = hi2.x; acc[q][3] = hi2.y;
-            }
+            for (int cc = 0; cc < 4; ++cc) zv[cc] = to_f32(zs[b][tx + 16 * cc][f]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) acc[q][cc] = fmaf(gv[q], zv[cc], acc[q][cc]);
         }
-        // the 16 read-modify-writes: every load issued before the first store (the
-        // positions are distinct)
-        int64_t at[4][4];
-        bool in[4][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int64_t j = k0 + 4 * tx + cc;
-                in[q][cc] = j >= rlo[q] && j <= rhi[q] && j <= kend;
-                at[q][cc] = kBlk ? rp0[q] + kChunk * (c - c_begin) + 4 * tx + cc : rp0[q] + (j - rlo[q]);
-            }
-        float old[4][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) old[q][cc] = in[q][cc] ? dAu[at[q][cc]] : 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
                 if (in[q][cc]) dAu[at[q][cc]] = fmaf(keep, acc[q][cc], old[q][cc]);
+        __syncthreads();                          // buffer b is read before chunk c + 2 refills it
     }
 }
 
-// The band kernels' launches: block-graph runs or window runs.
+// The band kernels' launches: block-graph runs or window runs.  The product kernels
+// take their two staging buffers (and tables) as dynamic shared memory.
+template <typename TX>
+constexpr size_t rows_smem() {
+    return 2 * kChunk * kHeadDim * sizeof(TX) + 2 * kTile * kWStride * sizeof(float) + 3 * kTile * sizeof(int64_t);
+}
+template <typename TX>
+constexpr size_t keys_smem() {
+    return 2 * kChunk * kHeadDim * sizeof(TX) + 2 * kChunk * kWStride * sizeof(float) + kMaxRange * sizeof(int64_t);
+}
+template <typename K>
+void allow_smem(K kernel, size_t bytes) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
 template <typename TX>
 void band_rows(const BwdArgs& a, dim3 grid, cudaStream_t s, const float* W, const TX* X, float* P) {
-    if (a.bptr) bwd_band_rows_kernel<TX, true><<<grid, kBandThreads, 0, s>>>(a, W, X, P);
-    else bwd_band_rows_kernel<TX, false><<<grid, kBandThreads, 0, s>>>(a, W, X, P);
+    static std::once_flag once;
+    std::call_once(once, [] {
+        allow_smem(bwd_band_rows_kernel<TX, true>, rows_smem<TX>());
+        allow_smem(bwd_band_rows_kernel<TX, false>, rows_smem<TX>());
+    });
+    if (a.bptr) bwd_band_rows_kernel<TX, true><<<grid, kBandThreads, rows_smem<TX>(), s>>>(a, W, X, P);
+    else bwd_band_rows_kernel<TX, false><<<grid, kBandThreads, rows_smem<TX>(), s>>>(a, W, X, P);
 }
 template <typename TX>
 void band_keys(const BwdArgs& a, dim3 grid, cudaStream_t s, const float* W, const TX* X, float* P) {
-    if (a.bptr) bwd_band_keys_kernel<TX, true><<<grid, kBandThreads, 0, s>>>(a, W, X, P);
-    else bwd_band_keys_kernel<TX, false><<<grid, kBandThreads, 0, s>>>(a, W, X, P);
+    static std::once_flag once;
+    std::call_once(once, [] {
+        allow_smem(bwd_band_keys_kernel<TX, true>, keys_smem<TX>());
+        allow_smem(bwd_band_keys_kernel<TX, false>, keys_smem<TX>());
+    });
+    if (a.bptr) bwd_band_keys_kernel<TX, true><<<grid, kBandThreads, keys_smem<TX>(), s>>>(a, W, X, P);
+    else bwd_band_keys_kernel<TX, false><<<grid, kBandThreads, keys_smem<TX>(), s>>>(a, W, X, P);
+}
+template <typename TZ>
+constexpr size_t sddmm_smem() {
+    return kHeadDim * kWStride * sizeof(float) + 2 * kChunk * ZRow<TZ>::kStride * sizeof(TZ);
 }
 template <typename TG, typename TZ>
 void band_sddmm(const BwdArgs& a, dim3 grid, cudaStream_t s, const TG* G, const TZ* Z, float* dA, float keep) {
-    if (a.bptr) bwd_band_sddmm_kernel<TG, TZ, true><<<grid, kBandThreads, 0, s>>>(a, G, Z, dA, keep);
-    else bwd_band_sddmm_kernel<TG, TZ, false><<<grid, kBandThreads, 0, s>>>(a, G, Z, dA, keep);
+    static std::once_flag once;
+    std::call_once(once, [] {
+        allow_smem(bwd_band_sddmm_kernel<TG, TZ, true>, sddmm_smem<TZ>());
+        allow_smem(bwd_band_sddmm_kernel<TG, TZ, false>, sddmm_smem<TZ>());
+    });
+    if (a.bptr) bwd_band_sddmm_kernel<TG, TZ, true><<<grid, kBandThreads, sddmm_smem<TZ>(), s>>>(a, G, Z, dA, keep);
+    else bwd_band_sddmm_kernel<TG, TZ, false><<<grid, kBandThreads, sddmm_smem<TZ>(), s>>>(a, G, Z, dA, keep);
 }
 
 // ---------------------------------------------------------------- CSR kernels
