@@ -596,10 +596,6 @@ __device__ __forceinline__ bool edge_item(const BwdArgs& a, const int32_t* order
     i = order[heavy + (item - u * rest)];
     return false;
 }
-// the CTAs of an edge kernel launch
-unsigned edge_grid(const BwdArgs& a, int64_t heavy) {
-    return (unsigned)(a.units * heavy + (a.units * (a.n - heavy) + kBwdWarps - 1) / kBwdWarps);
-}
 // A heavy item's warp takes the edges [v0, v1) of the len outside the run.
 __device__ __forceinline__ void heavy_share(int64_t len, int warp, int64_t& v0, int64_t& v1) {
     const int64_t per = (len + kBwdWarps - 1) / kBwdWarps;
@@ -651,6 +647,104 @@ __device__ __forceinline__ bool heavy_total(float2 (*part)[32], int warp, int la
     return true;
 }
 
+
+// ---- light rows (keys) by quarter-warps: 4 a warp, 32 a CTA after the heavy CTAs.
+// Lane l of a quarter owns 8 features: 8l .. 8l+7 of bf16 operands (one 16-byte
+// load per row), 4l .. 4l+3 and 32 + 4l .. +3 of fp32 ones (two); each quarter-warp
+// reads whole 128-byte lines.  A batch of kQB edges (rows in flight per lane) at a
+// time, the next batch's indices and weights loading meanwhile.
+constexpr int kQItems = kBwdWarps * 4;
+
+__device__ __forceinline__ bool quarter_item(const BwdArgs& a, const int32_t* order, int64_t heavy, int q,
+                                             int64_t& u, int64_t& i) {
+    const int64_t hb = a.units * heavy, rest = a.n - heavy;
+    const int64_t item = ((int64_t)blockIdx.x - hb) * kQItems + q;
+    if (rest <= 0 || item >= a.units * rest) return false;
+    u = item / rest;
+    i = order[heavy + (item - u * rest)];
+    return true;
+}
+unsigned quarter_grid(const BwdArgs& a, int64_t heavy) {
+    return (unsigned)(a.units * heavy + (a.units * (a.n - heavy) + kQItems - 1) / kQItems);
+}
+
+template <bool kWide>
+__device__ __forceinline__ void load8(const float* row, int ql, float (&v)[8]) {
+    const float4 x = *reinterpret_cast<const float4*>(row + (kWide ? 8 * ql : 4 * ql));
+    const float4 y = *reinterpret_cast<const float4*>(row + (kWide ? 8 * ql + 4 : 32 + 4 * ql));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+}
+template <bool kWide>
+__device__ __forceinline__ void load8(const __nv_bfloat16* row, int ql, float (&v)[8]) {
+    uint2 x, y;
+    if (kWide) {
+        const uint4 w = *reinterpret_cast<const uint4*>(row + 8 * ql);
+        x = make_uint2(w.x, w.y);
+        y = make_uint2(w.z, w.w);
+    } else {
+        x = *reinterpret_cast<const uint2*>(row + 4 * ql);
+        y = *reinterpret_cast<const uint2*>(row + 32 + 4 * ql);
+    }
+    v[0] = bf16lo(x.x); v[1] = bf16hi(x.x); v[2] = bf16lo(x.y); v[3] = bf16hi(x.y);
+    v[4] = bf16lo(y.x); v[5] = bf16hi(y.x); v[6] = bf16lo(y.y); v[7] = bf16hi(y.y);
+}
+template <bool kWide>
+__device__ __forceinline__ void store8(float* row, int ql, const float (&v)[8]) {
+    *reinterpret_cast<float4*>(row + (kWide ? 8 * ql : 4 * ql)) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(row + (kWide ? 8 * ql + 4 : 32 + 4 * ql)) = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <bool kWide>
+__device__ __forceinline__ void store8(__nv_bfloat16* row, int ql, const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    if (kWide) {
+        *reinterpret_cast<uint4*>(row + 8 * ql) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+        *reinterpret_cast<uint2*>(row + 4 * ql) = make_uint2(w[0], w[1]);
+        *reinterpret_cast<uint2*>(row + 32 + 4 * ql) = make_uint2(w[2], w[3]);
+    }
+}
+
+// acc += sum over the edges 0 .. len-1 outside the run of weight(v) X[row(v)] (this
+// lane's 8 features), in edge order.
+template <typename TX, class Row, class Weight>
+__device__ __forceinline__ void quarter_sum(int ql, unsigned qmask, int64_t len, const TX* Xu, Row row,
+                                            Weight weight, float (&acc)[8]) {
+    constexpr bool kWide = sizeof(TX) == 2;
+    constexpr int kQB = kWide ? 8 : 4;
+    int32_t jc = 0;
+    float wc = 0.f;
+    if (ql < kQB && ql < len) { jc = row(ql); wc = weight(ql); }
+    for (int64_t vb = 0; vb < len; vb += kQB) {
+        float x[kQB][8];
+#pragma unroll
+        for (int b = 0; b < kQB; ++b) {
+            const int32_t j = __shfl_sync(qmask, jc, b, 8);
+            if (vb + b < len) {
+                load8<kWide>(Xu + (size_t)j * kHeadDim, ql, x[b]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x[b][k] = 0.f;
+            }
+        }
+        int32_t jn = 0;
+        float wn = 0.f;
+        if (ql < kQB && vb + kQB + ql < len) { jn = row(vb + kQB + ql); wn = weight(vb + kQB + ql); }
+#pragma unroll
+        for (int b = 0; b < kQB; ++b) {
+            const float w = __shfl_sync(qmask, wc, b, 8);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] = fmaf(w, x[b][k], acc[k]);
+        }
+        jc = jn;
+        wc = wn;
+    }
+}
+
 // Recomputed hop: Y[i] = (1 - alpha) (P[i] + sum_e A_e X[j]) + alpha V[i] (P: the
 // band kernel's window sum, or null).
 template <typename TX, typename TV>
@@ -659,24 +753,46 @@ bwd_hop_rows_kernel(BwdArgs a, const float* __restrict__ A, const TX* __restrict
                     const float* __restrict__ P, const TV* __restrict__ V, float* __restrict__ Y, float alpha) {
     __shared__ float2 part[kBwdWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float keep = 1.f - alpha;
     int64_t u, i;
-    const bool heavy = edge_item(a, a.row_order, a.heavy_rows, warp, u, i);
-    if (!heavy && u >= a.units) return;
+    if ((int64_t)blockIdx.x >= a.units * a.heavy_rows) {
+        const int ql = lane & 7;
+        const unsigned qmask = 0xFFu << (lane & 24);
+        if (!quarter_item(a, a.row_order, a.heavy_rows, 4 * warp + (lane >> 3), u, i)) return;
+        constexpr bool kWide = sizeof(TX) == 2;
+        const size_t unit = (size_t)u * a.n * kHeadDim, row = unit + (size_t)i * kHeadDim;
+        const float* Au = A + (size_t)u * a.nnz;
+        const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+        int64_t s0, s1;
+        row_run(a, i, e0, e1, s0, s1);
+        float acc[8];
+        if (P) load8<kWide>(P + row, ql, acc);
+        else for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+        quarter_sum(ql, qmask, (e1 - e0) - (s1 - s0), X + unit,
+                    [&](int64_t v) { return a.col[rest_pos(e0, v, s0, s1)]; },
+                    [&](int64_t v) { return Au[rest_pos(e0, v, s0, s1)]; }, acc);
+        float v[8], y[8];
+        load8<kWide>(V + row, ql, v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[k] = fmaf(keep, acc[k], alpha * v[k]);
+        store8<kWide>(Y + row, ql, y);
+        return;
+    }
+    edge_item(a, a.row_order, a.heavy_rows, warp, u, i);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const float* Au = A + (size_t)u * a.nnz;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     int64_t s0, s1;
     row_run(a, i, e0, e1, s0, s1);
     const int64_t len = (e1 - e0) - (s1 - s0);
-    int64_t v0 = 0, v1 = len;
-    if (heavy) heavy_share(len, warp, v0, v1);
+    int64_t v0, v1;
+    heavy_share(len, warp, v0, v1);
     const size_t at = unit + (size_t)i * kHeadDim + 2 * lane;
-    float2 acc = (P && (!heavy || warp == 0)) ? load2(P + at) : make_float2(0.f, 0.f);
+    float2 acc = (P && warp == 0) ? load2(P + at) : make_float2(0.f, 0.f);
     acc = edge_sum(lane, v0, v1, X + unit + 2 * lane,
                    [&](int64_t v) { return a.col[rest_pos(e0, v, s0, s1)]; },
                    [&](int64_t v) { return Au[rest_pos(e0, v, s0, s1)]; }, acc);
-    if (heavy && !heavy_total(part, warp, lane, acc)) return;
-    const float keep = 1.f - alpha;
+    if (!heavy_total(part, warp, lane, acc)) return;
     const float2 v = load2(V + at);
     store2(Y + at, make_float2(fmaf(keep, acc.x, alpha * v.x), fmaf(keep, acc.y, alpha * v.y)));
 }
@@ -689,15 +805,68 @@ bwd_weight_grad_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict
                        float* __restrict__ dA, float keep) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t u, i;
-    const bool heavy = edge_item(a, a.row_order, a.heavy_rows, warp, u, i);
-    if (!heavy && u >= a.units) return;
+    if ((int64_t)blockIdx.x >= a.units * a.heavy_rows) {
+        // a light row by a quarter-warp: kQB edges a batch, each edge's dot product
+        // summed by its lanes' 8 features and then over the quarter (xor butterfly:
+        // the same bits in every lane); the edge's own lane updates dA
+        const int ql = lane & 7;
+        const unsigned qmask = 0xFFu << (lane & 24);
+        if (!quarter_item(a, a.row_order, a.heavy_rows, 4 * warp + (lane >> 3), u, i)) return;
+        constexpr bool kWide = sizeof(TZ) == 2;
+        constexpr int kQB = kWide ? 8 : 4;
+        const size_t unit = (size_t)u * a.n * kHeadDim;
+        const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+        int64_t s0, s1;
+        row_run(a, i, e0, e1, s0, s1);
+        const int64_t len = (e1 - e0) - (s1 - s0);
+        float g[8];
+        load8<kWide>(G + unit + (size_t)i * kHeadDim, ql, g);
+        const TZ* Zu = Z + unit;
+        float* dAu = dA + (size_t)u * a.nnz;
+        bool okc = ql < kQB && ql < len;
+        int64_t ec = rest_pos(e0, ql, s0, s1);
+        int32_t jc = okc ? a.col[ec] : 0;
+        for (int64_t vb = 0; vb < len; vb += kQB) {
+            float z[kQB][8];
+#pragma unroll
+            for (int b = 0; b < kQB; ++b) {
+                const int32_t j = __shfl_sync(qmask, jc, b, 8);
+                if (vb + b < len) {
+                    load8<kWide>(Zu + (size_t)j * kHeadDim, ql, z[b]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) z[b][k] = 0.f;
+                }
+            }
+            const bool okn = ql < kQB && vb + kQB + ql < len;
+            const int64_t en = rest_pos(e0, vb + kQB + ql, s0, s1);
+            const int32_t jn = okn ? a.col[en] : 0;
+            float mine = 0.f;
+#pragma unroll
+            for (int b = 0; b < kQB; ++b) {
+                float d = g[0] * z[b][0];
+#pragma unroll
+                for (int k = 1; k < 8; ++k) d = fmaf(g[k], z[b][k], d);
+                d += __shfl_xor_sync(qmask, d, 1, 8);
+                d += __shfl_xor_sync(qmask, d, 2, 8);
+                d += __shfl_xor_sync(qmask, d, 4, 8);
+                if (ql == b) mine = d;
+            }
+            if (okc) dAu[ec] += keep * mine;
+            okc = okn;
+            ec = en;
+            jc = jn;
+        }
+        return;
+    }
+    edge_item(a, a.row_order, a.heavy_rows, warp, u, i);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     int64_t s0, s1;
     row_run(a, i, e0, e1, s0, s1);
     const int64_t len = (e1 - e0) - (s1 - s0);
-    int64_t v0 = 0, v1 = len;
-    if (heavy) heavy_share(len, warp, v0, v1);
+    int64_t v0, v1;
+    heavy_share(len, warp, v0, v1);
     const float2 g = load2(G + unit + (size_t)i * kHeadDim + 2 * lane);
     const TZ* Zu = Z + unit + 2 * lane;
     float* dAu = dA + (size_t)u * a.nnz;
@@ -733,24 +902,58 @@ bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ 
                  TIo* __restrict__ dV_out, float alpha, bool first) {
     __shared__ float2 part[kBwdWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float keep = 1.f - alpha;
     int64_t u, j;
-    const bool heavy = edge_item(a, a.key_order, a.heavy_keys, warp, u, j);
-    if (!heavy && u >= a.units) return;
+    if ((int64_t)blockIdx.x >= a.units * a.heavy_keys) {
+        const int ql = lane & 7;
+        const unsigned qmask = 0xFFu << (lane & 24);
+        if (!quarter_item(a, a.key_order, a.heavy_keys, 4 * warp + (lane >> 3), u, j)) return;
+        constexpr bool kWide = sizeof(TG) == 2;
+        const size_t unit = (size_t)u * a.n * kHeadDim, row = unit + (size_t)j * kHeadDim;
+        const float* Au = A + (size_t)u * a.nnz;
+        const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
+        int64_t s0, s1;
+        key_run(a, j, t0, t1, s0, s1);
+        float acc[8];
+        if (P) load8<kWide>(P + row, ql, acc);
+        else for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+        quarter_sum(ql, qmask, (t1 - t0) - (s1 - s0), G + unit,
+                    [&](int64_t v) { return a.t_row[rest_pos(t0, v, s0, s1)]; },
+                    [&](int64_t v) { return Au[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
+        float gj[8], dv[8], gn[8];
+        load8<kWide>(G + row, ql, gj);
+        if (first) for (int k = 0; k < 8; ++k) dv[k] = 0.f;
+        else load8<kWide>(dV_acc + row, ql, dv);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            dv[k] = fmaf(alpha, gj[k], dv[k]);
+            gn[k] = keep * acc[k];
+        }
+        if (dV_out) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) dv[k] += gn[k];
+            store8<kWide>(dV_out + row, ql, dv);
+        } else {
+            store8<kWide>(dV_acc + row, ql, dv);
+            store8<kWide>(Gn + row, ql, gn);
+        }
+        return;
+    }
+    edge_item(a, a.key_order, a.heavy_keys, warp, u, j);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const float* Au = A + (size_t)u * a.nnz;
     const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
     int64_t s0, s1;
     key_run(a, j, t0, t1, s0, s1);
     const int64_t len = (t1 - t0) - (s1 - s0);
-    int64_t v0 = 0, v1 = len;
-    if (heavy) heavy_share(len, warp, v0, v1);
+    int64_t v0, v1;
+    heavy_share(len, warp, v0, v1);
     const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
-    float2 acc = (P && (!heavy || warp == 0)) ? load2(P + at) : make_float2(0.f, 0.f);
+    float2 acc = (P && warp == 0) ? load2(P + at) : make_float2(0.f, 0.f);
     acc = edge_sum(lane, v0, v1, G + unit + 2 * lane,
                    [&](int64_t v) { return a.t_row[rest_pos(t0, v, s0, s1)]; },
                    [&](int64_t v) { return Au[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
-    if (heavy && !heavy_total(part, warp, lane, acc)) return;
-    const float keep = 1.f - alpha;
+    if (!heavy_total(part, warp, lane, acc)) return;
     const float2 gj = load2(G + at);
     float2 dv = first ? make_float2(0.f, 0.f) : load2(dV_acc + at);
     dv.x = fmaf(alpha, gj.x, dv.x);
@@ -812,22 +1015,40 @@ bwd_rows_out_kernel(BwdArgs a, const float* __restrict__ W, const TIo* __restric
     __shared__ float2 part[kBwdWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t u, i;
-    const bool heavy = edge_item(a, a.row_order, a.heavy_rows, warp, u, i);
-    if (!heavy && u >= a.units) return;
+    if ((int64_t)blockIdx.x >= a.units * a.heavy_rows) {
+        const int ql = lane & 7;
+        const unsigned qmask = 0xFFu << (lane & 24);
+        if (!quarter_item(a, a.row_order, a.heavy_rows, 4 * warp + (lane >> 3), u, i)) return;
+        constexpr bool kWide = sizeof(TIo) == 2;
+        const size_t unit = (size_t)u * a.n * kHeadDim, row = unit + (size_t)i * kHeadDim;
+        const float* Wu = W + (size_t)u * a.nnz;
+        const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
+        int64_t s0, s1;
+        row_run(a, i, e0, e1, s0, s1);
+        float acc[8];
+        if (P) load8<kWide>(P + row, ql, acc);
+        else for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+        quarter_sum(ql, qmask, (e1 - e0) - (s1 - s0), X + unit,
+                    [&](int64_t v) { return a.col[rest_pos(e0, v, s0, s1)]; },
+                    [&](int64_t v) { return Wu[rest_pos(e0, v, s0, s1)]; }, acc);
+        store8<kWide>(out + row, ql, acc);
+        return;
+    }
+    edge_item(a, a.row_order, a.heavy_rows, warp, u, i);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const float* Wu = W + (size_t)u * a.nnz;
     const int64_t e0 = a.row_ptr[i], e1 = a.row_ptr[i + 1];
     int64_t s0, s1;
     row_run(a, i, e0, e1, s0, s1);
     const int64_t len = (e1 - e0) - (s1 - s0);
-    int64_t v0 = 0, v1 = len;
-    if (heavy) heavy_share(len, warp, v0, v1);
+    int64_t v0, v1;
+    heavy_share(len, warp, v0, v1);
     const size_t at = unit + (size_t)i * kHeadDim + 2 * lane;
-    float2 acc = (P && (!heavy || warp == 0)) ? load2(P + at) : make_float2(0.f, 0.f);
+    float2 acc = (P && warp == 0) ? load2(P + at) : make_float2(0.f, 0.f);
     acc = edge_sum(lane, v0, v1, X + unit + 2 * lane,
                    [&](int64_t v) { return a.col[rest_pos(e0, v, s0, s1)]; },
                    [&](int64_t v) { return Wu[rest_pos(e0, v, s0, s1)]; }, acc);
-    if (heavy && !heavy_total(part, warp, lane, acc)) return;
+    if (!heavy_total(part, warp, lane, acc)) return;
     store2(out + at, acc);
 }
 
@@ -839,22 +1060,40 @@ bwd_dk_kernel(BwdArgs a, const float* __restrict__ dS, const TIo* __restrict__ Q
     __shared__ float2 part[kBwdWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t u, j;
-    const bool heavy = edge_item(a, a.key_order, a.heavy_keys, warp, u, j);
-    if (!heavy && u >= a.units) return;
+    if ((int64_t)blockIdx.x >= a.units * a.heavy_keys) {
+        const int ql = lane & 7;
+        const unsigned qmask = 0xFFu << (lane & 24);
+        if (!quarter_item(a, a.key_order, a.heavy_keys, 4 * warp + (lane >> 3), u, j)) return;
+        constexpr bool kWide = sizeof(TIo) == 2;
+        const size_t unit = (size_t)u * a.n * kHeadDim, row = unit + (size_t)j * kHeadDim;
+        const float* dSu = dS + (size_t)u * a.nnz;
+        const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
+        int64_t s0, s1;
+        key_run(a, j, t0, t1, s0, s1);
+        float acc[8];
+        if (P) load8<kWide>(P + row, ql, acc);
+        else for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+        quarter_sum(ql, qmask, (t1 - t0) - (s1 - s0), Q + unit,
+                    [&](int64_t v) { return a.t_row[rest_pos(t0, v, s0, s1)]; },
+                    [&](int64_t v) { return dSu[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
+        store8<kWide>(dK + row, ql, acc);
+        return;
+    }
+    edge_item(a, a.key_order, a.heavy_keys, warp, u, j);
     const size_t unit = (size_t)u * a.n * kHeadDim;
     const float* dSu = dS + (size_t)u * a.nnz;
     const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
     int64_t s0, s1;
     key_run(a, j, t0, t1, s0, s1);
     const int64_t len = (t1 - t0) - (s1 - s0);
-    int64_t v0 = 0, v1 = len;
-    if (heavy) heavy_share(len, warp, v0, v1);
+    int64_t v0, v1;
+    heavy_share(len, warp, v0, v1);
     const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
-    float2 acc = (P && (!heavy || warp == 0)) ? load2(P + at) : make_float2(0.f, 0.f);
+    float2 acc = (P && warp == 0) ? load2(P + at) : make_float2(0.f, 0.f);
     acc = edge_sum(lane, v0, v1, Q + unit + 2 * lane,
                    [&](int64_t v) { return a.t_row[rest_pos(t0, v, s0, s1)]; },
                    [&](int64_t v) { return dSu[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
-    if (heavy && !heavy_total(part, warp, lane, acc)) return;
+    if (!heavy_total(part, warp, lane, acc)) return;
     store2(dK + at, acc);
 }
 
@@ -873,7 +1112,7 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
                    float alpha, TIo* dQ, TIo* dK, TIo* dV, char* ws, const BwdLayout& L,
                    cudaStream_t stream) {
     const dim3 grid(bwd_grid(a)), block(kBwdWarps * 32);
-    const dim3 rgrid(edge_grid(a, a.heavy_rows)), kgrid(edge_grid(a, a.heavy_keys));   // the edge kernels
+    const dim3 qrgrid(quarter_grid(a, a.heavy_rows)), qkgrid(quarter_grid(a, a.heavy_keys));   // the products
     const bool band = a.wp0 != nullptr || a.bptr != nullptr;
     const dim3 bgrid((unsigned)(a.units * ((a.n + kTile - 1) / kTile)));
     const size_t io = (size_t)a.units * a.n * kHeadDim * sizeof(TIo);
@@ -902,7 +1141,7 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         err = cudaMemsetAsync(A, 0, (size_t)a.units * a.nnz * sizeof(float), stream);
         if (err != cudaSuccess) return cuda_fail(err, "clearing A");
         score([&] { band_sddmm<TIo, TIo>(a, bgrid, stream, Q, K, A, kScale); });
-        score([&] { bwd_weight_grad_kernel<TIo, TIo><<<rgrid, block, 0, stream>>>(a, Q, K, A, kScale); });
+        score([&] { bwd_weight_grad_kernel<TIo, TIo><<<qrgrid, block, 0, stream>>>(a, Q, K, A, kScale); });
         score([&] { bwd_scores_softmax_kernel<<<grid, block, 0, stream>>>(a, A); });
         if ((st = launched("bwd_scores_softmax_kernel"))) return st;
     } else if ((st = launch_score_csr(ca, Q, K, dtype, A, stream))) {
@@ -911,11 +1150,11 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
     for (int32_t k = 1; k < hops; ++k) {
         if (k == 1) {
             if (band) hop([&] { band_rows(a, bgrid, stream, A, V, P); });
-            hop([&] { bwd_hop_rows_kernel<TIo, TIo><<<rgrid, block, 0, stream>>>(a, A, V, P, V, zstate(k), alpha); });
+            hop([&] { bwd_hop_rows_kernel<TIo, TIo><<<qrgrid, block, 0, stream>>>(a, A, V, P, V, zstate(k), alpha); });
         } else {
             if (band) hop([&] { band_rows(a, bgrid, stream, A, zstate(k - 1), P); });
             hop([&] {
-                bwd_hop_rows_kernel<float, TIo><<<rgrid, block, 0, stream>>>(a, A, zstate(k - 1), P, V, zstate(k), alpha);
+                bwd_hop_rows_kernel<float, TIo><<<qrgrid, block, 0, stream>>>(a, A, zstate(k - 1), P, V, zstate(k), alpha);
             });
         }
         if ((st = launched("bwd_hop_rows_kernel"))) return st;
@@ -929,40 +1168,40 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         const float* Gf = Gbuf[(k + 1) & 1];         // G_{k+1} for k < hops - 1
         if (top && k == 0) {
             if (band) hop([&] { band_sddmm<TIo, TIo>(a, bgrid, stream, dOut, V, dA, keep); });
-            hop([&] { bwd_weight_grad_kernel<TIo, TIo><<<rgrid, block, 0, stream>>>(a, dOut, V, dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<TIo, TIo><<<qrgrid, block, 0, stream>>>(a, dOut, V, dA, keep); });
         } else if (top) {
             if (band)
                 hop([&] { band_sddmm<TIo, float>(a, bgrid, stream, dOut, zstate(k), dA, keep); });
-            hop([&] { bwd_weight_grad_kernel<TIo, float><<<rgrid, block, 0, stream>>>(a, dOut, zstate(k), dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<TIo, float><<<qrgrid, block, 0, stream>>>(a, dOut, zstate(k), dA, keep); });
         } else if (k == 0) {
             if (band) hop([&] { band_sddmm<float, TIo>(a, bgrid, stream, Gf, V, dA, keep); });
-            hop([&] { bwd_weight_grad_kernel<float, TIo><<<rgrid, block, 0, stream>>>(a, Gf, V, dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<float, TIo><<<qrgrid, block, 0, stream>>>(a, Gf, V, dA, keep); });
         } else {
             if (band)
                 hop([&] { band_sddmm<float, float>(a, bgrid, stream, Gf, zstate(k), dA, keep); });
-            hop([&] { bwd_weight_grad_kernel<float, float><<<rgrid, block, 0, stream>>>(a, Gf, zstate(k), dA, keep); });
+            hop([&] { bwd_weight_grad_kernel<float, float><<<qrgrid, block, 0, stream>>>(a, Gf, zstate(k), dA, keep); });
         }
         if ((st = launched("bwd_weight_grad_kernel"))) return st;
         TIo* out = k == 0 ? dV : nullptr;
         if (top) {
             if (band) hop([&] { band_keys(a, bgrid, stream, A, dOut, P); });
             hop([&] {
-                bwd_hop_t_kernel<TIo, TIo><<<kgrid, block, 0, stream>>>(a, A, dOut, P, Gn, dVacc, out, alpha, true);
+                bwd_hop_t_kernel<TIo, TIo><<<qkgrid, block, 0, stream>>>(a, A, dOut, P, Gn, dVacc, out, alpha, true);
             });
         } else {
             if (band) hop([&] { band_keys(a, bgrid, stream, A, Gf, P); });
             hop([&] {
-                bwd_hop_t_kernel<float, TIo><<<kgrid, block, 0, stream>>>(a, A, Gf, P, Gn, dVacc, out, alpha, false);
+                bwd_hop_t_kernel<float, TIo><<<qkgrid, block, 0, stream>>>(a, A, Gf, P, Gn, dVacc, out, alpha, false);
             });
         }
         if ((st = launched("bwd_hop_t_kernel"))) return st;
     }
     score([&] { bwd_softmax_kernel<<<grid, block, 0, stream>>>(a, A, dA); });
     if (band) score([&] { band_rows(a, bgrid, stream, dA, K, P); });
-    score([&] { bwd_rows_out_kernel<TIo><<<rgrid, block, 0, stream>>>(a, dA, K, P, dQ); });
+    score([&] { bwd_rows_out_kernel<TIo><<<qrgrid, block, 0, stream>>>(a, dA, K, P, dQ); });
     if ((st = launched("bwd_rows_out_kernel"))) return st;
     if (band) score([&] { band_keys(a, bgrid, stream, dA, Q, P); });
-    score([&] { bwd_dk_kernel<TIo><<<kgrid, block, 0, stream>>>(a, dA, Q, P, dK); });
+    score([&] { bwd_dk_kernel<TIo><<<qkgrid, block, 0, stream>>>(a, dA, Q, P, dK); });
     return launched("bwd_dk_kernel");
 }
 
