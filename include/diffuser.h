@@ -274,7 +274,7 @@ DIFFUSER_API int diffuser_forward_host(const void* Q, const void* K, const void*
  * The forward's weights and states Z_1 .. Z_{K-1} are recomputed inside the
  * call.  The first backward on a graph also builds its transposed edge list
  * (on the host, then a synchronous upload: 12 bytes per edge and 8 per
- * position of device memory, plus 16 per position on token graphs with a plain
+ * position of device memory, plus 24 per position on token graphs with a plain
  * window or 12 per block pair on block graphs, held with the graph), so make
  * that first call outside any stream capture.  All arithmetic is fp32; dQ, dK, dV are written in the I/O dtype.
  * On a token graph with a plain window (dilation 1) the window's edges run as
@@ -291,7 +291,11 @@ DIFFUSER_API int diffuser_forward_host(const void* Q, const void* K, const void*
  *   dQ, dK, dV      device [B][H][n][d] in dtype, written; they may not overlap
  *                   the inputs or each other
  *   workspace       diffuser_backward_workspace_size bytes, 256-byte aligned:
- *                   2 units nnz + (3 + max(K, 1)) units n 64 fp32 values
+ *                   2 units nnz + (3 + max(K, 1)) units n 64 fp32 values, and
+ *                   on a token graph with a plain window units (nnz - the
+ *                   window's pairs) more: the weights of the edges outside the
+ *                   window, copied into key order once per call for the
+ *                   transposed hops
  * Asynchronous on `stream`.  Errors: as diffuser_forward.
  */
 DIFFUSER_API int diffuser_backward_workspace_size(const diffuser_graph* g, int64_t B, int64_t H,

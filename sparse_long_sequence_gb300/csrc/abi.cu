@@ -702,6 +702,7 @@ void diffuser_graph_free(diffuser_graph* g) {
     cudaFree(g->d_t_edge);
     cudaFree(g->d_wp0);
     cudaFree(g->d_tw0);
+    cudaFree(g->d_trest);
     cudaFree(g->d_orders);
     cudaFree(g->d_bruns);
     cudaFree(g->d_blk_chunks);

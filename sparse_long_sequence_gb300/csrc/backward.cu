@@ -80,6 +80,8 @@ struct BwdArgs {
     int64_t heavy_rows, heavy_keys;   // how many come first in each order
     int64_t n, nnz, units;
     int32_t r, causal;        // the window: keys i - r .. i + r (.. i when causal), clipped
+    const int64_t* trest;     // [n + 1] where key j's incoming edges outside its window run start in
+    int64_t nrest;            //   the key-ordered weights ([units][nrest]); null: none are kept
 };
 
 // The keys lo .. hi of row i's window, and the rows lo .. hi whose windows hold key j.
@@ -141,26 +143,6 @@ constexpr int kWStride = kChunk + 4;   // a staged weight row (float4-aligned)
 constexpr int kMaxRange = 1088;        // rows of a key tile whose runs are staged in shared memory
 constexpr int kXPer = kChunk * (kHeadDim / 4) / kBandThreads;   // float4s of X a thread stages (dA)
 static_assert(kXPer * kBandThreads == kChunk * (kHeadDim / 4), "staging shares");
-
-// A chunk's 64 operand rows (first .. first + 63, zero past last) as fp32 in xs:
-// every load issued before the first store.
-template <int kThreads, typename TX>
-__device__ __forceinline__ void stage_rows(float (*xs)[kHeadDim], const TX* Xu, int64_t first, int64_t last,
-                                           int tid) {
-    constexpr int kPer = kChunk * (kHeadDim / 4) / kThreads;
-    float4 v[kPer];
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-        const int idx = tid + kThreads * q, rr = idx >> 4, f4 = idx & 15;
-        const int64_t j = first + rr;
-        v[q] = j <= last ? load4(Xu + j * kHeadDim + 4 * f4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-        const int idx = tid + kThreads * q, rr = idx >> 4, f4 = idx & 15;
-        *reinterpret_cast<float4*>(&xs[rr][4 * f4]) = v[q];
-    }
-}
 
 // The tiles of a band launch: unit-major on token graphs (neighbouring tiles of a
 // unit run together); tile-major on block graphs, so that the heavy global block
@@ -897,9 +879,9 @@ bwd_weight_grad_kernel(BwdArgs a, const TG* __restrict__ G, const TZ* __restrict
 // dV_out[j] = dV_acc[j] + alpha G[j] + Gn[j] in the I/O dtype and Gn is not written.
 template <typename TG, typename TIo>
 __global__ void __launch_bounds__(kBwdWarps * 32)
-bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ G,
-                 const float* __restrict__ P, float* __restrict__ Gn, float* __restrict__ dV_acc,
-                 TIo* __restrict__ dV_out, float alpha, bool first) {
+bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const float* __restrict__ At,
+                 const TG* __restrict__ G, const float* __restrict__ P, float* __restrict__ Gn,
+                 float* __restrict__ dV_acc, TIo* __restrict__ dV_out, float alpha, bool first) {
     __shared__ float2 part[kBwdWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float keep = 1.f - alpha;
@@ -917,9 +899,10 @@ bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ 
         float acc[8];
         if (P) load8<kWide>(P + row, ql, acc);
         else for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+        const float* Atj = At ? At + (size_t)u * a.nrest + a.trest[j] : nullptr;
         quarter_sum(ql, qmask, (t1 - t0) - (s1 - s0), G + unit,
                     [&](int64_t v) { return a.t_row[rest_pos(t0, v, s0, s1)]; },
-                    [&](int64_t v) { return Au[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
+                    [&](int64_t v) { return Atj ? Atj[v] : Au[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
         float gj[8], dv[8], gn[8];
         load8<kWide>(G + row, ql, gj);
         if (first) for (int k = 0; k < 8; ++k) dv[k] = 0.f;
@@ -950,9 +933,10 @@ bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ 
     heavy_share(len, warp, v0, v1);
     const size_t at = unit + (size_t)j * kHeadDim + 2 * lane;
     float2 acc = (P && warp == 0) ? load2(P + at) : make_float2(0.f, 0.f);
+    const float* Atj = At ? At + (size_t)u * a.nrest + a.trest[j] : nullptr;
     acc = edge_sum(lane, v0, v1, G + unit + 2 * lane,
                    [&](int64_t v) { return a.t_row[rest_pos(t0, v, s0, s1)]; },
-                   [&](int64_t v) { return Au[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
+                   [&](int64_t v) { return Atj ? Atj[v] : Au[a.t_edge[rest_pos(t0, v, s0, s1)]]; }, acc);
     if (!heavy_total(part, warp, lane, acc)) return;
     const float2 gj = load2(G + at);
     float2 dv = first ? make_float2(0.f, 0.f) : load2(dV_acc + at);
@@ -964,6 +948,55 @@ bwd_hop_t_kernel(BwdArgs a, const float* __restrict__ A, const TG* __restrict__ 
     } else {
         store2(dV_acc + at, dv);
         store2(Gn + at, gn);
+    }
+}
+
+// The weights of every key's incoming edges outside its window run, in key order:
+// At[u][trest[j] + v] = A_e of the v-th such edge of key j, so that the transposed
+// hops read them in sequence instead of through the edge ids.  Heavy keys take a
+// CTA each (first), the others a warp each; kU loads in flight per thread.
+unsigned weights_t_grid(const BwdArgs& a) {
+    return (unsigned)(a.units * a.heavy_keys + (a.units * (a.n - a.heavy_keys) + kBwdWarps - 1) / kBwdWarps);
+}
+__global__ void __launch_bounds__(kBwdWarps * 32)
+bwd_weights_t_kernel(BwdArgs a, const float* __restrict__ A, float* __restrict__ At) {
+    constexpr int kU = 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t hb = a.units * a.heavy_keys;
+    int64_t u, j;
+    int first, stride;
+    if ((int64_t)blockIdx.x < hb) {
+        const int64_t rk = blockIdx.x / a.units;
+        u = blockIdx.x - rk * a.units;
+        j = a.key_order[rk];
+        first = threadIdx.x;
+        stride = kBwdWarps * 32;
+    } else {
+        const int64_t item = ((int64_t)blockIdx.x - hb) * kBwdWarps + warp, rest = a.n - a.heavy_keys;
+        if (rest <= 0 || item >= a.units * rest) return;
+        u = item / rest;
+        j = a.key_order[a.heavy_keys + (item - u * rest)];
+        first = lane;
+        stride = 32;
+    }
+    const float* Au = A + (size_t)u * a.nnz;
+    float* Atj = At + (size_t)u * a.nrest + a.trest[j];
+    const int64_t t0 = a.t_ptr[j], t1 = a.t_ptr[j + 1];
+    int64_t s0, s1;
+    key_run(a, j, t0, t1, s0, s1);
+    const int64_t len = (t1 - t0) - (s1 - s0);
+    for (int64_t vb = first; vb < len; vb += (int64_t)kU * stride) {
+        float w[kU];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            const int64_t v = vb + (int64_t)q * stride;
+            w[q] = v < len ? Au[a.t_edge[rest_pos(t0, v, s0, s1)]] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            const int64_t v = vb + (int64_t)q * stride;
+            if (v < len) Atj[v] = w[q];
+        }
     }
 }
 
@@ -1120,6 +1153,7 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
     float* dA = reinterpret_cast<float*>(ws + L.da);
     float* dVacc = reinterpret_cast<float*>(ws + L.dv);
     float* P = band ? reinterpret_cast<float*>(ws + L.p) : nullptr;   // the band kernels' window sums
+    float* At = a.trest ? reinterpret_cast<float*>(ws + L.at) : nullptr;   // key-ordered weights
     float* Gbuf[2] = {reinterpret_cast<float*>(ws + L.g[0]), reinterpret_cast<float*>(ws + L.g[1])};
     auto zstate = [&](int32_t k) { return reinterpret_cast<float*>(ws + L.z + (size_t)(k - 1) * L.z_stride); };
     cudaError_t err;
@@ -1144,6 +1178,10 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         score([&] { bwd_weight_grad_kernel<TIo, TIo><<<qrgrid, block, 0, stream>>>(a, Q, K, A, kScale); });
         score([&] { bwd_scores_softmax_kernel<<<grid, block, 0, stream>>>(a, A); });
         if ((st = launched("bwd_scores_softmax_kernel"))) return st;
+        if (At) {
+            score([&] { bwd_weights_t_kernel<<<weights_t_grid(a), block, 0, stream>>>(a, A, At); });
+            if ((st = launched("bwd_weights_t_kernel"))) return st;
+        }
     } else if ((st = launch_score_csr(ca, Q, K, dtype, A, stream))) {
         return st;
     }
@@ -1186,12 +1224,12 @@ int backward_typed(const BwdArgs& a, const CsrArgs& ca, const TIo* Q,
         if (top) {
             if (band) hop([&] { band_keys(a, bgrid, stream, A, dOut, P); });
             hop([&] {
-                bwd_hop_t_kernel<TIo, TIo><<<qkgrid, block, 0, stream>>>(a, A, dOut, P, Gn, dVacc, out, alpha, true);
+                bwd_hop_t_kernel<TIo, TIo><<<qkgrid, block, 0, stream>>>(a, A, At, dOut, P, Gn, dVacc, out, alpha, true);
             });
         } else {
             if (band) hop([&] { band_keys(a, bgrid, stream, A, Gf, P); });
             hop([&] {
-                bwd_hop_t_kernel<float, TIo><<<qkgrid, block, 0, stream>>>(a, A, Gf, P, Gn, dVacc, out, alpha, false);
+                bwd_hop_t_kernel<float, TIo><<<qkgrid, block, 0, stream>>>(a, A, At, Gf, P, Gn, dVacc, out, alpha, false);
             });
         }
         if ((st = launched("bwd_hop_t_kernel"))) return st;
@@ -1286,6 +1324,20 @@ bool block_runs(const diffuser_graph* g, std::vector<int32_t>& runs) {
     return true;
 }
 
+// The edges outside the window runs of a token graph with a plain window (its nnz
+// less the window's pairs: row i's window holds the keys max(i - r, 0) ..
+// min(i + r, n - 1), .. i when causal); 0 on other graphs.
+int64_t window_rest(const diffuser_graph* g) {
+    if (g->kind != kTokenGraph || g->dilation != 1) return 0;
+    int64_t pairs = 0;
+    for (int64_t i = 0; i < g->n; ++i) {
+        const int64_t lo = i - g->r > 0 ? i - g->r : 0;
+        const int64_t hi = g->causal ? i : std::min<int64_t>(i + g->r, g->n - 1);
+        pairs += hi - lo + 1;
+    }
+    return g->nnz - pairs;
+}
+
 // The transposed graph (incoming edges of every key, rows ascending), built on
 // the host from the CSR copy by a counting sort and uploaded (synchronously),
 // with the window runs where the graph has them.  On failure the arrays
@@ -1306,7 +1358,19 @@ int build_transposed_graph(diffuser_graph* g) {
         }
     }
     std::vector<int64_t> wp0, tw0;
-    const bool runs = window_runs(g, t_ptr, t_row, wp0, tw0);
+    bool runs = window_runs(g, t_ptr, t_row, wp0, tw0);
+    // where key j's incoming edges outside its window run start in the key-ordered
+    // weights; their total must be the count the workspace was sized by
+    std::vector<int64_t> trest;
+    if (runs) {
+        trest.assign((size_t)n + 1, 0);
+        for (int64_t j = 0; j < n; ++j) {
+            const int64_t lo = g->causal ? j : (j - g->r > 0 ? j - g->r : 0);
+            const int64_t hi = std::min<int64_t>(j + g->r, n - 1);
+            trest[(size_t)j + 1] = trest[(size_t)j] + (t_ptr[(size_t)j + 1] - t_ptr[(size_t)j]) - (hi - lo + 1);
+        }
+        if (trest[(size_t)n] != window_rest(g)) runs = false;
+    }
     std::vector<int32_t> bruns;
     const bool blk = block_runs(g, bruns);
     // the heavy rows (keys): more than twice the mean edge count, heaviest first
@@ -1327,6 +1391,7 @@ int build_transposed_graph(diffuser_graph* g) {
     int64_t* d_edge = nullptr;
     int64_t* d_wp0 = nullptr;
     int64_t* d_tw0 = nullptr;
+    int64_t* d_trest = nullptr;
     int32_t* d_orders = nullptr;             // [2][n]: row_order, key_order
     int32_t* d_bruns = nullptr;
     cudaError_t err = cudaMalloc(&d_ptr, sizeof(int64_t) * (n + 1));
@@ -1350,6 +1415,9 @@ int build_transposed_graph(diffuser_graph* g) {
             err = cudaMemcpy(d_wp0, wp0.data(), sizeof(int64_t) * (size_t)n, cudaMemcpyHostToDevice);
         if (err == cudaSuccess)
             err = cudaMemcpy(d_tw0, tw0.data(), sizeof(int64_t) * (size_t)n, cudaMemcpyHostToDevice);
+        if (err == cudaSuccess) err = cudaMalloc(&d_trest, sizeof(int64_t) * ((size_t)n + 1));
+        if (err == cudaSuccess)
+            err = cudaMemcpy(d_trest, trest.data(), sizeof(int64_t) * ((size_t)n + 1), cudaMemcpyHostToDevice);
     }
     if (blk) {
         if (err == cudaSuccess) err = cudaMalloc(&d_bruns, sizeof(int32_t) * bruns.size());
@@ -1362,6 +1430,7 @@ int build_transposed_graph(diffuser_graph* g) {
         cudaFree(d_edge);
         cudaFree(d_wp0);
         cudaFree(d_tw0);
+        cudaFree(d_trest);
         cudaFree(d_orders);
         cudaFree(d_bruns);
         return cuda_fail(err, "building the transposed graph");
@@ -1373,6 +1442,7 @@ int build_transposed_graph(diffuser_graph* g) {
     g->heavy_keys = heavy_keys;
     g->d_wp0 = d_wp0;
     g->d_tw0 = d_tw0;
+    g->d_trest = d_trest;
     g->d_t_row = d_row;
     g->d_t_edge = d_edge;
     g->d_t_ptr = d_ptr;      // set last: non-null means the transposed graph is complete
@@ -1381,9 +1451,11 @@ int build_transposed_graph(diffuser_graph* g) {
 
 int plan_backward_layout(const diffuser_graph* g, int64_t units, int32_t hops, BwdLayout* L) {
     // A, dA: [units][nnz] fp32; dV_acc, G (x2), the band kernels' window sums P,
-    // Z_1 .. Z_{K-1}: [units][n][64] fp32
+    // Z_1 .. Z_{K-1}: [units][n][64] fp32; the weights outside the window runs in
+    // key order: [units][nrest] fp32
+    const int64_t nrest = window_rest(g);
     const double states = 4.0 + (hops > 1 ? hops - 1 : 0);
-    const double need = (double)units * (2.0 * 4.0 * (double)g->nnz +
+    const double need = (double)units * (2.0 * 4.0 * (double)g->nnz + 4.0 * (double)nrest +
                                          states * 4.0 * kHeadDim * (double)g->n);
     if (need > 4.0e18) return fail(DIFFUSER_ERR_OVERFLOW, "backward workspace size overflows size_t");
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -1396,6 +1468,8 @@ int plan_backward_layout(const diffuser_graph* g, int64_t units, int32_t hops, B
     L->g[0] = off; off += state;
     L->g[1] = off; off += state;
     L->p = off; off += state;
+    L->at = off; off += al(U * (size_t)nrest * sizeof(float));
+    L->nrest = nrest;
     L->z = off;
     L->z_stride = state;
     off += (hops > 1 ? (size_t)(hops - 1) : 0) * state;
@@ -1416,7 +1490,8 @@ int launch_backward_csr(const diffuser_graph* g, int64_t units, const void* Q, c
               blk ? br : nullptr, blk ? br + nb + 1 : nullptr, blk ? br + nb + 1 + m : nullptr,
               blk ? br + 2 * (nb + 1) + m : nullptr, blk ? br + 2 * (nb + 1) + 2 * m : nullptr,
               g->d_orders, g->d_orders + g->n,
-              g->heavy_rows, g->heavy_keys, g->n, g->nnz, units, g->r, g->causal ? 1 : 0};
+              g->heavy_rows, g->heavy_keys, g->n, g->nnz, units, g->r, g->causal ? 1 : 0,
+              runs && g->d_trest && L.nrest > 0 ? g->d_trest : nullptr, L.nrest};
     CsrArgs ca{g->d_row_ptr, g->d_col, g->n, g->nnz, units};
     if (dtype == DIFFUSER_DTYPE_BF16) {
         using T = __nv_bfloat16;

@@ -50,6 +50,9 @@ struct BwdLayout {
     size_t dv;          // the dV accumulator, [units][n][64]
     size_t g[2];        // G_k, the gradient reaching Z_k, ping-pong, [units][n][64]
     size_t p;           // the band kernels' window sums, [units][n][64]
+    size_t at;          // the weights of the edges outside the keys' window runs in key order,
+                        // [units][nrest] (token graphs with a plain window; nrest = 0 otherwise)
+    int64_t nrest;
     size_t z, z_stride; // Z_1 .. Z_{K-1}, each [units][n][64]
     size_t total;
 };
@@ -91,6 +94,8 @@ struct diffuser_graph {
     int64_t* d_t_edge = nullptr;      // [nnz] its CSR edge id
     int64_t* d_wp0 = nullptr;         // [n] token graph, plain window: CSR position of row i's window run
     int64_t* d_tw0 = nullptr;         // [n] ... and transposed-list position of key j's (null otherwise)
+    int64_t* d_trest = nullptr;       // [n+1] ... and where key j's incoming edges outside its run start
+                                      //   in the key-ordered weights (null otherwise)
     int32_t* d_orders = nullptr;      // [2][n] the backward's row and key orders (heavy ones first)
     int64_t heavy_rows = 0, heavy_keys = 0;
     int32_t* d_bruns = nullptr;       // block graph, 64-token blocks: the backward's key-block runs
