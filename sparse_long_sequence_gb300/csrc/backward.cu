@@ -1335,7 +1335,7 @@ int64_t window_rest(const diffuser_graph* g) {
         const int64_t hi = g->causal ? i : std::min<int64_t>(i + g->r, g->n - 1);
         pairs += hi - lo + 1;
     }
-    return g->nnz - pairs;
+    return g->nnz > pairs ? g->nnz - pairs : 0;
 }
 
 // The transposed graph (incoming edges of every key, rows ascending), built on
