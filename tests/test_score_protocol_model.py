@@ -17,12 +17,15 @@ quadrant, named barriers:
 
 A mistake in the protocol shows up on the GPU as a wait that never ends, so the
 roles' wait/arrive sequences are restated here step for step and played out with
-the barriers' arrival counts and phases: for any tile count, chunk count, with and
-without globals and images, every role must finish.  It checks the protocol as
-designed; keeping it in step with the kernel is a review duty whenever either
-changes.
+the barriers' arrival counts and phases (tests/barrier_model.py): for any tile
+count, chunk count, with and without globals and images, every role must finish,
+and no wait may find its barrier two phases ahead (the parity would alias).  It
+checks the protocol as designed; keeping it in step with the kernel is a review
+duty whenever either changes.
 """
 import pytest
+
+from tests.barrier_model import play
 
 K_STAGES, S_BUFS = 8, 5        # the kernel's K ring and TMEM score buffers
 ROW_WARPS = 8                  # 4 lane quadrants x 2 column halves
@@ -44,7 +47,8 @@ def my_tiles(total, G, b):
 
 def simulate(my, nc, c0, has_g, images, k_stages=K_STAGES, s_bufs=S_BUFS, es_count=ROW_WARPS, egr_count=2):
     """Play the roles' waits and arrivals for one CTA with `my` tiles; True if
-    every role finishes."""
+    every role finishes under every schedule tried, with no wait overtaken by
+    two phases of its barrier."""
     per_tile = 2 * nc if images else nc
     counts = {}
     for s in range(2):
@@ -141,27 +145,7 @@ def simulate(my, nc, c0, has_g, images, k_stages=K_STAGES, s_bufs=S_BUFS, es_cou
             pair()
         rows.append(seq)
 
-    roles = [tma, mma, gld] + rows
-    pos = [0] * len(roles)
-    arrived = {k: 0 for k in counts}
-    phases = {k: 0 for k in counts}
-    progress = True
-    while progress:
-        progress = False
-        for ri, role in enumerate(roles):
-            while pos[ri] < len(role):
-                op = role[pos[ri]]
-                if op[0] == "w":
-                    if phases[op[1]] <= op[2]:
-                        break
-                else:
-                    arrived[op[1]] += 1
-                    if arrived[op[1]] == counts[op[1]]:
-                        arrived[op[1]] = 0
-                        phases[op[1]] += 1
-                pos[ri] += 1
-                progress = True
-    return all(pos[ri] == len(role) for ri, role in enumerate(roles))
+    return play([tma, mma, gld] + rows, counts) == "done"
 
 
 CASES = [(4096, 256, False), (4096, 256, True), (1024, 32, False), (1024, 32, True), (16384, 256, False),
