@@ -12,13 +12,17 @@ roles' wait/arrive sequences, and checked on the CPU:
     covers every key of each of its rows' windows (bidirectional [i - r, i + r]
     or causal [i - r, i]);
   * the roles' waits and arrivals, played out with the barriers' arrival counts
-    and phases, run to completion (no deadlock) for any tile list, with and
-    without globals, on the first hop (row-sum hand-off) and later ones.
+    and phases (tests/barrier_model.py), run to completion (no deadlock) for any
+    tile list, with and without globals, on the first hop (row-sum hand-off) and
+    later ones, and no wait finds its barrier two phases ahead (where the
+    parity would alias).
 
 It checks the protocol as designed; keeping it in step with the kernel is a
 review duty whenever either changes.
 """
 import pytest
+
+from tests.barrier_model import play
 
 CK, TR = 128, 128          # keys per chunk, rows per tile
 
@@ -92,7 +96,8 @@ def cta_tiles(n, r, causal, units, G, b):
 
 
 def simulate(tiles, c0, r64, has_g, hop0, slots=2, fp_arrivals=2):
-    """Play the roles' waits and arrivals; True if every role finishes."""
+    """Play the roles' waits and arrivals; True if every role finishes under every
+    schedule tried, with no wait overtaken by two phases of its barrier."""
     counts = {}
     for s in range(2):
         counts[("fQ", s)] = counts[("eQ", s)] = 1
@@ -171,27 +176,7 @@ def simulate(tiles, c0, r64, has_g, hop0, slots=2, fp_arrivals=2):
         ep += [W("accF", lt), A("accE")]
         if has_g:
             ep.append(A("gE"))
-    roles = [kq, zp, si, pv, ep, sw]
-    pos = [0] * len(roles)
-    arrived = {k: 0 for k in counts}
-    phases = {k: 0 for k in counts}
-    progress = True
-    while progress:
-        progress = False
-        for ri, role in enumerate(roles):
-            while pos[ri] < len(role):
-                op = role[pos[ri]]
-                if op[0] == "w":
-                    if phases[op[1]] <= op[2]:
-                        break
-                else:
-                    arrived[op[1]] += 1
-                    if arrived[op[1]] == counts[op[1]]:
-                        arrived[op[1]] = 0
-                        phases[op[1]] += 1
-                pos[ri] += 1
-                progress = True
-    return all(pos[ri] == len(role) for ri, role in enumerate(roles))
+    return play([kq, zp, si, pv, ep, sw], counts) == "done"
 
 
 CASES = [(4096, 256, 24), (1024, 32, 32), (513, 16, 2), (300, 8, 3), (200, 300, 3), (129, 64, 5),
