@@ -56,7 +56,7 @@ typedef struct diffuser_graph diffuser_graph;
 typedef enum {
     DIFFUSER_OK = 0,
     DIFFUSER_ERR_INVALID_ARG = 1,  /* a null pointer, a size out of range, misalignment */
-    DIFFUSER_ERR_UNSUPPORTED = 2,  /* a dtype, head width or option this build lacks */
+    DIFFUSER_ERR_UNSUPPORTED = 2,  /* a dtype, head width or option the library does not support */
     DIFFUSER_ERR_OVERFLOW = 3,     /* an edge count or buffer size overflows its index type */
     DIFFUSER_ERR_ALLOC = 4,        /* a device or host allocation failed */
     DIFFUSER_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
