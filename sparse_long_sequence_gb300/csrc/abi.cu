@@ -802,6 +802,7 @@ namespace {
 int per_head_need(const diffuser_graph* const* graphs, int64_t B, int64_t H, int32_t d,
                   int32_t dtype, size_t* staging, size_t* need) {
     if (!graphs) return fail(DIFFUSER_ERR_INVALID_ARG, "graphs is NULL");
+    if (H < 1) return fail(DIFFUSER_ERR_INVALID_ARG, "B and H must be >= 1");   // before graphs[0] is read
     int st = check_shape(graphs[0], B, H, d, dtype);
     if (st) return st;
     size_t fwd = 0;
@@ -1077,6 +1078,7 @@ int diffuser_layer_forward(const void* X, const void* Wqkv, const void* Wo, int6
 
 int diffuser_host_workspace_size(const diffuser_graph* g, int64_t B, int64_t H, int32_t d,
                                  int32_t dtype, size_t* bytes) {
+    if (!bytes) return fail(DIFFUSER_ERR_INVALID_ARG, "bytes is NULL");
     size_t base = 0;
     int st = diffuser_workspace_size(g, B, H, d, dtype, &base);
     if (st) return st;

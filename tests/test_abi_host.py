@@ -103,6 +103,80 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.diffuser_last_error() != b""
 
 
+def test_every_other_entry_point_rejects_bad_arguments_on_host(lib):
+    # each of these returns before any device call: INVALID_ARG (1) for a NULL or an
+    # out-of-range argument, UNSUPPORTED (2) for a head width or model width it lacks
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    out, nbytes = vp(), sz()
+    fu = lib.diffuser_build_uniform_graph
+    fu.argtypes = [i64, i32, i32, ctypes.POINTER(i32), i32, i32, ctypes.POINTER(vp)]
+    assert fu(0, 1, 0, None, 4, 0, ctypes.byref(out)) == 1          # n < 1
+    assert fu(10, -1, 0, None, 4, 0, ctypes.byref(out)) == 1        # r < 0
+    assert fu(10, 1, 0, None, 2000, 0, ctypes.byref(out)) == 1      # too many positions per row
+    assert fu(10, 1, 0, None, 4, 0, None) == 1                      # null out
+    lib.diffuser_graph_info.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    assert lib.diffuser_graph_info(None, None, None) == 1
+    lib.diffuser_graph_copy_csr.argtypes = [vp, vp, vp]
+    assert lib.diffuser_graph_copy_csr(None, None, None) == 1
+    hws = lib.diffuser_host_workspace_size
+    hws.argtypes = [vp, i64, i64, i32, i32, ctypes.POINTER(sz)]
+    assert hws(None, 1, 1, 64, 1, ctypes.byref(nbytes)) == 1        # null graph
+    assert hws(None, 1, 1, 64, 1, None) == 1                        # null result
+    fh = lib.diffuser_forward_host
+    fh.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, i32, f32, vp, vp, sz, vp]
+    assert fh(None, None, None, 1, 1, 1, 64, None, 5, 0.1, None, None, 0, None) == 1
+    phws = lib.diffuser_per_head_workspace_size
+    phws.argtypes = [vp, i64, i64, i32, i32, ctypes.POINTER(sz)]
+    assert phws(None, 1, 2, 64, 1, ctypes.byref(nbytes)) == 1       # null graph list
+    heads = (vp * 1)(None)
+    assert phws(ctypes.cast(heads, vp), 1, 0, 64, 1, ctypes.byref(nbytes)) == 1   # H < 1
+    assert phws(ctypes.cast(heads, vp), 1, 1, 64, 1, ctypes.byref(nbytes)) == 1   # a NULL head graph
+    assert phws(ctypes.cast(heads, vp), 1, 1, 64, 1, None) == 1
+    fph = lib.diffuser_forward_per_head
+    fph.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, i32, f32, vp, vp, sz, vp]
+    assert fph(None, None, None, 1, 1, 1, 64, None, 5, 0.1, None, None, 0, None) == 1
+    fq = lib.diffuser_qkv_projection
+    fq.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp, vp, vp]
+    assert fq(None, None, 0, 16, 768, 12, 64, None, None, None, None) == 1     # B < 1
+    assert fq(None, None, 1, 16, 768, 12, 32, None, None, None, None) == 2     # d != 64
+    assert fq(None, None, 1, 16, 770, 12, 64, None, None, None, None) == 2     # D not a multiple of 8
+    assert fq(None, None, 1, 16, 768, 12, 64, None, None, None, None) == 1     # null tensors
+    fo = lib.diffuser_output_projection
+    fo.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp]
+    assert fo(None, None, 1, 0, 768, 12, 64, None, None) == 1                  # n < 1
+    assert fo(None, None, 1, 16, 768, 12, 64, None, None) == 1                 # null tensors
+    lib.diffuser_projection_status.argtypes = [vp, ctypes.c_int]
+    assert lib.diffuser_projection_status(None, 0) == 1
+    lws = lib.diffuser_layer_workspace_size
+    lws.argtypes = [vp, i64, i32, i32, i32, ctypes.POINTER(sz)]
+    assert lws(None, 1, 768, 12, 64, ctypes.byref(nbytes)) == 1
+    lf = lib.diffuser_layer_forward
+    lf.argtypes = [vp, vp, vp, i64, i32, i32, i32, vp, i32, f32, vp, vp, sz, vp]
+    assert lf(None, None, None, 1, 768, 12, 64, None, 5, 0.1, None, None, 0, None) == 1
+    na = lib.diffuser_forward_no_alloc
+    na.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, i32, f32, vp, vp]
+    assert na(None, None, None, 1, 1, 1, 64, None, 5, 0.1, None, None) == 1
+    lib.diffuser_no_alloc_scratch_bytes.restype = sz
+    assert lib.diffuser_no_alloc_scratch_bytes() == 32 << 20
+    aw = lib.diffuser_attention_weights
+    aw.argtypes = [vp, vp, i32, i64, i64, i32, vp, vp, vp, sz, vp]
+    assert aw(None, None, 1, 1, 1, 64, None, None, None, 0, None) == 1
+    dc = lib.diffuser_diffuse_csr
+    dc.argtypes = [vp, vp, vp, i32, i64, i64, i32, i32, f32, vp, vp, sz, vp]
+    assert dc(None, None, None, 1, 1, 1, 64, 5, 0.1, None, None, 0, None) == 1
+    assert lib.diffuser_set_path(7) == 1
+    assert lib.diffuser_get_path() == 0                              # unchanged by the refusal
+    assert lib.diffuser_set_path(1) == 0 and lib.diffuser_get_path() == 1
+    assert lib.diffuser_set_path(0) == 0 and lib.diffuser_get_path() == 0
+    lib.diffuser_kernels_for.argtypes = [vp, i32, vp]
+    assert lib.diffuser_kernels_for(None, 1, None) == 1
+    lib.diffuser_graph_status.argtypes = [vp, vp, ctypes.c_int]
+    assert lib.diffuser_graph_status(None, None, 0) == 1
+    lib.diffuser_graph_set_status.argtypes = [vp, ctypes.c_int]
+    assert lib.diffuser_graph_set_status(None, 6) == 1
+
+
 def test_launch_counter_and_profiler_without_gpu(lib):
     arr = (ctypes.c_int64 * 5)()
     lib.diffuser_launch_count.restype = ctypes.c_int64
