@@ -1,5 +1,6 @@
 """CPU checks of bench.py's measurement arithmetic: the byte model behind the
-roofline fraction, the traffic record lookup, and the clock record parsing."""
+roofline fraction, the traffic record lookup, the clock record parsing, and the
+sampled-unit comparison with the oracle that guards every printed line."""
 import json
 import os
 import sys
@@ -90,3 +91,26 @@ def test_clock_record_reports_throttling(tmp_path):
             return 0
     s.proc, s.fh = Done(), open(os.devnull, "w")
     assert s.stop()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def _unit_reference(w, Qh, Kh, Vh, unit):
+    import oracle
+    b, h = divmod(unit, w.H)
+    row_ptr, col = oracle.token_graph(**w.graph_args(), causal=w.kind == "causal")
+    one = [oracle.widen(x[b:b + 1, h:h + 1], w.dtype) for x in (Qh, Kh, Vh)]
+    return oracle.forward(*one, row_ptr, col, w.hops, w.alpha)[0, 0]
+
+
+def test_sampled_unit_check_fires_on_a_wrong_output():
+    import pytest
+    from sparse_long_sequence_gb300 import synthetic
+    for w, bump in ((workloads.BY_NAME["tiny_fp32_n512"], 2e-5), (workloads.BY_NAME["lra_bf16_b32h8_n1024"], 6e-3)):
+        Qh, Kh, Vh = synthetic.qkv(w.B, w.H, w.n, w.d, w.dtype, seed=w.seed)
+        unit = w.units - 1
+        ref = _unit_reference(w, Qh, Kh, Vh, unit)
+        ok = bench.check_sampled_unit(w, ref, Qh, Kh, Vh, unit)
+        assert ok["error"] == 0.0 and ok["unit"] == unit
+        bad = ref.copy()
+        bad[7, 3] += bump * (1.0 if w.dtype == "fp32" else abs(ref[7]).max())
+        with pytest.raises(bench.BenchCheckFailed):
+            bench.check_sampled_unit(w, bad, Qh, Kh, Vh, unit)
